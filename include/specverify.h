@@ -1,0 +1,169 @@
+/*
+ * specverify.h - C ABI of libspecverify: the batched target-side verify/sample
+ * step of speculative decoding, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (from "11.1 核心原理: Draft + Verify 与 Rejection Sampling",
+ * sections 11.1.1-11.1.3 and its code listing 10-1, and from the notes "Fast
+ * Inference from Transformers via Speculative Decoding", speculative-sampling
+ * paragraph):
+ *
+ *   A draft proposed gamma tokens d_0..d_{gamma-1}, drawing d_i from its actual
+ *   proposal distribution q_i.  One target forward over the context plus the
+ *   drafts gave gamma+1 rows of logits; row i predicts the token at draft
+ *   position i (it was computed from the prefix ending just before d_i), row
+ *   gamma is the distribution after all drafts (section 11.1.1).  The target
+ *   distribution of row i is p_i = softmax(logits_i / temperature), optionally
+ *   restricted by top-k and then top-p and renormalised (section 11.1.2: the
+ *   same transforms the draft applied to q_i).
+ *
+ *   Sampling (sv_verify_sample): for i = 0, 1, ... accept d_i iff
+ *   u_i < a_i = min(1, p_i(d_i) / q_i(d_i)); stop at the first rejection n.
+ *   On a rejection draw the next token from the residual
+ *   norm(max(p_n - q_n, 0)); if every draft was accepted (n = gamma) draw the
+ *   bonus token from p_gamma.  Emit d_0..d_{n-1} followed by that token.
+ *
+ *   Greedy (sv_verify_greedy): accept while d_i == argmax p_i (ties -> the
+ *   lowest index); at the first mismatch n emit argmax p_n; if all match emit
+ *   argmax p_gamma.
+ *
+ * Readings where the pages are silent (fixed by this ABI):
+ *   - the caller supplies gamma+1 uniforms per sequence: uniforms[b][i] is the
+ *     accept test of position i, uniforms[b][gamma] the one final draw;
+ *   - a categorical draw with uniform u from weights r is the inverse CDF in
+ *     token-index order: the smallest v with sum_{w<=v} r(w) > u * sum(r);
+ *   - truncation order: temperature, then top-k ranked by (logit descending,
+ *     index ascending), renormalise, then top-p keeps the shortest prefix of
+ *     that ranking whose mass reaches top_p (the crossing token is kept);
+ *   - q is used as given: it must already be the draft's actual (truncated,
+ *     renormalised) proposal; the step never re-truncates it.
+ *
+ * Memory and execution conventions (all entry points):
+ *   - Every pointer argument is DEVICE memory owned by the caller, contiguous
+ *     row-major, left unmodified except outputs and workspace.  The library
+ *     allocates nothing.
+ *   - logits and q must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Arguments are validated on the host first; a failed
+ *     validation returns an error status and launches nothing.  A launch
+ *     failure returns SV_ERR_CUDA.
+ *   - The workspace must be zero-filled before its first use (for example with
+ *     cudaMemsetAsync).  Every call that completes leaves it zero-filled again,
+ *     so one workspace can be reused for any sequence of calls on one stream.
+ *     Calls that run concurrently must use different workspaces.
+ *   - Problems in the DATA never fault or trap: they set bits in the
+ *     per-sequence status word (SV_SEQ_*) and the outputs stay in range.
+ *   - B = 0 is a valid empty call: nothing is launched.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,  /* a size, pointer, alignment or parameter is invalid */
+  SV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (see sv_verify_sample) */
+  SV_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than sv_workspace_bytes() */
+  SV_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+  SV_ERR_TIMEOUT = 5       /* reserved: a bounded device wait gave up */
+} sv_status;
+
+typedef enum {
+  SV_DTYPE_F32 = 0,
+  SV_DTYPE_BF16 = 1,
+  SV_DTYPE_F16 = 2
+} sv_dtype;
+
+/* Per-sequence status bits written to out_status[b]. */
+#define SV_SEQ_DRAFT_OUT_OF_RANGE 1 /* some d_i outside [0, V): that position is rejected (a_i = 0) */
+#define SV_SEQ_Q_NOT_POSITIVE 2     /* some q_i(d_i) <= 0 or NaN: a_i = 1 if p_i(d_i) > 0, else 0 */
+#define SV_SEQ_BAD_ROW 4            /* a row holds NaN or +inf, or only -inf: outputs undefined but in range */
+#define SV_SEQ_RESIDUAL_ZERO 8      /* rejection with zero residual mass: the token was drawn from p_n */
+
+/* Opaque stream handle, binary-compatible with cudaStream_t. */
+typedef struct CUstream_st* sv_stream_t;
+
+/* Limits checked by the entry points. */
+#define SV_MAX_GAMMA 64
+#define SV_MAX_VOCAB (1 << 24)
+#define SV_MAX_TOP_K 1024
+
+/*
+ * Bytes of device workspace that sv_verify_sample / sv_verify_greedy need for
+ * this problem size (any logits dtype).  top_k = 0 for greedy or for sampling
+ * without top-k.  Returns 0 for invalid sizes (B < 0, gamma < 0 or above
+ * SV_MAX_GAMMA, V < 1 or above SV_MAX_VOCAB, top_k outside [0, SV_MAX_TOP_K]).
+ */
+size_t sv_workspace_bytes(int B, int gamma, int V, int top_k);
+
+/*
+ * Sampling verify (speculative sampling, section 11.1.2 and listing 10-1).
+ *
+ *   B, gamma, V      batch size (>= 0), drafts per sequence (0..SV_MAX_GAMMA),
+ *                    vocabulary size (1..SV_MAX_VOCAB)
+ *   logits           [B][gamma+1][V] of logits_dtype; row i predicts the token
+ *                    at draft position i, row gamma the bonus position
+ *   q                [B][gamma][V] float32, the draft's actual proposal
+ *                    probabilities (non-negative); may be NULL when gamma = 0
+ *   draft_tokens     [B][gamma] int32 drafted ids; may be NULL when gamma = 0
+ *   uniforms         [B][gamma+1] float32 in [0, 1)
+ *   temperature      > 0 and finite
+ *   top_k            0 = off, else 1..SV_MAX_TOP_K
+ *   top_p            in (0, 1]; 1 = off.  top_p < 1 with top_k = 0 is
+ *                    supported only for V <= SV_MAX_TOP_K (else
+ *                    SV_ERR_UNSUPPORTED).
+ *   out_tokens       [B][gamma+1] int32: d_0..d_{n-1}, the drawn token, then -1
+ *   out_num_accepted [B] int32: n in 0..gamma (n+1 tokens were emitted)
+ *   out_accept_prob  [B][gamma] float32 a_i for every position, or NULL
+ *   out_status       [B] int32 SV_SEQ_* bits, or NULL
+ *   workspace        device scratch of at least sv_workspace_bytes(B, gamma, V, top_k)
+ */
+sv_status sv_verify_sample(int B, int gamma, int V,
+                           const void* logits, sv_dtype logits_dtype,
+                           const float* q, const int32_t* draft_tokens,
+                           const float* uniforms,
+                           float temperature, int top_k, float top_p,
+                           int32_t* out_tokens, int32_t* out_num_accepted,
+                           float* out_accept_prob, int32_t* out_status,
+                           void* workspace, size_t workspace_bytes,
+                           sv_stream_t stream);
+
+/*
+ * Greedy verify (section 11.1.2, greedy rule).  Arguments as in
+ * sv_verify_sample; no q, uniforms, temperature or truncation (they do not move
+ * the argmax).  Ties of the argmax go to the lowest index; -0.0 equals +0.0.
+ */
+sv_status sv_verify_greedy(int B, int gamma, int V,
+                           const void* logits, sv_dtype logits_dtype,
+                           const int32_t* draft_tokens,
+                           int32_t* out_tokens, int32_t* out_num_accepted,
+                           int32_t* out_status,
+                           void* workspace, size_t workspace_bytes,
+                           sv_stream_t stream);
+
+/* Static description of a status code. */
+const char* sv_status_string(sv_status s);
+
+/*
+ * Measurement hook (outside the verify computation; used by the benchmark to
+ * time each kernel with CUDA events).  Registers n = 3 caller-created CUDA
+ * events (cudaEvent_t handles cast to void*) that every later call records on
+ * its stream: events[0] before its first kernel, events[1] after the kernel
+ * that streams the logits, events[2] after its last kernel.  n = 0 clears the
+ * registration.  The record between the two kernels of an untruncated sampling
+ * call prevents their overlapped (programmatic) launch, so time headline
+ * throughput with the hook cleared.  Process-wide state; not thread-safe.
+ * Returns SV_ERR_INVALID_ARG for n other than 0 or 3 or NULL events.
+ */
+sv_status sv_set_timing_events(void* const* events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,283 @@
+// Host side of libspecverify: argument validation, workspace layout and kernel
+// dispatch for the C ABI declared in include/specverify.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+
+#include "specverify.h"
+#include "sv_device.cuh"
+
+namespace {
+
+// sv_set_timing_events registration (benchmark hook)
+cudaEvent_t g_timing[3] = {nullptr, nullptr, nullptr};
+bool g_timing_on = false;
+
+void timing_record(int which, cudaStream_t stream) {
+  if (g_timing_on) cudaEventRecord(g_timing[which], stream);
+}
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Length of the top-k candidate lists the workspace reserves for (top_k, V):
+// top_k itself, or the whole vocabulary when top-p alone is allowed (V <= 1024).
+int list_len(int V, int top_k) {
+  if (top_k > 0) return top_k < V ? top_k : V;
+  return V <= SV_MAX_TOP_K ? V : 0;
+}
+
+struct Layout {
+  size_t seq_ticket, seq_ticket2, row_ticket, seq, acc, part, lists, rowres, chunk, total;
+  int S_part, S_list, C_max, klist;
+};
+
+// One layout for any dtype and launch shape: slices are sized for the
+// smallest slice the dispatcher may pick (float32, one vector per thread) and
+// chunks for the smallest chunk (8 elements per thread).
+Layout make_layout(int B, int gamma, int V, int top_k) {
+  Layout L{};
+  const long long R = (long long)B * (gamma + 1);
+  L.klist = list_len(V, top_k);
+  L.S_part = (int)ceil_div(V, sv::kThreads * 1 * 4);
+  L.S_list = L.klist > 0 ? (int)ceil_div(V, sv::kThreads * sv::kMaxU * 4) : 0;
+  // residual sub-ranges per row: chunks x slots = about V / (256 * vector width)
+  L.C_max = (int)ceil_div(V, sv::kThreads * 4) + sv::kResMaxEPT / 4;
+  size_t o = 0;
+  L.seq_ticket = o;  o += up(sizeof(int) * (size_t)B);
+  L.seq_ticket2 = o; o += up(sizeof(int) * (size_t)B);
+  L.row_ticket = o;  o += up(sizeof(int) * (size_t)R);
+  L.seq = o;         o += up(sizeof(sv::SeqState) * (size_t)B);
+  L.acc = o;         o += up(sizeof(double) * (size_t)B * gamma);
+  L.part = o;        o += up(sizeof(float4) * (size_t)R * L.S_part);
+  L.lists = o;       o += up(sizeof(unsigned long long) * (size_t)R * L.S_list * L.klist);
+  L.rowres = o;      o += up(L.klist > 0 ? sizeof(int2) * (size_t)R * (L.klist + 1) : 0);
+  L.chunk = o;       o += up(sizeof(double) * (size_t)B * L.C_max);
+  L.total = o;
+  return L;
+}
+
+bool sizes_ok(int B, int gamma, int V) {
+  return B >= 0 && gamma >= 0 && gamma <= SV_MAX_GAMMA && V >= 1 && V <= SV_MAX_VOCAB &&
+         (long long)B * (gamma + 1) <= (1ll << 24);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+int vec_width(sv_dtype dt) { return dt == SV_DTYPE_F32 ? 4 : 8; }
+
+// Carve the workspace and fill the pointer fields of p.
+void bind_workspace(sv::Params& p, const Layout& L, void* ws) {
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  p.seq_ticket = reinterpret_cast<int*>(w + L.seq_ticket);
+  p.seq_ticket2 = reinterpret_cast<int*>(w + L.seq_ticket2);
+  p.row_ticket = reinterpret_cast<int*>(w + L.row_ticket);
+  p.seq = reinterpret_cast<sv::SeqState*>(w + L.seq);
+  p.acc = reinterpret_cast<double*>(w + L.acc);
+  p.part = reinterpret_cast<float4*>(w + L.part);
+  p.lists = reinterpret_cast<unsigned long long*>(w + L.lists);
+  p.rowres = reinterpret_cast<int2*>(w + L.rowres);
+  p.chunk_mass = reinterpret_cast<double*>(w + L.chunk);
+}
+
+// Rows-kernel slicing: 8 vectors per thread unless that leaves fewer than two
+// CTAs per SM, in which case the slices shrink (latency-bound small batches).
+void choose_slices(sv::Params& p, sv_dtype dt, bool topk) {
+  const int VW = vec_width(dt);
+  const long long R = (long long)p.B * (p.gamma + 1);
+  int U = sv::kMaxU;
+  if (!topk) {
+    const long long want = 2ll * sm_count();
+    while (U > 1 && R * ceil_div(p.V, (long long)sv::kThreads * U * VW) < want) U >>= 1;
+  }
+  p.U = U;
+  p.SL = sv::kThreads * U * VW;
+  p.S = (int)ceil_div(p.V, p.SL);
+}
+
+// Residual-kernel chunking: 32, 16 or 8 elements per thread, the largest that
+// still gives two CTAs per SM.
+void choose_chunks(sv::Params& p) {
+  const long long want = 2ll * sm_count();
+  int ept = sv::kResMaxEPT;
+  while (ept > 8 && (long long)p.B * ceil_div(p.V, (long long)sv::kThreads * ept) < want) ept >>= 1;
+  p.EPT = ept;
+  p.CL = sv::kThreads * ept;
+  p.C = (int)ceil_div(p.V, p.CL);
+}
+
+template <typename T, int MODE>
+sv_status launch_rows(const sv::Params& p, cudaStream_t stream) {
+  const size_t smem = MODE == sv::MODE_TOPK ? sizeof(sv::RowsSmem) : offsetof(sv::RowsSmem, cand);
+  auto kern = sv::rows_kernel<T, MODE>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return SV_ERR_CUDA;
+  const long long grid = (long long)p.B * (p.gamma + 1) * p.S;
+  kern<<<(unsigned)grid, sv::kThreads, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+template <typename T>
+sv_status launch_residual(const sv::Params& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long long)p.B * p.C));
+  cfg.blockDim = dim3(sv::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, sv::residual_kernel<T>, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+template <typename T>
+sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream) {
+  timing_record(0, stream);
+  sv_status st = SV_OK;
+  if (mode == sv::MODE_GREEDY) st = launch_rows<T, sv::MODE_GREEDY>(p, stream);
+  else if (mode == sv::MODE_TOPK) st = launch_rows<T, sv::MODE_TOPK>(p, stream);
+  else st = launch_rows<T, sv::MODE_SOFTMAX>(p, stream);
+  if (st != SV_OK) return st;
+  timing_record(1, stream);
+  if (mode == sv::MODE_SOFTMAX) st = launch_residual<T>(p, stream);
+  timing_record(2, stream);
+  return st;
+}
+
+sv_status run(sv::Params& p, sv_dtype dt, int mode, void* workspace, size_t workspace_bytes, int top_k_layout,
+              cudaStream_t stream) {
+  const Layout L = make_layout(p.B, p.gamma, p.V, top_k_layout);
+  if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return SV_ERR_WORKSPACE;
+  bind_workspace(p, L, workspace);
+  choose_slices(p, dt, mode == sv::MODE_TOPK);
+  if (mode == sv::MODE_SOFTMAX) choose_chunks(p);
+  switch (dt) {
+    case SV_DTYPE_F32: return dispatch<float>(p, mode, stream);
+    case SV_DTYPE_BF16: return dispatch<__nv_bfloat16>(p, mode, stream);
+    case SV_DTYPE_F16: return dispatch<__half>(p, mode, stream);
+  }
+  return SV_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" size_t sv_workspace_bytes(int B, int gamma, int V, int top_k) {
+  if (!sizes_ok(B, gamma, V) || top_k < 0 || top_k > SV_MAX_TOP_K) return 0;
+  return make_layout(B, gamma, V, top_k).total;
+}
+
+extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                                      const float* q, const int32_t* draft_tokens, const float* uniforms,
+                                      float temperature, int top_k, float top_p, int32_t* out_tokens,
+                                      int32_t* out_num_accepted, float* out_accept_prob, int32_t* out_status,
+                                      void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
+  if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
+    return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  if (top_k < 0 || top_k > SV_MAX_TOP_K) return SV_ERR_INVALID_ARG;
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !uniforms || !out_tokens || !out_num_accepted) return SV_ERR_INVALID_ARG;
+  if (gamma > 0 && (!q || !draft_tokens)) return SV_ERR_INVALID_ARG;
+  if (!aligned16(logits) || (gamma > 0 && !aligned16(q))) return SV_ERR_INVALID_ARG;
+
+  // top-k below V, or top-p: the candidate-list path.  top-p without an
+  // effective top-k ranks the whole vocabulary, supported for V <= SV_MAX_TOP_K.
+  const bool truncate = (top_k > 0 && top_k < V) || top_p < 1.0f;
+  int klist = 0;
+  if (truncate) {
+    klist = (top_k > 0 && top_k < V) ? top_k : V;
+    if (klist > SV_MAX_TOP_K) return SV_ERR_UNSUPPORTED;
+  }
+
+  sv::Params p{};
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.top_k = klist;
+  p.top_p = top_p;
+  p.c = (float)(1.4426950408889634 / (double)temperature);
+  p.logits = logits;
+  p.q = q;
+  p.draft = draft_tokens;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.out_n = out_num_accepted;
+  p.out_a = out_accept_prob;
+  p.out_status = out_status;
+  // list_len(V, top_k) == klist whenever truncate holds
+  return run(p, logits_dtype, truncate ? sv::MODE_TOPK : sv::MODE_SOFTMAX, workspace, workspace_bytes, top_k,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" sv_status sv_verify_greedy(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                                      const int32_t* draft_tokens, int32_t* out_tokens, int32_t* out_num_accepted,
+                                      int32_t* out_status, void* workspace, size_t workspace_bytes,
+                                      sv_stream_t stream) {
+  if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
+  if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
+    return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !out_tokens || !out_num_accepted) return SV_ERR_INVALID_ARG;
+  if (gamma > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;
+  if (!aligned16(logits)) return SV_ERR_INVALID_ARG;
+  sv::Params p{};
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.top_k = 0;
+  p.top_p = 1.0f;
+  p.c = 1.0f;
+  p.logits = logits;
+  p.draft = draft_tokens;
+  p.out_tokens = out_tokens;
+  p.out_n = out_num_accepted;
+  p.out_status = out_status;
+  return run(p, logits_dtype, sv::MODE_GREEDY, workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "SV_OK";
+    case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: a size, pointer, alignment or parameter is invalid";
+    case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: valid arguments this library does not implement";
+    case SV_ERR_WORKSPACE: return "SV_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA launch or runtime call failed";
+    case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded device wait gave up";
+  }
+  return "unknown sv_status";
+}
+
+extern "C" sv_status sv_set_timing_events(void* const* events, int n) {
+  if (n == 0) {
+    g_timing_on = false;
+    g_timing[0] = g_timing[1] = g_timing[2] = nullptr;
+    return SV_OK;
+  }
+  if (n != 3 || events == nullptr || !events[0] || !events[1] || !events[2]) return SV_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i) g_timing[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+  g_timing_on = true;
+  return SV_OK;
+}

@@ -1,0 +1,1122 @@
+// Device code of libspecverify: the batched verify/sample step of speculative
+// decoding for sm_103a (GB300).
+//
+// The operation follows "11.1 核心原理: Draft + Verify 与 Rejection Sampling"
+// (sections 11.1.1-11.1.3, code listing 10-1) and the notes "Fast Inference
+// from Transformers via Speculative Decoding" (speculative-sampling paragraph):
+// p_i = softmax(logits_i / T) (optionally top-k then top-p), accept d_i iff
+// u_i < min(1, p_i(d_i) / q_i(d_i)), stop at the first rejection n, then draw
+// from norm(max(p_n - q_n, 0)), or the bonus from p_gamma if all accepted.
+// Greedy: accept while d_i == argmax p_i.
+//
+// Nothing here is a dense contraction: every kernel is bound by HBM bandwidth
+// (the logits are streamed once; one row per sequence is touched again by the
+// final draw).  Layout of the work:
+//
+//   rows_kernel      one CTA per (row, vocabulary slice); the slice is held in
+//                    registers (U x 16-byte vectors per thread, 128-bit
+//                    coalesced loads), reduced to a per-slice partial in
+//                    workspace.  The last CTA to finish a sequence (an atomic
+//                    ticket, no CTA ever waits) merges the partials and runs the
+//                    acceptance scan.  In top-k mode a per-row ticket first
+//                    merges the per-slice candidate lists of a row.
+//   residual_kernel  (untruncated sampling) one CTA per (sequence, chunk) of
+//                    the one row each sequence draws from: chunk masses of
+//                    max(p - q, 0) (or p for the bonus), then the last CTA of the
+//                    sequence locates the inverse-CDF step chunk -> thread ->
+//                    element using exactly the same float32 partial sums.
+//
+// Data problems never trap: they set per-sequence status bits.  There are no
+// spin-waits: cross-CTA hand-off is only "last arriving CTA continues".
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxU = 8;          // 16-byte vectors per thread per slice
+constexpr int kCandCap = 2048;    // top-k candidate buffer (entries) per CTA
+constexpr int kMaxK = 1024;       // largest top-k list
+constexpr int kMaxG1 = 65;        // gamma + 1 <= 65
+constexpr int kResMaxEPT = 32;    // residual kernel: elements per thread (max)
+
+// per-sequence status bits (same values as the public header)
+constexpr int SEQ_OOB = 1;
+constexpr int SEQ_QBAD = 2;
+constexpr int SEQ_BADROW = 4;
+constexpr int SEQ_RESID0 = 8;
+
+struct SeqState {
+  int n;          // accepted count
+  int status;     // SEQ_* bits gathered so far
+  float M;        // max logit of the row the final draw uses
+  int pad;
+  double s;       // sum_v 2^((L_v - M) c) of that row
+};
+
+struct Params {
+  int B, gamma, V;
+  int S, U, SL;          // rows kernel: slices per row, vectors per thread, slice length
+  int C, CL, EPT;        // residual kernel: chunks per row, chunk length, elements per thread
+  int top_k;             // top-k list length (top-k mode)
+  float top_p;
+  float c;               // log2(e) / temperature
+  const void* logits;
+  const float* q;
+  const int32_t* draft;
+  const float* uniforms;
+  int32_t* out_tokens;
+  int32_t* out_n;
+  float* out_a;
+  int32_t* out_status;
+  int* seq_ticket;
+  int* seq_ticket2;
+  int* row_ticket;
+  SeqState* seq;
+  double* acc;                    // [B][gamma] acceptance probabilities (top-k mode)
+  float4* part;                   // [R][S] per-slice partials
+  unsigned long long* lists;      // [R][S][top_k] per-slice top-k candidates
+  int2* rowres;                   // [R][top_k + 1] kept (index, probability) lists
+  double* chunk_mass;             // [B][C * slots] residual sub-range masses
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue early / wait until this grid's memory is visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+}
+__device__ __forceinline__ void set_word(uint4& v, int w, uint32_t x) {
+  if (w == 0) v.x = x; else if (w == 1) v.y = x; else if (w == 2) v.z = x; else v.w = x;
+}
+
+// Order-preserving 32-bit key of a float; -0.0 is first made +0.0 so that equal
+// values get equal keys.
+__device__ __forceinline__ uint32_t okey(float x) {
+  uint32_t u = __float_as_uint(x + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+// Composite ranking key: larger value first, then lower index first.
+__device__ __forceinline__ unsigned long long comp_key(float x, int idx) {
+  return ((unsigned long long)okey(x) << 32) | (unsigned long long)(~(uint32_t)idx);
+}
+__device__ __forceinline__ int comp_idx(unsigned long long c) {
+  return (int)(~(uint32_t)(c & 0xffffffffull));
+}
+__device__ __forceinline__ float comp_val(unsigned long long c) {
+  return key_to_float((uint32_t)(c >> 32));
+}
+
+// ------------------------------------------------------------------ dtype traits
+
+template <typename T> struct Tr;
+
+template <> struct Tr<float> {
+  static constexpr int VW = 4;                // elements per 16-byte vector
+  static constexpr int KEY_LOW_BIT = 0;       // lowest key bit that can differ
+  static constexpr uint32_t kPadWord = 0xff800000u;   // -inf
+  __device__ static __forceinline__ float get(const uint4& v, int t) {
+    return __uint_as_float(word_of(v, t));
+  }
+  __device__ static __forceinline__ uint32_t scalar_bits(const float* p) {
+    return __ldg(reinterpret_cast<const unsigned int*>(p));
+  }
+  __device__ static __forceinline__ void put(uint4& v, int t, uint32_t bits) { set_word(v, t, bits); }
+  // max of the 4 values; NANPROP: a NaN anywhere gives NaN
+  template <bool NANPROP>
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    float a = __uint_as_float(v.x), b = __uint_as_float(v.y);
+    float c = __uint_as_float(v.z), d = __uint_as_float(v.w);
+    float m = fmaxf(fmaxf(a, b), fmaxf(c, d));
+    if (NANPROP && (a != a || b != b || c != c || d != d)) m = __uint_as_float(0x7fffffffu);
+    return m;
+  }
+};
+
+template <> struct Tr<__nv_bfloat16> {
+  static constexpr int VW = 8;
+  static constexpr int KEY_LOW_BIT = 16;
+  static constexpr uint32_t kPadWord = 0xff80ff80u;
+  __device__ static __forceinline__ float get(const uint4& v, int t) {
+    uint32_t w = word_of(v, t >> 1);
+    uint32_t bits = (t & 1) ? (w & 0xffff0000u) : (w << 16);
+    return __uint_as_float(bits);
+  }
+  __device__ static __forceinline__ uint32_t scalar_bits(const __nv_bfloat16* p) {
+    return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
+  }
+  __device__ static __forceinline__ void put(uint4& v, int t, uint32_t bits) {
+    uint32_t w = word_of(v, t >> 1);
+    w = (t & 1) ? ((w & 0x0000ffffu) | (bits << 16)) : ((w & 0xffff0000u) | bits);
+    set_word(v, t >> 1, w);
+  }
+  template <bool NANPROP>
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+    __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+    __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+    __nv_bfloat162 m = NANPROP ? __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d))
+                               : __hmax2(__hmax2(a, b), __hmax2(c, d));
+    float lo = __low2float(m), hi = __high2float(m);
+    if (NANPROP && (lo != lo || hi != hi)) return __uint_as_float(0x7fffffffu);
+    return fmaxf(lo, hi);
+  }
+};
+
+template <> struct Tr<__half> {
+  static constexpr int VW = 8;
+  static constexpr int KEY_LOW_BIT = 13;
+  static constexpr uint32_t kPadWord = 0xfc00fc00u;
+  __device__ static __forceinline__ float get(const uint4& v, int t) {
+    uint32_t w = word_of(v, t >> 1);
+    unsigned short bits = (unsigned short)((t & 1) ? (w >> 16) : (w & 0xffffu));
+    return __half2float(__ushort_as_half(bits));
+  }
+  __device__ static __forceinline__ uint32_t scalar_bits(const __half* p) {
+    return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
+  }
+  __device__ static __forceinline__ void put(uint4& v, int t, uint32_t bits) {
+    uint32_t w = word_of(v, t >> 1);
+    w = (t & 1) ? ((w & 0x0000ffffu) | (bits << 16)) : ((w & 0xffff0000u) | bits);
+    set_word(v, t >> 1, w);
+  }
+  template <bool NANPROP>
+  __device__ static __forceinline__ float vmax(const uint4& v) {
+    __half2 a = *reinterpret_cast<const __half2*>(&v.x);
+    __half2 b = *reinterpret_cast<const __half2*>(&v.y);
+    __half2 c = *reinterpret_cast<const __half2*>(&v.z);
+    __half2 d = *reinterpret_cast<const __half2*>(&v.w);
+    __half2 m = NANPROP ? __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d))
+                        : __hmax2(__hmax2(a, b), __hmax2(c, d));
+    float lo = __low2float(m), hi = __high2float(m);
+    if (NANPROP && (lo != lo || hi != hi)) return __uint_as_float(0x7fffffffu);
+    return fmaxf(lo, hi);
+  }
+};
+
+// One 16-byte slot of VW elements starting at element e0 of `row`; the first
+// nv (1..VW) are real, the rest are -inf.  Vector load when the slot is full and
+// 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ uint4 load_slot(const T* row, int e0, int nv, bool vec_ok) {
+  using TR = Tr<T>;
+  if (nv == TR::VW && vec_ok) return ldg_v4(row + e0);
+  uint4 v = make_uint4(TR::kPadWord, TR::kPadWord, TR::kPadWord, TR::kPadWord);
+#pragma unroll
+  for (int t = 0; t < TR::VW; ++t)
+    if (t < nv) TR::put(v, t, TR::scalar_bits(row + e0 + t));
+  return v;
+}
+
+// ------------------------------------------------------------------ reductions
+
+// Two-float (hi + lo) sums: error-free transformation per addition, so block
+// totals keep about 44 bits while every operation stays on the float32 pipes.
+struct F2 {
+  float hi, lo;
+};
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  float s = a.hi + b.hi;
+  float bb = s - a.hi;
+  float e = (a.hi - (s - bb)) + (b.hi - bb);
+  e += a.lo + b.lo;
+  float h = s + e;
+  return F2{h, e - (h - s)};
+}
+__device__ __forceinline__ F2 f2_shfl_xor(F2 a, int m) {
+  return F2{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
+}
+__device__ __forceinline__ F2 f2_shfl_up(F2 a, int m) {
+  return F2{__shfl_up_sync(0xffffffffu, a.hi, m), __shfl_up_sync(0xffffffffu, a.lo, m)};
+}
+
+// Block-wide F2 sum; every thread gets the total.  Uses `sm` (kWarps entries).
+__device__ __forceinline__ F2 block_sum_f2(F2 v, F2* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = f2_add(v, f2_shfl_xor(v, m));
+  __syncthreads();
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  F2 t = sm[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) t = f2_add(t, sm[w]);
+  return t;
+}
+
+// Block-wide exclusive prefix of F2 values in thread order, plus the total.
+__device__ __forceinline__ F2 block_exclusive_f2(F2 v, F2* sm, F2* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  F2 inc = v;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    F2 o = f2_shfl_up(inc, m);
+    if (lane >= m) inc = f2_add(o, inc);
+  }
+  __syncthreads();
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  F2 base{0.f, 0.f}, tot{0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) base = f2_add(base, sm[w]);
+    tot = f2_add(tot, sm[w]);
+  }
+  *total = tot;
+  // exclusive prefix = warp base + inclusive prefix of the lane below
+  F2 below = f2_shfl_up(inc, 1);
+  if (lane == 0) below = F2{0.f, 0.f};
+  return f2_add(base, below);
+}
+
+__device__ __forceinline__ float block_max(float v, float* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  __syncthreads();
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  float t = sm[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) t = fmaxf(t, sm[w]);
+  return t;
+}
+
+__device__ __forceinline__ int block_sum_int(int v, int* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  __syncthreads();
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += sm[w];
+  return t;
+}
+
+// "Does (va, ia) beat (vb, ib)?" for the greedy argmax: a larger value wins,
+// equal values (-0.0 == +0.0) go to the lower index; NaN wins (it is flagged).
+__device__ __forceinline__ bool argmax_better(float va, int ia, float vb, int ib) {
+  const bool na = va != va, nb = vb != vb;
+  if (na || nb) return (na && nb) ? (ia < ib) : na;
+  if (va > vb) return true;
+  if (va < vb) return false;
+  return ia < ib;
+}
+
+// Last-arriving-CTA hand-off.  Every thread publishes its writes, one thread
+// takes a ticket; the CTA that takes ticket count-1 resets the counter and
+// returns true (its later reads of other CTAs' data use ld.global.cg).
+__device__ __forceinline__ bool arrive_last(int* ticket, int count, int* s_flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(ticket, 1);
+    const int last = (prev == count - 1);
+    if (last) *ticket = 0;
+    *s_flag = last;
+  }
+  __syncthreads();
+  const bool last = *s_flag != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// ------------------------------------------------------------------ rows kernel
+
+enum { MODE_GREEDY = 0, MODE_SOFTMAX = 1, MODE_TOPK = 2 };
+
+struct RowsSmem {
+  float fred[kWarps];
+  int ired[kWarps];
+  F2 f2red[kWarps];
+  float2 pair[kWarps];
+  int flag;
+  int count;
+  int n;
+  int token;
+  float M[kMaxG1];
+  double s[kMaxG1];
+  double a[kMaxG1];
+  int g[kMaxG1];
+  int bad[kMaxG1];
+  int status;
+  double dred[kWarps];
+  unsigned long long cand[kCandCap];   // top-k candidates; reused by the row merge
+  unsigned long long mout[kMaxK];
+  double w[kMaxK];
+  int widx[kMaxK];
+};
+
+// Greedy / softmax sequence finisher: merge the S partials of each of the
+// gamma+1 rows, then the acceptance scan.
+template <typename T, int MODE>
+__device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
+  const int tid = threadIdx.x;
+  const int G = p.gamma, G1 = G + 1, V = p.V;
+  if (tid < G1) {
+    const int rr = b * G1 + tid;
+    const float4* pp = p.part + (size_t)rr * p.S;
+    if (MODE == MODE_GREEDY) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int s2 = 0; s2 < p.S; ++s2) {
+        const float4 v = __ldcg(pp + s2);
+        const int vi = __float_as_int(v.y);
+        if (argmax_better(v.x, vi, bv, bi)) { bv = v.x; bi = vi; }
+      }
+      const bool nan = bv != bv;
+      sm.g[tid] = (nan || bi == 0x7fffffff) ? 0 : bi;
+      sm.bad[tid] = nan ? 1 : 0;
+    } else {
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < p.S; ++s2) M = fmaxf(M, __ldcg(pp + s2).x);
+      double s = 0.0;
+      if (M > -INFINITY && M < INFINITY) {
+        for (int s2 = 0; s2 < p.S; ++s2) {
+          const float4 v = __ldcg(pp + s2);
+          if (v.x > -INFINITY) s += ((double)v.y + (double)v.z) * (double)exp2f((v.x - M) * p.c);
+        }
+      }
+      const bool bad = !(M > -INFINITY && M < INFINITY) || !(s > 0.0 && s < 1e300);
+      sm.M[tid] = M;
+      sm.s[tid] = s;
+      sm.bad[tid] = bad ? 1 : 0;
+      if (tid < G) {
+        const int d = p.draft[b * G + tid];
+        double a = 0.0;
+        int st = 0;
+        if (d < 0 || d >= V) {
+          st |= SEQ_OOB;
+        } else {
+          const T* row = static_cast<const T*>(p.logits) + (size_t)rr * V;
+          const float l = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
+          const float qd = __ldg(p.q + ((size_t)b * G + tid) * V + d);
+          const double pd = bad ? 0.0 : exp2(((double)l - (double)M) * (double)p.c) / s;
+          if (qd > 0.0f) {
+            a = fmin(1.0, pd / (double)qd);
+          } else {
+            a = pd > 0.0 ? 1.0 : 0.0;
+            st |= SEQ_QBAD;
+          }
+        }
+        sm.a[tid] = a;
+        sm.g[tid] = st;
+        if (p.out_a) p.out_a[b * G + tid] = (float)a;
+      }
+    }
+  }
+  __syncthreads();
+  // every partial of this sequence has been read: leave the workspace zeroed
+  for (int e = tid; e < G1 * p.S; e += kThreads)
+    p.part[(size_t)b * G1 * p.S + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid == 0) {
+    int status = 0, n = G;
+    for (int i = 0; i < G1; ++i)
+      if (sm.bad[i]) status |= SEQ_BADROW;
+    if (MODE == MODE_GREEDY) {
+      for (int i = 0; i < G; ++i) {
+        const int d = p.draft[b * G + i];
+        if (d < 0 || d >= V) status |= SEQ_OOB;
+      }
+      for (int i = 0; i < G; ++i)
+        if (p.draft[b * G + i] != sm.g[i]) { n = i; break; }
+      sm.token = sm.g[n];
+    } else {
+      for (int i = 0; i < G; ++i) status |= sm.g[i];
+      for (int i = 0; i < G; ++i) {
+        const double u = (double)p.uniforms[b * G1 + i];
+        if (!(u < sm.a[i])) { n = i; break; }
+      }
+      SeqState st;
+      st.n = n;
+      st.status = status;
+      st.M = sm.M[n];
+      st.pad = 0;
+      st.s = sm.s[n];
+      p.seq[b] = st;
+    }
+    sm.n = n;
+    sm.status = status;
+    p.out_n[b] = n;
+    if (MODE == MODE_GREEDY && p.out_status) p.out_status[b] = status;
+  }
+  __syncthreads();
+  const int n = sm.n;
+  for (int j = tid; j < G1; j += kThreads) {
+    if (j < n) p.out_tokens[b * G1 + j] = p.draft[b * G + j];
+    else if (j > n) p.out_tokens[b * G1 + j] = -1;
+    else if (MODE == MODE_GREEDY) p.out_tokens[b * G1 + j] = sm.token;
+  }
+}
+
+// Number of entries of the descending list X[0..n) that beat key v.
+__device__ __forceinline__ int count_greater(const unsigned long long* X, int n, unsigned long long v) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (X[mid] > v) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Top-k row finisher: merge the S per-slice lists of row rr into the row's
+// top-k, apply softmax(./T) over it, cut by top-p, renormalise, store the kept
+// (index, probability) list and the acceptance probability of the row's draft.
+__device__ void finish_row_topk(const Params& p, int b, int i, int rr, RowsSmem& sm) {
+  const int tid = threadIdx.x;
+  const int k = p.top_k, G = p.gamma, V = p.V;
+  unsigned long long* A = sm.cand;            // running merged list
+  unsigned long long* Bl = sm.cand + kMaxK;   // next slice list
+  unsigned long long* O = sm.mout;
+  const unsigned long long* L0 = p.lists + (size_t)rr * p.S * k;
+  int na = 0;
+  {
+    int c = 0;
+    for (int e = tid; e < k; e += kThreads) {
+      const unsigned long long v = __ldcg(L0 + e);
+      A[e] = v;
+      c += v != 0ull;
+    }
+    na = block_sum_int(c, sm.ired);
+  }
+  for (int s2 = 1; s2 < p.S; ++s2) {
+    const unsigned long long* Ls = L0 + (size_t)s2 * k;
+    int c = 0;
+    for (int e = tid; e < k; e += kThreads) {
+      const unsigned long long v = __ldcg(Ls + e);
+      Bl[e] = v;
+      c += v != 0ull;
+    }
+    const int nb = block_sum_int(c, sm.ired);   // includes a __syncthreads
+    for (int e = tid; e < na; e += kThreads) {
+      const int rank = e + count_greater(Bl, nb, A[e]);
+      if (rank < k) O[rank] = A[e];
+    }
+    for (int e = tid; e < nb; e += kThreads) {
+      const int rank = e + count_greater(A, na, Bl[e]);
+      if (rank < k) O[rank] = Bl[e];
+    }
+    na = min(k, na + nb);
+    __syncthreads();
+    for (int e = tid; e < na; e += kThreads) A[e] = O[e];
+    __syncthreads();
+  }
+  // the slice lists have been consumed: leave the workspace zeroed
+  for (int e = tid; e < p.S * k; e += kThreads) p.lists[(size_t)rr * p.S * k + e] = 0ull;
+  // softmax over the merged top-k (descending), then the top-p cut
+  const float m = na > 0 ? comp_val(A[0]) : -INFINITY;
+  const bool bad = !(m > -INFINITY && m < INFINITY);
+  for (int e = tid; e < na; e += kThreads) {
+    sm.w[e] = bad ? 0.0 : (double)exp2f((comp_val(A[e]) - m) * p.c);
+    sm.widx[e] = comp_idx(A[e]);
+  }
+  __syncthreads();
+  int2* out = p.rowres + (size_t)rr * (k + 1);
+  if (tid == 0) {
+    int J = na;
+    double W = 0.0;
+    for (int e = 0; e < na; ++e) W += sm.w[e];
+    if (bad || na == 0) {
+      J = na > 0 ? 1 : 0;
+      if (na > 0) sm.w[0] = 1.0;
+      W = 1.0;
+      if (bad) atomicOr(&p.seq[b].status, SEQ_BADROW);
+    } else if (p.top_p < 1.0f) {
+      const double tp = (double)p.top_p;
+      double cum = 0.0;
+      for (int e = 0; e < na; ++e) {
+        cum += sm.w[e];
+        if (cum / W >= tp) { J = e + 1; break; }
+      }
+    }
+    double WJ = 0.0;
+    for (int e = 0; e < J; ++e) WJ += sm.w[e];
+    sm.count = J;
+    sm.s[0] = WJ;
+    out[0] = make_int2(J, 0);
+  }
+  __syncthreads();
+  const int J = sm.count;
+  const double WJ = sm.s[0];
+  for (int e = tid; e < J; e += kThreads)
+    out[1 + e] = make_int2(sm.widx[e], __float_as_int((float)(sm.w[e] / WJ)));
+  // acceptance probability of this row's draft
+  if (i < G) {
+    const int d = p.draft[b * G + i];
+    if (tid == 0) sm.dred[0] = 0.0;
+    __syncthreads();
+    if (d >= 0 && d < V)
+      for (int e = tid; e < J; e += kThreads)
+        if (sm.widx[e] == d) sm.dred[0] = sm.w[e] / WJ;
+    __syncthreads();
+    if (tid == 0) {
+      double a = 0.0;
+      int st = 0;
+      if (d < 0 || d >= V) {
+        st |= SEQ_OOB;
+      } else {
+        const double pd = sm.dred[0];
+        const float qd = __ldg(p.q + ((size_t)b * G + i) * V + d);
+        if (qd > 0.0f) {
+          a = fmin(1.0, pd / (double)qd);
+        } else {
+          a = pd > 0.0 ? 1.0 : 0.0;
+          st |= SEQ_QBAD;
+        }
+      }
+      if (st) atomicOr(&p.seq[b].status, st);
+      p.acc[b * G + i] = a;
+      if (p.out_a) p.out_a[b * G + i] = (float)a;
+    }
+  }
+}
+
+// Top-k sequence finisher: scan, then the final draw from the kept list of
+// row n (residual against q gathered at the kept indices) or row gamma.
+__device__ void finish_sequence_topk(const Params& p, int b, RowsSmem& sm) {
+  const int tid = threadIdx.x;
+  const int k = p.top_k, G = p.gamma, G1 = G + 1, V = p.V;
+  if (tid == 0) {
+    int n = G;
+    for (int i = 0; i < G; ++i) {
+      const double u = (double)p.uniforms[b * G1 + i];
+      if (!(u < __ldcg(p.acc + b * G + i))) { n = i; break; }
+    }
+    sm.n = n;
+    sm.status = __ldcg(&p.seq[b].status);
+  }
+  __syncthreads();
+  const int n = sm.n;
+  const int rr = b * G1 + n;
+  const int2* kept = p.rowres + (size_t)rr * (k + 1);
+  const int J = __ldcg(kept).x;
+  const bool resid = n < G;
+  const float* qrow = resid ? p.q + ((size_t)b * G + n) * V : nullptr;
+  // r_j in index order: rank each kept entry by its index
+  for (int e = tid; e < J; e += kThreads) {
+    const int2 en = __ldcg(kept + 1 + e);
+    sm.widx[e] = en.x;
+    sm.w[e] = (double)__int_as_float(en.y);
+  }
+  __syncthreads();
+  for (int e = tid; e < J; e += kThreads) {
+    const int me = sm.widx[e];
+    int rank = 0;
+    for (int j = 0; j < J; ++j) rank += sm.widx[j] < me;
+    double r = sm.w[e];
+    if (resid) r = fmax(r - (double)__ldg(qrow + me), 0.0);
+    sm.mout[rank] = (unsigned long long)me;
+    reinterpret_cast<double*>(sm.cand)[rank] = r;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double* rs = reinterpret_cast<double*>(sm.cand);
+    int status = sm.status;
+    double R = 0.0;
+    for (int e = 0; e < J; ++e) R += rs[e];
+    if (resid && !(R > 0.0)) {
+      // zero residual mass (only through rounding): draw from p_n instead
+      status |= SEQ_RESID0;
+      for (int e = 0; e < J; ++e) {
+        double pe = 0.0;
+        for (int j = 0; j < J; ++j)
+          if (sm.widx[j] == (int)sm.mout[e]) pe = sm.w[j];
+        rs[e] = pe;
+      }
+      R = 0.0;
+      for (int e = 0; e < J; ++e) R += rs[e];
+    }
+    const double t = (double)p.uniforms[b * G1 + G] * R;
+    int tok = -1, lastpos = -1;
+    double C = 0.0;
+    for (int e = 0; e < J; ++e) {
+      C += rs[e];
+      if (rs[e] > 0.0) lastpos = e;
+      if (C > t) { tok = (int)sm.mout[e]; break; }
+    }
+    if (tok < 0) tok = lastpos >= 0 ? (int)sm.mout[lastpos] : (J > 0 ? (int)sm.mout[0] : 0);
+    if (tok < 0 || tok >= V) tok = 0;
+    sm.token = tok;
+    p.out_n[b] = n;
+    if (p.out_status) p.out_status[b] = status;
+    p.seq[b].status = 0;
+  }
+  __syncthreads();
+  for (int j = tid; j < G1; j += kThreads)
+    p.out_tokens[b * G1 + j] = j < n ? p.draft[b * G + j] : (j == n ? sm.token : -1);
+  // kept lists and acceptance probabilities have been consumed: zero them
+  for (int e = tid; e < G1 * (k + 1); e += kThreads) p.rowres[(size_t)b * G1 * (k + 1) + e] = make_int2(0, 0);
+  for (int e = tid; e < G; e += kThreads) p.acc[b * G + e] = 0.0;
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kThreads)
+rows_kernel(const Params p) {
+  using TR = Tr<T>;
+  constexpr int VW = TR::VW;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  RowsSmem& sm = *reinterpret_cast<RowsSmem*>(smem_raw);
+
+  const int tid = threadIdx.x;
+  const int G1 = p.gamma + 1;
+  const int s = blockIdx.x % p.S;
+  const int r = blockIdx.x / p.S;
+  const int b = r / G1;
+  const int i = r - b * G1;
+
+  pdl_launch_dependents();
+
+  const T* row = static_cast<const T*>(p.logits) + (size_t)r * p.V;
+  const int s0 = s * p.SL;
+  const int s1 = min(s0 + p.SL, p.V);
+  const bool vec_ok = (p.V % VW) == 0;
+
+  // the whole slice goes to registers first: U 16-byte loads in flight per thread
+  uint4 buf[kMaxU];
+#pragma unroll
+  for (int j = 0; j < kMaxU; ++j) {
+    buf[j] = make_uint4(TR::kPadWord, TR::kPadWord, TR::kPadWord, TR::kPadWord);
+    if (j < p.U) {
+      const int e0 = s0 + (j * kThreads + tid) * VW;
+      const int nv = min(max(s1 - e0, 0), VW);
+      if (nv > 0) buf[j] = load_slot<T>(row, e0, nv, vec_ok);
+    }
+  }
+
+  if (MODE == MODE_GREEDY) {
+    // thread max (NaN propagates), the first slot holding it, its first element
+    float tmax = -INFINITY;
+    int tslot = -1;
+#pragma unroll
+    for (int j = 0; j < kMaxU; ++j) {
+      if (j < p.U && s0 + (j * kThreads + tid) * VW < s1) {
+        const float m = TR::template vmax<true>(buf[j]);
+        if (tslot < 0 || argmax_better(m, 1, tmax, 0)) { tmax = m; tslot = j; }  // equal: keep the earlier slot
+      }
+    }
+    int tidx = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kMaxU; ++j) {
+      if (j == tslot) {
+        const int e0 = s0 + (j * kThreads + tid) * VW;
+        const int nv = min(s1 - e0, VW);
+#pragma unroll
+        for (int t = VW - 1; t >= 0; --t) {
+          const float x = TR::get(buf[j], t);
+          const bool hit = (tmax != tmax) ? (x != x) : (x == tmax);
+          if (t < nv && hit) tidx = e0 + t;
+        }
+      }
+    }
+    if (tslot < 0) tmax = -INFINITY;
+    // block argmax
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, tmax, m);
+      const int oi = __shfl_xor_sync(0xffffffffu, tidx, m);
+      if (argmax_better(ov, oi, tmax, tidx)) { tmax = ov; tidx = oi; }
+    }
+    if (lane == 0) sm.pair[warp] = make_float2(tmax, __int_as_float(tidx));
+    __syncthreads();
+    if (tid == 0) {
+      float bv = sm.pair[0].x;
+      int bi = __float_as_int(sm.pair[0].y);
+      for (int w = 1; w < kWarps; ++w) {
+        const float ov = sm.pair[w].x;
+        const int oi = __float_as_int(sm.pair[w].y);
+        if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      p.part[(size_t)r * p.S + s] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+    }
+    if (arrive_last(p.seq_ticket + b, p.S * G1, &sm.flag)) finish_sequence_dense<T, MODE>(p, b, sm);
+    return;
+  }
+
+  if (MODE == MODE_SOFTMAX) {
+    // slice max, then sum of 2^((x - M) c) over the registers
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxU; ++j)
+      if (j < p.U) tmax = fmaxf(tmax, TR::template vmax<false>(buf[j]));
+    const float M = block_max(tmax, sm.fred);
+    float a0 = 0.f, a1 = 0.f;
+    if (M > -INFINITY) {
+      const float Mc = M * p.c;
+#pragma unroll
+      for (int j = 0; j < kMaxU; ++j) {
+        if (j < p.U) {
+#pragma unroll
+          for (int t = 0; t < VW; t += 2) {
+            a0 += ex2_approx(fmaf(TR::get(buf[j], t), p.c, -Mc));
+            a1 += ex2_approx(fmaf(TR::get(buf[j], t + 1), p.c, -Mc));
+          }
+        }
+      }
+    }
+    F2 tot = block_sum_f2(F2{a0 + a1, 0.f}, sm.f2red);
+    if (tid == 0) p.part[(size_t)r * p.S + s] = make_float4(M, tot.hi, tot.lo, 0.f);
+    if (arrive_last(p.seq_ticket + b, p.S * G1, &sm.flag)) finish_sequence_dense<T, MODE>(p, b, sm);
+    return;
+  }
+
+  // ---------------------------------------------------------------- top-k mode
+  const int k = p.top_k;
+  float tmax = -INFINITY;
+  int has_nan = 0, nreal = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxU; ++j) {
+    if (j < p.U) {
+      const int e0 = s0 + (j * kThreads + tid) * VW;
+      const int nv = min(max(s1 - e0, 0), VW);
+#pragma unroll
+      for (int t = 0; t < VW; ++t) {
+        if (t < nv) {
+          const float x = TR::get(buf[j], t);
+          if (x != x) has_nan = 1;
+          else { tmax = fmaxf(tmax, x); ++nreal; }
+        }
+      }
+    }
+  }
+  if (tid == 0) sm.count = 0;
+  if (__syncthreads_or(has_nan) && tid == 0) atomicOr(&p.seq[b].status, SEQ_BADROW);
+  const int total_real = block_sum_int(nreal, sm.ired);
+  // threshold key K: the k-th largest of the per-thread maxima (a lower bound
+  // of the slice's k-th largest value: those k threads each hold one element >= it)
+  const uint32_t tkey = nreal > 0 ? okey(tmax) : 0u;
+  uint32_t K = 0u;
+  if (total_real > k) {
+    for (int bit = 31; bit >= TR::KEY_LOW_BIT; --bit) {
+      const uint32_t Kt = K | (1u << bit);
+      if (__syncthreads_count(tkey >= Kt) >= k) K = Kt;
+    }
+  }
+  // collect the candidates (value key >= K) into shared memory
+  auto collect = [&](auto pred) {
+    int mine = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxU; ++j) {
+      if (j < p.U) {
+        const int e0 = s0 + (j * kThreads + tid) * VW;
+        const int nv = min(max(s1 - e0, 0), VW);
+#pragma unroll
+        for (int t = 0; t < VW; ++t) {
+          const float x = TR::get(buf[j], t);
+          if (t < nv && x == x && pred(x, e0 + t)) ++mine;
+        }
+      }
+    }
+    const int lane = tid & 31;
+    int inc = mine;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, inc, m);
+      if (lane >= m) inc += o;
+    }
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&sm.count, inc);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int pos = base + inc - mine;
+#pragma unroll
+    for (int j = 0; j < kMaxU; ++j) {
+      if (j < p.U) {
+        const int e0 = s0 + (j * kThreads + tid) * VW;
+        const int nv = min(max(s1 - e0, 0), VW);
+#pragma unroll
+        for (int t = 0; t < VW; ++t) {
+          const float x = TR::get(buf[j], t);
+          if (t < nv && x == x && pred(x, e0 + t)) {
+            if (pos < kCandCap) sm.cand[pos] = comp_key(x, e0 + t);
+            ++pos;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    return sm.count;
+  };
+  int N = collect([&](float x, int) { return okey(x) >= K; });
+  if (N > kCandCap) {
+    // too many ties / too large k: find the exact k-th largest composite key by
+    // bisection over the slice held in registers, then collect exactly k
+    unsigned long long K64 = 0ull;
+    for (int bit = 63; bit >= 0; --bit) {
+      const unsigned long long Kt = K64 | (1ull << bit);
+      int mine = 0;
+#pragma unroll
+      for (int j = 0; j < kMaxU; ++j) {
+        if (j < p.U) {
+          const int e0 = s0 + (j * kThreads + tid) * VW;
+          const int nv = min(max(s1 - e0, 0), VW);
+#pragma unroll
+          for (int t = 0; t < VW; ++t) {
+            const float x = TR::get(buf[j], t);
+            if (t < nv && x == x && comp_key(x, e0 + t) >= Kt) ++mine;
+          }
+        }
+      }
+      if (block_sum_int(mine, sm.ired) >= k) K64 = Kt;
+    }
+    __syncthreads();
+    if (tid == 0) sm.count = 0;
+    __syncthreads();
+    N = collect([&](float x, int e) { return comp_key(x, e) >= K64; });
+  }
+  // rank-select the slice's top-k, written in descending order
+  const int kk = min(k, N);
+  unsigned long long* list = p.lists + ((size_t)r * p.S + s) * k;
+  for (int e = tid; e < N; e += kThreads) {
+    const unsigned long long me = sm.cand[e];
+    int rank = 0;
+    for (int j = 0; j < N; ++j) rank += sm.cand[j] > me;
+    if (rank < kk) list[rank] = me;
+  }
+  for (int e = kk + tid; e < k; e += kThreads) list[e] = 0ull;
+  if (!arrive_last(p.row_ticket + r, p.S, &sm.flag)) return;
+  finish_row_topk(p, b, i, r, sm);
+  if (!arrive_last(p.seq_ticket + b, G1, &sm.flag)) return;
+  finish_sequence_topk(p, b, sm);
+}
+
+// ------------------------------------------------------------------ residual kernel
+//
+// Element order.  A chunk of CL = 256 * EPT elements is read as NS = EPT / VW
+// "slots": slot j of thread t holds elements c0 + (j*256 + t)*VW + [0, VW), so
+// each warp-wide 16-byte load is coalesced.  Slot j of all threads is one
+// contiguous sub-range of the vocabulary, and the sub-ranges (chunk c, slot j)
+// follow the token index in (c, j) order.  The inverse-CDF search therefore
+// goes sub-range -> thread -> element, and every level sums exactly the same
+// float32 slot partials that the mass pass summed.
+
+// Sum over one slot (VW elements from e0, the first nv real) of
+//   r(v) = max(p(v) - q(v), 0)  (q != nullptr)   or   p(v)  (bonus),
+// p(v) = 2^((L_v - M) c) / s, in index order with explicit rounding steps so
+// that the search recomputes the same float32 value bit for bit.
+template <typename T>
+__device__ __forceinline__ float slot_mass(const T* row, const float* qrow, int e0, int nv, float c, float Mc,
+                                           float inv_s, bool vec_ok) {
+  using TR = Tr<T>;
+  constexpr int VW = TR::VW;
+  if (nv <= 0) return 0.f;
+  const uint4 v = load_slot<T>(row, e0, nv, vec_ok);
+  float qv[VW];
+  if (qrow) {
+    if (nv == VW && vec_ok) {
+#pragma unroll
+      for (int h = 0; h < VW; h += 4) {
+        const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow + e0 + h));
+        qv[h] = q4.x; qv[h + 1] = q4.y; qv[h + 2] = q4.z; qv[h + 3] = q4.w;
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < VW; ++t) qv[t] = t < nv ? __ldg(qrow + e0 + t) : 0.f;
+    }
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int t = 0; t < VW; ++t) {
+    if (t < nv) {
+      const float pv = __fmul_rn(ex2_approx(fmaf(TR::get(v, t), c, -Mc)), inv_s);
+      acc = __fadd_rn(acc, qrow ? fmaxf(__fsub_rn(pv, qv[t]), 0.f) : pv);
+    }
+  }
+  return acc;
+}
+
+// Walk one slot: the element at which base + (running float32 sum) first
+// exceeds target, or -1; *last_pos = the last element with a positive weight.
+template <typename T>
+__device__ __forceinline__ int slot_walk(const T* row, const float* qrow, int e0, int nv, float c, float Mc,
+                                         float inv_s, bool vec_ok, double base, double target, int* last_pos) {
+  using TR = Tr<T>;
+  int found = -1, lastp = -1;
+  if (nv > 0) {
+    const uint4 v = load_slot<T>(row, e0, nv, vec_ok);
+    float acc = 0.f;
+    for (int t = 0; t < nv; ++t) {
+      const float pv = __fmul_rn(ex2_approx(fmaf(TR::get(v, t), c, -Mc)), inv_s);
+      const float rv = qrow ? fmaxf(__fsub_rn(pv, __ldg(qrow + e0 + t)), 0.f) : pv;
+      acc = __fadd_rn(acc, rv);
+      if (rv > 0.f) lastp = e0 + t;
+      if (found < 0 && base + (double)acc > target) found = e0 + t;
+    }
+  }
+  *last_pos = lastp;
+  return found;
+}
+
+struct ResSmem {
+  F2 f2red[kWarps];
+  int ired[kWarps];
+  int flag;
+  int sub;        // selected sub-range (chunk * NS + slot), -1 if none
+  int token;
+  int use_p;
+  double target;
+  double base;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+residual_kernel(const Params p) {
+  using TR = Tr<T>;
+  constexpr int VW = TR::VW;
+  constexpr int kMaxNS = kResMaxEPT / VW;
+  __shared__ ResSmem sm;
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int c = blockIdx.x % p.C;
+  const int b = blockIdx.x / p.C;
+  const int G = p.gamma, G1 = G + 1, V = p.V;
+  const int NS = p.EPT / VW;              // slots per thread per chunk
+  const int NT = p.C * NS;                // sub-ranges per row
+  SeqState st;
+  st.n = __ldcg(&p.seq[b].n);
+  st.status = __ldcg(&p.seq[b].status);
+  st.M = __ldcg(&p.seq[b].M);
+  st.s = __ldcg(&p.seq[b].s);
+  const int n = st.n;
+  const bool resid = n < G;
+  const bool bad = (st.status & SEQ_BADROW) != 0;
+  const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
+  const float* qrow = resid ? p.q + ((size_t)b * G + n) * V : nullptr;
+  const float Mc = st.M * p.c;
+  const float inv_s = (float)(1.0 / st.s);
+  const bool vec_ok = (V % VW) == 0;
+  double* cm = p.chunk_mass + (size_t)b * NT;
+
+  // ---- masses of this chunk's NS sub-ranges
+  const int c0 = c * p.CL;
+  float part[kMaxNS];
+#pragma unroll
+  for (int j = 0; j < kMaxNS; ++j) {
+    part[j] = 0.f;
+    if (j < NS && !bad) {
+      const int e0 = c0 + (j * kThreads + tid) * VW;
+      part[j] = slot_mass<T>(row, qrow, e0, min(max(V - e0, 0), VW), p.c, Mc, inv_s, vec_ok);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxNS; ++j) {
+    if (j < NS) {
+      const F2 tot = block_sum_f2(F2{part[j], 0.f}, sm.f2red);
+      if (tid == 0) cm[c * NS + j] = (double)tot.hi + (double)tot.lo;
+    }
+  }
+  if (!arrive_last(p.seq_ticket2 + b, p.C, &sm.flag)) return;
+
+  // ---- last CTA of sequence b: locate the inverse-CDF step
+  int status = st.status;
+  if (tid == 0) {
+    double R = 0.0;
+    for (int k2 = 0; k2 < NT; ++k2) R += __ldcg(cm + k2);
+    sm.use_p = (resid && !bad && !(R > 0.0)) ? 1 : 0;
+  }
+  __syncthreads();
+  const float* qsel = qrow;
+  if (sm.use_p) {
+    // zero residual mass (only through rounding): draw from p_n instead
+    status |= SEQ_RESID0;
+    qsel = nullptr;
+    for (int k2 = 0; k2 < NT; ++k2) {
+      const int e0 = (k2 / NS) * p.CL + ((k2 % NS) * kThreads + tid) * VW;
+      const float m2 = slot_mass<T>(row, nullptr, e0, min(max(V - e0, 0), VW), p.c, Mc, inv_s, vec_ok);
+      const F2 tot = block_sum_f2(F2{m2, 0.f}, sm.f2red);
+      if (tid == 0) cm[k2] = (double)tot.hi + (double)tot.lo;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    double R = 0.0;
+    for (int k2 = 0; k2 < NT; ++k2) R += __ldcg(cm + k2);
+    const double t = (double)p.uniforms[b * G1 + G] * R;
+    int sub = -1, lastsub = -1;
+    double pref = 0.0, lastbase = 0.0;
+    for (int k2 = 0; k2 < NT; ++k2) {
+      const double m2 = __ldcg(cm + k2);
+      if (m2 > 0.0) { lastsub = k2; lastbase = pref; }
+      if (pref + m2 > t) { sub = k2; break; }
+      pref += m2;
+    }
+    double base = pref;
+    if (sub < 0) { sub = lastsub; base = lastbase; }
+    sm.sub = (bad || !(R > 0.0)) ? -1 : sub;
+    sm.base = base;
+    sm.target = t;
+    sm.token = -1;
+  }
+  __syncthreads();
+  int token = 0;
+  if (sm.sub >= 0) {
+    const int e0 = (sm.sub / NS) * p.CL + ((sm.sub % NS) * kThreads + tid) * VW;
+    const int nv = min(max(V - e0, 0), VW);
+    const float m2 = slot_mass<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok);
+    F2 total;
+    const F2 ex = block_exclusive_f2(F2{m2, 0.f}, sm.f2red, &total);
+    const double tbase = sm.base + (double)ex.hi + (double)ex.lo;
+    const double target = sm.target;
+    int lastp = -1;
+    if (m2 > 0.f && tbase <= target && tbase + (double)m2 > target) {
+      const int found = slot_walk<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok, tbase, target, &lastp);
+      if (found >= 0) sm.token = found;
+    }
+    __syncthreads();
+    if (sm.token < 0) {
+      // rounding left no step above the target: take the last positive weight
+      int lp = -1;
+      slot_walk<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok, 0.0, 1e300, &lp);
+      int m = lp;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if ((tid & 31) == 0) sm.ired[tid >> 5] = m;
+      __syncthreads();
+      if (tid == 0) {
+        int mm = -1;
+        for (int w = 0; w < kWarps; ++w) mm = max(mm, sm.ired[w]);
+        sm.token = mm;
+      }
+      __syncthreads();
+    }
+    token = sm.token < 0 ? 0 : sm.token;
+  }
+  for (int k2 = tid; k2 < NT; k2 += kThreads) cm[k2] = 0.0;
+  if (tid == 0) {
+    p.out_tokens[b * G1 + n] = token;
+    if (p.out_status) p.out_status[b] = status;
+    SeqState z;
+    z.n = 0; z.status = 0; z.M = 0.f; z.pad = 0; z.s = 0.0;
+    p.seq[b] = z;
+  }
+}
+
+}  // namespace sv

@@ -1,0 +1,127 @@
+"""The C ABI library builds, loads and exports every declared symbol; host-side
+argument validation returns the documented status codes.  No kernel is
+launched here (these run without a GPU): every call below fails validation
+before any CUDA call, or is the empty B = 0 call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sv():
+    from speculative_decoding_verification_46_gb300 import build
+
+    build.build_library()
+    import speculative_decoding_verification_46_gb300 as pkg
+
+    pkg.load_library()
+    return pkg
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "specverify.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(sv):
+    lib = ctypes.CDLL(sv.load_library()._name)
+    names = _declared_functions()
+    assert set(names) == {"sv_workspace_bytes", "sv_verify_sample", "sv_verify_greedy", "sv_status_string",
+                          "sv_set_timing_events"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(sv):
+    for code in range(6):
+        assert sv.sv_status_string(code).startswith("SV_")
+    assert "unknown" in sv.sv_status_string(99)
+
+
+def test_workspace_bytes(sv):
+    a = sv.sv_workspace_bytes(64, 4, 128256, 0)
+    b = sv.sv_workspace_bytes(128, 4, 128256, 0)
+    assert 0 < a < b and a % 256 == 0
+    assert sv.sv_workspace_bytes(256, 8, 152064, 50) > sv.sv_workspace_bytes(256, 8, 152064, 0)
+    for bad in [(-1, 4, 10, 0), (4, -1, 10, 0), (4, 65, 10, 0), (4, 4, 0, 0), (4, 4, (1 << 24) + 1, 0),
+                (4, 4, 10, -1), (4, 4, 10, 1025)]:
+        assert sv.sv_workspace_bytes(*bad) == 0, bad
+
+
+# fake, never dereferenced device addresses (validation fails before any use)
+A = 1 << 20
+
+
+def _sample(sv, **kw):
+    args = dict(B=4, gamma=3, V=100, logits=A, logits_dtype=sv.SV_DTYPE_BF16, q=A + 4096, draft_tokens=A + 8192,
+                uniforms=A + 12288, temperature=1.0, top_k=0, top_p=1.0, out_tokens=A + 16384,
+                out_num_accepted=A + 20480, out_accept_prob=None, out_status=None, workspace=A + 65536,
+                workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    return sv.sv_verify_sample(*args.values())
+
+
+def _greedy(sv, **kw):
+    args = dict(B=4, gamma=3, V=100, logits=A, logits_dtype=sv.SV_DTYPE_BF16, draft_tokens=A + 8192,
+                out_tokens=A + 16384, out_num_accepted=A + 20480, out_status=None, workspace=A + 65536,
+                workspace_bytes=1 << 30, stream=None)
+    args.update(kw)
+    return sv.sv_verify_greedy(*args.values())
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(gamma=-1), dict(gamma=65), dict(V=0), dict(V=(1 << 24) + 1),
+                                dict(logits_dtype=7), dict(temperature=0.0), dict(temperature=-1.0),
+                                dict(temperature=float("inf")), dict(temperature=float("nan")), dict(top_k=-1),
+                                dict(top_k=1025), dict(top_p=0.0), dict(top_p=1.5), dict(top_p=float("nan")),
+                                dict(logits=None), dict(q=None), dict(draft_tokens=None), dict(uniforms=None),
+                                dict(out_tokens=None), dict(out_num_accepted=None), dict(logits=A + 2),
+                                dict(q=A + 4100)])
+def test_sample_rejects_invalid_arguments(sv, kw):
+    assert _sample(sv, **kw) == sv.SV_ERR_INVALID_ARG
+
+
+def test_sample_workspace_and_unsupported(sv):
+    assert _sample(sv, workspace=None) == sv.SV_ERR_WORKSPACE
+    assert _sample(sv, workspace_bytes=16) == sv.SV_ERR_WORKSPACE
+    assert _sample(sv, workspace=A + 3) == sv.SV_ERR_WORKSPACE
+    # top-p without top-k over a vocabulary larger than the largest list
+    assert _sample(sv, V=5000, top_k=0, top_p=0.9) == sv.SV_ERR_UNSUPPORTED
+    # gamma = 0 needs neither q nor drafts; B = 0 is an empty call
+    assert _sample(sv, B=0) == sv.SV_OK
+    assert _sample(sv, gamma=0, q=None, draft_tokens=None, workspace_bytes=16) == sv.SV_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(gamma=-1), dict(V=0), dict(logits_dtype=3), dict(logits=None),
+                                dict(draft_tokens=None), dict(out_tokens=None), dict(out_num_accepted=None),
+                                dict(logits=A + 8)])
+def test_greedy_rejects_invalid_arguments(sv, kw):
+    assert _greedy(sv, **kw) == sv.SV_ERR_INVALID_ARG
+
+
+def test_greedy_workspace(sv):
+    assert _greedy(sv, workspace_bytes=8) == sv.SV_ERR_WORKSPACE
+    assert _greedy(sv, B=0) == sv.SV_OK
+
+
+def test_torch_wrappers_refuse_cpu_tensors(sv):
+    import torch
+
+    L = torch.zeros(2, 3, 10, dtype=torch.bfloat16)
+    d = torch.zeros(2, 2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        sv.verify_greedy(L, d)
+    with pytest.raises(ValueError):
+        sv.verify_sample(L, torch.zeros(2, 2, 10), d, torch.zeros(2, 3), 1.0)
+
+
+def test_timing_hook_validation(sv):
+    lib = sv.load_library()
+    assert lib.sv_set_timing_events(None, 0) == sv.SV_OK
+    assert lib.sv_set_timing_events(None, 3) == sv.SV_ERR_INVALID_ARG
+    assert lib.sv_set_timing_events(None, 2) == sv.SV_ERR_INVALID_ARG

@@ -1,0 +1,84 @@
+"""Host logic of bench.py: the max-over-ranks timing reduction across two
+gloo processes (the N > 1 replicas path, on CPU) and the algorithmic-byte
+accounting the roofline uses."""
+
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        q.put((rank, bench.max_over_ranks(1.5 + rank, ws)))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: 2.5, 1: 2.5}
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_algorithmic_bytes():
+    w = workloads.WORKLOADS["sample_b64_g4_v128256_bf16_s0.7"]
+    n = np.array([4] * 10 + [1] * 54)
+    ab = bench.algorithmic_bytes(w, n)
+    assert ab["stream"] == 64 * 5 * 128256 * 2 + 64 * 4 * 6
+    assert ab["final"] == 54 * 128256 * 6 + 10 * 128256 * 2
+    g = workloads.WORKLOADS["greedy_b512_g4_v128256_bf16"]
+    assert bench.algorithmic_bytes(g, np.zeros(512, int)) == {"stream": 512 * 5 * 128256 * 2, "final": 0}
+    t = workloads.WORKLOADS["topk50_topp0.9_b256_g8_v152064_bf16"]
+    assert bench.algorithmic_bytes(t, np.zeros(256, int))["final"] == 0
+
+
+@pytest.mark.parametrize("name", sorted(workloads.WORKLOADS))
+def test_reference_arm_fields(name):
+    """The reference arm's JSON line (oracle on host cores) for a tiny run."""
+    import json
+    import subprocess
+
+    if workloads.WORKLOADS[name].B * workloads.WORKLOADS[name].V > 10 ** 6:
+        pytest.skip("large workload: input generation is slow on CPU")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", name,
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == name
