@@ -146,6 +146,34 @@ sv_status sv_verify_greedy(int B, int gamma, int V,
                            void* workspace, size_t workspace_bytes,
                            sv_stream_t stream);
 
+/*
+ * Greedy verify for callers that cannot allocate device memory - for example
+ * a plugin whose host framework owns every device allocation and passes none
+ * down, a runtime that fixes its memory budget before serving, or a loop that
+ * must not call cudaMalloc because it can synchronise the device.  (The pages
+ * have no counterpart: this is a deployment convenience, not part of the
+ * method.)  Same arguments, results and status bits as sv_verify_greedy,
+ * without the workspace.
+ *
+ * Scratch: the library holds one array of SV_NOALLOC_SCRATCH_BYTES (8 MiB)
+ * in device memory on every GPU that loads it, until the process exits.  A
+ * problem whose sv_workspace_bytes(B, gamma, V, 0) exceeds that size returns
+ * SV_ERR_WORKSPACE and launches nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call clears the part
+ * of the array it uses (cudaMemsetAsync on `stream`) and then runs the greedy
+ * kernel on it.  All calls on a device share the one array: calls that can
+ * overlap on the GPU (different streams, several host threads) race and must
+ * be serialised by the caller.  Allocates nothing: no cudaMalloc / cudaFree.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+sv_status sv_verify_greedy_noalloc(int B, int gamma, int V,
+                                   const void* logits, sv_dtype logits_dtype,
+                                   const int32_t* draft_tokens,
+                                   int32_t* out_tokens, int32_t* out_num_accepted,
+                                   int32_t* out_status,
+                                   sv_stream_t stream);
+
 /* Static description of a status code. */
 const char* sv_status_string(sv_status s);
 

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     sv_set_timing_events,
     sv_status_string,
     sv_verify_greedy,
+    sv_verify_greedy_noalloc,
     sv_verify_sample,
     sv_workspace_bytes,
     verify_greedy,

@@ -66,6 +66,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sv_verify_greedy.restype = _c_int
     lib.sv_status_string.argtypes = [_c_int]
     lib.sv_status_string.restype = ctypes.c_char_p
+    lib.sv_verify_greedy_noalloc.argtypes = [_c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_ptr,
+                                             _c_ptr, _c_ptr]
+    lib.sv_verify_greedy_noalloc.restype = _c_int
     lib.sv_set_timing_events.argtypes = [ctypes.POINTER(_c_ptr), _c_int]
     lib.sv_set_timing_events.restype = _c_int
     _lib = lib
@@ -95,6 +98,14 @@ def sv_verify_greedy(B, gamma, V, logits, logits_dtype, draft_tokens, out_tokens
                      workspace, workspace_bytes, stream) -> int:
     return int(load_library().sv_verify_greedy(B, gamma, V, logits, logits_dtype, draft_tokens, out_tokens,
                                                out_num_accepted, out_status, workspace, workspace_bytes, stream))
+
+
+def sv_verify_greedy_noalloc(B, gamma, V, logits, logits_dtype, draft_tokens, out_tokens, out_num_accepted,
+                             out_status, stream) -> int:
+    """Greedy verify on the library's own scratch (no workspace argument), for
+    callers that cannot allocate device memory; see include/specverify.h."""
+    return int(load_library().sv_verify_greedy_noalloc(B, gamma, V, logits, logits_dtype, draft_tokens, out_tokens,
+                                                       out_num_accepted, out_status, stream))
 
 
 def sv_set_timing_events(events) -> int:

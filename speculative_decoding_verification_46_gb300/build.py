@@ -20,7 +20,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIBNAME = "libspecverify.so"
 LIB_PATH = os.path.join(LIBDIR, LIBNAME)
 
-SOURCES = ["sv_api.cu"]
+SOURCES = ["sv_api.cu", "sv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

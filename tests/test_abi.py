@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(sv):
     lib = ctypes.CDLL(sv.load_library()._name)
     names = _declared_functions()
     assert set(names) == {"sv_workspace_bytes", "sv_verify_sample", "sv_verify_greedy", "sv_status_string",
-                          "sv_set_timing_events"}
+                          "sv_set_timing_events", "sv_verify_greedy_noalloc"}
     for n in names:
         assert hasattr(lib, n), n
 
