@@ -53,6 +53,8 @@ def _args():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size B (smaller cases for ncu captures)")
     return ap.parse_args()
 
 
@@ -219,6 +221,8 @@ def run_gb300(args, rank, ws_n, local):
     dev = torch.device("cuda", local)
     sv.load_library()
     w = workloads.WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = w.with_(B=args.batch, name=f"{w.name}@B={args.batch}")
     B, G, V = w.B, w.gamma, w.V
     positions = B * (G + 1)
 
@@ -282,17 +286,24 @@ def run_gb300(args, rank, ws_n, local):
     ms_max = max_over_ranks(ms, ws_n, dev)
     value = positions * ws_n / (ms_max / 1e3)
 
-    # per-kernel durations (events recorded between the kernels of each call)
-    n_roof = min(max(50, steps // 20), 2000)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_roof)]
+    # per-kernel durations: events recorded before, between and after the
+    # kernels of each call.  A fixed-length sleep kernel first keeps the GPU
+    # busy while the host queues a batch of calls, so that the gaps between
+    # events are device time, not host submission time.
+    n_batch, batch = 4, 100
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_batch * batch)]
     with torch.cuda.stream(stream):
         for trio in evs:
             for e in trio:
                 e.record(stream)          # torch creates the CUDA event on first record
-        for j in range(n_roof):
-            if sv.sv_set_timing_events(evs[j]) != sv.SV_OK:
-                raise RuntimeError("sv_set_timing_events failed")
-            _call(sv, w, sets[j % n_sets], outs[j % n_sets], wsp, stream)
+        j = 0
+        for _ in range(n_batch):
+            torch.cuda._sleep(40_000_000)  # ~20 ms at 2 GHz
+            for _ in range(batch):
+                if sv.sv_set_timing_events(evs[j]) != sv.SV_OK:
+                    raise RuntimeError("sv_set_timing_events failed")
+                _call(sv, w, sets[j % n_sets], outs[j % n_sets], wsp, stream)
+                j += 1
         sv.sv_set_timing_events(None)
     torch.cuda.synchronize()
     t_stream = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) * 1e-3

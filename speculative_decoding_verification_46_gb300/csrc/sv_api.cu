@@ -2,12 +2,18 @@
 // dispatch for the C ABI declared in include/specverify.h.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "specverify.h"
+#include "sv_cluster.cuh"
 #include "sv_device.cuh"
+#include "sv_topk.cuh"
 
 namespace {
 
@@ -151,11 +157,123 @@ sv_status launch_residual(const sv::Params& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- cluster path
+// Small problems run as one kernel with one thread-block cluster per sequence
+// (sv_cluster.cuh).  SPECVERIFY_PATH=grid / =cluster overrides the choice
+// (tests use it to cover both paths).
+constexpr size_t kClusterMaxBytes = 8u << 20;      // logits of the whole batch
+constexpr size_t kClusterBytesPerCta = 16u << 10;  // slice bytes a CTA aims for
+constexpr size_t kClusterMaxSmem = 200u << 10;
+
+int path_override() {
+  const char* e = std::getenv("SPECVERIFY_PATH");
+  if (!e) return 0;
+  if (!std::strcmp(e, "grid")) return 1;
+  if (!std::strcmp(e, "cluster")) return 2;
+  if (!std::strcmp(e, "slices")) return 3;   // top-k: the per-slice kernel instead of the per-row one
+  return 0;
+}
+
+bool plan_cluster(const sv::Params& p, sv_dtype dt, int mode, sv::ClusterParams* cp, size_t* smem) {
+  if (mode == sv::MODE_TOPK) return false;
+  const int ov = path_override();
+  if (ov == 1) return false;
+  const int VW = vec_width(dt);
+  const size_t sl = dt == SV_DTYPE_F32 ? 4 : 2;
+  if (p.V % VW != 0) return false;
+  const size_t G1 = (size_t)p.gamma + 1;
+  const size_t per_seq = G1 * p.V * sl + (mode == sv::MODE_SOFTMAX ? (size_t)p.gamma * p.V * 4 : 0);
+  if (ov != 2 && (size_t)p.B * G1 * p.V * sl > kClusterMaxBytes) return false;
+  int CN = (int)std::min<size_t>(sv::kClusterMax, std::max<size_t>(1, (per_seq + kClusterBytesPerCta - 1) / kClusterBytesPerCta));
+  int W = (int)ceil_div(p.V, CN);
+  W = (W + 7) / 8 * 8;
+  CN = (int)ceil_div(p.V, W);
+  const int NS = (int)ceil_div(W / VW, sv::kThreads);
+  if (NS > sv::kClusterMaxNS) return false;
+  const size_t sm = ((sizeof(sv::ClusterSmem) + 15) & ~size_t(15)) + G1 * W * sl +
+                    (mode == sv::MODE_SOFTMAX ? (size_t)p.gamma * W * 4 : 0);
+  if (sm > kClusterMaxSmem) return false;
+  cp->p = p;
+  cp->CN = CN;
+  cp->W = W;
+  cp->NS = NS;
+  *smem = sm;
+  return true;
+}
+
+template <typename T, int MODE>
+sv_status launch_cluster(const sv::ClusterParams& cp, size_t smem, cudaStream_t stream, bool* launched) {
+  auto kern = sv::cluster_kernel<T, MODE>;
+  *launched = false;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      (cp.CN > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+    cudaGetLastError();
+    return SV_OK;   // not available: the caller takes the grid path
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(cp.p.B * cp.CN));
+  cfg.blockDim = dim3(sv::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cp.CN;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters < 1) {
+    cudaGetLastError();
+    return SV_OK;
+  }
+  if (cudaLaunchKernelEx(&cfg, kern, cp) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  *launched = true;
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Top-k / top-p with V a multiple of the vector width: the persistent
+// two-pass kernel (sv_topk.cuh), about two CTAs per SM, rows dealt out evenly.
 template <typename T>
-sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream) {
+sv_status launch_topk_rows(const sv::Params& p, cudaStream_t stream) {
+  auto kern = sv::topk_rows_kernel<T>;
+  const size_t smem = sizeof(sv::TopkSmem);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  const long long R = (long long)p.B * (p.gamma + 1);
+  const long long slots = 2ll * sm_count();
+  const long long per = ceil_div(R, std::min(R, slots));
+  const long long grid = ceil_div(R, per);
+  kern<<<(unsigned)grid, sv::kTkThreads, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+template <typename T>
+sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
+  sv::ClusterParams cp;
+  size_t smem = 0;
+  if (plan_cluster(p, dt, mode, &cp, &smem)) {
+    bool launched = false;
+    timing_record(0, stream);
+    const sv_status st = mode == sv::MODE_GREEDY ? launch_cluster<T, sv::MODE_GREEDY>(cp, smem, stream, &launched)
+                                                 : launch_cluster<T, sv::MODE_SOFTMAX>(cp, smem, stream, &launched);
+    if (st != SV_OK) return st;
+    if (launched) {
+      timing_record(1, stream);
+      timing_record(2, stream);
+      return SV_OK;
+    }
+  }
   timing_record(0, stream);
   sv_status st = SV_OK;
   if (mode == sv::MODE_GREEDY) st = launch_rows<T, sv::MODE_GREEDY>(p, stream);
+  else if (mode == sv::MODE_TOPK && p.V % vec_width(dt) == 0 && path_override() != 3)
+    st = launch_topk_rows<T>(p, stream);
   else if (mode == sv::MODE_TOPK) st = launch_rows<T, sv::MODE_TOPK>(p, stream);
   else st = launch_rows<T, sv::MODE_SOFTMAX>(p, stream);
   if (st != SV_OK) return st;
@@ -173,9 +291,9 @@ sv_status run(sv::Params& p, sv_dtype dt, int mode, void* workspace, size_t work
   choose_slices(p, dt, mode == sv::MODE_TOPK);
   if (mode == sv::MODE_SOFTMAX) choose_chunks(p);
   switch (dt) {
-    case SV_DTYPE_F32: return dispatch<float>(p, mode, stream);
-    case SV_DTYPE_BF16: return dispatch<__nv_bfloat16>(p, mode, stream);
-    case SV_DTYPE_F16: return dispatch<__half>(p, mode, stream);
+    case SV_DTYPE_F32: return dispatch<float>(p, mode, stream, dt);
+    case SV_DTYPE_BF16: return dispatch<__nv_bfloat16>(p, mode, stream, dt);
+    case SV_DTYPE_F16: return dispatch<__half>(p, mode, stream, dt);
   }
   return SV_ERR_INVALID_ARG;
 }

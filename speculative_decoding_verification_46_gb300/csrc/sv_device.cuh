@@ -322,6 +322,78 @@ __device__ __forceinline__ int block_sum_int(int v, int* sm) {
   return t;
 }
 
+__device__ __forceinline__ double warp_incl_scan_d(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, v, m);
+    if (lane >= m) v += o;
+  }
+  return v;
+}
+
+struct LocateSmem {
+  double wsum[kWarps];
+  double carry;
+  double base;
+  int found;
+  int last;
+  double lastbase;
+};
+
+// Block-wide inverse-CDF search over NT masses in index order (global or
+// shared memory): total R, then the first k whose running interval
+// [prefix_k, prefix_k + m_k) holds t = u * R.  Both passes sum in the same
+// order, so t < R always lands inside unless rounding pushes it to the end, in
+// which case the last positive mass is taken.  Returns k (or -1 if R <= 0)
+// and its exclusive prefix in *base; every thread gets the result.
+__device__ int block_locate(const double* masses, int NT, double u, double* R_out, double* base_out,
+                            LocateSmem& ls, bool from_global) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  double R = 0.0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const double t = u * R;
+    __syncthreads();   // every thread has read ls (the previous pass's total) before it is reset
+    if (tid == 0) { ls.carry = 0.0; ls.found = 0x7fffffff; ls.last = -1; ls.lastbase = 0.0; }
+    __syncthreads();
+    for (int c0 = 0; c0 < NT; c0 += kThreads) {
+      const int k = c0 + tid;
+      const double m = k < NT ? (from_global ? __ldcg(masses + k) : masses[k]) : 0.0;
+      const double inc = warp_incl_scan_d(m);
+      if (lane == 31) ls.wsum[warp] = inc;
+      __syncthreads();
+      double off = ls.carry;
+      double tot = ls.carry;
+      for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) off += ls.wsum[w];
+        tot += ls.wsum[w];
+      }
+      double below = __shfl_up_sync(0xffffffffu, inc, 1);
+      if (lane == 0) below = 0.0;
+      const double excl = off + below;
+      if (pass == 1 && k < NT && m > 0.0) {
+        if (excl <= t && excl + m > t) atomicMin(&ls.found, k);   // at most one k qualifies
+        atomicMax(&ls.last, k);
+      }
+      __syncthreads();
+      if (pass == 1) {
+        if (ls.found == k && k < NT) ls.base = excl;
+        if (ls.last == k && k < NT) ls.lastbase = excl;
+      }
+      if (tid == 0) ls.carry = tot;
+      __syncthreads();
+      if (pass == 1 && ls.found != 0x7fffffff) break;
+    }
+    if (pass == 0) R = ls.carry;
+  }
+  __syncthreads();
+  *R_out = R;
+  if (!(R > 0.0)) return -1;
+  if (ls.found != 0x7fffffff) { *base_out = ls.base; return ls.found; }
+  *base_out = ls.lastbase;
+  return ls.last;
+}
+
 // "Does (va, ia) beat (vb, ib)?" for the greedy argmax: a larger value wins,
 // equal values (-0.0 == +0.0) go to the lower index; NaN wins (it is flagged).
 __device__ __forceinline__ bool argmax_better(float va, int ia, float vb, int ib) {
@@ -335,10 +407,13 @@ __device__ __forceinline__ bool argmax_better(float va, int ia, float vb, int ib
 // Last-arriving-CTA hand-off.  Every thread publishes its writes, one thread
 // takes a ticket; the CTA that takes ticket count-1 resets the counter and
 // returns true (its later reads of other CTAs' data use ld.global.cg).
-__device__ __forceinline__ bool arrive_last(int* ticket, int count, int* s_flag) {
-  __threadfence();
+// With single_writer, only thread 0 wrote what the other CTAs will read, so
+// only thread 0 fences.
+__device__ __forceinline__ bool arrive_last(int* ticket, int count, int* s_flag, bool single_writer = false) {
+  if (!single_writer) __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    if (single_writer) __threadfence();
     const int prev = atomicAdd(ticket, 1);
     const int last = (prev == count - 1);
     if (last) *ticket = 0;
@@ -365,97 +440,118 @@ struct RowsSmem {
   int token;
   float M[kMaxG1];
   double s[kMaxG1];
-  double a[kMaxG1];
+  float a[kMaxG1];
   int g[kMaxG1];
   int bad[kMaxG1];
   int status;
   double dred[kWarps];
+  int dr[kMaxG1];          // this sequence's drafts, loaded at kernel start
+  float ur[kMaxG1];        // and its uniforms
   unsigned long long cand[kCandCap];   // top-k candidates; reused by the row merge
   unsigned long long mout[kMaxK];
   double w[kMaxK];
   int widx[kMaxK];
 };
 
-// Greedy / softmax sequence finisher: merge the S partials of each of the
-// gamma+1 rows, then the acceptance scan.
+// Greedy / softmax sequence finisher: one warp per row merges that row's S
+// slice partials (lanes load them in parallel), then the acceptance scan.
 template <typename T, int MODE>
 __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
-  const int tid = threadIdx.x;
-  const int G = p.gamma, G1 = G + 1, V = p.V;
-  if (tid < G1) {
-    const int rr = b * G1 + tid;
-    const float4* pp = p.part + (size_t)rr * p.S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.gamma, G1 = G + 1, V = p.V, S = p.S;
+  for (int i = warp; i < G1; i += kWarps) {
+    const int rr = b * G1 + i;
+    const float4* pp = p.part + (size_t)rr * S;
     if (MODE == MODE_GREEDY) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
-      for (int s2 = 0; s2 < p.S; ++s2) {
+#pragma unroll 4
+      for (int s2 = lane; s2 < S; s2 += 32) {
         const float4 v = __ldcg(pp + s2);
         const int vi = __float_as_int(v.y);
         if (argmax_better(v.x, vi, bv, bi)) { bv = v.x; bi = vi; }
       }
-      const bool nan = bv != bv;
-      sm.g[tid] = (nan || bi == 0x7fffffff) ? 0 : bi;
-      sm.bad[tid] = nan ? 1 : 0;
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, m);
+        if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) {
+        const bool nan = bv != bv;
+        sm.g[i] = (nan || bi == 0x7fffffff) ? 0 : bi;
+        sm.bad[i] = nan ? 1 : 0;
+      }
     } else {
       float M = -INFINITY;
-      for (int s2 = 0; s2 < p.S; ++s2) M = fmaxf(M, __ldcg(pp + s2).x);
-      double s = 0.0;
+#pragma unroll 4
+      for (int s2 = lane; s2 < S; s2 += 32) M = fmaxf(M, __ldcg(pp + s2).x);
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+      F2 acc{0.f, 0.f};
       if (M > -INFINITY && M < INFINITY) {
-        for (int s2 = 0; s2 < p.S; ++s2) {
+#pragma unroll 4
+        for (int s2 = lane; s2 < S; s2 += 32) {
           const float4 v = __ldcg(pp + s2);
-          if (v.x > -INFINITY) s += ((double)v.y + (double)v.z) * (double)exp2f((v.x - M) * p.c);
-        }
-      }
-      const bool bad = !(M > -INFINITY && M < INFINITY) || !(s > 0.0 && s < 1e300);
-      sm.M[tid] = M;
-      sm.s[tid] = s;
-      sm.bad[tid] = bad ? 1 : 0;
-      if (tid < G) {
-        const int d = p.draft[b * G + tid];
-        double a = 0.0;
-        int st = 0;
-        if (d < 0 || d >= V) {
-          st |= SEQ_OOB;
-        } else {
-          const T* row = static_cast<const T*>(p.logits) + (size_t)rr * V;
-          const float l = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
-          const float qd = __ldg(p.q + ((size_t)b * G + tid) * V + d);
-          const double pd = bad ? 0.0 : exp2(((double)l - (double)M) * (double)p.c) / s;
-          if (qd > 0.0f) {
-            a = fmin(1.0, pd / (double)qd);
-          } else {
-            a = pd > 0.0 ? 1.0 : 0.0;
-            st |= SEQ_QBAD;
+          if (v.x > -INFINITY) {
+            const float sc = exp2f((v.x - M) * p.c);
+            acc = f2_add(acc, f2_add(F2{v.y * sc, 0.f}, F2{v.z * sc, 0.f}));
           }
         }
-        sm.a[tid] = a;
-        sm.g[tid] = st;
-        if (p.out_a) p.out_a[b * G + tid] = (float)a;
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) acc = f2_add(acc, f2_shfl_xor(acc, m));
+      if (lane == 0) {
+        const double s = (double)acc.hi + (double)acc.lo;
+        const bool bad = !(M > -INFINITY && M < INFINITY) || !(s > 0.0 && s < 1e300);
+        sm.M[i] = M;
+        sm.s[i] = s;
+        sm.bad[i] = bad ? 1 : 0;
+        if (i < G) {
+          const int d = sm.dr[i];
+          float a = 0.f;
+          int st = 0;
+          if (d < 0 || d >= V) {
+            st |= SEQ_OOB;
+          } else {
+            const T* row = static_cast<const T*>(p.logits) + (size_t)rr * V;
+            const float l = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
+            const float qd = __ldg(p.q + ((size_t)b * G + i) * V + d);
+            const float pd = bad ? 0.f : exp2f((l - M) * p.c) / (float)s;
+            if (qd > 0.0f) {
+              a = fminf(1.f, pd / qd);
+            } else {
+              a = pd > 0.f ? 1.f : 0.f;
+              st |= SEQ_QBAD;
+            }
+          }
+          sm.a[i] = a;
+          sm.g[i] = st;
+          if (p.out_a) p.out_a[b * G + i] = a;
+        }
       }
     }
   }
   __syncthreads();
   // every partial of this sequence has been read: leave the workspace zeroed
-  for (int e = tid; e < G1 * p.S; e += kThreads)
-    p.part[(size_t)b * G1 * p.S + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int e = tid; e < G1 * S; e += kThreads)
+    p.part[(size_t)b * G1 * S + e] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid == 0) {
     int status = 0, n = G;
     for (int i = 0; i < G1; ++i)
       if (sm.bad[i]) status |= SEQ_BADROW;
     if (MODE == MODE_GREEDY) {
       for (int i = 0; i < G; ++i) {
-        const int d = p.draft[b * G + i];
+        const int d = sm.dr[i];
         if (d < 0 || d >= V) status |= SEQ_OOB;
       }
       for (int i = 0; i < G; ++i)
-        if (p.draft[b * G + i] != sm.g[i]) { n = i; break; }
+        if (sm.dr[i] != sm.g[i]) { n = i; break; }
       sm.token = sm.g[n];
     } else {
       for (int i = 0; i < G; ++i) status |= sm.g[i];
-      for (int i = 0; i < G; ++i) {
-        const double u = (double)p.uniforms[b * G1 + i];
-        if (!(u < sm.a[i])) { n = i; break; }
-      }
+      for (int i = 0; i < G; ++i)
+        if (!(sm.ur[i] < (float)sm.a[i])) { n = i; break; }
       SeqState st;
       st.n = n;
       st.status = status;
@@ -472,7 +568,7 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
   __syncthreads();
   const int n = sm.n;
   for (int j = tid; j < G1; j += kThreads) {
-    if (j < n) p.out_tokens[b * G1 + j] = p.draft[b * G + j];
+    if (j < n) p.out_tokens[b * G1 + j] = sm.dr[j];
     else if (j > n) p.out_tokens[b * G1 + j] = -1;
     else if (MODE == MODE_GREEDY) p.out_tokens[b * G1 + j] = sm.token;
   }
@@ -694,6 +790,11 @@ rows_kernel(const Params p) {
   const int i = r - b * G1;
 
   pdl_launch_dependents();
+  if (MODE != MODE_TOPK) {
+    // the sequence finisher needs the drafts and uniforms; fetch them with the data
+    if (tid < p.gamma) sm.dr[tid] = p.draft[b * p.gamma + tid];
+    if (MODE == MODE_SOFTMAX && tid < G1) sm.ur[tid] = p.uniforms[b * G1 + tid];
+  }
 
   const T* row = static_cast<const T*>(p.logits) + (size_t)r * p.V;
   const int s0 = s * p.SL;
@@ -758,7 +859,7 @@ rows_kernel(const Params p) {
       }
       p.part[(size_t)r * p.S + s] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
     }
-    if (arrive_last(p.seq_ticket + b, p.S * G1, &sm.flag)) finish_sequence_dense<T, MODE>(p, b, sm);
+    if (arrive_last(p.seq_ticket + b, p.S * G1, &sm.flag, true)) finish_sequence_dense<T, MODE>(p, b, sm);
     return;
   }
 
@@ -785,7 +886,7 @@ rows_kernel(const Params p) {
     }
     F2 tot = block_sum_f2(F2{a0 + a1, 0.f}, sm.f2red);
     if (tid == 0) p.part[(size_t)r * p.S + s] = make_float4(M, tot.hi, tot.lo, 0.f);
-    if (arrive_last(p.seq_ticket + b, p.S * G1, &sm.flag)) finish_sequence_dense<T, MODE>(p, b, sm);
+    if (arrive_last(p.seq_ticket + b, p.S * G1, &sm.flag, true)) finish_sequence_dense<T, MODE>(p, b, sm);
     return;
   }
 
@@ -981,9 +1082,9 @@ struct ResSmem {
   int flag;
   int sub;        // selected sub-range (chunk * NS + slot), -1 if none
   int token;
-  int use_p;
   double target;
   double base;
+  LocateSmem loc;
 };
 
 template <typename T>
@@ -1011,7 +1112,7 @@ residual_kernel(const Params p) {
   const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
   const float* qrow = resid ? p.q + ((size_t)b * G + n) * V : nullptr;
   const float Mc = st.M * p.c;
-  const float inv_s = (float)(1.0 / st.s);
+  const float inv_s = 1.0f / (float)st.s;
   const bool vec_ok = (V % VW) == 0;
   double* cm = p.chunk_mass + (size_t)b * NT;
 
@@ -1033,18 +1134,15 @@ residual_kernel(const Params p) {
       if (tid == 0) cm[c * NS + j] = (double)tot.hi + (double)tot.lo;
     }
   }
-  if (!arrive_last(p.seq_ticket2 + b, p.C, &sm.flag)) return;
+  if (!arrive_last(p.seq_ticket2 + b, p.C, &sm.flag, true)) return;
 
   // ---- last CTA of sequence b: locate the inverse-CDF step
   int status = st.status;
-  if (tid == 0) {
-    double R = 0.0;
-    for (int k2 = 0; k2 < NT; ++k2) R += __ldcg(cm + k2);
-    sm.use_p = (resid && !bad && !(R > 0.0)) ? 1 : 0;
-  }
-  __syncthreads();
+  const double u = (double)__ldg(p.uniforms + b * G1 + G);
+  double R = 0.0, base = 0.0;
+  int sub = block_locate(cm, NT, u, &R, &base, sm.loc, true);
   const float* qsel = qrow;
-  if (sm.use_p) {
+  if (resid && !bad && !(R > 0.0)) {
     // zero residual mass (only through rounding): draw from p_n instead
     status |= SEQ_RESID0;
     qsel = nullptr;
@@ -1055,24 +1153,12 @@ residual_kernel(const Params p) {
       if (tid == 0) cm[k2] = (double)tot.hi + (double)tot.lo;
     }
     __syncthreads();
+    sub = block_locate(cm, NT, u, &R, &base, sm.loc, true);
   }
   if (tid == 0) {
-    double R = 0.0;
-    for (int k2 = 0; k2 < NT; ++k2) R += __ldcg(cm + k2);
-    const double t = (double)p.uniforms[b * G1 + G] * R;
-    int sub = -1, lastsub = -1;
-    double pref = 0.0, lastbase = 0.0;
-    for (int k2 = 0; k2 < NT; ++k2) {
-      const double m2 = __ldcg(cm + k2);
-      if (m2 > 0.0) { lastsub = k2; lastbase = pref; }
-      if (pref + m2 > t) { sub = k2; break; }
-      pref += m2;
-    }
-    double base = pref;
-    if (sub < 0) { sub = lastsub; base = lastbase; }
     sm.sub = (bad || !(R > 0.0)) ? -1 : sub;
     sm.base = base;
-    sm.target = t;
+    sm.target = u * R;
     sm.token = -1;
   }
   __syncthreads();

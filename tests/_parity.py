@@ -69,7 +69,13 @@ def compare_sample(gpu, ref, V, rows=None):
     stats["draws"] = int((np.minimum(ref["n_accepted"] + 1, G) + 1)[good].sum())
     keep = ~np.int64(svref.SEQ_RESIDUAL_ZERO)
     assert np.array_equal((st[good] & keep), (ref["status"][good] & keep)), "status bits differ"
-    assert stats["hard"] == 0, f"{stats['hard']} non-boundary mismatches: rows {np.nonzero(hard)[0][:10]}"
+    if stats["hard"]:
+        lines = []
+        for bidx in np.nonzero(hard)[0][:5]:
+            lines.append(f"seq {bidx}: gpu n={n[bidx]} tok={tok[bidx].tolist()} | ref n={ref['n_accepted'][bidx]} "
+                         f"tok={ref['out_tokens'][bidx].tolist()} a_ref={np.round(ref['accept_prob'][bidx], 7).tolist()}"
+                         + (f" a_gpu={np.round(a[bidx], 7).tolist()}" if a is not None and G > 0 else ""))
+        raise AssertionError(f"{stats['hard']} non-boundary mismatches:\n" + "\n".join(lines))
     assert stats["boundary_mismatch"] <= BOUNDARY_FRACTION * max(stats["draws"], 1), stats
     return stats
 

@@ -59,9 +59,21 @@ def _random_case(seed, B, G, V, dtype, T=1.0, ties=False, spread=2.0, top_k=0, t
 
 # ------------------------------------------------------------------ greedy
 
+@pytest.fixture(params=["auto", "grid", "cluster"])
+def path(request, monkeypatch):
+    """Which kernel path the library takes: its own choice (small problems go
+    to the one-cluster-per-sequence kernel), or forced."""
+    if request.param != "auto":
+        monkeypatch.setenv("SPECVERIFY_PATH", request.param)
+    else:
+        monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("V,G,B", [(1, 2, 5), (7, 4, 33), (1000, 1, 17), (40003, 4, 9), (128256, 4, 6)])
-def test_greedy_small(sv, dt, V, G, B):
+@pytest.mark.parametrize("V,G,B", [(1, 2, 5), (7, 4, 33), (1000, 1, 17), (40003, 4, 9), (128256, 4, 6),
+                                   (4096, 8, 3), (32000, 5, 2)])
+def test_greedy_small(sv, path, dt, V, G, B):
     inp = _random_case(10 + V + G, B, G, V, DTYPES[dt], ties=True)
     # drafts: the row argmax most of the time, so that long accepted prefixes occur
     best = inp["logits"][:, :G].float().argmax(-1).to(torch.int32)
@@ -72,7 +84,7 @@ def test_greedy_small(sv, dt, V, G, B):
     P.compare_greedy(out, P.oracle_greedy(inp), V)
 
 
-def test_greedy_degenerate_rows(sv):
+def test_greedy_degenerate_rows(sv, path):
     B, G, V = 6, 3, 300
     L = torch.randn(B, G + 1, V)
     L[0, 1, 17] = float("nan")
@@ -102,8 +114,9 @@ def test_greedy_full_size(sv):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("V,G,B,T", [(2, 4, 300, 1.0), (3, 1, 200, 0.7), (7, 8, 100, 1.3), (1024, 4, 40, 1.0),
-                                     (32000, 5, 8, 0.7), (40003, 0, 8, 1.0), (40003, 8, 6, 0.9)])
-def test_sample_small(sv, dt, V, G, B, T):
+                                     (32000, 5, 8, 0.7), (40003, 0, 8, 1.0), (40003, 8, 6, 0.9),
+                                     (4096, 0, 5, 1.0), (8192, 8, 4, 0.8), (32000, 1, 3, 1.1)])
+def test_sample_small(sv, path, dt, V, G, B, T):
     inp = _random_case(100 + V + G, B, G, V, DTYPES[dt], T=T, spread=1.5)
     g = _gpu(inp)
     out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], T)
@@ -126,7 +139,10 @@ def test_sample_config_b4_g4_v1024_f32_rounds(sv):
     assert totals["boundary_mismatch"] <= P.BOUNDARY_FRACTION * totals["draws"]
 
 
-def test_sample_config_b1_g5_v32000_bf16_rounds(sv):
+@pytest.mark.parametrize("force", [None, "grid"])
+def test_sample_config_b1_g5_v32000_bf16_rounds(sv, force, monkeypatch):
+    if force:
+        monkeypatch.setenv("SPECVERIFY_PATH", force)
     w = workloads.WORKLOADS["sample_b1_g5_v32000_bf16"]
     ws = sv.alloc_workspace(w.B, w.gamma, w.V, 0, DEV)
     acc = []
@@ -150,15 +166,39 @@ def test_sample_full_size_b64(sv, name):
 
 # ------------------------------------------------------------------ top-k / top-p
 
+@pytest.fixture(params=["auto", "slices"])
+def topk_path(request, monkeypatch):
+    """Top-k kernel: the per-row persistent one (library's choice when V is a
+    multiple of the vector width) or the per-slice one (forced)."""
+    if request.param == "slices":
+        monkeypatch.setenv("SPECVERIFY_PATH", "slices")
+    else:
+        monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("V,G,B,k,tp", [(7, 2, 50, 3, 1.0), (100, 4, 30, 1, 1.0), (5000, 4, 12, 50, 0.9),
                                         (40003, 8, 4, 50, 0.9), (40003, 3, 4, 200, 0.5), (600, 2, 20, 0, 0.8),
-                                        (33, 3, 40, 40, 0.95)])
-def test_topk_small(sv, dt, V, G, B, k, tp):
+                                        (33, 3, 40, 40, 0.95), (40000, 8, 6, 50, 0.9), (16384, 4, 8, 600, 0.7),
+                                        (1024, 2, 16, 1000, 0.99)])
+def test_topk_small(sv, topk_path, dt, V, G, B, k, tp):
     inp = _random_case(300 + V + k, B, G, V, DTYPES[dt], T=0.8, ties=True, spread=1.0, top_k=k, top_p=tp)
     g = _gpu(inp)
     out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], 0.8, k, tp)
     P.compare_sample(out, P.oracle_sample(inp, 0.8, k, tp), V)
+
+
+def test_topk_heavy_ties_take_the_exact_fallback(sv):
+    """All-equal rows: every element ties at the threshold, the candidate
+    buffers overflow and the exact (value, index) bisection must pick the
+    k lowest indices."""
+    B, G, V = 3, 2, 20000
+    inp = _random_case(5, B, G, V, torch.bfloat16, top_k=50, top_p=1.0)
+    inp["logits"][:, 1, :] = 1.0
+    g = _gpu(inp)
+    out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], 1.0, 50, 1.0)
+    P.compare_sample(out, P.oracle_sample(inp, 1.0, 50, 1.0), V)
 
 
 def test_topk_full_size_sampled(sv):
@@ -172,7 +212,7 @@ def test_topk_full_size_sampled(sv):
 
 # ------------------------------------------------------------------ degenerate data, edges, reuse
 
-def test_sample_degenerate_rows_and_flags(sv):
+def test_sample_degenerate_rows_and_flags(sv, path):
     B, G, V = 8, 3, 257
     inp = _random_case(7, B, G, V, torch.float32)
     inp["logits"][0, 2, 100] = float("nan")
