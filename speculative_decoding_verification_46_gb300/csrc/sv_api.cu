@@ -13,6 +13,7 @@
 #include "specverify.h"
 #include "sv_cluster.cuh"
 #include "sv_device.cuh"
+#include "sv_stream.cuh"
 #include "sv_topk.cuh"
 
 namespace {
@@ -97,7 +98,7 @@ void bind_workspace(sv::Params& p, const Layout& L, void* ws) {
   p.part = reinterpret_cast<float4*>(w + L.part);
   p.lists = reinterpret_cast<unsigned long long*>(w + L.lists);
   p.rowres = reinterpret_cast<int2*>(w + L.rowres);
-  p.chunk_mass = reinterpret_cast<double*>(w + L.chunk);
+  p.chunk_mass = reinterpret_cast<float2*>(w + L.chunk);
 }
 
 // Rows-kernel slicing: 8 vectors per thread unless that leaves fewer than two
@@ -235,21 +236,42 @@ sv_status launch_cluster(const sv::ClusterParams& cp, size_t smem, cudaStream_t 
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Top-k / top-p with V a multiple of the vector width: the persistent
-// two-pass kernel (sv_topk.cuh), about two CTAs per SM, rows dealt out evenly.
+// Streaming kernels (sv_stream.cuh): persistent CTAs, balanced row counts.
+template <typename K>
+long long stream_grid(K kern, size_t smem, long long R) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sv::kSt, smem) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const long long slots = (long long)per_sm * sm_count();
+  const long long per = ceil_div(R, std::min(R, slots));
+  return ceil_div(R, per);
+}
+
 template <typename T>
-sv_status launch_topk_rows(const sv::Params& p, cudaStream_t stream) {
-  auto kern = sv::topk_rows_kernel<T>;
-  const size_t smem = sizeof(sv::TopkSmem);
+sv_status launch_stream_topk(const sv::Params& p, cudaStream_t stream) {
+  auto kern = sv::stream_topk_kernel<T>;
+  const size_t smem = (size_t)sv::kStSTopk * sv::kStU * sv::kSt * sizeof(uint4) + sizeof(sv::TopkSmem);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_CUDA;
   }
-  const long long R = (long long)p.B * (p.gamma + 1);
-  const long long slots = 2ll * sm_count();
-  const long long per = ceil_div(R, std::min(R, slots));
-  const long long grid = ceil_div(R, per);
-  kern<<<(unsigned)grid, sv::kTkThreads, smem, stream>>>(p);
+  const long long grid = stream_grid(kern, smem, (long long)p.B * (p.gamma + 1));
+  kern<<<(unsigned)grid, sv::kSt, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+template <typename T, int MODE>
+sv_status launch_stream_dense(const sv::Params& p, cudaStream_t stream) {
+  auto kern = sv::stream_dense_kernel<T, MODE>;
+  const size_t smem = (size_t)sv::kStS * sv::kStU * sv::kSt * sizeof(uint4) + sizeof(sv::StreamSmem);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  const long long grid = stream_grid(kern, smem, (long long)p.B * (p.gamma + 1));
+  kern<<<(unsigned)grid, sv::kSt, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -271,11 +293,13 @@ sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype 
   }
   timing_record(0, stream);
   sv_status st = SV_OK;
-  if (mode == sv::MODE_GREEDY) st = launch_rows<T, sv::MODE_GREEDY>(p, stream);
-  else if (mode == sv::MODE_TOPK && p.V % vec_width(dt) == 0 && path_override() != 3)
-    st = launch_topk_rows<T>(p, stream);
-  else if (mode == sv::MODE_TOPK) st = launch_rows<T, sv::MODE_TOPK>(p, stream);
-  else st = launch_rows<T, sv::MODE_SOFTMAX>(p, stream);
+  const bool streamable = p.V % vec_width(dt) == 0 && path_override() != 3;
+  if (mode == sv::MODE_GREEDY)
+    st = streamable ? launch_stream_dense<T, sv::MODE_GREEDY>(p, stream) : launch_rows<T, sv::MODE_GREEDY>(p, stream);
+  else if (mode == sv::MODE_TOPK)
+    st = streamable ? launch_stream_topk<T>(p, stream) : launch_rows<T, sv::MODE_TOPK>(p, stream);
+  else
+    st = streamable ? launch_stream_dense<T, sv::MODE_SOFTMAX>(p, stream) : launch_rows<T, sv::MODE_SOFTMAX>(p, stream);
   if (st != SV_OK) return st;
   timing_record(1, stream);
   if (mode == sv::MODE_SOFTMAX) st = launch_residual<T>(p, stream);

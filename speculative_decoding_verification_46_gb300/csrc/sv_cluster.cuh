@@ -71,7 +71,7 @@ __device__ __forceinline__ float smem_slot_mass(const T* Lrow, const float* Qrow
 
 template <typename T>
 __device__ __forceinline__ int smem_slot_walk(const T* Lrow, const float* Qrow, int e0, float c, float Mc,
-                                              float inv_s, double base, double target, int* last_pos) {
+                                              float inv_s, F2 base, F2 target, int* last_pos) {
   using TR = Tr<T>;
   constexpr int VW = TR::VW;
   const uint4 v = *reinterpret_cast<const uint4*>(Lrow + e0);
@@ -83,7 +83,7 @@ __device__ __forceinline__ int smem_slot_walk(const T* Lrow, const float* Qrow, 
     const float rv = Qrow ? fmaxf(__fsub_rn(pv, Qrow[e0 + t]), 0.f) : pv;
     acc = __fadd_rn(acc, rv);
     if (rv > 0.f) lastp = e0 + t;
-    if (found < 0 && base + (double)acc > target) found = e0 + t;
+    if (found < 0 && f2_lt(target, f2_add(base, F2{acc, 0.f}))) found = e0 + t;
   }
   *last_pos = lastp;
   return found;
@@ -93,8 +93,8 @@ struct ClusterSmem {
   float4 part[kMaxG1];       // this CTA's per-row partial: (max, s_hi, s_lo) or (max, index)
   float ell[kMaxG1];         // l(d_i) if d_i lies in this CTA's slice
   float qd[kMaxG1];          // q_i(d_i) if d_i lies in this CTA's slice
-  double smass[kClusterMaxNS];                 // this CTA's residual sub-range masses
-  double allmass[kClusterMax * kClusterMaxNS]; // every CTA's, in index order
+  F2 smass[kClusterMaxNS];                 // this CTA's residual sub-range masses
+  F2 allmass[kClusterMax * kClusterMaxNS]; // every CTA's, in index order
   float M[kMaxG1];
   double S[kMaxG1];
   float a[kMaxG1];
@@ -108,8 +108,8 @@ struct ClusterSmem {
   int owner;      // rank owning the inverse-CDF step (-1 none)
   int sub;
   int token;
-  double base;
-  double target;
+  F2 base;
+  F2 target;
   LocateSmem loc;
 };
 
@@ -360,7 +360,7 @@ cluster_kernel(const ClusterParams cp) {
     for (int j = 0; j < kClusterMaxNS; ++j) {
       if (j < NS) {
         const F2 t = block_sum_f2(F2{part[j], 0.f}, sm.f2red);
-        if (tid == 0) sm.smass[j] = (double)t.hi + (double)t.lo;
+        if (tid == 0) sm.smass[j] = t;
       }
     }
     cluster.sync();
@@ -368,16 +368,16 @@ cluster_kernel(const ClusterParams cp) {
       sm.allmass[e] = *cluster.map_shared_rank(&sm.smass[e % NS], e / NS);
     __syncthreads();
     {
-      const double u = (double)p.uniforms[b * G1 + G];
-      double R = 0.0, base = 0.0;
-      int sub = block_locate(sm.allmass, CN * NS, u, &R, &base, sm.loc, false);
+      const float u = p.uniforms[b * G1 + G];
+      F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
+      int sub = block_locate(sm.allmass, CN * NS, u, &R, &base, &tgt, sm.loc, false);
       if (tid == 0) {
-        sm.use_p = (attempt == 0 && resid && !bad && !(R > 0.0)) ? 1 : 0;
-        if (bad || !(R > 0.0)) sub = -1;
+        sm.use_p = (attempt == 0 && resid && !bad && !f2_pos(R)) ? 1 : 0;
+        if (bad || !f2_pos(R)) sub = -1;
         sm.owner = sub < 0 ? -1 : sub / NS;
         sm.sub = sub < 0 ? -1 : sub % NS;
         sm.base = base;
-        sm.target = u * R;
+        sm.target = tgt;
         sm.token = -1;
       }
     }
@@ -397,16 +397,16 @@ cluster_kernel(const ClusterParams cp) {
         if (jj == j) mine = part[jj];
       F2 total;
       const F2 ex = block_exclusive_f2(F2{mine, 0.f}, sm.f2red, &total);
-      const double tb = sm.base + (double)ex.hi + (double)ex.lo;
+      const F2 tb = f2_add(sm.base, ex);
       int lastp = -1;
-      if (k < nvec && mine > 0.f && tb <= sm.target && tb + (double)mine > sm.target) {
+      if (k < nvec && mine > 0.f && !f2_lt(sm.target, tb) && f2_lt(sm.target, f2_add(tb, F2{mine, 0.f}))) {
         const int found = smem_slot_walk<T>(Lf, Qf, k * VW, p.c, Mc, inv_s, tb, sm.target, &lastp);
         if (found >= 0) sm.token = v0 + found;
       }
       __syncthreads();
       if (sm.token < 0) {
         int lp = -1;
-        if (k < nvec) smem_slot_walk<T>(Lf, Qf, k * VW, p.c, Mc, inv_s, 0.0, 1e300, &lp);
+        if (k < nvec) smem_slot_walk<T>(Lf, Qf, k * VW, p.c, Mc, inv_s, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
         int m = lp >= 0 ? v0 + lp : -1;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));

@@ -82,7 +82,7 @@ struct Params {
   float4* part;                   // [R][S] per-slice partials
   unsigned long long* lists;      // [R][S][top_k] per-slice top-k candidates
   int2* rowres;                   // [R][top_k + 1] kept (index, probability) lists
-  double* chunk_mass;             // [B][C * slots] residual sub-range masses
+  float2* chunk_mass;             // [B][C * slots] residual sub-range masses (two-float)
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -250,6 +250,18 @@ __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
   float h = s + e;
   return F2{h, e - (h - s)};
 }
+// Ordering of normalised two-float numbers (|lo| <= ulp(hi) / 2, as f2_add
+// returns them).
+__device__ __forceinline__ bool f2_lt(F2 a, F2 b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ bool f2_pos(F2 a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
+// u * a with the product's rounding error kept (FMA two-product).
+__device__ __forceinline__ F2 f2_scale(F2 a, float u) {
+  const float p = u * a.hi;
+  float e = fmaf(u, a.hi, -p);
+  e = fmaf(u, a.lo, e);
+  const float h = p + e;
+  return F2{h, e - (h - p)};
+}
 __device__ __forceinline__ F2 f2_shfl_xor(F2 a, int m) {
   return F2{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
 }
@@ -332,53 +344,78 @@ __device__ __forceinline__ double warp_incl_scan_d(double v) {
   return v;
 }
 
+__device__ __forceinline__ F2 warp_incl_scan_f2(F2 v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const F2 o = f2_shfl_up(v, m);
+    if (lane >= m) v = f2_add(o, v);
+  }
+  return v;
+}
+
 struct LocateSmem {
-  double wsum[kWarps];
-  double carry;
-  double base;
+  F2 wsum[32];
+  F2 carry;
+  F2 base;
+  F2 lastbase;
   int found;
   int last;
-  double lastbase;
 };
 
-// Block-wide inverse-CDF search over NT masses in index order (global or
-// shared memory): total R, then the first k whose running interval
-// [prefix_k, prefix_k + m_k) holds t = u * R.  Both passes sum in the same
-// order, so t < R always lands inside unless rounding pushes it to the end, in
-// which case the last positive mass is taken.  Returns k (or -1 if R <= 0)
-// and its exclusive prefix in *base; every thread gets the result.
-__device__ int block_locate(const double* masses, int NT, double u, double* R_out, double* base_out,
+// Block-wide inverse-CDF search over NT two-float masses in index order
+// (global or shared memory): total R, then the first k whose running interval
+// [prefix_k, prefix_k + m_k) holds t = u * R.  Both passes add in the same
+// order, so t < R lands inside unless rounding pushes it to the very end, in
+// which case the last positive mass is taken.  Returns k (-1 if R <= 0), its
+// exclusive prefix in *base_out and t in *t_out; every thread gets them.
+// Float32 pipes only (two-float sums): this part's float64 rate is low.
+__device__ int block_locate(const F2* masses, int NT, float u, F2* R_out, F2* base_out, F2* t_out,
                             LocateSmem& ls, bool from_global) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  double R = 0.0;
+  const int nw = blockDim.x >> 5, nt = blockDim.x;
+  F2 R{0.f, 0.f};
+  F2 t{0.f, 0.f};
   for (int pass = 0; pass < 2; ++pass) {
-    const double t = u * R;
+    t = f2_scale(R, u);
     __syncthreads();   // every thread has read ls (the previous pass's total) before it is reset
-    if (tid == 0) { ls.carry = 0.0; ls.found = 0x7fffffff; ls.last = -1; ls.lastbase = 0.0; }
+    if (tid == 0) {
+      ls.carry = F2{0.f, 0.f};
+      ls.found = 0x7fffffff;
+      ls.last = -1;
+      ls.lastbase = F2{0.f, 0.f};
+    }
     __syncthreads();
-    for (int c0 = 0; c0 < NT; c0 += kThreads) {
+    for (int c0 = 0; c0 < NT; c0 += nt) {
       const int k = c0 + tid;
-      const double m = k < NT ? (from_global ? __ldcg(masses + k) : masses[k]) : 0.0;
-      const double inc = warp_incl_scan_d(m);
+      F2 m{0.f, 0.f};
+      if (k < NT) {
+        if (from_global) {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(masses) + k);
+          m = F2{v.x, v.y};
+        } else {
+          m = masses[k];
+        }
+      }
+      const F2 inc = warp_incl_scan_f2(m);
       if (lane == 31) ls.wsum[warp] = inc;
       __syncthreads();
-      double off = ls.carry;
-      double tot = ls.carry;
-      for (int w = 0; w < kWarps; ++w) {
-        if (w < warp) off += ls.wsum[w];
-        tot += ls.wsum[w];
+      F2 off = ls.carry, tot = ls.carry;
+      for (int w = 0; w < nw; ++w) {
+        if (w < warp) off = f2_add(off, ls.wsum[w]);
+        tot = f2_add(tot, ls.wsum[w]);
       }
-      double below = __shfl_up_sync(0xffffffffu, inc, 1);
-      if (lane == 0) below = 0.0;
-      const double excl = off + below;
-      if (pass == 1 && k < NT && m > 0.0) {
-        if (excl <= t && excl + m > t) atomicMin(&ls.found, k);   // at most one k qualifies
+      F2 below = f2_shfl_up(inc, 1);
+      if (lane == 0) below = F2{0.f, 0.f};
+      const F2 excl = f2_add(off, below);
+      if (pass == 1 && k < NT && f2_pos(m)) {
+        if (!f2_lt(t, excl) && f2_lt(t, f2_add(excl, m))) atomicMin(&ls.found, k);   // at most one k
         atomicMax(&ls.last, k);
       }
       __syncthreads();
-      if (pass == 1) {
-        if (ls.found == k && k < NT) ls.base = excl;
-        if (ls.last == k && k < NT) ls.lastbase = excl;
+      if (pass == 1 && k < NT) {
+        if (ls.found == k) ls.base = excl;
+        if (ls.last == k) ls.lastbase = excl;
       }
       if (tid == 0) ls.carry = tot;
       __syncthreads();
@@ -388,7 +425,8 @@ __device__ int block_locate(const double* masses, int NT, double u, double* R_ou
   }
   __syncthreads();
   *R_out = R;
-  if (!(R > 0.0)) return -1;
+  *t_out = t;
+  if (!f2_pos(R)) return -1;
   if (ls.found != 0x7fffffff) { *base_out = ls.base; return ls.found; }
   *base_out = ls.lastbase;
   return ls.last;
@@ -1058,7 +1096,7 @@ __device__ __forceinline__ float slot_mass(const T* row, const float* qrow, int 
 // exceeds target, or -1; *last_pos = the last element with a positive weight.
 template <typename T>
 __device__ __forceinline__ int slot_walk(const T* row, const float* qrow, int e0, int nv, float c, float Mc,
-                                         float inv_s, bool vec_ok, double base, double target, int* last_pos) {
+                                         float inv_s, bool vec_ok, F2 base, F2 target, int* last_pos) {
   using TR = Tr<T>;
   int found = -1, lastp = -1;
   if (nv > 0) {
@@ -1069,7 +1107,7 @@ __device__ __forceinline__ int slot_walk(const T* row, const float* qrow, int e0
       const float rv = qrow ? fmaxf(__fsub_rn(pv, __ldg(qrow + e0 + t)), 0.f) : pv;
       acc = __fadd_rn(acc, rv);
       if (rv > 0.f) lastp = e0 + t;
-      if (found < 0 && base + (double)acc > target) found = e0 + t;
+      if (found < 0 && f2_lt(target, f2_add(base, F2{acc, 0.f}))) found = e0 + t;
     }
   }
   *last_pos = lastp;
@@ -1082,8 +1120,8 @@ struct ResSmem {
   int flag;
   int sub;        // selected sub-range (chunk * NS + slot), -1 if none
   int token;
-  double target;
-  double base;
+  F2 target;
+  F2 base;
   LocateSmem loc;
 };
 
@@ -1114,7 +1152,7 @@ residual_kernel(const Params p) {
   const float Mc = st.M * p.c;
   const float inv_s = 1.0f / (float)st.s;
   const bool vec_ok = (V % VW) == 0;
-  double* cm = p.chunk_mass + (size_t)b * NT;
+  float2* cm = p.chunk_mass + (size_t)b * NT;
 
   // ---- masses of this chunk's NS sub-ranges
   const int c0 = c * p.CL;
@@ -1131,18 +1169,19 @@ residual_kernel(const Params p) {
   for (int j = 0; j < kMaxNS; ++j) {
     if (j < NS) {
       const F2 tot = block_sum_f2(F2{part[j], 0.f}, sm.f2red);
-      if (tid == 0) cm[c * NS + j] = (double)tot.hi + (double)tot.lo;
+      if (tid == 0) cm[c * NS + j] = make_float2(tot.hi, tot.lo);
     }
   }
   if (!arrive_last(p.seq_ticket2 + b, p.C, &sm.flag, true)) return;
 
   // ---- last CTA of sequence b: locate the inverse-CDF step
   int status = st.status;
-  const double u = (double)__ldg(p.uniforms + b * G1 + G);
-  double R = 0.0, base = 0.0;
-  int sub = block_locate(cm, NT, u, &R, &base, sm.loc, true);
+  const float u = __ldg(p.uniforms + b * G1 + G);
+  F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
+  const F2* cmf = reinterpret_cast<const F2*>(cm);
+  int sub = block_locate(cmf, NT, u, &R, &base, &tgt, sm.loc, true);
   const float* qsel = qrow;
-  if (resid && !bad && !(R > 0.0)) {
+  if (resid && !bad && !f2_pos(R)) {
     // zero residual mass (only through rounding): draw from p_n instead
     status |= SEQ_RESID0;
     qsel = nullptr;
@@ -1150,15 +1189,16 @@ residual_kernel(const Params p) {
       const int e0 = (k2 / NS) * p.CL + ((k2 % NS) * kThreads + tid) * VW;
       const float m2 = slot_mass<T>(row, nullptr, e0, min(max(V - e0, 0), VW), p.c, Mc, inv_s, vec_ok);
       const F2 tot = block_sum_f2(F2{m2, 0.f}, sm.f2red);
-      if (tid == 0) cm[k2] = (double)tot.hi + (double)tot.lo;
+      if (tid == 0) cm[k2] = make_float2(tot.hi, tot.lo);
     }
+    __threadfence_block();
     __syncthreads();
-    sub = block_locate(cm, NT, u, &R, &base, sm.loc, true);
+    sub = block_locate(cmf, NT, u, &R, &base, &tgt, sm.loc, true);
   }
   if (tid == 0) {
-    sm.sub = (bad || !(R > 0.0)) ? -1 : sub;
+    sm.sub = (bad || !f2_pos(R)) ? -1 : sub;
     sm.base = base;
-    sm.target = u * R;
+    sm.target = tgt;
     sm.token = -1;
   }
   __syncthreads();
@@ -1169,10 +1209,10 @@ residual_kernel(const Params p) {
     const float m2 = slot_mass<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok);
     F2 total;
     const F2 ex = block_exclusive_f2(F2{m2, 0.f}, sm.f2red, &total);
-    const double tbase = sm.base + (double)ex.hi + (double)ex.lo;
-    const double target = sm.target;
+    const F2 tbase = f2_add(sm.base, ex);
+    const F2 target = sm.target;
     int lastp = -1;
-    if (m2 > 0.f && tbase <= target && tbase + (double)m2 > target) {
+    if (m2 > 0.f && !f2_lt(target, tbase) && f2_lt(target, f2_add(tbase, F2{m2, 0.f}))) {
       const int found = slot_walk<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok, tbase, target, &lastp);
       if (found >= 0) sm.token = found;
     }
@@ -1180,7 +1220,7 @@ residual_kernel(const Params p) {
     if (sm.token < 0) {
       // rounding left no step above the target: take the last positive weight
       int lp = -1;
-      slot_walk<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok, 0.0, 1e300, &lp);
+      slot_walk<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
       int m = lp;
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -1195,7 +1235,7 @@ residual_kernel(const Params p) {
     }
     token = sm.token < 0 ? 0 : sm.token;
   }
-  for (int k2 = tid; k2 < NT; k2 += kThreads) cm[k2] = 0.0;
+  for (int k2 = tid; k2 < NT; k2 += kThreads) cm[k2] = make_float2(0.f, 0.f);
   if (tid == 0) {
     p.out_tokens[b * G1 + n] = token;
     if (p.out_status) p.out_status[b] = status;

@@ -1,0 +1,457 @@
+// Streaming path of libspecverify for large batches: persistent CTAs, one
+// whole row at a time, each thread prefetching its own future 16-byte vectors
+// with cp.async into a thread-private shared-memory ring S stages deep.
+//
+// Why this shape.  Every mode is bound by HBM bandwidth, which needs ~50 KB
+// of reads in flight per SM at all times.  A CTA that loads, then reduces,
+// then hands off, leaves HBM idle during the last two; here a thread's ring
+// already holds (or is fetching) the next S chunks of its row sequence -
+// including the first chunks of its NEXT row - while the current row is being
+// finished.  The ring is private to the thread that filled it (the thread
+// copies and later reads its own slots), so completion is tracked per thread
+// with cp.async.wait_group: there are no cross-thread waits, no mbarriers and
+// no spin loops.  Rows are dealt to CTAs round-robin; counts are balanced on
+// the host so that every CTA gets the same number of rows.
+//
+//   greedy   per-row argmax (ties -> lowest index; NaN flagged)
+//   softmax  per-row online max / sum of 2^((L - m) c) with rescaling when the
+//            running max grows; p(d_i) and a_i at the row's end
+//   top-k    pass 1 (the ring) keeps per-thread maxima; the k-th largest is a
+//            lower bound tau of the row's k-th value; pass 2 re-reads the row
+//            (an L2 hit, evict-first) and keeps the elements >= tau; exact rank
+//            selection; softmax(./T) + top-p over the k; a_i
+//
+// The last row of a sequence to finish (atomic ticket, no waiting) runs the
+// acceptance scan.  Greedy and top-k also do the final draw there; softmax
+// hands (n, m_n, s_n) to residual_kernel.
+#pragma once
+
+#include "sv_device.cuh"
+#include "sv_topk.cuh"
+
+namespace sv {
+
+constexpr int kSt = 256;      // threads per CTA
+constexpr int kStU = 4;       // vectors per thread per ring stage
+constexpr int kStS = 4;       // ring stages (dense modes)
+constexpr int kStSTopk = 3;   // ring stages (top-k; leaves room for its selection buffers)
+static_assert(kSt == kThreads, "the block reductions assume kThreads threads");
+
+__device__ __forceinline__ void cpa16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cpa_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+struct StreamSmem {
+  float fred[kSt / 32];
+  F2 f2red[kSt / 32];
+  float2 pair[kSt / 32];
+  int flag;
+  int n;
+  int status;
+  int token;
+  int g[kMaxG1];
+  int bad[kMaxG1];
+  float M[kMaxG1];
+  double s[kMaxG1];
+  float a[kMaxG1];
+  int dr[kMaxG1];
+  float ur[kMaxG1];
+};
+
+// Per-thread sequence of ring items: item = (j-th row of this CTA, chunk c).
+struct RowWalk {
+  int R, G1, NV, CH, NCH, nrows;
+  __device__ __forceinline__ int row_of(int j) const { return blockIdx.x + j * gridDim.x; }
+};
+
+template <typename T, int S>
+__device__ __forceinline__ void ring_issue(uint4* ring, const T* logits, size_t V, const RowWalk& w, int item) {
+  const int total = w.nrows * w.NCH;
+  if (item < total) {
+    const int j = item / w.NCH, c = item - j * w.NCH;
+    const T* row = logits + (size_t)w.row_of(j) * V;
+    uint4* slot = ring + (size_t)(item % S) * kStU * kSt;
+#pragma unroll
+    for (int u = 0; u < kStU; ++u) {
+      const int v = c * w.CH + u * kSt + (int)threadIdx.x;
+      if (v < w.NV) cpa16(slot + u * kSt + threadIdx.x, row + (size_t)v * Tr<T>::VW);
+    }
+  }
+  cpa_commit();   // empty groups keep every thread's group count in step
+}
+
+// ---- dense finisher: per-row statistics already merged (one entry per row)
+template <int MODE>
+__device__ void stream_finish_dense(const Params& p, int b, StreamSmem& sm) {
+  const int tid = threadIdx.x;
+  const int G = p.gamma, G1 = G + 1, V = p.V;
+  if (tid < G1) {
+    const float4 v = __ldcg(p.part + (size_t)b * G1 + tid);
+    if (MODE == MODE_GREEDY) {
+      const bool nan = v.x != v.x;
+      const int bi = __float_as_int(v.y);
+      sm.g[tid] = (nan || bi == 0x7fffffff) ? 0 : bi;
+      sm.bad[tid] = nan;
+    } else {
+      const double s = (double)v.y + (double)v.z;
+      sm.M[tid] = v.x;
+      sm.s[tid] = s;
+      sm.bad[tid] = !(v.x > -INFINITY && v.x < INFINITY) || !(s > 0.0 && s < 1e300);
+      if (tid < G) sm.a[tid] = (float)__ldcg(p.acc + b * G + tid);
+    }
+    sm.ur[tid] = MODE == MODE_SOFTMAX ? __ldg(p.uniforms + b * G1 + tid) : 0.f;
+    if (tid < G) sm.dr[tid] = __ldg(p.draft + b * G + tid);
+  }
+  if (tid == 0) sm.status = __ldcg(&p.seq[b].status);
+  __syncthreads();
+  for (int e = tid; e < G1; e += kSt) p.part[(size_t)b * G1 + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int e = tid; e < G; e += kSt) p.acc[b * G + e] = 0.0;
+  if (tid == 0) {
+    int status = sm.status, n = G;
+    for (int i = 0; i < G1; ++i)
+      if (sm.bad[i]) status |= SEQ_BADROW;
+    if (MODE == MODE_GREEDY) {
+      for (int i = 0; i < G; ++i)
+        if (sm.dr[i] != sm.g[i]) { n = i; break; }
+      sm.token = sm.g[n];
+      p.seq[b].status = 0;
+      if (p.out_status) p.out_status[b] = status;
+    } else {
+      for (int i = 0; i < G; ++i)
+        if (!(sm.ur[i] < sm.a[i])) { n = i; break; }
+      SeqState st;
+      st.n = n;
+      st.status = status;
+      st.M = sm.M[n];
+      st.pad = 0;
+      st.s = sm.s[n];
+      p.seq[b] = st;
+    }
+    sm.n = n;
+    p.out_n[b] = n;
+  }
+  __syncthreads();
+  const int n = sm.n;
+  for (int j = tid; j < G1; j += kSt) {
+    if (j < n) p.out_tokens[b * G1 + j] = sm.dr[j];
+    else if (j > n) p.out_tokens[b * G1 + j] = -1;
+    else if (MODE == MODE_GREEDY) p.out_tokens[b * G1 + j] = sm.token;
+  }
+}
+
+// ---- greedy / softmax streaming kernel
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kSt, 3)
+stream_dense_kernel(const Params p) {
+  using TR = Tr<T>;
+  constexpr int VW = TR::VW;
+  constexpr int S = kStS;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint4* ring = reinterpret_cast<uint4*>(smem_raw);
+  StreamSmem& sm = *reinterpret_cast<StreamSmem*>(smem_raw + (size_t)S * kStU * kSt * sizeof(uint4));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.gamma, G1 = G + 1, V = p.V;
+  RowWalk w;
+  w.R = p.B * G1;
+  w.G1 = G1;
+  w.NV = V / VW;
+  w.CH = kStU * kSt;
+  w.NCH = (w.NV + w.CH - 1) / w.CH;
+  w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const T* logits = static_cast<const T*>(p.logits);
+
+#pragma unroll
+  for (int s = 0; s < S; ++s) ring_issue<T, S>(ring, logits, V, w, s);
+  int item = 0;
+  for (int j = 0; j < w.nrows; ++j) {
+    const int r = w.row_of(j);
+    const int b = r / G1, i = r - b * G1;
+    // the draft's logit and q(d) for this row, fetched early (softmax only)
+    float l_d = 0.f, q_d = 0.f;
+    int d = -1;
+    if (MODE == MODE_SOFTMAX && tid == 0 && i < G) {
+      d = __ldg(p.draft + b * G + i);
+      if (d >= 0 && d < V) {
+        l_d = Tr<T>::get(load_slot<T>(logits + (size_t)r * V, d, 1, false), 0);
+        q_d = __ldg(p.q + ((size_t)b * G + i) * V + d);
+      }
+    }
+    float bv = -INFINITY;            // greedy: best value / index; softmax: running max
+    int bi = 0x7fffffff;
+    float m = -INFINITY, s0 = 0.f, s1 = 0.f;
+    for (int c = 0; c < w.NCH; ++c, ++item) {
+      cpa_wait<S - 1>();
+      const uint4* slot = ring + (size_t)(item % S) * kStU * kSt;
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) {
+        const int v = c * w.CH + u * kSt + tid;
+        if (v < w.NV) {
+          const uint4 x = slot[u * kSt + tid];
+          if (MODE == MODE_GREEDY) {
+            const float vm = TR::template vmax<true>(x);
+            if (argmax_better(vm, 1, bv, 0) || bi == 0x7fffffff) {
+#pragma unroll
+              for (int t = VW - 1; t >= 0; --t) {
+                const float e = TR::get(x, t);
+                if ((vm != vm) ? (e != e) : (e == vm)) bi = v * VW + t;
+              }
+              bv = vm;
+            }
+          } else {
+            const float vm = TR::template vmax<false>(x);
+            if (vm > m) {
+              const float sc = (m == -INFINITY) ? 0.f : ex2_approx((m - vm) * p.c);
+              s0 *= sc;
+              s1 *= sc;
+              m = vm;
+            }
+            if (m > -INFINITY) {
+              const float mc = m * p.c;
+#pragma unroll
+              for (int t = 0; t < VW; t += 2) {
+                s0 += ex2_approx(fmaf(TR::get(x, t), p.c, -mc));
+                s1 += ex2_approx(fmaf(TR::get(x, t + 1), p.c, -mc));
+              }
+            }
+          }
+        }
+      }
+      ring_issue<T, S>(ring, logits, V, w, item + S);
+    }
+    // ---- the row's statistic
+    if (MODE == MODE_GREEDY) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) sm.pair[warp] = make_float2(bv, __int_as_float(bi));
+      __syncthreads();
+      if (tid == 0) {
+        float v0 = sm.pair[0].x;
+        int i0 = __float_as_int(sm.pair[0].y);
+        for (int k2 = 1; k2 < kSt / 32; ++k2) {
+          const float ov = sm.pair[k2].x;
+          const int oi = __float_as_int(sm.pair[k2].y);
+          if (argmax_better(ov, oi, v0, i0)) { v0 = ov; i0 = oi; }
+        }
+        p.part[r] = make_float4(v0, __int_as_float(i0), 0.f, 0.f);
+        if (i < G) {
+          const int dd = __ldg(p.draft + b * G + i);
+          if (dd < 0 || dd >= V) atomicOr(&p.seq[b].status, SEQ_OOB);
+        }
+      }
+    } else {
+      float M = m;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      if (lane == 0) sm.fred[warp] = M;
+      __syncthreads();
+      M = sm.fred[0];
+#pragma unroll
+      for (int k2 = 1; k2 < kSt / 32; ++k2) M = fmaxf(M, sm.fred[k2]);
+      F2 acc{0.f, 0.f};
+      if (m > -INFINITY && M < INFINITY) {
+        const float sc = ex2_approx((m - M) * p.c);
+        acc = f2_add(F2{s0 * sc, 0.f}, F2{s1 * sc, 0.f});
+      }
+      const F2 tot = block_sum_f2(acc, sm.f2red);
+      if (tid == 0) {
+        p.part[r] = make_float4(M, tot.hi, tot.lo, 0.f);
+        if (i < G) {
+          float a = 0.f;
+          int st = 0;
+          const float ssum = tot.hi + tot.lo;
+          const bool bad = !(M > -INFINITY && M < INFINITY) || !(ssum > 0.f && ssum < INFINITY);
+          if (d < 0 || d >= V) {
+            st |= SEQ_OOB;
+          } else {
+            const float pd = bad ? 0.f : exp2f((l_d - M) * p.c) / ssum;
+            if (q_d > 0.f) {
+              a = fminf(1.f, pd / q_d);
+            } else {
+              a = pd > 0.f ? 1.f : 0.f;
+              st |= SEQ_QBAD;
+            }
+          }
+          if (st) atomicOr(&p.seq[b].status, st);
+          p.acc[b * G + i] = (double)a;
+          if (p.out_a) p.out_a[b * G + i] = a;
+        }
+      }
+    }
+    if (arrive_last(p.seq_ticket + b, G1, &sm.flag, true)) stream_finish_dense<MODE>(p, b, sm);
+  }
+  cpa_wait<0>();
+}
+
+// ---- top-k streaming kernel (pass 1 through the ring)
+template <typename T>
+__global__ void __launch_bounds__(kSt, 2)
+stream_topk_kernel(const Params p) {
+  using TR = Tr<T>;
+  constexpr int VW = TR::VW;
+  constexpr int S = kStSTopk;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  uint4* ring = reinterpret_cast<uint4*>(smem_raw);
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw + (size_t)S * kStU * kSt * sizeof(uint4));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.gamma, G1 = G + 1, V = p.V, k = p.top_k;
+  RowWalk w;
+  w.R = p.B * G1;
+  w.G1 = G1;
+  w.NV = V / VW;
+  w.CH = kStU * kSt;
+  w.NCH = (w.NV + w.CH - 1) / w.CH;
+  w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const T* logits = static_cast<const T*>(p.logits);
+  const uint64_t pol_first = policy_evict_first();
+  constexpr int kWarpsHere = kSt / 32;
+  constexpr int kCapW = kTkCap / kWarpsHere;   // candidate entries per warp
+
+#pragma unroll
+  for (int s = 0; s < S; ++s) ring_issue<T, S>(ring, logits, V, w, s);
+  int item = 0;
+  for (int j = 0; j < w.nrows; ++j) {
+    const int r = w.row_of(j);
+    const int b = r / G1, i = r - b * G1;
+    const T* row = logits + (size_t)r * V;
+    __syncthreads();   // the previous row's shared state is no longer in use
+    if (tid < kWarpsHere) sm.wcount[tid] = 0;
+    int d_row = -1;
+    float q_row = 0.f;
+    if (tid == 0 && i < G) {
+      d_row = __ldg(p.draft + b * G + i);
+      if (d_row >= 0 && d_row < V) q_row = __ldg(p.q + ((size_t)b * G + i) * V + d_row);
+    }
+    // ---- pass 1 through the ring: thread maxima
+    float tmax = -INFINITY;
+    int any = 0;
+    for (int c = 0; c < w.NCH; ++c, ++item) {
+      cpa_wait<S - 1>();
+      const uint4* slot = ring + (size_t)(item % S) * kStU * kSt;
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) {
+        if (c * w.CH + u * kSt + tid < w.NV) {
+          tmax = fmaxf(tmax, TR::template vmax<false>(slot[u * kSt + tid]));
+          any = 1;
+        }
+      }
+      ring_issue<T, S>(ring, logits, V, w, item + S);
+    }
+    const uint32_t tkey = any ? okey(tmax) : 0u;
+    uint32_t K = 0u;
+    if (V > k) {
+      for (int bit = 31; bit >= TR::KEY_LOW_BIT; --bit) {
+        const uint32_t Kt = K | (1u << bit);
+        if (__syncthreads_count(tkey >= Kt) >= k) K = Kt;
+      }
+    } else {
+      __syncthreads();
+    }
+    const float tau = K == 0u ? -INFINITY : key_to_float(K);
+    // ---- pass 2 (L2): candidates >= tau
+    int nan_seen = 0;
+    unsigned long long* wbuf = sm.cand + warp * kCapW;
+    for (int v0 = tid; v0 < w.NV; v0 += kSt * kStU) {
+      uint4 buf[kStU];
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) {
+        const int vi = v0 + u * kSt;
+        if (vi < w.NV) buf[u] = ldg_v4_hint(row + (size_t)vi * VW, pol_first);
+      }
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) {
+        const int vi = v0 + u * kSt;
+        if (vi < w.NV) {
+          const float mm = TR::template vmax<true>(buf[u]);
+          if (!(mm < tau)) {
+#pragma unroll
+            for (int t = 0; t < VW; ++t) {
+              const float x = TR::get(buf[u], t);
+              if (x != x) {
+                nan_seen = 1;
+              } else if (x >= tau) {
+                const int pos = atomicAdd(&sm.wcount[warp], 1);
+                if (pos < kCapW) wbuf[pos] = comp_key(x, vi * VW + t);
+              }
+            }
+          }
+        }
+      }
+    }
+    const int bad_nan = __syncthreads_or(nan_seen);
+    int overflow = 0, N = 0;
+    for (int w2 = 0; w2 < kWarpsHere; ++w2) {
+      overflow |= sm.wcount[w2] > kCapW;
+      N += min(sm.wcount[w2], kCapW);
+    }
+    if (overflow) {
+      // exact k-th largest (value, index) key by bisection over the row
+      unsigned long long K64 = 0ull;
+      for (int bit = 63; bit >= 0; --bit) {
+        const unsigned long long Kt = K64 | (1ull << bit);
+        int mine = 0;
+        for (int vi = tid; vi < w.NV; vi += kSt) {
+          const uint4 v = ldg_v4(row + (size_t)vi * VW);
+#pragma unroll
+          for (int t = 0; t < VW; ++t) {
+            const float x = TR::get(v, t);
+            mine += (x == x && comp_key(x, vi * VW + t) >= Kt);
+          }
+        }
+        if (block_sum_int_n(mine, sm.ired) >= k) K64 = Kt;
+      }
+      __syncthreads();
+      if (tid == 0) sm.count = 0;
+      __syncthreads();
+      for (int vi = tid; vi < w.NV; vi += kSt) {
+        const uint4 v = ldg_v4(row + (size_t)vi * VW);
+#pragma unroll
+        for (int t = 0; t < VW; ++t) {
+          const float x = TR::get(v, t);
+          if (x == x) {
+            const unsigned long long ck = comp_key(x, vi * VW + t);
+            if (ck >= K64) {
+              const int pos = atomicAdd(&sm.count, 1);
+              if (pos < kTkCap) sm.cand[pos] = ck;
+            }
+          }
+        }
+      }
+      __syncthreads();
+      N = min(sm.count, kTkCap);
+      for (int e = tid; e < N; e += kSt) {
+        const unsigned long long me = sm.cand[e];
+        int rank = 0;
+        for (int jj = 0; jj < N; ++jj) rank += sm.cand[jj] > me;
+        if (rank < k) sm.sel[rank] = me;
+      }
+    } else {
+      for (int w2 = 0; w2 < kWarpsHere; ++w2) {
+        const int cw = min(sm.wcount[w2], kCapW);
+        for (int s2 = tid; s2 < cw; s2 += kSt) {
+          const unsigned long long me = sm.cand[w2 * kCapW + s2];
+          int rank = 0;
+          for (int w3 = 0; w3 < kWarpsHere; ++w3) {
+            const int c3 = min(sm.wcount[w3], kCapW);
+            const unsigned long long* src = sm.cand + w3 * kCapW;
+            for (int jj = 0; jj < c3; ++jj) rank += src[jj] > me;
+          }
+          if (rank < k) sm.sel[rank] = me;
+        }
+      }
+    }
+    __syncthreads();
+    topk_row_epilogue(p, b, i, r, min(k, N), bad_nan != 0, d_row, q_row, sm);
+    if (arrive_last(p.seq_ticket + b, G1, &sm.flag)) topk_finish_sequence(p, b, sm);
+  }
+  cpa_wait<0>();
+}
+
+}  // namespace sv

@@ -59,10 +59,12 @@ def _random_case(seed, B, G, V, dtype, T=1.0, ties=False, spread=2.0, top_k=0, t
 
 # ------------------------------------------------------------------ greedy
 
-@pytest.fixture(params=["auto", "grid", "cluster"])
+@pytest.fixture(params=["auto", "grid", "cluster", "slices"])
 def path(request, monkeypatch):
     """Which kernel path the library takes: its own choice (small problems go
-    to the one-cluster-per-sequence kernel), or forced."""
+    to the one-cluster-per-sequence kernel, larger ones to the streaming
+    kernels), or forced: grid = streaming kernels (when V is a multiple of the
+    vector width), cluster, slices = the per-slice grid kernels."""
     if request.param != "auto":
         monkeypatch.setenv("SPECVERIFY_PATH", request.param)
     else:
@@ -139,7 +141,7 @@ def test_sample_config_b4_g4_v1024_f32_rounds(sv):
     assert totals["boundary_mismatch"] <= P.BOUNDARY_FRACTION * totals["draws"]
 
 
-@pytest.mark.parametrize("force", [None, "grid"])
+@pytest.mark.parametrize("force", [None, "grid", "slices"])
 def test_sample_config_b1_g5_v32000_bf16_rounds(sv, force, monkeypatch):
     if force:
         monkeypatch.setenv("SPECVERIFY_PATH", force)
@@ -168,7 +170,7 @@ def test_sample_full_size_b64(sv, name):
 
 @pytest.fixture(params=["auto", "slices"])
 def topk_path(request, monkeypatch):
-    """Top-k kernel: the per-row persistent one (library's choice when V is a
+    """Top-k kernel: the streaming per-row one (library's choice when V is a
     multiple of the vector width) or the per-slice one (forced)."""
     if request.param == "slices":
         monkeypatch.setenv("SPECVERIFY_PATH", "slices")
