@@ -55,6 +55,8 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size B (smaller cases for ncu captures)")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the short summary runs of the other workloads (N=1 only)")
     return ap.parse_args()
 
 
@@ -389,6 +391,61 @@ def run_gb300(args, rank, ws_n, local):
     return line, w
 
 
+def other_workloads(args, local):
+    """Short device-side runs of the other workloads (graph replay, rotating
+    input sets, no flush), each ~0.3 s of timed work: value, ms/step, HBM GB/s
+    and the fraction of the measured peak for the whole step."""
+    import speculative_decoding_verification_46_gb300 as sv
+
+    dev = torch.device("cuda", local)
+    peak, _ = _peaks()
+    out = {}
+    for name, w in workloads.WORKLOADS.items():
+        if name == args.workload:
+            continue
+        B, G, V = w.B, w.gamma, w.V
+        per_set = B * (G + 1) * V * _elt_bytes(w) + (B * G * V * 4 if w.mode == "sample" else 0)
+        n_sets = max(2, min(512, math.ceil(2 * L2_BYTES / per_set) + 1))
+        sets = _input_sets(w, n_sets, dev)
+        outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
+                 torch.empty(B, G, dtype=torch.float32, device=dev) if w.mode == "sample" and G > 0 else None,
+                 torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
+        wsp = sv.alloc_workspace(B, G, V, w.top_k if w.mode == "sample" else 0, dev)
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            for i in range(n_sets):
+                _call(sv, w, sets[i], outs[i], wsp, stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n_sets):
+                _call(sv, w, sets[i], outs[i], wsp, stream)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, int(0.3 / max(time.perf_counter() - t0, 1e-6)))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * n_sets)
+        nacc = np.concatenate([o[1].cpu().numpy() for o in outs])
+        ab = algorithmic_bytes(w, nacc)
+        gbs = (ab["stream"] + ab["final"]) / n_sets / (ms / 1e3) / 1e9
+        out[name] = {"value": B * (G + 1) / (ms / 1e3), "ms_per_step": ms, "hbm_gbs": gbs,
+                     "frac_of_measured_peak": gbs / peak, "steps": reps * n_sets}
+        del sets, outs, wsp, graph
+        torch.cuda.empty_cache()
+    return out
+
+
 def oracle_throughput(w, budget_s: float, device="cpu"):
     """The CPU oracle on a bounded sample of the workload: whole batches of
     B sequences when they fit the budget, else a prefix of one batch."""
@@ -469,6 +526,8 @@ def main():
         return
 
     line, w = run_gb300(args, rank, ws_n, local)
+    if rank == 0 and ws_n == 1 and not args.no_other_workloads and args.batch is None:
+        line["other_workloads"] = other_workloads(args, local)
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         v, sample = oracle_throughput(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,

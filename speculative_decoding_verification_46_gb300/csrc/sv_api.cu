@@ -62,7 +62,7 @@ Layout make_layout(int B, int gamma, int V, int top_k) {
   L.part = o;        o += up(sizeof(float4) * (size_t)R * L.S_part);
   L.lists = o;       o += up(sizeof(unsigned long long) * (size_t)R * L.S_list * L.klist);
   L.rowres = o;      o += up(L.klist > 0 ? sizeof(int2) * (size_t)R * (L.klist + 1) : 0);
-  L.chunk = o;       o += up(sizeof(double) * (size_t)B * L.C_max);
+  L.chunk = o;       o += up(3 * sizeof(float2) * (size_t)B * L.C_max);
   L.total = o;
   return L;
 }
@@ -360,7 +360,11 @@ extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logit
   p.V = V;
   p.top_k = klist;
   p.top_p = top_p;
-  p.c = (float)(1.4426950408889634 / (double)temperature);
+  {
+    const double c = 1.4426950408889634 / (double)temperature;
+    p.c = (float)c;
+    p.c_lo = (float)(c - (double)p.c);
+  }
   p.logits = logits;
   p.q = q;
   p.draft = draft_tokens;

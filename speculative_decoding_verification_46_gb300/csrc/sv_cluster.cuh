@@ -52,49 +52,15 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Shared-memory counterparts of slot_mass / slot_walk (same arithmetic, same
-// rounding steps): one 16-byte vector of the slice at element offset e0.
-template <typename T>
-__device__ __forceinline__ float smem_slot_mass(const T* Lrow, const float* Qrow, int e0, float c, float Mc,
-                                                float inv_s) {
-  using TR = Tr<T>;
-  constexpr int VW = TR::VW;
-  const uint4 v = *reinterpret_cast<const uint4*>(Lrow + e0);
-  float acc = 0.f;
-#pragma unroll
-  for (int t = 0; t < VW; ++t) {
-    const float pv = __fmul_rn(ex2_approx(fmaf(TR::get(v, t), c, -Mc)), inv_s);
-    acc = __fadd_rn(acc, Qrow ? fmaxf(__fsub_rn(pv, Qrow[e0 + t]), 0.f) : pv);
-  }
-  return acc;
-}
-
-template <typename T>
-__device__ __forceinline__ int smem_slot_walk(const T* Lrow, const float* Qrow, int e0, float c, float Mc,
-                                              float inv_s, F2 base, F2 target, int* last_pos) {
-  using TR = Tr<T>;
-  constexpr int VW = TR::VW;
-  const uint4 v = *reinterpret_cast<const uint4*>(Lrow + e0);
-  float acc = 0.f;
-  int found = -1, lastp = -1;
-#pragma unroll
-  for (int t = 0; t < VW; ++t) {
-    const float pv = __fmul_rn(ex2_approx(fmaf(TR::get(v, t), c, -Mc)), inv_s);
-    const float rv = Qrow ? fmaxf(__fsub_rn(pv, Qrow[e0 + t]), 0.f) : pv;
-    acc = __fadd_rn(acc, rv);
-    if (rv > 0.f) lastp = e0 + t;
-    if (found < 0 && f2_lt(target, f2_add(base, F2{acc, 0.f}))) found = e0 + t;
-  }
-  *last_pos = lastp;
-  return found;
-}
-
 struct ClusterSmem {
   float4 part[kMaxG1];       // this CTA's per-row partial: (max, s_hi, s_lo) or (max, index)
-  float ell[kMaxG1];         // l(d_i) if d_i lies in this CTA's slice
-  float qd[kMaxG1];          // q_i(d_i) if d_i lies in this CTA's slice
-  F2 smass[kClusterMaxNS];                 // this CTA's residual sub-range masses
-  F2 allmass[kClusterMax * kClusterMaxNS]; // every CTA's, in index order
+  float ur[kMaxG1];          // this sequence's uniforms
+  F2x3 sub3[kClusterMaxNS];                // this CTA's (S, A, Q) per sub-range
+  F2 allmass[kClusterMax * kClusterMaxNS]; // every CTA's masses, in index order
+  F2 allS[kClusterMax * kClusterMaxNS];
+  float allQ[kClusterMax * kClusterMaxNS];
+  F2x3 red[kWarps];
+  F2 ds;
   float M[kMaxG1];
   double S[kMaxG1];
   float a[kMaxG1];
@@ -146,7 +112,7 @@ __device__ __forceinline__ float4 group_merge(float4 v, int CN, float c) {
 }
 
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 cluster_kernel(const ClusterParams cp) {
   using TR = Tr<T>;
   constexpr int VW = TR::VW;
@@ -182,11 +148,19 @@ cluster_kernel(const ClusterParams cp) {
     }
   }
   cp_async_commit();
+  // this sequence's drafts with their logit and q value (plain loads, in
+  // flight together with the slices; every CTA needs them for the scan)
   int d_own = -1;
+  float l_own = 0.f, q_own = 0.f, u_own = 0.f;
   if (tid < G) {
-    const int d = p.draft[b * G + tid];
-    d_own = d;
+    d_own = __ldg(p.draft + b * G + tid);
+    if (d_own >= 0 && d_own < V) {
+      l_own = Tr<T>::get(load_slot<T>(Lg + (size_t)tid * V, d_own, 1, false), 0);
+      if (MODE == MODE_SOFTMAX) q_own = __ldg(p.q + ((size_t)b * G + tid) * V + d_own);
+    }
   }
+  if (MODE == MODE_SOFTMAX && tid < G1) u_own = __ldg(p.uniforms + b * G1 + tid);
+  if (tid < G1) sm.ur[tid] = u_own;
   cp_async_wait<1>();
   __syncthreads();
 
@@ -239,16 +213,6 @@ cluster_kernel(const ClusterParams cp) {
       if (lane == 0) sm.part[i] = make_float4(M, s.hi, s.lo, 0.f);
     }
   }
-  if (MODE == MODE_SOFTMAX) cp_async_wait<0>();
-  __syncthreads();
-  // l(d_i), q(d_i) of the drafts whose token lies in this slice
-  if (tid < G) {
-    const int d = d_own;
-    if (d >= v0 && d < v1) {
-      sm.ell[tid] = TR::get(*reinterpret_cast<const uint4*>(Ls + (size_t)tid * W + (d - v0) / VW * VW), (d - v0) % VW);
-      if (MODE == MODE_SOFTMAX) sm.qd[tid] = Qs[(size_t)tid * W + (d - v0)];
-    }
-  }
   cluster.sync();
 
   // ---- merge the CN partials of every row (16 lanes per row), then the scan
@@ -281,9 +245,8 @@ cluster_kernel(const ClusterParams cp) {
     if (d < 0 || d >= V) {
       st |= SEQ_OOB;
     } else {
-      const int own = d / W;
-      const float l = *cluster.map_shared_rank(&sm.ell[tid], own);
-      const float qd = *cluster.map_shared_rank(&sm.qd[tid], own);
+      const float l = l_own;
+      const float qd = q_own;
       const float pd = sm.bad[tid] ? 0.f : exp2f((l - sm.M[tid]) * p.c) / (float)sm.S[tid];
       if (qd > 0.0f) {
         a = fminf(1.f, pd / qd);
@@ -311,7 +274,7 @@ cluster_kernel(const ClusterParams cp) {
     } else {
       for (int i = 0; i < G; ++i) status |= sm.st[i];
       for (int i = 0; i < G; ++i)
-        if (!(p.uniforms[b * G1 + i] < sm.a[i])) { n = i; break; }
+        if (!(sm.ur[i] < sm.a[i])) { n = i; break; }
     }
     sm.n = n;
     sm.status = status;
@@ -337,99 +300,133 @@ cluster_kernel(const ClusterParams cp) {
   }
 
   // ---- final draw: residual of row n, or the bonus from row gamma
+  // (precise weights and the (S, A, Q) decomposition, as in residual_kernel)
   const bool resid = n < G;
   const bool bad = (sm.status & SEQ_BADROW) != 0;
   const T* Lf = Ls + (size_t)n * W;
   const float* Qf = resid ? Qs + (size_t)n * W : nullptr;
-  const float Mc = sm.M[n] * p.c;
-  const float inv_s = 1.0f / (float)sm.S[n];
+  const float M = sm.M[n];
+  const float s_a = (float)sm.S[n];
   const int NS = cp.NS;
   int status = sm.status;
-  int token = 0;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    // this CTA's sub-range masses (sub-range j = vectors [256 j, 256 j + 256))
-    float part[kClusterMaxNS];
+  cp_async_wait<0>();     // this thread's q copies have landed
+  __syncthreads();        // ... and every thread's are visible to all
 #pragma unroll
-    for (int j = 0; j < kClusterMaxNS; ++j) {
-      part[j] = 0.f;
+  for (int j = 0; j < kClusterMaxNS; ++j) {
+    if (j < NS) {
+      SlotRun run;
+      run.zero();
       const int k = j * kThreads + tid;
-      if (j < NS && k < nvec && !bad)
-        part[j] = smem_slot_mass<T>(Lf, Qf, k * VW, p.c, Mc, inv_s);
-    }
+      if (k < nvec && !bad) {
+        const uint4 v = *reinterpret_cast<const uint4*>(Lf + k * VW);
+        float qv[VW];
 #pragma unroll
-    for (int j = 0; j < kClusterMaxNS; ++j) {
-      if (j < NS) {
-        const F2 t = block_sum_f2(F2{part[j], 0.f}, sm.f2red);
-        if (tid == 0) sm.smass[j] = t;
+        for (int t = 0; t < VW; ++t) qv[t] = resid ? Qf[k * VW + t] : 0.f;
+        run = slot_run<T>(v, qv, VW, resid, M, p.c, p.c_lo, s_a);
       }
+      const F2x3 t = block_sum_f2x3(F2x3{run.S(), run.A(), F2{run.q, 0.f}}, sm.red);
+      if (tid == 0) sm.sub3[j] = t;
     }
-    cluster.sync();
-    for (int e = tid; e < CN * NS; e += kThreads)
-      sm.allmass[e] = *cluster.map_shared_rank(&sm.smass[e % NS], e / NS);
-    __syncthreads();
-    {
-      const float u = p.uniforms[b * G1 + G];
-      F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
-      int sub = block_locate(sm.allmass, CN * NS, u, &R, &base, &tgt, sm.loc, false);
-      if (tid == 0) {
-        sm.use_p = (attempt == 0 && resid && !bad && !f2_pos(R)) ? 1 : 0;
-        if (bad || !f2_pos(R)) sub = -1;
-        sm.owner = sub < 0 ? -1 : sub / NS;
-        sm.sub = sub < 0 ? -1 : sub % NS;
-        sm.base = base;
-        sm.target = tgt;
-        sm.token = -1;
-      }
+  }
+  cluster.sync();
+  // every CTA: the exact normaliser and the masses of all CN * NS sub-ranges
+  F2 sl{0.f, 0.f};
+  for (int e = tid; e < CN * NS; e += kThreads) {
+    const F2x3 r3 = *cluster.map_shared_rank(&sm.sub3[e % NS], e / NS);
+    sm.allS[e] = r3.a;
+    sm.allmass[e] = r3.b;                 // A; corrected below once s is known
+    sl = f2_add(sl, r3.a);
+    sm.allQ[e] = r3.c.hi;
+  }
+  const F2 s = block_sum_f2(sl, sm.f2red);
+  const F2 ds = f2_add(s, F2{-s_a, 0.f});
+  for (int e = tid; e < CN * NS; e += kThreads) {
+    if (resid) {
+      F2 m = f2_add(sm.allmass[e], f2_neg(f2_scale(ds, sm.allQ[e])));
+      if (m.hi < 0.f) m = F2{0.f, 0.f};
+      sm.allmass[e] = m;
+    } else {
+      sm.allmass[e] = sm.allS[e];
     }
-    cluster.sync();   // everyone has read the masses before they can change
-    if (sm.use_p) {
+  }
+  __syncthreads();
+  {
+    const float u = sm.ur[G];
+    F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
+    bool use_q = resid;
+    int sub = locate(sm.allmass, CN * NS, u, &R, &base, &tgt, sm.loc, false);
+    if (resid && !bad && !f2_pos(R)) {
       // zero residual mass (only through rounding): draw from p_n instead
       status |= SEQ_RESID0;
-      Qf = nullptr;
-      continue;
+      use_q = false;
+      sub = locate(sm.allS, CN * NS, u, &R, &base, &tgt, sm.loc, false);
     }
-    if (sm.owner == rank) {
-      const int j = sm.sub;
-      const int k = j * kThreads + tid;
-      float mine = 0.f;
+    if (tid == 0) {
+      if (bad || !f2_pos(R)) sub = -1;
+      sm.owner = sub < 0 ? -1 : sub / NS;
+      sm.sub = sub < 0 ? -1 : sub % NS;
+      sm.base = base;
+      sm.target = tgt;
+      sm.token = -1;
+      sm.use_p = use_q ? 0 : 1;
+      sm.ds = ds;
+    }
+  }
+  __syncthreads();
+  // every remote read of this CTA is done: arrive now, wait before leaving
+  // (no CTA may exit while others can still read its shared memory)
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  if (sm.owner == rank) {
+    const bool uq = sm.use_p == 0;
+    const int k = sm.sub * kThreads + tid;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    float qv[VW];
 #pragma unroll
-      for (int jj = 0; jj < kClusterMaxNS; ++jj)
-        if (jj == j) mine = part[jj];
-      F2 total;
-      const F2 ex = block_exclusive_f2(F2{mine, 0.f}, sm.f2red, &total);
-      const F2 tb = f2_add(sm.base, ex);
-      int lastp = -1;
-      if (k < nvec && mine > 0.f && !f2_lt(sm.target, tb) && f2_lt(sm.target, f2_add(tb, F2{mine, 0.f}))) {
-        const int found = smem_slot_walk<T>(Lf, Qf, k * VW, p.c, Mc, inv_s, tb, sm.target, &lastp);
-        if (found >= 0) sm.token = v0 + found;
+    for (int t = 0; t < VW; ++t) qv[t] = 0.f;
+    F2 mine{0.f, 0.f};
+    if (k < nvec) {
+      v = *reinterpret_cast<const uint4*>(Lf + k * VW);
+#pragma unroll
+      for (int t = 0; t < VW; ++t) qv[t] = uq ? Qf[k * VW + t] : 0.f;
+      mine = slot_run<T>(v, qv, VW, uq, M, p.c, p.c_lo, s_a).mass(uq, sm.ds);
+      if (mine.hi < 0.f) mine = F2{0.f, 0.f};
+    }
+    F2 total;
+    const F2 ex = block_exclusive_f2(mine, sm.f2red, &total);
+    const F2 tb = f2_add(sm.base, ex);
+    int lastp = -1;
+    if (k < nvec && f2_pos(mine) && !f2_lt(sm.target, tb) && f2_lt(sm.target, f2_add(tb, mine))) {
+      const int f = slot_find<T>(v, qv, VW, uq, M, p.c, p.c_lo, s_a, sm.ds, tb, sm.target, &lastp);
+      if (f >= 0) sm.token = v0 + k * VW + f;
+    }
+    __syncthreads();
+    if (sm.token < 0) {
+      int m = -1;
+      if (k < nvec) {
+        int lp = -1;
+        slot_find<T>(v, qv, VW, uq, M, p.c, p.c_lo, s_a, sm.ds, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
+        if (lp >= 0) m = v0 + k * VW + lp;
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) sm.st[warp] = m;
+      __syncthreads();
+      if (tid == 0) {
+        int mm = -1;
+        for (int w = 0; w < kWarps; ++w) mm = max(mm, sm.st[w]);
+        sm.token = mm;
       }
       __syncthreads();
-      if (sm.token < 0) {
-        int lp = -1;
-        if (k < nvec) smem_slot_walk<T>(Lf, Qf, k * VW, p.c, Mc, inv_s, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
-        int m = lp >= 0 ? v0 + lp : -1;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) sm.g[warp] = m;
-        __syncthreads();
-        if (tid == 0) {
-          int mm = -1;
-          for (int w = 0; w < kWarps; ++w) mm = max(mm, sm.g[w]);
-          sm.token = mm;
-        }
-        __syncthreads();
-      }
-      token = sm.token < 0 ? 0 : sm.token;
-      if (tid == 0) {
-        p.out_tokens[b * G1 + n] = token;
-        if (p.out_status) p.out_status[b] = status;
-      }
-    } else if (sm.owner < 0 && rank == 0 && tid == 0) {
-      p.out_tokens[b * G1 + n] = 0;
+    }
+    if (tid == 0) {
+      p.out_tokens[b * G1 + n] = sm.token < 0 ? 0 : sm.token;
       if (p.out_status) p.out_status[b] = status;
     }
-    break;
+  } else if (sm.owner < 0 && rank == 0 && tid == 0) {
+    p.out_tokens[b * G1 + n] = 0;
+    if (p.out_status) p.out_status[b] = status;
   }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace sv

@@ -65,7 +65,8 @@ struct Params {
   int C, CL, EPT;        // residual kernel: chunks per row, chunk length, elements per thread
   int top_k;             // top-k list length (top-k mode)
   float top_p;
-  float c;               // log2(e) / temperature
+  float c;               // log2(e) / temperature (rounded to float)
+  float c_lo;            // log2(e) / temperature - c
   const void* logits;
   const float* q;
   const int32_t* draft;
@@ -250,6 +251,46 @@ __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
   float h = s + e;
   return F2{h, e - (h - s)};
 }
+// Two-float (Dekker) products and a two-float exp2, for the one row per
+// sequence whose inverse CDF must agree with a float64 reference to ~1e-10.
+__device__ __forceinline__ F2 f2_norm(float s, float e) {
+  const float h = s + e;
+  return F2{h, e - (h - s)};
+}
+// a * b, both two-float
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return f2_norm(p, e);
+}
+__device__ __forceinline__ F2 f2_neg(F2 a) { return F2{-a.hi, -a.lo}; }
+
+// 2^a for a two-float a <= 0: a = n + f with n = rint(a.hi), |f| <= 1/2; 2^f =
+// e^(f ln 2) summed by its Taylor series to degree 11 (remainder < 7e-15 for
+// |f ln 2| <= 0.35) in two-float Horner form; then an exact scaling by 2^n.
+// ln 2 and 1/k! are given as float pairs (hi + lo) taken from their exact
+// values.
+__device__ __forceinline__ F2 exp2_f2(F2 a) {
+  const F2 kLn2{6.931471825e-01f, -1.904654212e-09f};
+  const float kInvFactHi[12] = {1.000000000e+00f, 1.000000000e+00f, 5.000000000e-01f, 1.666666716e-01f,
+                                4.166666791e-02f, 8.333333768e-03f, 1.388888923e-03f, 1.984127011e-04f,
+                                2.480158764e-05f, 2.755731884e-06f, 2.755731998e-07f, 2.505210794e-08f};
+  const float kInvFactLo[12] = {0.0f, 0.0f, 0.0f, -4.967053879e-09f, -1.241763470e-09f, -4.346172033e-10f,
+                                -3.363109444e-11f, -2.725596875e-12f, -3.406996094e-13f, 3.793571224e-14f,
+                                -7.575112209e-15f, 4.417623045e-16f};
+  if (a.hi < -125.f) return F2{0.f, 0.f};
+  const float n = rintf(a.hi);
+  const F2 f = f2_norm(a.hi - n, a.lo);      // a.hi - n is exact
+  const F2 g = f2_mul(f, kLn2);
+  F2 r{kInvFactHi[11], kInvFactLo[11]};
+#pragma unroll
+  for (int k = 10; k >= 0; --k) r = f2_add(f2_mul(r, g), F2{kInvFactHi[k], kInvFactLo[k]});
+  const int ni = (int)n;
+  return F2{ldexpf(r.hi, ni), ldexpf(r.lo, ni)};
+}
+
 // Ordering of normalised two-float numbers (|lo| <= ulp(hi) / 2, as f2_add
 // returns them).
 __device__ __forceinline__ bool f2_lt(F2 a, F2 b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
@@ -430,6 +471,74 @@ __device__ int block_locate(const F2* masses, int NT, float u, F2* R_out, F2* ba
   if (ls.found != 0x7fffffff) { *base_out = ls.base; return ls.found; }
   *base_out = ls.lastbase;
   return ls.last;
+}
+
+// The same search done by warp 0 alone (no block barriers during the scan;
+// one __syncthreads publishes the result).  Same summation order for the
+// total and the prefixes: 32-wide chunks, two-float inclusive scans, carry.
+__device__ int warp_locate(const F2* masses, int NT, float u, F2* R_out, F2* base_out, F2* t_out,
+                           LocateSmem& ls, bool from_global) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int lane = tid;
+    auto load = [&](int k) -> F2 {
+      if (k >= NT) return F2{0.f, 0.f};
+      if (from_global) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(masses) + k);
+        return F2{v.x, v.y};
+      }
+      return masses[k];
+    };
+    F2 carry{0.f, 0.f};
+    for (int c0 = 0; c0 < NT; c0 += 32) {
+      const F2 inc = f2_add(carry, warp_incl_scan_f2(load(c0 + lane)));
+      carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+    }
+    const F2 R = carry;
+    const F2 t = f2_scale(R, u);
+    int found = -1, last = -1;
+    F2 fbase{0.f, 0.f}, lbase{0.f, 0.f};
+    carry = F2{0.f, 0.f};
+    for (int c0 = 0; c0 < NT && found < 0; c0 += 32) {
+      const F2 m = load(c0 + lane);
+      const F2 inc = f2_add(carry, warp_incl_scan_f2(m));
+      F2 excl = F2{__shfl_up_sync(0xffffffffu, inc.hi, 1), __shfl_up_sync(0xffffffffu, inc.lo, 1)};
+      if (lane == 0) excl = carry;
+      const bool live = c0 + lane < NT && f2_pos(m);
+      const unsigned hit = __ballot_sync(0xffffffffu, live && !f2_lt(t, excl) && f2_lt(t, f2_add(excl, m)));
+      const unsigned pos = __ballot_sync(0xffffffffu, live);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        found = c0 + l;
+        fbase = F2{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
+      }
+      if (pos) {
+        const int l = 31 - __clz(pos);
+        last = c0 + l;
+        lbase = F2{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
+      }
+      carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+    }
+    if (lane == 0) {
+      ls.carry = R;
+      ls.wsum[0] = t;
+      ls.found = found >= 0 ? found : last;
+      ls.base = found >= 0 ? fbase : lbase;
+    }
+  }
+  __syncthreads();
+  *R_out = ls.carry;
+  *t_out = ls.wsum[0];
+  *base_out = ls.base;
+  const int k = f2_pos(ls.carry) ? ls.found : -1;
+  __syncthreads();   // ls may be reused right after
+  return k;
+}
+
+__device__ __forceinline__ int locate(const F2* masses, int NT, float u, F2* R_out, F2* base_out, F2* t_out,
+                                      LocateSmem& ls, bool from_global) {
+  return NT <= 1024 ? warp_locate(masses, NT, u, R_out, base_out, t_out, ls, from_global)
+                    : block_locate(masses, NT, u, R_out, base_out, t_out, ls, from_global);
 }
 
 // "Does (va, ia) beat (vb, ib)?" for the greedy argmax: a larger value wins,
@@ -1047,28 +1156,126 @@ rows_kernel(const Params p) {
   finish_sequence_topk(p, b, sm);
 }
 
+// Weight 2^((x - M) c) of one token of the final-draw row, c = log2(e) / T
+// given as (c, c_lo).  The exponent is formed in two-float (x - M exactly,
+// times c + c_lo).  Tokens within 2^-8 of the row maximum ("top" tokens carry
+// most of the mass, so their rounding would shift every later CDF step) get
+// the two-float exp2 in *wt and the function returns true; the rest get
+// exp2f with a first-order correction for the exponent's low part in *wf.
+// -inf logits weigh 0; NaN propagates (such rows are flagged, not drawn).
+__device__ __forceinline__ bool tok_weight(float x, float M, float c, float c_lo, F2* wt, float* wf) {
+  if (x == -INFINITY) {
+    *wf = 0.f;
+    return false;
+  }
+  const float dh = x - M;
+  const float bb = dh - x;
+  const float dl = (x - (dh - bb)) + (-M - bb);   // x - M = dh + dl exactly
+  const float p = dh * c;
+  float e = fmaf(dh, c, -p);
+  e = fmaf(dh, c_lo, e);
+  e = fmaf(dl, c, e);
+  if (p > -8.f) {
+    *wt = exp2_f2(f2_norm(p, e));
+    return true;
+  }
+  const float y = exp2f(p);
+  *wf = fmaf(y * 6.931471825e-01f, e, y);
+  return false;
+}
+
+// Running sums of one thread over one slot of the final-draw row, in token
+// order.  S: all weights; A: the residual max(w - s' q, 0) over the support
+// {w > s' q} with the row-statistics kernel's float normaliser s'; Q: q over
+// the same support.  Top tokens add in two-float, the others in float.  The
+// exact residual mass is A - (s - s') Q once the exact normaliser s is known.
+struct SlotRun {
+  F2 s_top, a_top;
+  float s_tail, a_tail, q;
+  __device__ __forceinline__ void zero() {
+    s_top = a_top = F2{0.f, 0.f};
+    s_tail = a_tail = q = 0.f;
+  }
+  __device__ __forceinline__ void add(float x, float qv, bool use_q, float M, float c, float c_lo, float s_a) {
+    F2 wt;
+    float wf;
+    if (tok_weight(x, M, c, c_lo, &wt, &wf)) {
+      s_top = f2_add(s_top, wt);
+      if (use_q && wt.hi > s_a * qv) {
+        const float pr = s_a * qv;
+        const F2 sq = f2_norm(pr, fmaf(s_a, qv, -pr));
+        a_top = f2_add(a_top, f2_add(wt, f2_neg(sq)));
+        q += qv;
+      }
+    } else {
+      s_tail += wf;
+      if (use_q && wf > s_a * qv) {
+        a_tail += fmaf(-s_a, qv, wf);
+        q += qv;
+      }
+    }
+  }
+  __device__ __forceinline__ F2 S() const { return f2_add(s_top, F2{s_tail, 0.f}); }
+  __device__ __forceinline__ F2 A() const { return f2_add(a_top, F2{a_tail, 0.f}); }
+  // the value the inverse CDF walks: S (bonus / fallback to p) or A - ds Q
+  __device__ __forceinline__ F2 mass(bool resid, F2 ds) const {
+    return resid ? f2_add(A(), f2_neg(f2_scale(ds, q))) : S();
+  }
+};
+
+// Three two-float block sums in one pass (one pair of barriers).
+struct F2x3 {
+  F2 a, b, c;
+};
+__device__ __forceinline__ F2x3 block_sum_f2x3(F2x3 v, F2x3* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    v.a = f2_add(v.a, f2_shfl_xor(v.a, m));
+    v.b = f2_add(v.b, f2_shfl_xor(v.b, m));
+    v.c = f2_add(v.c, f2_shfl_xor(v.c, m));
+  }
+  __syncthreads();
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  F2x3 t = sm[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+    t.a = f2_add(t.a, sm[w].a);
+    t.b = f2_add(t.b, sm[w].b);
+    t.c = f2_add(t.c, sm[w].c);
+  }
+  return t;
+}
+
 // ------------------------------------------------------------------ residual kernel
 //
 // Element order.  A chunk of CL = 256 * EPT elements is read as NS = EPT / VW
 // "slots": slot j of thread t holds elements c0 + (j*256 + t)*VW + [0, VW), so
 // each warp-wide 16-byte load is coalesced.  Slot j of all threads is one
 // contiguous sub-range of the vocabulary, and the sub-ranges (chunk c, slot j)
-// follow the token index in (c, j) order.  The inverse-CDF search therefore
-// goes sub-range -> thread -> element, and every level sums exactly the same
-// float32 slot partials that the mass pass summed.
+// follow the token index in (c, j) order.  The inverse-CDF search goes
+// sub-range -> thread -> element.
+//
+// Precision.  This is the one row per sequence whose inverse CDF is compared
+// step by step with a float64 reference over up to ~10^5 steps, so token
+// weights come from tok_weight() (two-float exponent; two-float exp2 for the
+// tokens that carry the mass) and the running sums keep those in two-float
+// (SlotRun).  The residual max(p - q, 0) = max(w - s q, 0) / s is kept
+// unnormalised (the inverse CDF does not change under scaling).  Each
+// sub-range reports (S, A, Q) - the sum of its weights, and over its residual
+// support {w > s' q} (s' the row-statistics kernel's float normaliser) the sum
+// of w - s' q and of q.  The finisher forms the exact normaliser s = sum S and
+// the masses A - (s - s') Q: no second pass, and no cancellation, since
+// s - s' is tiny.  Tokens whose support membership s' and s would decide
+// differently have |w - s q| < 1e-6 w and contribute nothing measurable.
 
-// Sum over one slot (VW elements from e0, the first nv real) of
-//   r(v) = max(p(v) - q(v), 0)  (q != nullptr)   or   p(v)  (bonus),
-// p(v) = 2^((L_v - M) c) / s, in index order with explicit rounding steps so
-// that the search recomputes the same float32 value bit for bit.
+// One slot of the final-draw row from global memory: VW logits and (for a
+// residual) the VW q values.
 template <typename T>
-__device__ __forceinline__ float slot_mass(const T* row, const float* qrow, int e0, int nv, float c, float Mc,
-                                           float inv_s, bool vec_ok) {
-  using TR = Tr<T>;
-  constexpr int VW = TR::VW;
-  if (nv <= 0) return 0.f;
-  const uint4 v = load_slot<T>(row, e0, nv, vec_ok);
-  float qv[VW];
+__device__ __forceinline__ void load_final_slot(const T* row, const float* qrow, int e0, int nv, bool vec_ok,
+                                                uint4* v, float* qv) {
+  constexpr int VW = Tr<T>::VW;
+  *v = load_slot<T>(row, e0, nv, vec_ok);
   if (qrow) {
     if (nv == VW && vec_ok) {
 #pragma unroll
@@ -1080,48 +1287,61 @@ __device__ __forceinline__ float slot_mass(const T* row, const float* qrow, int 
 #pragma unroll
       for (int t = 0; t < VW; ++t) qv[t] = t < nv ? __ldg(qrow + e0 + t) : 0.f;
     }
+  } else {
+#pragma unroll
+    for (int t = 0; t < VW; ++t) qv[t] = 0.f;
   }
-  float acc = 0.f;
+}
+
+// Running sums over the first nv tokens of one loaded slot.
+template <typename T>
+__device__ __forceinline__ SlotRun slot_run(const uint4& v, const float* qv, int nv, bool use_q, float M, float c,
+                                            float c_lo, float s_a) {
+  constexpr int VW = Tr<T>::VW;
+  SlotRun r;
+  r.zero();
+#pragma unroll
+  for (int t = 0; t < VW; ++t)
+    if (t < nv) r.add(Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a);
+  return r;
+}
+
+// The same running sums, stopping at the first token where base + the walked
+// value exceeds target (returns its offset in the slot, or -1); *last is the
+// last token with a positive increment.
+template <typename T>
+__device__ __forceinline__ int slot_find(const uint4& v, const float* qv, int nv, bool use_q, float M, float c,
+                                         float c_lo, float s_a, F2 ds, F2 base, F2 target, int* last) {
+  constexpr int VW = Tr<T>::VW;
+  SlotRun r;
+  r.zero();
+  F2 prev{0.f, 0.f};
+  int found = -1, lastp = -1;
 #pragma unroll
   for (int t = 0; t < VW; ++t) {
     if (t < nv) {
-      const float pv = __fmul_rn(ex2_approx(fmaf(TR::get(v, t), c, -Mc)), inv_s);
-      acc = __fadd_rn(acc, qrow ? fmaxf(__fsub_rn(pv, qv[t]), 0.f) : pv);
+      r.add(Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a);
+      const F2 cur = r.mass(use_q, ds);
+      if (f2_lt(prev, cur)) lastp = t;
+      if (found < 0 && f2_lt(target, f2_add(base, cur))) found = t;
+      prev = cur;
     }
   }
-  return acc;
-}
-
-// Walk one slot: the element at which base + (running float32 sum) first
-// exceeds target, or -1; *last_pos = the last element with a positive weight.
-template <typename T>
-__device__ __forceinline__ int slot_walk(const T* row, const float* qrow, int e0, int nv, float c, float Mc,
-                                         float inv_s, bool vec_ok, F2 base, F2 target, int* last_pos) {
-  using TR = Tr<T>;
-  int found = -1, lastp = -1;
-  if (nv > 0) {
-    const uint4 v = load_slot<T>(row, e0, nv, vec_ok);
-    float acc = 0.f;
-    for (int t = 0; t < nv; ++t) {
-      const float pv = __fmul_rn(ex2_approx(fmaf(TR::get(v, t), c, -Mc)), inv_s);
-      const float rv = qrow ? fmaxf(__fsub_rn(pv, __ldg(qrow + e0 + t)), 0.f) : pv;
-      acc = __fadd_rn(acc, rv);
-      if (rv > 0.f) lastp = e0 + t;
-      if (found < 0 && f2_lt(target, f2_add(base, F2{acc, 0.f}))) found = e0 + t;
-    }
-  }
-  *last_pos = lastp;
+  *last = lastp;
   return found;
 }
 
 struct ResSmem {
+  F2x3 red[kWarps];
   F2 f2red[kWarps];
   int ired[kWarps];
   int flag;
   int sub;        // selected sub-range (chunk * NS + slot), -1 if none
   int token;
+  int use_q;
   F2 target;
   F2 base;
+  F2 ds;
   LocateSmem loc;
 };
 
@@ -1149,79 +1369,116 @@ residual_kernel(const Params p) {
   const bool bad = (st.status & SEQ_BADROW) != 0;
   const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
   const float* qrow = resid ? p.q + ((size_t)b * G + n) * V : nullptr;
-  const float Mc = st.M * p.c;
-  const float inv_s = 1.0f / (float)st.s;
+  const float M = st.M;
+  const float s_a = (float)st.s;
   const bool vec_ok = (V % VW) == 0;
-  float2* cm = p.chunk_mass + (size_t)b * NT;
+  // per sequence: [S block | A block | Q block], NT two-float entries each
+  F2* cS = reinterpret_cast<F2*>(p.chunk_mass) + (size_t)b * 3 * NT;
+  F2* cA = cS + NT;
+  F2* cQ = cA + NT;
 
-  // ---- masses of this chunk's NS sub-ranges
+  // ---- (S, A, Q) of this chunk's NS sub-ranges
   const int c0 = c * p.CL;
-  float part[kMaxNS];
+  SlotRun part[kMaxNS];
 #pragma unroll
   for (int j = 0; j < kMaxNS; ++j) {
-    part[j] = 0.f;
+    part[j].zero();
     if (j < NS && !bad) {
       const int e0 = c0 + (j * kThreads + tid) * VW;
-      part[j] = slot_mass<T>(row, qrow, e0, min(max(V - e0, 0), VW), p.c, Mc, inv_s, vec_ok);
+      const int nv = min(max(V - e0, 0), VW);
+      if (nv > 0) {
+        uint4 v;
+        float qv[VW];
+        load_final_slot<T>(row, qrow, e0, nv, vec_ok, &v, qv);
+        part[j] = slot_run<T>(v, qv, nv, resid, M, p.c, p.c_lo, s_a);
+      }
     }
   }
 #pragma unroll
   for (int j = 0; j < kMaxNS; ++j) {
     if (j < NS) {
-      const F2 tot = block_sum_f2(F2{part[j], 0.f}, sm.f2red);
-      if (tid == 0) cm[c * NS + j] = make_float2(tot.hi, tot.lo);
+      const F2x3 t = block_sum_f2x3(F2x3{part[j].S(), part[j].A(), F2{part[j].q, 0.f}}, sm.red);
+      if (tid == 0) {
+        cS[c * NS + j] = t.a;
+        cA[c * NS + j] = t.b;
+        cQ[c * NS + j] = t.c;
+      }
     }
   }
   if (!arrive_last(p.seq_ticket2 + b, p.C, &sm.flag, true)) return;
 
-  // ---- last CTA of sequence b: locate the inverse-CDF step
+  // ---- last CTA of sequence b: exact normaliser, masses, inverse-CDF step
   int status = st.status;
-  const float u = __ldg(p.uniforms + b * G1 + G);
-  F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
-  const F2* cmf = reinterpret_cast<const F2*>(cm);
-  int sub = block_locate(cmf, NT, u, &R, &base, &tgt, sm.loc, true);
-  const float* qsel = qrow;
-  if (resid && !bad && !f2_pos(R)) {
-    // zero residual mass (only through rounding): draw from p_n instead
-    status |= SEQ_RESID0;
-    qsel = nullptr;
-    for (int k2 = 0; k2 < NT; ++k2) {
-      const int e0 = (k2 / NS) * p.CL + ((k2 % NS) * kThreads + tid) * VW;
-      const float m2 = slot_mass<T>(row, nullptr, e0, min(max(V - e0, 0), VW), p.c, Mc, inv_s, vec_ok);
-      const F2 tot = block_sum_f2(F2{m2, 0.f}, sm.f2red);
-      if (tid == 0) cm[k2] = make_float2(tot.hi, tot.lo);
+  F2 sl{0.f, 0.f};
+  for (int k2 = tid; k2 < NT; k2 += kThreads) {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(cS) + k2);
+    sl = f2_add(sl, F2{v.x, v.y});
+  }
+  const F2 s = block_sum_f2(sl, sm.f2red);
+  const F2 ds = f2_add(s, F2{-s_a, 0.f});          // s - s', tiny
+  if (resid) {
+    // residual masses A - (s - s') Q overwrite the A block
+    for (int k2 = tid; k2 < NT; k2 += kThreads) {
+      const float2 a2 = __ldcg(reinterpret_cast<const float2*>(cA) + k2);
+      const float2 q2 = __ldcg(reinterpret_cast<const float2*>(cQ) + k2);
+      F2 m = f2_add(F2{a2.x, a2.y}, f2_neg(f2_mul(ds, F2{q2.x, q2.y})));
+      if (m.hi < 0.f) m = F2{0.f, 0.f};
+      cA[k2] = m;
     }
     __threadfence_block();
     __syncthreads();
-    sub = block_locate(cmf, NT, u, &R, &base, &tgt, sm.loc, true);
+  }
+  const float u = __ldg(p.uniforms + b * G1 + G);
+  F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
+  bool use_q = resid;
+  int sub = locate(resid ? cA : cS, NT, u, &R, &base, &tgt, sm.loc, true);
+  if (resid && !bad && !f2_pos(R)) {
+    // zero residual mass (only through rounding): draw from p_n instead
+    status |= SEQ_RESID0;
+    use_q = false;
+    sub = locate(cS, NT, u, &R, &base, &tgt, sm.loc, true);
   }
   if (tid == 0) {
     sm.sub = (bad || !f2_pos(R)) ? -1 : sub;
     sm.base = base;
     sm.target = tgt;
     sm.token = -1;
+    sm.use_q = use_q;
+    sm.ds = ds;
   }
   __syncthreads();
   int token = 0;
   if (sm.sub >= 0) {
+    const bool uq = sm.use_q != 0;
     const int e0 = (sm.sub / NS) * p.CL + ((sm.sub % NS) * kThreads + tid) * VW;
     const int nv = min(max(V - e0, 0), VW);
-    const float m2 = slot_mass<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    float qv[VW];
+#pragma unroll
+    for (int t = 0; t < VW; ++t) qv[t] = 0.f;
+    F2 mine{0.f, 0.f};
+    if (nv > 0) {
+      load_final_slot<T>(row, uq ? qrow : nullptr, e0, nv, vec_ok, &v, qv);
+      mine = slot_run<T>(v, qv, nv, uq, M, p.c, p.c_lo, s_a).mass(uq, sm.ds);
+      if (mine.hi < 0.f) mine = F2{0.f, 0.f};
+    }
     F2 total;
-    const F2 ex = block_exclusive_f2(F2{m2, 0.f}, sm.f2red, &total);
+    const F2 ex = block_exclusive_f2(mine, sm.f2red, &total);
     const F2 tbase = f2_add(sm.base, ex);
-    const F2 target = sm.target;
     int lastp = -1;
-    if (m2 > 0.f && !f2_lt(target, tbase) && f2_lt(target, f2_add(tbase, F2{m2, 0.f}))) {
-      const int found = slot_walk<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok, tbase, target, &lastp);
-      if (found >= 0) sm.token = found;
+    if (nv > 0 && f2_pos(mine) && !f2_lt(sm.target, tbase) && f2_lt(sm.target, f2_add(tbase, mine))) {
+      const int f = slot_find<T>(v, qv, nv, uq, M, p.c, p.c_lo, s_a, sm.ds, tbase, sm.target, &lastp);
+      if (f >= 0) sm.token = e0 + f;
     }
     __syncthreads();
     if (sm.token < 0) {
       // rounding left no step above the target: take the last positive weight
-      int lp = -1;
-      slot_walk<T>(row, qsel, e0, nv, p.c, Mc, inv_s, vec_ok, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
-      int m = lp;
+      int m = -1;
+      if (nv > 0) {
+        int lp = -1;
+        slot_find<T>(v, qv, nv, uq, M, p.c, p.c_lo, s_a, sm.ds, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
+        if (lp >= 0) m = e0 + lp;
+      }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       if ((tid & 31) == 0) sm.ired[tid >> 5] = m;
@@ -1235,7 +1492,7 @@ residual_kernel(const Params p) {
     }
     token = sm.token < 0 ? 0 : sm.token;
   }
-  for (int k2 = tid; k2 < NT; k2 += kThreads) cm[k2] = make_float2(0.f, 0.f);
+  for (int k2 = tid; k2 < 3 * NT; k2 += kThreads) cS[k2] = F2{0.f, 0.f};
   if (tid == 0) {
     p.out_tokens[b * G1 + n] = token;
     if (p.out_status) p.out_status[b] = status;

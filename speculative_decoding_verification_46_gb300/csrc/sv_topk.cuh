@@ -112,11 +112,11 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   __syncthreads();
   const float u = sm.fu[G];
   F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
-  int pos = block_locate(rs, J, u, &R, &base, &tgt, sm.loc, false);
+  int pos = locate(rs, J, u, &R, &base, &tgt, sm.loc, false);
   int status = sm.status;
   if (resid && !f2_pos(R)) {
     status |= SEQ_RESID0;   // zero residual mass (rounding only): draw from p_n
-    pos = block_locate(ps, J, u, &R, &base, &tgt, sm.loc, false);
+    pos = locate(ps, J, u, &R, &base, &tgt, sm.loc, false);
   }
   if (tid == 0) {
     int tok = pos >= 0 ? sm.sidx[pos] : (J > 0 ? sm.sidx[0] : 0);
