@@ -178,6 +178,15 @@ sv_status sv_verify_greedy_noalloc(int B, int gamma, int V,
 const char* sv_status_string(sv_status s);
 
 /*
+ * Names of the kernels the last sv_verify_sample / sv_verify_greedy call made
+ * on this host thread launched, comma-separated in launch order (for example
+ * "cluster_kernel" or "stream_dense_kernel,residual_kernel"); "" before the
+ * first call, after a call that launched nothing (B = 0, an argument error)
+ * or a launch failure.  Static storage owned by the library; thread-local.
+ */
+const char* sv_last_kernels(void);
+
+/*
  * Measurement hook (outside the verify computation; used by the benchmark to
  * time each kernel with CUDA events).  Registers n = 3 caller-created CUDA
  * events (cudaEvent_t handles cast to void*) that every later call records on

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     SvError,
     alloc_workspace,
     load_library,
+    sv_last_kernels,
     sv_set_timing_events,
     sv_status_string,
     sv_verify_greedy,

@@ -71,6 +71,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sv_verify_greedy_noalloc.restype = _c_int
     lib.sv_set_timing_events.argtypes = [ctypes.POINTER(_c_ptr), _c_int]
     lib.sv_set_timing_events.restype = _c_int
+    lib.sv_last_kernels.argtypes = []
+    lib.sv_last_kernels.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -106,6 +108,12 @@ def sv_verify_greedy_noalloc(B, gamma, V, logits, logits_dtype, draft_tokens, ou
     callers that cannot allocate device memory; see include/specverify.h."""
     return int(load_library().sv_verify_greedy_noalloc(B, gamma, V, logits, logits_dtype, draft_tokens, out_tokens,
                                                        out_num_accepted, out_status, stream))
+
+
+def sv_last_kernels() -> list:
+    """Kernels launched by the last verify call on this thread, in order."""
+    names = load_library().sv_last_kernels().decode()
+    return names.split(",") if names else []
 
 
 def sv_set_timing_events(events) -> int:

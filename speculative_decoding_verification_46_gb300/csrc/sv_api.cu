@@ -275,10 +275,14 @@ sv_status launch_stream_dense(const sv::Params& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+// Kernels launched by the last call on this host thread (sv_last_kernels).
+thread_local const char* g_last_kernels = "";
+
 template <typename T>
 sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
   sv::ClusterParams cp;
   size_t smem = 0;
+  g_last_kernels = "";
   if (plan_cluster(p, dt, mode, &cp, &smem)) {
     bool launched = false;
     timing_record(0, stream);
@@ -286,6 +290,7 @@ sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype 
                                                  : launch_cluster<T, sv::MODE_SOFTMAX>(cp, smem, stream, &launched);
     if (st != SV_OK) return st;
     if (launched) {
+      g_last_kernels = "cluster_kernel";
       timing_record(1, stream);
       timing_record(2, stream);
       return SV_OK;
@@ -294,13 +299,20 @@ sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype 
   timing_record(0, stream);
   sv_status st = SV_OK;
   const bool streamable = p.V % vec_width(dt) == 0 && path_override() != 3;
-  if (mode == sv::MODE_GREEDY)
+  if (mode == sv::MODE_GREEDY) {
     st = streamable ? launch_stream_dense<T, sv::MODE_GREEDY>(p, stream) : launch_rows<T, sv::MODE_GREEDY>(p, stream);
-  else if (mode == sv::MODE_TOPK)
+    g_last_kernels = streamable ? "stream_dense_kernel" : "rows_kernel";
+  } else if (mode == sv::MODE_TOPK) {
     st = streamable ? launch_stream_topk<T>(p, stream) : launch_rows<T, sv::MODE_TOPK>(p, stream);
-  else
+    g_last_kernels = streamable ? "stream_topk_kernel" : "rows_kernel";
+  } else {
     st = streamable ? launch_stream_dense<T, sv::MODE_SOFTMAX>(p, stream) : launch_rows<T, sv::MODE_SOFTMAX>(p, stream);
-  if (st != SV_OK) return st;
+    g_last_kernels = streamable ? "stream_dense_kernel,residual_kernel" : "rows_kernel,residual_kernel";
+  }
+  if (st != SV_OK) {
+    g_last_kernels = "";
+    return st;
+  }
   timing_record(1, stream);
   if (mode == sv::MODE_SOFTMAX) st = launch_residual<T>(p, stream);
   timing_record(2, stream);
@@ -334,6 +346,7 @@ extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logit
                                       float temperature, int top_k, float top_p, int32_t* out_tokens,
                                       int32_t* out_num_accepted, float* out_accept_prob, int32_t* out_status,
                                       void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  g_last_kernels = "";
   if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
   if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
     return SV_ERR_INVALID_ARG;
@@ -382,6 +395,7 @@ extern "C" sv_status sv_verify_greedy(int B, int gamma, int V, const void* logit
                                       const int32_t* draft_tokens, int32_t* out_tokens, int32_t* out_num_accepted,
                                       int32_t* out_status, void* workspace, size_t workspace_bytes,
                                       sv_stream_t stream) {
+  g_last_kernels = "";
   if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
   if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
     return SV_ERR_INVALID_ARG;
@@ -415,6 +429,8 @@ extern "C" const char* sv_status_string(sv_status s) {
   }
   return "unknown sv_status";
 }
+
+extern "C" const char* sv_last_kernels(void) { return g_last_kernels; }
 
 extern "C" sv_status sv_set_timing_events(void* const* events, int n) {
   if (n == 0) {

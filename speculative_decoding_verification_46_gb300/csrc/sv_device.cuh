@@ -35,6 +35,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace sv {
 
 constexpr int kThreads = 256;
@@ -267,28 +269,64 @@ __device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
 }
 __device__ __forceinline__ F2 f2_neg(F2 a) { return F2{-a.hi, -a.lo}; }
 
-// 2^a for a two-float a <= 0: a = n + f with n = rint(a.hi), |f| <= 1/2; 2^f =
-// e^(f ln 2) summed by its Taylor series to degree 11 (remainder < 7e-15 for
-// |f ln 2| <= 0.35) in two-float Horner form; then an exact scaling by 2^n.
-// ln 2 and 1/k! are given as float pairs (hi + lo) taken from their exact
-// values.
-__device__ __forceinline__ F2 exp2_f2(F2 a) {
+// 2^(j/64), j = 0..63, as float pairs (hi + lo) rounded from the exact values.
+__device__ const float kExp2Hi[64] = {
+    1.000000000e+00f, 1.010889292e+00f, 1.021897197e+00f, 1.033024907e+00f,
+    1.044273734e+00f, 1.055645227e+00f, 1.067140460e+00f, 1.078760743e+00f,
+    1.090507746e+00f, 1.102382541e+00f, 1.114386797e+00f, 1.126521587e+00f,
+    1.138788581e+00f, 1.151189208e+00f, 1.163724899e+00f, 1.176396966e+00f,
+    1.189207077e+00f, 1.202156782e+00f, 1.215247393e+00f, 1.228480577e+00f,
+    1.241857767e+00f, 1.255380750e+00f, 1.269050956e+00f, 1.282870054e+00f,
+    1.296839595e+00f, 1.310961246e+00f, 1.325236678e+00f, 1.339667559e+00f,
+    1.354255557e+00f, 1.369002461e+00f, 1.383909941e+00f, 1.398979664e+00f,
+    1.414213538e+00f, 1.429613352e+00f, 1.445180774e+00f, 1.460917830e+00f,
+    1.476826191e+00f, 1.492907763e+00f, 1.509164453e+00f, 1.525598168e+00f,
+    1.542210817e+00f, 1.559004426e+00f, 1.575980902e+00f, 1.593142152e+00f,
+    1.610490322e+00f, 1.628027439e+00f, 1.645755529e+00f, 1.663676620e+00f,
+    1.681792855e+00f, 1.700106382e+00f, 1.718619347e+00f, 1.737333894e+00f,
+    1.756252170e+00f, 1.775376439e+00f, 1.794709086e+00f, 1.814252138e+00f,
+    1.834008098e+00f, 1.853979111e+00f, 1.874167681e+00f, 1.894575953e+00f,
+    1.915206552e+00f, 1.936061740e+00f, 1.957144141e+00f, 1.978456020e+00f,
+};
+__device__ const float kExp2Lo[64] = {
+    0.000000000e+00f, -5.711605411e-09f, -4.811559862e-08f, -2.809089317e-08f,
+    4.833470157e-08f, -4.907169426e-08f, -5.933751979e-08f, 5.461594554e-08f,
+    -1.307753994e-08f, 4.260501996e-08f, -5.435540018e-08f, 3.123641434e-08f,
+    5.386222313e-08f, 2.192228266e-08f, -4.051441493e-08f, 2.566975077e-08f,
+    3.797635273e-08f, -5.069756526e-08f, -3.267394888e-08f, -4.136200360e-08f,
+    4.496838102e-08f, 7.322237483e-09f, 1.419333318e-09f, -3.816621685e-08f,
+    -4.018999533e-08f, -3.496571566e-08f, -3.496373324e-08f, -3.461673970e-08f,
+    -1.012334927e-08f, -3.845881835e-08f, -5.875577358e-08f, 8.689434061e-09f,
+    2.420323497e-08f, -1.342992917e-08f, 3.324199938e-08f, -3.628657552e-08f,
+    -4.500898854e-08f, -3.423620143e-08f, -2.495937323e-08f, -1.762856883e-08f,
+    8.070904833e-09f, -2.576466507e-08f, -5.661025426e-08f, -4.903136785e-10f,
+    9.836217174e-09f, -1.726008314e-08f, -5.124972091e-08f, -3.920298752e-08f,
+    -2.475532668e-08f, -2.865147231e-08f, -4.849617596e-08f, -5.850223417e-08f,
+    -9.235770371e-09f, 5.343197884e-08f, -1.141504491e-08f, 3.736258236e-08f,
+    -1.123927795e-08f, 1.436561181e-08f, -4.663005626e-08f, 2.810338451e-08f,
+    9.845328108e-09f, 5.357072297e-08f, -1.702180441e-08f, 6.032726318e-09f,
+};
+
+// 2^a for a two-float a (a <= 0): a = n + j/64 + r with |r| <= 1/128, so
+// 2^a = 2^n * 2^(j/64) * e^g with g = r ln 2, |g| <= 0.0055, and
+// e^g = 1 + g + (g^2/2 + g^3/6 + g^4/24) to ~4e-14 (the bracket, below 1.6e-5,
+// is evaluated in float).  ln 2 is a float pair from its exact value.  Out of
+// line: it runs only for the few tokens that carry most of a row's mass.
+__device__ __noinline__ F2 exp2_f2(F2 a) {
   const F2 kLn2{6.931471825e-01f, -1.904654212e-09f};
-  const float kInvFactHi[12] = {1.000000000e+00f, 1.000000000e+00f, 5.000000000e-01f, 1.666666716e-01f,
-                                4.166666791e-02f, 8.333333768e-03f, 1.388888923e-03f, 1.984127011e-04f,
-                                2.480158764e-05f, 2.755731884e-06f, 2.755731998e-07f, 2.505210794e-08f};
-  const float kInvFactLo[12] = {0.0f, 0.0f, 0.0f, -4.967053879e-09f, -1.241763470e-09f, -4.346172033e-10f,
-                                -3.363109444e-11f, -2.725596875e-12f, -3.406996094e-13f, 3.793571224e-14f,
-                                -7.575112209e-15f, 4.417623045e-16f};
   if (a.hi < -125.f) return F2{0.f, 0.f};
-  const float n = rintf(a.hi);
-  const F2 f = f2_norm(a.hi - n, a.lo);      // a.hi - n is exact
-  const F2 g = f2_mul(f, kLn2);
-  F2 r{kInvFactHi[11], kInvFactLo[11]};
-#pragma unroll
-  for (int k = 10; k >= 0; --k) r = f2_add(f2_mul(r, g), F2{kInvFactHi[k], kInvFactLo[k]});
-  const int ni = (int)n;
-  return F2{ldexpf(r.hi, ni), ldexpf(r.lo, ni)};
+  const float k = rintf(a.hi * 64.f);            // a.hi * 64 is exact
+  const F2 r = f2_norm(a.hi - k * 0.015625f, a.lo);  // a.hi - k/64 is exact
+  const F2 g = f2_mul(r, kLn2);
+  const float gh = g.hi;
+  const float small = gh * gh * fmaf(gh, fmaf(gh, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f);
+  const F2 e = f2_add(f2_add(F2{1.f, 0.f}, g), F2{small, 0.f});
+  const int ki = (int)k;
+  const int j = ki & 63;
+  const int n = ki >> 6;                          // floor(k / 64)
+  const F2 t{__ldg(kExp2Hi + j), __ldg(kExp2Lo + j)};
+  const F2 y = f2_mul(t, e);
+  return F2{ldexpf(y.hi, n), ldexpf(y.lo, n)};
 }
 
 // Ordering of normalised two-float numbers (|lo| <= ulp(hi) / 2, as f2_add

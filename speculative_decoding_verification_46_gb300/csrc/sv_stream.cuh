@@ -16,10 +16,10 @@
 //   greedy   per-row argmax (ties -> lowest index; NaN flagged)
 //   softmax  per-row online max / sum of 2^((L - m) c) with rescaling when the
 //            running max grows; p(d_i) and a_i at the row's end
-//   top-k    pass 1 (the ring) keeps per-thread maxima; the k-th largest is a
-//            lower bound tau of the row's k-th value; pass 2 re-reads the row
-//            (an L2 hit, evict-first) and keeps the elements >= tau; exact rank
-//            selection; softmax(./T) + top-p over the k; a_i
+//   top-k    pass 1 keeps per-thread maxima; the k-th largest is a lower
+//            bound tau of the row's k-th value; pass 2 re-reads the row (an L2
+//            hit), also through the ring, and keeps the elements
+//            >= tau; exact rank selection; softmax(./T) + top-p over the k; a_i
 //
 // The last row of a sequence to finish (atomic ticket, no waiting) runs the
 // acceptance scan.  Greedy and top-k also do the final draw there; softmax
@@ -38,8 +38,8 @@ constexpr int kStSTopk = 3;   // ring stages (top-k; leaves room for its selecti
 static_assert(kSt == kThreads, "the block reductions assume kThreads threads");
 
 __device__ __forceinline__ void cpa16(void* smem, const void* gmem) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -62,33 +62,50 @@ struct StreamSmem {
   float ur[kMaxG1];
 };
 
-// Per-thread sequence of ring items: item = (j-th row of this CTA, chunk c).
+// Per-thread sequence of ring items: (j-th row of this CTA, pass, chunk c),
+// PASSES passes over each row.  The issuer walks it S items ahead of the
+// consumer with running counters (no divisions); each item copies this
+// thread's kStU vectors of one chunk (kStU * kSt vectors) of a row.
 struct RowWalk {
   int R, G1, NV, CH, NCH, nrows;
   __device__ __forceinline__ int row_of(int j) const { return blockIdx.x + j * gridDim.x; }
 };
 
-template <typename T, int S>
-__device__ __forceinline__ void ring_issue(uint4* ring, const T* logits, size_t V, const RowWalk& w, int item) {
-  const int total = w.nrows * w.NCH;
-  if (item < total) {
-    const int j = item / w.NCH, c = item - j * w.NCH;
-    const T* row = logits + (size_t)w.row_of(j) * V;
-    uint4* slot = ring + (size_t)(item % S) * kStU * kSt;
-#pragma unroll
-    for (int u = 0; u < kStU; ++u) {
-      const int v = c * w.CH + u * kSt + (int)threadIdx.x;
-      if (v < w.NV) cpa16(slot + u * kSt + threadIdx.x, row + (size_t)v * Tr<T>::VW);
-    }
+template <typename T, int S, int PASSES>
+struct Issuer {
+  int j = 0, pass = 0, c = 0, stage = 0;
+  const T* row = nullptr;
+  __device__ __forceinline__ void start(const T* logits, size_t V, const RowWalk& w) {
+    row = logits + (size_t)w.row_of(0) * V;
   }
-  cpa_commit();   // empty groups keep every thread's group count in step
-}
+  // issue the next item into its stage (an empty group past the end)
+  __device__ __forceinline__ void issue(uint4* ring, const T* logits, size_t V, const RowWalk& w) {
+    if (j < w.nrows) {
+      uint4* slot = ring + (size_t)stage * kStU * kSt + threadIdx.x;
+      const int v0 = c * w.CH + (int)threadIdx.x;
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) {
+        const int v = v0 + u * kSt;
+        if (v < w.NV) cpa16(slot + u * kSt, row + (size_t)v * Tr<T>::VW);
+      }
+      if (++c == w.NCH) {
+        c = 0;
+        if (++pass == PASSES) {
+          pass = 0;
+          if (++j < w.nrows) row = logits + (size_t)w.row_of(j) * V;
+        }
+      }
+    }
+    cpa_commit();   // empty groups keep every thread's group count in step
+    stage = (stage + 1 == S) ? 0 : stage + 1;
+  }
+};
 
 // ---- dense finisher: per-row statistics already merged (one entry per row)
 template <int MODE>
 __device__ void stream_finish_dense(const Params& p, int b, StreamSmem& sm) {
   const int tid = threadIdx.x;
-  const int G = p.gamma, G1 = G + 1, V = p.V;
+  const int G = p.gamma, G1 = G + 1;
   if (tid < G1) {
     const float4 v = __ldcg(p.part + (size_t)b * G1 + tid);
     if (MODE == MODE_GREEDY) {
@@ -143,6 +160,60 @@ __device__ void stream_finish_dense(const Params& p, int b, StreamSmem& sm) {
   }
 }
 
+// Greedy helpers over one ring stage (this thread's kStU vectors, element
+// index (c0 + u*kSt + tid)*VW + t).  stage_max: the maximum, NaN if any element
+// is NaN, -inf if the stage holds no real vector.  16-bit types reduce packed
+// pairs first and convert once.
+template <typename T>
+__device__ __forceinline__ float stage_max(const uint4* slot, int c0, int NV) {
+  using TR = Tr<T>;
+  const int tid = threadIdx.x;
+  if constexpr (TR::VW == 8) {
+    using H2 = typename std::conditional<std::is_same<T, __half>::value, __half2, __nv_bfloat162>::type;
+    uint32_t padw = TR::kPadWord;
+    H2 acc = *reinterpret_cast<const H2*>(&padw);
+#pragma unroll
+    for (int u = 0; u < kStU; ++u) {
+      if (c0 + u * kSt + tid < NV) {
+        const uint4 x = slot[u * kSt + tid];
+        const H2 a = *reinterpret_cast<const H2*>(&x.x), b = *reinterpret_cast<const H2*>(&x.y);
+        const H2 cc = *reinterpret_cast<const H2*>(&x.z), d = *reinterpret_cast<const H2*>(&x.w);
+        acc = __hmax2_nan(acc, __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(cc, d)));
+      }
+    }
+    const float lo = __low2float(acc), hi = __high2float(acc);
+    if (lo != lo || hi != hi) return __uint_as_float(0x7fffffffu);
+    return fmaxf(lo, hi);
+  } else {
+    float m = -INFINITY;
+    bool nan = false;
+#pragma unroll
+    for (int u = 0; u < kStU; ++u) {
+      if (c0 + u * kSt + tid < NV) {
+        const float vm = TR::template vmax<true>(slot[u * kSt + tid]);
+        nan |= (vm != vm);
+        m = fmaxf(m, vm);
+      }
+    }
+    return nan ? __uint_as_float(0x7fffffffu) : m;
+  }
+}
+// lowest element index of the stage holding the value m (m is not NaN)
+template <typename T>
+__device__ __noinline__ int stage_first_index(const uint4* slot, int c0, int NV, float m) {
+  using TR = Tr<T>;
+  const int tid = threadIdx.x;
+  for (int u = 0; u < kStU; ++u) {
+    const int v = c0 + u * kSt + tid;
+    if (v < NV) {
+      const uint4 x = slot[u * kSt + tid];
+      for (int t = 0; t < TR::VW; ++t)
+        if (TR::get(x, t) == m) return v * TR::VW + t;
+    }
+  }
+  return 0x7fffffff;
+}
+
 // ---- greedy / softmax streaming kernel
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kSt, 3)
@@ -164,44 +235,45 @@ stream_dense_kernel(const Params p) {
   w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const T* logits = static_cast<const T*>(p.logits);
 
+  Issuer<T, S, 1> iss;
+  iss.start(logits, V, w);
 #pragma unroll
-  for (int s = 0; s < S; ++s) ring_issue<T, S>(ring, logits, V, w, s);
-  int item = 0;
+  for (int s2 = 0; s2 < S; ++s2) iss.issue(ring, logits, V, w);
+  int stage = 0;
   for (int j = 0; j < w.nrows; ++j) {
     const int r = w.row_of(j);
     const int b = r / G1, i = r - b * G1;
+    const T* row = logits + (size_t)r * V;
     // the draft's logit and q(d) for this row, fetched early (softmax only)
     float l_d = 0.f, q_d = 0.f;
     int d = -1;
     if (MODE == MODE_SOFTMAX && tid == 0 && i < G) {
       d = __ldg(p.draft + b * G + i);
       if (d >= 0 && d < V) {
-        l_d = Tr<T>::get(load_slot<T>(logits + (size_t)r * V, d, 1, false), 0);
+        l_d = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
         q_d = __ldg(p.q + ((size_t)b * G + i) * V + d);
       }
     }
-    float bv = -INFINITY;            // greedy: best value / index; softmax: running max
-    int bi = 0x7fffffff;
-    float m = -INFINITY, s0 = 0.f, s1 = 0.f;
-    for (int c = 0; c < w.NCH; ++c, ++item) {
+    float best = -INFINITY;          // greedy: this thread's max, its first index, NaN seen
+    int best_i = 0x7fffffff, nan_seen = 0;
+    float m = -INFINITY, s0 = 0.f, s1 = 0.f;   // softmax: running max and sums
+    for (int c = 0; c < w.NCH; ++c) {
       cpa_wait<S - 1>();
-      const uint4* slot = ring + (size_t)(item % S) * kStU * kSt;
+      const uint4* slot = ring + (size_t)stage * kStU * kSt;
+      if (MODE == MODE_GREEDY) {
+        // one max over the stage's kStU vectors; only a new best looks further
+        const float cm = stage_max<T>(slot, c * w.CH, w.NV);
+        nan_seen |= (cm != cm);
+        if (cm > best) {
+          best = cm;
+          best_i = stage_first_index<T>(slot, c * w.CH, w.NV, cm);
+        }
+      } else {
 #pragma unroll
-      for (int u = 0; u < kStU; ++u) {
-        const int v = c * w.CH + u * kSt + tid;
-        if (v < w.NV) {
-          const uint4 x = slot[u * kSt + tid];
-          if (MODE == MODE_GREEDY) {
-            const float vm = TR::template vmax<true>(x);
-            if (argmax_better(vm, 1, bv, 0) || bi == 0x7fffffff) {
-#pragma unroll
-              for (int t = VW - 1; t >= 0; --t) {
-                const float e = TR::get(x, t);
-                if ((vm != vm) ? (e != e) : (e == vm)) bi = v * VW + t;
-              }
-              bv = vm;
-            }
-          } else {
+        for (int u = 0; u < kStU; ++u) {
+          const int v = c * w.CH + u * kSt + tid;
+          if (v < w.NV) {
+            const uint4 x = slot[u * kSt + tid];
             const float vm = TR::template vmax<false>(x);
             if (vm > m) {
               const float sc = (m == -INFINITY) ? 0.f : ex2_approx((m - vm) * p.c);
@@ -220,10 +292,14 @@ stream_dense_kernel(const Params p) {
           }
         }
       }
-      ring_issue<T, S>(ring, logits, V, w, item + S);
+      iss.issue(ring, logits, V, w);
+      stage = (stage + 1 == S) ? 0 : stage + 1;
     }
     // ---- the row's statistic
     if (MODE == MODE_GREEDY) {
+      int bi = best_i;
+      float bv = best;
+      if (__syncthreads_or(nan_seen)) bv = __int_as_float(0x7fffffff);
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -290,7 +366,7 @@ stream_dense_kernel(const Params p) {
   cpa_wait<0>();
 }
 
-// ---- top-k streaming kernel (pass 1 through the ring)
+// ---- top-k streaming kernel (both passes through the ring)
 template <typename T>
 __global__ void __launch_bounds__(kSt, 2)
 stream_topk_kernel(const Params p) {
@@ -300,7 +376,7 @@ stream_topk_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw + (size_t)S * kStU * kSt * sizeof(uint4));
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int G = p.gamma, G1 = G + 1, V = p.V, k = p.top_k;
   RowWalk w;
   w.R = p.B * G1;
@@ -310,13 +386,16 @@ stream_topk_kernel(const Params p) {
   w.NCH = (w.NV + w.CH - 1) / w.CH;
   w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const T* logits = static_cast<const T*>(p.logits);
-  const uint64_t pol_first = policy_evict_first();
   constexpr int kWarpsHere = kSt / 32;
   constexpr int kCapW = kTkCap / kWarpsHere;   // candidate entries per warp
 
+  // both passes stream through the ring: pass 2's first chunks are already
+  // in flight while the threshold is being found
+  Issuer<T, S, 2> iss;
+  iss.start(logits, V, w);
 #pragma unroll
-  for (int s = 0; s < S; ++s) ring_issue<T, S>(ring, logits, V, w, s);
-  int item = 0;
+  for (int s = 0; s < S; ++s) iss.issue(ring, logits, V, w);
+  int stage = 0;
   for (int j = 0; j < w.nrows; ++j) {
     const int r = w.row_of(j);
     const int b = r / G1, i = r - b * G1;
@@ -329,12 +408,12 @@ stream_topk_kernel(const Params p) {
       d_row = __ldg(p.draft + b * G + i);
       if (d_row >= 0 && d_row < V) q_row = __ldg(p.q + ((size_t)b * G + i) * V + d_row);
     }
-    // ---- pass 1 through the ring: thread maxima
+    // ---- pass 1: thread maxima
     float tmax = -INFINITY;
     int any = 0;
-    for (int c = 0; c < w.NCH; ++c, ++item) {
+    for (int c = 0; c < w.NCH; ++c) {
       cpa_wait<S - 1>();
-      const uint4* slot = ring + (size_t)(item % S) * kStU * kSt;
+      const uint4* slot = ring + (size_t)stage * kStU * kSt;
 #pragma unroll
       for (int u = 0; u < kStU; ++u) {
         if (c * w.CH + u * kSt + tid < w.NV) {
@@ -342,7 +421,8 @@ stream_topk_kernel(const Params p) {
           any = 1;
         }
       }
-      ring_issue<T, S>(ring, logits, V, w, item + S);
+      iss.issue(ring, logits, V, w);
+      stage = (stage + 1 == S) ? 0 : stage + 1;
     }
     const uint32_t tkey = any ? okey(tmax) : 0u;
     uint32_t K = 0u;
@@ -355,35 +435,34 @@ stream_topk_kernel(const Params p) {
       __syncthreads();
     }
     const float tau = K == 0u ? -INFINITY : key_to_float(K);
-    // ---- pass 2 (L2): candidates >= tau
+    // ---- pass 2: candidates >= tau
     int nan_seen = 0;
     unsigned long long* wbuf = sm.cand + warp * kCapW;
-    for (int v0 = tid; v0 < w.NV; v0 += kSt * kStU) {
-      uint4 buf[kStU];
+    for (int c = 0; c < w.NCH; ++c) {
+      cpa_wait<S - 1>();
+      const uint4* slot = ring + (size_t)stage * kStU * kSt;
 #pragma unroll
       for (int u = 0; u < kStU; ++u) {
-        const int vi = v0 + u * kSt;
-        if (vi < w.NV) buf[u] = ldg_v4_hint(row + (size_t)vi * VW, pol_first);
-      }
-#pragma unroll
-      for (int u = 0; u < kStU; ++u) {
-        const int vi = v0 + u * kSt;
+        const int vi = c * w.CH + u * kSt + tid;
         if (vi < w.NV) {
-          const float mm = TR::template vmax<true>(buf[u]);
+          const uint4 x = slot[u * kSt + tid];
+          const float mm = TR::template vmax<true>(x);
           if (!(mm < tau)) {
 #pragma unroll
             for (int t = 0; t < VW; ++t) {
-              const float x = TR::get(buf[u], t);
-              if (x != x) {
+              const float xv = TR::get(x, t);
+              if (xv != xv) {
                 nan_seen = 1;
-              } else if (x >= tau) {
+              } else if (xv >= tau) {
                 const int pos = atomicAdd(&sm.wcount[warp], 1);
-                if (pos < kCapW) wbuf[pos] = comp_key(x, vi * VW + t);
+                if (pos < kCapW) wbuf[pos] = comp_key(xv, vi * VW + t);
               }
             }
           }
         }
       }
+      iss.issue(ring, logits, V, w);
+      stage = (stage + 1 == S) ? 0 : stage + 1;
     }
     const int bad_nan = __syncthreads_or(nan_seen);
     int overflow = 0, N = 0;

@@ -1,5 +1,5 @@
 // Top-k / top-p pieces shared by the streaming top-k kernel (sv_stream.cuh):
-// shared-memory layout, L2 cache-policy loads, the per-row epilogue
+// shared-memory layout, the per-row epilogue
 // (softmax(./T) over the row's top-k, the top-p cut, the kept list and the
 // acceptance probability of the row's draft) and the per-sequence finisher
 // (acceptance scan, final draw over the kept list of row n in token order,
@@ -38,24 +38,6 @@ struct TopkSmem {
   float WJ;
   float pd;
 };
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint4 ldg_v4_hint(const void* ptr, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(pol));
-  return v;
-}
 
 __device__ __forceinline__ int block_sum_int_n(int v, int* sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;

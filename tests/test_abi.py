@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(sv):
     lib = ctypes.CDLL(sv.load_library()._name)
     names = _declared_functions()
     assert set(names) == {"sv_workspace_bytes", "sv_verify_sample", "sv_verify_greedy", "sv_status_string",
-                          "sv_set_timing_events", "sv_verify_greedy_noalloc"}
+                          "sv_set_timing_events", "sv_verify_greedy_noalloc", "sv_last_kernels"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -125,3 +125,13 @@ def test_timing_hook_validation(sv):
     assert lib.sv_set_timing_events(None, 0) == sv.SV_OK
     assert lib.sv_set_timing_events(None, 3) == sv.SV_ERR_INVALID_ARG
     assert lib.sv_set_timing_events(None, 2) == sv.SV_ERR_INVALID_ARG
+
+
+def test_last_kernels_empty_without_launch(sv):
+    lib = sv.load_library()
+    assert sv.sv_last_kernels() == []
+    # an argument error and the empty batch launch nothing
+    assert lib.sv_verify_greedy(1, 2, 0, None, 0, None, None, None, None, None, 0, None) == sv.SV_ERR_INVALID_ARG
+    assert sv.sv_last_kernels() == []
+    assert lib.sv_verify_greedy(0, 2, 10, None, 0, None, None, None, None, None, 0, None) == sv.SV_OK
+    assert sv.sv_last_kernels() == []
