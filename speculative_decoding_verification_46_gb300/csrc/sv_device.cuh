@@ -24,7 +24,7 @@
 //                    the one row each sequence draws from: chunk masses of
 //                    max(p - q, 0) (or p for the bonus), then the last CTA of the
 //                    sequence locates the inverse-CDF step chunk -> thread ->
-//                    element using exactly the same float32 partial sums.
+//                    token with the same two-float partial sums.
 //
 // Data problems never trap: they set per-sequence status bits.  There are no
 // spin-waits: cross-CTA hand-off is only "last arriving CTA continues".
@@ -85,7 +85,7 @@ struct Params {
   float4* part;                   // [R][S] per-slice partials
   unsigned long long* lists;      // [R][S][top_k] per-slice top-k candidates
   int2* rowres;                   // [R][top_k + 1] kept (index, probability) lists
-  float2* chunk_mass;             // [B][C * slots] residual sub-range masses (two-float)
+  float2* chunk_mass;             // [B][3][C] residual chunk sums (S, A, Q; two-float)
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -307,26 +307,28 @@ __device__ const float kExp2Lo[64] = {
     9.845328108e-09f, 5.357072297e-08f, -1.702180441e-08f, 6.032726318e-09f,
 };
 
-// 2^a for a two-float a (a <= 0): a = n + j/64 + r with |r| <= 1/128, so
-// 2^a = 2^n * 2^(j/64) * e^g with g = r ln 2, |g| <= 0.0055, and
-// e^g = 1 + g + (g^2/2 + g^3/6 + g^4/24) to ~4e-14 (the bracket, below 1.6e-5,
-// is evaluated in float).  ln 2 is a float pair from its exact value.  Out of
-// line: it runs only for the few tokens that carry most of a row's mass.
-__device__ __noinline__ F2 exp2_f2(F2 a) {
+// 2^a for a two-float a with a.hi <= ~127, to ~2e-12 relative (Tang's
+// table-driven method): k = round(64 a), 2^a = 2^(k>>6) * 2^((k&63)/64) * e^g
+// with g = (a - k/64) ln 2, |g| <= ln 2 / 128.  The 64 values 2^(j/64) are
+// float pairs from their exact values; e^g = 1 + g + (g^2/2 + g^3/6 + g^4/24),
+// the bracket (< 2e-5) in float32.  a.hi < -125 gives 0.
+__device__ __forceinline__ F2 exp2_f2(F2 a) {
   const F2 kLn2{6.931471825e-01f, -1.904654212e-09f};
   if (a.hi < -125.f) return F2{0.f, 0.f};
-  const float k = rintf(a.hi * 64.f);            // a.hi * 64 is exact
-  const F2 r = f2_norm(a.hi - k * 0.015625f, a.lo);  // a.hi - k/64 is exact
-  const F2 g = f2_mul(r, kLn2);
-  const float gh = g.hi;
+  const float k = rintf(a.hi * 64.f);
+  const F2 r = f2_norm(a.hi - k * 0.015625f, a.lo);   // the subtraction is exact
+  const float gh = r.hi * kLn2.hi;
+  const float gl = fmaf(r.hi, kLn2.hi, -gh) + fmaf(r.hi, kLn2.lo, r.lo * kLn2.hi);
   const float small = gh * gh * fmaf(gh, fmaf(gh, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f);
-  const F2 e = f2_add(f2_add(F2{1.f, 0.f}, g), F2{small, 0.f});
+  const float eh = 1.f + gh;                          // |gh| < 1: Fast2Sum
+  const float el = ((1.f - eh) + gh) + (gl + small);
   const int ki = (int)k;
   const int j = ki & 63;
-  const int n = ki >> 6;                          // floor(k / 64)
-  const F2 t{__ldg(kExp2Hi + j), __ldg(kExp2Lo + j)};
-  const F2 y = f2_mul(t, e);
-  return F2{ldexpf(y.hi, n), ldexpf(y.lo, n)};
+  const float th = __ldg(kExp2Hi + j), tl = __ldg(kExp2Lo + j);
+  const float yh = th * eh;
+  const float yl = fmaf(th, eh, -yh) + fmaf(th, el, tl * eh);
+  const float scale = __int_as_float((127 + (ki >> 6)) << 23);   // 2^(k>>6), k>>6 in [-125, 127]
+  return F2{yh * scale, yl * scale};
 }
 
 // Ordering of normalised two-float numbers (|lo| <= ulp(hi) / 2, as f2_add
@@ -1285,14 +1287,13 @@ __device__ __forceinline__ F2x3 block_sum_f2x3(F2x3 v, F2x3* sm) {
   return t;
 }
 
-// ------------------------------------------------------------------ residual kernel
+// ------------------------------------------------------------------ final draw
 //
-// Element order.  A chunk of CL = 256 * EPT elements is read as NS = EPT / VW
-// "slots": slot j of thread t holds elements c0 + (j*256 + t)*VW + [0, VW), so
-// each warp-wide 16-byte load is coalesced.  Slot j of all threads is one
-// contiguous sub-range of the vocabulary, and the sub-ranges (chunk c, slot j)
-// follow the token index in (c, j) order.  The inverse-CDF search goes
-// sub-range -> thread -> element.
+// Slot helpers (used by the cluster kernel, whose CTA slices are read as
+// "slots": slot j of thread t holds elements (j*256 + t)*VW + [0, VW) of the
+// slice, so each warp-wide 16-byte load is coalesced; slot j of all threads is
+// one contiguous sub-range of the vocabulary).  The residual kernel further
+// down gives each thread a run of consecutive tokens instead.
 //
 // Precision.  This is the one row per sequence whose inverse CDF is compared
 // step by step with a float64 reference over up to ~10^5 steps, so token
@@ -1369,16 +1370,114 @@ __device__ __forceinline__ int slot_find(const uint4& v, const float* qv, int nv
   return found;
 }
 
+// ---- residual kernel: per-thread runs
+//
+// Element order.  A chunk of CL = 256 * EPT tokens is split into 256 runs of
+// EPT consecutive tokens, run t to thread t, so the inverse-CDF search goes
+// chunk -> thread -> token with every level contiguous in token order.  A
+// thread's EPT / VW vector loads are adjacent in memory (the first one of a
+// run brings the line the others hit in L1).
+
+// (S, A, Q) of one thread's run (see "Precision" above), two-float with the
+// error of every addition collected in the low words.
+struct RunAcc {
+  float sh, sl, ah, al, q;
+  __device__ __forceinline__ void zero() { sh = sl = ah = al = q = 0.f; }
+  __device__ static __forceinline__ void acc2(float& h, float& l, float x, float xl) {
+    const float s = h + x;
+    const float bb = s - h;
+    l += ((h - (s - bb)) + (x - bb)) + xl;
+    h = s;
+  }
+  __device__ __forceinline__ void add(F2 w, float qv, bool use_q, float s_a) {
+    acc2(sh, sl, w.hi, w.lo);
+    if (use_q) {
+      const float pr = s_a * qv;
+      if (w.hi > pr) {
+        const float pe = fmaf(s_a, qv, -pr);
+        const float dh = w.hi - pr;
+        const float bb = dh - w.hi;
+        const float de = (w.hi - (dh - bb)) + (-pr - bb);
+        acc2(ah, al, dh, de + (w.lo - pe));
+        q += qv;
+      }
+    }
+  }
+  __device__ __forceinline__ F2 S() const { return f2_norm(sh, sl); }
+  __device__ __forceinline__ F2 A() const { return f2_norm(ah, al); }
+  __device__ __forceinline__ F2 mass(bool resid, F2 ds) const {
+    return resid ? f2_add(A(), f2_neg(f2_scale(ds, q))) : S();
+  }
+};
+
+// One token's weight as a two-float (tok_weight's tail weights have lo = 0).
+__device__ __forceinline__ F2 tok_weight_f2(float x, float M, float c, float c_lo) {
+  F2 wt;
+  float wf;
+  if (tok_weight(x, M, c, c_lo, &wt, &wf)) return wt;
+  return F2{wf, 0.f};
+}
+
+// One token's increment of the walked mass: w (bonus / fallback to p) or, on
+// the residual support {w > s' q}, w - s' q - (s - s') q.
+__device__ __forceinline__ F2 token_mass(F2 w, float qv, bool use_q, float s_a, F2 ds) {
+  if (!use_q) return w;
+  const float pr = s_a * qv;
+  if (!(w.hi > pr)) return F2{0.f, 0.f};
+  const float pe = fmaf(s_a, qv, -pr);
+  const float dh = w.hi - pr;
+  const float bb = dh - w.hi;
+  const float de = (w.hi - (dh - bb)) + (-pr - bb);
+  F2 m = f2_add(f2_norm(dh, de + (w.lo - pe)), f2_neg(f2_scale(ds, qv)));
+  if (m.hi < 0.f) m = F2{0.f, 0.f};
+  return m;
+}
+
+// (S, A, Q) of the run [e0, e0 + NS * VW) of the final-draw row (tokens >= V
+// are skipped); all loads are issued before any arithmetic.
+template <typename T>
+__device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, int e0, int NS, int V, bool vec_ok,
+                                               bool use_q, float M, float c, float c_lo, float s_a, RunAcc* acc) {
+  constexpr int VW = Tr<T>::VW;
+  constexpr int kMaxNS = kResMaxEPT / VW;
+  uint4 v[kMaxNS];
+  float qv[kMaxNS][VW];
+#pragma unroll
+  for (int j = 0; j < kMaxNS; ++j) {
+    const int e = e0 + j * VW;
+    const int nv = (j < NS) ? min(max(V - e, 0), VW) : 0;
+    if (nv > 0) {
+      load_final_slot<T>(row, qrow, e, nv, vec_ok, &v[j], qv[j]);
+    } else {
+      v[j] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int t = 0; t < VW; ++t) qv[j][t] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxNS; ++j) {
+    if (j < NS) {
+#pragma unroll
+      for (int t = 0; t < VW; ++t) {
+        if (e0 + j * VW + t < V)
+          acc->add(tok_weight_f2(Tr<T>::get(v[j], t), M, c, c_lo), qv[j][t], use_q, s_a);
+      }
+    }
+  }
+}
+
 struct ResSmem {
   F2x3 red[kWarps];
   F2 f2red[kWarps];
-  int ired[kWarps];
   int flag;
-  int sub;        // selected sub-range (chunk * NS + slot), -1 if none
+  int sub;        // selected chunk, -1 if none
   int token;
   int use_q;
+  int owner;      // thread whose run holds the target
+  int lastpos;    // last thread with a positive mass
   F2 target;
   F2 base;
+  F2 tbase;       // the owner's exclusive prefix
   F2 ds;
   LocateSmem loc;
 };
@@ -1388,15 +1487,14 @@ __global__ void __launch_bounds__(kThreads)
 residual_kernel(const Params p) {
   using TR = Tr<T>;
   constexpr int VW = TR::VW;
-  constexpr int kMaxNS = kResMaxEPT / VW;
   __shared__ ResSmem sm;
   pdl_wait();
-  const int tid = threadIdx.x;
-  const int c = blockIdx.x % p.C;
-  const int b = blockIdx.x / p.C;
-  const int G = p.gamma, G1 = G + 1, V = p.V;
-  const int NS = p.EPT / VW;              // slots per thread per chunk
-  const int NT = p.C * NS;                // sub-ranges per row
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int C = p.C;
+  const int c = blockIdx.x % C;
+  const int b = blockIdx.x / C;
+  const int G = p.gamma, G1 = G + 1, V = p.V, EPT = p.EPT;
+  const int NS = EPT / VW;                // vectors per thread run
   SeqState st;
   st.n = __ldcg(&p.seq[b].n);
   st.status = __ldcg(&p.seq[b].status);
@@ -1410,45 +1508,29 @@ residual_kernel(const Params p) {
   const float M = st.M;
   const float s_a = (float)st.s;
   const bool vec_ok = (V % VW) == 0;
-  // per sequence: [S block | A block | Q block], NT two-float entries each
-  F2* cS = reinterpret_cast<F2*>(p.chunk_mass) + (size_t)b * 3 * NT;
-  F2* cA = cS + NT;
-  F2* cQ = cA + NT;
+  // per sequence: [S block | A block | Q block], C two-float entries each
+  F2* cS = reinterpret_cast<F2*>(p.chunk_mass) + (size_t)b * 3 * C;
+  F2* cA = cS + C;
+  F2* cQ = cA + C;
 
-  // ---- (S, A, Q) of this chunk's NS sub-ranges
-  const int c0 = c * p.CL;
-  SlotRun part[kMaxNS];
-#pragma unroll
-  for (int j = 0; j < kMaxNS; ++j) {
-    part[j].zero();
-    if (j < NS && !bad) {
-      const int e0 = c0 + (j * kThreads + tid) * VW;
-      const int nv = min(max(V - e0, 0), VW);
-      if (nv > 0) {
-        uint4 v;
-        float qv[VW];
-        load_final_slot<T>(row, qrow, e0, nv, vec_ok, &v, qv);
-        part[j] = slot_run<T>(v, qv, nv, resid, M, p.c, p.c_lo, s_a);
-      }
+  // ---- (S, A, Q) of this chunk
+  RunAcc acc;
+  acc.zero();
+  if (!bad) run_accumulate<T>(row, qrow, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, &acc);
+  {
+    const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
+    if (tid == 0) {
+      cS[c] = t.a;
+      cA[c] = t.b;
+      cQ[c] = t.c;
     }
   }
-#pragma unroll
-  for (int j = 0; j < kMaxNS; ++j) {
-    if (j < NS) {
-      const F2x3 t = block_sum_f2x3(F2x3{part[j].S(), part[j].A(), F2{part[j].q, 0.f}}, sm.red);
-      if (tid == 0) {
-        cS[c * NS + j] = t.a;
-        cA[c * NS + j] = t.b;
-        cQ[c * NS + j] = t.c;
-      }
-    }
-  }
-  if (!arrive_last(p.seq_ticket2 + b, p.C, &sm.flag, true)) return;
+  if (!arrive_last(p.seq_ticket2 + b, C, &sm.flag, true)) return;
 
-  // ---- last CTA of sequence b: exact normaliser, masses, inverse-CDF step
+  // ---- last CTA of sequence b: exact normaliser, masses, chunk -> thread -> token
   int status = st.status;
   F2 sl{0.f, 0.f};
-  for (int k2 = tid; k2 < NT; k2 += kThreads) {
+  for (int k2 = tid; k2 < C; k2 += kThreads) {
     const float2 v = __ldcg(reinterpret_cast<const float2*>(cS) + k2);
     sl = f2_add(sl, F2{v.x, v.y});
   }
@@ -1456,7 +1538,7 @@ residual_kernel(const Params p) {
   const F2 ds = f2_add(s, F2{-s_a, 0.f});          // s - s', tiny
   if (resid) {
     // residual masses A - (s - s') Q overwrite the A block
-    for (int k2 = tid; k2 < NT; k2 += kThreads) {
+    for (int k2 = tid; k2 < C; k2 += kThreads) {
       const float2 a2 = __ldcg(reinterpret_cast<const float2*>(cA) + k2);
       const float2 q2 = __ldcg(reinterpret_cast<const float2*>(cQ) + k2);
       F2 m = f2_add(F2{a2.x, a2.y}, f2_neg(f2_mul(ds, F2{q2.x, q2.y})));
@@ -1469,12 +1551,12 @@ residual_kernel(const Params p) {
   const float u = __ldg(p.uniforms + b * G1 + G);
   F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
   bool use_q = resid;
-  int sub = locate(resid ? cA : cS, NT, u, &R, &base, &tgt, sm.loc, true);
+  int sub = locate(resid ? cA : cS, C, u, &R, &base, &tgt, sm.loc, true);
   if (resid && !bad && !f2_pos(R)) {
     // zero residual mass (only through rounding): draw from p_n instead
     status |= SEQ_RESID0;
     use_q = false;
-    sub = locate(cS, NT, u, &R, &base, &tgt, sm.loc, true);
+    sub = locate(cS, C, u, &R, &base, &tgt, sm.loc, true);
   }
   if (tid == 0) {
     sm.sub = (bad || !f2_pos(R)) ? -1 : sub;
@@ -1483,54 +1565,55 @@ residual_kernel(const Params p) {
     sm.token = -1;
     sm.use_q = use_q;
     sm.ds = ds;
+    sm.owner = 0x7fffffff;
+    sm.lastpos = -1;
   }
   __syncthreads();
   int token = 0;
   if (sm.sub >= 0) {
     const bool uq = sm.use_q != 0;
-    const int e0 = (sm.sub / NS) * p.CL + ((sm.sub % NS) * kThreads + tid) * VW;
-    const int nv = min(max(V - e0, 0), VW);
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    float qv[VW];
-#pragma unroll
-    for (int t = 0; t < VW; ++t) qv[t] = 0.f;
-    F2 mine{0.f, 0.f};
-    if (nv > 0) {
-      load_final_slot<T>(row, uq ? qrow : nullptr, e0, nv, vec_ok, &v, qv);
-      mine = slot_run<T>(v, qv, nv, uq, M, p.c, p.c_lo, s_a).mass(uq, sm.ds);
-      if (mine.hi < 0.f) mine = F2{0.f, 0.f};
-    }
+    const int c0 = sm.sub * p.CL;
+    RunAcc r;
+    r.zero();
+    run_accumulate<T>(row, uq ? qrow : nullptr, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, &r);
+    F2 mine = r.mass(uq, sm.ds);
+    if (mine.hi < 0.f) mine = F2{0.f, 0.f};
     F2 total;
     const F2 ex = block_exclusive_f2(mine, sm.f2red, &total);
     const F2 tbase = f2_add(sm.base, ex);
-    int lastp = -1;
-    if (nv > 0 && f2_pos(mine) && !f2_lt(sm.target, tbase) && f2_lt(sm.target, f2_add(tbase, mine))) {
-      const int f = slot_find<T>(v, qv, nv, uq, M, p.c, p.c_lo, s_a, sm.ds, tbase, sm.target, &lastp);
-      if (f >= 0) sm.token = e0 + f;
+    const bool pos = f2_pos(mine);
+    if (pos && !f2_lt(sm.target, tbase) && f2_lt(sm.target, f2_add(tbase, mine))) atomicMin(&sm.owner, tid);
+    if (pos) atomicMax(&sm.lastpos, tid);
+    __syncthreads();
+    // rounding can leave no run above the target: take the last positive one
+    const bool take_last = sm.owner == 0x7fffffff;
+    const int owner = take_last ? sm.lastpos : sm.owner;
+    if (tid == owner) sm.tbase = tbase;
+    __syncthreads();
+    if (owner >= 0 && tid < 32) {
+      // warp 0 walks the owner's run, one token per lane (EPT <= 32)
+      const int e = c0 + owner * EPT + lane;
+      F2 m{0.f, 0.f};
+      if (lane < EPT && e < V) {
+        const float x = TR::get(load_slot<T>(row, e, 1, false), 0);
+        const float qv = uq ? __ldg(qrow + e) : 0.f;
+        m = token_mass(tok_weight_f2(x, M, p.c, p.c_lo), qv, uq, s_a, sm.ds);
+      }
+      const F2 inc = warp_incl_scan_f2(m);
+      F2 excl = f2_shfl_up(inc, 1);
+      if (lane == 0) excl = F2{0.f, 0.f};
+      const F2 lb = f2_add(sm.tbase, excl);
+      const bool live = f2_pos(m);
+      const unsigned hit = __ballot_sync(0xffffffffu, live && !take_last && !f2_lt(sm.target, lb) &&
+                                                          f2_lt(sm.target, f2_add(lb, m)));
+      const unsigned any = __ballot_sync(0xffffffffu, live);
+      const int pick = hit ? __ffs(hit) - 1 : (any ? 31 - __clz(any) : -1);
+      if (lane == 0) sm.token = pick >= 0 ? c0 + owner * EPT + pick : -1;
     }
     __syncthreads();
-    if (sm.token < 0) {
-      // rounding left no step above the target: take the last positive weight
-      int m = -1;
-      if (nv > 0) {
-        int lp = -1;
-        slot_find<T>(v, qv, nv, uq, M, p.c, p.c_lo, s_a, sm.ds, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
-        if (lp >= 0) m = e0 + lp;
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if ((tid & 31) == 0) sm.ired[tid >> 5] = m;
-      __syncthreads();
-      if (tid == 0) {
-        int mm = -1;
-        for (int w = 0; w < kWarps; ++w) mm = max(mm, sm.ired[w]);
-        sm.token = mm;
-      }
-      __syncthreads();
-    }
     token = sm.token < 0 ? 0 : sm.token;
   }
-  for (int k2 = tid; k2 < 3 * NT; k2 += kThreads) cS[k2] = F2{0.f, 0.f};
+  for (int k2 = tid; k2 < 3 * C; k2 += kThreads) cS[k2] = F2{0.f, 0.f};
   if (tid == 0) {
     p.out_tokens[b * G1 + n] = token;
     if (p.out_status) p.out_status[b] = status;
