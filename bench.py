@@ -319,9 +319,11 @@ def run_gb300(args, rank, ws_n, local):
 
     # algorithmic bytes: average over the input sets (the final draw depends on the data)
     nacc = np.concatenate([o[1].cpu().numpy() for o in outs])
-    kept = 0
     ab = algorithmic_bytes(w, nacc)
     ab = {k: v / n_sets for k, v in ab.items()}
+    if kernels_per_call == 1:
+        # one kernel does the whole step (its final draw included)
+        ab = {"stream": ab["stream"] + ab["final"], "final": 0.0}
     peak, peak_kind = _peaks()
     kern = "stream" if t_stream >= t_final else "final"
     kname = kernel_names[0] if kern == "stream" else kernel_names[1]

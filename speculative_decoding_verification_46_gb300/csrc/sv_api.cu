@@ -141,10 +141,16 @@ sv_status launch_rows(const sv::Params& p, cudaStream_t stream) {
 
 template <typename T>
 sv_status launch_residual(const sv::Params& p, cudaStream_t stream) {
+  const size_t smem = sv::ResStage<T>::bytes;
+  if (cudaFuncSetAttribute(sv::residual_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((long long)p.B * p.C));
   cfg.blockDim = dim3(sv::kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -252,7 +258,7 @@ long long stream_grid(K kern, size_t smem, long long R) {
 template <typename T>
 sv_status launch_stream_topk(const sv::Params& p, cudaStream_t stream) {
   auto kern = sv::stream_topk_kernel<T>;
-  const size_t smem = (size_t)sv::kStSTopk * sv::kStU * sv::kSt * sizeof(uint4) + sizeof(sv::TopkSmem);
+  const size_t smem = (size_t)sv::kStSTopk * sv::kStUTopk * sv::kSt * sizeof(uint4) + sizeof(sv::TopkSmem);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_CUDA;

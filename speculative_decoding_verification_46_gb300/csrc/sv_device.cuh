@@ -1410,59 +1410,147 @@ struct RunAcc {
   }
 };
 
-// One token's weight as a two-float (tok_weight's tail weights have lo = 0).
-__device__ __forceinline__ F2 tok_weight_f2(float x, float M, float c, float c_lo) {
-  F2 wt;
-  float wf;
-  if (tok_weight(x, M, c, c_lo, &wt, &wf)) return wt;
-  return F2{wf, 0.f};
+// Adds one token of the final-draw row to a run: the weight 2^((x - M) c)
+// as in tok_weight (two-float exponent; near the maximum the two-float exp2),
+// the residual part on the support {w > s' q}.  Tail weights carry exp2f's
+// rounding already, so their residual w - s' q takes a single rounding (fma);
+// near the maximum it is formed exactly.  run_tail handles a tail token and
+// returns false, or returns true and adds nothing for a token near the
+// maximum, which run_top then adds.
+__device__ __forceinline__ float tok_exponent(float x, float M, float c, float c_lo, float* e_out) {
+  const float dh = x - M;
+  const float bb = dh - x;
+  const float dl = (x - (dh - bb)) + (-M - bb);   // x - M = dh + dl exactly
+  const float p = dh * c;
+  float e = fmaf(dh, c, -p);
+  e = fmaf(dh, c_lo, e);
+  *e_out = fmaf(dl, c, e);
+  return p;
+}
+__device__ __forceinline__ bool run_tail(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
+                                         float s_a) {
+  float e;
+  const float p = tok_exponent(x, M, c, c_lo, &e);
+  const bool top = p > -8.f;
+  const float y = exp2f(p);
+  const float w = (top || x == -INFINITY) ? 0.f : fmaf(y * 6.931471825e-01f, e, y);
+  RunAcc::acc2(acc.sh, acc.sl, w, 0.f);
+  if (use_q) {
+    const float pr = s_a * qv;
+    if (w > pr) {
+      RunAcc::acc2(acc.ah, acc.al, fmaf(-s_a, qv, w), 0.f);
+      acc.q += qv;
+    }
+  }
+  return top;
+}
+__device__ __forceinline__ void run_top(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
+                                        float s_a) {
+  float e;
+  const float p = tok_exponent(x, M, c, c_lo, &e);
+  acc.add(exp2_f2(f2_norm(p, e)), qv, use_q, s_a);
+}
+__device__ __forceinline__ void run_add(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
+                                        float s_a) {
+  if (run_tail(acc, x, qv, use_q, M, c, c_lo, s_a)) run_top(acc, x, qv, use_q, M, c, c_lo, s_a);
 }
 
-// One token's increment of the walked mass: w (bonus / fallback to p) or, on
-// the residual support {w > s' q}, w - s' q - (s - s') q.
-__device__ __forceinline__ F2 token_mass(F2 w, float qv, bool use_q, float s_a, F2 ds) {
-  if (!use_q) return w;
-  const float pr = s_a * qv;
-  if (!(w.hi > pr)) return F2{0.f, 0.f};
-  const float pe = fmaf(s_a, qv, -pr);
-  const float dh = w.hi - pr;
-  const float bb = dh - w.hi;
-  const float de = (w.hi - (dh - bb)) + (-pr - bb);
-  F2 m = f2_add(f2_norm(dh, de + (w.lo - pe)), f2_neg(f2_scale(ds, qv)));
+// One token's increment of the walked mass, with run_add's arithmetic: the
+// weight w (bonus / fallback to p) or, on the residual support {w > s' q},
+// w - s' q - (s - s') q.
+__device__ __forceinline__ F2 token_mass(float x, float qv, bool use_q, float M, float c, float c_lo, float s_a,
+                                         F2 ds) {
+  RunAcc one;
+  one.zero();
+  run_add(one, x, qv, use_q, M, c, c_lo, s_a);
+  F2 m = one.mass(use_q, ds);
   if (m.hi < 0.f) m = F2{0.f, 0.f};
   return m;
 }
 
+// Per-thread staging of a run in shared memory, thread-interleaved:
+// kResStageVec(T) logits vectors then kResStageQ q vectors per thread.
+template <typename T>
+struct ResStage {
+  static constexpr int VW = Tr<T>::VW;
+  static constexpr int NL = kResMaxEPT / VW;    // 16-byte logits vectors per run
+  static constexpr int NQ = kResMaxEPT / 4;     // 16-byte q vectors per run
+  static constexpr size_t bytes = (size_t)(NL + NQ) * kThreads * sizeof(uint4);
+};
+
+__device__ __forceinline__ void res_cp16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
 // (S, A, Q) of the run [e0, e0 + NS * VW) of the final-draw row (tokens >= V
-// are skipped); all loads are issued before any arithmetic.
+// are skipped).  The whole run is copied into this thread's slots of `stage`
+// first (all copies in flight at once), then walked by a rolled loop.
 template <typename T>
 __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, int e0, int NS, int V, bool vec_ok,
-                                               bool use_q, float M, float c, float c_lo, float s_a, RunAcc* acc) {
-  constexpr int VW = Tr<T>::VW;
-  constexpr int kMaxNS = kResMaxEPT / VW;
-  uint4 v[kMaxNS];
-  float qv[kMaxNS][VW];
-#pragma unroll
-  for (int j = 0; j < kMaxNS; ++j) {
+                                               bool use_q, float M, float c, float c_lo, float s_a, uint4* stage,
+                                               RunAcc* acc) {
+  using RS = ResStage<T>;
+  constexpr int VW = RS::VW;
+  const int tid = threadIdx.x;
+  uint4* lg = stage;
+  uint4* qq = stage + RS::NL * kThreads;
+  for (int j = 0; j < NS; ++j) {
     const int e = e0 + j * VW;
-    const int nv = (j < NS) ? min(max(V - e, 0), VW) : 0;
-    if (nv > 0) {
-      load_final_slot<T>(row, qrow, e, nv, vec_ok, &v[j], qv[j]);
+    const int nv = min(max(V - e, 0), VW);
+    if (nv == VW && vec_ok) {
+      res_cp16(lg + j * kThreads + tid, row + e);
+      if (qrow) {
+#pragma unroll
+        for (int h = 0; h < VW / 4; ++h) res_cp16(qq + (j * (VW / 4) + h) * kThreads + tid, qrow + e + 4 * h);
+      }
     } else {
-      v[j] = make_uint4(0u, 0u, 0u, 0u);
+      lg[j * kThreads + tid] = load_slot<T>(row, e, max(nv, 0), vec_ok && nv == VW);
+      if (qrow) {
 #pragma unroll
-      for (int t = 0; t < VW; ++t) qv[j][t] = 0.f;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxNS; ++j) {
-    if (j < NS) {
-#pragma unroll
-      for (int t = 0; t < VW; ++t) {
-        if (e0 + j * VW + t < V)
-          acc->add(tok_weight_f2(Tr<T>::get(v[j], t), M, c, c_lo), qv[j][t], use_q, s_a);
+        for (int h = 0; h < VW / 4; ++h) {
+          float4 q4;
+          q4.x = (4 * h + 0 < nv) ? __ldg(qrow + e + 4 * h + 0) : 0.f;
+          q4.y = (4 * h + 1 < nv) ? __ldg(qrow + e + 4 * h + 1) : 0.f;
+          q4.z = (4 * h + 2 < nv) ? __ldg(qrow + e + 4 * h + 2) : 0.f;
+          q4.w = (4 * h + 3 < nv) ? __ldg(qrow + e + 4 * h + 3) : 0.f;
+          qq[(j * (VW / 4) + h) * kThreads + tid] = *reinterpret_cast<const uint4*>(&q4);
+        }
       }
     }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  // tail tokens in one branch-free sweep; tokens near the maximum (bit set
+  // in `top`) in a second loop
+  uint32_t top = 0u;
+#pragma unroll 1
+  for (int j = 0; j < NS; ++j) {
+    const uint4 v = lg[j * kThreads + tid];
+    float qv[VW];
+#pragma unroll
+    for (int h = 0; h < VW / 4; ++h) {
+      if (qrow) {
+        const uint4 q4 = qq[(j * (VW / 4) + h) * kThreads + tid];
+        qv[4 * h + 0] = __uint_as_float(q4.x);
+        qv[4 * h + 1] = __uint_as_float(q4.y);
+        qv[4 * h + 2] = __uint_as_float(q4.z);
+        qv[4 * h + 3] = __uint_as_float(q4.w);
+      } else {
+        qv[4 * h + 0] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
+      }
+    }
+    const int ev = e0 + j * VW;
+#pragma unroll
+    for (int t = 0; t < VW; ++t)
+      if (ev + t < V && run_tail(*acc, Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a)) top |= 1u << (j * VW + t);
+  }
+  while (top) {
+    const int o = __ffs(top) - 1;   // offset in the run
+    top &= top - 1;
+    const int j = o / VW, t = o - j * VW;
+    const float x = Tr<T>::get(lg[j * kThreads + tid], t);
+    const float qv = qrow ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3)) : 0.f;
+    run_top(*acc, x, qv, use_q, M, c, c_lo, s_a);
   }
 }
 
@@ -1488,6 +1576,8 @@ residual_kernel(const Params p) {
   using TR = Tr<T>;
   constexpr int VW = TR::VW;
   __shared__ ResSmem sm;
+  extern __shared__ __align__(16) unsigned char res_dyn[];
+  uint4* stage = reinterpret_cast<uint4*>(res_dyn);   // ResStage<T>::bytes
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31;
   const int C = p.C;
@@ -1516,7 +1606,8 @@ residual_kernel(const Params p) {
   // ---- (S, A, Q) of this chunk
   RunAcc acc;
   acc.zero();
-  if (!bad) run_accumulate<T>(row, qrow, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, &acc);
+  if (!bad)
+    run_accumulate<T>(row, qrow, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc);
   {
     const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
     if (tid == 0) {
@@ -1575,7 +1666,7 @@ residual_kernel(const Params p) {
     const int c0 = sm.sub * p.CL;
     RunAcc r;
     r.zero();
-    run_accumulate<T>(row, uq ? qrow : nullptr, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, &r);
+    run_accumulate<T>(row, uq ? qrow : nullptr, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, stage, &r);
     F2 mine = r.mass(uq, sm.ds);
     if (mine.hi < 0.f) mine = F2{0.f, 0.f};
     F2 total;
@@ -1597,7 +1688,7 @@ residual_kernel(const Params p) {
       if (lane < EPT && e < V) {
         const float x = TR::get(load_slot<T>(row, e, 1, false), 0);
         const float qv = uq ? __ldg(qrow + e) : 0.f;
-        m = token_mass(tok_weight_f2(x, M, p.c, p.c_lo), qv, uq, s_a, sm.ds);
+        m = token_mass(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
       }
       const F2 inc = warp_incl_scan_f2(m);
       F2 excl = f2_shfl_up(inc, 1);

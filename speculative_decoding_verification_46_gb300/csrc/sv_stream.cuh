@@ -17,9 +17,9 @@
 //   softmax  per-row online max / sum of 2^((L - m) c) with rescaling when the
 //            running max grows; p(d_i) and a_i at the row's end
 //   top-k    pass 1 keeps per-thread maxima; the k-th largest is a lower
-//            bound tau of the row's k-th value; pass 2 re-reads the row (an L2
-//            hit), also through the ring, and keeps the elements
-//            >= tau; exact rank selection; softmax(./T) + top-p over the k; a_i
+//            bound tau of the row's k-th value; pass 2 re-reads (L2) only the
+//            elements of threads whose maximum reaches tau; exact rank
+//            selection of the candidates >= tau; softmax(./T) + top-p; a_i
 //
 // The last row of a sequence to finish (atomic ticket, no waiting) runs the
 // acceptance scan.  Greedy and top-k also do the final draw there; softmax
@@ -35,6 +35,7 @@ constexpr int kSt = 256;      // threads per CTA
 constexpr int kStU = 4;       // vectors per thread per ring stage
 constexpr int kStS = 4;       // ring stages (dense modes)
 constexpr int kStSTopk = 3;   // ring stages (top-k; leaves room for its selection buffers)
+constexpr int kStUTopk = 4;   // vectors per thread per ring stage (top-k)
 static_assert(kSt == kThreads, "the block reductions assume kThreads threads");
 
 __device__ __forceinline__ void cpa16(void* smem, const void* gmem) {
@@ -65,13 +66,13 @@ struct StreamSmem {
 // Per-thread sequence of ring items: (j-th row of this CTA, pass, chunk c),
 // PASSES passes over each row.  The issuer walks it S items ahead of the
 // consumer with running counters (no divisions); each item copies this
-// thread's kStU vectors of one chunk (kStU * kSt vectors) of a row.
+// thread's U vectors of one chunk (U * kSt vectors) of a row.
 struct RowWalk {
   int R, G1, NV, CH, NCH, nrows;
   __device__ __forceinline__ int row_of(int j) const { return blockIdx.x + j * gridDim.x; }
 };
 
-template <typename T, int S, int PASSES>
+template <typename T, int S, int PASSES, int U = kStU>
 struct Issuer {
   int j = 0, pass = 0, c = 0, stage = 0;
   const T* row = nullptr;
@@ -81,10 +82,10 @@ struct Issuer {
   // issue the next item into its stage (an empty group past the end)
   __device__ __forceinline__ void issue(uint4* ring, const T* logits, size_t V, const RowWalk& w) {
     if (j < w.nrows) {
-      uint4* slot = ring + (size_t)stage * kStU * kSt + threadIdx.x;
+      uint4* slot = ring + (size_t)stage * U * kSt + threadIdx.x;
       const int v0 = c * w.CH + (int)threadIdx.x;
 #pragma unroll
-      for (int u = 0; u < kStU; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int v = v0 + u * kSt;
         if (v < w.NV) cpa16(slot + u * kSt, row + (size_t)v * Tr<T>::VW);
       }
@@ -366,32 +367,37 @@ stream_dense_kernel(const Params p) {
   cpa_wait<0>();
 }
 
-// ---- top-k streaming kernel (both passes through the ring)
+// ---- top-k streaming kernel
+//
+// Pass 1 (the ring) keeps each thread's maximum.  tau = the k-th largest
+// thread maximum is a lower bound of the row's k-th largest value, and only
+// threads whose maximum reaches tau can hold elements >= tau: pass 2 re-reads
+// just those threads' elements (about k of the 256 threads; an L2 hit), the
+// work spread over the whole CTA.  The candidates (all elements >= tau) are
+// ranked exactly by (value desc, index asc).
 template <typename T>
-__global__ void __launch_bounds__(kSt, 2)
+__global__ void __launch_bounds__(kSt, 3)
 stream_topk_kernel(const Params p) {
   using TR = Tr<T>;
   constexpr int VW = TR::VW;
   constexpr int S = kStSTopk;
+  constexpr int U = kStUTopk;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw + (size_t)S * kStU * kSt * sizeof(uint4));
-  const int tid = threadIdx.x, warp = tid >> 5;
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw + (size_t)S * U * kSt * sizeof(uint4));
+  const int tid = threadIdx.x;
   const int G = p.gamma, G1 = G + 1, V = p.V, k = p.top_k;
   RowWalk w;
   w.R = p.B * G1;
   w.G1 = G1;
   w.NV = V / VW;
-  w.CH = kStU * kSt;
+  w.CH = U * kSt;
   w.NCH = (w.NV + w.CH - 1) / w.CH;
   w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int MV = (w.NV + kSt - 1) / kSt;   // vectors of the thread with the most
   const T* logits = static_cast<const T*>(p.logits);
-  constexpr int kWarpsHere = kSt / 32;
-  constexpr int kCapW = kTkCap / kWarpsHere;   // candidate entries per warp
 
-  // both passes stream through the ring: pass 2's first chunks are already
-  // in flight while the threshold is being found
-  Issuer<T, S, 2> iss;
+  Issuer<T, S, 1, U> iss;
   iss.start(logits, V, w);
 #pragma unroll
   for (int s = 0; s < S; ++s) iss.issue(ring, logits, V, w);
@@ -401,77 +407,83 @@ stream_topk_kernel(const Params p) {
     const int b = r / G1, i = r - b * G1;
     const T* row = logits + (size_t)r * V;
     __syncthreads();   // the previous row's shared state is no longer in use
-    if (tid < kWarpsHere) sm.wcount[tid] = 0;
+    if (tid == 0) {
+      sm.count = 0;
+      sm.nrel = 0;
+    }
     int d_row = -1;
     float q_row = 0.f;
     if (tid == 0 && i < G) {
       d_row = __ldg(p.draft + b * G + i);
       if (d_row >= 0 && d_row < V) q_row = __ldg(p.q + ((size_t)b * G + i) * V + d_row);
     }
-    // ---- pass 1: thread maxima
+    // ---- pass 1 through the ring: thread maxima (NaN noted)
     float tmax = -INFINITY;
-    int any = 0;
+    int nan_seen = 0;
     for (int c = 0; c < w.NCH; ++c) {
       cpa_wait<S - 1>();
-      const uint4* slot = ring + (size_t)stage * kStU * kSt;
+      const uint4* slot = ring + (size_t)stage * U * kSt;
 #pragma unroll
-      for (int u = 0; u < kStU; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (c * w.CH + u * kSt + tid < w.NV) {
-          tmax = fmaxf(tmax, TR::template vmax<false>(slot[u * kSt + tid]));
-          any = 1;
+          const float vm = TR::template vmax<true>(slot[u * kSt + tid]);
+          nan_seen |= (vm != vm);
+          tmax = fmaxf(tmax, vm);
         }
       }
       iss.issue(ring, logits, V, w);
       stage = (stage + 1 == S) ? 0 : stage + 1;
     }
-    const uint32_t tkey = any ? okey(tmax) : 0u;
+    // ---- tau: the k-th largest finite thread maximum (bisection on keys)
+    const uint32_t tkey = tmax > -INFINITY ? okey(tmax) : 0u;
     uint32_t K = 0u;
-    if (V > k) {
-      for (int bit = 31; bit >= TR::KEY_LOW_BIT; --bit) {
-        const uint32_t Kt = K | (1u << bit);
-        if (__syncthreads_count(tkey >= Kt) >= k) K = Kt;
-      }
-    } else {
-      __syncthreads();
+    for (int bit = 31; bit >= TR::KEY_LOW_BIT; --bit) {
+      const uint32_t Kt = K | (1u << bit);
+      if (__syncthreads_count(tkey >= Kt) >= k) K = Kt;
     }
     const float tau = K == 0u ? -INFINITY : key_to_float(K);
-    // ---- pass 2: candidates >= tau
-    int nan_seen = 0;
-    unsigned long long* wbuf = sm.cand + warp * kCapW;
-    for (int c = 0; c < w.NCH; ++c) {
-      cpa_wait<S - 1>();
-      const uint4* slot = ring + (size_t)stage * kStU * kSt;
+    if (tmax > -INFINITY && tmax >= tau) sm.rel[atomicAdd(&sm.nrel, 1)] = tid;
+    const int bad_nan = __syncthreads_or(nan_seen);
+    // ---- pass 2 (L2): the elements >= tau of the listed threads
+    {
+      const int nrel = sm.nrel;
+      const int items = nrel * MV;
+      for (int q0 = tid; q0 < items; q0 += kSt * 4) {
+        uint4 x[4];
+        int vv[4];
 #pragma unroll
-      for (int u = 0; u < kStU; ++u) {
-        const int vi = c * w.CH + u * kSt + tid;
-        if (vi < w.NV) {
-          const uint4 x = slot[u * kSt + tid];
-          const float mm = TR::template vmax<true>(x);
-          if (!(mm < tau)) {
+        for (int h = 0; h < 4; ++h) {
+          const int q = q0 + h * kSt;
+          vv[h] = -1;
+          if (q < items) {
+            const int l = q / MV, m = q - l * MV;
+            const int v = sm.rel[l] + m * kSt;
+            if (v < w.NV) {
+              vv[h] = v;
+              x[h] = ldg_v4(row + (size_t)v * VW);
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          if (vv[h] >= 0 && !(TR::template vmax<false>(x[h]) < tau)) {
 #pragma unroll
             for (int t = 0; t < VW; ++t) {
-              const float xv = TR::get(x, t);
-              if (xv != xv) {
-                nan_seen = 1;
-              } else if (xv >= tau) {
-                const int pos = atomicAdd(&sm.wcount[warp], 1);
-                if (pos < kCapW) wbuf[pos] = comp_key(xv, vi * VW + t);
+              const float xv = TR::get(x[h], t);
+              if (xv > -INFINITY && xv >= tau) {   // NaN fails both
+                const int pos = atomicAdd(&sm.count, 1);
+                if (pos < kTkCap) sm.cand[pos] = comp_key(xv, vv[h] * VW + t);
               }
             }
           }
         }
       }
-      iss.issue(ring, logits, V, w);
-      stage = (stage + 1 == S) ? 0 : stage + 1;
     }
-    const int bad_nan = __syncthreads_or(nan_seen);
-    int overflow = 0, N = 0;
-    for (int w2 = 0; w2 < kWarpsHere; ++w2) {
-      overflow |= sm.wcount[w2] > kCapW;
-      N += min(sm.wcount[w2], kCapW);
-    }
-    if (overflow) {
-      // exact k-th largest (value, index) key by bisection over the row
+    __syncthreads();
+    int N = sm.count;
+    if (N > kTkCap) {
+      // more candidates than the buffer holds (heavy ties at tau): the exact
+      // k-th largest (value, index) key by bisection over the row
       unsigned long long K64 = 0ull;
       for (int bit = 63; bit >= 0; --bit) {
         const unsigned long long Kt = K64 | (1ull << bit);
@@ -505,25 +517,15 @@ stream_topk_kernel(const Params p) {
       }
       __syncthreads();
       N = min(sm.count, kTkCap);
-      for (int e = tid; e < N; e += kSt) {
-        const unsigned long long me = sm.cand[e];
-        int rank = 0;
-        for (int jj = 0; jj < N; ++jj) rank += sm.cand[jj] > me;
-        if (rank < k) sm.sel[rank] = me;
-      }
-    } else {
-      for (int w2 = 0; w2 < kWarpsHere; ++w2) {
-        const int cw = min(sm.wcount[w2], kCapW);
-        for (int s2 = tid; s2 < cw; s2 += kSt) {
-          const unsigned long long me = sm.cand[w2 * kCapW + s2];
-          int rank = 0;
-          for (int w3 = 0; w3 < kWarpsHere; ++w3) {
-            const int c3 = min(sm.wcount[w3], kCapW);
-            const unsigned long long* src = sm.cand + w3 * kCapW;
-            for (int jj = 0; jj < c3; ++jj) rank += src[jj] > me;
-          }
-          if (rank < k) sm.sel[rank] = me;
-        }
+    }
+    // exact ranks among the candidates (keys are distinct: the index is in them)
+    for (int e = tid; e < N; e += kSt) {
+      const unsigned long long me = sm.cand[e];
+      int rank = 0;
+      for (int jj = 0; jj < N; ++jj) rank += sm.cand[jj] > me;
+      if (rank < k) {
+        sm.w[rank] = comp_val(me);
+        sm.widx[rank] = comp_idx(me);
       }
     }
     __syncthreads();

@@ -12,25 +12,22 @@
 
 namespace sv {
 
-constexpr int kTkThreads = 512;
-constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kTkU = 4;
-constexpr int kTkWarpCap = 256;
-constexpr int kTkCap = kTkWarps * kTkWarpCap;
+constexpr int kTkCap = kMaxK;   // candidates >= tau held per row (more: the exact fallback)
+constexpr int kTkWarps = 256 / 32;
 
 struct TopkSmem {
-  unsigned long long cand[kTkCap];   // per-warp candidate buffers (warp w: [w*cap, (w+1)*cap))
-  unsigned long long sel[kMaxK];     // the row's top-k, descending
-  float w[kMaxK];                    // exp2 weights of the top-k, in rank order
-  int widx[kMaxK];
+  unsigned long long cand[kTkCap];   // candidates >= tau; the finisher's two-float weights
+  float w[kMaxK];                    // the row's top-k in rank order: logits, then exp2 weights
+  int widx[kMaxK];                   // and their token indices
   int sidx[kMaxK];                   // finisher: kept indices in token order
-  int wcount[kTkWarps];
+  int rel[256];                      // threads whose maximum reaches tau
   int ired[kTkWarps];
   float fu[kMaxG1];                  // finisher: uniforms and acceptance probabilities
   float fa[kMaxG1];
   LocateSmem loc;
   int flag;
   int count;
+  int nrel;
   int n;
   int status;
   int token;
@@ -38,6 +35,7 @@ struct TopkSmem {
   float WJ;
   float pd;
 };
+static_assert(sizeof(unsigned long long) * kTkCap >= sizeof(F2) * kMaxK, "finisher weights fit in cand");
 
 __device__ __forceinline__ int block_sum_int_n(int v, int* sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -80,7 +78,6 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   __syncthreads();
   // kept entries in token order; weights r_j = max(p_j - q_j, 0), or p_j
   F2* rs = reinterpret_cast<F2*>(sm.cand);
-  F2* ps = rs + kMaxK;
   for (int e = tid; e < J; e += nt) {
     const int me = sm.widx[e];
     int rank = 0;
@@ -89,7 +86,6 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
     const float r = resid ? fmaxf(__fsub_rn(pe, __ldg(qrow + me)), 0.f) : pe;
     sm.sidx[rank] = me;
     rs[rank] = F2{r, 0.f};
-    ps[rank] = F2{pe, 0.f};
   }
   __syncthreads();
   const float u = sm.fu[G];
@@ -98,7 +94,14 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   int status = sm.status;
   if (resid && !f2_pos(R)) {
     status |= SEQ_RESID0;   // zero residual mass (rounding only): draw from p_n
-    pos = locate(ps, J, u, &R, &base, &tgt, sm.loc, false);
+    for (int e = tid; e < J; e += nt) {
+      const int me = sm.widx[e];
+      int rank = 0;
+      for (int j = 0; j < J; ++j) rank += sm.widx[j] < me;
+      rs[rank] = F2{sm.w[e], 0.f};
+    }
+    __syncthreads();
+    pos = locate(rs, J, u, &R, &base, &tgt, sm.loc, false);
   }
   if (tid == 0) {
     int tok = pos >= 0 ? sm.sidx[pos] : (J > 0 ? sm.sidx[0] : 0);
@@ -117,7 +120,8 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
 }
 
 // Per-row epilogue of the top-k path: softmax(./T) over the row's top-k (in
-// sm.sel[0, kk), descending), the top-p cut with two-float sums, the kept
+// sm.w / sm.widx [0, kk), descending by (logit, -index)), the top-p cut with
+// two-float sums, the kept
 // (index, probability) list written to rowres[r], and the acceptance
 // probability of the row's draft (d_row, q_row prefetched by thread 0).
 __device__ void topk_row_epilogue(const Params& p, int b, int i, int r, int kk, bool bad_nan, int d_row,
@@ -125,12 +129,10 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int r, int kk, 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
   const int G = p.gamma, V = p.V, k = p.top_k;
     // ---- softmax(./T) over the top-k, then the top-p cut (two-float sums)
-    const float m0 = kk > 0 ? comp_val(sm.sel[0]) : -INFINITY;
+    const float m0 = kk > 0 ? sm.w[0] : -INFINITY;
     const bool bad = bad_nan || !(m0 > -INFINITY && m0 < INFINITY);
-    for (int e = tid; e < kk; e += nt) {
-      sm.w[e] = bad ? 0.f : exp2f((comp_val(sm.sel[e]) - m0) * p.c);
-      sm.widx[e] = comp_idx(sm.sel[e]);
-    }
+    __syncthreads();   // every thread has read w[0]
+    for (int e = tid; e < kk; e += nt) sm.w[e] = bad ? 0.f : exp2f((sm.w[e] - m0) * p.c);
     __syncthreads();
     if (warp == 0) {
       F2 W{0.f, 0.f};
