@@ -204,6 +204,7 @@ bool plan_cluster(const sv::Params& p, sv_dtype dt, int mode, sv::ClusterParams*
   cp->CN = CN;
   cp->W = W;
   cp->NS = NS;
+  cp->EPT = NS * VW;
   *smem = sm;
   return true;
 }

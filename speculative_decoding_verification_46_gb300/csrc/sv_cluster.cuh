@@ -12,14 +12,15 @@
 //     argmax) into a per-row partial in the CTA's shared memory;
 //   * after a cluster barrier every CTA reads the CN partials of each row
 //     through distributed shared memory, merges them in rank order (so all
-//     CTAs hold identical row statistics), gathers l(d_i) and q(d_i) from the
-//     owning CTA and runs the acceptance scan;
-//   * sampling: each CTA sums the residual max(p_n - q_n, 0) (or p_gamma) over
-//     its slice in 256-vector sub-ranges; after a second barrier the CTAs read
-//     all sub-range masses, agree on the sub-range holding the inverse-CDF
-//     step, and its owner walks it thread -> element with the same float32
-//     partials.  A last barrier keeps every CTA's shared memory alive until
-//     the others have finished reading it.
+//     CTAs hold identical row statistics) and runs the acceptance scan (the
+//     drafts' l(d_i), q(d_i) were loaded at the start);
+//   * sampling: each thread sums (S, A, Q) of its run of the final-draw row
+//     (residual max(p_n - q_n, 0), or p_gamma) and keeps them in registers;
+//     after a second barrier warp 0 of every CTA reads the CN slice sums,
+//     forms the exact normaliser and agrees on the slice holding the
+//     inverse-CDF step; its owner goes thread -> token with the same sums.
+//     A last barrier keeps every CTA's shared memory alive until the others
+//     have finished reading it.
 //
 // The barriers are hardware cluster barriers (barrier.cluster): every CTA of
 // the cluster arrives at each of them unconditionally, so none can wait on a
@@ -35,13 +36,14 @@ namespace sv {
 namespace cg = cooperative_groups;
 
 constexpr int kClusterMax = 16;
-constexpr int kClusterMaxNS = 8;   // 256-vector sub-ranges per CTA slice
+constexpr int kClusterMaxNS = 8;   // vectors per thread for a whole slice (final-draw runs <= 64 tokens)
 
 struct ClusterParams {
   Params p;
   int CN;      // CTAs per cluster
   int W;       // slice width in elements (multiple of the vector width)
-  int NS;      // sub-ranges of 256 vectors per slice
+  int NS;      // vectors per thread for a whole slice (ceil(W / VW / 256))
+  int EPT;     // final draw: tokens per thread run (NS * VW)
 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -55,28 +57,28 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 struct ClusterSmem {
   float4 part[kMaxG1];       // this CTA's per-row partial: (max, s_hi, s_lo) or (max, index)
   float ur[kMaxG1];          // this sequence's uniforms
-  F2x3 sub3[kClusterMaxNS];                // this CTA's (S, A, Q) per sub-range
-  F2 allmass[kClusterMax * kClusterMaxNS]; // every CTA's masses, in index order
-  F2 allS[kClusterMax * kClusterMaxNS];
-  float allQ[kClusterMax * kClusterMaxNS];
+  F2x3 sub3;                     // this CTA's (S, A, Q) of the final-draw row
   F2x3 red[kWarps];
   F2 ds;
   float M[kMaxG1];
   double S[kMaxG1];
   float a[kMaxG1];
   int g[kMaxG1];
-  int st[kMaxG1];
-  int bad[kMaxG1];
+  int st[kMaxG1];          // per-row status bits
+  int dr[kMaxG1];          // drafts with their logit and q value
+  float dl[kMaxG1];
+  float dq[kMaxG1];
   F2 f2red[kWarps];
   int n;
   int status;
   int use_p;
   int owner;      // rank owning the inverse-CDF step (-1 none)
-  int sub;
+  int othread;    // thread of the owner whose run holds it
+  int lastpos;    // last thread with a positive mass
   int token;
   F2 base;
   F2 target;
-  LocateSmem loc;
+  F2 tbase;       // the owning thread's exclusive prefix
 };
 
 // Merge the CN partials of row i held by lanes [0, CN) of a 16-lane group.
@@ -109,6 +111,38 @@ __device__ __forceinline__ float4 group_merge(float4 v, int CN, float c) {
     s = f2_add(s, o);
   }
   return make_float4(M, s.hi, s.lo, 0.f);
+}
+
+// (S, A, Q) of one thread's run of the final-draw row held in shared memory
+// (len tokens, a multiple of VW; q = nullptr for the bonus row): the tail
+// tokens in one sweep, the tokens near the maximum (bits of `top`) after.
+template <typename T>
+__device__ __forceinline__ void cluster_run(const T* L, const float* Q, int len, bool use_q, float M, float c,
+                                            float c_lo, float s_a, RunAcc* acc) {
+  constexpr int VW = Tr<T>::VW;
+  constexpr bool EXACT = sizeof(T) == 2;
+  uint64_t top = 0ull;
+  for (int j = 0; j * VW < len; ++j) {
+    const uint4 v = *reinterpret_cast<const uint4*>(L + j * VW);
+    float qv[VW];
+#pragma unroll
+    for (int h = 0; h < VW / 4; ++h) {
+      const float4 q4 = Q ? *reinterpret_cast<const float4*>(Q + j * VW + 4 * h) : make_float4(0.f, 0.f, 0.f, 0.f);
+      qv[4 * h + 0] = q4.x;
+      qv[4 * h + 1] = q4.y;
+      qv[4 * h + 2] = q4.z;
+      qv[4 * h + 3] = q4.w;
+    }
+#pragma unroll
+    for (int t = 0; t < VW; ++t)
+      if (run_tail<EXACT>(*acc, Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a)) top |= 1ull << (j * VW + t);
+  }
+  while (top) {
+    const int o = __ffsll((long long)top) - 1;
+    top &= top - 1;
+    const float x = Tr<T>::get(*reinterpret_cast<const uint4*>(L + (o / VW) * VW), o % VW);
+    run_top<EXACT>(*acc, x, Q ? Q[o] : 0.f, use_q, M, c, c_lo, s_a);
+  }
 }
 
 template <typename T, int MODE>
@@ -161,6 +195,11 @@ cluster_kernel(const ClusterParams cp) {
   }
   if (MODE == MODE_SOFTMAX && tid < G1) u_own = __ldg(p.uniforms + b * G1 + tid);
   if (tid < G1) sm.ur[tid] = u_own;
+  if (tid < G) {
+    sm.dr[tid] = d_own;
+    sm.dl[tid] = l_own;
+    sm.dq[tid] = q_own;
+  }
   cp_async_wait<1>();
   __syncthreads();
 
@@ -215,7 +254,8 @@ cluster_kernel(const ClusterParams cp) {
   }
   cluster.sync();
 
-  // ---- merge the CN partials of every row (16 lanes per row), then the scan
+  // ---- merge the CN partials of every row (16 lanes per row); the merging
+  // lane also forms the row's acceptance test, then warp 0 runs the scan
   for (int base = 0; base < G1; base += 2 * kWarps) {
     const int i = base + (tid >> 4);
     const bool rowok = i < G1;
@@ -224,66 +264,60 @@ cluster_kernel(const ClusterParams cp) {
     if (rowok && r < CN) v = *cluster.map_shared_rank(&sm.part[i], r);
     const float4 mg = group_merge<MODE>(v, CN, p.c);
     if (rowok && r == 0) {
+      int st = 0;
+      const int d = i < G ? sm.dr[i] : 0;
+      if (i < G && (d < 0 || d >= V)) st |= SEQ_OOB;
       if (MODE == MODE_GREEDY) {
         const bool nan = mg.x != mg.x;
         const int bi = __float_as_int(mg.y);
         sm.g[i] = (nan || bi == 0x7fffffff) ? 0 : bi;
-        sm.bad[i] = nan;
+        if (nan) st |= SEQ_BADROW;
       } else {
-        const double s = (double)mg.y + (double)mg.z;
+        const double sd = (double)mg.y + (double)mg.z;
+        const bool badrow = !(mg.x > -INFINITY && mg.x < INFINITY) || !(sd > 0.0 && sd < 1e300);
         sm.M[i] = mg.x;
-        sm.S[i] = s;
-        sm.bad[i] = !(mg.x > -INFINITY && mg.x < INFINITY) || !(s > 0.0 && s < 1e300);
+        sm.S[i] = sd;
+        if (badrow) st |= SEQ_BADROW;
+        if (i < G) {
+          float a = 0.f;
+          if (d >= 0 && d < V) {
+            const float pd = badrow ? 0.f : exp2f((sm.dl[i] - mg.x) * p.c) / (float)sd;
+            const float qd = sm.dq[i];
+            if (qd > 0.0f) {
+              a = fminf(1.f, pd / qd);
+            } else {
+              a = pd > 0.f ? 1.f : 0.f;
+              st |= SEQ_QBAD;
+            }
+          }
+          sm.a[i] = a;
+        }
       }
+      sm.st[i] = st;
     }
   }
   __syncthreads();
-  if (MODE == MODE_SOFTMAX && tid < G) {
-    const int d = d_own;
-    float a = 0.f;
-    int st = 0;
-    if (d < 0 || d >= V) {
-      st |= SEQ_OOB;
-    } else {
-      const float l = l_own;
-      const float qd = q_own;
-      const float pd = sm.bad[tid] ? 0.f : exp2f((l - sm.M[tid]) * p.c) / (float)sm.S[tid];
-      if (qd > 0.0f) {
-        a = fminf(1.f, pd / qd);
-      } else {
-        a = pd > 0.f ? 1.f : 0.f;
-        st |= SEQ_QBAD;
-      }
-    }
-    sm.a[tid] = a;
-    sm.st[tid] = st;
-  }
-  __syncthreads();
-  if (tid == 0) {
+  if (warp == 0) {
     int status = 0, n = G;
-    for (int i = 0; i < G1; ++i)
-      if (sm.bad[i]) status |= SEQ_BADROW;
-    if (MODE == MODE_GREEDY) {
-      for (int i = 0; i < G; ++i) {
-        const int d = p.draft[b * G + i];
-        if (d < 0 || d >= V) status |= SEQ_OOB;
-      }
-      for (int i = 0; i < G; ++i)
-        if (p.draft[b * G + i] != sm.g[i]) { n = i; break; }
-      sm.token = sm.g[n];
-    } else {
-      for (int i = 0; i < G; ++i) status |= sm.st[i];
-      for (int i = 0; i < G; ++i)
-        if (!(sm.ur[i] < sm.a[i])) { n = i; break; }
+    for (int c0 = 0; c0 < G1; c0 += 32) {
+      const int i = c0 + lane;
+      if (i < G1) status |= sm.st[i];
+      const bool rej = i < G && (MODE == MODE_GREEDY ? sm.dr[i] != sm.g[i] : !(sm.ur[i] < sm.a[i]));
+      const unsigned rb = __ballot_sync(0xffffffffu, rej);
+      if (rb && n == G) n = c0 + __ffs(rb) - 1;
     }
-    sm.n = n;
-    sm.status = status;
+    status = __reduce_or_sync(0xffffffffu, status);
+    if (lane == 0) {
+      sm.n = n;
+      sm.status = status;
+      if (MODE == MODE_GREEDY) sm.token = sm.g[n];
+    }
   }
   __syncthreads();
   const int n = sm.n;
   if (rank == 0) {
     for (int j = tid; j < G1; j += kThreads) {
-      if (j < n) p.out_tokens[b * G1 + j] = p.draft[b * G + j];
+      if (j < n) p.out_tokens[b * G1 + j] = sm.dr[j];
       else if (j > n) p.out_tokens[b * G1 + j] = -1;
       else if (MODE == MODE_GREEDY) p.out_tokens[b * G1 + j] = sm.token;
     }
@@ -300,124 +334,136 @@ cluster_kernel(const ClusterParams cp) {
   }
 
   // ---- final draw: residual of row n, or the bonus from row gamma
-  // (precise weights and the (S, A, Q) decomposition, as in residual_kernel)
+  // (precise weights and the (S, A, Q) decomposition, as in residual_kernel;
+  // thread t of a CTA owns the run of EPT tokens at t * EPT of its slice)
   const bool resid = n < G;
   const bool bad = (sm.status & SEQ_BADROW) != 0;
   const T* Lf = Ls + (size_t)n * W;
   const float* Qf = resid ? Qs + (size_t)n * W : nullptr;
   const float M = sm.M[n];
   const float s_a = (float)sm.S[n];
-  const int NS = cp.NS;
+  const int EPT = cp.EPT;
+  const int r0 = tid * EPT;
+  const int rlen = min(EPT, max(v1 - v0 - r0, 0));   // a multiple of VW
   int status = sm.status;
   cp_async_wait<0>();     // this thread's q copies have landed
   __syncthreads();        // ... and every thread's are visible to all
-#pragma unroll
-  for (int j = 0; j < kClusterMaxNS; ++j) {
-    if (j < NS) {
-      SlotRun run;
-      run.zero();
-      const int k = j * kThreads + tid;
-      if (k < nvec && !bad) {
-        const uint4 v = *reinterpret_cast<const uint4*>(Lf + k * VW);
-        float qv[VW];
-#pragma unroll
-        for (int t = 0; t < VW; ++t) qv[t] = resid ? Qf[k * VW + t] : 0.f;
-        run = slot_run<T>(v, qv, VW, resid, M, p.c, p.c_lo, s_a);
-      }
-      const F2x3 t = block_sum_f2x3(F2x3{run.S(), run.A(), F2{run.q, 0.f}}, sm.red);
-      if (tid == 0) sm.sub3[j] = t;
-    }
+  // this thread's run sums stay in registers: the owner walks them again below
+  RunAcc acc;
+  acc.zero();
+  if (!bad) cluster_run<T>(Lf + r0, Qf ? Qf + r0 : nullptr, rlen, resid, M, p.c, p.c_lo, s_a, &acc);
+  {
+    const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
+    if (tid == 0) sm.sub3 = t;
   }
   cluster.sync();
-  // every CTA: the exact normaliser and the masses of all CN * NS sub-ranges
-  F2 sl{0.f, 0.f};
-  for (int e = tid; e < CN * NS; e += kThreads) {
-    const F2x3 r3 = *cluster.map_shared_rank(&sm.sub3[e % NS], e / NS);
-    sm.allS[e] = r3.a;
-    sm.allmass[e] = r3.b;                 // A; corrected below once s is known
-    sl = f2_add(sl, r3.a);
-    sm.allQ[e] = r3.c.hi;
-  }
-  const F2 s = block_sum_f2(sl, sm.f2red);
-  const F2 ds = f2_add(s, F2{-s_a, 0.f});
-  for (int e = tid; e < CN * NS; e += kThreads) {
-    if (resid) {
-      F2 m = f2_add(sm.allmass[e], f2_neg(f2_scale(ds, sm.allQ[e])));
-      if (m.hi < 0.f) m = F2{0.f, 0.f};
-      sm.allmass[e] = m;
-    } else {
-      sm.allmass[e] = sm.allS[e];
+  // warp 0 of every CTA: the exact normaliser s, the masses of the CN slices
+  // (lane r = rank r) and the inverse-CDF step: the first slice whose
+  // interval [prefix, prefix + mass) holds u * R (R = the total); if rounding
+  // leaves none, the last slice with positive mass
+  if (warp == 0) {
+    F2 S_l{0.f, 0.f}, m_l{0.f, 0.f};
+    float Q_l = 0.f;
+    if (lane < CN) {
+      const F2x3 r3 = *cluster.map_shared_rank(&sm.sub3, lane);
+      S_l = r3.a;
+      m_l = r3.b;
+      Q_l = r3.c.hi;
     }
-  }
-  __syncthreads();
-  {
-    const float u = sm.ur[G];
-    F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
+    const F2 sinc = warp_incl_scan_f2(S_l);
+    const F2 s = F2{__shfl_sync(0xffffffffu, sinc.hi, 31), __shfl_sync(0xffffffffu, sinc.lo, 31)};
+    const F2 ds = f2_add(s, F2{-s_a, 0.f});          // s - s', tiny
     bool use_q = resid;
-    int sub = locate(sm.allmass, CN * NS, u, &R, &base, &tgt, sm.loc, false);
+    if (resid) {
+      m_l = f2_add(m_l, f2_neg(f2_scale(ds, Q_l)));
+      if (m_l.hi < 0.f) m_l = F2{0.f, 0.f};
+    } else {
+      m_l = S_l;
+    }
+    F2 inc = warp_incl_scan_f2(m_l);
+    F2 R = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
     if (resid && !bad && !f2_pos(R)) {
       // zero residual mass (only through rounding): draw from p_n instead
       status |= SEQ_RESID0;
       use_q = false;
-      sub = locate(sm.allS, CN * NS, u, &R, &base, &tgt, sm.loc, false);
+      m_l = S_l;
+      inc = sinc;
+      R = s;
     }
-    if (tid == 0) {
-      if (bad || !f2_pos(R)) sub = -1;
-      sm.owner = sub < 0 ? -1 : sub / NS;
-      sm.sub = sub < 0 ? -1 : sub % NS;
+    const F2 tgt = f2_scale(R, sm.ur[G]);
+    F2 excl = f2_shfl_up(inc, 1);
+    if (lane == 0) excl = F2{0.f, 0.f};
+    const bool live = lane < CN && f2_pos(m_l);
+    const unsigned hit = __ballot_sync(0xffffffffu, live && !f2_lt(tgt, excl) && f2_lt(tgt, f2_add(excl, m_l)));
+    const unsigned any = __ballot_sync(0xffffffffu, live);
+    int sub = hit ? __ffs(hit) - 1 : (any ? 31 - __clz(any) : -1);
+    if (bad || !f2_pos(R)) sub = -1;
+    const int src = sub < 0 ? 0 : sub;
+    const F2 base{__shfl_sync(0xffffffffu, excl.hi, src), __shfl_sync(0xffffffffu, excl.lo, src)};
+    if (lane == 0) {
+      sm.owner = sub;
       sm.base = base;
       sm.target = tgt;
       sm.token = -1;
       sm.use_p = use_q ? 0 : 1;
       sm.ds = ds;
+      sm.othread = 0x7fffffff;
+      sm.lastpos = -1;
+      sm.status = status;
     }
   }
   __syncthreads();
+  status = sm.status;
   // every remote read of this CTA is done: arrive now, wait before leaving
   // (no CTA may exit while others can still read its shared memory)
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   if (sm.owner == rank) {
     const bool uq = sm.use_p == 0;
-    const int k = sm.sub * kThreads + tid;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    float qv[VW];
-#pragma unroll
-    for (int t = 0; t < VW; ++t) qv[t] = 0.f;
-    F2 mine{0.f, 0.f};
-    if (k < nvec) {
-      v = *reinterpret_cast<const uint4*>(Lf + k * VW);
-#pragma unroll
-      for (int t = 0; t < VW; ++t) qv[t] = uq ? Qf[k * VW + t] : 0.f;
-      mine = slot_run<T>(v, qv, VW, uq, M, p.c, p.c_lo, s_a).mass(uq, sm.ds);
-      if (mine.hi < 0.f) mine = F2{0.f, 0.f};
-    }
+    F2 mine = acc.mass(uq, sm.ds);
+    if (mine.hi < 0.f) mine = F2{0.f, 0.f};
     F2 total;
     const F2 ex = block_exclusive_f2(mine, sm.f2red, &total);
     const F2 tb = f2_add(sm.base, ex);
-    int lastp = -1;
-    if (k < nvec && f2_pos(mine) && !f2_lt(sm.target, tb) && f2_lt(sm.target, f2_add(tb, mine))) {
-      const int f = slot_find<T>(v, qv, VW, uq, M, p.c, p.c_lo, s_a, sm.ds, tb, sm.target, &lastp);
-      if (f >= 0) sm.token = v0 + k * VW + f;
+    const bool pos = f2_pos(mine);
+    if (pos && !f2_lt(sm.target, tb) && f2_lt(sm.target, f2_add(tb, mine))) atomicMin(&sm.othread, tid);
+    if (pos) atomicMax(&sm.lastpos, tid);
+    __syncthreads();
+    // rounding can leave no run above the target: take the last positive one
+    const bool take_last = sm.othread == 0x7fffffff;
+    const int owner_t = take_last ? sm.lastpos : sm.othread;
+    if (tid == owner_t) sm.tbase = tb;
+    __syncthreads();
+    if (owner_t >= 0 && tid < 32) {
+      // warp 0 walks the owning run, 32 tokens at a time
+      const int o0 = owner_t * EPT;
+      const int olen = min(EPT, max(v1 - v0 - o0, 0));
+      F2 carry = sm.tbase;
+      int pick = -1, lastp = -1;
+      for (int c0 = 0; c0 < olen && pick < 0; c0 += 32) {
+        const int e = o0 + c0 + lane;
+        F2 m{0.f, 0.f};
+        if (c0 + lane < olen) {
+          const float x = TR::get(*reinterpret_cast<const uint4*>(Lf + (e / VW) * VW), e % VW);
+          const float qv = uq ? Qf[e] : 0.f;
+          m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
+        }
+        const F2 inc = warp_incl_scan_f2(m);
+        F2 excl = f2_shfl_up(inc, 1);
+        if (lane == 0) excl = F2{0.f, 0.f};
+        const F2 lb = f2_add(carry, excl);
+        const bool live = f2_pos(m);
+        const unsigned hit = __ballot_sync(0xffffffffu, live && !take_last && !f2_lt(sm.target, lb) &&
+                                                            f2_lt(sm.target, f2_add(lb, m)));
+        const unsigned any = __ballot_sync(0xffffffffu, live);
+        if (hit) pick = c0 + __ffs(hit) - 1;
+        if (any) lastp = c0 + 31 - __clz(any);
+        const F2 tot = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+        carry = f2_add(carry, tot);
+      }
+      if (pick < 0) pick = lastp;
+      if (lane == 0) sm.token = pick >= 0 ? v0 + o0 + pick : -1;
     }
     __syncthreads();
-    if (sm.token < 0) {
-      int m = -1;
-      if (k < nvec) {
-        int lp = -1;
-        slot_find<T>(v, qv, VW, uq, M, p.c, p.c_lo, s_a, sm.ds, F2{0.f, 0.f}, F2{INFINITY, 0.f}, &lp);
-        if (lp >= 0) m = v0 + k * VW + lp;
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) sm.st[warp] = m;
-      __syncthreads();
-      if (tid == 0) {
-        int mm = -1;
-        for (int w = 0; w < kWarps; ++w) mm = max(mm, sm.st[w]);
-        sm.token = mm;
-      }
-      __syncthreads();
-    }
     if (tid == 0) {
       p.out_tokens[b * G1 + n] = sm.token < 0 ? 0 : sm.token;
       if (p.out_status) p.out_status[b] = status;

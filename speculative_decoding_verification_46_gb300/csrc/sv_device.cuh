@@ -1196,73 +1196,6 @@ rows_kernel(const Params p) {
   finish_sequence_topk(p, b, sm);
 }
 
-// Weight 2^((x - M) c) of one token of the final-draw row, c = log2(e) / T
-// given as (c, c_lo).  The exponent is formed in two-float (x - M exactly,
-// times c + c_lo).  Tokens within 2^-8 of the row maximum ("top" tokens carry
-// most of the mass, so their rounding would shift every later CDF step) get
-// the two-float exp2 in *wt and the function returns true; the rest get
-// exp2f with a first-order correction for the exponent's low part in *wf.
-// -inf logits weigh 0; NaN propagates (such rows are flagged, not drawn).
-__device__ __forceinline__ bool tok_weight(float x, float M, float c, float c_lo, F2* wt, float* wf) {
-  if (x == -INFINITY) {
-    *wf = 0.f;
-    return false;
-  }
-  const float dh = x - M;
-  const float bb = dh - x;
-  const float dl = (x - (dh - bb)) + (-M - bb);   // x - M = dh + dl exactly
-  const float p = dh * c;
-  float e = fmaf(dh, c, -p);
-  e = fmaf(dh, c_lo, e);
-  e = fmaf(dl, c, e);
-  if (p > -8.f) {
-    *wt = exp2_f2(f2_norm(p, e));
-    return true;
-  }
-  const float y = exp2f(p);
-  *wf = fmaf(y * 6.931471825e-01f, e, y);
-  return false;
-}
-
-// Running sums of one thread over one slot of the final-draw row, in token
-// order.  S: all weights; A: the residual max(w - s' q, 0) over the support
-// {w > s' q} with the row-statistics kernel's float normaliser s'; Q: q over
-// the same support.  Top tokens add in two-float, the others in float.  The
-// exact residual mass is A - (s - s') Q once the exact normaliser s is known.
-struct SlotRun {
-  F2 s_top, a_top;
-  float s_tail, a_tail, q;
-  __device__ __forceinline__ void zero() {
-    s_top = a_top = F2{0.f, 0.f};
-    s_tail = a_tail = q = 0.f;
-  }
-  __device__ __forceinline__ void add(float x, float qv, bool use_q, float M, float c, float c_lo, float s_a) {
-    F2 wt;
-    float wf;
-    if (tok_weight(x, M, c, c_lo, &wt, &wf)) {
-      s_top = f2_add(s_top, wt);
-      if (use_q && wt.hi > s_a * qv) {
-        const float pr = s_a * qv;
-        const F2 sq = f2_norm(pr, fmaf(s_a, qv, -pr));
-        a_top = f2_add(a_top, f2_add(wt, f2_neg(sq)));
-        q += qv;
-      }
-    } else {
-      s_tail += wf;
-      if (use_q && wf > s_a * qv) {
-        a_tail += fmaf(-s_a, qv, wf);
-        q += qv;
-      }
-    }
-  }
-  __device__ __forceinline__ F2 S() const { return f2_add(s_top, F2{s_tail, 0.f}); }
-  __device__ __forceinline__ F2 A() const { return f2_add(a_top, F2{a_tail, 0.f}); }
-  // the value the inverse CDF walks: S (bonus / fallback to p) or A - ds Q
-  __device__ __forceinline__ F2 mass(bool resid, F2 ds) const {
-    return resid ? f2_add(A(), f2_neg(f2_scale(ds, q))) : S();
-  }
-};
-
 // Three two-float block sums in one pass (one pair of barriers).
 struct F2x3 {
   F2 a, b, c;
@@ -1289,17 +1222,18 @@ __device__ __forceinline__ F2x3 block_sum_f2x3(F2x3 v, F2x3* sm) {
 
 // ------------------------------------------------------------------ final draw
 //
-// Slot helpers (used by the cluster kernel, whose CTA slices are read as
-// "slots": slot j of thread t holds elements (j*256 + t)*VW + [0, VW) of the
-// slice, so each warp-wide 16-byte load is coalesced; slot j of all threads is
-// one contiguous sub-range of the vocabulary).  The residual kernel further
-// down gives each thread a run of consecutive tokens instead.
+// Both final-draw paths (residual_kernel below, and the cluster kernel) give
+// each thread a run of consecutive tokens, so the inverse-CDF search goes
+// (chunk or CTA slice) -> thread -> token, every level contiguous in token
+// order.
 //
 // Precision.  This is the one row per sequence whose inverse CDF is compared
-// step by step with a float64 reference over up to ~10^5 steps, so token
-// weights come from tok_weight() (two-float exponent; two-float exp2 for the
-// tokens that carry the mass) and the running sums keep those in two-float
-// (SlotRun).  The residual max(p - q, 0) = max(w - s q, 0) / s is kept
+// step by step with a float64 reference over up to ~10^5 steps.  A token's
+// weight 2^((x - M) c) takes its exponent in two-float; the tokens within
+// 2^-8 of the row maximum (they carry most of the mass, so their rounding
+// would shift every later CDF step) get the two-float exp2, the rest
+// ex2.approx with a first-order correction for the exponent's low part; all
+// running sums are two-float (RunAcc).  The residual max(p - q, 0) = max(w - s q, 0) / s is kept
 // unnormalised (the inverse CDF does not change under scaling).  Each
 // sub-range reports (S, A, Q) - the sum of its weights, and over its residual
 // support {w > s' q} (s' the row-statistics kernel's float normaliser) the sum
@@ -1307,76 +1241,6 @@ __device__ __forceinline__ F2x3 block_sum_f2x3(F2x3 v, F2x3* sm) {
 // the masses A - (s - s') Q: no second pass, and no cancellation, since
 // s - s' is tiny.  Tokens whose support membership s' and s would decide
 // differently have |w - s q| < 1e-6 w and contribute nothing measurable.
-
-// One slot of the final-draw row from global memory: VW logits and (for a
-// residual) the VW q values.
-template <typename T>
-__device__ __forceinline__ void load_final_slot(const T* row, const float* qrow, int e0, int nv, bool vec_ok,
-                                                uint4* v, float* qv) {
-  constexpr int VW = Tr<T>::VW;
-  *v = load_slot<T>(row, e0, nv, vec_ok);
-  if (qrow) {
-    if (nv == VW && vec_ok) {
-#pragma unroll
-      for (int h = 0; h < VW; h += 4) {
-        const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow + e0 + h));
-        qv[h] = q4.x; qv[h + 1] = q4.y; qv[h + 2] = q4.z; qv[h + 3] = q4.w;
-      }
-    } else {
-#pragma unroll
-      for (int t = 0; t < VW; ++t) qv[t] = t < nv ? __ldg(qrow + e0 + t) : 0.f;
-    }
-  } else {
-#pragma unroll
-    for (int t = 0; t < VW; ++t) qv[t] = 0.f;
-  }
-}
-
-// Running sums over the first nv tokens of one loaded slot.
-template <typename T>
-__device__ __forceinline__ SlotRun slot_run(const uint4& v, const float* qv, int nv, bool use_q, float M, float c,
-                                            float c_lo, float s_a) {
-  constexpr int VW = Tr<T>::VW;
-  SlotRun r;
-  r.zero();
-#pragma unroll
-  for (int t = 0; t < VW; ++t)
-    if (t < nv) r.add(Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a);
-  return r;
-}
-
-// The same running sums, stopping at the first token where base + the walked
-// value exceeds target (returns its offset in the slot, or -1); *last is the
-// last token with a positive increment.
-template <typename T>
-__device__ __forceinline__ int slot_find(const uint4& v, const float* qv, int nv, bool use_q, float M, float c,
-                                         float c_lo, float s_a, F2 ds, F2 base, F2 target, int* last) {
-  constexpr int VW = Tr<T>::VW;
-  SlotRun r;
-  r.zero();
-  F2 prev{0.f, 0.f};
-  int found = -1, lastp = -1;
-#pragma unroll
-  for (int t = 0; t < VW; ++t) {
-    if (t < nv) {
-      r.add(Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a);
-      const F2 cur = r.mass(use_q, ds);
-      if (f2_lt(prev, cur)) lastp = t;
-      if (found < 0 && f2_lt(target, f2_add(base, cur))) found = t;
-      prev = cur;
-    }
-  }
-  *last = lastp;
-  return found;
-}
-
-// ---- residual kernel: per-thread runs
-//
-// Element order.  A chunk of CL = 256 * EPT tokens is split into 256 runs of
-// EPT consecutive tokens, run t to thread t, so the inverse-CDF search goes
-// chunk -> thread -> token with every level contiguous in token order.  A
-// thread's EPT / VW vector loads are adjacent in memory (the first one of a
-// run brings the line the others hit in L1).
 
 // (S, A, Q) of one thread's run (see "Precision" above), two-float with the
 // error of every addition collected in the low words.
@@ -1389,6 +1253,7 @@ struct RunAcc {
     l += ((h - (s - bb)) + (x - bb)) + xl;
     h = s;
   }
+  // a weight near the maximum (two-float), its residual formed exactly
   __device__ __forceinline__ void add(F2 w, float qv, bool use_q, float s_a) {
     acc2(sh, sl, w.hi, w.lo);
     if (use_q) {
@@ -1410,30 +1275,38 @@ struct RunAcc {
   }
 };
 
-// Adds one token of the final-draw row to a run: the weight 2^((x - M) c)
-// as in tok_weight (two-float exponent; near the maximum the two-float exp2),
-// the residual part on the support {w > s' q}.  Tail weights carry exp2f's
-// rounding already, so their residual w - s' q takes a single rounding (fma);
-// near the maximum it is formed exactly.  run_tail handles a tail token and
-// returns false, or returns true and adds nothing for a token near the
-// maximum, which run_top then adds.
+// The exponent (x - M) c of one token as p + e: x - M is exact for 16-bit
+// logits (EXACT_DIFF); for float32 its rounding error is kept (two-diff).  A
+// weight whose p is not above -1e30 (x = -inf, or an exponent that overflows)
+// is 0.
+template <bool EXACT_DIFF>
 __device__ __forceinline__ float tok_exponent(float x, float M, float c, float c_lo, float* e_out) {
   const float dh = x - M;
-  const float bb = dh - x;
-  const float dl = (x - (dh - bb)) + (-M - bb);   // x - M = dh + dl exactly
   const float p = dh * c;
   float e = fmaf(dh, c, -p);
   e = fmaf(dh, c_lo, e);
-  *e_out = fmaf(dl, c, e);
+  if (!EXACT_DIFF) {
+    const float bb = dh - x;
+    const float dl = (x - (dh - bb)) + (-M - bb);   // x - M = dh + dl exactly
+    e = fmaf(dl, c, e);
+  }
+  *e_out = e;
   return p;
 }
+
+// One token of the final-draw row: a tail token (p <= -8) is added here
+// (weight ex2.approx(p) with a first-order correction for e - on this range
+// ex2.approx.ftz.f32 and exp2f agree - and its residual w - s' q with one
+// rounding) and run_tail returns false; a token near the maximum is left to
+// run_top (two-float exp2, exact residual) and run_tail returns true.
+template <bool EXACT_DIFF>
 __device__ __forceinline__ bool run_tail(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
                                          float s_a) {
   float e;
-  const float p = tok_exponent(x, M, c, c_lo, &e);
+  const float p = tok_exponent<EXACT_DIFF>(x, M, c, c_lo, &e);
   const bool top = p > -8.f;
-  const float y = exp2f(p);
-  const float w = (top || x == -INFINITY) ? 0.f : fmaf(y * 6.931471825e-01f, e, y);
+  const float y = ex2_approx(p);   // results below 2^-126 flush to 0
+  const float w = (top || !(p > -1e30f)) ? 0.f : fmaf(y * 6.931471825e-01f, e, y);
   RunAcc::acc2(acc.sh, acc.sl, w, 0.f);
   if (use_q) {
     const float pr = s_a * qv;
@@ -1444,25 +1317,24 @@ __device__ __forceinline__ bool run_tail(RunAcc& acc, float x, float qv, bool us
   }
   return top;
 }
+template <bool EXACT_DIFF>
 __device__ __forceinline__ void run_top(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
                                         float s_a) {
   float e;
-  const float p = tok_exponent(x, M, c, c_lo, &e);
+  const float p = tok_exponent<EXACT_DIFF>(x, M, c, c_lo, &e);
   acc.add(exp2_f2(f2_norm(p, e)), qv, use_q, s_a);
 }
-__device__ __forceinline__ void run_add(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
-                                        float s_a) {
-  if (run_tail(acc, x, qv, use_q, M, c, c_lo, s_a)) run_top(acc, x, qv, use_q, M, c, c_lo, s_a);
-}
 
-// One token's increment of the walked mass, with run_add's arithmetic: the
+// One token's increment of the walked mass, with the run's arithmetic: the
 // weight w (bonus / fallback to p) or, on the residual support {w > s' q},
 // w - s' q - (s - s') q.
+template <bool EXACT_DIFF>
 __device__ __forceinline__ F2 token_mass(float x, float qv, bool use_q, float M, float c, float c_lo, float s_a,
                                          F2 ds) {
   RunAcc one;
   one.zero();
-  run_add(one, x, qv, use_q, M, c, c_lo, s_a);
+  if (run_tail<EXACT_DIFF>(one, x, qv, use_q, M, c, c_lo, s_a))
+    run_top<EXACT_DIFF>(one, x, qv, use_q, M, c, c_lo, s_a);
   F2 m = one.mass(use_q, ds);
   if (m.hi < 0.f) m = F2{0.f, 0.f};
   return m;
@@ -1492,6 +1364,7 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
                                                RunAcc* acc) {
   using RS = ResStage<T>;
   constexpr int VW = RS::VW;
+  constexpr bool EXACT = sizeof(T) == 2;
   const int tid = threadIdx.x;
   uint4* lg = stage;
   uint4* qq = stage + RS::NL * kThreads;
@@ -1542,7 +1415,8 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
     const int ev = e0 + j * VW;
 #pragma unroll
     for (int t = 0; t < VW; ++t)
-      if (ev + t < V && run_tail(*acc, Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a)) top |= 1u << (j * VW + t);
+      if (ev + t < V && run_tail<EXACT>(*acc, Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a))
+        top |= 1u << (j * VW + t);
   }
   while (top) {
     const int o = __ffs(top) - 1;   // offset in the run
@@ -1550,7 +1424,7 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
     const int j = o / VW, t = o - j * VW;
     const float x = Tr<T>::get(lg[j * kThreads + tid], t);
     const float qv = qrow ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3)) : 0.f;
-    run_top(*acc, x, qv, use_q, M, c, c_lo, s_a);
+    run_top<EXACT>(*acc, x, qv, use_q, M, c, c_lo, s_a);
   }
 }
 
@@ -1688,7 +1562,7 @@ residual_kernel(const Params p) {
       if (lane < EPT && e < V) {
         const float x = TR::get(load_slot<T>(row, e, 1, false), 0);
         const float qv = uq ? __ldg(qrow + e) : 0.f;
-        m = token_mass(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
+        m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
       }
       const F2 inc = warp_incl_scan_f2(m);
       F2 excl = f2_shfl_up(inc, 1);

@@ -16,10 +16,11 @@
 //   greedy   per-row argmax (ties -> lowest index; NaN flagged)
 //   softmax  per-row online max / sum of 2^((L - m) c) with rescaling when the
 //            running max grows; p(d_i) and a_i at the row's end
-//   top-k    pass 1 keeps per-thread maxima; the k-th largest is a lower
-//            bound tau of the row's k-th value; pass 2 re-reads (L2) only the
-//            elements of threads whose maximum reaches tau; exact rank
-//            selection of the candidates >= tau; softmax(./T) + top-p; a_i
+//   top-k    pass 1 keeps per-thread maxima (and the vector holding it); the
+//            k-th largest is a lower bound tau of the row's k-th value; only
+//            threads with a second vector reaching tau are re-read (L2);
+//            exact rank selection of the candidates >= tau; softmax(./T) +
+//            top-p; a_i
 //
 // The last row of a sequence to finish (atomic ticket, no waiting) runs the
 // acceptance scan.  Greedy and top-k also do the final draw there; softmax
@@ -369,12 +370,13 @@ stream_dense_kernel(const Params p) {
 
 // ---- top-k streaming kernel
 //
-// Pass 1 (the ring) keeps each thread's maximum.  tau = the k-th largest
-// thread maximum is a lower bound of the row's k-th largest value, and only
-// threads whose maximum reaches tau can hold elements >= tau: pass 2 re-reads
-// just those threads' elements (about k of the 256 threads; an L2 hit), the
-// work spread over the whole CTA.  The candidates (all elements >= tau) are
-// ranked exactly by (value desc, index asc).
+// Pass 1 (the ring) keeps each thread's maximum m1, the 16-byte vector that
+// holds it and m2, the largest maximum of its other vectors.  tau = the k-th
+// largest thread maximum is a lower bound of the row's k-th largest value.
+// Only threads with m1 >= tau hold elements >= tau; if m2 < tau they are all
+// in the kept vector.  The few threads with m2 >= tau too are re-read (pass 2,
+// an L2 hit, spread over the whole CTA).  The candidates (all elements >=
+// tau) are ranked exactly by (value desc, index asc).
 template <typename T>
 __global__ void __launch_bounds__(kSt, 3)
 stream_topk_kernel(const Params p) {
@@ -417,32 +419,58 @@ stream_topk_kernel(const Params p) {
       d_row = __ldg(p.draft + b * G + i);
       if (d_row >= 0 && d_row < V) q_row = __ldg(p.q + ((size_t)b * G + i) * V + d_row);
     }
-    // ---- pass 1 through the ring: thread maxima (NaN noted)
-    float tmax = -INFINITY;
+    // ---- pass 1 through the ring: per thread its maximum m1, the vector
+    // holding it (first such vector; kept in registers) and m2 = the largest
+    // maximum among its other vectors
+    float m1 = -INFINITY, m2 = -INFINITY;
+    uint4 bvec = make_uint4(0u, 0u, 0u, 0u);
+    int bv = -1;
     int nan_seen = 0;
     for (int c = 0; c < w.NCH; ++c) {
       cpa_wait<S - 1>();
       const uint4* slot = ring + (size_t)stage * U * kSt;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (c * w.CH + u * kSt + tid < w.NV) {
-          const float vm = TR::template vmax<true>(slot[u * kSt + tid]);
+        const int v = c * w.CH + u * kSt + tid;
+        if (v < w.NV) {
+          const uint4 x = slot[u * kSt + tid];
+          const float vm = TR::template vmax<true>(x);
           nan_seen |= (vm != vm);
-          tmax = fmaxf(tmax, vm);
+          m2 = fmaxf(m2, fminf(vm, m1));
+          if (vm > m1) {
+            m1 = vm;
+            bvec = x;
+            bv = v;
+          }
         }
       }
       iss.issue(ring, logits, V, w);
       stage = (stage + 1 == S) ? 0 : stage + 1;
     }
     // ---- tau: the k-th largest finite thread maximum (bisection on keys)
-    const uint32_t tkey = tmax > -INFINITY ? okey(tmax) : 0u;
+    const uint32_t tkey = m1 > -INFINITY ? okey(m1) : 0u;
     uint32_t K = 0u;
     for (int bit = 31; bit >= TR::KEY_LOW_BIT; --bit) {
       const uint32_t Kt = K | (1u << bit);
       if (__syncthreads_count(tkey >= Kt) >= k) K = Kt;
     }
     const float tau = K == 0u ? -INFINITY : key_to_float(K);
-    if (tmax > -INFINITY && tmax >= tau) sm.rel[atomicAdd(&sm.nrel, 1)] = tid;
+    // ---- candidates.  A thread with m1 >= tau and m2 < tau has all its
+    // elements >= tau in bvec; one with m2 >= tau too is re-read (pass 2).
+    if (m1 > -INFINITY && m1 >= tau) {
+      if (m2 > -INFINITY && m2 >= tau) {
+        sm.rel[atomicAdd(&sm.nrel, 1)] = tid;
+      } else {
+#pragma unroll
+        for (int t = 0; t < VW; ++t) {
+          const float xv = TR::get(bvec, t);
+          if (xv > -INFINITY && xv >= tau) {
+            const int pos = atomicAdd(&sm.count, 1);
+            if (pos < kTkCap) sm.cand[pos] = comp_key(xv, bv * VW + t);
+          }
+        }
+      }
+    }
     const int bad_nan = __syncthreads_or(nan_seen);
     // ---- pass 2 (L2): the elements >= tau of the listed threads
     {
