@@ -10,21 +10,25 @@
 //     of the step is in flight at once;
 //   * one warp per row reduces the slice (max / sum of 2^((L - m) c), or the
 //     argmax) into a per-row partial in the CTA's shared memory;
-//   * after a cluster barrier every CTA reads the CN partials of each row
-//     through distributed shared memory, merges them in rank order (so all
-//     CTAs hold identical row statistics) and runs the acceptance scan (the
-//     drafts' l(d_i), q(d_i) were loaded at the start);
+//   * every CTA pushes its partials to all CTAs of the cluster; after a
+//     cluster barrier each merges the CN partials of each row in rank order
+//     (so all CTAs hold identical row statistics) and runs the acceptance
+//     scan (the drafts' l(d_i), q(d_i) were loaded at the start);
 //   * sampling: each thread sums (S, A, Q) of its run of the final-draw row
 //     (residual max(p_n - q_n, 0), or p_gamma) and keeps them in registers;
-//     after a second barrier warp 0 of every CTA reads the CN slice sums,
-//     forms the exact normaliser and agrees on the slice holding the
-//     inverse-CDF step; its owner goes thread -> token with the same sums.
-//     A last barrier keeps every CTA's shared memory alive until the others
-//     have finished reading it.
+//     the CTA's slice sums are pushed to all CTAs; after a second barrier warp
+//     0 of every CTA forms the exact normaliser and agrees on the slice
+//     holding the inverse-CDF step; its owner goes thread -> token with the
+//     same sums.
 //
-// The barriers are hardware cluster barriers (barrier.cluster): every CTA of
-// the cluster arrives at each of them unconditionally, so none can wait on a
-// CTA that never arrives.
+// CTAs exchange data only by pushing it into each other's shared memory
+// (distributed shared memory stores) before a cluster barrier and reading
+// their own copy after it; no CTA reads another's shared memory, so a CTA may
+// leave once the last barrier it takes part in has passed.  The barriers are
+// hardware cluster barriers (barrier.cluster): every CTA of the cluster
+// arrives at each of them unconditionally, so none can wait on a CTA that
+// never arrives.  The first one (arrive at entry, wait before the first push)
+// makes sure every CTA of the cluster runs before any remote store.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -55,9 +59,10 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 struct ClusterSmem {
-  float4 part[kMaxG1];       // this CTA's per-row partial: (max, s_hi, s_lo) or (max, index)
+  float4 allpart[kClusterMax][kMaxG1];   // every CTA's per-row partial (pushed by its owner):
+                                         // (max, s_hi, s_lo) or (max, index)
   float ur[kMaxG1];          // this sequence's uniforms
-  F2x3 sub3;                     // this CTA's (S, A, Q) of the final-draw row
+  F2x3 allsub[kClusterMax];      // every CTA's (S, A, Q) of the final-draw row (pushed)
   F2x3 red[kWarps];
   F2 ds;
   float M[kMaxG1];
@@ -165,20 +170,25 @@ cluster_kernel(const ClusterParams cp) {
   const int v1 = min(v0 + W, V);
   const int nvec = max(v1 - v0, 0) / VW;               // vectors in this slice (V % VW == 0 on this path)
   float* Qs = reinterpret_cast<float*>(Ls + (size_t)G1 * W);
+  // distributed shared memory may only be written once every CTA of the
+  // cluster runs: arrive now, wait just before the first remote store
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // ---- issue every load of the step: logits slices, then q slices
   const T* Lg = static_cast<const T*>(p.logits) + (size_t)b * G1 * V;
-  for (int e = tid; e < G1 * nvec; e += kThreads) {
-    const int i = e / nvec, k = e - i * nvec;
-    cp_async16(Ls + (size_t)i * W + k * VW, Lg + (size_t)i * V + v0 + k * VW);
+  for (int i = 0; i < G1; ++i) {
+    const T* src = Lg + (size_t)i * V + v0;
+    T* dst = Ls + (size_t)i * W;
+    for (int k = tid; k < nvec; k += kThreads) cp_async16(dst + k * VW, src + k * VW);
   }
   cp_async_commit();
   const int nq = max(v1 - v0, 0) / 4;
   if (MODE == MODE_SOFTMAX) {
     const float* Qg = p.q + (size_t)b * G * V;
-    for (int e = tid; e < G * nq; e += kThreads) {
-      const int i = e / nq, k = e - i * nq;
-      cp_async16(Qs + (size_t)i * W + k * 4, Qg + (size_t)i * V + v0 + k * 4);
+    for (int i = 0; i < G; ++i) {
+      const float* src = Qg + (size_t)i * V + v0;
+      float* dst = Qs + (size_t)i * W;
+      for (int k = tid; k < nq; k += kThreads) cp_async16(dst + k * 4, src + k * 4);
     }
   }
   cp_async_commit();
@@ -203,6 +213,7 @@ cluster_kernel(const ClusterParams cp) {
   cp_async_wait<1>();
   __syncthreads();
 
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   // ---- per-row partials of this slice: one warp per row
   for (int i = warp; i < G1; i += kWarps) {
     const T* Lr = Ls + (size_t)i * W;
@@ -227,29 +238,27 @@ cluster_kernel(const ClusterParams cp) {
         const int oi = __shfl_xor_sync(0xffffffffu, bi, m);
         if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
       }
-      if (lane == 0) sm.part[i] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+      // push the row partial into every CTA of the cluster (lane r -> rank r)
+      if (lane < CN) *cluster.map_shared_rank(&sm.allpart[rank][i], lane) = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
     } else {
       float M = -INFINITY;
       for (int k = lane; k < nvec; k += 32)
         M = fmaxf(M, TR::template vmax<false>(*reinterpret_cast<const uint4*>(Lr + k * VW)));
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-      float a0 = 0.f, a1 = 0.f;
+      float a[4] = {0.f, 0.f, 0.f, 0.f};   // independent chains
       if (M > -INFINITY) {
         const float Mc = M * p.c;
         for (int k = lane; k < nvec; k += 32) {
           const uint4 v = *reinterpret_cast<const uint4*>(Lr + k * VW);
 #pragma unroll
-          for (int t = 0; t < VW; t += 2) {
-            a0 += ex2_approx(fmaf(TR::get(v, t), p.c, -Mc));
-            a1 += ex2_approx(fmaf(TR::get(v, t + 1), p.c, -Mc));
-          }
+          for (int t = 0; t < VW; ++t) a[t & 3] += ex2_approx(fmaf(TR::get(v, t), p.c, -Mc));
         }
       }
-      F2 s{a0 + a1, 0.f};
+      F2 s{(a[0] + a[1]) + (a[2] + a[3]), 0.f};
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) s = f2_add(s, f2_shfl_xor(s, m));
-      if (lane == 0) sm.part[i] = make_float4(M, s.hi, s.lo, 0.f);
+      if (lane < CN) *cluster.map_shared_rank(&sm.allpart[rank][i], lane) = make_float4(M, s.hi, s.lo, 0.f);
     }
   }
   cluster.sync();
@@ -261,7 +270,7 @@ cluster_kernel(const ClusterParams cp) {
     const bool rowok = i < G1;
     float4 v = make_float4(-INFINITY, 0.f, 0.f, 0.f);
     const int r = tid & 15;
-    if (rowok && r < CN) v = *cluster.map_shared_rank(&sm.part[i], r);
+    if (rowok && r < CN) v = sm.allpart[r][i];
     const float4 mg = group_merge<MODE>(v, CN, p.c);
     if (rowok && r == 0) {
       int st = 0;
@@ -329,8 +338,7 @@ cluster_kernel(const ClusterParams cp) {
     }
   }
   if (MODE == MODE_GREEDY) {
-    cluster.sync();   // no CTA leaves while others may still read its partials
-    return;
+    return;   // every remote access (the pushes) happened before the barrier
   }
 
   // ---- final draw: residual of row n, or the bonus from row gamma
@@ -354,7 +362,7 @@ cluster_kernel(const ClusterParams cp) {
   if (!bad) cluster_run<T>(Lf + r0, Qf ? Qf + r0 : nullptr, rlen, resid, M, p.c, p.c_lo, s_a, &acc);
   {
     const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
-    if (tid == 0) sm.sub3 = t;
+    if (tid < CN) *cluster.map_shared_rank(&sm.allsub[rank], tid) = t;
   }
   cluster.sync();
   // warp 0 of every CTA: the exact normaliser s, the masses of the CN slices
@@ -365,7 +373,7 @@ cluster_kernel(const ClusterParams cp) {
     F2 S_l{0.f, 0.f}, m_l{0.f, 0.f};
     float Q_l = 0.f;
     if (lane < CN) {
-      const F2x3 r3 = *cluster.map_shared_rank(&sm.sub3, lane);
+      const F2x3 r3 = sm.allsub[lane];
       S_l = r3.a;
       m_l = r3.b;
       Q_l = r3.c.hi;
@@ -414,9 +422,6 @@ cluster_kernel(const ClusterParams cp) {
   }
   __syncthreads();
   status = sm.status;
-  // every remote read of this CTA is done: arrive now, wait before leaving
-  // (no CTA may exit while others can still read its shared memory)
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   if (sm.owner == rank) {
     const bool uq = sm.use_p == 0;
     F2 mine = acc.mass(uq, sm.ds);
@@ -472,7 +477,6 @@ cluster_kernel(const ClusterParams cp) {
     p.out_tokens[b * G1 + n] = 0;
     if (p.out_status) p.out_status[b] = status;
   }
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace sv
