@@ -166,12 +166,28 @@ def inverse_cdf(weights, u):
     return v, boundary
 
 
+def deterministic_proposal(draft, V):
+    """q of a deterministic draft (n-gram / prompt lookup, [SD-notes] notes an
+    arbitrary drafting model M_q; [Ch11.1] §11.1.2 asks for the draft's actual
+    q): all mass on the drafted token, q_i = one-hot(d_i).  An out-of-range
+    draft gets no mass anywhere."""
+    draft = np.asarray(draft, dtype=np.int64)
+    B, G = draft.shape
+    q = np.zeros((B, G, V))
+    for b in range(B):
+        for i in range(G):
+            if 0 <= draft[b, i] < V:
+                q[b, i, draft[b, i]] = 1.0
+    return q
+
+
 def verify_sample(logits, q, draft, uniforms, temperature, top_k=0, top_p=1.0):
     """The sampling verify step for a batch, following listing 10-1 of [Ch11.1].
 
     logits   [B, gamma+1, V]  target logits (any float dtype holding the exact
                               values), row i predicts d_{i+1} (§11.1.1)
-    q        [B, gamma, V]    the draft's actual proposal probabilities
+    q        [B, gamma, V]    the draft's actual proposal probabilities, or None
+                              for a deterministic draft (q_i = one-hot at d_i)
     draft    [B, gamma]       drafted token ids
     uniforms [B, gamma+1]     U[b, i] accept test i, U[b, gamma] final draw
 
@@ -182,8 +198,13 @@ def verify_sample(logits, q, draft, uniforms, temperature, top_k=0, top_p=1.0):
     logits = np.asarray(logits)
     B, G1, V = logits.shape
     gamma = G1 - 1
-    q = np.zeros((B, 0, V)) if gamma == 0 else np.asarray(q)
     draft = np.asarray(draft, dtype=np.int64).reshape(B, gamma)
+    if gamma == 0:
+        q = np.zeros((B, 0, V))
+    elif q is None:
+        q = deterministic_proposal(draft, V)
+    else:
+        q = np.asarray(q)
     uniforms = np.asarray(uniforms, dtype=np.float32).reshape(B, G1)
 
     out = np.full((B, G1), -1, dtype=np.int64)

@@ -454,3 +454,78 @@ def test_expected_tokens_closed_form_matches_blog_numbers():
         # and the geometric series it sums: 1 + alpha + ... + alpha^gamma
         assert e == pytest.approx(sum(c["alpha"] ** j for j in range(c["gamma"] + 1)), rel=1e-14)
     assert not math.isclose(svref.expected_tokens_per_round(0.7, 4), 1 + 0.7 * 4)
+
+
+# ------------------------------------------------- deterministic drafts (q = None)
+
+def _oracle_law_deterministic(L, d, T):
+    """Exact law of the emitted sequence for one fixed deterministic draft d
+    (q passed as None), by integrating the uniforms through the oracle."""
+    G1, V = L.shape
+    G = G1 - 1
+    law = {}
+    one_minus = float(np.nextafter(np.float32(1), np.float32(0)))
+
+    def run(us):
+        res = svref.verify_sample(L[None], None, np.array([d]), np.array([us], dtype=np.float32), T)
+        return int(res["n_accepted"][0]), [int(t) for t in res["out_tokens"][0]]
+
+    reach = 1.0
+    for n in range(G1):
+        a_n = _threshold(lambda x: run([0.0] * n + [x] + [0.0] * (G - n))[0] > n) if n < G else 0.0
+        p_stop = 1.0 - a_n
+        if p_stop > 0.0:
+            stop = [one_minus] if n < G else []
+            below = 0.0
+            for v in range(V):
+                us = lambda x: [0.0] * n + stop + [0.0] * (G - n - len(stop)) + [x]
+                upto = _threshold(lambda x: run(us(x))[1][n] <= v)
+                if upto - below > 0.0:
+                    key = tuple(d[:n]) + (v,)
+                    law[key] = law.get(key, 0.0) + reach * p_stop * (upto - below)
+                below = upto
+        reach *= a_n
+    return law
+
+
+@pytest.mark.parametrize("V,G,T,seed", [(3, 1, 1.0, 5), (4, 2, 0.8, 6), (3, 3, 1.2, 7)])
+def test_deterministic_draft_law_closed_form(V, G, T, seed):
+    """q = one-hot(d_i): a_i = p_i(d_i) (min(1, p/1)), and a rejection at n
+    draws from p_n with d_n removed, renormalised (max(p - onehot, 0))."""
+    rng = np.random.default_rng(seed)
+    L = rng.normal(0, 1.5, size=(G + 1, V))
+    d = [int(x) for x in rng.integers(0, V, size=G)]
+    P = [scipy.special.softmax(L[i] / np.float64(np.float32(T))) for i in range(G + 1)]
+    ref = {}
+    reach = 1.0
+    for n in range(G + 1):
+        if n < G:
+            stop = 1.0 - P[n][d[n]]
+            for v in range(V):
+                if v != d[n] and P[n][v] > 0:
+                    ref[tuple(d[:n]) + (v,)] = reach * stop * P[n][v] / (1.0 - P[n][d[n]])
+            reach *= P[n][d[n]]
+        else:
+            for v in range(V):
+                ref[tuple(d) + (v,)] = reach * P[G][v]
+    law = _oracle_law_deterministic(L, d, T)
+    for k in set(law) | set(ref):
+        assert law.get(k, 0.0) == pytest.approx(ref.get(k, 0.0), abs=2e-6), k
+
+
+def test_deterministic_draft_accept_prob_is_target_prob():
+    rng = np.random.default_rng(11)
+    B, G, V, T = 5, 3, 50, 0.9
+    L = rng.normal(0, 2, size=(B, G + 1, V))
+    d = rng.integers(0, V, size=(B, G))
+    u = rng.random((B, G + 1)).astype(np.float32)
+    r = svref.verify_sample(L, None, d, u, T)
+    for b in range(B):
+        for i in range(G):
+            p = scipy.special.softmax(L[b, i] / np.float64(np.float32(T)))
+            assert r["accept_prob"][b, i] == pytest.approx(p[d[b, i]], rel=1e-12)
+    # a rejected position never re-emits its own draft
+    for b in range(B):
+        n = r["n_accepted"][b]
+        if n < G:
+            assert r["out_tokens"][b, n] != d[b, n]
