@@ -105,16 +105,18 @@ def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0):
     streaming kernel: every logit once, plus the gathers of l(d_i) and q(d_i);
     final-draw kernel (untruncated sampling): one row of logits per sequence,
     plus the q row of a rejected sequence.  With top-k the final draw reads
-    only the kept candidates' q values (inside the streaming kernel)."""
+    only the kept candidates' q values (inside the streaming kernel).
+    Deterministic drafts (q one-hot, passed as None) read no q bytes."""
     s = _elt_bytes(w)
     B, G, V = len(n_accepted), w.gamma, w.V
+    qb = 0 if w.deterministic else 4
     if w.mode == "greedy":
         return {"stream": B * (G + 1) * V * s, "final": 0}
-    stream = B * (G + 1) * V * s + B * G * (4 + s)
+    stream = B * (G + 1) * V * s + B * G * (qb + s)
     if w.top_k > 0 or w.top_p < 1.0:
-        return {"stream": stream + B * kept_per_row * 4, "final": 0}
+        return {"stream": stream + B * kept_per_row * qb, "final": 0}
     rejected = int((n_accepted < G).sum())
-    final = rejected * V * (4 + s) + (B - rejected) * V * s
+    final = rejected * V * (qb + s) + (B - rejected) * V * s
     return {"stream": stream, "final": final}
 
 
@@ -228,7 +230,7 @@ def run_gb300(args, rank, ws_n, local):
     B, G, V = w.B, w.gamma, w.V
     positions = B * (G + 1)
 
-    per_set = B * (G + 1) * V * _elt_bytes(w) + (B * G * V * 4 if w.mode == "sample" else 0)
+    per_set = B * (G + 1) * V * _elt_bytes(w) + (B * G * V * 4 if (w.mode == "sample" and not w.deterministic) else 0)
     n_sets = max(2, min(1024, math.ceil(2 * L2_BYTES / per_set) + 1))
     sets = _input_sets(w, n_sets, dev)
     outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
@@ -412,7 +414,7 @@ def other_workloads(args, local):
         if name == args.workload:
             continue
         B, G, V = w.B, w.gamma, w.V
-        per_set = B * (G + 1) * V * _elt_bytes(w) + (B * G * V * 4 if w.mode == "sample" else 0)
+        per_set = B * (G + 1) * V * _elt_bytes(w) + (B * G * V * 4 if (w.mode == "sample" and not w.deterministic) else 0)
         n_sets = max(2, min(512, math.ceil(2 * L2_BYTES / per_set) + 1))
         sets = _input_sets(w, n_sets, dev)
         outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
@@ -472,7 +474,8 @@ def oracle_throughput(w, budget_s: float, device="cpu"):
         if w.mode == "greedy":
             svref.verify_greedy(L[sl], d[sl])
         else:
-            svref.verify_sample(L[sl], q[sl], d[sl], u[sl], w.temperature, w.top_k, w.top_p)
+            svref.verify_sample(L[sl], q[sl] if q is not None else None, d[sl], u[sl], w.temperature, w.top_k,
+                                w.top_p)
         seqs += 1
         b = (b + 1) % w.B
         done = time.perf_counter() - t0
@@ -503,7 +506,8 @@ def main():
         if w.mode == "greedy":
             svref.verify_greedy(L[:1], d[:1])
         else:
-            svref.verify_sample(L[:1], q[:1], d[:1], u[:1], w.temperature, w.top_k, w.top_p)
+            svref.verify_sample(L[:1], q[:1] if q is not None else None, d[:1], u[:1], w.temperature, w.top_k,
+                                w.top_p)
         per_seq = time.perf_counter() - t0
         per_step_budget = min(2.0, 120.0 / max(1, steps + warmup))
         nseq = int(max(1, min(w.B, per_step_budget / max(per_seq, 1e-6))))

@@ -109,7 +109,12 @@ size_t sv_workspace_bytes(int B, int gamma, int V, int top_k);
  *   logits           [B][gamma+1][V] of logits_dtype; row i predicts the token
  *                    at draft position i, row gamma the bonus position
  *   q                [B][gamma][V] float32, the draft's actual proposal
- *                    probabilities (non-negative); may be NULL when gamma = 0
+ *                    probabilities (non-negative), 16-byte aligned; or NULL:
+ *                    deterministic drafts (n-gram, prompt lookup), each q_i
+ *                    one-hot at d_i.  Then a_i = p_i(d_i) and a rejection at
+ *                    i draws from p_i with d_i removed, renormalised; no q
+ *                    bytes are read.  (The pages use the draft's actual q,
+ *                    section 11.1.2; a one-hot q is that q for such drafts.)
  *   draft_tokens     [B][gamma] int32 drafted ids; may be NULL when gamma = 0
  *   uniforms         [B][gamma+1] float32 in [0, 1)
  *   temperature      > 0 and finite

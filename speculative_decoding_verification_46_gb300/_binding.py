@@ -161,9 +161,10 @@ def verify_sample(logits, q, draft, uniforms, temperature=1.0, top_k=0, top_p=1.
     """Speculative-sampling verify of a batch on the GPU.
 
     logits [B, gamma+1, V] (float32 / bfloat16 / float16), q [B, gamma, V]
-    float32, draft [B, gamma] int32, uniforms [B, gamma+1] float32, all CUDA
-    tensors.  Returns (out_tokens [B, gamma+1] int32, n_accepted [B] int32,
-    accept_prob [B, gamma] float32 or None, status [B] int32).
+    float32 (or None: deterministic drafts, q one-hot at each drafted token),
+    draft [B, gamma] int32, uniforms [B, gamma+1] float32, all CUDA tensors.
+    Returns (out_tokens [B, gamma+1] int32, n_accepted [B] int32, accept_prob
+    [B, gamma] float32 or None, status [B] int32).
     """
     B, G1, V = logits.shape
     G = G1 - 1

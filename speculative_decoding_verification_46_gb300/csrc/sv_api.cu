@@ -189,7 +189,8 @@ bool plan_cluster(const sv::Params& p, sv_dtype dt, int mode, sv::ClusterParams*
   const size_t sl = dt == SV_DTYPE_F32 ? 4 : 2;
   if (p.V % VW != 0) return false;
   const size_t G1 = (size_t)p.gamma + 1;
-  const size_t per_seq = G1 * p.V * sl + (mode == sv::MODE_SOFTMAX ? (size_t)p.gamma * p.V * 4 : 0);
+  const bool qrows = mode == sv::MODE_SOFTMAX && p.q != nullptr;   // q rows staged in shared memory
+  const size_t per_seq = G1 * p.V * sl + (qrows ? (size_t)p.gamma * p.V * 4 : 0);
   if (ov != 2 && (size_t)p.B * G1 * p.V * sl > kClusterMaxBytes) return false;
   int CN = (int)std::min<size_t>(sv::kClusterMax, std::max<size_t>(1, (per_seq + kClusterBytesPerCta - 1) / kClusterBytesPerCta));
   int W = (int)ceil_div(p.V, CN);
@@ -198,7 +199,7 @@ bool plan_cluster(const sv::Params& p, sv_dtype dt, int mode, sv::ClusterParams*
   const int NS = (int)ceil_div(W / VW, sv::kThreads);
   if (NS > sv::kClusterMaxNS) return false;
   const size_t sm = ((sizeof(sv::ClusterSmem) + 15) & ~size_t(15)) + G1 * W * sl +
-                    (mode == sv::MODE_SOFTMAX ? (size_t)p.gamma * W * 4 : 0);
+                    (qrows ? (size_t)p.gamma * W * 4 : 0);
   if (sm > kClusterMaxSmem) return false;
   cp->p = p;
   cp->CN = CN;
@@ -362,8 +363,8 @@ extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logit
   if (!(top_p > 0.0f && top_p <= 1.0f)) return SV_ERR_INVALID_ARG;
   if (B == 0) return SV_OK;
   if (!logits || !uniforms || !out_tokens || !out_num_accepted) return SV_ERR_INVALID_ARG;
-  if (gamma > 0 && (!q || !draft_tokens)) return SV_ERR_INVALID_ARG;
-  if (!aligned16(logits) || (gamma > 0 && !aligned16(q))) return SV_ERR_INVALID_ARG;
+  if (gamma > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;   // q == NULL: deterministic drafts
+  if (!aligned16(logits) || (q && !aligned16(q))) return SV_ERR_INVALID_ARG;
 
   // top-k below V, or top-p: the candidate-list path.  top-p without an
   // effective top-k ranks the whole vocabulary, supported for V <= SV_MAX_TOP_K.

@@ -119,11 +119,13 @@ __device__ __forceinline__ float4 group_merge(float4 v, int CN, float c) {
 }
 
 // (S, A, Q) of one thread's run of the final-draw row held in shared memory
-// (len tokens, a multiple of VW; q = nullptr for the bonus row): the tail
-// tokens in one sweep, the tokens near the maximum (bits of `top`) after.
+// (len tokens, a multiple of VW; q = nullptr for the bonus row or a
+// deterministic draft, whose one-hot q is infinite at run offset xq - so that
+// token is outside the residual support - and 0 elsewhere): the tail tokens
+// in one sweep, the tokens near the maximum (bits of `top`) after.
 template <typename T>
-__device__ __forceinline__ void cluster_run(const T* L, const float* Q, int len, bool use_q, float M, float c,
-                                            float c_lo, float s_a, RunAcc* acc) {
+__device__ __forceinline__ void cluster_run(const T* L, const float* Q, int xq, int len, bool use_q, float M,
+                                            float c, float c_lo, float s_a, RunAcc* acc) {
   constexpr int VW = Tr<T>::VW;
   constexpr bool EXACT = sizeof(T) == 2;
   uint64_t top = 0ull;
@@ -139,14 +141,16 @@ __device__ __forceinline__ void cluster_run(const T* L, const float* Q, int len,
       qv[4 * h + 3] = q4.w;
     }
 #pragma unroll
-    for (int t = 0; t < VW; ++t)
-      if (run_tail<EXACT>(*acc, Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a)) top |= 1ull << (j * VW + t);
+    for (int t = 0; t < VW; ++t) {
+      const float qt = (j * VW + t == xq) ? INFINITY : qv[t];
+      if (run_tail<EXACT>(*acc, Tr<T>::get(v, t), qt, use_q, M, c, c_lo, s_a)) top |= 1ull << (j * VW + t);
+    }
   }
   while (top) {
     const int o = __ffsll((long long)top) - 1;
     top &= top - 1;
     const float x = Tr<T>::get(*reinterpret_cast<const uint4*>(L + (o / VW) * VW), o % VW);
-    run_top<EXACT>(*acc, x, Q ? Q[o] : 0.f, use_q, M, c, c_lo, s_a);
+    run_top<EXACT>(*acc, x, o == xq ? INFINITY : (Q ? Q[o] : 0.f), use_q, M, c, c_lo, s_a);
   }
 }
 
@@ -183,7 +187,7 @@ cluster_kernel(const ClusterParams cp) {
   }
   cp_async_commit();
   const int nq = max(v1 - v0, 0) / 4;
-  if (MODE == MODE_SOFTMAX) {
+  if (MODE == MODE_SOFTMAX && p.q) {
     const float* Qg = p.q + (size_t)b * G * V;
     for (int i = 0; i < G; ++i) {
       const float* src = Qg + (size_t)i * V + v0;
@@ -200,7 +204,7 @@ cluster_kernel(const ClusterParams cp) {
     d_own = __ldg(p.draft + b * G + tid);
     if (d_own >= 0 && d_own < V) {
       l_own = Tr<T>::get(load_slot<T>(Lg + (size_t)tid * V, d_own, 1, false), 0);
-      if (MODE == MODE_SOFTMAX) q_own = __ldg(p.q + ((size_t)b * G + tid) * V + d_own);
+      if (MODE == MODE_SOFTMAX) q_own = p.q ? __ldg(p.q + ((size_t)b * G + tid) * V + d_own) : 1.f;
     }
   }
   if (MODE == MODE_SOFTMAX && tid < G1) u_own = __ldg(p.uniforms + b * G1 + tid);
@@ -347,7 +351,9 @@ cluster_kernel(const ClusterParams cp) {
   const bool resid = n < G;
   const bool bad = (sm.status & SEQ_BADROW) != 0;
   const T* Lf = Ls + (size_t)n * W;
-  const float* Qf = resid ? Qs + (size_t)n * W : nullptr;
+  const float* Qf = (resid && p.q) ? Qs + (size_t)n * W : nullptr;
+  // deterministic drafts (q == NULL): q_n is one-hot at d_n (slice index xq)
+  const int xq = (resid && !p.q) ? sm.dr[n] - v0 : -1;
   const float M = sm.M[n];
   const float s_a = (float)sm.S[n];
   const int EPT = cp.EPT;
@@ -359,7 +365,7 @@ cluster_kernel(const ClusterParams cp) {
   // this thread's run sums stay in registers: the owner walks them again below
   RunAcc acc;
   acc.zero();
-  if (!bad) cluster_run<T>(Lf + r0, Qf ? Qf + r0 : nullptr, rlen, resid, M, p.c, p.c_lo, s_a, &acc);
+  if (!bad) cluster_run<T>(Lf + r0, Qf ? Qf + r0 : nullptr, xq - r0, rlen, resid, M, p.c, p.c_lo, s_a, &acc);
   {
     const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
     if (tid < CN) *cluster.map_shared_rank(&sm.allsub[rank], tid) = t;
@@ -449,7 +455,7 @@ cluster_kernel(const ClusterParams cp) {
         F2 m{0.f, 0.f};
         if (c0 + lane < olen) {
           const float x = TR::get(*reinterpret_cast<const uint4*>(Lf + (e / VW) * VW), e % VW);
-          const float qv = uq ? Qf[e] : 0.f;
+          const float qv = uq ? (Qf ? Qf[e] : (e == xq ? INFINITY : 0.f)) : 0.f;
           m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
         }
         const F2 inc = warp_incl_scan_f2(m);

@@ -703,7 +703,7 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
           } else {
             const T* row = static_cast<const T*>(p.logits) + (size_t)rr * V;
             const float l = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
-            const float qd = __ldg(p.q + ((size_t)b * G + i) * V + d);
+            const float qd = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d) : 1.f;   // NULL: one-hot
             const float pd = bad ? 0.f : exp2f((l - M) * p.c) / (float)s;
             if (qd > 0.0f) {
               a = fminf(1.f, pd / qd);
@@ -868,7 +868,7 @@ __device__ void finish_row_topk(const Params& p, int b, int i, int rr, RowsSmem&
         st |= SEQ_OOB;
       } else {
         const double pd = sm.dred[0];
-        const float qd = __ldg(p.q + ((size_t)b * G + i) * V + d);
+        const float qd = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d) : 1.f;   // NULL: one-hot
         if (qd > 0.0f) {
           a = fmin(1.0, pd / (double)qd);
         } else {
@@ -903,7 +903,8 @@ __device__ void finish_sequence_topk(const Params& p, int b, RowsSmem& sm) {
   const int2* kept = p.rowres + (size_t)rr * (k + 1);
   const int J = __ldcg(kept).x;
   const bool resid = n < G;
-  const float* qrow = resid ? p.q + ((size_t)b * G + n) * V : nullptr;
+  const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
+  const int dn = (resid && !p.q) ? __ldg(p.draft + b * G + n) : -1;   // deterministic draft: q_n one-hot
   // r_j in index order: rank each kept entry by its index
   for (int e = tid; e < J; e += kThreads) {
     const int2 en = __ldcg(kept + 1 + e);
@@ -916,7 +917,7 @@ __device__ void finish_sequence_topk(const Params& p, int b, RowsSmem& sm) {
     int rank = 0;
     for (int j = 0; j < J; ++j) rank += sm.widx[j] < me;
     double r = sm.w[e];
-    if (resid) r = fmax(r - (double)__ldg(qrow + me), 0.0);
+    if (resid) r = fmax(r - (qrow ? (double)__ldg(qrow + me) : (me == dn ? 1.0 : 0.0)), 0.0);
     sm.mout[rank] = (unsigned long long)me;
     reinterpret_cast<double*>(sm.cand)[rank] = r;
   }
@@ -1359,7 +1360,8 @@ __device__ __forceinline__ void res_cp16(void* smem, const void* gmem) {
 // are skipped).  The whole run is copied into this thread's slots of `stage`
 // first (all copies in flight at once), then walked by a rolled loop.
 template <typename T>
-__device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, int e0, int NS, int V, bool vec_ok,
+__device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, int xq, int e0, int NS, int V,
+                                               bool vec_ok,
                                                bool use_q, float M, float c, float c_lo, float s_a, uint4* stage,
                                                RunAcc* acc) {
   using RS = ResStage<T>;
@@ -1414,16 +1416,20 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
     }
     const int ev = e0 + j * VW;
 #pragma unroll
-    for (int t = 0; t < VW; ++t)
-      if (ev + t < V && run_tail<EXACT>(*acc, Tr<T>::get(v, t), qv[t], use_q, M, c, c_lo, s_a))
+    for (int t = 0; t < VW; ++t) {
+      const float qt = (ev + t == xq) ? INFINITY : qv[t];
+      if (ev + t < V && run_tail<EXACT>(*acc, Tr<T>::get(v, t), qt, use_q, M, c, c_lo, s_a))
         top |= 1u << (j * VW + t);
+    }
   }
   while (top) {
     const int o = __ffs(top) - 1;   // offset in the run
     top &= top - 1;
     const int j = o / VW, t = o - j * VW;
     const float x = Tr<T>::get(lg[j * kThreads + tid], t);
-    const float qv = qrow ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3)) : 0.f;
+    const float qv = (e0 + o == xq) ? INFINITY
+                                    : (qrow ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3))
+                                            : 0.f);
     run_top<EXACT>(*acc, x, qv, use_q, M, c, c_lo, s_a);
   }
 }
@@ -1468,7 +1474,9 @@ residual_kernel(const Params p) {
   const bool resid = n < G;
   const bool bad = (st.status & SEQ_BADROW) != 0;
   const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
-  const float* qrow = resid ? p.q + ((size_t)b * G + n) * V : nullptr;
+  const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
+  // deterministic drafts (q == NULL): q_n is one-hot at d_n
+  const int xq = (resid && !p.q) ? __ldg(p.draft + b * G + n) : -1;
   const float M = st.M;
   const float s_a = (float)st.s;
   const bool vec_ok = (V % VW) == 0;
@@ -1481,7 +1489,7 @@ residual_kernel(const Params p) {
   RunAcc acc;
   acc.zero();
   if (!bad)
-    run_accumulate<T>(row, qrow, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc);
+    run_accumulate<T>(row, qrow, xq, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc);
   {
     const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
     if (tid == 0) {
@@ -1540,7 +1548,8 @@ residual_kernel(const Params p) {
     const int c0 = sm.sub * p.CL;
     RunAcc r;
     r.zero();
-    run_accumulate<T>(row, uq ? qrow : nullptr, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, stage, &r);
+    run_accumulate<T>(row, uq ? qrow : nullptr, xq, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, stage,
+                      &r);
     F2 mine = r.mass(uq, sm.ds);
     if (mine.hi < 0.f) mine = F2{0.f, 0.f};
     F2 total;
@@ -1561,7 +1570,7 @@ residual_kernel(const Params p) {
       F2 m{0.f, 0.f};
       if (lane < EPT && e < V) {
         const float x = TR::get(load_slot<T>(row, e, 1, false), 0);
-        const float qv = uq ? __ldg(qrow + e) : 0.f;
+        const float qv = uq ? (qrow ? __ldg(qrow + e) : (e == xq ? INFINITY : 0.f)) : 0.f;
         m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
       }
       const F2 inc = warp_incl_scan_f2(m);

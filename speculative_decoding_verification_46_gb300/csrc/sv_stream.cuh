@@ -253,7 +253,7 @@ stream_dense_kernel(const Params p) {
       d = __ldg(p.draft + b * G + i);
       if (d >= 0 && d < V) {
         l_d = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
-        q_d = __ldg(p.q + ((size_t)b * G + i) * V + d);
+        q_d = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d) : 1.f;   // NULL: one-hot draft
       }
     }
     float best = -INFINITY;          // greedy: this thread's max, its first index, NaN seen
@@ -417,7 +417,7 @@ stream_topk_kernel(const Params p) {
     float q_row = 0.f;
     if (tid == 0 && i < G) {
       d_row = __ldg(p.draft + b * G + i);
-      if (d_row >= 0 && d_row < V) q_row = __ldg(p.q + ((size_t)b * G + i) * V + d_row);
+      if (d_row >= 0 && d_row < V) q_row = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d_row) : 1.f;
     }
     // ---- pass 1 through the ring: per thread its maximum m1, the vector
     // holding it (first such vector; kept in registers) and m2 = the largest

@@ -69,7 +69,8 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   const int2* kept = p.rowres + (size_t)(b * G1 + n) * (k + 1);
   const int J = __ldcg(kept).x;
   const bool resid = n < G;
-  const float* qrow = resid ? p.q + ((size_t)b * G + n) * V : nullptr;
+  const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
+  const int dn = (resid && !p.q) ? __ldg(p.draft + b * G + n) : -1;   // deterministic draft: q_n one-hot
   for (int e = tid; e < J; e += nt) {
     const int2 en = __ldcg(kept + 1 + e);
     sm.widx[e] = en.x;
@@ -83,7 +84,8 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
     int rank = 0;
     for (int j = 0; j < J; ++j) rank += sm.widx[j] < me;
     const float pe = sm.w[e];
-    const float r = resid ? fmaxf(__fsub_rn(pe, __ldg(qrow + me)), 0.f) : pe;
+    const float qm = qrow ? __ldg(qrow + me) : (me == dn ? 1.f : 0.f);
+    const float r = resid ? fmaxf(__fsub_rn(pe, qm), 0.f) : pe;
     sm.sidx[rank] = me;
     rs[rank] = F2{r, 0.f};
   }

@@ -79,7 +79,7 @@ def _greedy(sv, **kw):
                                 dict(logits_dtype=7), dict(temperature=0.0), dict(temperature=-1.0),
                                 dict(temperature=float("inf")), dict(temperature=float("nan")), dict(top_k=-1),
                                 dict(top_k=1025), dict(top_p=0.0), dict(top_p=1.5), dict(top_p=float("nan")),
-                                dict(logits=None), dict(q=None), dict(draft_tokens=None), dict(uniforms=None),
+                                dict(logits=None), dict(draft_tokens=None), dict(uniforms=None),
                                 dict(out_tokens=None), dict(out_num_accepted=None), dict(logits=A + 2),
                                 dict(q=A + 4100)])
 def test_sample_rejects_invalid_arguments(sv, kw):
@@ -95,6 +95,8 @@ def test_sample_workspace_and_unsupported(sv):
     # gamma = 0 needs neither q nor drafts; B = 0 is an empty call
     assert _sample(sv, B=0) == sv.SV_OK
     assert _sample(sv, gamma=0, q=None, draft_tokens=None, workspace_bytes=16) == sv.SV_ERR_WORKSPACE
+    # q = NULL with gamma > 0 is valid (deterministic drafts): it reaches the workspace check
+    assert _sample(sv, q=None, workspace_bytes=16) == sv.SV_ERR_WORKSPACE
 
 
 @pytest.mark.parametrize("kw", [dict(B=-1), dict(gamma=-1), dict(V=0), dict(logits_dtype=3), dict(logits=None),

@@ -17,7 +17,7 @@ def test_shapes_and_support(name):
     assert inp["uniforms"].shape == (2, G + 1) and inp["uniforms"].dtype == torch.float32
     assert torch.all((inp["uniforms"] >= 0) & (inp["uniforms"] < 1))
     assert torch.all((inp["draft"] >= 0) & (inp["draft"] < V))
-    if w.mode == "greedy":
+    if w.mode == "greedy" or w.deterministic:
         assert inp["q"] is None
     else:
         q = inp["q"]

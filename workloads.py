@@ -48,6 +48,7 @@ class Workload:
     draft_scale: float = 1.0
     draft_sigma: float = 0.7
     seed: int = 0
+    deterministic: bool = False   # q = None: the drafter's guess argmax(target + noise)
 
     @property
     def rows(self) -> int:
@@ -63,7 +64,7 @@ class Workload:
 
 # The five workloads of the verify step (sizes and distributions as stated for
 # the step's headline measurements), plus the two other draft-noise levels of
-# the B=64 sweep.
+# the B=64 sweep and the deterministic-draft (q one-hot, passed as None) case.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -78,6 +79,8 @@ WORKLOADS = {
         Workload("sample_b64_g4_v128256_bf16_s1.5", 64, 4, 128256, "bf16", "sample", 1.0,
                  draft_sigma=1.5, seed=49),
         Workload("greedy_b512_g4_v128256_bf16", 512, 4, 128256, "bf16", "greedy", seed=50),
+        Workload("sample_det_b64_g4_v128256_bf16", 64, 4, 128256, "bf16", "sample", 1.0,
+                 draft_sigma=0.7, seed=52, deterministic=True),
         Workload("topk50_topp0.9_b256_g8_v152064_bf16", 256, 8, 152064, "bf16", "sample", 0.8,
                  top_k=50, top_p=0.9, draft_sigma=0.7, seed=51),
     ]
@@ -144,6 +147,12 @@ def make_inputs(w: Workload, seed: int | None = None, device="cpu", B: int | Non
         coin = torch.rand(B, G, generator=g, device=device) < 0.7
         rnd = torch.randint(0, w.V, (B, G), generator=g, device=device)
         draft = torch.where(coin, best, rnd)
+    elif w.deterministic:
+        # a deterministic drafter (n-gram / prompt lookup stand-in): its guess
+        # is the argmax of the target logits plus noise; q is one-hot (None)
+        guess = w.draft_scale * Lf + w.draft_sigma * torch.randn(B, G, w.V, generator=g, device=device)
+        draft = guess.argmax(dim=-1)
+        del guess
     else:
         q = _draft_proposal(w, Lf, g)
         if G > 0:
