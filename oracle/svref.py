@@ -311,3 +311,85 @@ def expected_tokens_per_round(alpha: float, gamma: int) -> float:
     if alpha == 1.0:
         return float(gamma + 1)
     return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)
+
+
+# ----------------------------------------------------------------- ragged rounds
+
+def verify_sample_ragged(logits, q, draft, uniforms, temperature, gamma_b, top_k=0, top_p=1.0):
+    """A ragged batch ([SD-notes] and the lmnt.cn blog §3.2 let gamma change
+    from round to round, per sequence): sequence b drafted only gamma_b[b] <=
+    gamma tokens.  Reading: b is then exactly the single-sequence step with
+    gamma = gamma_b[b] on its first gamma_b[b] + 1 logit rows, gamma_b[b] q
+    rows and drafts, and uniforms U[b, 0..gamma_b[b]] (U[b, gamma_b[b]] for
+    the final draw).  Rows and drafts beyond gamma_b[b] are not read.  Outputs
+    are padded to gamma + 1 with -1 (accept_prob with 0)."""
+    logits = np.asarray(logits)
+    B, G1, V = logits.shape
+    gamma = G1 - 1
+    draft = np.asarray(draft, dtype=np.int64).reshape(B, gamma)
+    uniforms = np.asarray(uniforms, dtype=np.float32).reshape(B, G1)
+    gamma_b = np.asarray(gamma_b, dtype=np.int64).reshape(B)
+    out = np.full((B, G1), -1, dtype=np.int64)
+    n_acc = np.zeros(B, dtype=np.int64)
+    acc_prob = np.zeros((B, gamma), dtype=np.float64)
+    status = np.zeros(B, dtype=np.int64)
+    boundary = np.zeros(B, dtype=bool)
+    for b in range(B):
+        g = int(gamma_b[b])
+        if not (0 <= g <= gamma):
+            raise ValueError("gamma_b must lie in [0, gamma]")
+        qb = None if q is None else np.asarray(q)[b:b + 1, :g]
+        r = verify_sample(logits[b:b + 1, :g + 1], qb, draft[b:b + 1, :g], uniforms[b:b + 1, :g + 1],
+                          temperature, top_k, top_p)
+        out[b, :g + 1] = r["out_tokens"][0]
+        n_acc[b] = r["n_accepted"][0]
+        acc_prob[b, :g] = r["accept_prob"][0]
+        status[b] = r["status"][0]
+        boundary[b] = r["boundary"][0]
+    return dict(out_tokens=out, n_accepted=n_acc, accept_prob=acc_prob, status=status, boundary=boundary)
+
+
+def verify_greedy_ragged(logits, draft, gamma_b):
+    """Greedy verify of a ragged batch, with the same reading as
+    verify_sample_ragged."""
+    logits = np.asarray(logits)
+    B, G1, V = logits.shape
+    gamma = G1 - 1
+    draft = np.asarray(draft, dtype=np.int64).reshape(B, gamma)
+    gamma_b = np.asarray(gamma_b, dtype=np.int64).reshape(B)
+    out = np.full((B, G1), -1, dtype=np.int64)
+    n_acc = np.zeros(B, dtype=np.int64)
+    status = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        g = int(gamma_b[b])
+        if not (0 <= g <= gamma):
+            raise ValueError("gamma_b must lie in [0, gamma]")
+        r = verify_greedy(logits[b:b + 1, :g + 1], draft[b:b + 1, :g])
+        out[b, :g + 1] = r["out_tokens"][0]
+        n_acc[b] = r["n_accepted"][0]
+        status[b] = r["status"][0]
+    return dict(out_tokens=out, n_accepted=n_acc, status=status)
+
+
+def truncate_emitted(out_tokens, n_accepted, stop_tokens=(), max_new=None):
+    """End a round early ([Ch11.1] listing 10-1's comment: EOS / stop tokens
+    and max_new_tokens may end the round, and no bonus is forced): the round
+    emitted out_tokens[b, :n_b + 1]; keep them up to and including the first
+    stop token, and at most max_new[b] of them.  Returns (tokens [B, gamma+1]
+    with -1 after the cut, num_emitted [B])."""
+    tok = np.array(out_tokens, dtype=np.int64, copy=True)
+    n = np.asarray(n_accepted, dtype=np.int64)
+    B, G1 = tok.shape
+    stops = set(int(s) for s in stop_tokens)
+    emitted = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        k = int(n[b]) + 1
+        for j in range(k):
+            if int(tok[b, j]) in stops:
+                k = j + 1
+                break
+        if max_new is not None:
+            k = min(k, max(int(max_new[b]), 0))
+        tok[b, k:] = -1
+        emitted[b] = k
+    return tok, emitted

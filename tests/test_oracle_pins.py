@@ -529,3 +529,115 @@ def test_deterministic_draft_accept_prob_is_target_prob():
         n = r["n_accepted"][b]
         if n < G:
             assert r["out_tokens"][b, n] != d[b, n]
+
+
+# ------------------------------------------------------------- ragged rounds
+
+def test_ragged_with_full_gamma_is_the_plain_step():
+    rng = np.random.default_rng(21)
+    B, G, V = 6, 4, 30
+    L = rng.normal(0, 2, size=(B, G + 1, V))
+    q = rng.dirichlet(np.ones(V), size=(B, G))
+    d = np.array([[rng.choice(V, p=q[b, i]) for i in range(G)] for b in range(B)])
+    u = rng.random((B, G + 1)).astype(np.float32)
+    a = svref.verify_sample(L, q, d, u, 0.9)
+    r = svref.verify_sample_ragged(L, q, d, u, 0.9, [G] * B)
+    for k in ("out_tokens", "n_accepted", "status"):
+        np.testing.assert_array_equal(a[k], r[k])
+    np.testing.assert_allclose(a["accept_prob"], r["accept_prob"], rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("V,g,T,seed", [(3, 1, 1.0, 31), (2, 0, 0.8, 32), (3, 2, 1.1, 33)])
+def test_ragged_sequence_law_is_the_theorem_law_for_its_gamma(V, g, T, seed):
+    """One sequence of a batch padded to gamma = 3 that drafted only g tokens:
+    its emitted law is the theorem's law for gamma = g on its first g + 1 rows
+    (rows and uniforms beyond are filled with junk that must not matter)."""
+    G = 3
+    rng = np.random.default_rng(seed)
+    L = rng.normal(0, 1.5, size=(G + 1, V))
+    L[g + 1:] = rng.normal(0, 50, size=(G - g, V))          # junk rows beyond gamma_b
+    q = rng.dirichlet(np.ones(V), size=G).astype(np.float32)
+    law = {}
+    one_minus = float(np.nextafter(np.float32(1), np.float32(0)))
+
+    def run(d, us):
+        res = svref.verify_sample_ragged(L[None], q[None], np.array([list(d) + [0] * (G - g)]),
+                                         np.array([us + [0.5] * (G - g)], dtype=np.float32), T, [g])
+        return int(res["n_accepted"][0]), [int(t) for t in res["out_tokens"][0]]
+
+    for d in itertools.product(range(V), repeat=g):
+        wd = float(np.prod([q[i, d[i]] for i in range(g)])) if g else 1.0
+        reach = 1.0
+        for n in range(g + 1):
+            a_n = _threshold(lambda x: run(d, [0.0] * n + [x] + [0.0] * (g - n))[0] > n) if n < g else 0.0
+            p_stop = 1.0 - a_n
+            if p_stop > 0.0:
+                stop = [one_minus] if n < g else []
+                below = 0.0
+                for v in range(V):
+                    us = lambda x: [0.0] * n + stop + [0.0] * (g - n - len(stop)) + [x]
+                    upto = _threshold(lambda x: run(d, us(x))[1][n] <= v)
+                    if upto - below > 0.0:
+                        key = tuple(d[:n]) + (v,)
+                        law[key] = law.get(key, 0.0) + wd * reach * p_stop * (upto - below)
+                    below = upto
+            reach *= a_n
+    ref = _theorem_law(L[:g + 1], q[:g], T)
+    for k in set(law) | set(ref):
+        assert law.get(k, 0.0) == pytest.approx(ref.get(k, 0.0), abs=2e-6), k
+
+
+def test_ragged_ignores_rows_and_drafts_beyond_gamma_b():
+    rng = np.random.default_rng(41)
+    B, G, V = 4, 4, 20
+    L = rng.normal(0, 1, size=(B, G + 1, V))
+    q = rng.dirichlet(np.ones(V), size=(B, G))
+    d = rng.integers(0, V, size=(B, G))
+    u = rng.random((B, G + 1)).astype(np.float32)
+    gb = np.array([2, 0, 4, 1])
+    L2, d2 = L.copy(), d.copy()
+    for b in range(B):
+        L2[b, gb[b] + 1:] = np.nan          # would flag a bad row if read
+        d2[b, gb[b]:] = V + 5              # would flag an out-of-range draft if read
+    a = svref.verify_sample_ragged(L, q, d, u, 1.0, gb)
+    r = svref.verify_sample_ragged(L2, q, d2, u, 1.0, gb)
+    for k in ("out_tokens", "n_accepted", "status"):
+        np.testing.assert_array_equal(a[k], r[k])
+    assert np.all(r["status"] == 0)
+    assert np.all(r["n_accepted"] <= gb)
+    assert np.all(r["out_tokens"][np.arange(G + 1)[None, :] > gb[:, None]] == -1)
+    g = svref.verify_greedy_ragged(L2, d2, gb)
+    for b in range(B):
+        gg = int(gb[b])
+        best = [int(np.argmax(L[b, i])) for i in range(gg + 1)]
+        n = next((i for i in range(gg) if d[b, i] != best[i]), gg)
+        assert g["n_accepted"][b] == n
+        assert list(g["out_tokens"][b, :n + 1]) == [int(x) for x in d[b, :n]] + [best[n]]
+        assert g["status"][b] == 0
+
+
+def test_truncate_emitted_is_the_longest_valid_prefix():
+    """Brute force: the kept length is the largest k such that every kept
+    token was emitted (k <= n + 1), no stop token precedes the k-th, and k <=
+    max_new."""
+    rng = np.random.default_rng(51)
+    B, G = 200, 6
+    tok = rng.integers(0, 8, size=(B, G + 1))
+    n = rng.integers(0, G + 1, size=B)
+    for b in range(B):
+        tok[b, n[b] + 1:] = -1
+    stops = [3, 6]
+    max_new = rng.integers(0, G + 3, size=B)
+    t, e = svref.truncate_emitted(tok, n, stops, max_new)
+    for b in range(B):
+        best = 0
+        for k in range(0, G + 2):
+            ok = k <= n[b] + 1 and k <= max_new[b] and all(tok[b, j] not in stops for j in range(max(k - 1, 0)))
+            if ok:
+                best = k
+        assert e[b] == best, b
+        assert list(t[b, :best]) == list(tok[b, :best]) and np.all(t[b, best:] == -1)
+    # no stops and a large budget: nothing changes
+    t2, e2 = svref.truncate_emitted(tok, n, (), None)
+    np.testing.assert_array_equal(t2, tok)
+    np.testing.assert_array_equal(e2, n + 1)
