@@ -99,23 +99,26 @@ def _elt_bytes(w):
     return {"f32": 4, "bf16": 2, "f16": 2}[w.dtype]
 
 
-def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0):
+def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0, gamma_b=None):
     """Bytes the method must move for one step, split by kernel.
 
     streaming kernel: every logit once, plus the gathers of l(d_i) and q(d_i);
     final-draw kernel (untruncated sampling): one row of logits per sequence,
     plus the q row of a rejected sequence.  With top-k the final draw reads
     only the kept candidates' q values (inside the streaming kernel).
-    Deterministic drafts (q one-hot, passed as None) read no q bytes."""
+    Deterministic drafts (q one-hot, passed as None) read no q bytes.  A
+    ragged round (gamma_b given) needs only rows 0..gamma_b of each sequence."""
     s = _elt_bytes(w)
     B, G, V = len(n_accepted), w.gamma, w.V
     qb = 0 if w.deterministic else 4
+    gsum = int(np.sum(gamma_b)) if gamma_b is not None else B * G
     if w.mode == "greedy":
-        return {"stream": B * (G + 1) * V * s, "final": 0}
-    stream = B * (G + 1) * V * s + B * G * (qb + s)
+        return {"stream": (gsum + B) * V * s, "final": 0}
+    stream = (gsum + B) * V * s + gsum * (qb + s)
     if w.top_k > 0 or w.top_p < 1.0:
         return {"stream": stream + B * kept_per_row * qb, "final": 0}
-    rejected = int((n_accepted < G).sum())
+    gb = np.asarray(gamma_b) if gamma_b is not None else np.full(B, G)
+    rejected = int((n_accepted < gb).sum())
     final = rejected * V * (qb + s) + (B - rejected) * V * s
     return {"stream": stream, "final": final}
 
@@ -206,7 +209,8 @@ def _input_sets(w, n_sets: int, device):
     sets = []
     for i in range(n_sets):
         sl = slice(i * w.B, (i + 1) * w.B)
-        sets.append({k: (v[sl] if v is not None else None) for k, v in big.items()})
+        # stop_tokens is one list for the batch, everything else per sequence
+        sets.append({k: (v[sl] if v is not None and k != "stop_tokens" else v) for k, v in big.items()})
     return sets
 
 
@@ -214,8 +218,12 @@ def _call(sv, w, inp, out, ws, stream):
     if w.mode == "greedy":
         return sv.verify_greedy(inp["logits"], inp["draft"], workspace=ws, stream=stream,
                                 outputs=(out[0], out[1], out[3]))
-    return sv.verify_sample(inp["logits"], inp["q"], inp["draft"], inp["uniforms"], w.temperature, w.top_k,
-                            w.top_p, workspace=ws, stream=stream, outputs=out)
+    r = sv.verify_sample(inp["logits"], inp["q"], inp["draft"], inp["uniforms"], w.temperature, w.top_k,
+                         w.top_p, workspace=ws, stream=stream, outputs=out, gamma_b=inp.get("gamma_b"))
+    if w.ragged:
+        # end the round at stop tokens / token budgets (one more kernel)
+        sv.truncate_emitted(r[0], r[1], inp["stop_tokens"], inp["max_new"], stream=stream)
+    return r
 
 
 def run_gb300(args, rank, ws_n, local):
@@ -246,7 +254,7 @@ def run_gb300(args, rank, ws_n, local):
             _call(sv, w, sets[i], outs[i], wsp, stream)
     torch.cuda.synchronize()
     kernel_names = sv.sv_last_kernels()      # what one call launches (the path the library chose)
-    kernels_per_call = len(kernel_names)
+    kernels_per_call = len(kernel_names) + (1 if w.ragged else 0)   # + the truncation kernel
     if kernels_per_call == 0:
         raise RuntimeError("the verify call launched no kernel")
     t0 = time.perf_counter()
@@ -314,16 +322,21 @@ def run_gb300(args, rank, ws_n, local):
         sv.sv_set_timing_events(None)
     torch.cuda.synchronize()
     t_stream = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) * 1e-3
-    t_final = float(np.mean([e[1].elapsed_time(e[2]) for e in evs])) * 1e-3 if kernels_per_call == 2 else 0.0
+    t_final = float(np.mean([e[1].elapsed_time(e[2]) for e in evs])) * 1e-3 if len(kernel_names) == 2 else 0.0
     kernel_us = {kernel_names[0]: t_stream * 1e6}
-    if kernels_per_call == 2:
+    if len(kernel_names) == 2:
         kernel_us[kernel_names[1]] = t_final * 1e6
 
     # algorithmic bytes: average over the input sets (the final draw depends on the data)
     nacc = np.concatenate([o[1].cpu().numpy() for o in outs])
-    ab = algorithmic_bytes(w, nacc)
+    gbs = np.concatenate([st["gamma_b"].cpu().numpy() for st in sets]) if w.ragged else None
+    ab = algorithmic_bytes(w, nacc, gamma_b=gbs)
+    if w.ragged:
+        # a ragged round verifies sum_b (gamma_b + 1) positions (mean over the input sets)
+        positions = float(np.sum(gbs)) / n_sets + B
+        value = positions * ws_n / (ms_max / 1e3)
     ab = {k: v / n_sets for k, v in ab.items()}
-    if kernels_per_call == 1:
+    if len(kernel_names) == 1:
         # one kernel does the whole step (its final draw included)
         ab = {"stream": ab["stream"] + ab["final"], "final": 0.0}
     peak, peak_kind = _peaks()
@@ -364,6 +377,7 @@ def run_gb300(args, rank, ws_n, local):
         f1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, ws_n, dev)
+    pos_e2e = float((sets[0]["gamma_b"].sum() + B).item()) if w.ragged else positions   # the input set used
 
     line = {
         "metric": METRIC,
@@ -393,7 +407,7 @@ def run_gb300(args, rank, ws_n, local):
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "kernel_us": kernel_us,
-        "e2e": {"value": positions * ws_n / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": pos_e2e * ws_n / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": steps * kernels_per_call,
         "clocks": clk,
@@ -447,9 +461,11 @@ def other_workloads(args, local):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / (reps * n_sets)
         nacc = np.concatenate([o[1].cpu().numpy() for o in outs])
-        ab = algorithmic_bytes(w, nacc)
+        gb_all = np.concatenate([st["gamma_b"].cpu().numpy() for st in sets]) if w.ragged else None
+        ab = algorithmic_bytes(w, nacc, gamma_b=gb_all)
         gbs = (ab["stream"] + ab["final"]) / n_sets / (ms / 1e3) / 1e9
-        out[name] = {"value": B * (G + 1) / (ms / 1e3), "ms_per_step": ms, "hbm_gbs": gbs,
+        pos = (float(np.sum(gb_all)) / n_sets + B) if w.ragged else B * (G + 1)   # positions in the round
+        out[name] = {"value": pos / (ms / 1e3), "ms_per_step": ms, "hbm_gbs": gbs,
                      "frac_of_measured_peak": gbs / peak, "steps": reps * n_sets}
         del sets, outs, wsp, graph
         torch.cuda.empty_cache()
@@ -466,6 +482,9 @@ def oracle_throughput(w, budget_s: float, device="cpu"):
     d = inp["draft"].cpu().numpy()
     u = inp["uniforms"].cpu().numpy()
     q = inp["q"].cpu().numpy() if inp["q"] is not None else None
+    gbh = inp["gamma_b"].cpu().numpy() if w.ragged else None
+    stops = inp["stop_tokens"].cpu().numpy() if w.ragged else None
+    mxh = inp["max_new"].cpu().numpy() if w.ragged else None
     done, seqs = 0.0, 0
     t0 = time.perf_counter()
     b = 0
@@ -473,6 +492,10 @@ def oracle_throughput(w, budget_s: float, device="cpu"):
         sl = slice(b, b + 1)
         if w.mode == "greedy":
             svref.verify_greedy(L[sl], d[sl])
+        elif w.ragged:
+            r = svref.verify_sample_ragged(L[sl], q[sl] if q is not None else None, d[sl], u[sl], w.temperature,
+                                           gbh[sl], w.top_k, w.top_p)
+            svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[sl])
         else:
             svref.verify_sample(L[sl], q[sl] if q is not None else None, d[sl], u[sl], w.temperature, w.top_k,
                                 w.top_p)
@@ -501,10 +524,17 @@ def main():
         d = inp["draft"].cpu().numpy()
         u = inp["uniforms"].cpu().numpy()
         q = inp["q"].cpu().numpy() if inp["q"] is not None else None
+        gbh = inp["gamma_b"].cpu().numpy() if w.ragged else None
+        stops = inp["stop_tokens"].cpu().numpy() if w.ragged else None
+        mxh = inp["max_new"].cpu().numpy() if w.ragged else None
         # one step = a bounded sample of the batch (at most ~2 s of oracle work)
         t0 = time.perf_counter()
         if w.mode == "greedy":
             svref.verify_greedy(L[:1], d[:1])
+        elif w.ragged:
+            r = svref.verify_sample_ragged(L[:1], q[:1] if q is not None else None, d[:1], u[:1], w.temperature,
+                                           gbh[:1], w.top_k, w.top_p)
+            svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[:1])
         else:
             svref.verify_sample(L[:1], q[:1] if q is not None else None, d[:1], u[:1], w.temperature, w.top_k,
                                 w.top_p)

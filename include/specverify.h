@@ -92,6 +92,7 @@ typedef struct CUstream_st* sv_stream_t;
 #define SV_MAX_GAMMA 64
 #define SV_MAX_VOCAB (1 << 24)
 #define SV_MAX_TOP_K 1024
+#define SV_MAX_STOP_TOKENS 64
 
 /*
  * Bytes of device workspace that sv_verify_sample / sv_verify_greedy need for
@@ -178,6 +179,64 @@ sv_status sv_verify_greedy_noalloc(int B, int gamma, int V,
                                    int32_t* out_tokens, int32_t* out_num_accepted,
                                    int32_t* out_status,
                                    sv_stream_t stream);
+
+/*
+ * Ragged rounds (the lmnt.cn blog section 3.2 and the reading notes let the
+ * number of drafts change per round; here per sequence).  As sv_verify_sample
+ * / sv_verify_greedy, plus
+ *
+ *   gamma_b   [B] int32 device array, drafts of sequence b in this round, in
+ *             [0, gamma] (values outside are clamped).  Sequence b is then
+ *             exactly the step with gamma = gamma_b[b] on its first
+ *             gamma_b[b] + 1 logit rows, gamma_b[b] q rows and drafts: the
+ *             acceptance scan stops at gamma_b[b], the bonus comes from row
+ *             gamma_b[b], the final draw uses uniforms[b][gamma_b[b]].  Rows,
+ *             q rows and drafts beyond gamma_b[b] are ignored (they may hold
+ *             anything; they raise no status bit).  out_tokens is padded with
+ *             -1 after the drawn token, out_accept_prob with 0 beyond
+ *             gamma_b[b].  NULL gamma_b with B > 0 is SV_ERR_INVALID_ARG.
+ * The arrays keep their padded [B][gamma (+1)] shapes.
+ */
+sv_status sv_verify_sample_ragged(int B, int gamma, int V,
+                                  const void* logits, sv_dtype logits_dtype,
+                                  const float* q, const int32_t* draft_tokens,
+                                  const float* uniforms, const int32_t* gamma_b,
+                                  float temperature, int top_k, float top_p,
+                                  int32_t* out_tokens, int32_t* out_num_accepted,
+                                  float* out_accept_prob, int32_t* out_status,
+                                  void* workspace, size_t workspace_bytes,
+                                  sv_stream_t stream);
+sv_status sv_verify_greedy_ragged(int B, int gamma, int V,
+                                  const void* logits, sv_dtype logits_dtype,
+                                  const int32_t* draft_tokens, const int32_t* gamma_b,
+                                  int32_t* out_tokens, int32_t* out_num_accepted,
+                                  int32_t* out_status,
+                                  void* workspace, size_t workspace_bytes,
+                                  sv_stream_t stream);
+
+/*
+ * Ending a round early ("11.1 核心原理", listing 10-1's comment: an EOS / stop
+ * token or max_new_tokens may end the round, and no bonus token is forced).
+ * In place on the outputs of a verify call:
+ *
+ *   tokens          [B][gamma+1] int32 (device), out_tokens of the call;
+ *                   rewritten: the emitted tokens tokens[b][0 .. n_b] are
+ *                   kept up to and including the first stop token, and at
+ *                   most max_new[b] of them; the rest become -1
+ *   num_accepted    [B] int32 (device), n_b as the call wrote it (clamped to
+ *                   [0, gamma])
+ *   stop_tokens     n_stop int32 token ids (device), n_stop in
+ *                   [0, SV_MAX_STOP_TOKENS]; may be NULL when n_stop = 0
+ *   max_new         [B] int32 (device) token budgets (<= 0 keeps nothing), or
+ *                   NULL for no budget
+ *   out_num_emitted [B] int32 (device): how many tokens remain
+ *
+ * Returns SV_ERR_INVALID_ARG for bad sizes or NULL arrays, SV_ERR_CUDA if the
+ * launch fails.  Runs on `stream`.
+ */
+sv_status sv_truncate_emitted(int B, int gamma, int32_t* tokens, const int32_t* num_accepted,
+                              const int32_t* stop_tokens, int n_stop, const int32_t* max_new,
+                              int32_t* out_num_emitted, sv_stream_t stream);
 
 /* Static description of a status code. */
 const char* sv_status_string(sv_status s);

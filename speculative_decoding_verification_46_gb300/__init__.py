@@ -23,11 +23,15 @@ from ._binding import (  # noqa: F401
     load_library,
     sv_last_kernels,
     sv_set_timing_events,
+    sv_truncate_emitted,
     sv_status_string,
     sv_verify_greedy,
     sv_verify_greedy_noalloc,
+    sv_verify_greedy_ragged,
     sv_verify_sample,
+    sv_verify_sample_ragged,
     sv_workspace_bytes,
+    truncate_emitted,
     verify_greedy,
     verify_sample,
 )

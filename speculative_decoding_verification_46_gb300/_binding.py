@@ -71,6 +71,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sv_verify_greedy_noalloc.restype = _c_int
     lib.sv_set_timing_events.argtypes = [ctypes.POINTER(_c_ptr), _c_int]
     lib.sv_set_timing_events.restype = _c_int
+    lib.sv_verify_sample_ragged.argtypes = [_c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                            _c_float, _c_int, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                            _c_ptr, _c_size, _c_ptr]
+    lib.sv_verify_sample_ragged.restype = _c_int
+    lib.sv_verify_greedy_ragged.argtypes = [_c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                            _c_ptr, _c_ptr, _c_size, _c_ptr]
+    lib.sv_verify_greedy_ragged.restype = _c_int
+    lib.sv_truncate_emitted.argtypes = [_c_int, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_ptr]
+    lib.sv_truncate_emitted.restype = _c_int
     lib.sv_last_kernels.argtypes = []
     lib.sv_last_kernels.restype = ctypes.c_char_p
     _lib = lib
@@ -108,6 +117,28 @@ def sv_verify_greedy_noalloc(B, gamma, V, logits, logits_dtype, draft_tokens, ou
     callers that cannot allocate device memory; see include/specverify.h."""
     return int(load_library().sv_verify_greedy_noalloc(B, gamma, V, logits, logits_dtype, draft_tokens, out_tokens,
                                                        out_num_accepted, out_status, stream))
+
+
+def sv_verify_sample_ragged(B, gamma, V, logits, logits_dtype, q, draft_tokens, uniforms, gamma_b, temperature,
+                            top_k, top_p, out_tokens, out_num_accepted, out_accept_prob, out_status, workspace,
+                            workspace_bytes, stream) -> int:
+    return int(load_library().sv_verify_sample_ragged(B, gamma, V, logits, logits_dtype, q, draft_tokens, uniforms,
+                                                       gamma_b, float(temperature), int(top_k), float(top_p),
+                                                       out_tokens, out_num_accepted, out_accept_prob, out_status,
+                                                       workspace, workspace_bytes, stream))
+
+
+def sv_verify_greedy_ragged(B, gamma, V, logits, logits_dtype, draft_tokens, gamma_b, out_tokens, out_num_accepted,
+                            out_status, workspace, workspace_bytes, stream) -> int:
+    return int(load_library().sv_verify_greedy_ragged(B, gamma, V, logits, logits_dtype, draft_tokens, gamma_b,
+                                                       out_tokens, out_num_accepted, out_status, workspace,
+                                                       workspace_bytes, stream))
+
+
+def sv_truncate_emitted(B, gamma, tokens, num_accepted, stop_tokens, n_stop, max_new, out_num_emitted,
+                        stream) -> int:
+    return int(load_library().sv_truncate_emitted(B, gamma, tokens, num_accepted, stop_tokens, n_stop, max_new,
+                                                   out_num_emitted, stream))
 
 
 def sv_last_kernels() -> list:
@@ -157,12 +188,14 @@ def _stream_handle(device, stream):
 
 
 def verify_sample(logits, q, draft, uniforms, temperature=1.0, top_k=0, top_p=1.0, *, workspace=None,
-                  stream=None, want_accept_prob=True, outputs=None):
+                  stream=None, want_accept_prob=True, outputs=None, gamma_b=None):
     """Speculative-sampling verify of a batch on the GPU.
 
     logits [B, gamma+1, V] (float32 / bfloat16 / float16), q [B, gamma, V]
     float32 (or None: deterministic drafts, q one-hot at each drafted token),
     draft [B, gamma] int32, uniforms [B, gamma+1] float32, all CUDA tensors.
+    gamma_b [B] int32 (CUDA) makes the round ragged: sequence b drafted only
+    gamma_b[b] tokens (sv_verify_sample_ragged).
     Returns (out_tokens [B, gamma+1] int32, n_accepted [B] int32, accept_prob
     [B, gamma] float32 or None, status [B] int32).
     """
@@ -184,17 +217,26 @@ def verify_sample(logits, q, draft, uniforms, temperature=1.0, top_k=0, top_p=1.
         out_tokens, out_n, out_a, out_status = outputs
     if workspace is None:
         workspace = alloc_workspace(B, G, V, top_k, dev)
-    st = sv_verify_sample(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype], _addr(q) if G > 0 else None,
-                          _addr(draft) if G > 0 else None, _addr(uniforms), temperature, top_k, top_p,
-                          _addr(out_tokens), _addr(out_n), _addr(out_a), _addr(out_status),
-                          _addr(workspace), workspace.numel(), _stream_handle(dev, stream))
+    if gamma_b is None:
+        st = sv_verify_sample(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype], _addr(q) if G > 0 else None,
+                              _addr(draft) if G > 0 else None, _addr(uniforms), temperature, top_k, top_p,
+                              _addr(out_tokens), _addr(out_n), _addr(out_a), _addr(out_status),
+                              _addr(workspace), workspace.numel(), _stream_handle(dev, stream))
+    else:
+        _need_cuda("gamma_b", gamma_b, torch.int32)
+        st = sv_verify_sample_ragged(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype],
+                                     _addr(q) if G > 0 else None, _addr(draft) if G > 0 else None, _addr(uniforms),
+                                     _addr(gamma_b), temperature, top_k, top_p, _addr(out_tokens), _addr(out_n),
+                                     _addr(out_a), _addr(out_status), _addr(workspace), workspace.numel(),
+                                     _stream_handle(dev, stream))
     if st != SV_OK:
         raise SvError(st, "sv_verify_sample")
     return out_tokens, out_n, out_a, out_status
 
 
-def verify_greedy(logits, draft, *, workspace=None, stream=None, outputs=None):
-    """Greedy verify of a batch on the GPU.  Returns (out_tokens, n_accepted, status)."""
+def verify_greedy(logits, draft, *, workspace=None, stream=None, outputs=None, gamma_b=None):
+    """Greedy verify of a batch on the GPU (gamma_b [B] int32 CUDA: a ragged
+    round).  Returns (out_tokens, n_accepted, status)."""
     B, G1, V = logits.shape
     G = G1 - 1
     dev = logits.device
@@ -210,9 +252,36 @@ def verify_greedy(logits, draft, *, workspace=None, stream=None, outputs=None):
         out_tokens, out_n, out_status = outputs
     if workspace is None:
         workspace = alloc_workspace(B, G, V, 0, dev)
-    st = sv_verify_greedy(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype], _addr(draft) if G > 0 else None,
-                          _addr(out_tokens), _addr(out_n), _addr(out_status), _addr(workspace), workspace.numel(),
-                          _stream_handle(dev, stream))
+    if gamma_b is None:
+        st = sv_verify_greedy(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype], _addr(draft) if G > 0 else None,
+                              _addr(out_tokens), _addr(out_n), _addr(out_status), _addr(workspace),
+                              workspace.numel(), _stream_handle(dev, stream))
+    else:
+        _need_cuda("gamma_b", gamma_b, torch.int32)
+        st = sv_verify_greedy_ragged(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype],
+                                     _addr(draft) if G > 0 else None, _addr(gamma_b), _addr(out_tokens),
+                                     _addr(out_n), _addr(out_status), _addr(workspace), workspace.numel(),
+                                     _stream_handle(dev, stream))
     if st != SV_OK:
         raise SvError(st, "sv_verify_greedy")
     return out_tokens, out_n, out_status
+
+
+def truncate_emitted(tokens, n_accepted, stop_tokens=None, max_new=None, *, stream=None):
+    """End the round early at stop tokens / a token budget, in place on
+    `tokens` [B, gamma+1] int32 (CUDA).  stop_tokens: int32 CUDA tensor of
+    token ids (or None); max_new: [B] int32 CUDA tensor (or None).  Returns
+    num_emitted [B] int32."""
+    B, G1 = tokens.shape
+    dev = tokens.device
+    _need_cuda("tokens", tokens, torch.int32)
+    _need_cuda("n_accepted", n_accepted, torch.int32)
+    _need_cuda("stop_tokens", stop_tokens, torch.int32)
+    _need_cuda("max_new", max_new, torch.int32)
+    out = torch.empty(B, dtype=torch.int32, device=dev)
+    n_stop = 0 if stop_tokens is None else stop_tokens.numel()
+    st = sv_truncate_emitted(B, G1 - 1, _addr(tokens), _addr(n_accepted), _addr(stop_tokens), n_stop,
+                             _addr(max_new), _addr(out), _stream_handle(dev, stream))
+    if st != SV_OK:
+        raise SvError(st, "sv_truncate_emitted")
+    return out

@@ -14,6 +14,7 @@
 #include "sv_cluster.cuh"
 #include "sv_device.cuh"
 #include "sv_stream.cuh"
+#include "sv_truncate.cuh"
 #include "sv_topk.cuh"
 
 namespace {
@@ -349,11 +350,13 @@ extern "C" size_t sv_workspace_bytes(int B, int gamma, int V, int top_k) {
   return make_layout(B, gamma, V, top_k).total;
 }
 
-extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
-                                      const float* q, const int32_t* draft_tokens, const float* uniforms,
-                                      float temperature, int top_k, float top_p, int32_t* out_tokens,
-                                      int32_t* out_num_accepted, float* out_accept_prob, int32_t* out_status,
-                                      void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+namespace {
+
+sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype, const float* q,
+                             const int32_t* draft_tokens, const float* uniforms, const int32_t* gamma_b,
+                             float temperature, int top_k, float top_p, int32_t* out_tokens,
+                             int32_t* out_num_accepted, float* out_accept_prob, int32_t* out_status, void* workspace,
+                             size_t workspace_bytes, sv_stream_t stream) {
   g_last_kernels = "";
   if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
   if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
@@ -390,6 +393,7 @@ extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logit
   p.q = q;
   p.draft = draft_tokens;
   p.uniforms = uniforms;
+  p.gamma_b = gamma_b;
   p.out_tokens = out_tokens;
   p.out_n = out_num_accepted;
   p.out_a = out_accept_prob;
@@ -399,10 +403,10 @@ extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logit
              reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" sv_status sv_verify_greedy(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
-                                      const int32_t* draft_tokens, int32_t* out_tokens, int32_t* out_num_accepted,
-                                      int32_t* out_status, void* workspace, size_t workspace_bytes,
-                                      sv_stream_t stream) {
+sv_status verify_greedy_impl(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                             const int32_t* draft_tokens, const int32_t* gamma_b, int32_t* out_tokens,
+                             int32_t* out_num_accepted, int32_t* out_status, void* workspace, size_t workspace_bytes,
+                             sv_stream_t stream) {
   g_last_kernels = "";
   if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
   if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
@@ -420,10 +424,70 @@ extern "C" sv_status sv_verify_greedy(int B, int gamma, int V, const void* logit
   p.c = 1.0f;
   p.logits = logits;
   p.draft = draft_tokens;
+  p.gamma_b = gamma_b;
   p.out_tokens = out_tokens;
   p.out_n = out_num_accepted;
   p.out_status = out_status;
   return run(p, logits_dtype, sv::MODE_GREEDY, workspace, workspace_bytes, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" sv_status sv_verify_sample(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                                      const float* q, const int32_t* draft_tokens, const float* uniforms,
+                                      float temperature, int top_k, float top_p, int32_t* out_tokens,
+                                      int32_t* out_num_accepted, float* out_accept_prob, int32_t* out_status,
+                                      void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  return verify_sample_impl(B, gamma, V, logits, logits_dtype, q, draft_tokens, uniforms, nullptr, temperature, top_k,
+                            top_p, out_tokens, out_num_accepted, out_accept_prob, out_status, workspace,
+                            workspace_bytes, stream);
+}
+
+extern "C" sv_status sv_verify_sample_ragged(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                                             const float* q, const int32_t* draft_tokens, const float* uniforms,
+                                             const int32_t* gamma_b, float temperature, int top_k, float top_p,
+                                             int32_t* out_tokens, int32_t* out_num_accepted, float* out_accept_prob,
+                                             int32_t* out_status, void* workspace, size_t workspace_bytes,
+                                             sv_stream_t stream) {
+  if (!gamma_b && B > 0) {
+    g_last_kernels = "";
+    return SV_ERR_INVALID_ARG;
+  }
+  return verify_sample_impl(B, gamma, V, logits, logits_dtype, q, draft_tokens, uniforms, gamma_b, temperature, top_k,
+                            top_p, out_tokens, out_num_accepted, out_accept_prob, out_status, workspace,
+                            workspace_bytes, stream);
+}
+
+extern "C" sv_status sv_verify_greedy(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                                      const int32_t* draft_tokens, int32_t* out_tokens, int32_t* out_num_accepted,
+                                      int32_t* out_status, void* workspace, size_t workspace_bytes,
+                                      sv_stream_t stream) {
+  return verify_greedy_impl(B, gamma, V, logits, logits_dtype, draft_tokens, nullptr, out_tokens, out_num_accepted,
+                            out_status, workspace, workspace_bytes, stream);
+}
+
+extern "C" sv_status sv_verify_greedy_ragged(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                                             const int32_t* draft_tokens, const int32_t* gamma_b,
+                                             int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_status,
+                                             void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  if (!gamma_b && B > 0) {
+    g_last_kernels = "";
+    return SV_ERR_INVALID_ARG;
+  }
+  return verify_greedy_impl(B, gamma, V, logits, logits_dtype, draft_tokens, gamma_b, out_tokens, out_num_accepted,
+                            out_status, workspace, workspace_bytes, stream);
+}
+
+extern "C" sv_status sv_truncate_emitted(int B, int gamma, int32_t* tokens, const int32_t* num_accepted,
+                                         const int32_t* stop_tokens, int n_stop, const int32_t* max_new,
+                                         int32_t* out_num_emitted, sv_stream_t stream) {
+  if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || n_stop < 0 || n_stop > SV_MAX_STOP_TOKENS) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!tokens || !num_accepted || !out_num_emitted || (n_stop > 0 && !stop_tokens)) return SV_ERR_INVALID_ARG;
+  const int threads = 128;
+  sv::truncate_kernel<<<(unsigned)((B + threads - 1) / threads), threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      B, gamma, tokens, num_accepted, stop_tokens, n_stop, max_new, out_num_emitted);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 extern "C" const char* sv_status_string(sv_status s) {

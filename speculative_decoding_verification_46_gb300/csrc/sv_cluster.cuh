@@ -170,6 +170,7 @@ cluster_kernel(const ClusterParams cp) {
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / CN;
   const int G = p.gamma, G1 = G + 1, V = p.V;
+  const int gb = seq_gamma(p, b);   // this sequence's drafts (ragged rounds)
   const int v0 = rank * W;
   const int v1 = min(v0 + W, V);
   const int nvec = max(v1 - v0, 0) / VW;               // vectors in this slice (V % VW == 0 on this path)
@@ -200,7 +201,7 @@ cluster_kernel(const ClusterParams cp) {
   // flight together with the slices; every CTA needs them for the scan)
   int d_own = -1;
   float l_own = 0.f, q_own = 0.f, u_own = 0.f;
-  if (tid < G) {
+  if (tid < gb) {
     d_own = __ldg(p.draft + b * G + tid);
     if (d_own >= 0 && d_own < V) {
       l_own = Tr<T>::get(load_slot<T>(Lg + (size_t)tid * V, d_own, 1, false), 0);
@@ -278,22 +279,22 @@ cluster_kernel(const ClusterParams cp) {
     const float4 mg = group_merge<MODE>(v, CN, p.c);
     if (rowok && r == 0) {
       int st = 0;
-      const int d = i < G ? sm.dr[i] : 0;
-      if (i < G && (d < 0 || d >= V)) st |= SEQ_OOB;
+      const int d = i < gb ? sm.dr[i] : 0;
+      if (i < gb && (d < 0 || d >= V)) st |= SEQ_OOB;
       if (MODE == MODE_GREEDY) {
         const bool nan = mg.x != mg.x;
         const int bi = __float_as_int(mg.y);
         sm.g[i] = (nan || bi == 0x7fffffff) ? 0 : bi;
-        if (nan) st |= SEQ_BADROW;
+        if (nan && i <= gb) st |= SEQ_BADROW;
       } else {
         const double sd = (double)mg.y + (double)mg.z;
         const bool badrow = !(mg.x > -INFINITY && mg.x < INFINITY) || !(sd > 0.0 && sd < 1e300);
         sm.M[i] = mg.x;
         sm.S[i] = sd;
-        if (badrow) st |= SEQ_BADROW;
+        if (badrow && i <= gb) st |= SEQ_BADROW;
         if (i < G) {
           float a = 0.f;
-          if (d >= 0 && d < V) {
+          if (i < gb && d >= 0 && d < V) {
             const float pd = badrow ? 0.f : exp2f((sm.dl[i] - mg.x) * p.c) / (float)sd;
             const float qd = sm.dq[i];
             if (qd > 0.0f) {
@@ -311,13 +312,13 @@ cluster_kernel(const ClusterParams cp) {
   }
   __syncthreads();
   if (warp == 0) {
-    int status = 0, n = G;
+    int status = 0, n = gb;
     for (int c0 = 0; c0 < G1; c0 += 32) {
       const int i = c0 + lane;
-      if (i < G1) status |= sm.st[i];
-      const bool rej = i < G && (MODE == MODE_GREEDY ? sm.dr[i] != sm.g[i] : !(sm.ur[i] < sm.a[i]));
+      if (i <= gb) status |= sm.st[i];
+      const bool rej = i < gb && (MODE == MODE_GREEDY ? sm.dr[i] != sm.g[i] : !(sm.ur[i] < sm.a[i]));
       const unsigned rb = __ballot_sync(0xffffffffu, rej);
-      if (rb && n == G) n = c0 + __ffs(rb) - 1;
+      if (rb && n == gb) n = c0 + __ffs(rb) - 1;
     }
     status = __reduce_or_sync(0xffffffffu, status);
     if (lane == 0) {
@@ -348,7 +349,7 @@ cluster_kernel(const ClusterParams cp) {
   // ---- final draw: residual of row n, or the bonus from row gamma
   // (precise weights and the (S, A, Q) decomposition, as in residual_kernel;
   // thread t of a CTA owns the run of EPT tokens at t * EPT of its slice)
-  const bool resid = n < G;
+  const bool resid = n < gb;
   const bool bad = (sm.status & SEQ_BADROW) != 0;
   const T* Lf = Ls + (size_t)n * W;
   const float* Qf = (resid && p.q) ? Qs + (size_t)n * W : nullptr;
@@ -404,7 +405,7 @@ cluster_kernel(const ClusterParams cp) {
       inc = sinc;
       R = s;
     }
-    const F2 tgt = f2_scale(R, sm.ur[G]);
+    const F2 tgt = f2_scale(R, sm.ur[gb]);
     F2 excl = f2_shfl_up(inc, 1);
     if (lane == 0) excl = F2{0.f, 0.f};
     const bool live = lane < CN && f2_pos(m_l);

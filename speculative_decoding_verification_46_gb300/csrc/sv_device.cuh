@@ -86,6 +86,7 @@ struct Params {
   unsigned long long* lists;      // [R][S][top_k] per-slice top-k candidates
   int2* rowres;                   // [R][top_k + 1] kept (index, probability) lists
   float2* chunk_mass;             // [B][3][C] residual chunk sums (S, A, Q; two-float)
+  const int* gamma_b;             // [B] drafts per sequence (ragged rounds), or nullptr: gamma
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -591,6 +592,13 @@ __device__ __forceinline__ bool argmax_better(float va, int ia, float vb, int ib
   return ia < ib;
 }
 
+// Drafts of sequence b in this round: gamma_b[b] clamped to [0, gamma] for a
+// ragged round, else gamma.  Its rows beyond gamma_b are not part of the round.
+__device__ __forceinline__ int seq_gamma(const Params& p, int b) {
+  if (!p.gamma_b) return p.gamma;
+  return min(max(__ldg(p.gamma_b + b), 0), p.gamma);
+}
+
 // Last-arriving-CTA hand-off.  Every thread publishes its writes, one thread
 // takes a ticket; the CTA that takes ticket count-1 resets the counter and
 // returns true (its later reads of other CTAs' data use ld.global.cg).
@@ -646,6 +654,7 @@ template <typename T, int MODE>
 __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.gamma, G1 = G + 1, V = p.V, S = p.S;
+  const int gb = seq_gamma(p, b);
   for (int i = warp; i < G1; i += kWarps) {
     const int rr = b * G1 + i;
     const float4* pp = p.part + (size_t)rr * S;
@@ -667,7 +676,7 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
       if (lane == 0) {
         const bool nan = bv != bv;
         sm.g[i] = (nan || bi == 0x7fffffff) ? 0 : bi;
-        sm.bad[i] = nan ? 1 : 0;
+        sm.bad[i] = (nan && i <= gb) ? 1 : 0;
       }
     } else {
       float M = -INFINITY;
@@ -693,8 +702,8 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
         const bool bad = !(M > -INFINITY && M < INFINITY) || !(s > 0.0 && s < 1e300);
         sm.M[i] = M;
         sm.s[i] = s;
-        sm.bad[i] = bad ? 1 : 0;
-        if (i < G) {
+        sm.bad[i] = (bad && i <= gb) ? 1 : 0;
+        if (i < gb) {
           const int d = sm.dr[i];
           float a = 0.f;
           int st = 0;
@@ -715,6 +724,8 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
           sm.a[i] = a;
           sm.g[i] = st;
           if (p.out_a) p.out_a[b * G + i] = a;
+        } else if (i < G && p.out_a) {
+          p.out_a[b * G + i] = 0.f;   // beyond this sequence's drafts
         }
       }
     }
@@ -724,20 +735,20 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
   for (int e = tid; e < G1 * S; e += kThreads)
     p.part[(size_t)b * G1 * S + e] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid == 0) {
-    int status = 0, n = G;
-    for (int i = 0; i < G1; ++i)
+    int status = 0, n = gb;
+    for (int i = 0; i <= gb; ++i)
       if (sm.bad[i]) status |= SEQ_BADROW;
     if (MODE == MODE_GREEDY) {
-      for (int i = 0; i < G; ++i) {
+      for (int i = 0; i < gb; ++i) {
         const int d = sm.dr[i];
         if (d < 0 || d >= V) status |= SEQ_OOB;
       }
-      for (int i = 0; i < G; ++i)
+      for (int i = 0; i < gb; ++i)
         if (sm.dr[i] != sm.g[i]) { n = i; break; }
       sm.token = sm.g[n];
     } else {
-      for (int i = 0; i < G; ++i) status |= sm.g[i];
-      for (int i = 0; i < G; ++i)
+      for (int i = 0; i < gb; ++i) status |= sm.g[i];
+      for (int i = 0; i < gb; ++i)
         if (!(sm.ur[i] < (float)sm.a[i])) { n = i; break; }
       SeqState st;
       st.n = n;
@@ -777,6 +788,7 @@ __device__ __forceinline__ int count_greater(const unsigned long long* X, int n,
 __device__ void finish_row_topk(const Params& p, int b, int i, int rr, RowsSmem& sm) {
   const int tid = threadIdx.x;
   const int k = p.top_k, G = p.gamma, V = p.V;
+  const int gb = seq_gamma(p, b);
   unsigned long long* A = sm.cand;            // running merged list
   unsigned long long* Bl = sm.cand + kMaxK;   // next slice list
   unsigned long long* O = sm.mout;
@@ -832,7 +844,7 @@ __device__ void finish_row_topk(const Params& p, int b, int i, int rr, RowsSmem&
       J = na > 0 ? 1 : 0;
       if (na > 0) sm.w[0] = 1.0;
       W = 1.0;
-      if (bad) atomicOr(&p.seq[b].status, SEQ_BADROW);
+      if (bad && i <= gb) atomicOr(&p.seq[b].status, SEQ_BADROW);
     } else if (p.top_p < 1.0f) {
       const double tp = (double)p.top_p;
       double cum = 0.0;
@@ -853,7 +865,7 @@ __device__ void finish_row_topk(const Params& p, int b, int i, int rr, RowsSmem&
   for (int e = tid; e < J; e += kThreads)
     out[1 + e] = make_int2(sm.widx[e], __float_as_int((float)(sm.w[e] / WJ)));
   // acceptance probability of this row's draft
-  if (i < G) {
+  if (i < gb) {
     const int d = p.draft[b * G + i];
     if (tid == 0) sm.dred[0] = 0.0;
     __syncthreads();
@@ -888,9 +900,10 @@ __device__ void finish_row_topk(const Params& p, int b, int i, int rr, RowsSmem&
 __device__ void finish_sequence_topk(const Params& p, int b, RowsSmem& sm) {
   const int tid = threadIdx.x;
   const int k = p.top_k, G = p.gamma, G1 = G + 1, V = p.V;
+  const int gb = seq_gamma(p, b);
   if (tid == 0) {
-    int n = G;
-    for (int i = 0; i < G; ++i) {
+    int n = gb;
+    for (int i = 0; i < gb; ++i) {
       const double u = (double)p.uniforms[b * G1 + i];
       if (!(u < __ldcg(p.acc + b * G + i))) { n = i; break; }
     }
@@ -902,7 +915,7 @@ __device__ void finish_sequence_topk(const Params& p, int b, RowsSmem& sm) {
   const int rr = b * G1 + n;
   const int2* kept = p.rowres + (size_t)rr * (k + 1);
   const int J = __ldcg(kept).x;
-  const bool resid = n < G;
+  const bool resid = n < gb;
   const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
   const int dn = (resid && !p.q) ? __ldg(p.draft + b * G + n) : -1;   // deterministic draft: q_n one-hot
   // r_j in index order: rank each kept entry by its index
@@ -939,7 +952,7 @@ __device__ void finish_sequence_topk(const Params& p, int b, RowsSmem& sm) {
       R = 0.0;
       for (int e = 0; e < J; ++e) R += rs[e];
     }
-    const double t = (double)p.uniforms[b * G1 + G] * R;
+    const double t = (double)p.uniforms[b * G1 + gb] * R;
     int tok = -1, lastpos = -1;
     double C = 0.0;
     for (int e = 0; e < J; ++e) {
@@ -957,6 +970,8 @@ __device__ void finish_sequence_topk(const Params& p, int b, RowsSmem& sm) {
   __syncthreads();
   for (int j = tid; j < G1; j += kThreads)
     p.out_tokens[b * G1 + j] = j < n ? p.draft[b * G + j] : (j == n ? sm.token : -1);
+  if (p.out_a)
+    for (int j = gb + tid; j < G; j += kThreads) p.out_a[b * G + j] = 0.f;   // beyond this sequence's drafts
   // kept lists and acceptance probabilities have been consumed: zero them
   for (int e = tid; e < G1 * (k + 1); e += kThreads) p.rowres[(size_t)b * G1 * (k + 1) + e] = make_int2(0, 0);
   for (int e = tid; e < G; e += kThreads) p.acc[b * G + e] = 0.0;
@@ -1098,7 +1113,7 @@ rows_kernel(const Params p) {
     }
   }
   if (tid == 0) sm.count = 0;
-  if (__syncthreads_or(has_nan) && tid == 0) atomicOr(&p.seq[b].status, SEQ_BADROW);
+  if (__syncthreads_or(has_nan) && tid == 0 && i <= seq_gamma(p, b)) atomicOr(&p.seq[b].status, SEQ_BADROW);
   const int total_real = block_sum_int(nreal, sm.ired);
   // threshold key K: the k-th largest of the per-thread maxima (a lower bound
   // of the slice's k-th largest value: those k threads each hold one element >= it)
@@ -1471,7 +1486,8 @@ residual_kernel(const Params p) {
   st.M = __ldcg(&p.seq[b].M);
   st.s = __ldcg(&p.seq[b].s);
   const int n = st.n;
-  const bool resid = n < G;
+  const int gb = seq_gamma(p, b);
+  const bool resid = n < gb;
   const bool bad = (st.status & SEQ_BADROW) != 0;
   const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
   const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
@@ -1521,7 +1537,7 @@ residual_kernel(const Params p) {
     __threadfence_block();
     __syncthreads();
   }
-  const float u = __ldg(p.uniforms + b * G1 + G);
+  const float u = __ldg(p.uniforms + b * G1 + gb);
   F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
   bool use_q = resid;
   int sub = locate(resid ? cA : cS, C, u, &R, &base, &tgt, sm.loc, true);

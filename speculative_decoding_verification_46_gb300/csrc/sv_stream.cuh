@@ -108,18 +108,19 @@ template <int MODE>
 __device__ void stream_finish_dense(const Params& p, int b, StreamSmem& sm) {
   const int tid = threadIdx.x;
   const int G = p.gamma, G1 = G + 1;
+  const int gb = seq_gamma(p, b);
   if (tid < G1) {
     const float4 v = __ldcg(p.part + (size_t)b * G1 + tid);
     if (MODE == MODE_GREEDY) {
       const bool nan = v.x != v.x;
       const int bi = __float_as_int(v.y);
       sm.g[tid] = (nan || bi == 0x7fffffff) ? 0 : bi;
-      sm.bad[tid] = nan;
+      sm.bad[tid] = nan && tid <= gb;
     } else {
       const double s = (double)v.y + (double)v.z;
       sm.M[tid] = v.x;
       sm.s[tid] = s;
-      sm.bad[tid] = !(v.x > -INFINITY && v.x < INFINITY) || !(s > 0.0 && s < 1e300);
+      sm.bad[tid] = (!(v.x > -INFINITY && v.x < INFINITY) || !(s > 0.0 && s < 1e300)) && tid <= gb;
       if (tid < G) sm.a[tid] = (float)__ldcg(p.acc + b * G + tid);
     }
     sm.ur[tid] = MODE == MODE_SOFTMAX ? __ldg(p.uniforms + b * G1 + tid) : 0.f;
@@ -130,17 +131,17 @@ __device__ void stream_finish_dense(const Params& p, int b, StreamSmem& sm) {
   for (int e = tid; e < G1; e += kSt) p.part[(size_t)b * G1 + e] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int e = tid; e < G; e += kSt) p.acc[b * G + e] = 0.0;
   if (tid == 0) {
-    int status = sm.status, n = G;
-    for (int i = 0; i < G1; ++i)
+    int status = sm.status, n = gb;
+    for (int i = 0; i <= gb; ++i)
       if (sm.bad[i]) status |= SEQ_BADROW;
     if (MODE == MODE_GREEDY) {
-      for (int i = 0; i < G; ++i)
+      for (int i = 0; i < gb; ++i)
         if (sm.dr[i] != sm.g[i]) { n = i; break; }
       sm.token = sm.g[n];
       p.seq[b].status = 0;
       if (p.out_status) p.out_status[b] = status;
     } else {
-      for (int i = 0; i < G; ++i)
+      for (int i = 0; i < gb; ++i)
         if (!(sm.ur[i] < sm.a[i])) { n = i; break; }
       SeqState st;
       st.n = n;
@@ -155,6 +156,8 @@ __device__ void stream_finish_dense(const Params& p, int b, StreamSmem& sm) {
   }
   __syncthreads();
   const int n = sm.n;
+  if (MODE == MODE_SOFTMAX && p.out_a)
+    for (int j = gb + tid; j < G; j += kSt) p.out_a[b * G + j] = 0.f;   // beyond this sequence's drafts
   for (int j = tid; j < G1; j += kSt) {
     if (j < n) p.out_tokens[b * G1 + j] = sm.dr[j];
     else if (j > n) p.out_tokens[b * G1 + j] = -1;
@@ -245,11 +248,12 @@ stream_dense_kernel(const Params p) {
   for (int j = 0; j < w.nrows; ++j) {
     const int r = w.row_of(j);
     const int b = r / G1, i = r - b * G1;
+    const int gb = seq_gamma(p, b);
     const T* row = logits + (size_t)r * V;
     // the draft's logit and q(d) for this row, fetched early (softmax only)
     float l_d = 0.f, q_d = 0.f;
     int d = -1;
-    if (MODE == MODE_SOFTMAX && tid == 0 && i < G) {
+    if (MODE == MODE_SOFTMAX && tid == 0 && i < gb) {
       d = __ldg(p.draft + b * G + i);
       if (d >= 0 && d < V) {
         l_d = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
@@ -319,7 +323,7 @@ stream_dense_kernel(const Params p) {
           if (argmax_better(ov, oi, v0, i0)) { v0 = ov; i0 = oi; }
         }
         p.part[r] = make_float4(v0, __int_as_float(i0), 0.f, 0.f);
-        if (i < G) {
+        if (i < gb) {
           const int dd = __ldg(p.draft + b * G + i);
           if (dd < 0 || dd >= V) atomicOr(&p.seq[b].status, SEQ_OOB);
         }
@@ -341,7 +345,7 @@ stream_dense_kernel(const Params p) {
       const F2 tot = block_sum_f2(acc, sm.f2red);
       if (tid == 0) {
         p.part[r] = make_float4(M, tot.hi, tot.lo, 0.f);
-        if (i < G) {
+        if (i < gb) {
           float a = 0.f;
           int st = 0;
           const float ssum = tot.hi + tot.lo;
@@ -407,6 +411,7 @@ stream_topk_kernel(const Params p) {
   for (int j = 0; j < w.nrows; ++j) {
     const int r = w.row_of(j);
     const int b = r / G1, i = r - b * G1;
+    const int gb = seq_gamma(p, b);
     const T* row = logits + (size_t)r * V;
     __syncthreads();   // the previous row's shared state is no longer in use
     if (tid == 0) {
@@ -415,7 +420,7 @@ stream_topk_kernel(const Params p) {
     }
     int d_row = -1;
     float q_row = 0.f;
-    if (tid == 0 && i < G) {
+    if (tid == 0 && i < gb) {
       d_row = __ldg(p.draft + b * G + i);
       if (d_row >= 0 && d_row < V) q_row = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d_row) : 1.f;
     }
@@ -557,7 +562,7 @@ stream_topk_kernel(const Params p) {
       }
     }
     __syncthreads();
-    topk_row_epilogue(p, b, i, r, min(k, N), bad_nan != 0, d_row, q_row, sm);
+    topk_row_epilogue(p, b, i, gb, r, min(k, N), bad_nan != 0, d_row, q_row, sm);
     if (arrive_last(p.seq_ticket + b, G1, &sm.flag)) topk_finish_sequence(p, b, sm);
   }
   cpa_wait<0>();

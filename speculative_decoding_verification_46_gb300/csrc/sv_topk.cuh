@@ -54,13 +54,14 @@ __device__ __forceinline__ int block_sum_int_n(int v, int* sm) {
 __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int k = p.top_k, G = p.gamma, G1 = G + 1, V = p.V;
+  const int gb = seq_gamma(p, b);
   if (tid < G1) sm.fu[tid] = __ldg(p.uniforms + b * G1 + tid);
   if (tid < G) sm.fa[tid] = (float)__ldcg(p.acc + b * G + tid);
   if (tid == 0) sm.status = __ldcg(&p.seq[b].status);
   __syncthreads();
   if (tid == 0) {
-    int n = G;
-    for (int i = 0; i < G; ++i)
+    int n = gb;
+    for (int i = 0; i < gb; ++i)
       if (!(sm.fu[i] < sm.fa[i])) { n = i; break; }
     sm.n = n;
   }
@@ -68,7 +69,7 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   const int n = sm.n;
   const int2* kept = p.rowres + (size_t)(b * G1 + n) * (k + 1);
   const int J = __ldcg(kept).x;
-  const bool resid = n < G;
+  const bool resid = n < gb;
   const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
   const int dn = (resid && !p.q) ? __ldg(p.draft + b * G + n) : -1;   // deterministic draft: q_n one-hot
   for (int e = tid; e < J; e += nt) {
@@ -90,7 +91,7 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
     rs[rank] = F2{r, 0.f};
   }
   __syncthreads();
-  const float u = sm.fu[G];
+  const float u = sm.fu[gb];
   F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
   int pos = locate(rs, J, u, &R, &base, &tgt, sm.loc, false);
   int status = sm.status;
@@ -116,6 +117,8 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   __syncthreads();
   for (int j = tid; j < G1; j += nt)
     p.out_tokens[b * G1 + j] = j < n ? __ldg(p.draft + b * G + j) : (j == n ? sm.token : -1);
+  if (p.out_a)
+    for (int j = gb + tid; j < G; j += nt) p.out_a[b * G + j] = 0.f;   // beyond this sequence's drafts
   // the kept lists and acceptance probabilities have been consumed: zero them
   for (int e = tid; e < G1 * (k + 1); e += nt) p.rowres[(size_t)b * G1 * (k + 1) + e] = make_int2(0, 0);
   for (int e = tid; e < G; e += nt) p.acc[b * G + e] = 0.0;
@@ -126,7 +129,7 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
 // two-float sums, the kept
 // (index, probability) list written to rowres[r], and the acceptance
 // probability of the row's draft (d_row, q_row prefetched by thread 0).
-__device__ void topk_row_epilogue(const Params& p, int b, int i, int r, int kk, bool bad_nan, int d_row,
+__device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int r, int kk, bool bad_nan, int d_row,
                                   float q_row, TopkSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
   const int G = p.gamma, V = p.V, k = p.top_k;
@@ -167,7 +170,7 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int r, int kk, 
       if (lane == 0) {
         sm.J = J;
         sm.WJ = WJ.hi + WJ.lo;
-        if (bad) atomicOr(&p.seq[b].status, SEQ_BADROW);
+        if (bad && i <= gb) atomicOr(&p.seq[b].status, SEQ_BADROW);
       }
     }
     __syncthreads();
@@ -177,7 +180,7 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int r, int kk, 
     if (tid == 0) out[0] = make_int2(J, 0);
     for (int e = tid; e < J; e += nt) out[1 + e] = make_int2(sm.widx[e], __float_as_int(sm.w[e] / WJ));
     // ---- acceptance probability of this row's draft
-    if (i < G) {
+    if (i < gb) {
       if (tid == 0) {
         sm.pd = 0.f;
         sm.token = d_row;

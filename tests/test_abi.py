@@ -33,7 +33,8 @@ def test_exports_every_declared_symbol(sv):
     lib = ctypes.CDLL(sv.load_library()._name)
     names = _declared_functions()
     assert set(names) == {"sv_workspace_bytes", "sv_verify_sample", "sv_verify_greedy", "sv_status_string",
-                          "sv_set_timing_events", "sv_verify_greedy_noalloc", "sv_last_kernels"}
+                          "sv_set_timing_events", "sv_verify_greedy_noalloc", "sv_last_kernels",
+                          "sv_verify_sample_ragged", "sv_verify_greedy_ragged", "sv_truncate_emitted"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -137,3 +138,26 @@ def test_last_kernels_empty_without_launch(sv):
     assert sv.sv_last_kernels() == []
     assert lib.sv_verify_greedy(0, 2, 10, None, 0, None, None, None, None, None, 0, None) == sv.SV_OK
     assert sv.sv_last_kernels() == []
+
+
+def test_ragged_and_truncate_validation(sv):
+    lib = sv.load_library()
+    # ragged calls need gamma_b (the empty batch needs nothing)
+    assert sv.sv_verify_sample_ragged(4, 3, 100, A, sv.SV_DTYPE_BF16, A + 4096, A + 8192, A + 12288, None, 1.0, 0,
+                                      1.0, A + 16384, A + 20480, None, None, A + 65536, 1 << 30,
+                                      None) == sv.SV_ERR_INVALID_ARG
+    assert sv.sv_verify_greedy_ragged(4, 3, 100, A, sv.SV_DTYPE_BF16, A + 8192, None, A + 16384, A + 20480, None,
+                                      A + 65536, 1 << 30, None) == sv.SV_ERR_INVALID_ARG
+    assert sv.sv_verify_greedy_ragged(0, 3, 100, None, sv.SV_DTYPE_BF16, None, None, None, None, None, None, 0,
+                                      None) == sv.SV_OK
+    # a ragged call with gamma_b given goes on to the usual checks
+    assert sv.sv_verify_sample_ragged(4, 3, 100, A, sv.SV_DTYPE_BF16, A + 4096, A + 8192, A + 12288, A + 32768, 1.0,
+                                      0, 1.0, A + 16384, A + 20480, None, None, A + 65536, 16,
+                                      None) == sv.SV_ERR_WORKSPACE
+    T = lib.sv_truncate_emitted
+    assert T(-1, 3, A, A, None, 0, None, A, None) == sv.SV_ERR_INVALID_ARG
+    assert T(4, 65, A, A, None, 0, None, A, None) == sv.SV_ERR_INVALID_ARG
+    assert T(4, 3, A, A, None, 65, None, A, None) == sv.SV_ERR_INVALID_ARG
+    assert T(4, 3, A, A, None, 2, None, A, None) == sv.SV_ERR_INVALID_ARG      # n_stop > 0 needs the ids
+    assert T(4, 3, None, A, None, 0, None, A, None) == sv.SV_ERR_INVALID_ARG
+    assert T(0, 3, None, None, None, 0, None, None, None) == sv.SV_OK

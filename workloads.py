@@ -49,6 +49,8 @@ class Workload:
     draft_sigma: float = 0.7
     seed: int = 0
     deterministic: bool = False   # q = None: the drafter's guess argmax(target + noise)
+    ragged: bool = False          # per-sequence gamma_b in [1, gamma], stop tokens and token budgets
+    n_stop: int = 0               # stop-token ids of a ragged round
 
     @property
     def rows(self) -> int:
@@ -64,7 +66,8 @@ class Workload:
 
 # The five workloads of the verify step (sizes and distributions as stated for
 # the step's headline measurements), plus the two other draft-noise levels of
-# the B=64 sweep and the deterministic-draft (q one-hot, passed as None) case.
+# the B=64 sweep, the deterministic-draft (q one-hot, passed as None) case and
+# a ragged round (per-sequence gamma_b, stop tokens, token budgets).
 WORKLOADS = {
     w.name: w
     for w in [
@@ -81,6 +84,8 @@ WORKLOADS = {
         Workload("greedy_b512_g4_v128256_bf16", 512, 4, 128256, "bf16", "greedy", seed=50),
         Workload("sample_det_b64_g4_v128256_bf16", 64, 4, 128256, "bf16", "sample", 1.0,
                  draft_sigma=0.7, seed=52, deterministic=True),
+        Workload("sample_ragged_b64_g8_v128256_bf16", 64, 8, 128256, "bf16", "sample", 1.0,
+                 draft_sigma=0.7, seed=53, ragged=True, n_stop=4),
         Workload("topk50_topp0.9_b256_g8_v152064_bf16", 256, 8, 152064, "bf16", "sample", 0.8,
                  top_k=50, top_p=0.9, draft_sigma=0.7, seed=51),
     ]
@@ -161,5 +166,14 @@ def make_inputs(w: Workload, seed: int | None = None, device="cpu", B: int | Non
             draft = torch.zeros(B, 0, dtype=torch.int64, device=device)
     del Lf
     uniforms = torch.rand(B, G + 1, generator=g, device=device, dtype=torch.float32)
-    return dict(logits=logits.contiguous(), q=None if q is None else q.contiguous(),
-                draft=draft.to(torch.int32).contiguous(), uniforms=uniforms.contiguous())
+    out = dict(logits=logits.contiguous(), q=None if q is None else q.contiguous(),
+               draft=draft.to(torch.int32).contiguous(), uniforms=uniforms.contiguous())
+    if w.ragged:
+        # gamma_b uniform in [1, gamma]; the stop ids are frequent target tokens
+        # (the argmax of sequence 0's rows) so that some rounds stop early;
+        # budgets uniform in [1, gamma + 2]
+        out["gamma_b"] = torch.randint(1, G + 1, (B,), generator=g, device=device, dtype=torch.int32)
+        stops = logits[0, : w.n_stop].float().argmax(-1).to(torch.int32)
+        out["stop_tokens"] = stops.contiguous()
+        out["max_new"] = torch.randint(1, G + 3, (B,), generator=g, device=device, dtype=torch.int32)
+    return out
