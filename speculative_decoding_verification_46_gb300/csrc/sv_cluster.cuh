@@ -368,7 +368,7 @@ cluster_kernel(const ClusterParams cp) {
   acc.zero();
   if (!bad) cluster_run<T>(Lf + r0, Qf ? Qf + r0 : nullptr, xq - r0, rlen, resid, M, p.c, p.c_lo, s_a, &acc);
   {
-    const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
+    const F2x3 t = block_sum_f2x3_w0(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);   // warp 0 pushes
     if (tid < CN) *cluster.map_shared_rank(&sm.allsub[rank], tid) = t;
   }
   cluster.sync();

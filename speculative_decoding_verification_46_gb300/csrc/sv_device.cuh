@@ -1212,12 +1212,16 @@ rows_kernel(const Params p) {
   finish_sequence_topk(p, b, sm);
 }
 
-// Three two-float block sums in one pass (one pair of barriers).
+// Three two-float sums reduced together.
 struct F2x3 {
   F2 a, b, c;
 };
-__device__ __forceinline__ F2x3 block_sum_f2x3(F2x3 v, F2x3* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+// Block-wide F2x3 sum (one pair of barriers), valid in the lanes of warp 0
+// only (the callers need the total in one thread or in warp 0): the per-warp
+// totals are combined by warp 0 in a shuffle tree instead of by every thread.
+__device__ __forceinline__ F2x3 block_sum_f2x3_w0(F2x3 v, F2x3* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
     v.a = f2_add(v.a, f2_shfl_xor(v.a, m));
@@ -1227,11 +1231,21 @@ __device__ __forceinline__ F2x3 block_sum_f2x3(F2x3 v, F2x3* sm) {
   __syncthreads();
   if (lane == 0) sm[warp] = v;
   __syncthreads();
-  F2x3 t = sm[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
-    t.a = f2_add(t.a, sm[w].a);
-    t.b = f2_add(t.b, sm[w].b);
-    t.c = f2_add(t.c, sm[w].c);
+  F2x3 t{F2{0.f, 0.f}, F2{0.f, 0.f}, F2{0.f, 0.f}};
+  if (warp == 0) {
+    if (lane < nw) t = sm[lane];
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      if (m < nw) {   // block-uniform: a tree over the first (power of two >= nw) lanes
+        t.a = f2_add(t.a, f2_shfl_xor(t.a, m));
+        t.b = f2_add(t.b, f2_shfl_xor(t.b, m));
+        t.c = f2_add(t.c, f2_shfl_xor(t.c, m));
+      }
+    }
+    // lanes 0 .. (power of two >= nw) - 1 hold the total: give it to all 32
+    t.a = F2{__shfl_sync(0xffffffffu, t.a.hi, 0), __shfl_sync(0xffffffffu, t.a.lo, 0)};
+    t.b = F2{__shfl_sync(0xffffffffu, t.b.hi, 0), __shfl_sync(0xffffffffu, t.b.lo, 0)};
+    t.c = F2{__shfl_sync(0xffffffffu, t.c.hi, 0), __shfl_sync(0xffffffffu, t.c.lo, 0)};
   }
   return t;
 }
@@ -1315,16 +1329,15 @@ __device__ __forceinline__ float tok_exponent(float x, float M, float c, float c
 // ex2.approx.ftz.f32 and exp2f agree - and its residual w - s' q with one
 // rounding) and run_tail returns false; a token near the maximum is left to
 // run_top (two-float exp2, exact residual) and run_tail returns true.
-template <bool EXACT_DIFF>
-__device__ __forceinline__ bool run_tail(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
-                                         float s_a) {
+template <bool EXACT_DIFF, bool USE_Q>
+__device__ __forceinline__ bool run_tail_t(RunAcc& acc, float x, float qv, float M, float c, float c_lo, float s_a) {
   float e;
   const float p = tok_exponent<EXACT_DIFF>(x, M, c, c_lo, &e);
   const bool top = p > -8.f;
   const float y = ex2_approx(p);   // results below 2^-126 flush to 0
   const float w = (top || !(p > -1e30f)) ? 0.f : fmaf(y * 6.931471825e-01f, e, y);
   RunAcc::acc2(acc.sh, acc.sl, w, 0.f);
-  if (use_q) {
+  if (USE_Q) {
     const float pr = s_a * qv;
     if (w > pr) {
       RunAcc::acc2(acc.ah, acc.al, fmaf(-s_a, qv, w), 0.f);
@@ -1332,6 +1345,12 @@ __device__ __forceinline__ bool run_tail(RunAcc& acc, float x, float qv, bool us
     }
   }
   return top;
+}
+template <bool EXACT_DIFF>
+__device__ __forceinline__ bool run_tail(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
+                                         float s_a) {
+  return use_q ? run_tail_t<EXACT_DIFF, true>(acc, x, qv, M, c, c_lo, s_a)
+               : run_tail_t<EXACT_DIFF, false>(acc, x, qv, M, c, c_lo, s_a);
 }
 template <bool EXACT_DIFF>
 __device__ __forceinline__ void run_top(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
@@ -1369,6 +1388,71 @@ struct ResStage {
 __device__ __forceinline__ void res_cp16(void* smem, const void* gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+// The branch-free tail sweep over a staged run (see run_accumulate): USE_Q
+// for a residual row, DET when q is a deterministic draft's one-hot (q = +inf
+// at token xq takes it out of the support, q = 0 elsewhere).  Returns the
+// bit mask of run offsets near the row maximum, left to run_top.
+template <typename T, bool USE_Q, bool DET>
+__device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, bool have_q, int xq, int e0, int NS,
+                                              int V, float M, float c, float c_lo, float s_a, RunAcc* acc) {
+  constexpr int VW = Tr<T>::VW;
+  constexpr bool EXACT = sizeof(T) == 2;
+  const int tid = threadIdx.x;
+  uint32_t top = 0u;
+#pragma unroll 1
+  for (int j = 0; j < NS; ++j) {
+    const uint4 v = lg[j * kThreads + tid];
+    float qv[VW];
+#pragma unroll
+    for (int h = 0; h < VW / 4; ++h) {
+      if (USE_Q && have_q) {
+        const uint4 q4 = qq[(j * (VW / 4) + h) * kThreads + tid];
+        qv[4 * h + 0] = __uint_as_float(q4.x);
+        qv[4 * h + 1] = __uint_as_float(q4.y);
+        qv[4 * h + 2] = __uint_as_float(q4.z);
+        qv[4 * h + 3] = __uint_as_float(q4.w);
+      } else {
+        qv[4 * h + 0] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
+      }
+    }
+    const int ev = e0 + j * VW;
+    const int lim = V - ev;          // tokens of this vector inside the row
+    const int xo = xq - ev;          // the one-hot token's offset (DET)
+    // no token of the vector near the maximum (the vector maximum's exponent,
+    // formed the same way, bounds every token's): the short path, for 16-bit
+    // logits whose x - M is exact; -inf is clamped to a weight that ex2.approx
+    // flushes to 0 (as any exponent below -126)
+    const bool vtop = (Tr<T>::template vmax<false>(v) - M) * c > -8.f;
+    if (EXACT && !vtop && lim >= VW) {
+#pragma unroll
+      for (int t = 0; t < VW; ++t) {
+        const float dh = fmaxf(Tr<T>::get(v, t) - M, -1.0e4f);
+        const float p = dh * c;
+        const float e = fmaf(dh, c_lo, fmaf(dh, c, -p));
+        const float y = ex2_approx(p);
+        const float w = fmaf(y * 6.931471825e-01f, e, y);
+        RunAcc::acc2(acc->sh, acc->sl, w, 0.f);
+        if (USE_Q) {
+          const float qt = (DET && t == xo) ? INFINITY : qv[t];
+          if (w > s_a * qt) {
+            RunAcc::acc2(acc->ah, acc->al, fmaf(-s_a, qt, w), 0.f);
+            acc->q += qt;
+          }
+        }
+      }
+      continue;
+    }
+    uint32_t tv = 0u;
+#pragma unroll
+    for (int t = 0; t < VW; ++t) {
+      const float qt = (DET && t == xo) ? INFINITY : qv[t];
+      if (t < lim && run_tail_t<EXACT, USE_Q>(*acc, Tr<T>::get(v, t), qt, M, c, c_lo, s_a)) tv |= 1u << t;
+    }
+    top |= tv << (j * VW);
+  }
+  return top;
 }
 
 // (S, A, Q) of the run [e0, e0 + NS * VW) of the final-draw row (tokens >= V
@@ -1410,33 +1494,16 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
-  // tail tokens in one branch-free sweep; tokens near the maximum (bit set
-  // in `top`) in a second loop
-  uint32_t top = 0u;
-#pragma unroll 1
-  for (int j = 0; j < NS; ++j) {
-    const uint4 v = lg[j * kThreads + tid];
-    float qv[VW];
-#pragma unroll
-    for (int h = 0; h < VW / 4; ++h) {
-      if (qrow) {
-        const uint4 q4 = qq[(j * (VW / 4) + h) * kThreads + tid];
-        qv[4 * h + 0] = __uint_as_float(q4.x);
-        qv[4 * h + 1] = __uint_as_float(q4.y);
-        qv[4 * h + 2] = __uint_as_float(q4.z);
-        qv[4 * h + 3] = __uint_as_float(q4.w);
-      } else {
-        qv[4 * h + 0] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
-      }
-    }
-    const int ev = e0 + j * VW;
-#pragma unroll
-    for (int t = 0; t < VW; ++t) {
-      const float qt = (ev + t == xq) ? INFINITY : qv[t];
-      if (ev + t < V && run_tail<EXACT>(*acc, Tr<T>::get(v, t), qt, use_q, M, c, c_lo, s_a))
-        top |= 1u << (j * VW + t);
-    }
-  }
+  // tail tokens in one branch-free sweep (specialised for the residual /
+  // bonus rows and for a deterministic draft's one-hot q); tokens near the
+  // maximum (bit set in `top`) in a second loop
+  uint32_t top;
+  if (!use_q)
+    top = run_sweep<T, false, false>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
+  else if (xq < 0)
+    top = run_sweep<T, true, false>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
+  else
+    top = run_sweep<T, true, true>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
   while (top) {
     const int o = __ffs(top) - 1;   // offset in the run
     top &= top - 1;
@@ -1507,7 +1574,7 @@ residual_kernel(const Params p) {
   if (!bad)
     run_accumulate<T>(row, qrow, xq, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc);
   {
-    const F2x3 t = block_sum_f2x3(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
+    const F2x3 t = block_sum_f2x3_w0(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
     if (tid == 0) {
       cS[c] = t.a;
       cA[c] = t.b;
