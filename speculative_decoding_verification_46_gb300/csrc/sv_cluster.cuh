@@ -59,6 +59,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 struct ClusterSmem {
+  float tab[128];            // exp2_f2 table
   float4 allpart[kClusterMax][kMaxG1];   // every CTA's per-row partial (pushed by its owner):
                                          // (max, s_hi, s_lo) or (max, index)
   float ur[kMaxG1];          // this sequence's uniforms
@@ -125,7 +126,7 @@ __device__ __forceinline__ float4 group_merge(float4 v, int CN, float c) {
 // in one sweep, the tokens near the maximum (bits of `top`) after.
 template <typename T>
 __device__ __forceinline__ void cluster_run(const T* L, const float* Q, int xq, int len, bool use_q, float M,
-                                            float c, float c_lo, float s_a, RunAcc* acc) {
+                                            float c, float c_lo, float s_a, RunAcc* acc, const float* tab) {
   constexpr int VW = Tr<T>::VW;
   constexpr bool EXACT = sizeof(T) == 2;
   uint64_t top = 0ull;
@@ -150,7 +151,7 @@ __device__ __forceinline__ void cluster_run(const T* L, const float* Q, int xq, 
     const int o = __ffsll((long long)top) - 1;
     top &= top - 1;
     const float x = Tr<T>::get(*reinterpret_cast<const uint4*>(L + (o / VW) * VW), o % VW);
-    run_top<EXACT>(*acc, x, o == xq ? INFINITY : (Q ? Q[o] : 0.f), use_q, M, c, c_lo, s_a);
+    run_top<EXACT>(*acc, x, o == xq ? INFINITY : (Q ? Q[o] : 0.f), use_q, M, c, c_lo, s_a, tab);
   }
 }
 
@@ -178,6 +179,7 @@ cluster_kernel(const ClusterParams cp) {
   // distributed shared memory may only be written once every CTA of the
   // cluster runs: arrive now, wait just before the first remote store
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  load_exp2_table(sm.tab);
 
   // ---- issue every load of the step: logits slices, then q slices
   const T* Lg = static_cast<const T*>(p.logits) + (size_t)b * G1 * V;
@@ -200,21 +202,18 @@ cluster_kernel(const ClusterParams cp) {
   // this sequence's drafts with their logit and q value (plain loads, in
   // flight together with the slices; every CTA needs them for the scan)
   int d_own = -1;
-  float l_own = 0.f, q_own = 0.f, u_own = 0.f;
+  uint32_t l_bits = 0u;   // the raw logit bits: converted where they are used
+  float q_own = 0.f, u_own = 0.f;
   if (tid < gb) {
     d_own = __ldg(p.draft + b * G + tid);
     if (d_own >= 0 && d_own < V) {
-      l_own = Tr<T>::get(load_slot<T>(Lg + (size_t)tid * V, d_own, 1, false), 0);
+      l_bits = Tr<T>::scalar_bits(Lg + (size_t)tid * V + d_own);
       if (MODE == MODE_SOFTMAX) q_own = p.q ? __ldg(p.q + ((size_t)b * G + tid) * V + d_own) : 1.f;
     }
   }
   if (MODE == MODE_SOFTMAX && tid < G1) u_own = __ldg(p.uniforms + b * G1 + tid);
   if (tid < G1) sm.ur[tid] = u_own;
-  if (tid < G) {
-    sm.dr[tid] = d_own;
-    sm.dl[tid] = l_own;
-    sm.dq[tid] = q_own;
-  }
+  if (tid < G) sm.dr[tid] = d_own;
   cp_async_wait<1>();
   __syncthreads();
 
@@ -265,6 +264,14 @@ cluster_kernel(const ClusterParams cp) {
       for (int m = 16; m >= 1; m >>= 1) s = f2_add(s, f2_shfl_xor(s, m));
       if (lane < CN) *cluster.map_shared_rank(&sm.allpart[rank][i], lane) = make_float4(M, s.hi, s.lo, 0.f);
     }
+  }
+  // the drafts' l(d_i), q(d_i): loaded at the start, consumed only now, so
+  // their latency hides behind the slice loads and the row partials
+  if (tid < G) {
+    uint4 lv = make_uint4(0u, 0u, 0u, 0u);
+    Tr<T>::put(lv, 0, l_bits);
+    sm.dl[tid] = Tr<T>::get(lv, 0);
+    sm.dq[tid] = q_own;
   }
   cluster.sync();
 
@@ -366,7 +373,7 @@ cluster_kernel(const ClusterParams cp) {
   // this thread's run sums stay in registers: the owner walks them again below
   RunAcc acc;
   acc.zero();
-  if (!bad) cluster_run<T>(Lf + r0, Qf ? Qf + r0 : nullptr, xq - r0, rlen, resid, M, p.c, p.c_lo, s_a, &acc);
+  if (!bad) cluster_run<T>(Lf + r0, Qf ? Qf + r0 : nullptr, xq - r0, rlen, resid, M, p.c, p.c_lo, s_a, &acc, sm.tab);
   {
     const F2x3 t = block_sum_f2x3_w0(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);   // warp 0 pushes
     if (tid < CN) *cluster.map_shared_rank(&sm.allsub[rank], tid) = t;
@@ -457,7 +464,7 @@ cluster_kernel(const ClusterParams cp) {
         if (c0 + lane < olen) {
           const float x = TR::get(*reinterpret_cast<const uint4*>(Lf + (e / VW) * VW), e % VW);
           const float qv = uq ? (Qf ? Qf[e] : (e == xq ? INFINITY : 0.f)) : 0.f;
-          m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
+          m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds, sm.tab);
         }
         const F2 inc = warp_incl_scan_f2(m);
         F2 excl = f2_shfl_up(inc, 1);

@@ -312,8 +312,9 @@ __device__ const float kExp2Lo[64] = {
 // table-driven method): k = round(64 a), 2^a = 2^(k>>6) * 2^((k&63)/64) * e^g
 // with g = (a - k/64) ln 2, |g| <= ln 2 / 128.  The 64 values 2^(j/64) are
 // float pairs from their exact values; e^g = 1 + g + (g^2/2 + g^3/6 + g^4/24),
-// the bracket (< 2e-5) in float32.  a.hi < -125 gives 0.
-__device__ __forceinline__ F2 exp2_f2(F2 a) {
+// the bracket (< 2e-5) in float32.  a.hi < -125 gives 0.  tab: the 64 high
+// then the 64 low parts, staged in shared memory by load_exp2_table.
+__device__ __forceinline__ F2 exp2_f2(F2 a, const float* tab) {
   const F2 kLn2{6.931471825e-01f, -1.904654212e-09f};
   if (a.hi < -125.f) return F2{0.f, 0.f};
   const float k = rintf(a.hi * 64.f);
@@ -325,11 +326,17 @@ __device__ __forceinline__ F2 exp2_f2(F2 a) {
   const float el = ((1.f - eh) + gh) + (gl + small);
   const int ki = (int)k;
   const int j = ki & 63;
-  const float th = __ldg(kExp2Hi + j), tl = __ldg(kExp2Lo + j);
+  const float th = tab[j], tl = tab[64 + j];
   const float yh = th * eh;
   const float yl = fmaf(th, eh, -yh) + fmaf(th, el, tl * eh);
   const float scale = __int_as_float((127 + (ki >> 6)) << 23);   // 2^(k>>6), k>>6 in [-125, 127]
   return F2{yh * scale, yl * scale};
+}
+
+// Stage the exp2_f2 table (128 floats) in shared memory; visible to the
+// block after its next barrier.
+__device__ __forceinline__ void load_exp2_table(float* tab) {
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = i < 64 ? __ldg(kExp2Hi + i) : __ldg(kExp2Lo + i - 64);
 }
 
 // Ordering of normalised two-float numbers (|lo| <= ulp(hi) / 2, as f2_add
@@ -1354,10 +1361,10 @@ __device__ __forceinline__ bool run_tail(RunAcc& acc, float x, float qv, bool us
 }
 template <bool EXACT_DIFF>
 __device__ __forceinline__ void run_top(RunAcc& acc, float x, float qv, bool use_q, float M, float c, float c_lo,
-                                        float s_a) {
+                                        float s_a, const float* tab) {
   float e;
   const float p = tok_exponent<EXACT_DIFF>(x, M, c, c_lo, &e);
-  acc.add(exp2_f2(f2_norm(p, e)), qv, use_q, s_a);
+  acc.add(exp2_f2(f2_norm(p, e), tab), qv, use_q, s_a);
 }
 
 // One token's increment of the walked mass, with the run's arithmetic: the
@@ -1365,11 +1372,11 @@ __device__ __forceinline__ void run_top(RunAcc& acc, float x, float qv, bool use
 // w - s' q - (s - s') q.
 template <bool EXACT_DIFF>
 __device__ __forceinline__ F2 token_mass(float x, float qv, bool use_q, float M, float c, float c_lo, float s_a,
-                                         F2 ds) {
+                                         F2 ds, const float* tab) {
   RunAcc one;
   one.zero();
   if (run_tail<EXACT_DIFF>(one, x, qv, use_q, M, c, c_lo, s_a))
-    run_top<EXACT_DIFF>(one, x, qv, use_q, M, c, c_lo, s_a);
+    run_top<EXACT_DIFF>(one, x, qv, use_q, M, c, c_lo, s_a, tab);
   F2 m = one.mass(use_q, ds);
   if (m.hi < 0.f) m = F2{0.f, 0.f};
   return m;
@@ -1462,7 +1469,7 @@ template <typename T>
 __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, int xq, int e0, int NS, int V,
                                                bool vec_ok,
                                                bool use_q, float M, float c, float c_lo, float s_a, uint4* stage,
-                                               RunAcc* acc) {
+                                               RunAcc* acc, const float* tab) {
   using RS = ResStage<T>;
   constexpr int VW = RS::VW;
   constexpr bool EXACT = sizeof(T) == 2;
@@ -1512,11 +1519,109 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
     const float qv = (e0 + o == xq) ? INFINITY
                                     : (qrow ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3))
                                             : 0.f);
-    run_top<EXACT>(*acc, x, qv, use_q, M, c, c_lo, s_a);
+    run_top<EXACT>(*acc, x, qv, use_q, M, c, c_lo, s_a, tab);
   }
 }
 
+// Warp 0 of the finishing CTA: the chunk sums (S, A, Q) of one sequence read
+// once into registers (C <= kPickChunks), the exact normaliser s, the masses
+// (A - (s - s') Q for a residual, S for the bonus) and the inverse-CDF step
+// over the chunks: the first chunk whose [prefix, prefix + mass) holds
+// u * R, else the last chunk with positive mass.  Both passes add in the same
+// order (32-chunk groups, a two-float scan per group, a running carry).
+constexpr int kPickGroups = 4;
+constexpr int kPickChunks = 32 * kPickGroups;
+
+struct ChunkPick {
+  int sub;        // chosen chunk, -1 if none
+  int resid0;     // the residual had no mass: drawn from p_n instead
+  F2 base, target, ds;
+};
+
+__device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, const F2* cQ, int C, bool resid,
+                                                   bool bad, float s_a, float u) {
+  const int lane = threadIdx.x & 31;
+  F2 Sg[kPickGroups], Mg[kPickGroups];
+  float Qg[kPickGroups];
+#pragma unroll
+  for (int g = 0; g < kPickGroups; ++g) {
+    const int k = g * 32 + lane;
+    Sg[g] = Mg[g] = F2{0.f, 0.f};
+    Qg[g] = 0.f;
+    if (k < C) {
+      const float2 sv = __ldcg(reinterpret_cast<const float2*>(cS) + k);
+      Sg[g] = F2{sv.x, sv.y};
+      if (resid) {
+        const float2 av = __ldcg(reinterpret_cast<const float2*>(cA) + k);
+        Mg[g] = F2{av.x, av.y};
+        Qg[g] = __ldcg(reinterpret_cast<const float2*>(cQ) + k).x;
+      }
+    }
+  }
+  F2 sl = Sg[0];
+#pragma unroll
+  for (int g = 1; g < kPickGroups; ++g) sl = f2_add(sl, Sg[g]);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) sl = f2_add(sl, f2_shfl_xor(sl, m));
+  ChunkPick r;
+  r.ds = f2_add(sl, F2{-s_a, 0.f});          // s - s', tiny
+  r.resid0 = 0;
+#pragma unroll
+  for (int g = 0; g < kPickGroups; ++g) {
+    if (resid) {
+      Mg[g] = f2_add(Mg[g], f2_neg(f2_scale(r.ds, Qg[g])));
+      if (Mg[g].hi < 0.f) Mg[g] = F2{0.f, 0.f};
+    } else {
+      Mg[g] = Sg[g];
+    }
+  }
+  auto total = [&](const F2* m) {
+    F2 carry{0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < kPickGroups; ++g) {
+      const F2 inc = f2_add(carry, warp_incl_scan_f2(m[g]));
+      carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+    }
+    return carry;
+  };
+  F2 R = total(Mg);
+  if (resid && !bad && !f2_pos(R)) {
+    r.resid0 = 1;   // zero residual mass (only through rounding): draw from p_n instead
+#pragma unroll
+    for (int g = 0; g < kPickGroups; ++g) Mg[g] = Sg[g];
+    R = total(Mg);
+  }
+  r.target = f2_scale(R, u);
+  int found = -1, last = -1;
+  F2 fbase{0.f, 0.f}, lbase{0.f, 0.f}, carry{0.f, 0.f};
+#pragma unroll
+  for (int g = 0; g < kPickGroups; ++g) {
+    const F2 inc = f2_add(carry, warp_incl_scan_f2(Mg[g]));
+    F2 excl = f2_shfl_up(inc, 1);
+    if (lane == 0) excl = carry;
+    const bool live = g * 32 + lane < C && f2_pos(Mg[g]);
+    const unsigned hit =
+        __ballot_sync(0xffffffffu, live && !f2_lt(r.target, excl) && f2_lt(r.target, f2_add(excl, Mg[g])));
+    const unsigned pos = __ballot_sync(0xffffffffu, live);
+    if (hit && found < 0) {
+      const int l = __ffs(hit) - 1;
+      found = g * 32 + l;
+      fbase = F2{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
+    }
+    if (pos) {
+      const int l = 31 - __clz(pos);
+      last = g * 32 + l;
+      lbase = F2{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
+    }
+    carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+  }
+  r.sub = (bad || !f2_pos(R)) ? -1 : (found >= 0 ? found : last);
+  r.base = found >= 0 ? fbase : lbase;
+  return r;
+}
+
 struct ResSmem {
+  float tab[128];   // exp2_f2 table
   F2x3 red[kWarps];
   F2 f2red[kWarps];
   int flag;
@@ -1540,6 +1645,7 @@ residual_kernel(const Params p) {
   __shared__ ResSmem sm;
   extern __shared__ __align__(16) unsigned char res_dyn[];
   uint4* stage = reinterpret_cast<uint4*>(res_dyn);   // ResStage<T>::bytes
+  load_exp2_table(sm.tab);   // independent of the previous kernel: before the wait
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31;
   const int C = p.C;
@@ -1572,7 +1678,8 @@ residual_kernel(const Params p) {
   RunAcc acc;
   acc.zero();
   if (!bad)
-    run_accumulate<T>(row, qrow, xq, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc);
+    run_accumulate<T>(row, qrow, xq, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc,
+                      sm.tab);
   {
     const F2x3 t = block_sum_f2x3_w0(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
     if (tid == 0) {
@@ -1585,44 +1692,64 @@ residual_kernel(const Params p) {
 
   // ---- last CTA of sequence b: exact normaliser, masses, chunk -> thread -> token
   int status = st.status;
-  F2 sl{0.f, 0.f};
-  for (int k2 = tid; k2 < C; k2 += kThreads) {
-    const float2 v = __ldcg(reinterpret_cast<const float2*>(cS) + k2);
-    sl = f2_add(sl, F2{v.x, v.y});
-  }
-  const F2 s = block_sum_f2(sl, sm.f2red);
-  const F2 ds = f2_add(s, F2{-s_a, 0.f});          // s - s', tiny
-  if (resid) {
-    // residual masses A - (s - s') Q overwrite the A block
-    for (int k2 = tid; k2 < C; k2 += kThreads) {
-      const float2 a2 = __ldcg(reinterpret_cast<const float2*>(cA) + k2);
-      const float2 q2 = __ldcg(reinterpret_cast<const float2*>(cQ) + k2);
-      F2 m = f2_add(F2{a2.x, a2.y}, f2_neg(f2_mul(ds, F2{q2.x, q2.y})));
-      if (m.hi < 0.f) m = F2{0.f, 0.f};
-      cA[k2] = m;
-    }
-    __threadfence_block();
-    __syncthreads();
-  }
   const float u = __ldg(p.uniforms + b * G1 + gb);
-  F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
-  bool use_q = resid;
-  int sub = locate(resid ? cA : cS, C, u, &R, &base, &tgt, sm.loc, true);
-  if (resid && !bad && !f2_pos(R)) {
-    // zero residual mass (only through rounding): draw from p_n instead
-    status |= SEQ_RESID0;
-    use_q = false;
-    sub = locate(cS, C, u, &R, &base, &tgt, sm.loc, true);
-  }
-  if (tid == 0) {
-    sm.sub = (bad || !f2_pos(R)) ? -1 : sub;
-    sm.base = base;
-    sm.target = tgt;
-    sm.token = -1;
-    sm.use_q = use_q;
-    sm.ds = ds;
-    sm.owner = 0x7fffffff;
-    sm.lastpos = -1;
+  if (C <= kPickChunks) {
+    if (tid < 32) {
+      const ChunkPick pk = chunk_pick_w0(cS, cA, cQ, C, resid, bad, s_a, u);
+      if (tid == 0) {
+        sm.sub = pk.sub;
+        sm.base = pk.base;
+        sm.target = pk.target;
+        sm.token = -1;
+        sm.use_q = resid && !pk.resid0;
+        sm.ds = pk.ds;
+        sm.owner = 0x7fffffff;
+        sm.lastpos = -1;
+        sm.flag = pk.resid0;
+      }
+    }
+    __syncthreads();
+    if (sm.flag) status |= SEQ_RESID0;
+  } else {
+    // many chunks (very large vocabularies): the block-wide search
+    F2 sl{0.f, 0.f};
+    for (int k2 = tid; k2 < C; k2 += kThreads) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(cS) + k2);
+      sl = f2_add(sl, F2{v.x, v.y});
+    }
+    const F2 s = block_sum_f2(sl, sm.f2red);
+    const F2 ds = f2_add(s, F2{-s_a, 0.f});          // s - s', tiny
+    if (resid) {
+      // residual masses A - (s - s') Q overwrite the A block
+      for (int k2 = tid; k2 < C; k2 += kThreads) {
+        const float2 a2 = __ldcg(reinterpret_cast<const float2*>(cA) + k2);
+        const float2 q2 = __ldcg(reinterpret_cast<const float2*>(cQ) + k2);
+        F2 m = f2_add(F2{a2.x, a2.y}, f2_neg(f2_mul(ds, F2{q2.x, q2.y})));
+        if (m.hi < 0.f) m = F2{0.f, 0.f};
+        cA[k2] = m;
+      }
+      __threadfence_block();
+      __syncthreads();
+    }
+    F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
+    bool use_q = resid;
+    int sub = locate(resid ? cA : cS, C, u, &R, &base, &tgt, sm.loc, true);
+    if (resid && !bad && !f2_pos(R)) {
+      // zero residual mass (only through rounding): draw from p_n instead
+      status |= SEQ_RESID0;
+      use_q = false;
+      sub = locate(cS, C, u, &R, &base, &tgt, sm.loc, true);
+    }
+    if (tid == 0) {
+      sm.sub = (bad || !f2_pos(R)) ? -1 : sub;
+      sm.base = base;
+      sm.target = tgt;
+      sm.token = -1;
+      sm.use_q = use_q;
+      sm.ds = ds;
+      sm.owner = 0x7fffffff;
+      sm.lastpos = -1;
+    }
   }
   __syncthreads();
   int token = 0;
@@ -1632,7 +1759,7 @@ residual_kernel(const Params p) {
     RunAcc r;
     r.zero();
     run_accumulate<T>(row, uq ? qrow : nullptr, xq, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, stage,
-                      &r);
+                      &r, sm.tab);
     F2 mine = r.mass(uq, sm.ds);
     if (mine.hi < 0.f) mine = F2{0.f, 0.f};
     F2 total;
@@ -1652,9 +1779,15 @@ residual_kernel(const Params p) {
       const int e = c0 + owner * EPT + lane;
       F2 m{0.f, 0.f};
       if (lane < EPT && e < V) {
-        const float x = TR::get(load_slot<T>(row, e, 1, false), 0);
-        const float qv = uq ? (qrow ? __ldg(qrow + e) : (e == xq ? INFINITY : 0.f)) : 0.f;
-        m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds);
+        // the owner's run is still staged in shared memory (run_accumulate)
+        const int j = lane / VW, t = lane - j * VW;
+        const float x = TR::get(stage[j * kThreads + owner], t);
+        const float qv =
+            uq ? (qrow ? __uint_as_float(word_of(
+                             stage[(ResStage<T>::NL + j * (VW / 4) + t / 4) * kThreads + owner], t & 3))
+                       : (e == xq ? INFINITY : 0.f))
+               : 0.f;
+        m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds, sm.tab);
       }
       const F2 inc = warp_incl_scan_f2(m);
       F2 excl = f2_shfl_up(inc, 1);
