@@ -16,9 +16,9 @@
 //   greedy   per-row argmax (ties -> lowest index; NaN flagged)
 //   softmax  per-row online max / sum of 2^((L - m) c) with rescaling when the
 //            running max grows; p(d_i) and a_i at the row's end
-//   top-k    pass 1 keeps per-thread maxima (and the vector holding it); the
+//   top-k    pass 1 keeps per-thread maxima (and the two best vectors); the
 //            k-th largest is a lower bound tau of the row's k-th value; only
-//            threads with a second vector reaching tau are re-read (L2);
+//            threads with a third vector reaching tau are re-read (L2);
 //            exact rank selection of the candidates >= tau; softmax(./T) +
 //            top-p; a_i
 //
@@ -374,13 +374,80 @@ stream_dense_kernel(const Params p) {
 
 // ---- top-k streaming kernel
 //
-// Pass 1 (the ring) keeps each thread's maximum m1, the 16-byte vector that
-// holds it and m2, the largest maximum of its other vectors.  tau = the k-th
+// Pass 1 (the ring) keeps each thread's two best 16-byte vectors (maxima m1 >=
+// m2) and m3, the largest maximum of its other vectors.  tau = the k-th
 // largest thread maximum is a lower bound of the row's k-th largest value.
-// Only threads with m1 >= tau hold elements >= tau; if m2 < tau they are all
-// in the kept vector.  The few threads with m2 >= tau too are re-read (pass 2,
-// an L2 hit, spread over the whole CTA).  The candidates (all elements >=
+// Only threads with m1 >= tau hold elements >= tau; if m3 < tau they are all
+// in the two kept vectors.  The rare threads with m3 >= tau too are re-read
+// (pass 2, an L2 hit, spread over the whole CTA).  The candidates (all elements >=
 // tau) are ranked exactly by (value desc, index asc).
+// The largest K (bits below LOW zero) such that at least k of the block's
+// 256 keys (one per thread; 0 = no key) are >= K: the k-th largest key with
+// its bits below LOW cleared, 0 if fewer than k keys are positive.  Radix
+// select from the top digit down: a shared-memory histogram of the digit
+// among the keys that match the digits found so far, then warp 0 finds the
+// digit holding the k-th largest by a scan from the top.
+template <int LOW>
+__device__ __forceinline__ uint32_t kth_largest_key(uint32_t key, int k, TopkSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t prefix = 0u;
+  int rank = k;   // rank sought among the keys matching prefix
+#pragma unroll
+  for (int hi = 31; hi >= LOW; hi -= 8) {
+    const int lo = hi - 7 > LOW ? hi - 7 : LOW;
+    const int nb = hi - lo + 1;
+    const uint32_t upper = hi == 31 ? 0u : ~((1u << (hi + 1)) - 1u);   // the digits already found
+    sm.hist[tid] = 0;
+    __syncthreads();
+    if (key != 0u && (key & upper) == prefix) atomicAdd(&sm.hist[(key >> lo) & ((1u << nb) - 1u)], 1);
+    __syncthreads();
+    if (tid < 32) {
+      // lane l holds digits 255 - 8l .. 248 - 8l (top first)
+      int c[8];
+      int lsum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        c[e] = sm.hist[255 - 8 * lane - e];
+        lsum += c[e];
+      }
+      int inc = lsum;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, m);
+        if (lane >= m) inc += o;
+      }
+      const int excl = inc - lsum;
+      const unsigned hit = __ballot_sync(0xffffffffu, excl < rank && inc >= rank);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        if (lane == l) {
+          int run = excl;
+          int dg = 255 - 8 * lane;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (run + c[e] >= rank) {
+              dg = 255 - 8 * lane - e;
+              break;
+            }
+            run += c[e];
+          }
+          sm.pick_digit = dg;
+          sm.pick_rank = rank - run;
+        }
+      } else if (lane == 0) {
+        sm.pick_digit = -1;   // fewer than rank keys left: no key qualifies
+        sm.pick_rank = rank;
+      }
+    }
+    __syncthreads();
+    const int dg = sm.pick_digit;
+    if (dg < 0) return 0u;
+    prefix |= (uint32_t)dg << lo;
+    rank = sm.pick_rank;
+  }
+  return prefix;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kSt, 3)
 stream_topk_kernel(const Params p) {
@@ -424,12 +491,12 @@ stream_topk_kernel(const Params p) {
       d_row = __ldg(p.draft + b * G + i);
       if (d_row >= 0 && d_row < V) q_row = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d_row) : 1.f;
     }
-    // ---- pass 1 through the ring: per thread its maximum m1, the vector
-    // holding it (first such vector; kept in registers) and m2 = the largest
-    // maximum among its other vectors
-    float m1 = -INFINITY, m2 = -INFINITY;
-    uint4 bvec = make_uint4(0u, 0u, 0u, 0u);
-    int bv = -1;
+    // ---- pass 1 through the ring: per thread its two best 16-byte vectors
+    // (by maximum; the first such vector on ties) kept in registers with
+    // their maxima m1 >= m2, and m3 = the largest maximum of its other vectors
+    float m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    uint4 bvec = make_uint4(0u, 0u, 0u, 0u), bvec2 = bvec;
+    int bv = -1, bv2 = -1;
     int nan_seen = 0;
     for (int c = 0; c < w.NCH; ++c) {
       cpa_wait<S - 1>();
@@ -441,29 +508,36 @@ stream_topk_kernel(const Params p) {
           const uint4 x = slot[u * kSt + tid];
           const float vm = TR::template vmax<true>(x);
           nan_seen |= (vm != vm);
-          m2 = fmaxf(m2, fminf(vm, m1));
-          if (vm > m1) {
-            m1 = vm;
-            bvec = x;
-            bv = v;
+          m3 = fmaxf(m3, fminf(vm, m2));   // the vector that leaves the top two
+          if (vm > m2) {
+            if (vm > m1) {
+              m2 = m1;
+              bvec2 = bvec;
+              bv2 = bv;
+              m1 = vm;
+              bvec = x;
+              bv = v;
+            } else {
+              m2 = vm;
+              bvec2 = x;
+              bv2 = v;
+            }
           }
         }
       }
       iss.issue(ring, logits, V, w);
       stage = (stage + 1 == S) ? 0 : stage + 1;
     }
-    // ---- tau: the k-th largest finite thread maximum (bisection on keys)
+    // ---- tau: the k-th largest finite thread maximum (its key bits from
+    // bit 31 down to KEY_LOW_BIT, found by a radix select)
     const uint32_t tkey = m1 > -INFINITY ? okey(m1) : 0u;
-    uint32_t K = 0u;
-    for (int bit = 31; bit >= TR::KEY_LOW_BIT; --bit) {
-      const uint32_t Kt = K | (1u << bit);
-      if (__syncthreads_count(tkey >= Kt) >= k) K = Kt;
-    }
+    const uint32_t K = kth_largest_key<TR::KEY_LOW_BIT>(tkey, k, sm);
     const float tau = K == 0u ? -INFINITY : key_to_float(K);
-    // ---- candidates.  A thread with m1 >= tau and m2 < tau has all its
-    // elements >= tau in bvec; one with m2 >= tau too is re-read (pass 2).
+    // ---- candidates.  A thread with m1 >= tau and m3 < tau has all its
+    // elements >= tau in its two kept vectors; one with m3 >= tau too is
+    // re-read (pass 2).
     if (m1 > -INFINITY && m1 >= tau) {
-      if (m2 > -INFINITY && m2 >= tau) {
+      if (m3 > -INFINITY && m3 >= tau) {
         sm.rel[atomicAdd(&sm.nrel, 1)] = tid;
       } else {
 #pragma unroll
@@ -472,6 +546,16 @@ stream_topk_kernel(const Params p) {
           if (xv > -INFINITY && xv >= tau) {
             const int pos = atomicAdd(&sm.count, 1);
             if (pos < kTkCap) sm.cand[pos] = comp_key(xv, bv * VW + t);
+          }
+        }
+        if (m2 > -INFINITY && m2 >= tau) {
+#pragma unroll
+          for (int t = 0; t < VW; ++t) {
+            const float xv = TR::get(bvec2, t);
+            if (xv > -INFINITY && xv >= tau) {
+              const int pos = atomicAdd(&sm.count, 1);
+              if (pos < kTkCap) sm.cand[pos] = comp_key(xv, bv2 * VW + t);
+            }
           }
         }
       }

@@ -21,6 +21,9 @@ struct TopkSmem {
   int widx[kMaxK];                   // and their token indices
   int sidx[kMaxK];                   // finisher: kept indices in token order
   int rel[256];                      // threads whose maximum reaches tau
+  int hist[256];                     // radix select of tau: one 8-bit digit's histogram
+  int pick_digit;
+  int pick_rank;
   int ired[kTkWarps];
   float fu[kMaxG1];                  // finisher: uniforms and acceptance probabilities
   float fa[kMaxG1];
