@@ -60,7 +60,9 @@ Layout make_layout(int B, int gamma, int V, int top_k) {
   L.row_ticket = o;  o += up(sizeof(int) * (size_t)R);
   L.seq = o;         o += up(sizeof(sv::SeqState) * (size_t)B);
   L.acc = o;         o += up(sizeof(double) * (size_t)B * gamma);
-  L.part = o;        o += up(sizeof(float4) * (size_t)R * L.S_part);
+  // rows path: S_part slice partials per row; streaming path: up to 4 parts x
+  // 8 warps per row
+  L.part = o;        o += up(sizeof(float4) * (size_t)R * std::max(L.S_part, 4 * sv::kWarps));
   L.lists = o;       o += up(sizeof(unsigned long long) * (size_t)R * L.S_list * L.klist);
   L.rowres = o;      o += up(L.klist > 0 ? sizeof(int2) * (size_t)R * (L.klist + 1) : 0);
   L.chunk = o;       o += up(3 * sizeof(float2) * (size_t)B * L.C_max);
@@ -271,24 +273,69 @@ sv_status launch_stream_topk(const sv::Params& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+// Parts per row for the dense streaming kernel.  Splitting each row into H
+// parts (each at least one ring chunk long; H * warps divides 32) gives the
+// CTAs more, smaller items: with fewer rows than CTA slots it evens the
+// per-SM work, and with many rows it lets every slot hold a CTA.  Measured on
+// 128K-vocabulary rows: H = 2 beats whole rows at 320 to 2560 rows, and
+// H = 4 loses to H = 2 at 320 rows; H = 4 is kept for batches small enough
+// that four parts per row still fit in one wave of CTAs.
+int stream_parts(long long R, long long slots, int V, int VW) {
+  const long long chunks = (V / VW) / ((long long)sv::kStU * sv::kSt);
+  if (R <= 0 || chunks < 2) return 1;
+  if (chunks >= 4 && R * 4 <= slots) return 4;
+  return 2;
+}
+
+// Sets p.H (parts per row), which the kernel that merges the partials reads too.
 template <typename T, int MODE>
-sv_status launch_stream_dense(const sv::Params& p, cudaStream_t stream) {
+sv_status launch_stream_dense(sv::Params& p, cudaStream_t stream) {
   auto kern = sv::stream_dense_kernel<T, MODE>;
   const size_t smem = (size_t)sv::kStS * sv::kStU * sv::kSt * sizeof(uint4) + sizeof(sv::StreamSmem);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_CUDA;
   }
-  const long long grid = stream_grid(kern, smem, (long long)p.B * (p.gamma + 1));
+  const long long R = (long long)p.B * (p.gamma + 1);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sv::kSt, smem) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const long long slots = (long long)per_sm * sm_count();
+  p.H = stream_parts(R, slots, p.V, sizeof(T) == 4 ? 4 : 8);
+  // whole rows: every CTA takes the same number of rows; parts: at most one
+  // CTA per slot, items dealt round-robin
+  const long long grid = p.H == 1 ? stream_grid(kern, smem, R) : std::min(R * p.H, slots);
   kern<<<(unsigned)grid, sv::kSt, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Greedy streaming path, second kernel: one CTA per sequence, launched as a
+// programmatic dependent of the streaming kernel.
+sv_status launch_greedy_finish(const sv::Params& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.B);
+  cfg.blockDim = dim3(sv::kSt);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, sv::stream_greedy_finish_kernel, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  return SV_OK;
 }
 
 // Kernels launched by the last call on this host thread (sv_last_kernels).
 thread_local const char* g_last_kernels = "";
 
 template <typename T>
-sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
+sv_status dispatch(sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
   sv::ClusterParams cp;
   size_t smem = 0;
   g_last_kernels = "";
@@ -310,7 +357,7 @@ sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype 
   const bool streamable = p.V % vec_width(dt) == 0 && path_override() != 3;
   if (mode == sv::MODE_GREEDY) {
     st = streamable ? launch_stream_dense<T, sv::MODE_GREEDY>(p, stream) : launch_rows<T, sv::MODE_GREEDY>(p, stream);
-    g_last_kernels = streamable ? "stream_dense_kernel" : "rows_kernel";
+    g_last_kernels = streamable ? "stream_dense_kernel,stream_greedy_finish_kernel" : "rows_kernel";
   } else if (mode == sv::MODE_TOPK) {
     st = streamable ? launch_stream_topk<T>(p, stream) : launch_rows<T, sv::MODE_TOPK>(p, stream);
     g_last_kernels = streamable ? "stream_topk_kernel" : "rows_kernel";
@@ -324,6 +371,7 @@ sv_status dispatch(const sv::Params& p, int mode, cudaStream_t stream, sv_dtype 
   }
   timing_record(1, stream);
   if (mode == sv::MODE_SOFTMAX) st = launch_residual<T>(p, stream);
+  else if (mode == sv::MODE_GREEDY && streamable) st = launch_greedy_finish(p, stream);
   timing_record(2, stream);
   return st;
 }

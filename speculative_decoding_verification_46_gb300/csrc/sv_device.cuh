@@ -66,6 +66,7 @@ struct Params {
   int S, U, SL;          // rows kernel: slices per row, vectors per thread, slice length
   int C, CL, EPT;        // residual kernel: chunks per row, chunk length, elements per thread
   int top_k;             // top-k list length (top-k mode)
+  int H;                 // streaming kernel: parts per row (1: whole rows)
   float top_p;
   float c;               // log2(e) / temperature (rounded to float)
   float c_lo;            // log2(e) / temperature - c
@@ -606,25 +607,30 @@ __device__ __forceinline__ int seq_gamma(const Params& p, int b) {
   return min(max(__ldg(p.gamma_b + b), 0), p.gamma);
 }
 
-// Last-arriving-CTA hand-off.  Every thread publishes its writes, one thread
-// takes a ticket; the CTA that takes ticket count-1 resets the counter and
-// returns true (its later reads of other CTAs' data use ld.global.cg).
-// With single_writer, only thread 0 wrote what the other CTAs will read, so
-// only thread 0 fences.
+// Last-arriving-CTA hand-off.  Every thread's writes are collected by the
+// barrier; thread 0 then takes a ticket with one acquire-release atomic (the
+// release publishes what the CTA wrote, the acquire makes the other CTAs'
+// writes visible to the last one; the closing barrier extends both to the
+// whole CTA).  The CTA that takes ticket count-1 resets the counter and
+// returns true; its later reads of other CTAs' data use ld.global.cg.
+// single_writer is kept for the call sites that document that only thread 0
+// wrote: the ordering is the same either way.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ bool arrive_last(int* ticket, int count, int* s_flag, bool single_writer = false) {
-  if (!single_writer) __threadfence();
+  (void)single_writer;
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (single_writer) __threadfence();
-    const int prev = atomicAdd(ticket, 1);
+    const int prev = atomic_add_acq_rel_gpu(ticket, 1);
     const int last = (prev == count - 1);
     if (last) *ticket = 0;
     *s_flag = last;
   }
   __syncthreads();
-  const bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
+  return *s_flag != 0;
 }
 
 // ------------------------------------------------------------------ rows kernel
@@ -1620,6 +1626,75 @@ __device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, c
   return r;
 }
 
+// ---- streaming-path row statistics
+// The streaming kernel leaves one partial per warp per row part: slot
+// (row * H + h) * kWarps + warp holds (max, first index) of that warp's
+// vectors (greedy) or (max M_w, sum of 2^((L - M_w) c) as two floats)
+// (sampling).  A row's NP = H * kWarps slots are contiguous, so sequence b's
+// G1 rows occupy slots [b * G1 * NP, (b + 1) * G1 * NP).  NP divides 32: one
+// aligned lane segment merges one row.
+__device__ __forceinline__ int stream_np(const Params& p) { return p.H * kWarps; }
+
+template <int MODE>
+__device__ __forceinline__ void merge_row_parts(const Params& p, int b, int G1, int gb, float* sM, double* sS,
+                                                int* sG, int* sBad) {
+  const int NP = stream_np(p);
+  const int E = G1 * NP;
+  const float4* base = p.part + (size_t)b * E;
+  for (int e0 = 0; e0 < E; e0 += kThreads) {        // uniform over the block: every lane shuffles
+    const int e = e0 + (int)threadIdx.x;
+    const bool ok = e < E;
+    const float4 v = ok ? __ldcg(base + e) : make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.f, 0.f);
+    const bool head = ok && (e % NP) == 0;
+    const int i = e / NP;
+    if (MODE == MODE_GREEDY) {
+      float bv = v.x;
+      int bi = __float_as_int(v.y);
+      for (int o = NP >> 1; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (head) {
+        const bool nan = bv != bv;
+        sG[i] = (nan || bi == 0x7fffffff) ? 0 : bi;
+        sBad[i] = nan && i <= gb;
+      }
+    } else {
+      float M = v.x;
+      for (int o = NP >> 1; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      F2 t{0.f, 0.f};
+      if (ok && v.x > -INFINITY && M < INFINITY) {
+        const float sc = ex2_approx((v.x - M) * p.c);
+        t = f2_add(F2{v.y * sc, 0.f}, F2{v.z * sc, 0.f});
+      }
+      for (int o = NP >> 1; o >= 1; o >>= 1) t = f2_add(t, f2_shfl_xor(t, o));
+      if (head) {
+        const double sum = (double)t.hi + (double)t.lo;
+        sM[i] = M;
+        sS[i] = sum;
+        sBad[i] = (!(M > -INFINITY && M < INFINITY) || !(sum > 0.0 && sum < 1e300)) && i <= gb;
+      }
+    }
+  }
+}
+
+// Warp 0: the first i < count with flags[i] != 0 (count if none), and
+// whether any flag2[i] is set for i <= last.
+__device__ __forceinline__ int first_flag_w0(const int* flags, int count, const int* flag2, int last, bool* any2) {
+  const int lane = threadIdx.x & 31;
+  int first = count;
+  bool a2 = false;
+  for (int k = 0; k <= last; k += 32) {
+    const int i = k + lane;
+    const unsigned hit = __ballot_sync(0xffffffffu, i < count && flags[i] != 0);
+    if (hit && first == count) first = k + __ffs(hit) - 1;
+    a2 |= __any_sync(0xffffffffu, i <= last && flag2[i] != 0);
+  }
+  *any2 = a2;
+  return first;
+}
+
 struct ResSmem {
   float tab[128];   // exp2_f2 table
   F2x3 red[kWarps];
@@ -1635,6 +1710,13 @@ struct ResSmem {
   F2 tbase;       // the owner's exclusive prefix
   F2 ds;
   LocateSmem loc;
+  // streaming path: the sequence's row statistics and acceptance scan
+  float rM[kMaxG1];
+  double rS[kMaxG1];
+  int rBad[kMaxG1];
+  int rRej[kMaxG1];
+  int rStatus;
+  int rN;
 };
 
 template <typename T>
@@ -1645,21 +1727,79 @@ residual_kernel(const Params p) {
   __shared__ ResSmem sm;
   extern __shared__ __align__(16) unsigned char res_dyn[];
   uint4* stage = reinterpret_cast<uint4*>(res_dyn);   // ResStage<T>::bytes
-  load_exp2_table(sm.tab);   // independent of the previous kernel: before the wait
-  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31;
   const int C = p.C;
   const int c = blockIdx.x % C;
   const int b = blockIdx.x / C;
   const int G = p.gamma, G1 = G + 1, V = p.V, EPT = p.EPT;
   const int NS = EPT / VW;                // vectors per thread run
-  SeqState st;
-  st.n = __ldcg(&p.seq[b].n);
-  st.status = __ldcg(&p.seq[b].status);
-  st.M = __ldcg(&p.seq[b].M);
-  st.s = __ldcg(&p.seq[b].s);
-  const int n = st.n;
   const int gb = seq_gamma(p, b);
+  const bool from_parts = p.H > 0;        // streaming path: per-warp row partials
+  // independent of the previous kernel, so before the wait: the exp2 table and,
+  // for the streaming path, thread i's draft d_i, its logit, q_i(d_i) and u_i
+  load_exp2_table(sm.tab);
+  int d_i = -1;
+  float l_d = 0.f, q_d = 0.f, u_i = 0.f;
+  if (from_parts && tid < gb) {
+    d_i = __ldg(p.draft + b * G + tid);
+    u_i = __ldg(p.uniforms + b * G1 + tid);
+    if (d_i >= 0 && d_i < V) {
+      l_d = TR::get(load_slot<T>(static_cast<const T*>(p.logits) + ((size_t)b * G1 + tid) * V, d_i, 1, false), 0);
+      q_d = p.q ? __ldg(p.q + ((size_t)b * G + tid) * V + d_i) : 1.f;   // NULL: one-hot draft
+    }
+  }
+  pdl_wait();
+  SeqState st;
+  if (from_parts) {
+    // merge the row partials, accept/reject, scan (every CTA of the sequence
+    // computes the same values; chunk 0 writes the per-draft outputs)
+    merge_row_parts<MODE_SOFTMAX>(p, b, G1, gb, sm.rM, sm.rS, nullptr, sm.rBad);
+    if (tid == 0) sm.rStatus = 0;
+    __syncthreads();
+    float a = 0.f;
+    if (tid < gb) {
+      int bits = 0;
+      const float ssum = (float)sm.rS[tid];
+      if (d_i < 0 || d_i >= V) {
+        bits |= SEQ_OOB;
+      } else {
+        const float pd = sm.rBad[tid] ? 0.f : exp2f((l_d - sm.rM[tid]) * p.c) / ssum;
+        if (q_d > 0.f) {
+          a = fminf(1.f, pd / q_d);
+        } else {
+          a = pd > 0.f ? 1.f : 0.f;
+          bits |= SEQ_QBAD;
+        }
+      }
+      sm.rRej[tid] = !(u_i < a);
+      if (bits) atomicOr(&sm.rStatus, bits);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      bool anybad = false;
+      const int n0 = first_flag_w0(sm.rRej, gb, sm.rBad, gb, &anybad);
+      if (tid == 0) {
+        sm.rN = n0;
+        if (anybad) sm.rStatus |= SEQ_BADROW;
+      }
+    }
+    __syncthreads();
+    st.n = sm.rN;
+    st.status = sm.rStatus;
+    st.M = sm.rM[st.n];
+    st.s = sm.rS[st.n];
+    if (c == 0) {
+      if (tid == 0) p.out_n[b] = st.n;
+      if (p.out_a && tid < G) p.out_a[b * G + tid] = tid < gb ? a : 0.f;
+      if (tid < G1 && tid != st.n) p.out_tokens[b * G1 + tid] = tid < st.n ? d_i : -1;
+    }
+  } else {
+    st.n = __ldcg(&p.seq[b].n);
+    st.status = __ldcg(&p.seq[b].status);
+    st.M = __ldcg(&p.seq[b].M);
+    st.s = __ldcg(&p.seq[b].s);
+  }
+  const int n = st.n;
   const bool resid = n < gb;
   const bool bad = (st.status & SEQ_BADROW) != 0;
   const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
@@ -1804,6 +1944,11 @@ residual_kernel(const Params p) {
     token = sm.token < 0 ? 0 : sm.token;
   }
   for (int k2 = tid; k2 < 3 * C; k2 += kThreads) cS[k2] = F2{0.f, 0.f};
+  if (from_parts) {
+    // every CTA of the sequence has read the row partials: zero them
+    const int E = G1 * stream_np(p);
+    for (int e = tid; e < E; e += kThreads) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (tid == 0) {
     p.out_tokens[b * G1 + n] = token;
     if (p.out_status) p.out_status[b] = status;

@@ -1,6 +1,6 @@
 // Streaming path of libspecverify for large batches: persistent CTAs, one
-// whole row at a time, each thread prefetching its own future 16-byte vectors
-// with cp.async into a thread-private shared-memory ring S stages deep.
+// row (or row part) at a time, each thread prefetching its own future 16-byte
+// vectors with cp.async into a thread-private shared-memory ring S stages deep.
 //
 // Why this shape.  Every mode is bound by HBM bandwidth, which needs ~50 KB
 // of reads in flight per SM at all times.  A CTA that loads, then reduces,
@@ -11,20 +11,25 @@
 // copies and later reads its own slots), so completion is tracked per thread
 // with cp.async.wait_group: there are no cross-thread waits, no mbarriers and
 // no spin loops.  Rows are dealt to CTAs round-robin; counts are balanced on
-// the host so that every CTA gets the same number of rows.
+// the host so that every CTA gets the same number of rows.  With fewer rows
+// than CTA slots, each row is split into H parts (H = 2 or 4) so that no SM
+// streams a whole row more than the others.
 //
-//   greedy   per-row argmax (ties -> lowest index; NaN flagged)
-//   softmax  per-row online max / sum of 2^((L - m) c) with rescaling when the
-//            running max grows; p(d_i) and a_i at the row's end
+//   greedy   per-warp argmax of each row part (ties -> lowest index; NaN
+//            flagged); stream_greedy_finish_kernel merges the parts, scans
+//            the drafts and emits the tokens
+//   softmax  per-warp online max / sum of 2^((L - m) c) with rescaling when
+//            the running max grows; residual_kernel merges the parts,
+//            computes p(d_i) and a_i, scans and makes the final draw
 //   top-k    pass 1 keeps per-thread maxima (and the two best vectors); the
 //            k-th largest is a lower bound tau of the row's k-th value; only
 //            threads with a third vector reaching tau are re-read (L2);
 //            exact rank selection of the candidates >= tau; softmax(./T) +
-//            top-p; a_i
+//            top-p; a_i.  The last row of a sequence to finish (atomic
+//            ticket, no waiting) runs the acceptance scan and the final draw.
 //
-// The last row of a sequence to finish (atomic ticket, no waiting) runs the
-// acceptance scan.  Greedy and top-k also do the final draw there; softmax
-// hands (n, m_n, s_n) to residual_kernel.
+// The dense kernel ends a row part with warp shuffles and one store per warp:
+// no block barrier, so no warp waits for another between rows.
 #pragma once
 
 #include "sv_device.cuh"
@@ -47,21 +52,10 @@ __device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_gro
 template <int N>
 __device__ __forceinline__ void cpa_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// The dense streaming kernel keeps no block-wide state: each warp ends a row
+// part on its own (shuffles and one store).
 struct StreamSmem {
-  float fred[kSt / 32];
-  F2 f2red[kSt / 32];
-  float2 pair[kSt / 32];
-  int flag;
-  int n;
-  int status;
-  int token;
-  int g[kMaxG1];
-  int bad[kMaxG1];
-  float M[kMaxG1];
-  double s[kMaxG1];
-  float a[kMaxG1];
-  int dr[kMaxG1];
-  float ur[kMaxG1];
+  int unused;
 };
 
 // Per-thread sequence of ring items: (j-th row of this CTA, pass, chunk c),
@@ -70,31 +64,43 @@ struct StreamSmem {
 // thread's U vectors of one chunk (U * kSt vectors) of a row.
 struct RowWalk {
   int R, G1, NV, CH, NCH, nrows;
+  int H = 1, NVP = 0;   // parts per row and vectors per part (NVP = NV when H = 1)
   __device__ __forceinline__ int row_of(int j) const { return blockIdx.x + j * gridDim.x; }
+  // item j of this CTA: row r, vectors [vb, ve)
+  __device__ __forceinline__ void item(int j, int* r, int* vb, int* ve) const {
+    const int g = row_of(j);
+    const int h = g % H;
+    *r = g / H;
+    *vb = h * NVP;
+    *ve = min(*vb + NVP, NV);
+  }
 };
 
 template <typename T, int S, int PASSES, int U = kStU>
 struct Issuer {
-  int j = 0, pass = 0, c = 0, stage = 0;
+  int j = 0, pass = 0, c = 0, stage = 0, vb = 0, ve = 0;
   const T* row = nullptr;
-  __device__ __forceinline__ void start(const T* logits, size_t V, const RowWalk& w) {
-    row = logits + (size_t)w.row_of(0) * V;
+  __device__ __forceinline__ void at(const T* logits, size_t V, const RowWalk& w) {
+    int r;
+    w.item(j, &r, &vb, &ve);
+    row = logits + (size_t)r * V;
   }
+  __device__ __forceinline__ void start(const T* logits, size_t V, const RowWalk& w) { at(logits, V, w); }
   // issue the next item into its stage (an empty group past the end)
   __device__ __forceinline__ void issue(uint4* ring, const T* logits, size_t V, const RowWalk& w) {
     if (j < w.nrows) {
       uint4* slot = ring + (size_t)stage * U * kSt + threadIdx.x;
-      const int v0 = c * w.CH + (int)threadIdx.x;
+      const int v0 = vb + c * w.CH + (int)threadIdx.x;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + u * kSt;
-        if (v < w.NV) cpa16(slot + u * kSt, row + (size_t)v * Tr<T>::VW);
+        if (v < ve) cpa16(slot + u * kSt, row + (size_t)v * Tr<T>::VW);
       }
       if (++c == w.NCH) {
         c = 0;
         if (++pass == PASSES) {
           pass = 0;
-          if (++j < w.nrows) row = logits + (size_t)w.row_of(j) * V;
+          if (++j < w.nrows) at(logits, V, w);
         }
       }
     }
@@ -103,66 +109,46 @@ struct Issuer {
   }
 };
 
-// ---- dense finisher: per-row statistics already merged (one entry per row)
-template <int MODE>
-__device__ void stream_finish_dense(const Params& p, int b, StreamSmem& sm) {
+// ---- greedy finish: one CTA per sequence after the streaming kernel
+// Merges each row's per-warp (max, first index) partials into the target's
+// argmax g_i, accepts drafts while d_i == g_i (stopping at the first
+// mismatch n), emits d_0..d_{n-1}, g_n and -1 padding, and zeroes the
+// partial slots it read.
+__global__ void __launch_bounds__(kSt) stream_greedy_finish_kernel(const Params p) {
+  __shared__ int sg[kMaxG1], sbad[kMaxG1], smis[kMaxG1];
+  __shared__ int s_status, s_n;
   const int tid = threadIdx.x;
-  const int G = p.gamma, G1 = G + 1;
+  const int b = blockIdx.x;
+  const int G = p.gamma, G1 = G + 1, V = p.V;
   const int gb = seq_gamma(p, b);
-  if (tid < G1) {
-    const float4 v = __ldcg(p.part + (size_t)b * G1 + tid);
-    if (MODE == MODE_GREEDY) {
-      const bool nan = v.x != v.x;
-      const int bi = __float_as_int(v.y);
-      sm.g[tid] = (nan || bi == 0x7fffffff) ? 0 : bi;
-      sm.bad[tid] = nan && tid <= gb;
-    } else {
-      const double s = (double)v.y + (double)v.z;
-      sm.M[tid] = v.x;
-      sm.s[tid] = s;
-      sm.bad[tid] = (!(v.x > -INFINITY && v.x < INFINITY) || !(s > 0.0 && s < 1e300)) && tid <= gb;
-      if (tid < G) sm.a[tid] = (float)__ldcg(p.acc + b * G + tid);
-    }
-    sm.ur[tid] = MODE == MODE_SOFTMAX ? __ldg(p.uniforms + b * G1 + tid) : 0.f;
-    if (tid < G) sm.dr[tid] = __ldg(p.draft + b * G + tid);
-  }
-  if (tid == 0) sm.status = __ldcg(&p.seq[b].status);
+  const int d = tid < gb ? __ldg(p.draft + b * G + tid) : -1;   // an input: before the wait
+  pdl_wait();
+  merge_row_parts<MODE_GREEDY>(p, b, G1, gb, nullptr, nullptr, sg, sbad);
+  if (tid == 0) s_status = 0;
   __syncthreads();
-  for (int e = tid; e < G1; e += kSt) p.part[(size_t)b * G1 + e] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int e = tid; e < G; e += kSt) p.acc[b * G + e] = 0.0;
+  if (tid < gb) {
+    const bool oob = d < 0 || d >= V;
+    if (oob) atomicOr(&s_status, SEQ_OOB);
+    smis[tid] = oob || d != sg[tid];
+  }
+  __syncthreads();
+  if (tid < 32) {
+    bool anybad = false;
+    const int n0 = first_flag_w0(smis, gb, sbad, gb, &anybad);
+    if (tid == 0) {
+      s_n = n0;
+      if (anybad) s_status |= SEQ_BADROW;
+    }
+  }
+  __syncthreads();
+  const int n = s_n;
+  if (tid < G1) p.out_tokens[b * G1 + tid] = tid < n ? d : (tid == n ? sg[n] : -1);
   if (tid == 0) {
-    int status = sm.status, n = gb;
-    for (int i = 0; i <= gb; ++i)
-      if (sm.bad[i]) status |= SEQ_BADROW;
-    if (MODE == MODE_GREEDY) {
-      for (int i = 0; i < gb; ++i)
-        if (sm.dr[i] != sm.g[i]) { n = i; break; }
-      sm.token = sm.g[n];
-      p.seq[b].status = 0;
-      if (p.out_status) p.out_status[b] = status;
-    } else {
-      for (int i = 0; i < gb; ++i)
-        if (!(sm.ur[i] < sm.a[i])) { n = i; break; }
-      SeqState st;
-      st.n = n;
-      st.status = status;
-      st.M = sm.M[n];
-      st.pad = 0;
-      st.s = sm.s[n];
-      p.seq[b] = st;
-    }
-    sm.n = n;
     p.out_n[b] = n;
+    if (p.out_status) p.out_status[b] = s_status;
   }
-  __syncthreads();
-  const int n = sm.n;
-  if (MODE == MODE_SOFTMAX && p.out_a)
-    for (int j = gb + tid; j < G; j += kSt) p.out_a[b * G + j] = 0.f;   // beyond this sequence's drafts
-  for (int j = tid; j < G1; j += kSt) {
-    if (j < n) p.out_tokens[b * G1 + j] = sm.dr[j];
-    else if (j > n) p.out_tokens[b * G1 + j] = -1;
-    else if (MODE == MODE_GREEDY) p.out_tokens[b * G1 + j] = sm.token;
-  }
+  const int E = G1 * stream_np(p);
+  for (int e = tid; e < E; e += kSt) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Greedy helpers over one ring stage (this thread's kStU vectors, element
@@ -228,16 +214,19 @@ stream_dense_kernel(const Params p) {
   constexpr int S = kStS;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
-  StreamSmem& sm = *reinterpret_cast<StreamSmem*>(smem_raw + (size_t)S * kStU * kSt * sizeof(uint4));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = p.gamma, G1 = G + 1, V = p.V;
+  const int G1 = p.gamma + 1, V = p.V;
+  // the kernel that merges the partials may start its input-only prologue now
+  pdl_launch_dependents();
   RowWalk w;
   w.R = p.B * G1;
   w.G1 = G1;
   w.NV = V / VW;
+  w.H = p.H;                              // parts per row (items = R * H)
+  w.NVP = (w.NV + w.H - 1) / w.H;
   w.CH = kStU * kSt;
-  w.NCH = (w.NV + w.CH - 1) / w.CH;
-  w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  w.NCH = (w.NVP + w.CH - 1) / w.CH;
+  w.nrows = (w.R * w.H - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const T* logits = static_cast<const T*>(p.logits);
 
   Issuer<T, S, 1> iss;
@@ -246,20 +235,8 @@ stream_dense_kernel(const Params p) {
   for (int s2 = 0; s2 < S; ++s2) iss.issue(ring, logits, V, w);
   int stage = 0;
   for (int j = 0; j < w.nrows; ++j) {
-    const int r = w.row_of(j);
-    const int b = r / G1, i = r - b * G1;
-    const int gb = seq_gamma(p, b);
-    const T* row = logits + (size_t)r * V;
-    // the draft's logit and q(d) for this row, fetched early (softmax only)
-    float l_d = 0.f, q_d = 0.f;
-    int d = -1;
-    if (MODE == MODE_SOFTMAX && tid == 0 && i < gb) {
-      d = __ldg(p.draft + b * G + i);
-      if (d >= 0 && d < V) {
-        l_d = Tr<T>::get(load_slot<T>(row, d, 1, false), 0);
-        q_d = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d) : 1.f;   // NULL: one-hot draft
-      }
-    }
+    int r, vb, ve;
+    w.item(j, &r, &vb, &ve);
     float best = -INFINITY;          // greedy: this thread's max, its first index, NaN seen
     int best_i = 0x7fffffff, nan_seen = 0;
     float m = -INFINITY, s0 = 0.f, s1 = 0.f;   // softmax: running max and sums
@@ -268,17 +245,17 @@ stream_dense_kernel(const Params p) {
       const uint4* slot = ring + (size_t)stage * kStU * kSt;
       if (MODE == MODE_GREEDY) {
         // one max over the stage's kStU vectors; only a new best looks further
-        const float cm = stage_max<T>(slot, c * w.CH, w.NV);
+        const float cm = stage_max<T>(slot, vb + c * w.CH, ve);
         nan_seen |= (cm != cm);
         if (cm > best) {
           best = cm;
-          best_i = stage_first_index<T>(slot, c * w.CH, w.NV, cm);
+          best_i = stage_first_index<T>(slot, vb + c * w.CH, ve, cm);
         }
       } else {
 #pragma unroll
         for (int u = 0; u < kStU; ++u) {
-          const int v = c * w.CH + u * kSt + tid;
-          if (v < w.NV) {
+          const int v = vb + c * w.CH + u * kSt + tid;
+          if (v < ve) {
             const uint4 x = slot[u * kSt + tid];
             const float vm = TR::template vmax<false>(x);
             if (vm > m) {
@@ -301,73 +278,33 @@ stream_dense_kernel(const Params p) {
       iss.issue(ring, logits, V, w);
       stage = (stage + 1 == S) ? 0 : stage + 1;
     }
-    // ---- the row's statistic
+    // ---- this warp's partial of the row part: shuffles and one store, no
+    // block-wide step (the merge is the next kernel's)
+    float4* slot = p.part + ((size_t)r * w.H + vb / w.NVP) * (kSt / 32) + warp;
     if (MODE == MODE_GREEDY) {
       int bi = best_i;
       float bv = best;
-      if (__syncthreads_or(nan_seen)) bv = __int_as_float(0x7fffffff);
+      if (__any_sync(0xffffffffu, nan_seen)) bv = __int_as_float(0x7fffffff);   // a NaN flags the row
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
       }
-      if (lane == 0) sm.pair[warp] = make_float2(bv, __int_as_float(bi));
-      __syncthreads();
-      if (tid == 0) {
-        float v0 = sm.pair[0].x;
-        int i0 = __float_as_int(sm.pair[0].y);
-        for (int k2 = 1; k2 < kSt / 32; ++k2) {
-          const float ov = sm.pair[k2].x;
-          const int oi = __float_as_int(sm.pair[k2].y);
-          if (argmax_better(ov, oi, v0, i0)) { v0 = ov; i0 = oi; }
-        }
-        p.part[r] = make_float4(v0, __int_as_float(i0), 0.f, 0.f);
-        if (i < gb) {
-          const int dd = __ldg(p.draft + b * G + i);
-          if (dd < 0 || dd >= V) atomicOr(&p.seq[b].status, SEQ_OOB);
-        }
-      }
+      if (lane == 0) *slot = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
     } else {
       float M = m;
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      if (lane == 0) sm.fred[warp] = M;
-      __syncthreads();
-      M = sm.fred[0];
-#pragma unroll
-      for (int k2 = 1; k2 < kSt / 32; ++k2) M = fmaxf(M, sm.fred[k2]);
       F2 acc{0.f, 0.f};
       if (m > -INFINITY && M < INFINITY) {
         const float sc = ex2_approx((m - M) * p.c);
         acc = f2_add(F2{s0 * sc, 0.f}, F2{s1 * sc, 0.f});
       }
-      const F2 tot = block_sum_f2(acc, sm.f2red);
-      if (tid == 0) {
-        p.part[r] = make_float4(M, tot.hi, tot.lo, 0.f);
-        if (i < gb) {
-          float a = 0.f;
-          int st = 0;
-          const float ssum = tot.hi + tot.lo;
-          const bool bad = !(M > -INFINITY && M < INFINITY) || !(ssum > 0.f && ssum < INFINITY);
-          if (d < 0 || d >= V) {
-            st |= SEQ_OOB;
-          } else {
-            const float pd = bad ? 0.f : exp2f((l_d - M) * p.c) / ssum;
-            if (q_d > 0.f) {
-              a = fminf(1.f, pd / q_d);
-            } else {
-              a = pd > 0.f ? 1.f : 0.f;
-              st |= SEQ_QBAD;
-            }
-          }
-          if (st) atomicOr(&p.seq[b].status, st);
-          p.acc[b * G + i] = (double)a;
-          if (p.out_a) p.out_a[b * G + i] = a;
-        }
-      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc = f2_add(acc, f2_shfl_xor(acc, o));
+      if (lane == 0) *slot = make_float4(M, acc.hi, acc.lo, 0.f);
     }
-    if (arrive_last(p.seq_ticket + b, G1, &sm.flag, true)) stream_finish_dense<MODE>(p, b, sm);
   }
   cpa_wait<0>();
 }
@@ -464,6 +401,7 @@ stream_topk_kernel(const Params p) {
   w.R = p.B * G1;
   w.G1 = G1;
   w.NV = V / VW;
+  w.NVP = w.NV;
   w.CH = U * kSt;
   w.NCH = (w.NV + w.CH - 1) / w.CH;
   w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
