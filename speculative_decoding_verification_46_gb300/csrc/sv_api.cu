@@ -39,7 +39,7 @@ int list_len(int V, int top_k) {
 }
 
 struct Layout {
-  size_t seq_ticket, seq_ticket2, row_ticket, seq, acc, part, lists, rowres, chunk, total;
+  size_t seq_ticket, seq_ticket2, row_ticket, ctr, seq, acc, part, lists, rowres, chunk, total;
   int S_part, S_list, C_max, klist;
 };
 
@@ -58,6 +58,7 @@ Layout make_layout(int B, int gamma, int V, int top_k) {
   L.seq_ticket = o;  o += up(sizeof(int) * (size_t)B);
   L.seq_ticket2 = o; o += up(sizeof(int) * (size_t)B);
   L.row_ticket = o;  o += up(sizeof(int) * (size_t)R);
+  L.ctr = o;         o += up(sizeof(int) * 4);
   L.seq = o;         o += up(sizeof(sv::SeqState) * (size_t)B);
   L.acc = o;         o += up(sizeof(double) * (size_t)B * gamma);
   // rows path: S_part slice partials per row; streaming path: up to 4 parts x
@@ -96,6 +97,7 @@ void bind_workspace(sv::Params& p, const Layout& L, void* ws) {
   p.seq_ticket = reinterpret_cast<int*>(w + L.seq_ticket);
   p.seq_ticket2 = reinterpret_cast<int*>(w + L.seq_ticket2);
   p.row_ticket = reinterpret_cast<int*>(w + L.row_ticket);
+  p.ctr = reinterpret_cast<int*>(w + L.ctr);
   p.seq = reinterpret_cast<sv::SeqState*>(w + L.seq);
   p.acc = reinterpret_cast<double*>(w + L.acc);
   p.part = reinterpret_cast<float4*>(w + L.part);
@@ -268,7 +270,21 @@ sv_status launch_stream_topk(const sv::Params& p, cudaStream_t stream) {
     cudaGetLastError();
     return SV_ERR_CUDA;
   }
-  const long long grid = stream_grid(kern, smem, (long long)p.B * (p.gamma + 1));
+  const long long R = (long long)p.B * (p.gamma + 1);
+  // rows of more than kStSTopk ring chunks are claimed at run time (the
+  // kernel makes the same test): then one CTA per slot; else equal static shares
+  const long long nch = ceil_div((long long)(p.V / (sizeof(T) == 4 ? 4 : 8)), (long long)sv::kStUTopk * sv::kSt);
+  long long grid;
+  if (nch > sv::kStSTopk) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sv::kSt, smem) != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    grid = std::min(R, (long long)per_sm * sm_count());
+  } else {
+    grid = stream_grid(kern, smem, R);
+  }
   kern<<<(unsigned)grid, sv::kSt, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -81,6 +81,7 @@ struct Params {
   int* seq_ticket;
   int* seq_ticket2;
   int* row_ticket;
+  int* ctr;                       // [4] streaming top-k: next unclaimed row, CTAs done
   SeqState* seq;
   double* acc;                    // [B][gamma] acceptance probabilities (top-k mode)
   float4* part;                   // [R][S] per-slice partials

@@ -65,7 +65,11 @@ struct StreamSmem {
 struct RowWalk {
   int R, G1, NV, CH, NCH, nrows;
   int H = 1, NVP = 0;   // parts per row and vectors per part (NVP = NV when H = 1)
-  __device__ __forceinline__ int row_of(int j) const { return blockIdx.x + j * gridDim.x; }
+  // rows claimed at run time (H = 1): the CTA's j-th row is dyn[j & 3], and
+  // the walk ends at the first claim >= R; otherwise rows are dealt statically
+  const int* dyn = nullptr;
+  __device__ __forceinline__ int row_of(int j) const { return dyn ? dyn[j & 3] : blockIdx.x + j * gridDim.x; }
+  __device__ __forceinline__ bool live(int j) const { return dyn ? dyn[j & 3] < R : j < nrows; }
   // item j of this CTA: row r, vectors [vb, ve)
   __device__ __forceinline__ void item(int j, int* r, int* vb, int* ve) const {
     const int g = row_of(j);
@@ -83,12 +87,12 @@ struct Issuer {
   __device__ __forceinline__ void at(const T* logits, size_t V, const RowWalk& w) {
     int r;
     w.item(j, &r, &vb, &ve);
-    row = logits + (size_t)r * V;
+    row = logits + (size_t)min(r, w.R - 1) * V;
   }
   __device__ __forceinline__ void start(const T* logits, size_t V, const RowWalk& w) { at(logits, V, w); }
   // issue the next item into its stage (an empty group past the end)
   __device__ __forceinline__ void issue(uint4* ring, const T* logits, size_t V, const RowWalk& w) {
-    if (j < w.nrows) {
+    if (w.live(j)) {
       uint4* slot = ring + (size_t)stage * U * kSt + threadIdx.x;
       const int v0 = vb + c * w.CH + (int)threadIdx.x;
 #pragma unroll
@@ -100,7 +104,8 @@ struct Issuer {
         c = 0;
         if (++pass == PASSES) {
           pass = 0;
-          if (++j < w.nrows) at(logits, V, w);
+          ++j;
+          if (w.live(j)) at(logits, V, w);
         }
       }
     }
@@ -407,21 +412,36 @@ stream_topk_kernel(const Params p) {
   w.nrows = (w.R - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const int MV = (w.NV + kSt - 1) / kSt;   // vectors of the thread with the most
   const T* logits = static_cast<const T*>(p.logits);
+  // Rows are claimed as CTAs get through them (static dealing leaves the
+  // CTAs that drew one row more, or share an SM with more CTAs, last): the
+  // first row is blockIdx.x, the rest come from a counter.  Thread 0 claims
+  // row j + 1 as row j starts and publishes it at a barrier before the issuer
+  // looks up row j + 1 (with row j's last chunk, issued S chunks ahead of the
+  // consumer, so at consumer chunk NCH - S - 1).  Needs rows of more than S
+  // chunks, so that the ring never reaches past the next row.
+  const bool dynamic = w.NCH > S;
+  if (dynamic) {
+    w.dyn = sm.rows;
+    if (tid == 0) sm.rows[0] = blockIdx.x;
+    __syncthreads();
+  }
 
   Issuer<T, S, 1, U> iss;
   iss.start(logits, V, w);
 #pragma unroll
   for (int s = 0; s < S; ++s) iss.issue(ring, logits, V, w);
   int stage = 0;
-  for (int j = 0; j < w.nrows; ++j) {
+  for (int j = 0; w.live(j); ++j) {
     const int r = w.row_of(j);
     const int b = r / G1, i = r - b * G1;
     const int gb = seq_gamma(p, b);
     const T* row = logits + (size_t)r * V;
     __syncthreads();   // the previous row's shared state is no longer in use
+    int claim = 0;
     if (tid == 0) {
       sm.count = 0;
       sm.nrel = 0;
+      if (dynamic) claim = (int)gridDim.x + atomicAdd(p.ctr, 1);   // row j + 1
     }
     int d_row = -1;
     float q_row = 0.f;
@@ -437,6 +457,11 @@ stream_topk_kernel(const Params p) {
     int bv = -1, bv2 = -1;
     int nan_seen = 0;
     for (int c = 0; c < w.NCH; ++c) {
+      if (dynamic && c == w.NCH - S - 1) {
+        // row j + 1's slot was row j - 3's: no longer read
+        if (tid == 0) sm.rows[(j + 1) & 3] = claim;
+        __syncthreads();
+      }
       cpa_wait<S - 1>();
       const uint4* slot = ring + (size_t)stage * U * kSt;
 #pragma unroll
@@ -588,6 +613,11 @@ stream_topk_kernel(const Params p) {
     if (arrive_last(p.seq_ticket + b, G1, &sm.flag)) topk_finish_sequence(p, b, sm);
   }
   cpa_wait<0>();
+  // every claim of this CTA has returned; the last CTA out resets the counter
+  if (dynamic && tid == 0 && atomicAdd(p.ctr + 1, 1) == (int)gridDim.x - 1) {
+    p.ctr[0] = 0;
+    p.ctr[1] = 0;
+  }
 }
 
 }  // namespace sv

@@ -29,6 +29,7 @@ struct TopkSmem {
   float fa[kMaxG1];
   LocateSmem loc;
   int flag;
+  int rows[4];                       // streaming: this CTA's rows j .. j + 3 (ring by j & 3)
   int count;
   int nrel;
   int n;
