@@ -443,12 +443,11 @@ stream_topk_kernel(const Params p) {
       sm.nrel = 0;
       if (dynamic) claim = (int)gridDim.x + atomicAdd(p.ctr, 1);   // row j + 1
     }
+    // the row's draft now, q(d) after pass 1 (its address needs the draft:
+    // loading both here would hold warp 0 for two round trips)
     int d_row = -1;
     float q_row = 0.f;
-    if (tid == 0 && i < gb) {
-      d_row = __ldg(p.draft + b * G + i);
-      if (d_row >= 0 && d_row < V) q_row = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d_row) : 1.f;
-    }
+    if (tid == 0 && i < gb) d_row = __ldg(p.draft + b * G + i);
     // ---- pass 1 through the ring: per thread its two best 16-byte vectors
     // (by maximum; the first such vector on ties) kept in registers with
     // their maxima m1 >= m2, and m3 = the largest maximum of its other vectors
@@ -491,6 +490,7 @@ stream_topk_kernel(const Params p) {
       iss.issue(ring, logits, V, w);
       stage = (stage + 1 == S) ? 0 : stage + 1;
     }
+    if (d_row >= 0 && d_row < V) q_row = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d_row) : 1.f;
     // ---- tau: the k-th largest finite thread maximum (its key bits from
     // bit 31 down to KEY_LOW_BIT, found by a radix select)
     const uint32_t tkey = m1 > -INFINITY ? okey(m1) : 0u;
