@@ -124,27 +124,77 @@ __device__ __forceinline__ float4 group_merge(float4 v, int CN, float c) {
 // deterministic draft, whose one-hot q is infinite at run offset xq - so that
 // token is outside the residual support - and 0 elsewhere): the tail tokens
 // in one sweep, the tokens near the maximum (bits of `top`) after.
-template <typename T>
-__device__ __forceinline__ void cluster_run(const T* L, const float* Q, int xq, int len, bool use_q, float M,
-                                            float c, float c_lo, float s_a, RunAcc* acc, const float* tab) {
+// The tail sweep of a run for 16-bit logits (x - M exact): every token takes
+// the same branch-free steps (the tail weight and its residual with one
+// rounding); a token near the maximum (p > -8) adds nothing and is flagged.
+// -inf is clamped to an exponent that ex2.approx flushes to 0.
+template <typename T, bool USE_Q>
+__device__ __forceinline__ uint64_t cluster_sweep16(const T* L, const float* Q, int xq, int len, float M, float c,
+                                                    float c_lo, float s_a, RunAcc* acc) {
   constexpr int VW = Tr<T>::VW;
-  constexpr bool EXACT = sizeof(T) == 2;
   uint64_t top = 0ull;
   for (int j = 0; j * VW < len; ++j) {
     const uint4 v = *reinterpret_cast<const uint4*>(L + j * VW);
     float qv[VW];
 #pragma unroll
     for (int h = 0; h < VW / 4; ++h) {
-      const float4 q4 = Q ? *reinterpret_cast<const float4*>(Q + j * VW + 4 * h) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 q4 = (USE_Q && Q) ? *reinterpret_cast<const float4*>(Q + j * VW + 4 * h)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
       qv[4 * h + 0] = q4.x;
       qv[4 * h + 1] = q4.y;
       qv[4 * h + 2] = q4.z;
       qv[4 * h + 3] = q4.w;
     }
+    uint32_t tv = 0u;
 #pragma unroll
     for (int t = 0; t < VW; ++t) {
-      const float qt = (j * VW + t == xq) ? INFINITY : qv[t];
-      if (run_tail<EXACT>(*acc, Tr<T>::get(v, t), qt, use_q, M, c, c_lo, s_a)) top |= 1ull << (j * VW + t);
+      const float dh = fmaxf(Tr<T>::get(v, t) - M, -1.0e4f);
+      const float p = dh * c;
+      const float e = fmaf(dh, c_lo, fmaf(dh, c, -p));
+      const float y = ex2_approx(p);
+      const bool near = p > -8.f;
+      const float w = near ? 0.f : fmaf(y * 6.931471825e-01f, e, y);
+      if (near) tv |= 1u << t;
+      RunAcc::acc2(acc->sh, acc->sl, w, 0.f);
+      if (USE_Q) {
+        const float qt = (j * VW + t == xq) ? INFINITY : qv[t];
+        if (w > s_a * qt) {
+          RunAcc::acc2(acc->ah, acc->al, fmaf(-s_a, qt, w), 0.f);
+          acc->q += qt;
+        }
+      }
+    }
+    top |= (uint64_t)tv << (j * VW);
+  }
+  return top;
+}
+
+template <typename T>
+__device__ __forceinline__ void cluster_run(const T* L, const float* Q, int xq, int len, bool use_q, float M,
+                                            float c, float c_lo, float s_a, RunAcc* acc, const float* tab) {
+  constexpr int VW = Tr<T>::VW;
+  constexpr bool EXACT = sizeof(T) == 2;
+  uint64_t top = 0ull;
+  if constexpr (EXACT) {
+    top = use_q ? cluster_sweep16<T, true>(L, Q, xq, len, M, c, c_lo, s_a, acc)
+                : cluster_sweep16<T, false>(L, Q, xq, len, M, c, c_lo, s_a, acc);
+  } else {
+    for (int j = 0; j * VW < len; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(L + j * VW);
+      float qv[VW];
+#pragma unroll
+      for (int h = 0; h < VW / 4; ++h) {
+        const float4 q4 = Q ? *reinterpret_cast<const float4*>(Q + j * VW + 4 * h) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[4 * h + 0] = q4.x;
+        qv[4 * h + 1] = q4.y;
+        qv[4 * h + 2] = q4.z;
+        qv[4 * h + 3] = q4.w;
+      }
+#pragma unroll
+      for (int t = 0; t < VW; ++t) {
+        const float qt = (j * VW + t == xq) ? INFINITY : qv[t];
+        if (run_tail<EXACT>(*acc, Tr<T>::get(v, t), qt, use_q, M, c, c_lo, s_a)) top |= 1ull << (j * VW + t);
+      }
     }
   }
   while (top) {

@@ -1434,19 +1434,23 @@ __device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, 
     const int ev = e0 + j * VW;
     const int lim = V - ev;          // tokens of this vector inside the row
     const int xo = xq - ev;          // the one-hot token's offset (DET)
-    // no token of the vector near the maximum (the vector maximum's exponent,
-    // formed the same way, bounds every token's): the short path, for 16-bit
-    // logits whose x - M is exact; -inf is clamped to a weight that ex2.approx
-    // flushes to 0 (as any exponent below -126)
-    const bool vtop = (Tr<T>::template vmax<false>(v) - M) * c > -8.f;
-    if (EXACT && !vtop && lim >= VW) {
+    if (EXACT) {
+      // 16-bit logits (x - M exact): every token takes the same branch-free
+      // steps; a token near the maximum (p > -8) adds nothing here and is
+      // flagged for run_top.  -inf is clamped to an exponent that ex2.approx
+      // flushes to 0 (as any exponent below -126); tokens past the row's end
+      // weigh 0 (their q is 0 too).
+      uint32_t tv = 0u;
 #pragma unroll
       for (int t = 0; t < VW; ++t) {
         const float dh = fmaxf(Tr<T>::get(v, t) - M, -1.0e4f);
         const float p = dh * c;
         const float e = fmaf(dh, c_lo, fmaf(dh, c, -p));
         const float y = ex2_approx(p);
-        const float w = fmaf(y * 6.931471825e-01f, e, y);
+        const bool in = t < lim;
+        const bool near = p > -8.f;
+        const float w = (in && !near) ? fmaf(y * 6.931471825e-01f, e, y) : 0.f;
+        if (in && near) tv |= 1u << t;
         RunAcc::acc2(acc->sh, acc->sl, w, 0.f);
         if (USE_Q) {
           const float qt = (DET && t == xo) ? INFINITY : qv[t];
@@ -1456,6 +1460,7 @@ __device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, 
           }
         }
       }
+      top |= tv << (j * VW);
       continue;
     }
     uint32_t tv = 0u;
