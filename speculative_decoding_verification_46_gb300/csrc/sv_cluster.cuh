@@ -157,11 +157,12 @@ __device__ __forceinline__ uint64_t cluster_sweep16(const T* L, const float* Q, 
       if (near) tv |= 1u << t;
       RunAcc::acc2(acc->sh, acc->sl, w, 0.f);
       if (USE_Q) {
+        // on the residual support {w > s' q}: w - s' q and q, else 0 (adding
+        // 0 leaves both sums as they were)
         const float qt = (j * VW + t == xq) ? INFINITY : qv[t];
-        if (w > s_a * qt) {
-          RunAcc::acc2(acc->ah, acc->al, fmaf(-s_a, qt, w), 0.f);
-          acc->q += qt;
-        }
+        const bool sup = w > s_a * qt;
+        RunAcc::acc2(acc->ah, acc->al, sup ? fmaf(-s_a, qt, w) : 0.f, 0.f);
+        acc->q += sup ? qt : 0.f;
       }
     }
     top |= (uint64_t)tv << (j * VW);

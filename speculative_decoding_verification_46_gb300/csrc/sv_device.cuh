@@ -1453,11 +1453,12 @@ __device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, 
         if (in && near) tv |= 1u << t;
         RunAcc::acc2(acc->sh, acc->sl, w, 0.f);
         if (USE_Q) {
+          // on the residual support {w > s' q}: w - s' q and q, else 0 (adding
+          // 0 leaves both sums as they were; selects, not a branch per token)
           const float qt = (DET && t == xo) ? INFINITY : qv[t];
-          if (w > s_a * qt) {
-            RunAcc::acc2(acc->ah, acc->al, fmaf(-s_a, qt, w), 0.f);
-            acc->q += qt;
-          }
+          const bool sup = w > s_a * qt;
+          RunAcc::acc2(acc->ah, acc->al, sup ? fmaf(-s_a, qt, w) : 0.f, 0.f);
+          acc->q += sup ? qt : 0.f;
         }
       }
       top |= tv << (j * VW);
@@ -1553,6 +1554,7 @@ struct ChunkPick {
 __device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, const F2* cQ, int C, bool resid,
                                                    bool bad, float s_a, float u) {
   const int lane = threadIdx.x & 31;
+  const int NG = (C + 31) >> 5;   // groups holding chunks; the others are all zero and skipped
   F2 Sg[kPickGroups], Mg[kPickGroups];
   float Qg[kPickGroups];
 #pragma unroll
@@ -1572,7 +1574,8 @@ __device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, c
   }
   F2 sl = Sg[0];
 #pragma unroll
-  for (int g = 1; g < kPickGroups; ++g) sl = f2_add(sl, Sg[g]);
+  for (int g = 1; g < kPickGroups; ++g)
+    if (g < NG) sl = f2_add(sl, Sg[g]);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) sl = f2_add(sl, f2_shfl_xor(sl, m));
   ChunkPick r;
@@ -1587,30 +1590,36 @@ __device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, c
       Mg[g] = Sg[g];
     }
   }
-  auto total = [&](const F2* m) {
+  // inclusive prefix of the masses (group scans chained by a carry), kept for
+  // the search below
+  F2 inc[kPickGroups], cin[kPickGroups];
+  auto scan = [&]() {
     F2 carry{0.f, 0.f};
 #pragma unroll
     for (int g = 0; g < kPickGroups; ++g) {
-      const F2 inc = f2_add(carry, warp_incl_scan_f2(m[g]));
-      carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+      cin[g] = carry;
+      if (g < NG) {
+        inc[g] = f2_add(carry, warp_incl_scan_f2(Mg[g]));
+        carry = F2{__shfl_sync(0xffffffffu, inc[g].hi, 31), __shfl_sync(0xffffffffu, inc[g].lo, 31)};
+      }
     }
     return carry;
   };
-  F2 R = total(Mg);
+  F2 R = scan();
   if (resid && !bad && !f2_pos(R)) {
     r.resid0 = 1;   // zero residual mass (only through rounding): draw from p_n instead
 #pragma unroll
     for (int g = 0; g < kPickGroups; ++g) Mg[g] = Sg[g];
-    R = total(Mg);
+    R = scan();
   }
   r.target = f2_scale(R, u);
   int found = -1, last = -1;
-  F2 fbase{0.f, 0.f}, lbase{0.f, 0.f}, carry{0.f, 0.f};
+  F2 fbase{0.f, 0.f}, lbase{0.f, 0.f};
 #pragma unroll
   for (int g = 0; g < kPickGroups; ++g) {
-    const F2 inc = f2_add(carry, warp_incl_scan_f2(Mg[g]));
-    F2 excl = f2_shfl_up(inc, 1);
-    if (lane == 0) excl = carry;
+    if (g >= NG) break;
+    F2 excl = f2_shfl_up(inc[g], 1);
+    if (lane == 0) excl = cin[g];
     const bool live = g * 32 + lane < C && f2_pos(Mg[g]);
     const unsigned hit =
         __ballot_sync(0xffffffffu, live && !f2_lt(r.target, excl) && f2_lt(r.target, f2_add(excl, Mg[g])));
@@ -1625,7 +1634,6 @@ __device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, c
       last = g * 32 + l;
       lbase = F2{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
     }
-    carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
   }
   r.sub = (bad || !f2_pos(R)) ? -1 : (found >= 0 ? found : last);
   r.base = found >= 0 ? fbase : lbase;
