@@ -1752,6 +1752,7 @@ residual_kernel(const Params p) {
   // independent of the previous kernel, so before the wait: the exp2 table and,
   // for the streaming path, thread i's draft d_i, its logit, q_i(d_i) and u_i
   load_exp2_table(sm.tab);
+  const float u_fin = __ldg(p.uniforms + b * G1 + gb);   // the final draw's uniform (last CTA)
   int d_i = -1;
   float l_d = 0.f, q_d = 0.f, u_i = 0.f;
   if (from_parts && tid < gb) {
@@ -1846,7 +1847,7 @@ residual_kernel(const Params p) {
 
   // ---- last CTA of sequence b: exact normaliser, masses, chunk -> thread -> token
   int status = st.status;
-  const float u = __ldg(p.uniforms + b * G1 + gb);
+  const float u = u_fin;
   if (C <= kPickChunks) {
     if (tid < 32) {
       const ChunkPick pk = chunk_pick_w0(cS, cA, cQ, C, resid, bad, s_a, u);
