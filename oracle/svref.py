@@ -393,3 +393,61 @@ def truncate_emitted(out_tokens, n_accepted, stop_tokens=(), max_new=None):
         tok[b, k:] = -1
         emitted[b] = k
     return tok, emitted
+
+
+# An absolute band on the final draw's CDF steps for q formed from the
+# draft's logits: the step materialises q in float32 (relative error of each
+# q(v) a few 1e-7, so sum_v |dq(v)| < 1e-6), and the residual max(p - q, 0)
+# moves by no more than q does.
+QLOGITS_CDF_BAND = 1e-6
+
+
+def draft_proposal_from_logits(q_logits, temperature, top_k=0, top_p=1.0):
+    """q_i from the draft model's logits, transformed exactly as the target's
+    ([Ch11.1] §11.1.2: temperature and top-k / top-p are applied to p_i and
+    q_i alike, and q must be the draft's actual proposal).
+
+    q_logits [B, gamma, V].  Returns (q float64 [B, gamma, V], top_p_boundary
+    [B, gamma]).  A draft row that defines no distribution (NaN, +inf, only
+    -inf) gives q_i = 0 everywhere, so its q_i(d_i) <= 0.
+    """
+    Q = np.asarray(q_logits, dtype=np.float64)
+    B, G, V = Q.shape
+    q = np.zeros((B, G, V))
+    tb = np.zeros((B, G), dtype=bool)
+    for b in range(B):
+        for i in range(G):
+            qi, _bad, bd = target_distribution(Q[b, i], temperature, top_k, top_p)
+            q[b, i] = qi
+            tb[b, i] = bd
+    return q, tb
+
+
+def verify_sample_qlogits(logits, q_logits, draft, uniforms, temperature, top_k=0, top_p=1.0):
+    """The sampling verify step with the draft's proposal supplied as its
+    logits: q_i = the truncated softmax of q_logits_i / T (the same transform
+    as p_i), then the step of verify_sample.  The boundary flag also marks a
+    final draw whose u * R lies within QLOGITS_CDF_BAND (absolute, in
+    probability units) of the drawn token's CDF step."""
+    q, qtb = draft_proposal_from_logits(q_logits, temperature, top_k, top_p)
+    r = verify_sample(logits, q, draft, uniforms, temperature, top_k, top_p)
+    L = np.asarray(logits)
+    B, G1, V = L.shape
+    gamma = G1 - 1
+    U = np.asarray(uniforms, dtype=np.float32).reshape(B, G1)
+    for b in range(B):
+        r["boundary"][b] |= bool(qtb[b].any())
+        if r["status"][b] & SEQ_BAD_ROW:
+            continue
+        n = int(r["n_accepted"][b])
+        p_n, _, _ = target_distribution(L[b, n], temperature, top_k, top_p)
+        w = residual(p_n, q[b, n]) if n < gamma else p_n
+        if not (w.sum() > 0.0):
+            w = p_n
+        C = np.cumsum(w)
+        t = _f32(U[b, gamma]) * C[-1]
+        v = int(r["out_tokens"][b, n])
+        lower, upper = C[v] - w[v], C[v]
+        if abs(t - lower) < QLOGITS_CDF_BAND or abs(upper - t) < QLOGITS_CDF_BAND:
+            r["boundary"][b] = True
+    return r

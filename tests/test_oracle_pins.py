@@ -641,3 +641,79 @@ def test_truncate_emitted_is_the_longest_valid_prefix():
     t2, e2 = svref.truncate_emitted(tok, n, (), None)
     np.testing.assert_array_equal(t2, tok)
     np.testing.assert_array_equal(e2, n + 1)
+
+
+# ---------------------------------------------------------------- q as draft logits
+
+def test_qlogits_constant_rows_give_closed_form_uniforms():
+    """softmax of a constant row is uniform; top-k of a constant row keeps the k
+    lowest indices (ties rank by index); top-p of a uniform keeps the shortest
+    prefix reaching top_p, ceil(top_p * V) tokens."""
+    B, G, V = 2, 3, 40
+    Q = np.full((B, G, V), 1.75)
+    q, tb = svref.draft_proposal_from_logits(Q, 0.7)
+    assert np.allclose(q, 1.0 / V, rtol=0, atol=1e-15) and not tb.any()
+    q, _ = svref.draft_proposal_from_logits(Q, 0.7, top_k=7)
+    assert np.allclose(q[..., :7], 1.0 / 7, rtol=0, atol=1e-15) and np.all(q[..., 7:] == 0.0)
+    q, _ = svref.draft_proposal_from_logits(Q, 1.3, top_p=0.5)
+    J = math.ceil(np.float32(0.5) * V)
+    assert np.allclose(q[..., :J], 1.0 / J, rtol=0, atol=1e-15) and np.all(q[..., J:] == 0.0)
+
+
+def test_qlogits_shift_invariance():
+    rng = np.random.default_rng(11)
+    Q = rng.normal(size=(3, 2, 64)) * 3.0
+    shift = rng.normal(size=(3, 2, 1)) * 50.0
+    a, _ = svref.draft_proposal_from_logits(Q, 0.9, top_k=20, top_p=0.8)
+    b, _ = svref.draft_proposal_from_logits(Q + shift, 0.9, top_k=20, top_p=0.8)
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_qlogits_step_is_the_step_with_library_softmax_q(seed):
+    """Untruncated: q_i = scipy.special.softmax(q_logits_i / T) fed to the plain
+    step gives the same tokens and acceptance probabilities."""
+    rng = np.random.default_rng(100 + seed)
+    B, G, V, T = 6, 4, 30, 0.8
+    L = rng.normal(size=(B, G + 1, V)) * 2.0
+    Q = L[:, :G] + rng.normal(size=(B, G, V))
+    d = rng.integers(0, V, size=(B, G))
+    u = rng.random(size=(B, G + 1)).astype(np.float32)
+    q_lib = scipy.special.softmax(Q / float(np.float32(T)), axis=-1)
+    ref = svref.verify_sample(L, q_lib, d, u, T)
+    got = svref.verify_sample_qlogits(L, Q, d, u, T)
+    assert np.array_equal(got["out_tokens"], ref["out_tokens"])
+    assert np.array_equal(got["n_accepted"], ref["n_accepted"])
+    assert np.allclose(got["accept_prob"], ref["accept_prob"], rtol=1e-12, atol=0)
+
+
+def test_qlogits_equal_to_target_logits_accept_every_draft():
+    """q = p: every a_i = 1, so every draft is accepted and the bonus is the
+    inverse CDF (numpy searchsorted) of scipy's softmax of row gamma."""
+    rng = np.random.default_rng(7)
+    B, G, V, T = 8, 3, 25, 1.1
+    L = rng.normal(size=(B, G + 1, V)) * 1.5
+    d = rng.integers(0, V, size=(B, G))
+    u = rng.random(size=(B, G + 1)).astype(np.float32)
+    r = svref.verify_sample_qlogits(L, L[:, :G].copy(), d, u, T)
+    assert np.all(r["n_accepted"] == G)
+    assert np.allclose(r["accept_prob"], 1.0, rtol=0, atol=1e-12)
+    for b in range(B):
+        pg = scipy.special.softmax(L[b, G] / float(np.float32(T)))
+        tok = int(np.searchsorted(np.cumsum(pg), float(np.float32(u[b, G])) * pg.sum(), side="right"))
+        assert r["out_tokens"][b, G] == min(tok, V - 1)
+        assert np.array_equal(r["out_tokens"][b, :G], d[b])
+
+
+def test_qlogits_bad_draft_row_is_a_zero_q():
+    rng = np.random.default_rng(3)
+    B, G, V = 2, 2, 16
+    L = rng.normal(size=(B, G + 1, V))
+    Q = rng.normal(size=(B, G, V))
+    Q[0, 0, 5] = np.nan
+    Q[1, 0, :] = -np.inf
+    d = np.array([[1, 2], [3, 4]])
+    u = np.full((B, G + 1), 0.5, dtype=np.float32)
+    r = svref.verify_sample_qlogits(L, Q, d, u, 1.0)
+    assert np.all(r["accept_prob"][:, 0] == 1.0)          # q_0(d_0) = 0 with p_0(d_0) > 0
+    assert np.all(r["status"] & svref.SEQ_Q_NOT_POSITIVE)
