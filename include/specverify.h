@@ -215,6 +215,39 @@ sv_status sv_verify_greedy_ragged(int B, int gamma, int V,
                                   sv_stream_t stream);
 
 /*
+ * Sampling verify with the draft's proposal supplied as the draft model's
+ * LOGITS ("11.1 核心原理", section 11.1.2: temperature and truncation are
+ * applied to the draft's q_i exactly as to the target's p_i, and q_i must be
+ * the draft's actual proposal).  As sv_verify_sample, except
+ *
+ *   q_logits        [B][gamma][V] of q_logits_dtype (float32, bfloat16 or
+ *                   float16), 16-byte aligned: the draft's logits at the
+ *                   drafted positions; may be NULL when gamma = 0.  The
+ *                   library forms q_i = softmax(q_logits_i / temperature) in
+ *                   float32 in the workspace (its own kernel, one CTA per
+ *                   draft row) and runs the sv_verify_sample path on it.  A
+ *                   row holding NaN or +inf, or only -inf, gives q_i = 0, so
+ *                   testing position i raises SV_SEQ_Q_NOT_POSITIVE.
+ *   top_k, top_p    truncation of q is not implemented yet: top_k in (0, V)
+ *                   or top_p < 1 returns SV_ERR_UNSUPPORTED.
+ *   workspace       at least sv_qlogits_workspace_bytes(B, gamma, V) bytes.
+ *                   Its first sv_workspace_bytes(B, gamma, V, 0) bytes follow
+ *                   the usual zero-fill contract; the bytes after them hold
+ *                   q (scratch, fully rewritten by every call, any content
+ *                   allowed before it).
+ */
+size_t sv_qlogits_workspace_bytes(int B, int gamma, int V);
+sv_status sv_verify_sample_qlogits(int B, int gamma, int V,
+                                   const void* logits, sv_dtype logits_dtype,
+                                   const void* q_logits, sv_dtype q_logits_dtype,
+                                   const int32_t* draft_tokens, const float* uniforms,
+                                   float temperature, int top_k, float top_p,
+                                   int32_t* out_tokens, int32_t* out_num_accepted,
+                                   float* out_accept_prob, int32_t* out_status,
+                                   void* workspace, size_t workspace_bytes,
+                                   sv_stream_t stream);
+
+/*
  * Ending a round early ("11.1 核心原理", listing 10-1's comment: an EOS / stop
  * token or max_new_tokens may end the round, and no bonus token is forced).
  * In place on the outputs of a verify call:

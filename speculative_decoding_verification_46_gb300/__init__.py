@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     SV_SEQ_Q_NOT_POSITIVE,
     SV_SEQ_RESIDUAL_ZERO,
     SvError,
+    alloc_qlogits_workspace,
     alloc_workspace,
     load_library,
     sv_last_kernels,
@@ -28,10 +29,13 @@ from ._binding import (  # noqa: F401
     sv_verify_greedy,
     sv_verify_greedy_noalloc,
     sv_verify_greedy_ragged,
+    sv_qlogits_workspace_bytes,
     sv_verify_sample,
+    sv_verify_sample_qlogits,
     sv_verify_sample_ragged,
     sv_workspace_bytes,
     truncate_emitted,
     verify_greedy,
     verify_sample,
+    verify_sample_qlogits,
 )

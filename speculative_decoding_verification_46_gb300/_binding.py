@@ -82,6 +82,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sv_truncate_emitted.restype = _c_int
     lib.sv_last_kernels.argtypes = []
     lib.sv_last_kernels.restype = ctypes.c_char_p
+    lib.sv_qlogits_workspace_bytes.argtypes = [_c_int, _c_int, _c_int]
+    lib.sv_qlogits_workspace_bytes.restype = _c_size
+    lib.sv_verify_sample_qlogits.argtypes = [_c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr,
+                                             _c_float, _c_int, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                             _c_ptr, _c_size, _c_ptr]
+    lib.sv_verify_sample_qlogits.restype = _c_int
     _lib = lib
     return lib
 
@@ -90,6 +96,19 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def sv_workspace_bytes(B: int, gamma: int, V: int, top_k: int = 0) -> int:
     return int(load_library().sv_workspace_bytes(B, gamma, V, top_k))
+
+
+def sv_qlogits_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return int(load_library().sv_qlogits_workspace_bytes(B, gamma, V))
+
+
+def sv_verify_sample_qlogits(B, gamma, V, logits, logits_dtype, q_logits, q_logits_dtype, draft_tokens, uniforms,
+                             temperature, top_k, top_p, out_tokens, out_num_accepted, out_accept_prob, out_status,
+                             workspace, workspace_bytes, stream) -> int:
+    return int(load_library().sv_verify_sample_qlogits(B, gamma, V, logits, logits_dtype, q_logits, q_logits_dtype,
+                                                        draft_tokens, uniforms, float(temperature), int(top_k),
+                                                        float(top_p), out_tokens, out_num_accepted, out_accept_prob,
+                                                        out_status, workspace, workspace_bytes, stream))
 
 
 def sv_status_string(status: int) -> str:
@@ -231,6 +250,52 @@ def verify_sample(logits, q, draft, uniforms, temperature=1.0, top_k=0, top_p=1.
                                      _stream_handle(dev, stream))
     if st != SV_OK:
         raise SvError(st, "sv_verify_sample")
+    return out_tokens, out_n, out_a, out_status
+
+
+def alloc_qlogits_workspace(B: int, gamma: int, V: int, device=None) -> torch.Tensor:
+    """A zero-filled device workspace large enough for verify_sample_qlogits."""
+    n = sv_qlogits_workspace_bytes(B, gamma, V)
+    if n == 0 and B > 0:
+        raise SvError(SV_ERR_INVALID_ARG, "sv_qlogits_workspace_bytes")
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def verify_sample_qlogits(logits, q_logits, draft, uniforms, temperature=1.0, top_k=0, top_p=1.0, *,
+                          workspace=None, stream=None, want_accept_prob=True, outputs=None):
+    """Speculative-sampling verify with the draft's proposal given as its
+    logits: q_logits [B, gamma, V] (float32 / bfloat16 / float16, CUDA);
+    q_i = softmax(q_logits_i / temperature) is formed on the GPU.  Other
+    arguments and the result as verify_sample."""
+    B, G1, V = logits.shape
+    G = G1 - 1
+    dev = logits.device
+    _need_cuda("logits", logits)
+    if logits.dtype not in _TORCH_DTYPE:
+        raise ValueError(f"unsupported logits dtype {logits.dtype}")
+    if G > 0:
+        _need_cuda("q_logits", q_logits)
+        if q_logits.dtype not in _TORCH_DTYPE:
+            raise ValueError(f"unsupported q_logits dtype {q_logits.dtype}")
+    _need_cuda("draft", draft if G > 0 else None, torch.int32)
+    _need_cuda("uniforms", uniforms, torch.float32)
+    if outputs is None:
+        out_tokens = torch.empty(B, G1, dtype=torch.int32, device=dev)
+        out_n = torch.empty(B, dtype=torch.int32, device=dev)
+        out_a = torch.empty(B, G, dtype=torch.float32, device=dev) if want_accept_prob and G > 0 else None
+        out_status = torch.empty(B, dtype=torch.int32, device=dev)
+    else:
+        out_tokens, out_n, out_a, out_status = outputs
+    if workspace is None:
+        workspace = alloc_qlogits_workspace(B, G, V, dev)
+    st = sv_verify_sample_qlogits(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype],
+                                  _addr(q_logits) if G > 0 else None,
+                                  _TORCH_DTYPE[q_logits.dtype] if G > 0 else 0,
+                                  _addr(draft) if G > 0 else None, _addr(uniforms), temperature, top_k, top_p,
+                                  _addr(out_tokens), _addr(out_n), _addr(out_a), _addr(out_status),
+                                  _addr(workspace), workspace.numel(), _stream_handle(dev, stream))
+    if st != SV_OK:
+        raise SvError(st, "sv_verify_sample_qlogits")
     return out_tokens, out_n, out_a, out_status
 
 

@@ -9,10 +9,12 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <string>
 
 #include "specverify.h"
 #include "sv_cluster.cuh"
 #include "sv_device.cuh"
+#include "sv_qsoftmax.cuh"
 #include "sv_stream.cuh"
 #include "sv_truncate.cuh"
 #include "sv_topk.cuh"
@@ -414,6 +416,14 @@ extern "C" size_t sv_workspace_bytes(int B, int gamma, int V, int top_k) {
   return make_layout(B, gamma, V, top_k).total;
 }
 
+// sv_verify_sample_qlogits: the usual layout first (so a later call of any
+// other entry point on the same workspace finds its part zero-filled), then
+// the float32 q the transform kernel writes.
+extern "C" size_t sv_qlogits_workspace_bytes(int B, int gamma, int V) {
+  if (!sizes_ok(B, gamma, V)) return 0;
+  return up(make_layout(B, gamma, V, 0).total) + up(sizeof(float) * (size_t)B * gamma * V);
+}
+
 namespace {
 
 sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype, const float* q,
@@ -520,6 +530,65 @@ extern "C" sv_status sv_verify_sample_ragged(int B, int gamma, int V, const void
   return verify_sample_impl(B, gamma, V, logits, logits_dtype, q, draft_tokens, uniforms, gamma_b, temperature, top_k,
                             top_p, out_tokens, out_num_accepted, out_accept_prob, out_status, workspace,
                             workspace_bytes, stream);
+}
+
+namespace {
+thread_local std::string g_qlogits_kernels;
+
+template <typename TQ>
+sv_status launch_q_softmax(const void* q_logits, float* q, int rows, int V, float c, float c_lo, cudaStream_t st) {
+  const TQ* src = static_cast<const TQ*>(q_logits);
+  if (V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0)
+    sv::q_softmax_kernel<TQ, true><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, c, c_lo);
+  else
+    sv::q_softmax_kernel<TQ, false><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, c, c_lo);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,
+                                              const void* q_logits, sv_dtype q_logits_dtype,
+                                              const int32_t* draft_tokens, const float* uniforms, float temperature,
+                                              int top_k, float top_p, int32_t* out_tokens, int32_t* out_num_accepted,
+                                              float* out_accept_prob, int32_t* out_status, void* workspace,
+                                              size_t workspace_bytes, sv_stream_t stream) {
+  g_last_kernels = "";
+  if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
+  auto dtype_ok = [](sv_dtype d) { return d == SV_DTYPE_F32 || d == SV_DTYPE_BF16 || d == SV_DTYPE_F16; };
+  if (!dtype_ok(logits_dtype) || !dtype_ok(q_logits_dtype)) return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  if (top_k < 0 || top_k > SV_MAX_TOP_K) return SV_ERR_INVALID_ARG;
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return SV_ERR_INVALID_ARG;
+  if ((top_k > 0 && top_k < V) || top_p < 1.0f) return SV_ERR_UNSUPPORTED;   // truncation of q: not yet
+  if (B == 0) return SV_OK;
+  if (!logits || !uniforms || !out_tokens || !out_num_accepted) return SV_ERR_INVALID_ARG;
+  if (gamma > 0 && (!draft_tokens || !q_logits)) return SV_ERR_INVALID_ARG;
+  if (!aligned16(logits) || (q_logits && !aligned16(q_logits))) return SV_ERR_INVALID_ARG;
+  const size_t q_off = up(make_layout(B, gamma, V, 0).total);
+  const size_t need = q_off + up(sizeof(float) * (size_t)B * gamma * V);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return SV_ERR_WORKSPACE;
+  float* qbuf = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + q_off);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (gamma > 0) {
+    const double cd = 1.4426950408889634 / (double)temperature;
+    const float c = (float)cd, c_lo = (float)(cd - (double)c);
+    const int rows = B * gamma;
+    sv_status s = SV_OK;
+    switch (q_logits_dtype) {
+      case SV_DTYPE_F32: s = launch_q_softmax<float>(q_logits, qbuf, rows, V, c, c_lo, st); break;
+      case SV_DTYPE_BF16: s = launch_q_softmax<__nv_bfloat16>(q_logits, qbuf, rows, V, c, c_lo, st); break;
+      case SV_DTYPE_F16: s = launch_q_softmax<__half>(q_logits, qbuf, rows, V, c, c_lo, st); break;
+    }
+    if (s != SV_OK) return s;
+  }
+  const sv_status s = verify_sample_impl(B, gamma, V, logits, logits_dtype, gamma > 0 ? qbuf : nullptr,
+                                         draft_tokens, uniforms, nullptr, temperature, top_k, top_p, out_tokens,
+                                         out_num_accepted, out_accept_prob, out_status, workspace, q_off, stream);
+  if (s == SV_OK && gamma > 0) {
+    g_qlogits_kernels = std::string("q_softmax_kernel,") + g_last_kernels;
+    g_last_kernels = g_qlogits_kernels.c_str();
+  }
+  return s;
 }
 
 extern "C" sv_status sv_verify_greedy(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,

@@ -34,7 +34,8 @@ def test_exports_every_declared_symbol(sv):
     names = _declared_functions()
     assert set(names) == {"sv_workspace_bytes", "sv_verify_sample", "sv_verify_greedy", "sv_status_string",
                           "sv_set_timing_events", "sv_verify_greedy_noalloc", "sv_last_kernels",
-                          "sv_verify_sample_ragged", "sv_verify_greedy_ragged", "sv_truncate_emitted"}
+                          "sv_verify_sample_ragged", "sv_verify_greedy_ragged", "sv_truncate_emitted",
+                          "sv_qlogits_workspace_bytes", "sv_verify_sample_qlogits"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -161,3 +162,31 @@ def test_ragged_and_truncate_validation(sv):
     assert T(4, 3, A, A, None, 2, None, A, None) == sv.SV_ERR_INVALID_ARG      # n_stop > 0 needs the ids
     assert T(4, 3, None, A, None, 0, None, A, None) == sv.SV_ERR_INVALID_ARG
     assert T(0, 3, None, None, None, 0, None, None, None) == sv.SV_OK
+
+
+def test_qlogits_validation(sv):
+    """Draft logits: the workspace adds float32 q after the usual layout;
+    truncation of q is refused as unsupported; argument errors launch nothing."""
+    B, G, V = 4, 3, 100
+    base = sv.sv_workspace_bytes(B, G, V, 0)
+    ws = sv.sv_qlogits_workspace_bytes(B, G, V)
+    assert ws >= base + 4 * B * G * V and ws % 256 == 0
+    assert sv.sv_qlogits_workspace_bytes(-1, G, V) == 0 and sv.sv_qlogits_workspace_bytes(B, 65, V) == 0
+
+    def call(**kw):
+        a = dict(B=B, gamma=G, V=V, logits=A, ldt=sv.SV_DTYPE_BF16, ql=A + 8192, qdt=sv.SV_DTYPE_BF16,
+                 d=A + 16384, u=A + 20480, T=1.0, k=0, p=1.0, tok=A + 24576, n=A + 28672, ws=A + 65536,
+                 wsb=ws)
+        a.update(kw)
+        return sv.sv_verify_sample_qlogits(a["B"], a["gamma"], a["V"], a["logits"], a["ldt"], a["ql"], a["qdt"],
+                                           a["d"], a["u"], a["T"], a["k"], a["p"], a["tok"], a["n"], None, None,
+                                           a["ws"], a["wsb"], None)
+    assert call(k=10) == sv.SV_ERR_UNSUPPORTED
+    assert call(p=0.9) == sv.SV_ERR_UNSUPPORTED
+    assert call(qdt=7) == sv.SV_ERR_INVALID_ARG
+    assert call(T=0.0) == sv.SV_ERR_INVALID_ARG
+    assert call(ql=None) == sv.SV_ERR_INVALID_ARG
+    assert call(ql=A + 8194) == sv.SV_ERR_INVALID_ARG         # not 16-byte aligned
+    assert call(wsb=ws - 256) == sv.SV_ERR_WORKSPACE
+    assert call(B=0, logits=None, ql=None) == sv.SV_OK
+    assert sv.sv_last_kernels() == []
