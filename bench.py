@@ -99,18 +99,34 @@ def _elt_bytes(w):
     return {"f32": 4, "bf16": 2, "f16": 2}[w.dtype]
 
 
+def _q_elt_bytes(w) -> int:
+    """Bytes per q element the step reads: float32 q, the draft's logits in
+    w's dtype, or none (greedy, deterministic drafts)."""
+    if w.mode != "sample" or w.deterministic:
+        return 0
+    return _elt_bytes(w) if w.qlogits else 4
+
+
+def _workspace(sv, w, B, G, V, dev):
+    if w.qlogits:
+        return sv.alloc_qlogits_workspace(B, G, V, dev)
+    return sv.alloc_workspace(B, G, V, w.top_k if w.mode == "sample" else 0, dev)
+
+
 def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0, gamma_b=None):
     """Bytes the method must move for one step, split by kernel.
 
     streaming kernel: every logit once, plus the gathers of l(d_i) and q(d_i);
     final-draw kernel (untruncated sampling): one row of logits per sequence,
-    plus the q row of a rejected sequence.  With top-k the final draw reads
+    plus the q row of a rejected sequence (q as the draft's logits: its
+    16-bit logits, counted once; the float32 q the library forms from them is
+    the implementation's own traffic).  With top-k the final draw reads
     only the kept candidates' q values (inside the streaming kernel).
     Deterministic drafts (q one-hot, passed as None) read no q bytes.  A
     ragged round (gamma_b given) needs only rows 0..gamma_b of each sequence."""
     s = _elt_bytes(w)
     B, G, V = len(n_accepted), w.gamma, w.V
-    qb = 0 if w.deterministic else 4
+    qb = _q_elt_bytes(w)
     gsum = int(np.sum(gamma_b)) if gamma_b is not None else B * G
     if w.mode == "greedy":
         return {"stream": (gsum + B) * V * s, "final": 0}
@@ -238,6 +254,9 @@ def _packed(named, dev):
 
 
 def _call(sv, w, inp, out, ws, stream):
+    if w.qlogits:
+        return sv.verify_sample_qlogits(inp["logits"], inp["q_logits"], inp["draft"], inp["uniforms"],
+                                        w.temperature, w.top_k, w.top_p, workspace=ws, stream=stream, outputs=out)
     if w.mode == "greedy":
         return sv.verify_greedy(inp["logits"], inp["draft"], workspace=ws, stream=stream,
                                 outputs=(out[0], out[1], out[3]))
@@ -261,14 +280,14 @@ def run_gb300(args, rank, ws_n, local):
     B, G, V = w.B, w.gamma, w.V
     positions = B * (G + 1)
 
-    per_set = B * (G + 1) * V * _elt_bytes(w) + (B * G * V * 4 if (w.mode == "sample" and not w.deterministic) else 0)
+    per_set = B * (G + 1) * V * _elt_bytes(w) + B * G * V * _q_elt_bytes(w)
     n_sets = max(2, min(1024, math.ceil(2 * L2_BYTES / per_set) + 1))
     sets = _input_sets(w, n_sets, dev)
     outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
              torch.empty(B, G, dtype=torch.float32, device=dev) if w.mode == "sample" and G > 0 else None,
              torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
     top_k_ws = w.top_k if w.mode == "sample" else 0
-    wsp = sv.alloc_workspace(B, G, V, top_k_ws, dev)
+    wsp = _workspace(sv, w, B, G, V, dev)
     stream = torch.cuda.Stream(device=dev)
 
     # default steps: about a second of timed work
@@ -276,8 +295,11 @@ def run_gb300(args, rank, ws_n, local):
         for i in range(n_sets):
             _call(sv, w, sets[i], outs[i], wsp, stream)
     torch.cuda.synchronize()
-    kernel_names = sv.sv_last_kernels()      # what one call launches (the path the library chose)
-    kernels_per_call = len(kernel_names) + (1 if w.ragged else 0)   # + the truncation kernel
+    all_kernels = sv.sv_last_kernels()       # what one call launches (the path the library chose)
+    kernels_per_call = len(all_kernels) + (1 if w.ragged else 0)   # + the truncation kernel
+    # the timing hook brackets the verify kernels; q_softmax_kernel (draft
+    # logits -> q) runs before its first event and is timed with the step only
+    kernel_names = [k for k in all_kernels if k != "q_softmax_kernel"]
     if kernels_per_call == 0:
         raise RuntimeError("the verify call launched no kernel")
     t0 = time.perf_counter()
@@ -460,13 +482,13 @@ def other_workloads(args, local):
         if name == args.workload:
             continue
         B, G, V = w.B, w.gamma, w.V
-        per_set = B * (G + 1) * V * _elt_bytes(w) + (B * G * V * 4 if (w.mode == "sample" and not w.deterministic) else 0)
+        per_set = B * (G + 1) * V * _elt_bytes(w) + B * G * V * _q_elt_bytes(w)
         n_sets = max(2, min(512, math.ceil(2 * L2_BYTES / per_set) + 1))
         sets = _input_sets(w, n_sets, dev)
         outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
                  torch.empty(B, G, dtype=torch.float32, device=dev) if w.mode == "sample" and G > 0 else None,
                  torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
-        wsp = sv.alloc_workspace(B, G, V, w.top_k if w.mode == "sample" else 0, dev)
+        wsp = _workspace(sv, w, B, G, V, dev)
         stream = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(stream):
             for i in range(n_sets):
@@ -514,6 +536,7 @@ def oracle_throughput(w, budget_s: float, device="cpu"):
     d = inp["draft"].cpu().numpy()
     u = inp["uniforms"].cpu().numpy()
     q = inp["q"].cpu().numpy() if inp["q"] is not None else None
+    qlg = inp["q_logits"].float().cpu().numpy() if w.qlogits else None
     gbh = inp["gamma_b"].cpu().numpy() if w.ragged else None
     stops = inp["stop_tokens"].cpu().numpy() if w.ragged else None
     mxh = inp["max_new"].cpu().numpy() if w.ragged else None
@@ -528,6 +551,8 @@ def oracle_throughput(w, budget_s: float, device="cpu"):
             r = svref.verify_sample_ragged(L[sl], q[sl] if q is not None else None, d[sl], u[sl], w.temperature,
                                            gbh[sl], w.top_k, w.top_p)
             svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[sl])
+        elif w.qlogits:
+            svref.verify_sample_qlogits(L[sl], qlg[sl], d[sl], u[sl], w.temperature, w.top_k, w.top_p)
         else:
             svref.verify_sample(L[sl], q[sl] if q is not None else None, d[sl], u[sl], w.temperature, w.top_k,
                                 w.top_p)
@@ -556,6 +581,7 @@ def main():
         d = inp["draft"].cpu().numpy()
         u = inp["uniforms"].cpu().numpy()
         q = inp["q"].cpu().numpy() if inp["q"] is not None else None
+        qlg = inp["q_logits"].float().cpu().numpy() if w.qlogits else None
         gbh = inp["gamma_b"].cpu().numpy() if w.ragged else None
         stops = inp["stop_tokens"].cpu().numpy() if w.ragged else None
         mxh = inp["max_new"].cpu().numpy() if w.ragged else None
@@ -567,6 +593,8 @@ def main():
             r = svref.verify_sample_ragged(L[:1], q[:1] if q is not None else None, d[:1], u[:1], w.temperature,
                                            gbh[:1], w.top_k, w.top_p)
             svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[:1])
+        elif w.qlogits:
+            svref.verify_sample_qlogits(L[:1], qlg[:1], d[:1], u[:1], w.temperature, w.top_k, w.top_p)
         else:
             svref.verify_sample(L[:1], q[:1] if q is not None else None, d[:1], u[:1], w.temperature, w.top_k,
                                 w.top_p)
@@ -577,8 +605,16 @@ def main():
         def step():
             if w.mode == "greedy":
                 svref.verify_greedy(L[:nseq], d[:nseq])
+            elif w.ragged:
+                r = svref.verify_sample_ragged(L[:nseq], q[:nseq] if q is not None else None, d[:nseq], u[:nseq],
+                                               w.temperature, gbh[:nseq], w.top_k, w.top_p)
+                svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[:nseq])
+            elif w.qlogits:
+                svref.verify_sample_qlogits(L[:nseq], qlg[:nseq], d[:nseq], u[:nseq], w.temperature, w.top_k,
+                                            w.top_p)
             else:
-                svref.verify_sample(L[:nseq], q[:nseq], d[:nseq], u[:nseq], w.temperature, w.top_k, w.top_p)
+                svref.verify_sample(L[:nseq], q[:nseq] if q is not None else None, d[:nseq], u[:nseq],
+                                    w.temperature, w.top_k, w.top_p)
 
         for _ in range(warmup):
             step()

@@ -17,7 +17,12 @@ def test_shapes_and_support(name):
     assert inp["uniforms"].shape == (2, G + 1) and inp["uniforms"].dtype == torch.float32
     assert torch.all((inp["uniforms"] >= 0) & (inp["uniforms"] < 1))
     assert torch.all((inp["draft"] >= 0) & (inp["draft"] < V))
-    if w.mode == "greedy" or w.deterministic:
+    if w.qlogits:
+        # the draft's logits in the workload's dtype; q is formed by the library
+        assert inp["q"] is None
+        ql = inp["q_logits"]
+        assert ql.shape == (2, G, V) and ql.dtype == w.torch_dtype and torch.isfinite(ql.float()).all()
+    elif w.mode == "greedy" or w.deterministic:
         assert inp["q"] is None
     else:
         q = inp["q"]

@@ -51,6 +51,7 @@ class Workload:
     deterministic: bool = False   # q = None: the drafter's guess argmax(target + noise)
     ragged: bool = False          # per-sequence gamma_b in [1, gamma], stop tokens and token budgets
     n_stop: int = 0               # stop-token ids of a ragged round
+    qlogits: bool = False         # the draft's proposal supplied as its logits (w's dtype), q formed on the GPU
 
     @property
     def rows(self) -> int:
@@ -88,6 +89,8 @@ WORKLOADS = {
                  draft_sigma=0.7, seed=53, ragged=True, n_stop=4),
         Workload("topk50_topp0.9_b256_g8_v152064_bf16", 256, 8, 152064, "bf16", "sample", 0.8,
                  top_k=50, top_p=0.9, draft_sigma=0.7, seed=51),
+        Workload("sample_qlogits_b64_g4_v128256_bf16", 64, 4, 128256, "bf16", "sample", 1.0,
+                 draft_sigma=0.7, seed=54, qlogits=True),
     ]
 }
 
@@ -152,6 +155,16 @@ def make_inputs(w: Workload, seed: int | None = None, device="cpu", B: int | Non
         coin = torch.rand(B, G, generator=g, device=device) < 0.7
         rnd = torch.randint(0, w.V, (B, G), generator=g, device=device)
         draft = torch.where(coin, best, rnd)
+    elif w.qlogits:
+        # the draft model's logits (target logits plus noise, w's dtype); its
+        # proposal softmax(q_logits / T) is formed by the library
+        ql = (w.draft_scale * Lf + w.draft_sigma * torch.randn(B, G, w.V, generator=g, device=device)).to(w.torch_dtype)
+        if G > 0:
+            qp = torch.softmax(ql.float() / w.temperature, dim=-1)
+            draft = torch.multinomial(qp.view(B * G, w.V), 1, generator=g).view(B, G)
+            del qp
+        else:
+            draft = torch.zeros(B, 0, dtype=torch.int64, device=device)
     elif w.deterministic:
         # a deterministic drafter (n-gram / prompt lookup stand-in): its guess
         # is the argmax of the target logits plus noise; q is one-hot (None)
@@ -168,6 +181,8 @@ def make_inputs(w: Workload, seed: int | None = None, device="cpu", B: int | Non
     uniforms = torch.rand(B, G + 1, generator=g, device=device, dtype=torch.float32)
     out = dict(logits=logits.contiguous(), q=None if q is None else q.contiguous(),
                draft=draft.to(torch.int32).contiguous(), uniforms=uniforms.contiguous())
+    if w.qlogits:
+        out["q_logits"] = ql.contiguous()
     if w.ragged:
         # gamma_b uniform in [1, gamma]; the stop ids are frequent target tokens
         # (the argmax of sequence 0's rows) so that some rounds stop early;
