@@ -189,7 +189,7 @@ int path_override() {
 }
 
 bool plan_cluster(const sv::Params& p, sv_dtype dt, int mode, sv::ClusterParams* cp, size_t* smem) {
-  if (mode == sv::MODE_TOPK) return false;
+  if (mode == sv::MODE_TOPK || p.ql) return false;   // q from draft logits: the streaming path
   const int ov = path_override();
   if (ov == 1) return false;
   const int VW = vec_width(dt);
@@ -314,7 +314,8 @@ sv_status launch_stream_dense(sv::Params& p, cudaStream_t stream) {
     cudaGetLastError();
     return SV_ERR_CUDA;
   }
-  const long long R = (long long)p.B * (p.gamma + 1);
+  // rows streamed: the target's, then (q formed from the draft's logits) the draft's
+  const long long R = (long long)p.B * (p.gamma + 1) + (p.ql ? (long long)p.B * p.gamma : 0);
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sv::kSt, smem) != cudaSuccess || per_sm < 1) {
     cudaGetLastError();
@@ -430,7 +431,8 @@ sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dty
                              const int32_t* draft_tokens, const float* uniforms, const int32_t* gamma_b,
                              float temperature, int top_k, float top_p, int32_t* out_tokens,
                              int32_t* out_num_accepted, float* out_accept_prob, int32_t* out_status, void* workspace,
-                             size_t workspace_bytes, sv_stream_t stream) {
+                             size_t workspace_bytes, sv_stream_t stream, const void* ql = nullptr,
+                             float4* qpart = nullptr) {
   g_last_kernels = "";
   if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
   if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
@@ -468,6 +470,8 @@ sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dty
   p.draft = draft_tokens;
   p.uniforms = uniforms;
   p.gamma_b = gamma_b;
+  p.ql = ql;
+  p.qpart = qpart;
   p.out_tokens = out_tokens;
   p.out_n = out_num_accepted;
   p.out_a = out_accept_prob;
@@ -569,6 +573,20 @@ extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const voi
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return SV_ERR_WORKSPACE;
   float* qbuf = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + q_off);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // Fused: the streaming kernel also streams the draft rows (their maximum and
+  // sum) and the final-draw kernel forms q from the draft's logits where it
+  // needs it, so q is never written out.  Needs the streaming path (16-byte
+  // vectors of one dtype on both sides); its draft-row partials (at most 4
+  // parts x 8 warps per row) use the q scratch.
+  const bool fused = gamma > 0 && q_logits_dtype == logits_dtype && V % vec_width(logits_dtype) == 0 &&
+                     path_override() != 3 && (size_t)V * sizeof(float) >= 4 * sv::kWarps * sizeof(float4);
+  if (fused) {
+    const sv_status s = verify_sample_impl(B, gamma, V, logits, logits_dtype, nullptr, draft_tokens, uniforms,
+                                           nullptr, temperature, top_k, top_p, out_tokens, out_num_accepted,
+                                           out_accept_prob, out_status, workspace, q_off, stream, q_logits,
+                                           reinterpret_cast<float4*>(qbuf));
+    return s;
+  }
   if (gamma > 0) {
     const double cd = 1.4426950408889634 / (double)temperature;
     const float c = (float)cd, c_lo = (float)(cd - (double)c);

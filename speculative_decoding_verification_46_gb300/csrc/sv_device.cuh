@@ -89,6 +89,9 @@ struct Params {
   int2* rowres;                   // [R][top_k + 1] kept (index, probability) lists
   float2* chunk_mass;             // [B][3][C] residual chunk sums (S, A, Q; two-float)
   const int* gamma_b;             // [B] drafts per sequence (ragged rounds), or nullptr: gamma
+  const void* ql;                 // [B][gamma][V] draft logits (same dtype as logits) when q is formed
+                                  // from them in the streaming path, else nullptr
+  float4* qpart;                  // [B * gamma][H][kWarps] the draft rows' streaming partials (with ql)
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -98,6 +101,29 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// q(v) of a draft row from its logit x, the row's maximum qm and sum qs of
+// 2^((x - qm) c): the weight is formed as every tail weight of the final draw
+// (16-bit x - qm exact; -inf clamped to an exponent that flushes to 0;
+// ex2.approx with a first-order correction), then divided by the sum.
+__device__ __forceinline__ float q_weight(float x, float qm, float c, float c_lo) {
+  const float dh = fmaxf(x - qm, -1.0e4f);
+  const float p = dh * c;
+  const float e = fmaf(dh, c_lo, fmaf(dh, c, -p));
+  const float y = ex2_approx(p);
+  return fmaf(y * 6.931471825e-01f, e, y);
+}
+
+// q of the final-draw row when it is formed from the draft's logits: the
+// row's maximum, 1 / its sum, and whether the row defines no distribution
+// (then q = 0).
+struct QLrow {
+  float m, inv;
+  bool bad;
+  __device__ __forceinline__ float q(float x, float c, float c_lo) const {
+    return bad ? 0.f : q_weight(x, m, c, c_lo) * inv;
+  }
+};
 
 // Programmatic dependent launch: let the next kernel on the stream start its
 // prologue early / wait until this grid's memory is visible.
@@ -1408,9 +1434,10 @@ __device__ __forceinline__ void res_cp16(void* smem, const void* gmem) {
 // for a residual row, DET when q is a deterministic draft's one-hot (q = +inf
 // at token xq takes it out of the support, q = 0 elsewhere).  Returns the
 // bit mask of run offsets near the row maximum, left to run_top.
-template <typename T, bool USE_Q, bool DET>
+template <typename T, bool USE_Q, bool DET, bool QL = false>
 __device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, bool have_q, int xq, int e0, int NS,
-                                              int V, float M, float c, float c_lo, float s_a, RunAcc* acc) {
+                                              int V, float M, float c, float c_lo, float s_a, RunAcc* acc,
+                                              QLrow qlr = QLrow{0.f, 0.f, true}) {
   constexpr int VW = Tr<T>::VW;
   constexpr bool EXACT = sizeof(T) == 2;
   const int tid = threadIdx.x;
@@ -1419,16 +1446,23 @@ __device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, 
   for (int j = 0; j < NS; ++j) {
     const uint4 v = lg[j * kThreads + tid];
     float qv[VW];
+    if (QL) {
+      // q from the staged draft logits (one 16-byte vector per VW tokens)
+      const uint4 qx = qq[j * kThreads + tid];
 #pragma unroll
-    for (int h = 0; h < VW / 4; ++h) {
-      if (USE_Q && have_q) {
-        const uint4 q4 = qq[(j * (VW / 4) + h) * kThreads + tid];
-        qv[4 * h + 0] = __uint_as_float(q4.x);
-        qv[4 * h + 1] = __uint_as_float(q4.y);
-        qv[4 * h + 2] = __uint_as_float(q4.z);
-        qv[4 * h + 3] = __uint_as_float(q4.w);
-      } else {
-        qv[4 * h + 0] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
+      for (int t = 0; t < VW; ++t) qv[t] = qlr.q(Tr<T>::get(qx, t), c, c_lo);
+    } else {
+#pragma unroll
+      for (int h = 0; h < VW / 4; ++h) {
+        if (USE_Q && have_q) {
+          const uint4 q4 = qq[(j * (VW / 4) + h) * kThreads + tid];
+          qv[4 * h + 0] = __uint_as_float(q4.x);
+          qv[4 * h + 1] = __uint_as_float(q4.y);
+          qv[4 * h + 2] = __uint_as_float(q4.z);
+          qv[4 * h + 3] = __uint_as_float(q4.w);
+        } else {
+          qv[4 * h + 0] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
+        }
       }
     }
     const int ev = e0 + j * VW;
@@ -1482,7 +1516,8 @@ template <typename T>
 __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, int xq, int e0, int NS, int V,
                                                bool vec_ok,
                                                bool use_q, float M, float c, float c_lo, float s_a, uint4* stage,
-                                               RunAcc* acc, const float* tab) {
+                                               RunAcc* acc, const float* tab, const T* qlrow = nullptr,
+                                               QLrow qlr = QLrow{0.f, 0.f, true}) {
   using RS = ResStage<T>;
   constexpr int VW = RS::VW;
   constexpr bool EXACT = sizeof(T) == 2;
@@ -1494,13 +1529,17 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
     const int nv = min(max(V - e, 0), VW);
     if (nv == VW && vec_ok) {
       res_cp16(lg + j * kThreads + tid, row + e);
-      if (qrow) {
+      if (qlrow) {
+        res_cp16(qq + j * kThreads + tid, qlrow + e);   // the draft's logits: one vector per VW tokens
+      } else if (qrow) {
 #pragma unroll
         for (int h = 0; h < VW / 4; ++h) res_cp16(qq + (j * (VW / 4) + h) * kThreads + tid, qrow + e + 4 * h);
       }
     } else {
       lg[j * kThreads + tid] = load_slot<T>(row, e, max(nv, 0), vec_ok && nv == VW);
-      if (qrow) {
+      if (qlrow) {
+        qq[j * kThreads + tid] = load_slot<T>(qlrow, e, max(nv, 0), vec_ok && nv == VW);
+      } else if (qrow) {
 #pragma unroll
         for (int h = 0; h < VW / 4; ++h) {
           float4 q4;
@@ -1515,11 +1554,14 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   // tail tokens in one branch-free sweep (specialised for the residual /
-  // bonus rows and for a deterministic draft's one-hot q); tokens near the
-  // maximum (bit set in `top`) in a second loop
+  // bonus rows, for q formed from the draft's logits and for a deterministic
+  // draft's one-hot q); tokens near the maximum (bit set in `top`) in a
+  // second loop
   uint32_t top;
   if (!use_q)
     top = run_sweep<T, false, false>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
+  else if (qlrow)
+    top = run_sweep<T, true, false, true>(lg, qq, true, -1, e0, NS, V, M, c, c_lo, s_a, acc, qlr);
   else if (xq < 0)
     top = run_sweep<T, true, false>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
   else
@@ -1529,9 +1571,11 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
     top &= top - 1;
     const int j = o / VW, t = o - j * VW;
     const float x = Tr<T>::get(lg[j * kThreads + tid], t);
-    const float qv = (e0 + o == xq) ? INFINITY
-                                    : (qrow ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3))
-                                            : 0.f);
+    const float qv =
+        (e0 + o == xq) ? INFINITY
+        : qlrow        ? qlr.q(Tr<T>::get(qq[j * kThreads + tid], t), c, c_lo)
+        : qrow         ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3))
+                       : 0.f;
     run_top<EXACT>(*acc, x, qv, use_q, M, c, c_lo, s_a, tab);
   }
 }
@@ -1649,12 +1693,14 @@ __device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, c
 // aligned lane segment merges one row.
 __device__ __forceinline__ int stream_np(const Params& p) { return p.H * kWarps; }
 
+// base: the first of the nrow rows' partial slots (sequence b's rows are
+// contiguous).  sBad[i] = the row defines no distribution (greedy: a NaN), for
+// i <= gb only when mask_gb.
 template <int MODE>
-__device__ __forceinline__ void merge_row_parts(const Params& p, int b, int G1, int gb, float* sM, double* sS,
-                                                int* sG, int* sBad) {
+__device__ __forceinline__ void merge_row_parts_at(const Params& p, const float4* base, int G1, int gb, bool mask_gb,
+                                                   float* sM, double* sS, int* sG, int* sBad) {
   const int NP = stream_np(p);
   const int E = G1 * NP;
-  const float4* base = p.part + (size_t)b * E;
   for (int e0 = 0; e0 < E; e0 += kThreads) {        // uniform over the block: every lane shuffles
     const int e = e0 + (int)threadIdx.x;
     const bool ok = e < E;
@@ -1672,7 +1718,7 @@ __device__ __forceinline__ void merge_row_parts(const Params& p, int b, int G1, 
       if (head) {
         const bool nan = bv != bv;
         sG[i] = (nan || bi == 0x7fffffff) ? 0 : bi;
-        sBad[i] = nan && i <= gb;
+        sBad[i] = nan && (!mask_gb || i <= gb);
       }
     } else {
       float M = v.x;
@@ -1687,11 +1733,17 @@ __device__ __forceinline__ void merge_row_parts(const Params& p, int b, int G1, 
         const double sum = (double)t.hi + (double)t.lo;
         sM[i] = M;
         sS[i] = sum;
-        sBad[i] = (!(M > -INFINITY && M < INFINITY) || !(sum > 0.0 && sum < 1e300)) && i <= gb;
+        sBad[i] = (!(M > -INFINITY && M < INFINITY) || !(sum > 0.0 && sum < 1e300)) && (!mask_gb || i <= gb);
       }
     }
   }
 }
+template <int MODE>
+__device__ __forceinline__ void merge_row_parts(const Params& p, int b, int G1, int gb, float* sM, double* sS,
+                                                int* sG, int* sBad) {
+  merge_row_parts_at<MODE>(p, p.part + (size_t)b * G1 * stream_np(p), G1, gb, true, sM, sS, sG, sBad);
+}
+
 
 // Warp 0: the first i < count with flags[i] != 0 (count if none), and
 // whether any flag2[i] is set for i <= last.
@@ -1729,6 +1781,9 @@ struct ResSmem {
   double rS[kMaxG1];
   int rBad[kMaxG1];
   int rRej[kMaxG1];
+  float qM[kMaxG1];      // draft rows (q from the draft's logits): maximum, sum, no distribution
+  double qS[kMaxG1];
+  int qBad[kMaxG1];
   int rStatus;
   int rN;
 };
@@ -1754,13 +1809,17 @@ residual_kernel(const Params p) {
   load_exp2_table(sm.tab);
   const float u_fin = __ldg(p.uniforms + b * G1 + gb);   // the final draw's uniform (last CTA)
   int d_i = -1;
-  float l_d = 0.f, q_d = 0.f, u_i = 0.f;
+  float l_d = 0.f, q_d = 0.f, u_i = 0.f, ql_d = 0.f;
+  const T* qlb = p.ql ? static_cast<const T*>(p.ql) + (size_t)b * G * V : nullptr;   // this sequence's draft logits
   if (from_parts && tid < gb) {
     d_i = __ldg(p.draft + b * G + tid);
     u_i = __ldg(p.uniforms + b * G1 + tid);
     if (d_i >= 0 && d_i < V) {
       l_d = TR::get(load_slot<T>(static_cast<const T*>(p.logits) + ((size_t)b * G1 + tid) * V, d_i, 1, false), 0);
-      q_d = p.q ? __ldg(p.q + ((size_t)b * G + tid) * V + d_i) : 1.f;   // NULL: one-hot draft
+      if (qlb)
+        ql_d = TR::get(load_slot<T>(qlb + (size_t)tid * V, d_i, 1, false), 0);
+      else
+        q_d = p.q ? __ldg(p.q + ((size_t)b * G + tid) * V + d_i) : 1.f;   // NULL: one-hot draft
     }
   }
   pdl_wait();
@@ -1769,9 +1828,14 @@ residual_kernel(const Params p) {
     // merge the row partials, accept/reject, scan (every CTA of the sequence
     // computes the same values; chunk 0 writes the per-draft outputs)
     merge_row_parts<MODE_SOFTMAX>(p, b, G1, gb, sm.rM, sm.rS, nullptr, sm.rBad);
+    if (qlb)   // the draft rows' statistics: q_i = 2^((x - m_i) c) / s_i
+      merge_row_parts_at<MODE_SOFTMAX>(p, p.qpart + (size_t)b * G * stream_np(p), G, gb, false, sm.qM, sm.qS, nullptr,
+                                       sm.qBad);
     if (tid == 0) sm.rStatus = 0;
     __syncthreads();
     float a = 0.f;
+    if (qlb && tid < gb && d_i >= 0 && d_i < V)
+      q_d = sm.qBad[tid] ? 0.f : q_weight(ql_d, sm.qM[tid], p.c, p.c_lo) * (float)(1.0 / sm.qS[tid]);
     if (tid < gb) {
       int bits = 0;
       const float ssum = (float)sm.rS[tid];
@@ -1819,8 +1883,12 @@ residual_kernel(const Params p) {
   const bool bad = (st.status & SEQ_BADROW) != 0;
   const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
   const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
+  // q from the draft's logits: row n of them and its statistics
+  const T* qlrow = (resid && qlb) ? qlb + (size_t)n * V : nullptr;
+  QLrow qlr{0.f, 0.f, true};
+  if (qlrow) qlr = QLrow{sm.qM[n], (float)(1.0 / sm.qS[n]), sm.qBad[n] != 0};
   // deterministic drafts (q == NULL): q_n is one-hot at d_n
-  const int xq = (resid && !p.q) ? __ldg(p.draft + b * G + n) : -1;
+  const int xq = (resid && !p.q && !qlb) ? __ldg(p.draft + b * G + n) : -1;
   const float M = st.M;
   const float s_a = (float)st.s;
   const bool vec_ok = (V % VW) == 0;
@@ -1834,7 +1902,7 @@ residual_kernel(const Params p) {
   acc.zero();
   if (!bad)
     run_accumulate<T>(row, qrow, xq, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc,
-                      sm.tab);
+                      sm.tab, qlrow, qlr);
   {
     const F2x3 t = block_sum_f2x3_w0(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
     if (tid == 0) {
@@ -1914,7 +1982,7 @@ residual_kernel(const Params p) {
     RunAcc r;
     r.zero();
     run_accumulate<T>(row, uq ? qrow : nullptr, xq, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, stage,
-                      &r, sm.tab);
+                      &r, sm.tab, uq ? qlrow : nullptr, qlr);
     F2 mine = r.mass(uq, sm.ds);
     if (mine.hi < 0.f) mine = F2{0.f, 0.f};
     F2 total;
@@ -1938,10 +2006,10 @@ residual_kernel(const Params p) {
         const int j = lane / VW, t = lane - j * VW;
         const float x = TR::get(stage[j * kThreads + owner], t);
         const float qv =
-            uq ? (qrow ? __uint_as_float(word_of(
-                             stage[(ResStage<T>::NL + j * (VW / 4) + t / 4) * kThreads + owner], t & 3))
-                       : (e == xq ? INFINITY : 0.f))
-               : 0.f;
+            !uq    ? 0.f
+            : qlrow ? qlr.q(TR::get(stage[(ResStage<T>::NL + j) * kThreads + owner], t), p.c, p.c_lo)
+            : qrow  ? __uint_as_float(word_of(stage[(ResStage<T>::NL + j * (VW / 4) + t / 4) * kThreads + owner], t & 3))
+                    : (e == xq ? INFINITY : 0.f);
         m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds, sm.tab);
       }
       const F2 inc = warp_incl_scan_f2(m);

@@ -68,6 +68,9 @@ struct RowWalk {
   // rows claimed at run time (H = 1): the CTA's j-th row is dyn[j & 3], and
   // the walk ends at the first claim >= R; otherwise rows are dealt statically
   const int* dyn = nullptr;
+  // rows from Rt on are the draft's logits (q formed from them), row r - Rt of ql
+  int Rt = 0x7fffffff;
+  const void* ql = nullptr;
   __device__ __forceinline__ int row_of(int j) const { return dyn ? dyn[j & 3] : blockIdx.x + j * gridDim.x; }
   __device__ __forceinline__ bool live(int j) const { return dyn ? dyn[j & 3] < R : j < nrows; }
   // item j of this CTA: row r, vectors [vb, ve)
@@ -87,7 +90,8 @@ struct Issuer {
   __device__ __forceinline__ void at(const T* logits, size_t V, const RowWalk& w) {
     int r;
     w.item(j, &r, &vb, &ve);
-    row = logits + (size_t)min(r, w.R - 1) * V;
+    r = min(r, w.R - 1);
+    row = r >= w.Rt ? static_cast<const T*>(w.ql) + (size_t)(r - w.Rt) * V : logits + (size_t)r * V;
   }
   __device__ __forceinline__ void start(const T* logits, size_t V, const RowWalk& w) { at(logits, V, w); }
   // issue the next item into its stage (an empty group past the end)
@@ -224,7 +228,10 @@ stream_dense_kernel(const Params p) {
   // the kernel that merges the partials may start its input-only prologue now
   pdl_launch_dependents();
   RowWalk w;
-  w.R = p.B * G1;
+  // target rows, then (q formed from the draft's logits) the draft rows
+  w.R = p.B * G1 + (p.ql ? p.B * p.gamma : 0);
+  w.Rt = p.B * G1;
+  w.ql = p.ql;
   w.G1 = G1;
   w.NV = V / VW;
   w.H = p.H;                              // parts per row (items = R * H)
@@ -285,7 +292,8 @@ stream_dense_kernel(const Params p) {
     }
     // ---- this warp's partial of the row part: shuffles and one store, no
     // block-wide step (the merge is the next kernel's)
-    float4* slot = p.part + ((size_t)r * w.H + vb / w.NVP) * (kSt / 32) + warp;
+    float4* slot = (r < w.Rt ? p.part + ((size_t)r * w.H + vb / w.NVP) * (kSt / 32)
+                             : p.qpart + ((size_t)(r - w.Rt) * w.H + vb / w.NVP) * (kSt / 32)) + warp;
     if (MODE == MODE_GREEDY) {
       int bi = best_i;
       float bv = best;

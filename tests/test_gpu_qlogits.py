@@ -1,7 +1,9 @@
 """q supplied as the draft model's logits (sv_verify_sample_qlogits) on the GPU
 against the oracle's verify_sample_qlogits (q_i = softmax(q_logits_i / T) in
-float64).  Acceptance probabilities within 1e-5 relative; tokens equal except
-at boundary draws, where the oracle also flags a final draw within 1e-6
+float64), on both of its paths: fused into the streaming and final-draw
+kernels (one dtype, 16-byte rows), or q formed by its own kernel first.
+Acceptance probabilities within 1e-5 relative; tokens equal except at
+boundary draws, where the oracle also flags a final draw within 1e-6
 (absolute, probability units) of a CDF step, the reach of a float32 q."""
 
 import numpy as np
@@ -97,8 +99,18 @@ def test_qlogits_full_size_sampled(sv):
     out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], T)
     rows = np.random.default_rng(1).choice(B, size=12, replace=False)
     P.compare_sample(out, _oracle(inp, T, rows=rows), V, rows=rows)
-    names = sv.sv_last_kernels()
-    assert names[0] == "q_softmax_kernel" and len(names) >= 2, names
+    # one dtype on both sides and 16-byte rows: the fused path (q never written out)
+    assert sv.sv_last_kernels() == ["stream_dense_kernel", "residual_kernel"]
+
+
+def test_qlogits_mixed_dtypes_materialise_q(sv):
+    """Draft logits in another dtype than the target's: q is formed by its own
+    kernel first (then the usual path)."""
+    inp = _ql_case(8, 16, 4, 32000, torch.bfloat16, torch.float32)
+    g = _gpu(inp)
+    out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], 0.9)
+    assert sv.sv_last_kernels()[0] == "q_softmax_kernel"
+    P.compare_sample(out, _oracle(inp, 0.9), 32000)
 
 
 def test_qlogits_truncation_unsupported(sv):
