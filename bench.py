@@ -109,7 +109,7 @@ def _q_elt_bytes(w) -> int:
 
 def _workspace(sv, w, B, G, V, dev):
     if w.qlogits:
-        return sv.alloc_qlogits_workspace(B, G, V, dev)
+        return sv.alloc_qlogits_workspace(B, G, V, w.top_k, dev)
     return sv.alloc_workspace(B, G, V, w.top_k if w.mode == "sample" else 0, dev)
 
 

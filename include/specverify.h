@@ -228,15 +228,19 @@ sv_status sv_verify_greedy_ragged(int B, int gamma, int V,
  *                   draft row) and runs the sv_verify_sample path on it.  A
  *                   row holding NaN or +inf, or only -inf, gives q_i = 0, so
  *                   testing position i raises SV_SEQ_Q_NOT_POSITIVE.
- *   top_k, top_p    truncation of q is not implemented yet: top_k in (0, V)
- *                   or top_p < 1 returns SV_ERR_UNSUPPORTED.
- *   workspace       at least sv_qlogits_workspace_bytes(B, gamma, V) bytes.
- *                   Its first sv_workspace_bytes(B, gamma, V, 0) bytes follow
+ *   top_k, top_p    as in sv_verify_sample, applied to q_i too: q_i is the
+ *                   draft's softmax renormalised over its own top-k then
+ *                   top-p set (one CTA per draft row: radix select of the
+ *                   k-th largest, ties to the lowest index, sorted top-p
+ *                   prefix), zero elsewhere.  Same limits as sv_verify_sample.
+ *   workspace       at least sv_qlogits_workspace_bytes(B, gamma, V, top_k)
+ *                   bytes.  Its first sv_workspace_bytes(B, gamma, V, top_k)
+ *                   bytes follow
  *                   the usual zero-fill contract; the bytes after them hold
  *                   q (scratch, fully rewritten by every call, any content
  *                   allowed before it).
  */
-size_t sv_qlogits_workspace_bytes(int B, int gamma, int V);
+size_t sv_qlogits_workspace_bytes(int B, int gamma, int V, int top_k);
 sv_status sv_verify_sample_qlogits(int B, int gamma, int V,
                                    const void* logits, sv_dtype logits_dtype,
                                    const void* q_logits, sv_dtype q_logits_dtype,

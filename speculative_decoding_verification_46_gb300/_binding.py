@@ -82,7 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sv_truncate_emitted.restype = _c_int
     lib.sv_last_kernels.argtypes = []
     lib.sv_last_kernels.restype = ctypes.c_char_p
-    lib.sv_qlogits_workspace_bytes.argtypes = [_c_int, _c_int, _c_int]
+    lib.sv_qlogits_workspace_bytes.argtypes = [_c_int, _c_int, _c_int, _c_int]
     lib.sv_qlogits_workspace_bytes.restype = _c_size
     lib.sv_verify_sample_qlogits.argtypes = [_c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr,
                                              _c_float, _c_int, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
@@ -98,8 +98,8 @@ def sv_workspace_bytes(B: int, gamma: int, V: int, top_k: int = 0) -> int:
     return int(load_library().sv_workspace_bytes(B, gamma, V, top_k))
 
 
-def sv_qlogits_workspace_bytes(B: int, gamma: int, V: int) -> int:
-    return int(load_library().sv_qlogits_workspace_bytes(B, gamma, V))
+def sv_qlogits_workspace_bytes(B: int, gamma: int, V: int, top_k: int = 0) -> int:
+    return int(load_library().sv_qlogits_workspace_bytes(B, gamma, V, top_k))
 
 
 def sv_verify_sample_qlogits(B, gamma, V, logits, logits_dtype, q_logits, q_logits_dtype, draft_tokens, uniforms,
@@ -253,9 +253,9 @@ def verify_sample(logits, q, draft, uniforms, temperature=1.0, top_k=0, top_p=1.
     return out_tokens, out_n, out_a, out_status
 
 
-def alloc_qlogits_workspace(B: int, gamma: int, V: int, device=None) -> torch.Tensor:
+def alloc_qlogits_workspace(B: int, gamma: int, V: int, top_k: int = 0, device=None) -> torch.Tensor:
     """A zero-filled device workspace large enough for verify_sample_qlogits."""
-    n = sv_qlogits_workspace_bytes(B, gamma, V)
+    n = sv_qlogits_workspace_bytes(B, gamma, V, top_k)
     if n == 0 and B > 0:
         raise SvError(SV_ERR_INVALID_ARG, "sv_qlogits_workspace_bytes")
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
@@ -265,7 +265,8 @@ def verify_sample_qlogits(logits, q_logits, draft, uniforms, temperature=1.0, to
                           workspace=None, stream=None, want_accept_prob=True, outputs=None):
     """Speculative-sampling verify with the draft's proposal given as its
     logits: q_logits [B, gamma, V] (float32 / bfloat16 / float16, CUDA);
-    q_i = softmax(q_logits_i / temperature) is formed on the GPU.  Other
+    q_i = softmax(q_logits_i / temperature), truncated by top_k / top_p like
+    p_i, is formed on the GPU.  Other
     arguments and the result as verify_sample."""
     B, G1, V = logits.shape
     G = G1 - 1
@@ -287,7 +288,7 @@ def verify_sample_qlogits(logits, q_logits, draft, uniforms, temperature=1.0, to
     else:
         out_tokens, out_n, out_a, out_status = outputs
     if workspace is None:
-        workspace = alloc_qlogits_workspace(B, G, V, dev)
+        workspace = alloc_qlogits_workspace(B, G, V, top_k, dev)
     st = sv_verify_sample_qlogits(B, G, V, _addr(logits), _TORCH_DTYPE[logits.dtype],
                                   _addr(q_logits) if G > 0 else None,
                                   _TORCH_DTYPE[q_logits.dtype] if G > 0 else 0,

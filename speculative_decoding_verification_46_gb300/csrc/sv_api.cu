@@ -420,9 +420,9 @@ extern "C" size_t sv_workspace_bytes(int B, int gamma, int V, int top_k) {
 // sv_verify_sample_qlogits: the usual layout first (so a later call of any
 // other entry point on the same workspace finds its part zero-filled), then
 // the float32 q the transform kernel writes.
-extern "C" size_t sv_qlogits_workspace_bytes(int B, int gamma, int V) {
-  if (!sizes_ok(B, gamma, V)) return 0;
-  return up(make_layout(B, gamma, V, 0).total) + up(sizeof(float) * (size_t)B * gamma * V);
+extern "C" size_t sv_qlogits_workspace_bytes(int B, int gamma, int V, int top_k) {
+  if (!sizes_ok(B, gamma, V) || top_k < 0 || top_k > SV_MAX_TOP_K) return 0;
+  return up(make_layout(B, gamma, V, top_k).total) + up(sizeof(float) * (size_t)B * gamma * V);
 }
 
 namespace {
@@ -540,9 +540,12 @@ namespace {
 thread_local std::string g_qlogits_kernels;
 
 template <typename TQ>
-sv_status launch_q_softmax(const void* q_logits, float* q, int rows, int V, float c, float c_lo, cudaStream_t st) {
+sv_status launch_q_softmax(const void* q_logits, float* q, int rows, int V, float c, float c_lo, int klist,
+                           float top_p, cudaStream_t st) {
   const TQ* src = static_cast<const TQ*>(q_logits);
-  if (V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0)
+  if (klist > 0)   // truncation: top-k then top-p, the target's transform
+    sv::q_truncate_kernel<TQ><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, klist, top_p, c, c_lo);
+  else if (V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0)
     sv::q_softmax_kernel<TQ, true><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, c, c_lo);
   else
     sv::q_softmax_kernel<TQ, false><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, c, c_lo);
@@ -563,12 +566,15 @@ extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const voi
   if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
   if (top_k < 0 || top_k > SV_MAX_TOP_K) return SV_ERR_INVALID_ARG;
   if (!(top_p > 0.0f && top_p <= 1.0f)) return SV_ERR_INVALID_ARG;
-  if ((top_k > 0 && top_k < V) || top_p < 1.0f) return SV_ERR_UNSUPPORTED;   // truncation of q: not yet
+  // truncation as in sv_verify_sample: k candidates at most SV_MAX_TOP_K
+  const bool truncate = (top_k > 0 && top_k < V) || top_p < 1.0f;
+  const int klist = truncate ? ((top_k > 0 && top_k < V) ? top_k : V) : 0;
+  if (klist > SV_MAX_TOP_K) return SV_ERR_UNSUPPORTED;
   if (B == 0) return SV_OK;
   if (!logits || !uniforms || !out_tokens || !out_num_accepted) return SV_ERR_INVALID_ARG;
   if (gamma > 0 && (!draft_tokens || !q_logits)) return SV_ERR_INVALID_ARG;
   if (!aligned16(logits) || (q_logits && !aligned16(q_logits))) return SV_ERR_INVALID_ARG;
-  const size_t q_off = up(make_layout(B, gamma, V, 0).total);
+  const size_t q_off = up(make_layout(B, gamma, V, top_k).total);
   const size_t need = q_off + up(sizeof(float) * (size_t)B * gamma * V);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return SV_ERR_WORKSPACE;
   float* qbuf = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + q_off);
@@ -578,7 +584,7 @@ extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const voi
   // needs it, so q is never written out.  Needs the streaming path (16-byte
   // vectors of one dtype on both sides); its draft-row partials (at most 4
   // parts x 8 warps per row) use the q scratch.
-  const bool fused = gamma > 0 && q_logits_dtype == logits_dtype && V % vec_width(logits_dtype) == 0 &&
+  const bool fused = gamma > 0 && !truncate && q_logits_dtype == logits_dtype && V % vec_width(logits_dtype) == 0 &&
                      path_override() != 3 && (size_t)V * sizeof(float) >= 4 * sv::kWarps * sizeof(float4);
   if (fused) {
     const sv_status s = verify_sample_impl(B, gamma, V, logits, logits_dtype, nullptr, draft_tokens, uniforms,
@@ -593,9 +599,9 @@ extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const voi
     const int rows = B * gamma;
     sv_status s = SV_OK;
     switch (q_logits_dtype) {
-      case SV_DTYPE_F32: s = launch_q_softmax<float>(q_logits, qbuf, rows, V, c, c_lo, st); break;
-      case SV_DTYPE_BF16: s = launch_q_softmax<__nv_bfloat16>(q_logits, qbuf, rows, V, c, c_lo, st); break;
-      case SV_DTYPE_F16: s = launch_q_softmax<__half>(q_logits, qbuf, rows, V, c, c_lo, st); break;
+      case SV_DTYPE_F32: s = launch_q_softmax<float>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, st); break;
+      case SV_DTYPE_BF16: s = launch_q_softmax<__nv_bfloat16>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, st); break;
+      case SV_DTYPE_F16: s = launch_q_softmax<__half>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, st); break;
     }
     if (s != SV_OK) return s;
   }

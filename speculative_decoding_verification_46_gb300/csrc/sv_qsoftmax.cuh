@@ -20,17 +20,8 @@ namespace sv {
 constexpr int kQsThreads = 1024;
 constexpr int kQsWarps = kQsThreads / 32;
 
-// The weight 2^((x - m) c) of one token (c = log2(e) / T as c + c_lo): x - m
-// is exact for 16-bit logits; -inf is clamped to an exponent whose ex2.approx
-// flushes to 0; ex2.approx with a first-order correction for the exponent's
-// low part.
-__device__ __forceinline__ float qs_weight(float x, float m, float c, float c_lo) {
-  const float dh = fmaxf(x - m, -1.0e4f);
-  const float p = dh * c;
-  const float e = fmaf(dh, c_lo, fmaf(dh, c, -p));
-  const float y = ex2_approx(p);
-  return fmaf(y * 6.931471825e-01f, e, y);
-}
+// The weight 2^((x - m) c) of one token: the final draw's q_weight.
+__device__ __forceinline__ float qs_weight(float x, float m, float c, float c_lo) { return q_weight(x, m, c, c_lo); }
 
 __device__ __forceinline__ float qs_block_max(float v, float* sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -145,6 +136,206 @@ __global__ void __launch_bounds__(kQsThreads) q_softmax_kernel(const T* __restri
   } else {
     for (int v0 = tid; v0 < V; v0 += kQsThreads)
       dst[v0] = bad ? 0.f : __fdiv_rn(qs_weight(TR::get(load_slot<T>(src, v0, 1, false), 0), m, c, c_lo), Sf);
+  }
+}
+
+}  // namespace sv
+
+namespace sv {
+
+// ---- q with truncation: top-k (value desc, index asc) then top-p over the
+// renormalised top-k, q renormalised over what is kept, zero elsewhere - the
+// transform the target's p gets.  One CTA of kQsThreads threads per draft
+// row, k <= kQsThreads candidates:
+//   1. the row maximum and NaN / +inf detection;
+//   2. K = the k-th largest value key, by a radix select over the row (one
+//      pass per 8-bit digit of the order-preserving key);
+//   3. the candidates: every value above K, then the lowest-index values
+//      equal to K (threads own contiguous index ranges, so a scan of their
+//      counts keeps index order);
+//   4. a bitonic sort of the (value, index) keys, largest first;
+//   5. softmax weights over the k, top-p prefix J, renormalised over J;
+//   6. the row written: zeros, then the J kept probabilities.
+struct QtSmem {
+  unsigned long long cand[kQsThreads];
+  float w[kQsThreads];
+  int hist[256];
+  int iscan[kQsWarps];
+  F2 f2scan[kQsWarps];
+  float fred[kQsWarps];
+  int ired[kQsWarps];
+  int count;
+  int digit;
+  int rank;
+  int J;
+};
+
+__device__ __forceinline__ F2 block_excl_f2_qs(F2 v, F2* sm, F2* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const F2 inc = warp_incl_scan_f2(v);
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  F2 base{0.f, 0.f}, tot{0.f, 0.f};
+  for (int w = 0; w < kQsWarps; ++w) {
+    if (w < warp) base = f2_add(base, sm[w]);
+    tot = f2_add(tot, sm[w]);
+  }
+  __syncthreads();
+  *total = tot;
+  F2 excl = f2_shfl_up(inc, 1);
+  if (lane == 0) excl = F2{0.f, 0.f};
+  return f2_add(base, excl);
+}
+
+__device__ __forceinline__ int qt_block_excl_int(int v, int* sm, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  int base = 0, tot = 0;
+  for (int w = 0; w < kQsWarps; ++w) {
+    if (w < warp) base += sm[w];
+    tot += sm[w];
+  }
+  __syncthreads();
+  *total = tot;
+  return base + inc - v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restrict__ ql, float* __restrict__ q, int V,
+                                                                int k, float top_p, float c, float c_lo) {
+  using TR = Tr<T>;
+  __shared__ QtSmem sm;
+  const int tid = threadIdx.x;
+  const T* src = ql + (size_t)blockIdx.x * V;
+  float* dst = q + (size_t)blockIdx.x * V;
+  auto val = [&](int v) { return TR::get(load_slot<T>(src, v, 1, false), 0); };
+  k = min(k, V);
+
+  // 1. maximum, bad row
+  float m = -INFINITY;
+  int bad = 0;
+#pragma unroll 8
+  for (int v = tid; v < V; v += kQsThreads) {
+    const float x = val(v);
+    bad |= (x != x) | (x == INFINITY);
+    m = fmaxf(m, x);
+  }
+  m = qs_block_max(m, sm.fred);
+  bad = qs_block_or(bad, sm.ired) || !(m > -INFINITY);
+  if (bad) {
+    for (int v = tid; v < V; v += kQsThreads) dst[v] = 0.f;
+    return;
+  }
+
+  // 2. K = the k-th largest value key (digits from the top, 8 bits a pass);
+  // the key bits below KEY_LOW_BIT carry nothing for 16-bit types and are masked
+  const uint32_t kmask = ~((1u << TR::KEY_LOW_BIT) - 1u);
+  uint32_t prefix = 0u;
+  int rank = k;   // rank sought among the keys matching prefix
+  for (int hi = 31; hi >= TR::KEY_LOW_BIT; hi -= 8) {
+    const int lo = hi - 7 > TR::KEY_LOW_BIT ? hi - 7 : TR::KEY_LOW_BIT;
+    const int nb = hi - lo + 1;
+    const uint32_t upper = hi == 31 ? 0u : ~((1u << (hi + 1)) - 1u);
+    if (tid < 256) sm.hist[tid] = 0;
+    __syncthreads();
+#pragma unroll 8
+    for (int v = tid; v < V; v += kQsThreads) {
+      const uint32_t key = okey(val(v)) & kmask;
+      if ((key & upper) == prefix) atomicAdd(&sm.hist[(key >> lo) & ((1u << nb) - 1u)], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0, dg = 0;
+      for (int d = (1 << nb) - 1; d >= 0; --d) {
+        if (run + sm.hist[d] >= rank) {
+          dg = d;
+          break;
+        }
+        run += sm.hist[d];
+      }
+      sm.digit = dg;
+      sm.rank = rank - run;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm.digit << lo;
+    rank = sm.rank;
+    __syncthreads();
+  }
+  const uint32_t K = prefix;
+
+  // 3. candidates: all keys above K, then the first `rank` keys equal to K in index order
+  if (tid == 0) sm.count = 0;
+  const int chunk = (V + kQsThreads - 1) / kQsThreads;
+  const int v0 = tid * chunk, v1 = min(v0 + chunk, V);
+  int eq = 0;
+  for (int v = v0; v < v1; ++v) eq += (okey(val(v)) & kmask) == K;
+  int tot_eq;
+  const int eq_base = qt_block_excl_int(eq, sm.iscan, &tot_eq);
+  for (int v = v0, seen = eq_base; v < v1; ++v) {
+    const float x = val(v);
+    const uint32_t key = okey(x) & kmask;
+    bool take = key > K;
+    if (key == K) take = seen++ < rank;
+    if (take) {
+      const int pos = atomicAdd(&sm.count, 1);
+      if (pos < kQsThreads) sm.cand[pos] = comp_key(x, v);
+    }
+  }
+  __syncthreads();
+  const int N = min(sm.count, kQsThreads);   // == k
+  if (tid >= N) sm.cand[tid] = 0ull;   // padding sorts last
+  __syncthreads();
+
+  // 4. bitonic sort, largest key first
+  for (int size = 2; size <= kQsThreads; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int partner = tid ^ stride;
+      if (partner > tid) {
+        const unsigned long long a = sm.cand[tid], b2 = sm.cand[partner];
+        const bool desc = (tid & size) == 0;
+        if (desc ? (a < b2) : (a > b2)) {
+          sm.cand[tid] = b2;
+          sm.cand[partner] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // 5. weights over the k, top-p prefix, renormalised over it
+  const float x = tid < N ? comp_val(sm.cand[tid]) : -INFINITY;
+  const float w = tid < N ? q_weight(x, m, c, c_lo) : 0.f;
+  sm.w[tid] = w;
+  F2 tot;
+  const F2 excl = block_excl_f2_qs(F2{w, 0.f}, sm.f2scan, &tot);
+  int J = N;
+  if (top_p < 1.0f) {
+    // the first rank whose cumulative renormalised mass reaches top_p
+    const float cum = (float)(((double)excl.hi + (double)excl.lo + (double)w) / ((double)tot.hi + (double)tot.lo));
+    if (tid == 0) sm.J = N;
+    __syncthreads();
+    if (tid < N && cum >= top_p) atomicMin(&sm.J, tid + 1);
+    __syncthreads();
+    J = sm.J;
+  }
+  // sum over the kept ranks (the first J)
+  F2 kept;
+  (void)block_excl_f2_qs(F2{tid < J ? w : 0.f, 0.f}, sm.f2scan, &kept);
+  const float Sk = kept.hi + kept.lo;
+
+  // 6. the row
+  for (int v = tid; v < V; v += kQsThreads) dst[v] = 0.f;
+  __syncthreads();
+  if (tid < J) {
+    const int idx = comp_idx(sm.cand[tid]);
+    if (idx >= 0 && idx < V) dst[idx] = __fdiv_rn(w, Sk);
   }
 }
 

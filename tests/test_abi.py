@@ -166,7 +166,7 @@ def test_ragged_and_truncate_validation(sv):
 
 def test_qlogits_validation(sv):
     """Draft logits: the workspace adds float32 q after the usual layout;
-    truncation of q is refused as unsupported; argument errors launch nothing."""
+    argument errors launch nothing (every call below fails validation)."""
     B, G, V = 4, 3, 100
     base = sv.sv_workspace_bytes(B, G, V, 0)
     ws = sv.sv_qlogits_workspace_bytes(B, G, V)
@@ -181,8 +181,9 @@ def test_qlogits_validation(sv):
         return sv.sv_verify_sample_qlogits(a["B"], a["gamma"], a["V"], a["logits"], a["ldt"], a["ql"], a["qdt"],
                                            a["d"], a["u"], a["T"], a["k"], a["p"], a["tok"], a["n"], None, None,
                                            a["ws"], a["wsb"], None)
-    assert call(k=10) == sv.SV_ERR_UNSUPPORTED
-    assert call(p=0.9) == sv.SV_ERR_UNSUPPORTED
+    assert call(k=2000) == sv.SV_ERR_INVALID_ARG             # top_k above SV_MAX_TOP_K
+    assert call(V=2000, p=0.9) == sv.SV_ERR_UNSUPPORTED       # top-p over more than SV_MAX_TOP_K tokens
+    assert call(k=10, wsb=sv.sv_qlogits_workspace_bytes(B, G, V, 10) - 256) == sv.SV_ERR_WORKSPACE
     assert call(qdt=7) == sv.SV_ERR_INVALID_ARG
     assert call(T=0.0) == sv.SV_ERR_INVALID_ARG
     assert call(ql=None) == sv.SV_ERR_INVALID_ARG

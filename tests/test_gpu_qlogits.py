@@ -113,13 +113,29 @@ def test_qlogits_mixed_dtypes_materialise_q(sv):
     P.compare_sample(out, _oracle(inp, 0.9), 32000)
 
 
-def test_qlogits_truncation_unsupported(sv):
-    inp = _gpu(_ql_case(5, 2, 2, 1000, torch.bfloat16, torch.bfloat16))
-    with pytest.raises(sv.SvError) as e:
-        sv.verify_sample_qlogits(inp["logits"], inp["q_logits"], inp["draft"], inp["uniforms"], 1.0, 50, 1.0)
-    assert e.value.status == sv.SV_ERR_UNSUPPORTED
-    with pytest.raises(sv.SvError):
+@pytest.mark.parametrize("tk_path", ["auto", "slices"])
+@pytest.mark.parametrize("ldt", ["bf16", "f32"])
+@pytest.mark.parametrize("V,G,B,k,tp,T", [(1000, 4, 12, 50, 1.0, 0.8), (1000, 4, 12, 50, 0.9, 0.8),
+                                          (40000, 3, 6, 50, 0.9, 1.0), (700, 2, 10, 0, 0.9, 1.2),
+                                          (5000, 4, 8, 1, 1.0, 1.0), (33, 3, 20, 40, 0.95, 0.7)])
+def test_qlogits_truncated(sv, monkeypatch, tk_path, ldt, V, G, B, k, tp, T):
+    """top-k / top-p applied to q_i as to p_i (the draft row's own kept set)."""
+    if tk_path == "slices":
+        monkeypatch.setenv("SPECVERIFY_PATH", "slices")
+    else:
+        monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
+    inp = _ql_case(6000 + V + k, B, G, V, DTYPES[ldt], DTYPES[ldt], spread=1.0, noise=0.5)
+    g = _gpu(inp)
+    out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], T, k, tp)
+    L, Q, d, u = (P.to_np(inp[x]) for x in ("logits", "q_logits", "draft", "uniforms"))
+    P.compare_sample(out, svref.verify_sample_qlogits(L, Q, d, u, T, k, tp), V)
+
+
+def test_qlogits_truncation_limits(sv):
+    inp = _gpu(_ql_case(5, 2, 2, 2000, torch.bfloat16, torch.bfloat16))
+    with pytest.raises(sv.SvError) as e:   # top-p over 2000 tokens with no top-k
         sv.verify_sample_qlogits(inp["logits"], inp["q_logits"], inp["draft"], inp["uniforms"], 1.0, 0, 0.9)
+    assert e.value.status == sv.SV_ERR_UNSUPPORTED
 
 
 def test_qlogits_workspace_shared_with_plain_calls(sv):
@@ -128,7 +144,7 @@ def test_qlogits_workspace_shared_with_plain_calls(sv):
     B, G, V, T = 8, 4, 4096, 0.9
     inp = _ql_case(99, B, G, V, torch.bfloat16, torch.bfloat16)
     g = _gpu(inp)
-    ws = sv.alloc_qlogits_workspace(B, G, V, DEV)
+    ws = sv.alloc_qlogits_workspace(B, G, V, device=DEV)
     for _ in range(2):
         out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], T, workspace=ws)
         P.compare_sample(out, _oracle(inp, T), V)
