@@ -543,9 +543,16 @@ template <typename TQ>
 sv_status launch_q_softmax(const void* q_logits, float* q, int rows, int V, float c, float c_lo, int klist,
                            float top_p, cudaStream_t st) {
   const TQ* src = static_cast<const TQ*>(q_logits);
-  if (klist > 0)   // truncation: top-k then top-p, the target's transform
-    sv::q_truncate_kernel<TQ><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, klist, top_p, c, c_lo);
-  else if (V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0)
+  if (klist > 0) {   // truncation: top-k then top-p, the target's transform
+    const bool vec = V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0;
+    auto kern = vec ? sv::q_truncate_kernel<TQ, true> : sv::q_truncate_kernel<TQ, false>;
+    const int smem = (int)sizeof(sv::QtSmem);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return SV_ERR_CUDA;
+    }
+    kern<<<(unsigned)rows, sv::kQsThreads, smem, st>>>(src, q, V, klist, top_p, c, c_lo);
+  } else if (V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0)
     sv::q_softmax_kernel<TQ, true><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, c, c_lo);
   else
     sv::q_softmax_kernel<TQ, false><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, c, c_lo);

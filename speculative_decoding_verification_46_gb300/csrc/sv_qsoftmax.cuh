@@ -146,20 +146,28 @@ namespace sv {
 // ---- q with truncation: top-k (value desc, index asc) then top-p over the
 // renormalised top-k, q renormalised over what is kept, zero elsewhere - the
 // transform the target's p gets.  One CTA of kQsThreads threads per draft
-// row, k <= kQsThreads candidates:
+// row, k <= kQsThreads:
 //   1. the row maximum and NaN / +inf detection;
-//   2. K = the k-th largest value key, by a radix select over the row (one
-//      pass per 8-bit digit of the order-preserving key);
-//   3. the candidates: every value above K, then the lowest-index values
-//      equal to K (threads own contiguous index ranges, so a scan of their
-//      counts keeps index order);
-//   4. a bitonic sort of the (value, index) keys, largest first;
+//   2. tau = the k-th largest of the threads' maxima, a lower bound of the
+//      k-th largest value (k distinct elements reach it): one pass collects
+//      every element >= tau (usually a few times k).  Only if more than
+//      kQtCap do, K = the exact k-th largest value key by a radix select over
+//      the row (one pass per 8-bit digit of the order-preserving key;
+//      warp-private histograms, lanes with equal digits add once), then
+//   3. the values above K and the ties at K; more than kQtCap of those (a
+//      flood of ties) keeps the lowest-index ties directly (threads own
+//      contiguous index ranges, a scan of their tie counts keeps index order);
+//   4. a bitonic sort of the (value, index) keys, largest first: the first k
+//      are the top-k with ties to the lowest index;
 //   5. softmax weights over the k, top-p prefix J, renormalised over J;
 //   6. the row written: zeros, then the J kept probabilities.
+// Every pass reads the row with coalesced 16-byte loads when V is a multiple
+// of the vector width.
+constexpr int kQtCap = 4096;
+
 struct QtSmem {
-  unsigned long long cand[kQsThreads];
-  float w[kQsThreads];
-  int hist[256];
+  unsigned long long cand[kQtCap];
+  int hist[kQsWarps][256];
   int iscan[kQsWarps];
   F2 f2scan[kQsWarps];
   float fred[kQsWarps];
@@ -207,26 +215,61 @@ __device__ __forceinline__ int qt_block_excl_int(int v, int* sm, int* total) {
   return base + inc - v;
 }
 
-template <typename T>
+// Bitonic sort of cand[0, P) (P a power of two, at most kQtCap), largest first.
+__device__ __forceinline__ void qt_sort_desc(unsigned long long* cand, int P) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P; i += kQsThreads) {
+        const int partner = i ^ stride;
+        if (partner > i) {
+          const unsigned long long a = cand[i], b2 = cand[partner];
+          const bool desc = (i & size) == 0;
+          if (desc ? (a < b2) : (a > b2)) {
+            cand[i] = b2;
+            cand[partner] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restrict__ ql, float* __restrict__ q, int V,
                                                                 int k, float top_p, float c, float c_lo) {
   using TR = Tr<T>;
-  __shared__ QtSmem sm;
-  const int tid = threadIdx.x;
+  constexpr int VW = TR::VW;
+  extern __shared__ __align__(16) unsigned char qt_raw[];
+  QtSmem& sm = *reinterpret_cast<QtSmem*>(qt_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const T* src = ql + (size_t)blockIdx.x * V;
   float* dst = q + (size_t)blockIdx.x * V;
+  const int NV = V / VW;
   auto val = [&](int v) { return TR::get(load_slot<T>(src, v, 1, false), 0); };
+  // every element once, coalesced: fn(value, index)
+  auto each = [&](auto&& fn) {
+    if (VEC) {
+#pragma unroll 4
+      for (int j = tid; j < NV; j += kQsThreads) {
+        const uint4 x = ldg_v4(src + (size_t)j * VW);
+#pragma unroll
+        for (int t = 0; t < VW; ++t) fn(TR::get(x, t), j * VW + t);
+      }
+    } else {
+      for (int v = tid; v < V; v += kQsThreads) fn(val(v), v);
+    }
+  };
   k = min(k, V);
 
-  // 1. maximum, bad row
+  // 1. maximum (this thread's, then the row's), bad row
   float m = -INFINITY;
   int bad = 0;
-#pragma unroll 8
-  for (int v = tid; v < V; v += kQsThreads) {
-    const float x = val(v);
+  each([&](float x, int) {
     bad |= (x != x) | (x == INFINITY);
     m = fmaxf(m, x);
-  }
+  });
+  const float m_thread = m;
   m = qs_block_max(m, sm.fred);
   bad = qs_block_or(bad, sm.ired) || !(m > -INFINITY);
   if (bad) {
@@ -234,8 +277,31 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
     return;
   }
 
-  // 2. K = the k-th largest value key (digits from the top, 8 bits a pass);
-  // the key bits below KEY_LOW_BIT carry nothing for 16-bit types and are masked
+  // 2a. tau = the k-th largest thread maximum: k distinct elements reach it,
+  // so every top-k element does; collect all elements >= tau (usually a few
+  // times k) and sort them
+  sm.cand[tid] = (unsigned long long)okey(m_thread);
+  __syncthreads();
+  qt_sort_desc(sm.cand, kQsThreads);
+  const uint32_t tau = (uint32_t)sm.cand[k - 1];
+  __syncthreads();
+  if (tid == 0) sm.count = 0;
+  __syncthreads();
+  each([&](float x, int v) {
+    if (okey(x) >= tau) {
+      const int pos = atomicAdd(&sm.count, 1);
+      if (pos < kQtCap) sm.cand[pos] = comp_key(x, v);
+    }
+  });
+  __syncthreads();
+  int N = sm.count;
+  int P = kQsThreads;
+  if (N <= kQtCap) {
+    while (P < N) P <<= 1;
+  } else {
+  // 2b. too many elements at or above tau: K = the k-th largest value key by
+  // a radix select (digits from the top, 8 bits a pass; the key bits below
+  // KEY_LOW_BIT carry nothing for 16-bit types and are masked)
   const uint32_t kmask = ~((1u << TR::KEY_LOW_BIT) - 1u);
   uint32_t prefix = 0u;
   int rank = k;   // rank sought among the keys matching prefix
@@ -243,22 +309,31 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
     const int lo = hi - 7 > TR::KEY_LOW_BIT ? hi - 7 : TR::KEY_LOW_BIT;
     const int nb = hi - lo + 1;
     const uint32_t upper = hi == 31 ? 0u : ~((1u << (hi + 1)) - 1u);
-    if (tid < 256) sm.hist[tid] = 0;
+    for (int e = tid; e < kQsWarps * 256; e += kQsThreads) (&sm.hist[0][0])[e] = 0;
     __syncthreads();
-#pragma unroll 8
-    for (int v = tid; v < V; v += kQsThreads) {
-      const uint32_t key = okey(val(v)) & kmask;
-      if ((key & upper) == prefix) atomicAdd(&sm.hist[(key >> lo) & ((1u << nb) - 1u)], 1);
+    each([&](float x, int) {
+      const uint32_t key = okey(x) & kmask;
+      const bool match = (key & upper) == prefix;
+      const uint32_t dg = (key >> lo) & ((1u << nb) - 1u);
+      const unsigned act = __activemask();
+      const unsigned same = __match_any_sync(act, match ? dg : 0xffffffffu);
+      if (match && lane == __ffs(same) - 1) atomicAdd(&sm.hist[warp][dg], __popc(same));
+    });
+    __syncthreads();
+    if (tid < 256) {
+      int t = 0;
+      for (int w = 0; w < kQsWarps; ++w) t += sm.hist[w][tid];
+      sm.hist[0][tid] = t;
     }
     __syncthreads();
     if (tid == 0) {
       int run = 0, dg = 0;
       for (int d = (1 << nb) - 1; d >= 0; --d) {
-        if (run + sm.hist[d] >= rank) {
+        if (run + sm.hist[0][d] >= rank) {
           dg = d;
           break;
         }
-        run += sm.hist[d];
+        run += sm.hist[0][d];
       }
       sm.digit = dg;
       sm.rank = rank - run;
@@ -270,49 +345,55 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
   }
   const uint32_t K = prefix;
 
-  // 3. candidates: all keys above K, then the first `rank` keys equal to K in index order
+  // 3. candidates: the values above K and the ties at K, sorted below
   if (tid == 0) sm.count = 0;
-  const int chunk = (V + kQsThreads - 1) / kQsThreads;
-  const int v0 = tid * chunk, v1 = min(v0 + chunk, V);
-  int eq = 0;
-  for (int v = v0; v < v1; ++v) eq += (okey(val(v)) & kmask) == K;
-  int tot_eq;
-  const int eq_base = qt_block_excl_int(eq, sm.iscan, &tot_eq);
-  for (int v = v0, seen = eq_base; v < v1; ++v) {
-    const float x = val(v);
-    const uint32_t key = okey(x) & kmask;
-    bool take = key > K;
-    if (key == K) take = seen++ < rank;
-    if (take) {
-      const int pos = atomicAdd(&sm.count, 1);
-      if (pos < kQsThreads) sm.cand[pos] = comp_key(x, v);
-    }
-  }
   __syncthreads();
-  const int N = min(sm.count, kQsThreads);   // == k
-  if (tid >= N) sm.cand[tid] = 0ull;   // padding sorts last
+  each([&](float x, int v) {
+    if ((okey(x) & kmask) >= K) {
+      const int pos = atomicAdd(&sm.count, 1);
+      if (pos < kQtCap) sm.cand[pos] = comp_key(x, v);
+    }
+  });
+  __syncthreads();
+  N = sm.count;
+  P = kQsThreads;
+  if (N <= kQtCap) {
+    while (P < N) P <<= 1;
+  } else {
+    // a flood of ties: the values above K, then the first `rank` ties in index order
+    __syncthreads();
+    if (tid == 0) sm.count = 0;
+    const int chunk = (V + kQsThreads - 1) / kQsThreads;
+    const int v0 = tid * chunk, v1 = min(v0 + chunk, V);
+    int eq = 0;
+    for (int v = v0; v < v1; ++v) eq += (okey(val(v)) & kmask) == K;
+    int tot_eq;
+    const int eq_base = qt_block_excl_int(eq, sm.iscan, &tot_eq);
+    for (int v = v0, seen = eq_base; v < v1; ++v) {
+      const float x = val(v);
+      const uint32_t key = okey(x) & kmask;
+      bool take = key > K;
+      if (key == K) take = seen++ < rank;
+      if (take) {
+        const int pos = atomicAdd(&sm.count, 1);
+        if (pos < kQsThreads) sm.cand[pos] = comp_key(x, v);
+      }
+    }
+    __syncthreads();
+    N = min(sm.count, kQsThreads);
+    P = kQsThreads;
+  }
+  }
+  for (int i = N + tid; i < P; i += kQsThreads) sm.cand[i] = 0ull;   // padding sorts last
   __syncthreads();
 
-  // 4. bitonic sort, largest key first
-  for (int size = 2; size <= kQsThreads; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int partner = tid ^ stride;
-      if (partner > tid) {
-        const unsigned long long a = sm.cand[tid], b2 = sm.cand[partner];
-        const bool desc = (tid & size) == 0;
-        if (desc ? (a < b2) : (a > b2)) {
-          sm.cand[tid] = b2;
-          sm.cand[partner] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  // 4. sort, largest key first; the first k are kept
+  qt_sort_desc(sm.cand, P);
+  N = min(N, k);
 
   // 5. weights over the k, top-p prefix, renormalised over it
   const float x = tid < N ? comp_val(sm.cand[tid]) : -INFINITY;
   const float w = tid < N ? q_weight(x, m, c, c_lo) : 0.f;
-  sm.w[tid] = w;
   F2 tot;
   const F2 excl = block_excl_f2_qs(F2{w, 0.f}, sm.f2scan, &tot);
   int J = N;
@@ -325,7 +406,6 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
     __syncthreads();
     J = sm.J;
   }
-  // sum over the kept ranks (the first J)
   F2 kept;
   (void)block_excl_f2_qs(F2{tid < J ? w : 0.f, 0.f}, sm.f2scan, &kept);
   const float Sk = kept.hi + kept.lo;
