@@ -297,9 +297,10 @@ def run_gb300(args, rank, ws_n, local):
     torch.cuda.synchronize()
     all_kernels = sv.sv_last_kernels()       # what one call launches (the path the library chose)
     kernels_per_call = len(all_kernels) + (1 if w.ragged else 0)   # + the truncation kernel
-    # the timing hook brackets the verify kernels; q_softmax_kernel (draft
-    # logits -> q) runs before its first event and is timed with the step only
-    kernel_names = [k for k in all_kernels if k != "q_softmax_kernel"]
+    # the timing hook brackets the verify kernels; the kernels that form q
+    # from draft logits (and clear it) run outside it and are timed with the
+    # step only
+    kernel_names = [k for k in all_kernels if k not in ("q_softmax_kernel", "q_truncate_kernel", "q_clear_kernel")]
     if kernels_per_call == 0:
         raise RuntimeError("the verify call launched no kernel")
     t0 = time.perf_counter()

@@ -234,11 +234,13 @@ sv_status sv_verify_greedy_ragged(int B, int gamma, int V,
  *                   k-th largest, ties to the lowest index, sorted top-p
  *                   prefix), zero elsewhere.  Same limits as sv_verify_sample.
  *   workspace       at least sv_qlogits_workspace_bytes(B, gamma, V, top_k)
- *                   bytes.  Its first sv_workspace_bytes(B, gamma, V, top_k)
- *                   bytes follow
- *                   the usual zero-fill contract; the bytes after them hold
- *                   q (scratch, fully rewritten by every call, any content
- *                   allowed before it).
+ *                   bytes: the layout of sv_workspace_bytes(B, gamma, V,
+ *                   top_k) first (so the other entry points can share it),
+ *                   then the float32 q and the kept-index lists of truncated
+ *                   draft rows.  The usual contract covers all of it: zero-
+ *                   filled before the first use, left zero-filled by every
+ *                   call that completes (truncated q is written only where
+ *                   kept, and cleared after the call).
  */
 size_t sv_qlogits_workspace_bytes(int B, int gamma, int V, int top_k);
 sv_status sv_verify_sample_qlogits(int B, int gamma, int V,

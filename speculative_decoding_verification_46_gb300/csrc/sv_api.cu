@@ -420,9 +420,14 @@ extern "C" size_t sv_workspace_bytes(int B, int gamma, int V, int top_k) {
 // sv_verify_sample_qlogits: the usual layout first (so a later call of any
 // other entry point on the same workspace finds its part zero-filled), then
 // the float32 q the transform kernel writes.
+// + the kept-index lists of truncated draft rows ([B * gamma][klist] int).
+size_t qlogits_list_bytes(int B, int gamma, int V, int top_k) {
+  return up(sizeof(int) * (size_t)B * gamma * std::max(list_len(V, top_k), 1));
+}
 extern "C" size_t sv_qlogits_workspace_bytes(int B, int gamma, int V, int top_k) {
   if (!sizes_ok(B, gamma, V) || top_k < 0 || top_k > SV_MAX_TOP_K) return 0;
-  return up(make_layout(B, gamma, V, top_k).total) + up(sizeof(float) * (size_t)B * gamma * V);
+  return up(make_layout(B, gamma, V, top_k).total) + up(sizeof(float) * (size_t)B * gamma * V) +
+         qlogits_list_bytes(B, gamma, V, top_k);
 }
 
 namespace {
@@ -541,7 +546,7 @@ thread_local std::string g_qlogits_kernels;
 
 template <typename TQ>
 sv_status launch_q_softmax(const void* q_logits, float* q, int rows, int V, float c, float c_lo, int klist,
-                           float top_p, cudaStream_t st) {
+                           float top_p, int* kept_list, cudaStream_t st) {
   const TQ* src = static_cast<const TQ*>(q_logits);
   if (klist > 0) {   // truncation: top-k then top-p, the target's transform
     const bool vec = V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0;
@@ -551,7 +556,7 @@ sv_status launch_q_softmax(const void* q_logits, float* q, int rows, int V, floa
       cudaGetLastError();
       return SV_ERR_CUDA;
     }
-    kern<<<(unsigned)rows, sv::kQsThreads, smem, st>>>(src, q, V, klist, top_p, c, c_lo);
+    kern<<<(unsigned)rows, sv::kQsThreads, smem, st>>>(src, q, V, klist, top_p, c, c_lo, kept_list);
   } else if (V % vec_width(std::is_same<TQ, float>::value ? SV_DTYPE_F32 : SV_DTYPE_BF16) == 0)
     sv::q_softmax_kernel<TQ, true><<<(unsigned)rows, sv::kQsThreads, 0, st>>>(src, q, V, c, c_lo);
   else
@@ -582,9 +587,11 @@ extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const voi
   if (gamma > 0 && (!draft_tokens || !q_logits)) return SV_ERR_INVALID_ARG;
   if (!aligned16(logits) || (q_logits && !aligned16(q_logits))) return SV_ERR_INVALID_ARG;
   const size_t q_off = up(make_layout(B, gamma, V, top_k).total);
-  const size_t need = q_off + up(sizeof(float) * (size_t)B * gamma * V);
+  const size_t q_bytes = up(sizeof(float) * (size_t)B * gamma * V);
+  const size_t need = q_off + q_bytes + qlogits_list_bytes(B, gamma, V, top_k);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return SV_ERR_WORKSPACE;
   float* qbuf = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + q_off);
+  int* klist_buf = reinterpret_cast<int*>(static_cast<unsigned char*>(workspace) + q_off + q_bytes);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // Fused: the streaming kernel also streams the draft rows (their maximum and
   // sum) and the final-draw kernel forms q from the draft's logits where it
@@ -606,19 +613,28 @@ extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const voi
     const int rows = B * gamma;
     sv_status s = SV_OK;
     switch (q_logits_dtype) {
-      case SV_DTYPE_F32: s = launch_q_softmax<float>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, st); break;
-      case SV_DTYPE_BF16: s = launch_q_softmax<__nv_bfloat16>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, st); break;
-      case SV_DTYPE_F16: s = launch_q_softmax<__half>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, st); break;
+      case SV_DTYPE_F32: s = launch_q_softmax<float>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, klist_buf, st); break;
+      case SV_DTYPE_BF16: s = launch_q_softmax<__nv_bfloat16>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, klist_buf, st); break;
+      case SV_DTYPE_F16: s = launch_q_softmax<__half>(q_logits, qbuf, rows, V, c, c_lo, klist, top_p, klist_buf, st); break;
     }
     if (s != SV_OK) return s;
   }
   const sv_status s = verify_sample_impl(B, gamma, V, logits, logits_dtype, gamma > 0 ? qbuf : nullptr,
                                          draft_tokens, uniforms, nullptr, temperature, top_k, top_p, out_tokens,
                                          out_num_accepted, out_accept_prob, out_status, workspace, q_off, stream);
-  if (s == SV_OK && gamma > 0) {
-    g_qlogits_kernels = std::string("q_softmax_kernel,") + g_last_kernels;
-    g_last_kernels = g_qlogits_kernels.c_str();
+  if (s != SV_OK || gamma == 0) return s;
+  // leave the q scratch zero-filled: the kept entries (truncated q) or all of it
+  const char* first = klist > 0 ? "q_truncate_kernel," : "q_softmax_kernel,";
+  const char* last = klist > 0 ? ",q_clear_kernel" : "";
+  if (klist > 0) {
+    sv::q_clear_kernel<<<(unsigned)(B * gamma), 256, 0, st>>>(qbuf, klist_buf, V, klist);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  } else if (cudaMemsetAsync(qbuf, 0, sizeof(float) * (size_t)B * gamma * V, st) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
   }
+  g_qlogits_kernels = std::string(first) + g_last_kernels + last;
+  g_last_kernels = g_qlogits_kernels.c_str();
   return s;
 }
 

@@ -2028,9 +2028,14 @@ residual_kernel(const Params p) {
   }
   for (int k2 = tid; k2 < 3 * C; k2 += kThreads) cS[k2] = F2{0.f, 0.f};
   if (from_parts) {
-    // every CTA of the sequence has read the row partials: zero them
+    // every CTA of the sequence has read the row partials: zero them (the
+    // draft rows' too, when q is formed from the draft's logits)
     const int E = G1 * stream_np(p);
     for (int e = tid; e < E; e += kThreads) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (qlb) {
+      const int Eq = G * stream_np(p);
+      for (int e = tid; e < Eq; e += kThreads) p.qpart[(size_t)b * Eq + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   if (tid == 0) {
     p.out_tokens[b * G1 + n] = token;

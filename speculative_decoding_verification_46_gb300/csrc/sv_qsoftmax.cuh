@@ -160,7 +160,7 @@ namespace sv {
 //   4. a bitonic sort of the (value, index) keys, largest first: the first k
 //      are the top-k with ties to the lowest index;
 //   5. softmax weights over the k, top-p prefix J, renormalised over J;
-//   6. the row written: zeros, then the J kept probabilities.
+//   6. the J kept probabilities written (the row holds zeros otherwise).
 // Every pass reads the row with coalesced 16-byte loads when V is a multiple
 // of the vector width.
 constexpr int kQtCap = 4096;
@@ -235,9 +235,13 @@ __device__ __forceinline__ void qt_sort_desc(unsigned long long* cand, int P) {
   }
 }
 
+// q is written only where it is kept: the row must hold zeros on entry (the
+// workspace contract) and q_clear_kernel restores them after the call, from
+// the list of kept indices (plus one; 0 = none) written here.
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restrict__ ql, float* __restrict__ q, int V,
-                                                                int k, float top_p, float c, float c_lo) {
+                                                                int k, float top_p, float c, float c_lo,
+                                                                int* __restrict__ kept_list) {
   using TR = Tr<T>;
   constexpr int VW = TR::VW;
   extern __shared__ __align__(16) unsigned char qt_raw[];
@@ -272,10 +276,7 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
   const float m_thread = m;
   m = qs_block_max(m, sm.fred);
   bad = qs_block_or(bad, sm.ired) || !(m > -INFINITY);
-  if (bad) {
-    for (int v = tid; v < V; v += kQsThreads) dst[v] = 0.f;
-    return;
-  }
+  if (bad) return;   // no distribution: q stays 0
 
   // 2a. tau = the k-th largest thread maximum: k distinct elements reach it,
   // so every top-k element does; collect all elements >= tau (usually a few
@@ -410,12 +411,25 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
   (void)block_excl_f2_qs(F2{tid < J ? w : 0.f, 0.f}, sm.f2scan, &kept);
   const float Sk = kept.hi + kept.lo;
 
-  // 6. the row
-  for (int v = tid; v < V; v += kQsThreads) dst[v] = 0.f;
-  __syncthreads();
+  // 6. the kept entries (the rest of the row is zero) and their list
   if (tid < J) {
     const int idx = comp_idx(sm.cand[tid]);
-    if (idx >= 0 && idx < V) dst[idx] = __fdiv_rn(w, Sk);
+    if (idx >= 0 && idx < V) {
+      dst[idx] = __fdiv_rn(w, Sk);
+      kept_list[(size_t)blockIdx.x * k + tid] = idx + 1;
+    }
+  }
+}
+
+// After the call: the kept entries back to zero, and the list with them.
+__global__ void q_clear_kernel(float* __restrict__ q, int* __restrict__ kept_list, int V, int k) {
+  for (int t = threadIdx.x; t < k; t += blockDim.x) {
+    int* e = kept_list + (size_t)blockIdx.x * k + t;
+    const int idx = *e - 1;
+    if (idx >= 0 && idx < V) {
+      q[(size_t)blockIdx.x * V + idx] = 0.f;
+      *e = 0;
+    }
   }
 }
 

@@ -138,6 +138,31 @@ def test_qlogits_truncation_limits(sv):
     assert e.value.status == sv.SV_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("kind", ["fused", "materialised", "truncated"])
+def test_qlogits_leaves_workspace_zero_filled(sv, kind):
+    """Every path leaves the whole workspace (layout, q scratch, kept lists)
+    zero-filled, as the contract says."""
+    B, G, V, T = 8, 4, 32000, 0.9
+    qdt = torch.float32 if kind == "materialised" else torch.bfloat16
+    k, tp = (50, 0.9) if kind == "truncated" else (0, 1.0)
+    inp = _ql_case(31, B, G, V, torch.bfloat16, qdt)
+    g = _gpu(inp)
+    ws = sv.alloc_qlogits_workspace(B, G, V, k, device=DEV)
+    for _ in range(2):
+        out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], T, k, tp, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws)) == 0
+        L, Q, d, u = (P.to_np(inp[x]) for x in ("logits", "q_logits", "draft", "uniforms"))
+        P.compare_sample(out, svref.verify_sample_qlogits(L, Q, d, u, T, k, tp), V)
+    names = sv.sv_last_kernels()
+    if kind == "truncated":
+        assert names[0] == "q_truncate_kernel" and names[-1] == "q_clear_kernel", names
+    elif kind == "materialised":
+        assert names[0] == "q_softmax_kernel", names
+    else:
+        assert names == ["stream_dense_kernel", "residual_kernel"], names
+
+
 def test_qlogits_workspace_shared_with_plain_calls(sv):
     """The q scratch sits after the usual layout: a plain call on the same
     workspace afterwards finds its part zero-filled and is exact."""
