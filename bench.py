@@ -118,9 +118,10 @@ def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0, gamma_b=
 
     streaming kernel: every logit once, plus the gathers of l(d_i) and q(d_i);
     final-draw kernel (untruncated sampling): one row of logits per sequence,
-    plus the q row of a rejected sequence (q as the draft's logits: its
-    16-bit logits, counted once; the float32 q the library forms from them is
-    the implementation's own traffic).  With top-k the final draw reads
+    plus the q row of a rejected sequence.  q as the draft's logits: every
+    draft row once more (to form q) and q elements counted at the logits'
+    size; the float32 q the library may form from them is the
+    implementation's own traffic.  With top-k the final draw reads
     only the kept candidates' q values (inside the streaming kernel).
     Deterministic drafts (q one-hot, passed as None) read no q bytes.  A
     ragged round (gamma_b given) needs only rows 0..gamma_b of each sequence."""
@@ -131,6 +132,8 @@ def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0, gamma_b=
     if w.mode == "greedy":
         return {"stream": (gsum + B) * V * s, "final": 0}
     stream = (gsum + B) * V * s + gsum * (qb + s)
+    if w.qlogits:
+        stream += gsum * V * s           # the draft rows, read once to form their q
     if w.top_k > 0 or w.top_p < 1.0:
         return {"stream": stream + B * kept_per_row * qb, "final": 0}
     gb = np.asarray(gamma_b) if gamma_b is not None else np.full(B, G)

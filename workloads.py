@@ -91,6 +91,8 @@ WORKLOADS = {
                  top_k=50, top_p=0.9, draft_sigma=0.7, seed=51),
         Workload("sample_qlogits_b64_g4_v128256_bf16", 64, 4, 128256, "bf16", "sample", 1.0,
                  draft_sigma=0.7, seed=54, qlogits=True),
+        Workload("topk50_topp0.9_qlogits_b256_g8_v152064_bf16", 256, 8, 152064, "bf16", "sample", 0.8,
+                 top_k=50, top_p=0.9, draft_sigma=0.7, seed=55, qlogits=True),
     ]
 }
 
@@ -117,6 +119,12 @@ def _draft_proposal(w: Workload, Lf: torch.Tensor, g: torch.Generator) -> torch.
     dl = w.draft_scale * Lf + w.draft_sigma * torch.randn(B, G, V, generator=g, device=Lf.device)
     z = dl / w.temperature
     del dl
+    return _proposal_of(w, z)
+
+
+def _proposal_of(w: Workload, z: torch.Tensor) -> torch.Tensor:
+    """softmax(z) after w's top-k / top-p (z = draft logits / T), float32 dense."""
+    B, G, V = z.shape
     if w.top_k <= 0 and w.top_p >= 1.0:
         return torch.softmax(z, dim=-1)
     k = V if w.top_k <= 0 else min(w.top_k, V)
@@ -129,7 +137,7 @@ def _draft_proposal(w: Workload, Lf: torch.Tensor, g: torch.Generator) -> torch.
         drop = (cum - pk) >= w.top_p
         pk = pk.masked_fill(drop, 0.0)
         pk = pk / pk.sum(-1, keepdim=True)
-    q = torch.zeros(B, G, V, dtype=torch.float32, device=Lf.device)
+    q = torch.zeros(B, G, V, dtype=torch.float32, device=z.device)
     q.scatter_(-1, idx, pk.float())
     return q
 
@@ -160,7 +168,7 @@ def make_inputs(w: Workload, seed: int | None = None, device="cpu", B: int | Non
         # proposal softmax(q_logits / T) is formed by the library
         ql = (w.draft_scale * Lf + w.draft_sigma * torch.randn(B, G, w.V, generator=g, device=device)).to(w.torch_dtype)
         if G > 0:
-            qp = torch.softmax(ql.float() / w.temperature, dim=-1)
+            qp = _proposal_of(w, ql.float() / w.temperature)   # the draft samples from its actual proposal
             draft = torch.multinomial(qp.view(B * G, w.V), 1, generator=g).view(B, G)
             del qp
         else:
