@@ -128,6 +128,7 @@ def _proposal_of(w: Workload, z: torch.Tensor) -> torch.Tensor:
     if w.top_k <= 0 and w.top_p >= 1.0:
         return torch.softmax(z, dim=-1)
     k = V if w.top_k <= 0 else min(w.top_k, V)
+    dev = z.device
     vals, idx = torch.topk(z, k, dim=-1, sorted=True)
     del z
     pk = torch.softmax(vals.double(), dim=-1)
@@ -137,7 +138,7 @@ def _proposal_of(w: Workload, z: torch.Tensor) -> torch.Tensor:
         drop = (cum - pk) >= w.top_p
         pk = pk.masked_fill(drop, 0.0)
         pk = pk / pk.sum(-1, keepdim=True)
-    q = torch.zeros(B, G, V, dtype=torch.float32, device=z.device)
+    q = torch.zeros(B, G, V, dtype=torch.float32, device=dev)
     q.scatter_(-1, idx, pk.float())
     return q
 
