@@ -215,6 +215,38 @@ __device__ __forceinline__ int qt_block_excl_int(int v, int* sm, int* total) {
   return base + inc - v;
 }
 
+// The k-th largest of the kQsThreads keys (one per thread), by a radix select
+// over 8-bit digits from the top; hist holds 256 ints.
+__device__ __forceinline__ uint32_t qt_kth_largest_key(uint32_t key, int k, int* hist, int* s_digit, int* s_rank) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0u;
+  int rank = k;
+  for (int lo = 24; lo >= 0; lo -= 8) {
+    const uint32_t upper = lo == 24 ? 0u : ~((1u << (lo + 8)) - 1u);
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    if ((key & upper) == prefix) atomicAdd(&hist[(key >> lo) & 255u], 1);
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0, dg = 0;
+      for (int d = 255; d >= 0; --d) {
+        if (run + hist[d] >= rank) {
+          dg = d;
+          break;
+        }
+        run += hist[d];
+      }
+      *s_digit = dg;
+      *s_rank = rank - run;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)*s_digit << lo;
+    rank = *s_rank;
+    __syncthreads();
+  }
+  return prefix;
+}
+
 // Bitonic sort of cand[0, P) (P a power of two, at most kQtCap), largest first.
 __device__ __forceinline__ void qt_sort_desc(unsigned long long* cand, int P) {
   for (int size = 2; size <= P; size <<= 1) {
@@ -281,11 +313,7 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
   // 2a. tau = the k-th largest thread maximum: k distinct elements reach it,
   // so every top-k element does; collect all elements >= tau (usually a few
   // times k) and sort them
-  sm.cand[tid] = (unsigned long long)okey(m_thread);
-  __syncthreads();
-  qt_sort_desc(sm.cand, kQsThreads);
-  const uint32_t tau = (uint32_t)sm.cand[k - 1];
-  __syncthreads();
+  const uint32_t tau = qt_kth_largest_key(okey(m_thread), k, &sm.hist[0][0], &sm.digit, &sm.rank);
   if (tid == 0) sm.count = 0;
   __syncthreads();
   each([&](float x, int v) {
@@ -296,7 +324,7 @@ __global__ void __launch_bounds__(kQsThreads) q_truncate_kernel(const T* __restr
   });
   __syncthreads();
   int N = sm.count;
-  int P = kQsThreads;
+  int P = 2;
   if (N <= kQtCap) {
     while (P < N) P <<= 1;
   } else {
