@@ -1435,15 +1435,15 @@ __device__ __forceinline__ void res_cp16(void* smem, const void* gmem) {
 // at token xq takes it out of the support, q = 0 elsewhere).  Returns the
 // bit mask of run offsets near the row maximum, left to run_top.
 template <typename T, bool USE_Q, bool DET, bool QL = false>
-__device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, bool have_q, int xq, int e0, int NS,
-                                              int V, float M, float c, float c_lo, float s_a, RunAcc* acc,
+__device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, bool have_q, int xq, int e0, int j0,
+                                              int j1, int V, float M, float c, float c_lo, float s_a, RunAcc* acc,
                                               QLrow qlr = QLrow{0.f, 0.f, true}) {
   constexpr int VW = Tr<T>::VW;
   constexpr bool EXACT = sizeof(T) == 2;
   const int tid = threadIdx.x;
   uint32_t top = 0u;
 #pragma unroll 1
-  for (int j = 0; j < NS; ++j) {
+  for (int j = j0; j < j1; ++j) {
     const uint4 v = lg[j * kThreads + tid];
     float qv[VW];
     if (QL) {
@@ -1524,6 +1524,8 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
   const int tid = threadIdx.x;
   uint4* lg = stage;
   uint4* qq = stage + RS::NL * kThreads;
+  // two copy groups: the first half of the run is swept while the second lands
+  const int NH = (NS + 1) >> 1;
   for (int j = 0; j < NS; ++j) {
     const int e = e0 + j * VW;
     const int nv = min(max(V - e, 0), VW);
@@ -1551,21 +1553,23 @@ __device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, 
         }
       }
     }
+    if (j == NH - 1) asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
   // tail tokens in one branch-free sweep (specialised for the residual /
   // bonus rows, for q formed from the draft's logits and for a deterministic
   // draft's one-hot q); tokens near the maximum (bit set in `top`) in a
   // second loop
-  uint32_t top;
-  if (!use_q)
-    top = run_sweep<T, false, false>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
-  else if (qlrow)
-    top = run_sweep<T, true, false, true>(lg, qq, true, -1, e0, NS, V, M, c, c_lo, s_a, acc, qlr);
-  else if (xq < 0)
-    top = run_sweep<T, true, false>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
-  else
-    top = run_sweep<T, true, true>(lg, qq, qrow != nullptr, xq, e0, NS, V, M, c, c_lo, s_a, acc);
+  auto sweep = [&](int j0, int j1) -> uint32_t {
+    if (!use_q) return run_sweep<T, false, false>(lg, qq, qrow != nullptr, xq, e0, j0, j1, V, M, c, c_lo, s_a, acc);
+    if (qlrow) return run_sweep<T, true, false, true>(lg, qq, true, -1, e0, j0, j1, V, M, c, c_lo, s_a, acc, qlr);
+    if (xq < 0) return run_sweep<T, true, false>(lg, qq, qrow != nullptr, xq, e0, j0, j1, V, M, c, c_lo, s_a, acc);
+    return run_sweep<T, true, true>(lg, qq, qrow != nullptr, xq, e0, j0, j1, V, M, c, c_lo, s_a, acc);
+  };
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+  uint32_t top = sweep(0, NH);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  top |= sweep(NH, NS);
   while (top) {
     const int o = __ffs(top) - 1;   // offset in the run
     top &= top - 1;
