@@ -65,6 +65,16 @@ def test_algorithmic_bytes():
     assert bench.algorithmic_bytes(g, np.zeros(512, int)) == {"stream": 512 * 5 * 128256 * 2, "final": 0}
     t = workloads.WORKLOADS["topk50_topp0.9_b256_g8_v152064_bf16"]
     assert bench.algorithmic_bytes(t, np.zeros(256, int))["final"] == 0
+    # q as bf16 draft logits: the draft rows once more, q elements at 2 bytes
+    ql = workloads.WORKLOADS["sample_qlogits_b64_g4_v128256_bf16"]
+    ab = bench.algorithmic_bytes(ql, n)
+    assert ab["stream"] == 64 * 5 * 128256 * 2 + 64 * 4 * (2 + 2) + 64 * 4 * 128256 * 2
+    assert ab["final"] == 54 * 128256 * (2 + 2) + 10 * 128256 * 2
+    # deterministic drafts read no q
+    dt = workloads.WORKLOADS["sample_det_b64_g4_v128256_bf16"]
+    ab = bench.algorithmic_bytes(dt, n)
+    assert ab["stream"] == 64 * 5 * 128256 * 2 + 64 * 4 * 2
+    assert ab["final"] == 64 * 128256 * 2
 
 
 @pytest.mark.parametrize("name", sorted(workloads.WORKLOADS))
