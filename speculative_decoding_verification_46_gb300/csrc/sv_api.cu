@@ -272,7 +272,8 @@ sv_status launch_stream_topk(const sv::Params& p, cudaStream_t stream) {
     cudaGetLastError();
     return SV_ERR_CUDA;
   }
-  const long long R = (long long)p.B * (p.gamma + 1);
+  // target rows, then (q formed from the draft's logits) the draft rows
+  const long long R = (long long)p.B * (p.gamma + 1) + (p.ql ? (long long)p.B * p.gamma : 0);
   // rows of more than kStSTopk ring chunks are claimed at run time (the
   // kernel makes the same test): then one CTA per slot; else equal static shares
   const long long nch = ceil_div((long long)(p.V / (sizeof(T) == 4 ? 4 : 8)), (long long)sv::kStUTopk * sv::kSt);
@@ -437,7 +438,7 @@ sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dty
                              float temperature, int top_k, float top_p, int32_t* out_tokens,
                              int32_t* out_num_accepted, float* out_accept_prob, int32_t* out_status, void* workspace,
                              size_t workspace_bytes, sv_stream_t stream, const void* ql = nullptr,
-                             float4* qpart = nullptr) {
+                             float4* qpart = nullptr, int2* qrowres = nullptr) {
   g_last_kernels = "";
   if (!sizes_ok(B, gamma, V)) return SV_ERR_INVALID_ARG;
   if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
@@ -477,6 +478,7 @@ sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dty
   p.gamma_b = gamma_b;
   p.ql = ql;
   p.qpart = qpart;
+  p.qrowres = qrowres;
   p.out_tokens = out_tokens;
   p.out_n = out_num_accepted;
   p.out_a = out_accept_prob;
@@ -607,6 +609,17 @@ extern "C" sv_status sv_verify_sample_qlogits(int B, int gamma, int V, const voi
                                            reinterpret_cast<float4*>(qbuf));
     return s;
   }
+  // Truncated, fused: the streaming top-k kernel selects the draft rows like
+  // the target rows and keeps their lists (in the q scratch), and the
+  // sequence finisher reads q_i(d_i) and q(v) from them.  Needs the streaming
+  // top-k path (16-byte vectors of one dtype) and room for the lists.
+  const bool fused_topk = gamma > 0 && truncate && q_logits_dtype == logits_dtype &&
+                          V % vec_width(logits_dtype) == 0 && path_override() != 3 &&
+                          (size_t)V * sizeof(float) >= (size_t)(klist + 1) * sizeof(int2);
+  if (fused_topk)
+    return verify_sample_impl(B, gamma, V, logits, logits_dtype, nullptr, draft_tokens, uniforms, nullptr,
+                              temperature, top_k, top_p, out_tokens, out_num_accepted, out_accept_prob, out_status,
+                              workspace, q_off, stream, q_logits, nullptr, reinterpret_cast<int2*>(qbuf));
   if (gamma > 0) {
     const double cd = 1.4426950408889634 / (double)temperature;
     const float c = (float)cd, c_lo = (float)(cd - (double)c);

@@ -92,6 +92,7 @@ struct Params {
   const void* ql;                 // [B][gamma][V] draft logits (same dtype as logits) when q is formed
                                   // from them in the streaming path, else nullptr
   float4* qpart;                  // [B * gamma][H][kWarps] the draft rows' streaming partials (with ql)
+  int2* qrowres;                  // [B * gamma][top_k + 1] the draft rows' kept lists (with ql and top-k / top-p)
 };
 
 // ------------------------------------------------------------------ PTX helpers

@@ -411,7 +411,11 @@ stream_topk_kernel(const Params p) {
   const int tid = threadIdx.x;
   const int G = p.gamma, G1 = G + 1, V = p.V, k = p.top_k;
   RowWalk w;
-  w.R = p.B * G1;
+  // target rows, then (q formed from the draft's logits) the draft rows,
+  // whose kept lists the sequence finisher reads q from
+  w.R = p.B * G1 + (p.ql ? p.B * G : 0);
+  w.Rt = p.B * G1;
+  w.ql = p.ql;
   w.G1 = G1;
   w.NV = V / VW;
   w.NVP = w.NV;
@@ -441,9 +445,12 @@ stream_topk_kernel(const Params p) {
   int stage = 0;
   for (int j = 0; w.live(j); ++j) {
     const int r = w.row_of(j);
-    const int b = r / G1, i = r - b * G1;
+    const bool draft_row = r >= w.Rt;
+    const int rd = r - w.Rt;                                   // draft row index (draft rows)
+    const int b = draft_row ? rd / G : r / G1;
+    const int i = draft_row ? rd - b * G : r - b * G1;
     const int gb = seq_gamma(p, b);
-    const T* row = logits + (size_t)r * V;
+    const T* row = draft_row ? static_cast<const T*>(p.ql) + (size_t)rd * V : logits + (size_t)r * V;
     __syncthreads();   // the previous row's shared state is no longer in use
     int claim = 0;
     if (tid == 0) {
@@ -455,7 +462,7 @@ stream_topk_kernel(const Params p) {
     // loading both here would hold warp 0 for two round trips)
     int d_row = -1;
     float q_row = 0.f;
-    if (tid == 0 && i < gb) d_row = __ldg(p.draft + b * G + i);
+    if (tid == 0 && i < gb && !p.ql) d_row = __ldg(p.draft + b * G + i);   // with ql: a_i in the finisher
     // ---- pass 1 through the ring: per thread its two best 16-byte vectors
     // (by maximum; the first such vector on ties) kept in registers with
     // their maxima m1 >= m2, and m3 = the largest maximum of its other vectors
@@ -617,8 +624,11 @@ stream_topk_kernel(const Params p) {
       }
     }
     __syncthreads();
-    topk_row_epilogue(p, b, i, gb, r, min(k, N), bad_nan != 0, d_row, q_row, sm);
-    if (arrive_last(p.seq_ticket + b, G1, &sm.flag)) topk_finish_sequence(p, b, sm);
+    topk_row_epilogue(p, b, i, gb,
+                      draft_row ? p.qrowres + (size_t)rd * (k + 1) : p.rowres + (size_t)r * (k + 1),
+                      min(k, N), bad_nan != 0, d_row, q_row, sm, draft_row);
+    // the sequence is done when its target rows (and draft rows) all are
+    if (arrive_last(p.seq_ticket + b, G1 + (p.ql ? G : 0), &sm.flag)) topk_finish_sequence(p, b, sm);
   }
   cpa_wait<0>();
   // every claim of this CTA has returned; the last CTA out resets the counter

@@ -53,8 +53,23 @@ __device__ __forceinline__ int block_sum_int_n(int v, int* sm) {
   return t;
 }
 
+// The probability a kept list ([0].x = J, then J (index, probability bits))
+// gives token v: 0 if v is not kept.
+__device__ __forceinline__ float kept_prob(const int2* list, int v) {
+  const int J = __ldcg(list).x;
+  float pv = 0.f;
+  for (int e = 0; e < J; ++e) {
+    const int2 en = __ldcg(list + 1 + e);
+    if (en.x == v) pv = __int_as_float(en.y);
+  }
+  return pv;
+}
+
 // Final step of a sequence (run by the CTA that finished its last row): the
 // acceptance scan, then the draw over the kept list of row n in token order.
+// With q formed from the draft's logits (p.ql), q_i is draft row i's kept
+// list: the acceptance tests are formed here, and q(v) of the final draw is
+// looked up in draft row n's list.
 __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int k = p.top_k, G = p.gamma, G1 = G + 1, V = p.V;
@@ -63,6 +78,29 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   if (tid < G) sm.fa[tid] = (float)__ldcg(p.acc + b * G + tid);
   if (tid == 0) sm.status = __ldcg(&p.seq[b].status);
   __syncthreads();
+  if (p.ql) {
+    if (tid < gb) {
+      const int d = __ldg(p.draft + b * G + tid);
+      float a = 0.f;
+      int bits = 0;
+      if (d < 0 || d >= V) {
+        bits |= SEQ_OOB;
+      } else {
+        const float pd = kept_prob(p.rowres + (size_t)(b * G1 + tid) * (k + 1), d);
+        const float qd = kept_prob(p.qrowres + (size_t)(b * G + tid) * (k + 1), d);
+        if (qd > 0.f) {
+          a = fminf(1.f, pd / qd);
+        } else {
+          a = pd > 0.f ? 1.f : 0.f;
+          bits |= SEQ_QBAD;
+        }
+      }
+      sm.fa[tid] = a;
+      if (p.out_a) p.out_a[b * G + tid] = a;
+      if (bits) atomicOr(&sm.status, bits);
+    }
+    __syncthreads();
+  }
   if (tid == 0) {
     int n = gb;
     for (int i = 0; i < gb; ++i)
@@ -75,7 +113,9 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
   const int J = __ldcg(kept).x;
   const bool resid = n < gb;
   const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
-  const int dn = (resid && !p.q) ? __ldg(p.draft + b * G + n) : -1;   // deterministic draft: q_n one-hot
+  const int2* qlist = (resid && p.ql) ? p.qrowres + (size_t)(b * G + n) * (k + 1) : nullptr;
+  // deterministic draft: q_n one-hot
+  const int dn = (resid && !p.q && !p.ql) ? __ldg(p.draft + b * G + n) : -1;
   for (int e = tid; e < J; e += nt) {
     const int2 en = __ldcg(kept + 1 + e);
     sm.widx[e] = en.x;
@@ -89,7 +129,7 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
     int rank = 0;
     for (int j = 0; j < J; ++j) rank += sm.widx[j] < me;
     const float pe = sm.w[e];
-    const float qm = qrow ? __ldg(qrow + me) : (me == dn ? 1.f : 0.f);
+    const float qm = qlist ? kept_prob(qlist, me) : qrow ? __ldg(qrow + me) : (me == dn ? 1.f : 0.f);
     const float r = resid ? fmaxf(__fsub_rn(pe, qm), 0.f) : pe;
     sm.sidx[rank] = me;
     rs[rank] = F2{r, 0.f};
@@ -125,6 +165,8 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
     for (int j = gb + tid; j < G; j += nt) p.out_a[b * G + j] = 0.f;   // beyond this sequence's drafts
   // the kept lists and acceptance probabilities have been consumed: zero them
   for (int e = tid; e < G1 * (k + 1); e += nt) p.rowres[(size_t)b * G1 * (k + 1) + e] = make_int2(0, 0);
+  if (p.ql)
+    for (int e = tid; e < G * (k + 1); e += nt) p.qrowres[(size_t)b * G * (k + 1) + e] = make_int2(0, 0);
   for (int e = tid; e < G; e += nt) p.acc[b * G + e] = 0.0;
 }
 
@@ -133,10 +175,15 @@ __device__ void topk_finish_sequence(const Params& p, int b, TopkSmem& sm) {
 // two-float sums, the kept
 // (index, probability) list written to rowres[r], and the acceptance
 // probability of the row's draft (d_row, q_row prefetched by thread 0).
-__device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int r, int kk, bool bad_nan, int d_row,
-                                  float q_row, TopkSmem& sm) {
+// out: where the kept list goes (rowres for a target row; for a draft row,
+// with q formed from the draft's logits, its own list, which q is read from).
+// A draft row with no distribution keeps nothing (q = 0); a draft row tests
+// no draft, and with q from the draft's logits the acceptance tests move to
+// the sequence finisher (q_i(d_i) comes from draft row i's list).
+__device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int2* out, int kk, bool bad_nan, int d_row,
+                                  float q_row, TopkSmem& sm, bool draft_row = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
-  const int G = p.gamma, V = p.V, k = p.top_k;
+  const int G = p.gamma, V = p.V;
     // ---- softmax(./T) over the top-k, then the top-p cut (two-float sums)
     const float m0 = kk > 0 ? sm.w[0] : -INFINITY;
     const bool bad = bad_nan || !(m0 > -INFINITY && m0 < INFINITY);
@@ -151,9 +198,9 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int r, 
       int J = kk;
       F2 WJ = W;
       if (bad || kk == 0) {
-        J = kk > 0 ? 1 : 0;
+        J = (kk > 0 && !draft_row) ? 1 : 0;
         WJ = F2{1.f, 0.f};
-        if (lane == 0 && kk > 0) sm.w[0] = 1.f;
+        if (lane == 0 && J > 0) sm.w[0] = 1.f;
       } else if (p.top_p < 1.0f) {
         const F2 target = f2_scale(W, p.top_p);   // cumulative mass / W >= top_p
         F2 carry{0.f, 0.f};
@@ -174,17 +221,16 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int r, 
       if (lane == 0) {
         sm.J = J;
         sm.WJ = WJ.hi + WJ.lo;
-        if (bad && i <= gb) atomicOr(&p.seq[b].status, SEQ_BADROW);
+        if (bad && i <= gb && !draft_row) atomicOr(&p.seq[b].status, SEQ_BADROW);
       }
     }
     __syncthreads();
     const int J = sm.J;
     const float WJ = sm.WJ;
-    int2* out = p.rowres + (size_t)r * (k + 1);
     if (tid == 0) out[0] = make_int2(J, 0);
     for (int e = tid; e < J; e += nt) out[1 + e] = make_int2(sm.widx[e], __float_as_int(sm.w[e] / WJ));
     // ---- acceptance probability of this row's draft
-    if (i < gb) {
+    if (i < gb && !draft_row && !p.ql) {
       if (tid == 0) {
         sm.pd = 0.f;
         sm.token = d_row;

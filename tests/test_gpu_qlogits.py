@@ -114,7 +114,7 @@ def test_qlogits_mixed_dtypes_materialise_q(sv):
 
 
 @pytest.mark.parametrize("tk_path", ["auto", "slices"])
-@pytest.mark.parametrize("ldt", ["bf16", "f32"])
+@pytest.mark.parametrize("ldt", ["bf16", "f32", "bf16/f32"])
 @pytest.mark.parametrize("V,G,B,k,tp,T", [(1000, 4, 12, 50, 1.0, 0.8), (1000, 4, 12, 50, 0.9, 0.8),
                                           (40000, 3, 6, 50, 0.9, 1.0), (700, 2, 10, 0, 0.9, 1.2),
                                           (5000, 4, 8, 1, 1.0, 1.0), (33, 3, 20, 40, 0.95, 0.7)])
@@ -124,7 +124,8 @@ def test_qlogits_truncated(sv, monkeypatch, tk_path, ldt, V, G, B, k, tp, T):
         monkeypatch.setenv("SPECVERIFY_PATH", "slices")
     else:
         monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
-    inp = _ql_case(6000 + V + k, B, G, V, DTYPES[ldt], DTYPES[ldt], spread=1.0, noise=0.5)
+    l_dt, q_dt = (ldt.split("/") * 2)[:2]   # "bf16/f32": target bf16, draft logits f32 (q materialised)
+    inp = _ql_case(6000 + V + k, B, G, V, DTYPES[l_dt], DTYPES[q_dt], spread=1.0, noise=0.5)
     g = _gpu(inp)
     out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], T, k, tp)
     L, Q, d, u = (P.to_np(inp[x]) for x in ("logits", "q_logits", "draft", "uniforms"))
@@ -138,13 +139,13 @@ def test_qlogits_truncation_limits(sv):
     assert e.value.status == sv.SV_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("kind", ["fused", "materialised", "truncated"])
+@pytest.mark.parametrize("kind", ["fused", "materialised", "truncated", "truncated_materialised"])
 def test_qlogits_leaves_workspace_zero_filled(sv, kind):
     """Every path leaves the whole workspace (layout, q scratch, kept lists)
     zero-filled, as the contract says."""
     B, G, V, T = 8, 4, 32000, 0.9
-    qdt = torch.float32 if kind == "materialised" else torch.bfloat16
-    k, tp = (50, 0.9) if kind == "truncated" else (0, 1.0)
+    qdt = torch.float32 if kind in ("materialised", "truncated_materialised") else torch.bfloat16
+    k, tp = (50, 0.9) if kind.startswith("truncated") else (0, 1.0)
     inp = _ql_case(31, B, G, V, torch.bfloat16, qdt)
     g = _gpu(inp)
     ws = sv.alloc_qlogits_workspace(B, G, V, k, device=DEV)
@@ -155,7 +156,9 @@ def test_qlogits_leaves_workspace_zero_filled(sv, kind):
         L, Q, d, u = (P.to_np(inp[x]) for x in ("logits", "q_logits", "draft", "uniforms"))
         P.compare_sample(out, svref.verify_sample_qlogits(L, Q, d, u, T, k, tp), V)
     names = sv.sv_last_kernels()
-    if kind == "truncated":
+    if kind == "truncated":       # one dtype: the draft rows go through the streaming top-k kernel
+        assert names == ["stream_topk_kernel"], names
+    elif kind == "truncated_materialised":
         assert names[0] == "q_truncate_kernel" and names[-1] == "q_clear_kernel", names
     elif kind == "materialised":
         assert names[0] == "q_softmax_kernel", names
