@@ -222,12 +222,17 @@ sv_status sv_verify_greedy_ragged(int B, int gamma, int V,
  *
  *   q_logits        [B][gamma][V] of q_logits_dtype (float32, bfloat16 or
  *                   float16), 16-byte aligned: the draft's logits at the
- *                   drafted positions; may be NULL when gamma = 0.  The
- *                   library forms q_i = softmax(q_logits_i / temperature) in
- *                   float32 in the workspace (its own kernel, one CTA per
- *                   draft row) and runs the sv_verify_sample path on it.  A
- *                   row holding NaN or +inf, or only -inf, gives q_i = 0, so
- *                   testing position i raises SV_SEQ_Q_NOT_POSITIVE.
+ *                   drafted positions; may be NULL when gamma = 0.  q_i =
+ *                   softmax(q_logits_i / temperature), truncated as below.
+ *                   When q_logits has the logits' dtype and V is a multiple
+ *                   of the 16-byte vector width (8 for 16-bit types, 4 for
+ *                   float32), the verify kernels stream the draft rows with
+ *                   the target rows and form q where they need it (it is
+ *                   never written out); otherwise a kernel first writes q in
+ *                   float32 into the workspace and the sv_verify_sample
+ *                   path runs on it.  A row holding NaN or +inf, or only
+ *                   -inf, gives q_i = 0, so testing position i raises
+ *                   SV_SEQ_Q_NOT_POSITIVE.
  *   top_k, top_p    as in sv_verify_sample, applied to q_i too: q_i is the
  *                   draft's softmax renormalised over its own top-k then
  *                   top-p set (one CTA per draft row: radix select of the
