@@ -74,7 +74,10 @@ def test_qlogits_small(sv, path, ldt, qdt, V, G, B, T):
     P.compare_sample(out, _oracle(inp, T), V)
 
 
-def test_qlogits_bad_draft_rows(sv, path):
+@pytest.mark.parametrize("k,tp", [(0, 1.0), (50, 1.0), (50, 0.9)])
+def test_qlogits_bad_draft_rows(sv, path, k, tp):
+    """Draft rows with NaN, +inf or only -inf give q = 0 (the q(d) <= 0 bit
+    where tested), untruncated and truncated."""
     B, G, V = 6, 3, 1000
     inp = _ql_case(77, B, G, V, torch.bfloat16, torch.bfloat16)
     Q = inp["q_logits"]
@@ -83,8 +86,9 @@ def test_qlogits_bad_draft_rows(sv, path):
     Q[2, 0, 9] = float("inf")
     Q[3, 1, :] = -float("inf")            # tested only if position 0 is accepted
     g = _gpu(inp)
-    out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], 1.0)
-    ref = _oracle(inp, 1.0)
+    out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], 1.0, k, tp)
+    L, Qn, d, u = (P.to_np(inp[x]) for x in ("logits", "q_logits", "draft", "uniforms"))
+    ref = svref.verify_sample_qlogits(L, Qn, d, u, 1.0, k, tp)
     assert np.all(ref["status"][:3] & svref.SEQ_Q_NOT_POSITIVE)
     P.compare_sample(out, ref, V)
 
