@@ -44,14 +44,21 @@ in the repository's design notes):
   residual mass 0 after a rejection: sample from p_n, with a status bit;
   a row holding NaN or +inf, or only -inf: status bit, outputs undefined
   (but in range);
-* greedy argmax ties go to the lowest index.
+* greedy argmax ties go to the lowest index;
+* q supplied as the draft's logits: q_i is the draft row transformed exactly
+  as p_i (temperature, then top-k / top-p); a row with no distribution gives
+  q_i = 0; a final draw within QLOGITS_CDF_BAND of a CDF step is a boundary
+  draw (the step forms q in float32).
 
 Parity pins (tests/test_oracle_*.py): the worked example of [Ch11.1] §11.1.3,
 the exact output law of the §11.1.3 proof by brute-force enumeration on tiny
 inputs, chi-square tests of distribution preservation, the E[N] closed form of
 [SD-notes] and its worked numbers in the lmnt.cn blog §2.3 by Monte Carlo,
 gamma = 0 against a library inverse CDF of scipy's softmax, greedy against
-numpy.argmax, and brute-force properties of top-k / top-p.
+numpy.argmax, brute-force properties of top-k / top-p, the closed forms of a
+one-hot q and of ragged rounds, and for q from draft logits: constant rows
+(uniforms), shift invariance, scipy's softmax fed to the plain step, and q = p
+accepting every draft.
 """
 
 from __future__ import annotations
