@@ -10,10 +10,11 @@
 // finished.  The ring is private to the thread that filled it (the thread
 // copies and later reads its own slots), so completion is tracked per thread
 // with cp.async.wait_group: there are no cross-thread waits, no mbarriers and
-// no spin loops.  Rows are dealt to CTAs round-robin; counts are balanced on
-// the host so that every CTA gets the same number of rows.  With fewer rows
-// than CTA slots, each row is split into H parts (H = 2 or 4) so that no SM
-// streams a whole row more than the others.
+// no spin loops.  The dense kernel splits rows into H parts (2, or 4 for
+// small batches) dealt round-robin to one CTA per slot; the top-k kernel
+// claims whole rows from a counter as its CTAs get through them.  With q
+// formed from the draft's logits, the draft rows follow the target rows
+// through both kernels.
 //
 //   greedy   per-warp argmax of each row part (ties -> lowest index; NaN
 //            flagged); stream_greedy_finish_kernel merges the parts, scans
@@ -25,8 +26,10 @@
 //            k-th largest is a lower bound tau of the row's k-th value; only
 //            threads with a third vector reaching tau are re-read (L2);
 //            exact rank selection of the candidates >= tau; softmax(./T) +
-//            top-p; a_i.  The last row of a sequence to finish (atomic
-//            ticket, no waiting) runs the acceptance scan and the final draw.
+//            top-p; a_i (with q from draft logits, in the finisher, from the
+//            two rows' kept lists).  The last row of a sequence to finish
+//            (atomic ticket, no waiting) runs the acceptance scan and the
+//            final draw.
 //
 // The dense kernel ends a row part with warp shuffles and one store per warp:
 // no block barrier, so no warp waits for another between rows.
