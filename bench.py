@@ -4,17 +4,26 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 A step is one verify call (every kernel of the path) over one batch of
-synthetic input.  Default workload: B=1, gamma=5, V=32000 bfloat16 logits,
-T=0.7 (the single-sequence verify); --workload picks another entry of
+synthetic input.  Default workload: the largest single-GPU one, B=256
+sequences, gamma=8 drafts, V=152064 bfloat16 logits, T=0.8, top-k 50 then
+top-p 0.9 applied to p and q; --workload picks another entry of
 workloads.WORKLOADS.  Inputs are resident in HBM before timing; each step uses
 its own input set and the sets together exceed twice the 129 MB L2, so no
-step starts with its inputs in L2.  The timed region replays a CUDA graph of
-calls (one call per input set) on one stream, bracketed by CUDA events and a
-synchronize; ms_per_step = elapsed / steps.
+step starts with its inputs in L2.  The timed region replays CUDA graphs of
+calls (one call per input set; a graph of n_sets calls replayed, plus one
+graph of the remaining calls when K is not a multiple of n_sets) on one
+stream, bracketed by CUDA events and a synchronize; ms_per_step = elapsed / K.
 
 Printed as one JSON line (rank 0).  Under torchrun each rank runs an
 independent replica on its own GPU (the path has no exchange step), the time
 is the max over ranks and value = all ranks' positions / that time.
+
+Besides the contract's keys the line carries: `roofline` for the step's
+dominant kernel, `kernel_us` per kernel, `parity` (the GPU's outputs against
+the CPU oracle on the cpu_baseline sample: draws, mismatches, boundary
+draws), `acceptance` (empirical alpha and tokens per round against the
+prediction from the same acceptance probabilities), and `other_workloads`
+(the same measurements, shorter, for every other workload).
 """
 
 from __future__ import annotations
@@ -42,6 +51,7 @@ METRIC = "verify positions/sec (B*(gamma+1)) and achieved HBM GB/s as % of GB300
 UNIT = "positions/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+BOUNDARY_LIMIT = 1e-4      # boundary mismatches allowed, as a fraction of all draws
 
 
 def _args():
@@ -113,7 +123,7 @@ def _workspace(sv, w, B, G, V, dev):
     return sv.alloc_workspace(B, G, V, w.top_k if w.mode == "sample" else 0, dev)
 
 
-def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0, gamma_b=None):
+def algorithmic_bytes(w, n_accepted: np.ndarray, kept_rejected: int = 0, gamma_b=None):
     """Bytes the method must move for one step, split by kernel.
 
     streaming kernel: every logit once, plus the gathers of l(d_i) and q(d_i);
@@ -121,10 +131,12 @@ def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0, gamma_b=
     plus the q row of a rejected sequence.  q as the draft's logits: every
     draft row once more (to form q) and q elements counted at the logits'
     size; the float32 q the library may form from them is the
-    implementation's own traffic.  With top-k the final draw reads
-    only the kept candidates' q values (inside the streaming kernel).
-    Deterministic drafts (q one-hot, passed as None) read no q bytes.  A
-    ragged round (gamma_b given) needs only rows 0..gamma_b of each sequence."""
+    implementation's own traffic.  With top-k / top-p the final draw of a
+    rejected sequence reads q only at the kept candidates of row n:
+    kept_rejected is their total over the batch (read inside the streaming
+    kernel's sequence finisher).  Deterministic drafts (q one-hot, passed as
+    None) read no q bytes.  A ragged round (gamma_b given) needs only rows
+    0..gamma_b of each sequence."""
     s = _elt_bytes(w)
     B, G, V = len(n_accepted), w.gamma, w.V
     qb = _q_elt_bytes(w)
@@ -135,11 +147,26 @@ def algorithmic_bytes(w, n_accepted: np.ndarray, kept_per_row: int = 0, gamma_b=
     if w.qlogits:
         stream += gsum * V * s           # the draft rows, read once to form their q
     if w.top_k > 0 or w.top_p < 1.0:
-        return {"stream": stream + B * kept_per_row * qb, "final": 0}
+        return {"stream": stream + int(kept_rejected) * qb, "final": 0}
     gb = np.asarray(gamma_b) if gamma_b is not None else np.full(B, G)
     rejected = int((n_accepted < gb).sum())
     final = rejected * V * (qb + s) + (B - rejected) * V * s
     return {"stream": stream, "final": final}
+
+
+def kept_counts(logits_rows: torch.Tensor, temperature: float, top_k: int, top_p: float) -> torch.Tensor:
+    """Number of tokens top-k then top-p keeps in each row (torch, on the
+    rows' device): bench-side accounting of the kept candidates whose q the
+    final draw reads; not part of the verify path."""
+    z = logits_rows.float() / temperature
+    V = z.shape[-1]
+    k = V if top_k <= 0 else min(top_k, V)
+    vals = torch.topk(z, k, dim=-1, sorted=True).values.double()
+    pk = torch.softmax(vals, dim=-1)
+    if top_p >= 1.0:
+        return torch.full(z.shape[:-1], k, dtype=torch.int64, device=z.device)
+    before = pk.cumsum(-1) - pk
+    return (before < top_p).sum(-1)
 
 
 class Clocks:
@@ -220,11 +247,11 @@ def _traffic(workload: str, kernel: str):
     return None
 
 
-def _input_sets(w, n_sets: int, device):
+def _input_sets(w, n_sets: int, device, seed_offset: int = 1000):
     """n_sets independent input batches, generated as one batch of
     n_sets * B sequences and sliced (each slice is contiguous)."""
-    big = workloads.make_inputs(w, seed=w.seed + 1000 * int(os.environ.get("RANK", "0")), device=device,
-                                B=n_sets * w.B)
+    big = workloads.make_inputs(w, seed=w.seed + seed_offset * (1 + int(os.environ.get("RANK", "0"))),
+                                device=device, B=n_sets * w.B)
     sets = []
     for i in range(n_sets):
         sl = slice(i * w.B, (i + 1) * w.B)
@@ -271,6 +298,172 @@ def _call(sv, w, inp, out, ws, stream):
     return r
 
 
+class Runner:
+    """Input sets, outputs, workspace and CUDA graphs of one workload."""
+
+    def __init__(self, sv, w, dev, max_sets: int = 1024):
+        self.sv, self.w, self.dev = sv, w, dev
+        B, G, V = w.B, w.gamma, w.V
+        self.per_set = B * (G + 1) * V * _elt_bytes(w) + B * G * V * _q_elt_bytes(w)
+        self.n_sets = max(2, min(max_sets, math.ceil(2 * L2_BYTES / self.per_set) + 1))
+        self.sets = _input_sets(w, self.n_sets, dev)
+        self.outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev),
+                      torch.empty(B, dtype=torch.int32, device=dev),
+                      torch.empty(B, G, dtype=torch.float32, device=dev) if w.mode == "sample" and G > 0 else None,
+                      torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(self.n_sets)]
+        self.ws = _workspace(sv, w, B, G, V, dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.graphs = {}
+
+    def call(self, i):
+        return _call(self.sv, self.w, self.sets[i], self.outs[i], self.ws, self.stream)
+
+    def eager(self, count):
+        with torch.cuda.stream(self.stream):
+            for i in range(count):
+                self.call(i % self.n_sets)
+
+    def graph(self, count):
+        """A CUDA graph of `count` calls on input sets 0..count-1 (captured once)."""
+        if count not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(count):
+                    self.call(i)
+            torch.cuda.synchronize()
+            self.graphs[count] = g
+        return self.graphs[count]
+
+    def prepare(self, k):
+        """Capture the graphs that run_steps(k) replays (outside any timing)."""
+        full, rem = divmod(k, self.n_sets)
+        if full:
+            self.graph(self.n_sets)
+        if rem:
+            self.graph(rem)
+
+    def run_steps(self, k):
+        """k calls, every one replayed from a CUDA graph."""
+        full, rem = divmod(k, self.n_sets)
+        with torch.cuda.stream(self.stream):
+            for _ in range(full):
+                self.graph(self.n_sets).replay()
+            if rem:
+                self.graph(rem).replay()
+
+    def kernel_times(self, n_batch: int, batch: int):
+        """Mean device time of the call's kernels, from CUDA events the
+        library records before its first kernel, after the kernel that streams
+        the logits, and after its last kernel.  A fixed-length sleep kernel
+        first keeps the GPU busy while the host queues a batch of calls, so
+        that the gaps between events are device time, not host submission."""
+        sv = self.sv
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_batch * batch)]
+        with torch.cuda.stream(self.stream):
+            for trio in evs:
+                for e in trio:
+                    e.record(self.stream)          # torch creates the CUDA event on first record
+            j = 0
+            for _ in range(n_batch):
+                torch.cuda._sleep(40_000_000)  # ~20 ms at 2 GHz
+                for _ in range(batch):
+                    if sv.sv_set_timing_events(evs[j]) != sv.SV_OK:
+                        raise RuntimeError("sv_set_timing_events failed")
+                    self.call(j % self.n_sets)
+                    j += 1
+            sv.sv_set_timing_events(None)
+        torch.cuda.synchronize()
+        t_stream = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) * 1e-3
+        t_final = float(np.mean([e[1].elapsed_time(e[2]) for e in evs])) * 1e-3
+        return t_stream, t_final
+
+    def kernels(self):
+        """(all kernels of one call, the ones between the timing events)."""
+        with torch.cuda.stream(self.stream):
+            self.call(0)
+        torch.cuda.synchronize()
+        allk = self.sv.sv_last_kernels()
+        # the kernels that form q from draft logits (and clear it) run outside
+        # the timing hook's events
+        timed = [k for k in allk if k not in ("q_softmax_kernel", "q_truncate_kernel", "q_clear_kernel")]
+        return allk, timed
+
+    def accounting(self):
+        """Algorithmic bytes per step (mean over the input sets, after the
+        last calls on every set), positions per step, and the acceptance
+        statistics of the outputs."""
+        w = self.w
+        nacc = np.concatenate([o[1].cpu().numpy() for o in self.outs])
+        gbs = np.concatenate([st["gamma_b"].cpu().numpy() for st in self.sets]) if w.ragged else None
+        kept = 0
+        if w.mode == "sample" and (w.top_k > 0 or w.top_p < 1.0) and _q_elt_bytes(w) > 0:
+            for st, o in zip(self.sets, self.outs):
+                n = o[1].long()
+                rej = n < w.gamma
+                if rej.any():
+                    rows = st["logits"][torch.nonzero(rej).flatten(), n[rej]]
+                    kept += int(kept_counts(rows, w.temperature, w.top_k, w.top_p).sum().item())
+        ab = algorithmic_bytes(w, nacc, kept_rejected=kept, gamma_b=gbs)
+        ab = {k: v / self.n_sets for k, v in ab.items()}
+        ab["kept_q_reads_per_step"] = kept / self.n_sets
+        if w.ragged:
+            positions = float(np.sum(gbs)) / self.n_sets + w.B
+        else:
+            positions = float(w.B * (w.gamma + 1))
+        return ab, positions, acceptance_stats(w, self.outs, self.sets)
+
+
+def acceptance_stats(w, outs, sets):
+    """Empirical alpha (the mean acceptance probability a_i over the tested
+    positions: E[min(1, p/q)] under d ~ q is sum_v min(p, q), the overlap the
+    notes call alpha) and tokens per round, mean n + 1 against
+    1 + sum_{k=1..gamma_b} prod_{i<k} a_i (an unbiased estimate of the
+    expected count when the rows' acceptances are independent).  Greedy
+    reports the tokens per round only."""
+    n = np.concatenate([o[1].cpu().numpy() for o in outs]).astype(np.float64)
+    res = {"tokens_per_round": {"empirical": float(np.mean(n + 1))}}
+    if w.mode != "sample" or w.gamma == 0 or outs[0][2] is None:
+        return res
+    a = np.concatenate([o[2].cpu().numpy() for o in outs]).astype(np.float64)
+    G = w.gamma
+    gb = (np.concatenate([st["gamma_b"].cpu().numpy() for st in sets]) if w.ragged
+          else np.full(len(n), G))
+    mask = np.arange(G)[None, :] < gb[:, None]
+    prod = np.cumprod(np.where(mask, a, 0.0), axis=1)          # prod_{i<=j} a_i
+    pred = 1.0 + prod.sum(1)
+    res["alpha"] = float(a[mask].mean())
+    res["tokens_per_round"]["predicted"] = float(pred.mean())
+    res["tokens_per_round"]["std_err"] = float(np.std(n + 1, ddof=1) / np.sqrt(len(n))) if len(n) > 1 else None
+    res["sequences"] = int(len(n))
+    return res
+
+
+def roofline_block(w, ab, t_stream, t_final, kernel_names, peak, peak_kind):
+    """The dominant kernel (the longer of the two timed intervals), its
+    algorithmic bytes per launch, average launch time and the fraction of
+    the measured copy bandwidth."""
+    if len(kernel_names) == 1:
+        # one kernel does the whole step (its final draw included)
+        ab = dict(ab, stream=ab["stream"] + ab["final"], final=0.0)
+        t_final = 0.0
+    kern = "stream" if t_stream >= t_final else "final"
+    kname = kernel_names[0] if kern == "stream" else kernel_names[1]
+    t_k = t_stream if kern == "stream" else t_final
+    achieved = ab[kern] / t_k / 1e9
+    return {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": _traffic(w.name, kname),
+            "algorithmic_bytes_per_launch": ab[kern], "avg_launch_us": t_k * 1e6,
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+
+
+def _kernel_us(kernel_names, t_stream, t_final):
+    d = {kernel_names[0]: t_stream * 1e6}
+    if len(kernel_names) == 2:
+        d[kernel_names[1]] = t_final * 1e6
+    return d
+
+
 def run_gb300(args, rank, ws_n, local):
     import speculative_decoding_verification_46_gb300 as sv
 
@@ -281,58 +474,25 @@ def run_gb300(args, rank, ws_n, local):
     if args.batch is not None:
         w = w.with_(B=args.batch, name=f"{w.name}@B={args.batch}")
     B, G, V = w.B, w.gamma, w.V
-    positions = B * (G + 1)
+    rn = Runner(sv, w, dev)
+    stream = rn.stream
 
-    per_set = B * (G + 1) * V * _elt_bytes(w) + B * G * V * _q_elt_bytes(w)
-    n_sets = max(2, min(1024, math.ceil(2 * L2_BYTES / per_set) + 1))
-    sets = _input_sets(w, n_sets, dev)
-    outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
-             torch.empty(B, G, dtype=torch.float32, device=dev) if w.mode == "sample" and G > 0 else None,
-             torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
-    top_k_ws = w.top_k if w.mode == "sample" else 0
-    wsp = _workspace(sv, w, B, G, V, dev)
-    stream = torch.cuda.Stream(device=dev)
-
-    # default steps: about a second of timed work
-    with torch.cuda.stream(stream):
-        for i in range(n_sets):
-            _call(sv, w, sets[i], outs[i], wsp, stream)
-    torch.cuda.synchronize()
-    all_kernels = sv.sv_last_kernels()       # what one call launches (the path the library chose)
+    all_kernels, kernel_names = rn.kernels()   # what one call launches (the path the library chose)
     kernels_per_call = len(all_kernels) + (1 if w.ragged else 0)   # + the truncation kernel
-    # the timing hook brackets the verify kernels; the kernels that form q
-    # from draft logits (and clear it) run outside it and are timed with the
-    # step only
-    kernel_names = [k for k in all_kernels if k not in ("q_softmax_kernel", "q_truncate_kernel", "q_clear_kernel")]
     if kernels_per_call == 0:
         raise RuntimeError("the verify call launched no kernel")
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(n_sets):
-            _call(sv, w, sets[i], outs[i], wsp, stream)
+    rn.eager(rn.n_sets)
     torch.cuda.synchronize()
-    est = (time.perf_counter() - t0) / n_sets
+    t0 = time.perf_counter()
+    rn.eager(rn.n_sets)
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / rn.n_sets
     steps = args.steps if args.steps is not None else int(min(200_000, max(200, 1.0 / max(est, 1e-6))))
     warmup = args.warmup if args.warmup is not None else max(3, min(steps // 10, 1000))
 
-    # a CUDA graph of n_sets calls (call i on input set i), replayed
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(n_sets):
-            _call(sv, w, sets[i], outs[i], wsp, stream)
-    torch.cuda.synchronize()
-
-    def run_steps(k):
-        full, rem = divmod(k, n_sets)
-        for _ in range(full):
-            graph.replay()
-        if rem:
-            with torch.cuda.stream(stream):
-                for i in range(rem):
-                    _call(sv, w, sets[i], outs[i], wsp, stream)
-
-    with torch.cuda.stream(stream):
-        run_steps(warmup)
+    rn.prepare(warmup)
+    rn.prepare(steps)
+    rn.run_steps(warmup)
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
@@ -341,91 +501,57 @@ def run_gb300(args, rank, ws_n, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        run_steps(steps)
+        rn.run_steps(steps)
         e1.record(stream)
     torch.cuda.synchronize()
     _barrier(ws_n)
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / steps
     ms_max = max_over_ranks(ms, ws_n, dev)
+
+    # per-kernel durations (timing hook), bytes, acceptance statistics
+    t_stream, t_final = rn.kernel_times(4, 100)
+    ab, positions, acc = rn.accounting()
     value = positions * ws_n / (ms_max / 1e3)
-
-    # per-kernel durations: events recorded before, between and after the
-    # kernels of each call.  A fixed-length sleep kernel first keeps the GPU
-    # busy while the host queues a batch of calls, so that the gaps between
-    # events are device time, not host submission time.
-    n_batch, batch = 4, 100
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_batch * batch)]
-    with torch.cuda.stream(stream):
-        for trio in evs:
-            for e in trio:
-                e.record(stream)          # torch creates the CUDA event on first record
-        j = 0
-        for _ in range(n_batch):
-            torch.cuda._sleep(40_000_000)  # ~20 ms at 2 GHz
-            for _ in range(batch):
-                if sv.sv_set_timing_events(evs[j]) != sv.SV_OK:
-                    raise RuntimeError("sv_set_timing_events failed")
-                _call(sv, w, sets[j % n_sets], outs[j % n_sets], wsp, stream)
-                j += 1
-        sv.sv_set_timing_events(None)
-    torch.cuda.synchronize()
-    t_stream = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) * 1e-3
-    t_final = float(np.mean([e[1].elapsed_time(e[2]) for e in evs])) * 1e-3 if len(kernel_names) == 2 else 0.0
-    kernel_us = {kernel_names[0]: t_stream * 1e6}
-    if len(kernel_names) == 2:
-        kernel_us[kernel_names[1]] = t_final * 1e6
-
-    # algorithmic bytes: average over the input sets (the final draw depends on the data)
-    nacc = np.concatenate([o[1].cpu().numpy() for o in outs])
-    gbs = np.concatenate([st["gamma_b"].cpu().numpy() for st in sets]) if w.ragged else None
-    ab = algorithmic_bytes(w, nacc, gamma_b=gbs)
-    if w.ragged:
-        # a ragged round verifies sum_b (gamma_b + 1) positions (mean over the input sets)
-        positions = float(np.sum(gbs)) / n_sets + B
-        value = positions * ws_n / (ms_max / 1e3)
-    ab = {k: v / n_sets for k, v in ab.items()}
-    if len(kernel_names) == 1:
-        # one kernel does the whole step (its final draw included)
-        ab = {"stream": ab["stream"] + ab["final"], "final": 0.0}
     peak, peak_kind = _peaks()
-    kern = "stream" if t_stream >= t_final else "final"
-    kname = kernel_names[0] if kern == "stream" else kernel_names[1]
-    t_k = t_stream if kern == "stream" else t_final
-    achieved = ab[kern] / t_k / 1e9
+    roof = roofline_block(w, ab, t_stream, t_final, kernel_names, peak, peak_kind)
     step_gbs = (ab["stream"] + ab["final"]) / (ms / 1e3) / 1e9
 
     # end to end: pinned host inputs -> device, the call, outputs -> host, every
     # step.  The step's inputs sit in one pinned host buffer and its outputs in
     # one device buffer (views at 256-byte offsets), so one copy moves each way;
     # copy in, call, copy out are captured in a CUDA graph replayed per step.
-    ins = dict(sets[0])
+    ins = dict(rn.sets[0])
     if w.mode == "greedy":
         ins["uniforms"] = None                     # greedy reads no uniforms
     host_in, dev_in_buf, dev_in = _packed(ins, dev)
-    out_named = {str(i): x for i, x in enumerate(outs[0])}
+    out_named = {str(i): x for i, x in enumerate(rn.outs[0])}
     if w.mode == "greedy":
         out_named["2"] = None                      # greedy writes no accept_prob
     host_out, dev_out_buf, dev_out_v = _packed(out_named, dev)
-    dev_out = tuple(dev_out_v[str(i)] for i in range(len(outs[0])))
+    dev_out = tuple(dev_out_v[str(i)] for i in range(len(rn.outs[0])))
     h2d = host_in.numel()
     d2h = host_out.numel()
-    n_e2e = min(steps, 2000)
     g_e2e = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for _ in range(3):
             dev_in_buf.copy_(host_in, non_blocking=True)
-            _call(sv, w, dev_in, dev_out, wsp, stream)
+            _call(sv, w, dev_in, dev_out, rn.ws, stream)
             host_out.copy_(dev_out_buf, non_blocking=True)
     torch.cuda.synchronize()
     with torch.cuda.graph(g_e2e, stream=stream):
         dev_in_buf.copy_(host_in, non_blocking=True)
-        _call(sv, w, dev_in, dev_out, wsp, stream)
+        _call(sv, w, dev_in, dev_out, rn.ws, stream)
         host_out.copy_(dev_out_buf, non_blocking=True)
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(3):
             g_e2e.replay()
+    torch.cuda.synchronize()
+    est_e2e = (time.perf_counter() - t0) / 3
+    n_e2e = max(3, min(steps, 2000, int(2.0 / max(est_e2e, 1e-6))))
+    with torch.cuda.stream(stream):
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for _ in range(n_e2e):
@@ -433,7 +559,8 @@ def run_gb300(args, rank, ws_n, local):
         f1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, ws_n, dev)
-    pos_e2e = float((sets[0]["gamma_b"].sum() + B).item()) if w.ragged else positions   # the input set used
+    pos_e2e = float((rn.sets[0]["gamma_b"].sum() + B).item()) if w.ragged else positions   # the input set used
+    del host_in, dev_in_buf, host_out, dev_out_buf, g_e2e
 
     line = {
         "metric": METRIC,
@@ -447,126 +574,174 @@ def run_gb300(args, rank, ws_n, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
+        "dtype_note": "float32 arithmetic (two-float sums where a draw is decided) on "
+                      f"{w.dtype} logits",
         "data": "synthetic",
         "config": {
             "workload": w.name, "B": B, "gamma": G, "V": V, "logits_dtype": w.dtype, "mode": w.mode,
             "temperature": w.temperature, "top_k": w.top_k, "top_p": w.top_p,
             "parallelism": f"replicas x{ws_n} (batch per GPU fixed)",
-            "l2": f"no flush: {n_sets} rotating input sets of {per_set / 1e6:.2f} MB (> 2x L2)",
-            "timing": "CUDA graph of calls replayed, CUDA events on the launching stream",
+            "l2": f"no flush: {rn.n_sets} rotating input sets of {rn.per_set / 1e6:.2f} MB (> 2x L2)",
+            "timing": f"CUDA graphs of calls replayed ({steps // rn.n_sets} x {rn.n_sets} calls"
+                      + (f" + 1 x {steps % rn.n_sets}" if steps % rn.n_sets else "")
+                      + "), CUDA events on the launching stream",
         },
         "hbm_gbs": step_gbs,
         "hbm_frac_of_peak": step_gbs / peak,
-        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _traffic(w.name, kname),
-                     "algorithmic_bytes_per_launch": ab[kern], "avg_launch_us": t_k * 1e6,
-                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s"},
-        "kernel_us": kernel_us,
+        "roofline": roof,
+        "kernel_us": _kernel_us(kernel_names, t_stream, t_final),
+        "algorithmic_bytes_per_step": ab,
+        "acceptance": acc,
         "e2e": {"value": pos_e2e * ws_n / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e,
                 "how": "inputs in one pinned host buffer, outputs in one device buffer; copy in, call, copy out "
                        "captured in a CUDA graph and replayed once per step"},
         "gpu_launches": steps * kernels_per_call,
         "clocks": clk,
     }
+    del rn
+    torch.cuda.empty_cache()
     return line, w
 
 
 def other_workloads(args, local):
     """Short device-side runs of the other workloads (graph replay, rotating
     input sets, no flush), each ~0.3 s of timed work: value, ms/step, HBM GB/s
-    and the fraction of the measured peak for the whole step."""
+    and the fraction of the measured peak for the whole step, the roofline of
+    the dominant kernel, the acceptance statistics and a parity sample."""
     import speculative_decoding_verification_46_gb300 as sv
 
     dev = torch.device("cuda", local)
-    peak, _ = _peaks()
+    peak, peak_kind = _peaks()
     out = {}
     for name, w in workloads.WORKLOADS.items():
         if name == args.workload:
             continue
-        B, G, V = w.B, w.gamma, w.V
-        per_set = B * (G + 1) * V * _elt_bytes(w) + B * G * V * _q_elt_bytes(w)
-        n_sets = max(2, min(512, math.ceil(2 * L2_BYTES / per_set) + 1))
-        sets = _input_sets(w, n_sets, dev)
-        outs = [(torch.empty(B, G + 1, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
-                 torch.empty(B, G, dtype=torch.float32, device=dev) if w.mode == "sample" and G > 0 else None,
-                 torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(n_sets)]
-        wsp = _workspace(sv, w, B, G, V, dev)
-        stream = torch.cuda.Stream(device=dev)
-        with torch.cuda.stream(stream):
-            for i in range(n_sets):
-                _call(sv, w, sets[i], outs[i], wsp, stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(n_sets):
-                _call(sv, w, sets[i], outs[i], wsp, stream)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            graph.replay()
+        rn = Runner(sv, w, dev, max_sets=512)
+        _, kernel_names = rn.kernels()
+        rn.prepare(rn.n_sets)
+        rn.run_steps(rn.n_sets)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            graph.replay()
+        rn.run_steps(rn.n_sets)
         torch.cuda.synchronize()
         reps = max(1, int(0.3 / max(time.perf_counter() - t0, 1e-6)))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                graph.replay()
-            e1.record(stream)
+        with torch.cuda.stream(rn.stream):
+            e0.record(rn.stream)
+            rn.run_steps(reps * rn.n_sets)
+            e1.record(rn.stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / (reps * n_sets)
-        nacc = np.concatenate([o[1].cpu().numpy() for o in outs])
-        gb_all = np.concatenate([st["gamma_b"].cpu().numpy() for st in sets]) if w.ragged else None
-        ab = algorithmic_bytes(w, nacc, gamma_b=gb_all)
-        gbs = (ab["stream"] + ab["final"]) / n_sets / (ms / 1e3) / 1e9
-        pos = (float(np.sum(gb_all)) / n_sets + B) if w.ragged else B * (G + 1)   # positions in the round
+        ms = e0.elapsed_time(e1) / (reps * rn.n_sets)
+        t_stream, t_final = rn.kernel_times(2, 50)
+        ab, pos, acc = rn.accounting()
+        gbs = (ab["stream"] + ab["final"]) / (ms / 1e3) / 1e9
         out[name] = {"value": pos / (ms / 1e3), "ms_per_step": ms, "hbm_gbs": gbs,
-                     "frac_of_measured_peak": gbs / peak, "steps": reps * n_sets}
-        del sets, outs, wsp, graph
+                     "frac_of_measured_peak": gbs / peak, "steps": reps * rn.n_sets,
+                     "roofline": roofline_block(w, ab, t_stream, t_final, kernel_names, peak, peak_kind),
+                     "kernel_us": _kernel_us(kernel_names, t_stream, t_final), "acceptance": acc}
+        del rn
         torch.cuda.empty_cache()
+        if not args.no_cpu_baseline:
+            out[name]["parity"] = parity_sample(w, 2.0, dev)[0]
     return out
 
 
-def oracle_throughput(w, budget_s: float, device="cpu"):
-    """The CPU oracle on a bounded sample of the workload: whole batches of
-    B sequences when they fit the budget, else a prefix of one batch."""
+# ---------------------------------------------------------------- the oracle legs
+
+def _oracle_one(svref, w, h, b):
+    """The oracle on sequence b of the host inputs h."""
+    sl = slice(b, b + 1)
+    if w.mode == "greedy":
+        return svref.verify_greedy(h["L"][sl], h["d"][sl])
+    if w.ragged:
+        # the round ends at stop tokens / budgets, as the GPU call does
+        r = svref.verify_sample_ragged(h["L"][sl], h["q"][sl] if h["q"] is not None else None, h["d"][sl],
+                                       h["u"][sl], w.temperature, h["gb"][sl], w.top_k, w.top_p)
+        r["out_tokens"], _ = svref.truncate_emitted(r["out_tokens"], r["n_accepted"], h["stops"], h["mx"][sl])
+        return r
+    if w.qlogits:
+        return svref.verify_sample_qlogits(h["L"][sl], h["ql"][sl], h["d"][sl], h["u"][sl], w.temperature,
+                                           w.top_k, w.top_p)
+    return svref.verify_sample(h["L"][sl], h["q"][sl] if h["q"] is not None else None, h["d"][sl], h["u"][sl],
+                               w.temperature, w.top_k, w.top_p)
+
+
+def _host_inputs(inp, w):
+    return {"L": inp["logits"].float().cpu().numpy(), "d": inp["draft"].cpu().numpy(),
+            "u": inp["uniforms"].cpu().numpy(),
+            "q": inp["q"].cpu().numpy() if inp.get("q") is not None else None,
+            "ql": inp["q_logits"].float().cpu().numpy() if w.qlogits else None,
+            "gb": inp["gamma_b"].cpu().numpy() if w.ragged else None,
+            "stops": inp["stop_tokens"].cpu().numpy() if w.ragged else None,
+            "mx": inp["max_new"].cpu().numpy() if w.ragged else None}
+
+
+def parity_sample(w, budget_s: float, dev):
+    """The GPU path and the oracle on the same inputs (seed + 7): the GPU call
+    over the whole batch, the oracle on sequences 0, 1, ... for about
+    budget_s seconds.  Returns (parity counts, oracle positions/s, sample
+    description).  A draw is an evaluated accept test or the final draw; a
+    boundary draw is one the oracle flags within 1e-6 of a decision boundary
+    (with q from draft logits also within the wider absolute band on the final
+    draw's CDF step, counted separately); a hard mismatch is a differing
+    sequence with no boundary draw."""
+    import speculative_decoding_verification_46_gb300 as sv
     from oracle import svref
 
-    inp = workloads.make_inputs(w, seed=w.seed + 7, device="cuda" if torch.cuda.is_available() else "cpu")
-    L = inp["logits"].float().cpu().numpy()
-    d = inp["draft"].cpu().numpy()
-    u = inp["uniforms"].cpu().numpy()
-    q = inp["q"].cpu().numpy() if inp["q"] is not None else None
-    qlg = inp["q_logits"].float().cpu().numpy() if w.qlogits else None
-    gbh = inp["gamma_b"].cpu().numpy() if w.ragged else None
-    stops = inp["stop_tokens"].cpu().numpy() if w.ragged else None
-    mxh = inp["max_new"].cpu().numpy() if w.ragged else None
-    done, seqs = 0.0, 0
-    t0 = time.perf_counter()
-    b = 0
-    while True:
-        sl = slice(b, b + 1)
-        if w.mode == "greedy":
-            svref.verify_greedy(L[sl], d[sl])
-        elif w.ragged:
-            r = svref.verify_sample_ragged(L[sl], q[sl] if q is not None else None, d[sl], u[sl], w.temperature,
-                                           gbh[sl], w.top_k, w.top_p)
-            svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[sl])
-        elif w.qlogits:
-            svref.verify_sample_qlogits(L[sl], qlg[sl], d[sl], u[sl], w.temperature, w.top_k, w.top_p)
-        else:
-            svref.verify_sample(L[sl], q[sl] if q is not None else None, d[sl], u[sl], w.temperature, w.top_k,
-                                w.top_p)
+    inp = workloads.make_inputs(w, seed=w.seed + 7, device=dev)
+    G = w.gamma
+    ws = _workspace(sv, w, w.B, G, w.V, dev)
+    out = (torch.empty(w.B, G + 1, dtype=torch.int32, device=dev), torch.empty(w.B, dtype=torch.int32, device=dev),
+           torch.empty(w.B, G, dtype=torch.float32, device=dev) if w.mode == "sample" and G > 0 else None,
+           torch.empty(w.B, dtype=torch.int32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+    _call(sv, w, inp, out, ws, stream)
+    torch.cuda.synchronize()
+    tok = out[0].cpu().numpy()
+    n = out[1].cpu().numpy()
+    a = out[2].cpu().numpy() if out[2] is not None else None
+    h = _host_inputs(inp, w)
+    del inp, ws
+    c = dict(sequences=0, draws=0, hard_mismatches=0, boundary_flagged=0, boundary_mismatches=0,
+             max_rel_err_accept_prob=0.0)
+    if w.qlogits:
+        c["widened_band_only"] = 0
+    seqs, t0 = 0, time.perf_counter()
+    while seqs < w.B:
+        r = _oracle_one(svref, w, h, seqs)
+        b = seqs
         seqs += 1
-        b = (b + 1) % w.B
-        done = time.perf_counter() - t0
-        if done >= budget_s:
+        rt = r["out_tokens"][0].copy()
+        rn_ = int(r["n_accepted"][0])
+        bad = (int(r["status"][0]) & svref.SEQ_BAD_ROW) != 0
+        if not bad:
+            gtok = tok[b]
+            mism = (not np.array_equal(gtok, rt)) or int(n[b]) != rn_
+            bnd = bool(r["boundary"][0]) if "boundary" in r else False
+            c["sequences"] += 1
+            gbb = int(h["gb"][b]) if w.ragged else G
+            c["draws"] += (min(rn_ + 1, gbb) + 1) if w.mode == "sample" else 1
+            c["boundary_flagged"] += int(bnd)
+            c["hard_mismatches"] += int(mism and not bnd)
+            c["boundary_mismatches"] += int(mism and bnd)
+            if w.qlogits and "qlogits_band_only" in r:
+                c["widened_band_only"] += int(r["qlogits_band_only"][0])
+            if a is not None and "accept_prob" in r and gbb > 0:
+                ar = r["accept_prob"][0][:gbb]
+                ag = a[b][:gbb].astype(np.float64)
+                rel = np.abs(ag - ar) / np.maximum(np.abs(ar), 1e-300)
+                rel[(np.abs(ag - ar) <= 1e-30)] = 0.0
+                c["max_rel_err_accept_prob"] = max(c["max_rel_err_accept_prob"], float(rel.max(initial=0.0)))
+        if time.perf_counter() - t0 >= budget_s:
             break
-    pos = seqs * (w.gamma + 1)
-    return pos / done, f"{seqs} sequences of the workload ({pos} positions) in {done:.2f} s, numpy float64"
+    el = time.perf_counter() - t0
+    c["boundary_mismatch_frac"] = c["boundary_mismatches"] / max(c["draws"], 1)
+    c["limit"] = BOUNDARY_LIMIT
+    c["tolerance"] = ("greedy bit-exact" if w.mode == "greedy" else
+                      "accept_prob 1e-5 relative; tokens and counts exact except draws within 1e-6 of a boundary")
+    pos = seqs * (G + 1)
+    return c, pos / el, f"sequences 0..{seqs - 1} of one batch ({pos} positions) in {el:.2f} s, numpy float64"
 
 
 def main():
@@ -581,44 +756,18 @@ def main():
         from oracle import svref
 
         inp = workloads.make_inputs(w, seed=w.seed + 7, device="cuda" if torch.cuda.is_available() else "cpu")
-        L = inp["logits"].float().cpu().numpy()
-        d = inp["draft"].cpu().numpy()
-        u = inp["uniforms"].cpu().numpy()
-        q = inp["q"].cpu().numpy() if inp["q"] is not None else None
-        qlg = inp["q_logits"].float().cpu().numpy() if w.qlogits else None
-        gbh = inp["gamma_b"].cpu().numpy() if w.ragged else None
-        stops = inp["stop_tokens"].cpu().numpy() if w.ragged else None
-        mxh = inp["max_new"].cpu().numpy() if w.ragged else None
+        h = _host_inputs(inp, w)
+        del inp
         # one step = a bounded sample of the batch (at most ~2 s of oracle work)
         t0 = time.perf_counter()
-        if w.mode == "greedy":
-            svref.verify_greedy(L[:1], d[:1])
-        elif w.ragged:
-            r = svref.verify_sample_ragged(L[:1], q[:1] if q is not None else None, d[:1], u[:1], w.temperature,
-                                           gbh[:1], w.top_k, w.top_p)
-            svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[:1])
-        elif w.qlogits:
-            svref.verify_sample_qlogits(L[:1], qlg[:1], d[:1], u[:1], w.temperature, w.top_k, w.top_p)
-        else:
-            svref.verify_sample(L[:1], q[:1] if q is not None else None, d[:1], u[:1], w.temperature, w.top_k,
-                                w.top_p)
+        _oracle_one(svref, w, h, 0)
         per_seq = time.perf_counter() - t0
         per_step_budget = min(2.0, 120.0 / max(1, steps + warmup))
         nseq = int(max(1, min(w.B, per_step_budget / max(per_seq, 1e-6))))
 
         def step():
-            if w.mode == "greedy":
-                svref.verify_greedy(L[:nseq], d[:nseq])
-            elif w.ragged:
-                r = svref.verify_sample_ragged(L[:nseq], q[:nseq] if q is not None else None, d[:nseq], u[:nseq],
-                                               w.temperature, gbh[:nseq], w.top_k, w.top_p)
-                svref.truncate_emitted(r["out_tokens"], r["n_accepted"], stops, mxh[:nseq])
-            elif w.qlogits:
-                svref.verify_sample_qlogits(L[:nseq], qlg[:nseq], d[:nseq], u[:nseq], w.temperature, w.top_k,
-                                            w.top_p)
-            else:
-                svref.verify_sample(L[:nseq], q[:nseq] if q is not None else None, d[:nseq], u[:nseq],
-                                    w.temperature, w.top_k, w.top_p)
+            for b in range(nseq):
+                _oracle_one(svref, w, h, b)
 
         for _ in range(warmup):
             step()
@@ -640,12 +789,13 @@ def main():
         return
 
     line, w = run_gb300(args, rank, ws_n, local)
-    if rank == 0 and ws_n == 1 and not args.no_other_workloads and args.batch is None:
-        line["other_workloads"] = other_workloads(args, local)
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        v, sample = oracle_throughput(w, args.cpu_seconds)
+        par, v, sample = parity_sample(w, args.cpu_seconds, torch.device("cuda", local))
+        line["parity"] = par
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
                                 "host": platform.machine(), "host_cpus": os.cpu_count()}
+    if rank == 0 and ws_n == 1 and not args.no_other_workloads and args.batch is None:
+        line["other_workloads"] = other_workloads(args, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_n > 1:

@@ -199,8 +199,11 @@ def verify_sample(logits, q, draft, uniforms, temperature, top_k=0, top_p=1.0):
     uniforms [B, gamma+1]     U[b, i] accept test i, U[b, gamma] final draw
 
     Returns a dict of numpy arrays: out_tokens [B, gamma+1] (-1 padded),
-    n_accepted [B], accept_prob [B, gamma], status [B] and boundary [B] (True
-    where any evaluated draw lay within BOUNDARY_EPS of a decision boundary).
+    n_accepted [B], accept_prob [B, gamma], status [B], boundary [B] (True
+    where any evaluated draw lay within BOUNDARY_EPS of a decision boundary)
+    and residual_mass [B] (R = sum max(p_n - q_n, 0) after a rejection, 1 for
+    the bonus draw; reported so that a comparison can tell a rejection whose
+    residual is zero only through rounding).
     """
     logits = np.asarray(logits)
     B, G1, V = logits.shape
@@ -219,6 +222,7 @@ def verify_sample(logits, q, draft, uniforms, temperature, top_k=0, top_p=1.0):
     acc_prob = np.zeros((B, gamma), dtype=np.float64)
     status = np.zeros(B, dtype=np.int64)
     boundary = np.zeros(B, dtype=bool)
+    rmass = np.ones(B, dtype=np.float64)
 
     for b in range(B):
         P = []
@@ -251,6 +255,7 @@ def verify_sample(logits, q, draft, uniforms, temperature, top_k=0, top_p=1.0):
         # one final draw: residual after a rejection, else the bonus from p_gamma
         if n < gamma:
             r = residual(P[n], q[b, n])
+            rmass[b] = r.sum()
             if not (r.sum() > 0.0):
                 status[b] |= SEQ_RESIDUAL_ZERO
                 r = P[n]
@@ -265,7 +270,7 @@ def verify_sample(logits, q, draft, uniforms, temperature, top_k=0, top_p=1.0):
         out[b, n] = tok
         n_acc[b] = n
     return dict(out_tokens=out, n_accepted=n_acc, accept_prob=acc_prob,
-                status=status, boundary=boundary)
+                status=status, boundary=boundary, residual_mass=rmass)
 
 
 def first_argmax(row) -> int:
@@ -341,6 +346,7 @@ def verify_sample_ragged(logits, q, draft, uniforms, temperature, gamma_b, top_k
     acc_prob = np.zeros((B, gamma), dtype=np.float64)
     status = np.zeros(B, dtype=np.int64)
     boundary = np.zeros(B, dtype=bool)
+    rmass = np.ones(B, dtype=np.float64)
     for b in range(B):
         g = int(gamma_b[b])
         if not (0 <= g <= gamma):
@@ -353,7 +359,9 @@ def verify_sample_ragged(logits, q, draft, uniforms, temperature, gamma_b, top_k
         acc_prob[b, :g] = r["accept_prob"][0]
         status[b] = r["status"][0]
         boundary[b] = r["boundary"][0]
-    return dict(out_tokens=out, n_accepted=n_acc, accept_prob=acc_prob, status=status, boundary=boundary)
+        rmass[b] = r["residual_mass"][0]
+    return dict(out_tokens=out, n_accepted=n_acc, accept_prob=acc_prob, status=status, boundary=boundary,
+                residual_mass=rmass)
 
 
 def verify_greedy_ragged(logits, draft, gamma_b):
@@ -442,6 +450,9 @@ def verify_sample_qlogits(logits, q_logits, draft, uniforms, temperature, top_k=
     B, G1, V = L.shape
     gamma = G1 - 1
     U = np.asarray(uniforms, dtype=np.float32).reshape(B, G1)
+    # reported separately: the sequences flagged only by the bands this
+    # function adds (not by the 1e-6 bands of verify_sample)
+    plain = r["boundary"].copy()
     for b in range(B):
         r["boundary"][b] |= bool(qtb[b].any())
         if r["status"][b] & SEQ_BAD_ROW:
@@ -457,4 +468,5 @@ def verify_sample_qlogits(logits, q_logits, draft, uniforms, temperature, top_k=
         lower, upper = C[v] - w[v], C[v]
         if abs(t - lower) < QLOGITS_CDF_BAND or abs(upper - t) < QLOGITS_CDF_BAND:
             r["boundary"][b] = True
+    r["qlogits_band_only"] = r["boundary"] & ~plain
     return r

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     SV_ERR_TIMEOUT,
     SV_ERR_UNSUPPORTED,
     SV_ERR_WORKSPACE,
+    SV_NOALLOC_SCRATCH_BYTES,
     SV_OK,
     SV_SEQ_BAD_ROW,
     SV_SEQ_DRAFT_OUT_OF_RANGE,

@@ -33,6 +33,10 @@ SV_SEQ_Q_NOT_POSITIVE = 2
 SV_SEQ_BAD_ROW = 4
 SV_SEQ_RESIDUAL_ZERO = 8
 
+# Size of the static scratch sv_verify_greedy_noalloc works in (the header's
+# SV_NOALLOC_SCRATCH_BYTES).
+SV_NOALLOC_SCRATCH_BYTES = 8 << 20
+
 _TORCH_DTYPE = {torch.float32: SV_DTYPE_F32, torch.bfloat16: SV_DTYPE_BF16, torch.float16: SV_DTYPE_F16}
 
 _c_int, _c_float, _c_size, _c_ptr = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p

@@ -9,6 +9,7 @@
 // They call this entry point instead of sv_verify_greedy.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "specverify.h"
@@ -20,7 +21,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRA
 namespace {
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+// One cached address per device.  Atomic: host threads making their first
+// call on the same device at the same time may both look the address up;
+// they store the same value and neither reads a torn one.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 // Device address of the scratch on the current device.  Looked up once per
 // device (with that device current) and cached; the array's name in host code
@@ -29,15 +33,15 @@ sv_status scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return SV_ERR_CUDA;
     }
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return SV_OK;
 }
 

@@ -17,6 +17,7 @@ from oracle import svref
 RTOL = 1e-5
 ATOL = 1e-30
 BOUNDARY_FRACTION = 1e-4
+RESID_TINY = 1e-6
 
 
 def to_np(t):
@@ -34,6 +35,40 @@ def oracle_sample(inp, T, top_k=0, top_p=1.0, rows=None):
         L, d, u = L[rows], d[rows], u[rows]
         q = q[rows] if q is not None else None
     return svref.verify_sample(L, q, d, u, T, top_k, top_p)
+
+
+def _oracle_chunk(job):
+    kind, arrays, scal = job
+    if kind == "sample":
+        return svref.verify_sample(*arrays, *scal)
+    if kind == "qlogits":
+        return svref.verify_sample_qlogits(*arrays, *scal)
+    L, q, d, u, gb = arrays          # ragged
+    T, top_k, top_p = scal
+    return svref.verify_sample_ragged(L, q, d, u, T, gb, top_k, top_p)
+
+
+def oracle_pool(kind, arrays, scal, workers=8, chunk=8):
+    """An oracle entry point ("sample": verify_sample(L, q, d, u, T, k, p);
+    "qlogits": verify_sample_qlogits(L, Q, d, u, T, k, p); "ragged":
+    verify_sample_ragged(L, q, d, u, T, gamma_b, k, p)) over the whole batch,
+    sequences split across a pool of `spawn` processes (the oracle works per
+    sequence; spawn, not fork, because the parent holds a CUDA context).
+    `arrays` are per-sequence numpy arrays (None allowed), `scal` the
+    trailing scalars.  Returns the oracle's result dict for the batch."""
+    import multiprocessing as mp
+
+    B = arrays[0].shape[0]
+    jobs = [(kind, [None if a is None else a[s:s + chunk] for a in arrays], scal) for s in range(0, B, chunk)]
+    with mp.get_context("spawn").Pool(max(1, min(workers, len(jobs), mp.cpu_count()))) as pool:
+        parts = pool.map_async(_oracle_chunk, jobs).get(timeout=900)
+    return {k: np.concatenate([r[k] for r in parts]) for k in parts[0]}
+
+
+def oracle_sample_pool(inp, T, top_k=0, top_p=1.0):
+    """oracle_sample over the whole batch on a process pool."""
+    L, q, d, u = (to_np(inp[k]) for k in ("logits", "q", "draft", "uniforms"))
+    return oracle_pool("sample", [L, q, d, u], (T, top_k, top_p))
 
 
 def oracle_greedy(inp, rows=None):
@@ -67,8 +102,16 @@ def compare_sample(gpu, ref, V, rows=None):
     stats["boundary_mismatch"] = int((mism & ref["boundary"] & good).sum())
     stats["boundary_flagged"] = int((ref["boundary"] & good).sum())
     stats["draws"] = int((np.minimum(ref["n_accepted"] + 1, G) + 1)[good].sum())
-    keep = ~np.int64(svref.SEQ_RESIDUAL_ZERO)
-    assert np.array_equal((st[good] & keep), (ref["status"][good] & keep)), "status bits differ"
+    # Every status bit is compared exactly.  The one exception is
+    # SEQ_RESIDUAL_ZERO on a rejection whose exact residual mass R is below
+    # RESID_TINY: the step forms the residual in float32 (probabilities
+    # rounded at ~6e-8 relative), so a float64 R of that size may round to
+    # zero (bit set, draw from p_n) or stay positive; both are the pages'
+    # rule applied to the values the step holds.
+    keep = np.full(st.shape, -1, dtype=np.int64)
+    if "residual_mass" in ref:
+        keep[ref["residual_mass"] < RESID_TINY] &= ~np.int64(svref.SEQ_RESIDUAL_ZERO)
+    assert np.array_equal((st & keep)[good], (ref["status"] & keep)[good]), "status bits differ"
     if stats["hard"]:
         lines = []
         for bidx in np.nonzero(hard)[0][:5]:

@@ -191,3 +191,11 @@ def test_qlogits_validation(sv):
     assert call(wsb=ws - 256) == sv.SV_ERR_WORKSPACE
     assert call(B=0, logits=None, ql=None) == sv.SV_OK
     assert sv.sv_last_kernels() == []
+
+
+def test_noalloc_scratch_size_matches_header(sv):
+    """The binding's SV_NOALLOC_SCRATCH_BYTES is the header's value."""
+    text = open(os.path.join(ROOT, "include", "specverify.h")).read()
+    m = re.search(r"#define\s+SV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "SV_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert sv.SV_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

@@ -92,3 +92,23 @@ def test_reference_arm_fields(name):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"] == name
+
+
+def test_kept_counts_match_the_oracle_keep_set():
+    """The bench's count of kept candidates (torch) equals the size of the
+    oracle's top-k then top-p keep set, row by row."""
+    from oracle import svref
+    import torch
+
+    g = torch.Generator().manual_seed(5)
+    rows = (torch.randn(12, 3000, generator=g) * 2).to(torch.bfloat16)
+    for k, tp in [(50, 0.9), (0, 0.5), (7, 1.0), (3000, 0.99)]:
+        got = bench.kept_counts(rows, 0.8, k, tp).numpy()
+        want = [len(svref.truncation_keep_set(r, 0.8, k, tp)[0]) for r in rows.float().numpy()]
+        assert list(got) == want, (k, tp)
+
+
+def test_algorithmic_bytes_counts_kept_q_reads():
+    t = workloads.WORKLOADS["topk50_topp0.9_b256_g8_v152064_bf16"]
+    base = bench.algorithmic_bytes(t, np.zeros(256, int))["stream"]
+    assert bench.algorithmic_bytes(t, np.zeros(256, int), kept_rejected=1000)["stream"] == base + 4000

@@ -95,12 +95,12 @@ def test_deterministic_single_sequence_rounds(sv):
     assert accepted > 0
 
 
-def test_deterministic_full_size_b64_sampled(sv):
+def test_deterministic_full_size_b64(sv):
     w = workloads.WORKLOADS["sample_b64_g4_v128256_bf16_s0.7"]
     inp = workloads.make_inputs(w, device=DEV)
     guess = inp["logits"][:, : w.gamma].float() + 0.7 * torch.randn(w.B, w.gamma, w.V, device=DEV,
                                                                       generator=torch.Generator(DEV).manual_seed(3))
     inp = dict(inp, q=None, draft=guess.argmax(-1).to(torch.int32).contiguous())
     out = sv.verify_sample(inp["logits"], None, inp["draft"], inp["uniforms"], w.temperature)
-    rows = np.random.default_rng(1).choice(w.B, size=16, replace=False)
-    P.compare_sample(out, P.oracle_sample(inp, w.temperature, rows=rows), w.V, rows=rows)
+    st = P.compare_sample(out, P.oracle_sample_pool(inp, w.temperature), w.V)
+    assert st["sequences"] == w.B

@@ -115,16 +115,14 @@ def test_ragged_greedy(sv, path, V, G, B):
     P.compare_greedy(out, ref, V)
 
 
-def test_ragged_full_size_b64_sampled(sv):
+def test_ragged_full_size_b64(sv):
     w = workloads.WORKLOADS["sample_b64_g4_v128256_bf16_s0.7"]
     inp = workloads.make_inputs(w, device=DEV)
     gb = torch.randint(0, w.gamma + 1, (w.B,), generator=torch.Generator().manual_seed(9), dtype=torch.int32)
     out = sv.verify_sample(inp["logits"], inp["q"], inp["draft"], inp["uniforms"], w.temperature, gamma_b=gb.to(DEV))
-    rows = np.random.default_rng(2).choice(w.B, size=16, replace=False)
-    L = P.to_np(inp["logits"])[rows]
-    ref = svref.verify_sample_ragged(L, P.to_np(inp["q"])[rows], P.to_np(inp["draft"])[rows],
-                                     P.to_np(inp["uniforms"])[rows], w.temperature, gb.numpy()[rows])
-    P.compare_sample(out, ref, w.V, rows=rows)
+    arrays = [P.to_np(inp[k]) for k in ("logits", "q", "draft", "uniforms")] + [gb.numpy()]
+    st = P.compare_sample(out, P.oracle_pool("ragged", arrays, (w.temperature, 0, 1.0)), w.V)
+    assert st["sequences"] == w.B
 
 
 @pytest.mark.parametrize("n_stop,with_budget", [(0, True), (1, False), (3, True), (64, True)])

@@ -1,10 +1,11 @@
 """sv_verify_greedy_noalloc: greedy verify for callers that cannot allocate
 device memory (the library's own static scratch replaces the workspace).
 
-Called through the C ABI and compared with sv_verify_greedy (workspace
-entry point) on the same inputs, on two calls in a row: the greedy tolerance
-is bit-exact.  This file is collected last so that a stop-at-first-failure run
-has already run every other test; it also passes alone in a fresh process.
+Called through the C ABI, on two calls in a row, and compared bit-exactly
+(the greedy tolerance) with the CPU oracle and with sv_verify_greedy (the
+workspace entry point) on the same inputs.  This file is collected last so
+that a stop-at-first-failure run has already run every other test; it also
+passes alone in a fresh process.
 """
 
 import numpy as np
@@ -12,6 +13,7 @@ import pytest
 import torch
 
 import workloads
+import _parity as P
 
 pytestmark = pytest.mark.gpu
 
@@ -43,22 +45,29 @@ def _noalloc(sv, logits, draft, stream):
 
 @pytest.mark.parametrize("B,V,dtype", [(512, 128256, torch.bfloat16), (37, 1001, torch.float32),
                                        (9, 40003, torch.float16)])
-def test_noalloc_matches_workspace_entry_point_on_two_calls(sv, B, V, dtype):
+def test_noalloc_matches_oracle_and_workspace_entry_point_on_two_calls(sv, B, V, dtype):
     w = workloads.WORKLOADS["greedy_b512_g4_v128256_bf16"].with_(V=V)
     inp = workloads.make_inputs(w, seed=B + V, device="cuda:0", B=B)
     logits = inp["logits"].to(dtype).contiguous()
     draft = inp["draft"]
+    assert sv.sv_workspace_bytes(B, w.gamma, V, 0) <= sv.SV_NOALLOC_SCRATCH_BYTES
     stream = torch.cuda.current_stream()
-    ref = sv.verify_greedy(logits, draft)
+    ref = P.oracle_greedy(dict(logits=logits, draft=draft))
+    ws_out = sv.verify_greedy(logits, draft)
     for _ in range(2):
         got = _noalloc(sv, logits, draft, stream)
         torch.cuda.synchronize()
-        for a, b in zip(got, ref):
+        P.compare_greedy(got, ref, V)
+        assert np.array_equal(P.to_np(got[2]), ref["status"])
+        for a, b in zip(got, ws_out):
             assert torch.equal(a, b)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(sv):
+    """A problem whose workspace exceeds the scratch is refused before any
+    pointer is used: every pointer here is NULL, so nothing can be read or
+    written whatever the order of the checks."""
     B, G, V = 4096, 8, 152064
-    assert sv.sv_workspace_bytes(B, G, V, 0) > (8 << 20)
-    rc = sv.sv_verify_greedy_noalloc(B, G, V, 1 << 20, sv.SV_DTYPE_BF16, 1 << 21, 1 << 22, 1 << 23, None, None)
-    assert rc == sv.SV_ERR_WORKSPACE
+    assert sv.sv_workspace_bytes(B, G, V, 0) > sv.SV_NOALLOC_SCRATCH_BYTES
+    rc = sv.sv_verify_greedy_noalloc(B, G, V, None, sv.SV_DTYPE_BF16, None, None, None, None, None)
+    assert rc == sv.SV_ERR_WORKSPACE, sv.sv_status_string(rc)
