@@ -447,7 +447,7 @@ def roofline_block(w, ab, t_stream, t_final, kernel_names, peak, peak_kind):
         ab = dict(ab, stream=ab["stream"] + ab["final"], final=0.0)
         t_final = 0.0
     kern = "stream" if t_stream >= t_final else "final"
-    kname = kernel_names[0] if kern == "stream" else kernel_names[1]
+    kname = kernel_names[0] if kern == "stream" else _final_name(kernel_names)
     t_k = t_stream if kern == "stream" else t_final
     achieved = ab[kern] / t_k / 1e9
     return {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -457,10 +457,15 @@ def roofline_block(w, ab, t_stream, t_final, kernel_names, peak, peak_kind):
             else "fallback 6.8 TB/s"}
 
 
+def _final_name(kernel_names):
+    """The kernels after the streaming one (timed together by the hook)."""
+    return "+".join(kernel_names[1:])
+
+
 def _kernel_us(kernel_names, t_stream, t_final):
     d = {kernel_names[0]: t_stream * 1e6}
-    if len(kernel_names) == 2:
-        d[kernel_names[1]] = t_final * 1e6
+    if len(kernel_names) >= 2:
+        d[_final_name(kernel_names)] = t_final * 1e6
     return d
 
 

@@ -14,6 +14,7 @@
 #include "specverify.h"
 #include "sv_cluster.cuh"
 #include "sv_device.cuh"
+#include "sv_final.cuh"
 #include "sv_qsoftmax.cuh"
 #include "sv_stream.cuh"
 #include "sv_truncate.cuh"
@@ -41,8 +42,8 @@ int list_len(int V, int top_k) {
 }
 
 struct Layout {
-  size_t seq_ticket, seq_ticket2, row_ticket, ctr, seq, acc, part, lists, rowres, chunk, total;
-  int S_part, S_list, C_max, klist;
+  size_t seq_ticket, seq_ticket2, row_ticket, ctr, seq, acc, part, lists, rowres, fd_part, fd_q, total;
+  int S_part, S_list, FC, klist;
 };
 
 // One layout for any dtype and launch shape: slices are sized for the
@@ -54,8 +55,8 @@ Layout make_layout(int B, int gamma, int V, int top_k) {
   L.klist = list_len(V, top_k);
   L.S_part = (int)ceil_div(V, sv::kThreads * 1 * 4);
   L.S_list = L.klist > 0 ? (int)ceil_div(V, sv::kThreads * sv::kMaxU * 4) : 0;
-  // residual sub-ranges per row: chunks x slots = about V / (256 * vector width)
-  L.C_max = (int)ceil_div(V, sv::kThreads * 4) + sv::kResMaxEPT / 4;
+  // final draw: 512-token items per row
+  L.FC = (int)ceil_div(V, sv::kFdTok);
   size_t o = 0;
   L.seq_ticket = o;  o += up(sizeof(int) * (size_t)B);
   L.seq_ticket2 = o; o += up(sizeof(int) * (size_t)B);
@@ -68,7 +69,8 @@ Layout make_layout(int B, int gamma, int V, int top_k) {
   L.part = o;        o += up(sizeof(float4) * (size_t)R * std::max(L.S_part, 4 * sv::kWarps));
   L.lists = o;       o += up(sizeof(unsigned long long) * (size_t)R * L.S_list * L.klist);
   L.rowres = o;      o += up(L.klist > 0 ? sizeof(int2) * (size_t)R * (L.klist + 1) : 0);
-  L.chunk = o;       o += up(3 * sizeof(float2) * (size_t)B * L.C_max);
+  L.fd_part = o;     o += up(sizeof(float4) * (size_t)B * L.FC);
+  L.fd_q = o;        o += up(sizeof(float) * (size_t)B * L.FC);
   L.total = o;
   return L;
 }
@@ -105,7 +107,9 @@ void bind_workspace(sv::Params& p, const Layout& L, void* ws) {
   p.part = reinterpret_cast<float4*>(w + L.part);
   p.lists = reinterpret_cast<unsigned long long*>(w + L.lists);
   p.rowres = reinterpret_cast<int2*>(w + L.rowres);
-  p.chunk_mass = reinterpret_cast<float2*>(w + L.chunk);
+  p.fd_part = reinterpret_cast<float4*>(w + L.fd_part);
+  p.fd_q = reinterpret_cast<float*>(w + L.fd_q);
+  p.FC = L.FC;
 }
 
 // Rows-kernel slicing: 8 vectors per thread unless that leaves fewer than two
@@ -123,17 +127,6 @@ void choose_slices(sv::Params& p, sv_dtype dt, bool topk) {
   p.S = (int)ceil_div(p.V, p.SL);
 }
 
-// Residual-kernel chunking: 32, 16 or 8 elements per thread, the largest that
-// still gives two CTAs per SM.
-void choose_chunks(sv::Params& p) {
-  const long long want = 2ll * sm_count();
-  int ept = sv::kResMaxEPT;
-  while (ept > 8 && (long long)p.B * ceil_div(p.V, (long long)sv::kThreads * ept) < want) ept >>= 1;
-  p.EPT = ept;
-  p.CL = sv::kThreads * ept;
-  p.C = (int)ceil_div(p.V, p.CL);
-}
-
 template <typename T, int MODE>
 sv_status launch_rows(const sv::Params& p, cudaStream_t stream) {
   const size_t smem = MODE == sv::MODE_TOPK ? sizeof(sv::RowsSmem) : offsetof(sv::RowsSmem, cand);
@@ -146,17 +139,12 @@ sv_status launch_rows(const sv::Params& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-template <typename T>
-sv_status launch_residual(const sv::Params& p, cudaStream_t stream) {
-  const size_t smem = sv::ResStage<T>::bytes;
-  if (cudaFuncSetAttribute(sv::residual_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return SV_ERR_CUDA;
-  }
+// Programmatic dependent launch of `kern` after the previous kernel on the stream.
+template <typename K>
+sv_status launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, const sv::Params& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((long long)p.B * p.C));
-  cfg.blockDim = dim3(sv::kThreads);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -164,11 +152,35 @@ sv_status launch_residual(const sv::Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, sv::residual_kernel<T>, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// The final draw: persistent CTAs (as many as fit, at most one warp per
+// item); each warp takes a contiguous range of the B * FC items.
+template <typename T>
+sv_status launch_final_draw(const sv::Params& p, cudaStream_t stream) {
+  auto kern = sv::final_draw_kernel<T>;
+  const size_t smem = sv::FdRing<T>::bytes;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sv::kFdThreads, smem) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const long long items = (long long)p.B * p.FC;
+  const long long grid = std::max(1ll, std::min((long long)per_sm * sm_count(), ceil_div(items, sv::kFdWarps)));
+  const sv_status st = launch_pdl(kern, dim3((unsigned)grid), dim3(sv::kFdThreads), smem, p, stream);
+  if (st != SV_OK) return st;
+  // the search: one CTA per sequence
+  return launch_pdl(sv::final_pick_kernel<T>, dim3((unsigned)p.B), dim3(sv::kPickThreads), 0, p, stream);
 }
 
 // ---------------------------------------------------------------- cluster path
@@ -292,21 +304,10 @@ sv_status launch_stream_topk(const sv::Params& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Parts per row for the dense streaming kernel.  Splitting each row into H
-// parts (each at least one ring chunk long; H * warps divides 32) gives the
-// CTAs more, smaller items: with fewer rows than CTA slots it evens the
-// per-SM work, and with many rows it lets every slot hold a CTA.  Measured on
-// 128K-vocabulary rows: H = 2 beats whole rows at 320 to 2560 rows, and
-// H = 4 loses to H = 2 at 320 rows; H = 4 is kept for batches small enough
-// that four parts per row still fit in one wave of CTAs.
-int stream_parts(long long R, long long slots, int V, int VW) {
-  const long long chunks = (V / VW) / ((long long)sv::kStU * sv::kSt);
-  if (R <= 0 || chunks < 2) return 1;
-  if (chunks >= 4 && R * 4 <= slots) return 4;
-  return 2;
-}
-
-// Sets p.H (parts per row), which the kernel that merges the partials reads too.
+// Dense streaming kernel: every CTA streams the same number of vectors (the
+// flattened rows split evenly, sv_stream.cuh).  Sets p.SG (the grid), p.NVT,
+// p.VWs and p.H (partial slots per row: a power of two at least the number of
+// CTAs that can share a row), which the kernels that merge the partials read.
 template <typename T, int MODE>
 sv_status launch_stream_dense(sv::Params& p, cudaStream_t stream) {
   auto kern = sv::stream_dense_kernel<T, MODE>;
@@ -317,16 +318,24 @@ sv_status launch_stream_dense(sv::Params& p, cudaStream_t stream) {
   }
   // rows streamed: the target's, then (q formed from the draft's logits) the draft's
   const long long R = (long long)p.B * (p.gamma + 1) + (p.ql ? (long long)p.B * p.gamma : 0);
+  const int VW = sizeof(T) == 4 ? 4 : 8;
+  const long long NV = p.V / VW;
+  const long long NVT = R * NV;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sv::kSt, smem) != cudaSuccess || per_sm < 1) {
     cudaGetLastError();
     per_sm = 1;
   }
-  const long long slots = (long long)per_sm * sm_count();
-  p.H = stream_parts(R, slots, p.V, sizeof(T) == 4 ? 4 : 8);
-  // whole rows: every CTA takes the same number of rows; parts: at most one
-  // CTA per slot, items dealt round-robin
-  const long long grid = p.H == 1 ? stream_grid(kern, smem, R) : std::min(R * p.H, slots);
+  const long long chunk = (long long)sv::kStU * sv::kSt;
+  long long grid = std::min((long long)per_sm * sm_count(), ceil_div(NVT, chunk));
+  // at most 4 CTAs share a row: every range at least ceil(NV / 3) vectors long
+  grid = std::max(1ll, std::min(grid, NVT / ceil_div(NV, 3)));
+  const long long L = NVT / grid;                       // shortest range
+  const long long segs = ceil_div(NV, std::max(L, 1ll)) + 1;
+  p.H = segs <= 1 ? 1 : (segs <= 2 ? 2 : 4);
+  p.SG = (int)grid;
+  p.NVT = NVT;
+  p.VWs = VW;
   kern<<<(unsigned)grid, sv::kSt, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -383,15 +392,20 @@ sv_status dispatch(sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
     g_last_kernels = streamable ? "stream_topk_kernel" : "rows_kernel";
   } else {
     st = streamable ? launch_stream_dense<T, sv::MODE_SOFTMAX>(p, stream) : launch_rows<T, sv::MODE_SOFTMAX>(p, stream);
-    g_last_kernels = streamable ? "stream_dense_kernel,residual_kernel" : "rows_kernel,residual_kernel";
+    g_last_kernels = streamable ? "stream_dense_kernel,final_draw_kernel,final_pick_kernel"
+                                  : "rows_kernel,final_draw_kernel,final_pick_kernel";
   }
   if (st != SV_OK) {
     g_last_kernels = "";
     return st;
   }
   timing_record(1, stream);
-  if (mode == sv::MODE_SOFTMAX) st = launch_residual<T>(p, stream);
-  else if (mode == sv::MODE_GREEDY && streamable) st = launch_greedy_finish(p, stream);
+  if (mode == sv::MODE_SOFTMAX) {
+    if (!streamable) p.H = 0;   // the rows kernel leaves merged statistics
+    st = launch_final_draw<T>(p, stream);
+  } else if (mode == sv::MODE_GREEDY && streamable) {
+    st = launch_greedy_finish(p, stream);
+  }
   timing_record(2, stream);
   return st;
 }
@@ -402,7 +416,6 @@ sv_status run(sv::Params& p, sv_dtype dt, int mode, void* workspace, size_t work
   if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return SV_ERR_WORKSPACE;
   bind_workspace(p, L, workspace);
   choose_slices(p, dt, mode == sv::MODE_TOPK);
-  if (mode == sv::MODE_SOFTMAX) choose_chunks(p);
   switch (dt) {
     case SV_DTYPE_F32: return dispatch<float>(p, mode, stream, dt);
     case SV_DTYPE_BF16: return dispatch<__nv_bfloat16>(p, mode, stream, dt);

@@ -157,12 +157,12 @@ __device__ __forceinline__ uint64_t cluster_sweep16(const T* L, const float* Q, 
       if (near) tv |= 1u << t;
       RunAcc::acc2(acc->sh, acc->sl, w, 0.f);
       if (USE_Q) {
-        // on the residual support {w > s' q}: w - s' q and q, else 0 (adding
-        // 0 leaves both sums as they were)
+        // on the residual support {w > s' q} (the sign of w - s' q rounded
+        // once): w - s' q and q, else 0 (adding 0 leaves both sums as they were)
         const float qt = (j * VW + t == xq) ? INFINITY : qv[t];
-        const bool sup = w > s_a * qt;
-        RunAcc::acc2(acc->ah, acc->al, sup ? fmaf(-s_a, qt, w) : 0.f, 0.f);
-        acc->q += sup ? qt : 0.f;
+        const float d = fmaf(-s_a, qt, w);
+        RunAcc::acc2(acc->ah, acc->al, d > 0.f ? d : 0.f, 0.f);
+        acc->q += d > 0.f ? qt : 0.f;
       }
     }
     top |= (uint64_t)tv << (j * VW);
@@ -405,7 +405,7 @@ cluster_kernel(const ClusterParams cp) {
   }
 
   // ---- final draw: residual of row n, or the bonus from row gamma
-  // (precise weights and the (S, A, Q) decomposition, as in residual_kernel;
+  // (precise weights and the (S, A, Q) decomposition, as in final_draw_kernel;
   // thread t of a CTA owns the run of EPT tokens at t * EPT of its slice)
   const bool resid = n < gb;
   const bool bad = (sm.status & SEQ_BADROW) != 0;

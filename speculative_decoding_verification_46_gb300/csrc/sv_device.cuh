@@ -20,11 +20,7 @@
 //                    ticket, no CTA ever waits) merges the partials and runs the
 //                    acceptance scan.  In top-k mode a per-row ticket first
 //                    merges the per-slice candidate lists of a row.
-//   residual_kernel  (untruncated sampling) one CTA per (sequence, chunk) of
-//                    the one row each sequence draws from: chunk masses of
-//                    max(p - q, 0) (or p for the bonus), then the last CTA of the
-//                    sequence locates the inverse-CDF step chunk -> thread ->
-//                    token with the same two-float partial sums.
+//   (untruncated sampling's final draw: sv_final.cuh)
 //
 // Data problems never trap: they set per-sequence status bits.  There are no
 // spin-waits: cross-CTA hand-off is only "last arriving CTA continues".
@@ -45,7 +41,6 @@ constexpr int kMaxU = 8;          // 16-byte vectors per thread per slice
 constexpr int kCandCap = 2048;    // top-k candidate buffer (entries) per CTA
 constexpr int kMaxK = 1024;       // largest top-k list
 constexpr int kMaxG1 = 65;        // gamma + 1 <= 65
-constexpr int kResMaxEPT = 32;    // residual kernel: elements per thread (max)
 
 // per-sequence status bits (same values as the public header)
 constexpr int SEQ_OOB = 1;
@@ -57,16 +52,21 @@ struct SeqState {
   int n;          // accepted count
   int status;     // SEQ_* bits gathered so far
   float M;        // max logit of the row the final draw uses
-  int pad;
-  double s;       // sum_v 2^((L_v - M) c) of that row
+  float qm;       // q formed from the draft's logits: that row's maximum,
+  double s;       // sum_v 2^((L_v - M) c) of the row the final draw uses
+  float qinv;     // 1 / its sum of 2^((x - qm) c),
+  int qbad;       // and whether it defines no distribution
 };
 
 struct Params {
   int B, gamma, V;
   int S, U, SL;          // rows kernel: slices per row, vectors per thread, slice length
-  int C, CL, EPT;        // residual kernel: chunks per row, chunk length, elements per thread
+  int FC;                // final draw: 512-token items per row
   int top_k;             // top-k list length (top-k mode)
-  int H;                 // streaming kernel: parts per row (1: whole rows)
+  int H;                 // streaming kernel: partial slots (segments) per row, 1, 2 or 4
+  int SG;                // streaming kernel: its grid (CTA j streams vectors [j NVT / SG, (j+1) NVT / SG))
+  int VWs;               // streaming kernel: elements per 16-byte vector
+  long long NVT;         // streaming kernel: vectors of all its rows
   float top_p;
   float c;               // log2(e) / temperature (rounded to float)
   float c_lo;            // log2(e) / temperature - c
@@ -87,7 +87,8 @@ struct Params {
   float4* part;                   // [R][S] per-slice partials
   unsigned long long* lists;      // [R][S][top_k] per-slice top-k candidates
   int2* rowres;                   // [R][top_k + 1] kept (index, probability) lists
-  float2* chunk_mass;             // [B][3][C] residual chunk sums (S, A, Q; two-float)
+  float4* fd_part;                // [B][FC] final-draw item sums (S, A as two-float pairs)
+  float* fd_q;                    // [B][FC] final-draw item sums of q over the residual support
   const int* gamma_b;             // [B] drafts per sequence (ragged rounds), or nullptr: gamma
   const void* ql;                 // [B][gamma][V] draft logits (same dtype as logits) when q is formed
                                   // from them in the streaming path, else nullptr
@@ -795,8 +796,10 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
       st.n = n;
       st.status = status;
       st.M = sm.M[n];
-      st.pad = 0;
+      st.qm = 0.f;
       st.s = sm.s[n];
+      st.qinv = 0.f;
+      st.qbad = 0;
       p.seq[b] = st;
     }
     sm.n = n;
@@ -1293,10 +1296,10 @@ __device__ __forceinline__ F2x3 block_sum_f2x3_w0(F2x3 v, F2x3* sm) {
 
 // ------------------------------------------------------------------ final draw
 //
-// Both final-draw paths (residual_kernel below, and the cluster kernel) give
-// each thread a run of consecutive tokens, so the inverse-CDF search goes
-// (chunk or CTA slice) -> thread -> token, every level contiguous in token
-// order.
+// The cluster kernel's final draw gives each thread a run of consecutive
+// tokens, so its inverse-CDF search goes CTA slice -> thread -> token, every
+// level contiguous in token order (the grid path's, in sv_final.cuh, goes
+// item -> 4-token group -> token).
 //
 // Precision.  This is the one row per sequence whose inverse CDF is compared
 // step by step with a float64 reference over up to ~10^5 steps.  A token's
@@ -1379,9 +1382,11 @@ __device__ __forceinline__ bool run_tail_t(RunAcc& acc, float x, float qv, float
   const float w = (top || !(p > -1e30f)) ? 0.f : fmaf(y * 6.931471825e-01f, e, y);
   RunAcc::acc2(acc.sh, acc.sl, w, 0.f);
   if (USE_Q) {
-    const float pr = s_a * qv;
-    if (w > pr) {
-      RunAcc::acc2(acc.ah, acc.al, fmaf(-s_a, qv, w), 0.f);
+    // on the residual support {w > s' q}: w - s' q, rounded once (its sign
+    // is the exact difference's sign), and q
+    const float d = fmaf(-s_a, qv, w);
+    if (d > 0.f) {
+      RunAcc::acc2(acc.ah, acc.al, d, 0.f);
       acc.q += qv;
     }
   }
@@ -1416,299 +1421,41 @@ __device__ __forceinline__ F2 token_mass(float x, float qv, bool use_q, float M,
   return m;
 }
 
-// Per-thread staging of a run in shared memory, thread-interleaved:
-// kResStageVec(T) logits vectors then kResStageQ q vectors per thread.
-template <typename T>
-struct ResStage {
-  static constexpr int VW = Tr<T>::VW;
-  static constexpr int NL = kResMaxEPT / VW;    // 16-byte logits vectors per run
-  static constexpr int NQ = kResMaxEPT / 4;     // 16-byte q vectors per run
-  static constexpr size_t bytes = (size_t)(NL + NQ) * kThreads * sizeof(uint4);
-};
-
-__device__ __forceinline__ void res_cp16(void* smem, const void* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-
-// The branch-free tail sweep over a staged run (see run_accumulate): USE_Q
-// for a residual row, DET when q is a deterministic draft's one-hot (q = +inf
-// at token xq takes it out of the support, q = 0 elsewhere).  Returns the
-// bit mask of run offsets near the row maximum, left to run_top.
-template <typename T, bool USE_Q, bool DET, bool QL = false>
-__device__ __forceinline__ uint32_t run_sweep(const uint4* lg, const uint4* qq, bool have_q, int xq, int e0, int j0,
-                                              int j1, int V, float M, float c, float c_lo, float s_a, RunAcc* acc,
-                                              QLrow qlr = QLrow{0.f, 0.f, true}) {
-  constexpr int VW = Tr<T>::VW;
-  constexpr bool EXACT = sizeof(T) == 2;
-  const int tid = threadIdx.x;
-  uint32_t top = 0u;
-#pragma unroll 1
-  for (int j = j0; j < j1; ++j) {
-    const uint4 v = lg[j * kThreads + tid];
-    float qv[VW];
-    if (QL) {
-      // q from the staged draft logits (one 16-byte vector per VW tokens)
-      const uint4 qx = qq[j * kThreads + tid];
-#pragma unroll
-      for (int t = 0; t < VW; ++t) qv[t] = qlr.q(Tr<T>::get(qx, t), c, c_lo);
-    } else {
-#pragma unroll
-      for (int h = 0; h < VW / 4; ++h) {
-        if (USE_Q && have_q) {
-          const uint4 q4 = qq[(j * (VW / 4) + h) * kThreads + tid];
-          qv[4 * h + 0] = __uint_as_float(q4.x);
-          qv[4 * h + 1] = __uint_as_float(q4.y);
-          qv[4 * h + 2] = __uint_as_float(q4.z);
-          qv[4 * h + 3] = __uint_as_float(q4.w);
-        } else {
-          qv[4 * h + 0] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
-        }
-      }
-    }
-    const int ev = e0 + j * VW;
-    const int lim = V - ev;          // tokens of this vector inside the row
-    const int xo = xq - ev;          // the one-hot token's offset (DET)
-    if (EXACT) {
-      // 16-bit logits (x - M exact): every token takes the same branch-free
-      // steps; a token near the maximum (p > -8) adds nothing here and is
-      // flagged for run_top.  -inf is clamped to an exponent that ex2.approx
-      // flushes to 0 (as any exponent below -126); tokens past the row's end
-      // weigh 0 (their q is 0 too).
-      uint32_t tv = 0u;
-#pragma unroll
-      for (int t = 0; t < VW; ++t) {
-        const float dh = fmaxf(Tr<T>::get(v, t) - M, -1.0e4f);
-        const float p = dh * c;
-        const float e = fmaf(dh, c_lo, fmaf(dh, c, -p));
-        const float y = ex2_approx(p);
-        const bool in = t < lim;
-        const bool near = p > -8.f;
-        const float w = (in && !near) ? fmaf(y * 6.931471825e-01f, e, y) : 0.f;
-        if (in && near) tv |= 1u << t;
-        RunAcc::acc2(acc->sh, acc->sl, w, 0.f);
-        if (USE_Q) {
-          // on the residual support {w > s' q}: w - s' q and q, else 0 (adding
-          // 0 leaves both sums as they were; selects, not a branch per token)
-          const float qt = (DET && t == xo) ? INFINITY : qv[t];
-          const bool sup = w > s_a * qt;
-          RunAcc::acc2(acc->ah, acc->al, sup ? fmaf(-s_a, qt, w) : 0.f, 0.f);
-          acc->q += sup ? qt : 0.f;
-        }
-      }
-      top |= tv << (j * VW);
-      continue;
-    }
-    uint32_t tv = 0u;
-#pragma unroll
-    for (int t = 0; t < VW; ++t) {
-      const float qt = (DET && t == xo) ? INFINITY : qv[t];
-      if (t < lim && run_tail_t<EXACT, USE_Q>(*acc, Tr<T>::get(v, t), qt, M, c, c_lo, s_a)) tv |= 1u << t;
-    }
-    top |= tv << (j * VW);
-  }
-  return top;
-}
-
-// (S, A, Q) of the run [e0, e0 + NS * VW) of the final-draw row (tokens >= V
-// are skipped).  The whole run is copied into this thread's slots of `stage`
-// first (all copies in flight at once), then walked by a rolled loop.
-template <typename T>
-__device__ __forceinline__ void run_accumulate(const T* row, const float* qrow, int xq, int e0, int NS, int V,
-                                               bool vec_ok,
-                                               bool use_q, float M, float c, float c_lo, float s_a, uint4* stage,
-                                               RunAcc* acc, const float* tab, const T* qlrow = nullptr,
-                                               QLrow qlr = QLrow{0.f, 0.f, true}) {
-  using RS = ResStage<T>;
-  constexpr int VW = RS::VW;
-  constexpr bool EXACT = sizeof(T) == 2;
-  const int tid = threadIdx.x;
-  uint4* lg = stage;
-  uint4* qq = stage + RS::NL * kThreads;
-  // two copy groups: the first half of the run is swept while the second lands
-  const int NH = (NS + 1) >> 1;
-  for (int j = 0; j < NS; ++j) {
-    const int e = e0 + j * VW;
-    const int nv = min(max(V - e, 0), VW);
-    if (nv == VW && vec_ok) {
-      res_cp16(lg + j * kThreads + tid, row + e);
-      if (qlrow) {
-        res_cp16(qq + j * kThreads + tid, qlrow + e);   // the draft's logits: one vector per VW tokens
-      } else if (qrow) {
-#pragma unroll
-        for (int h = 0; h < VW / 4; ++h) res_cp16(qq + (j * (VW / 4) + h) * kThreads + tid, qrow + e + 4 * h);
-      }
-    } else {
-      lg[j * kThreads + tid] = load_slot<T>(row, e, max(nv, 0), vec_ok && nv == VW);
-      if (qlrow) {
-        qq[j * kThreads + tid] = load_slot<T>(qlrow, e, max(nv, 0), vec_ok && nv == VW);
-      } else if (qrow) {
-#pragma unroll
-        for (int h = 0; h < VW / 4; ++h) {
-          float4 q4;
-          q4.x = (4 * h + 0 < nv) ? __ldg(qrow + e + 4 * h + 0) : 0.f;
-          q4.y = (4 * h + 1 < nv) ? __ldg(qrow + e + 4 * h + 1) : 0.f;
-          q4.z = (4 * h + 2 < nv) ? __ldg(qrow + e + 4 * h + 2) : 0.f;
-          q4.w = (4 * h + 3 < nv) ? __ldg(qrow + e + 4 * h + 3) : 0.f;
-          qq[(j * (VW / 4) + h) * kThreads + tid] = *reinterpret_cast<const uint4*>(&q4);
-        }
-      }
-    }
-    if (j == NH - 1) asm volatile("cp.async.commit_group;" ::: "memory");
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  // tail tokens in one branch-free sweep (specialised for the residual /
-  // bonus rows, for q formed from the draft's logits and for a deterministic
-  // draft's one-hot q); tokens near the maximum (bit set in `top`) in a
-  // second loop
-  auto sweep = [&](int j0, int j1) -> uint32_t {
-    if (!use_q) return run_sweep<T, false, false>(lg, qq, qrow != nullptr, xq, e0, j0, j1, V, M, c, c_lo, s_a, acc);
-    if (qlrow) return run_sweep<T, true, false, true>(lg, qq, true, -1, e0, j0, j1, V, M, c, c_lo, s_a, acc, qlr);
-    if (xq < 0) return run_sweep<T, true, false>(lg, qq, qrow != nullptr, xq, e0, j0, j1, V, M, c, c_lo, s_a, acc);
-    return run_sweep<T, true, true>(lg, qq, qrow != nullptr, xq, e0, j0, j1, V, M, c, c_lo, s_a, acc);
-  };
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
-  uint32_t top = sweep(0, NH);
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  top |= sweep(NH, NS);
-  while (top) {
-    const int o = __ffs(top) - 1;   // offset in the run
-    top &= top - 1;
-    const int j = o / VW, t = o - j * VW;
-    const float x = Tr<T>::get(lg[j * kThreads + tid], t);
-    const float qv =
-        (e0 + o == xq) ? INFINITY
-        : qlrow        ? qlr.q(Tr<T>::get(qq[j * kThreads + tid], t), c, c_lo)
-        : qrow         ? __uint_as_float(word_of(qq[(j * (VW / 4) + t / 4) * kThreads + tid], t & 3))
-                       : 0.f;
-    run_top<EXACT>(*acc, x, qv, use_q, M, c, c_lo, s_a, tab);
-  }
-}
-
-// Warp 0 of the finishing CTA: the chunk sums (S, A, Q) of one sequence read
-// once into registers (C <= kPickChunks), the exact normaliser s, the masses
-// (A - (s - s') Q for a residual, S for the bonus) and the inverse-CDF step
-// over the chunks: the first chunk whose [prefix, prefix + mass) holds
-// u * R, else the last chunk with positive mass.  Both passes add in the same
-// order (32-chunk groups, a two-float scan per group, a running carry).
-constexpr int kPickGroups = 4;
-constexpr int kPickChunks = 32 * kPickGroups;
-
-struct ChunkPick {
-  int sub;        // chosen chunk, -1 if none
-  int resid0;     // the residual had no mass: drawn from p_n instead
-  F2 base, target, ds;
-};
-
-__device__ __forceinline__ ChunkPick chunk_pick_w0(const F2* cS, const F2* cA, const F2* cQ, int C, bool resid,
-                                                   bool bad, float s_a, float u) {
-  const int lane = threadIdx.x & 31;
-  const int NG = (C + 31) >> 5;   // groups holding chunks; the others are all zero and skipped
-  F2 Sg[kPickGroups], Mg[kPickGroups];
-  float Qg[kPickGroups];
-#pragma unroll
-  for (int g = 0; g < kPickGroups; ++g) {
-    const int k = g * 32 + lane;
-    Sg[g] = Mg[g] = F2{0.f, 0.f};
-    Qg[g] = 0.f;
-    if (k < C) {
-      const float2 sv = __ldcg(reinterpret_cast<const float2*>(cS) + k);
-      Sg[g] = F2{sv.x, sv.y};
-      if (resid) {
-        const float2 av = __ldcg(reinterpret_cast<const float2*>(cA) + k);
-        Mg[g] = F2{av.x, av.y};
-        Qg[g] = __ldcg(reinterpret_cast<const float2*>(cQ) + k).x;
-      }
-    }
-  }
-  F2 sl = Sg[0];
-#pragma unroll
-  for (int g = 1; g < kPickGroups; ++g)
-    if (g < NG) sl = f2_add(sl, Sg[g]);
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) sl = f2_add(sl, f2_shfl_xor(sl, m));
-  ChunkPick r;
-  r.ds = f2_add(sl, F2{-s_a, 0.f});          // s - s', tiny
-  r.resid0 = 0;
-#pragma unroll
-  for (int g = 0; g < kPickGroups; ++g) {
-    if (resid) {
-      Mg[g] = f2_add(Mg[g], f2_neg(f2_scale(r.ds, Qg[g])));
-      if (Mg[g].hi < 0.f) Mg[g] = F2{0.f, 0.f};
-    } else {
-      Mg[g] = Sg[g];
-    }
-  }
-  // inclusive prefix of the masses (group scans chained by a carry), kept for
-  // the search below
-  F2 inc[kPickGroups], cin[kPickGroups];
-  auto scan = [&]() {
-    F2 carry{0.f, 0.f};
-#pragma unroll
-    for (int g = 0; g < kPickGroups; ++g) {
-      cin[g] = carry;
-      if (g < NG) {
-        inc[g] = f2_add(carry, warp_incl_scan_f2(Mg[g]));
-        carry = F2{__shfl_sync(0xffffffffu, inc[g].hi, 31), __shfl_sync(0xffffffffu, inc[g].lo, 31)};
-      }
-    }
-    return carry;
-  };
-  F2 R = scan();
-  if (resid && !bad && !f2_pos(R)) {
-    r.resid0 = 1;   // zero residual mass (only through rounding): draw from p_n instead
-#pragma unroll
-    for (int g = 0; g < kPickGroups; ++g) Mg[g] = Sg[g];
-    R = scan();
-  }
-  r.target = f2_scale(R, u);
-  int found = -1, last = -1;
-  F2 fbase{0.f, 0.f}, lbase{0.f, 0.f};
-#pragma unroll
-  for (int g = 0; g < kPickGroups; ++g) {
-    if (g >= NG) break;
-    F2 excl = f2_shfl_up(inc[g], 1);
-    if (lane == 0) excl = cin[g];
-    const bool live = g * 32 + lane < C && f2_pos(Mg[g]);
-    const unsigned hit =
-        __ballot_sync(0xffffffffu, live && !f2_lt(r.target, excl) && f2_lt(r.target, f2_add(excl, Mg[g])));
-    const unsigned pos = __ballot_sync(0xffffffffu, live);
-    if (hit && found < 0) {
-      const int l = __ffs(hit) - 1;
-      found = g * 32 + l;
-      fbase = F2{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
-    }
-    if (pos) {
-      const int l = 31 - __clz(pos);
-      last = g * 32 + l;
-      lbase = F2{__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
-    }
-  }
-  r.sub = (bad || !f2_pos(R)) ? -1 : (found >= 0 ? found : last);
-  r.base = found >= 0 ? fbase : lbase;
-  return r;
-}
-
 // ---- streaming-path row statistics
-// The streaming kernel leaves one partial per warp per row part: slot
-// (row * H + h) * kWarps + warp holds (max, first index) of that warp's
-// vectors (greedy) or (max M_w, sum of 2^((L - M_w) c) as two floats)
-// (sampling).  A row's NP = H * kWarps slots are contiguous, so sequence b's
-// G1 rows occupy slots [b * G1 * NP, (b + 1) * G1 * NP).  NP divides 32: one
-// aligned lane segment merges one row.
-__device__ __forceinline__ int stream_np(const Params& p) { return p.H * kWarps; }
+// The streaming kernel leaves one partial per row segment (the part of a row
+// one CTA streamed): slot row * H + h holds (max, first index) of the
+// segment (greedy) or (max M_h, sum of 2^((L - M_h) c) as two floats)
+// (sampling); slots past the row's last segment stay empty (seg_valid).  A
+// row's NP = H slots are contiguous, so sequence b's G1 rows occupy slots
+// [b * G1 * NP, (b + 1) * G1 * NP).  NP (1, 2 or 4) divides 32: one aligned
+// lane segment merges one row.
+__device__ __forceinline__ int stream_np(const Params& p) { return p.H; }
+
+// The CTA holding vector x of the flattened space: the largest j with
+// start(j) <= x.
+__device__ __forceinline__ int seg_cta(long long x, long long NVT, int grid) {
+  return (int)(((x + 1) * (long long)grid - 1) / NVT);
+}
+// Valid partial slot `seg` of row r (segments past the row's last CTA stay
+// empty): the merges skip the others.
+__device__ __forceinline__ bool seg_valid(const Params& p, long long r, int seg) {
+  const long long NV = p.V / p.VWs;
+  const long long NVT = p.NVT;
+  return seg < seg_cta((r + 1) * NV - 1, NVT, p.SG) - seg_cta(r * NV, NVT, p.SG) + 1;
+}
+
 
 // base: the first of the nrow rows' partial slots (sequence b's rows are
 // contiguous).  sBad[i] = the row defines no distribution (greedy: a NaN), for
 // i <= gb only when mask_gb.
 template <int MODE>
-__device__ __forceinline__ void merge_row_parts_at(const Params& p, const float4* base, int G1, int gb, bool mask_gb,
-                                                   float* sM, double* sS, int* sG, int* sBad) {
+__device__ __forceinline__ void merge_row_parts_at(const Params& p, const float4* base, long long r0, int G1, int gb,
+                                                   bool mask_gb, float* sM, double* sS, int* sG, int* sBad) {
   const int NP = stream_np(p);
   const int E = G1 * NP;
   for (int e0 = 0; e0 < E; e0 += kThreads) {        // uniform over the block: every lane shuffles
     const int e = e0 + (int)threadIdx.x;
-    const bool ok = e < E;
+    const bool ok = e < E && seg_valid(p, r0 + e / NP, e % NP);
     const float4 v = ok ? __ldcg(base + e) : make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.f, 0.f);
     const bool head = ok && (e % NP) == 0;
     const int i = e / NP;
@@ -1746,7 +1493,8 @@ __device__ __forceinline__ void merge_row_parts_at(const Params& p, const float4
 template <int MODE>
 __device__ __forceinline__ void merge_row_parts(const Params& p, int b, int G1, int gb, float* sM, double* sS,
                                                 int* sG, int* sBad) {
-  merge_row_parts_at<MODE>(p, p.part + (size_t)b * G1 * stream_np(p), G1, gb, true, sM, sS, sG, sBad);
+  merge_row_parts_at<MODE>(p, p.part + (size_t)b * G1 * stream_np(p), (long long)b * G1, G1, gb, true, sM, sS, sG,
+                           sBad);
 }
 
 
@@ -1764,291 +1512,6 @@ __device__ __forceinline__ int first_flag_w0(const int* flags, int count, const 
   }
   *any2 = a2;
   return first;
-}
-
-struct ResSmem {
-  float tab[128];   // exp2_f2 table
-  F2x3 red[kWarps];
-  F2 f2red[kWarps];
-  int flag;
-  int sub;        // selected chunk, -1 if none
-  int token;
-  int use_q;
-  int owner;      // thread whose run holds the target
-  int lastpos;    // last thread with a positive mass
-  F2 target;
-  F2 base;
-  F2 tbase;       // the owner's exclusive prefix
-  F2 ds;
-  LocateSmem loc;
-  // streaming path: the sequence's row statistics and acceptance scan
-  float rM[kMaxG1];
-  double rS[kMaxG1];
-  int rBad[kMaxG1];
-  int rRej[kMaxG1];
-  float qM[kMaxG1];      // draft rows (q from the draft's logits): maximum, sum, no distribution
-  double qS[kMaxG1];
-  int qBad[kMaxG1];
-  int rStatus;
-  int rN;
-};
-
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-residual_kernel(const Params p) {
-  using TR = Tr<T>;
-  constexpr int VW = TR::VW;
-  __shared__ ResSmem sm;
-  extern __shared__ __align__(16) unsigned char res_dyn[];
-  uint4* stage = reinterpret_cast<uint4*>(res_dyn);   // ResStage<T>::bytes
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int C = p.C;
-  const int c = blockIdx.x % C;
-  const int b = blockIdx.x / C;
-  const int G = p.gamma, G1 = G + 1, V = p.V, EPT = p.EPT;
-  const int NS = EPT / VW;                // vectors per thread run
-  const int gb = seq_gamma(p, b);
-  const bool from_parts = p.H > 0;        // streaming path: per-warp row partials
-  // independent of the previous kernel, so before the wait: the exp2 table and,
-  // for the streaming path, thread i's draft d_i, its logit, q_i(d_i) and u_i
-  load_exp2_table(sm.tab);
-  const float u_fin = __ldg(p.uniforms + b * G1 + gb);   // the final draw's uniform (last CTA)
-  int d_i = -1;
-  float l_d = 0.f, q_d = 0.f, u_i = 0.f, ql_d = 0.f;
-  const T* qlb = p.ql ? static_cast<const T*>(p.ql) + (size_t)b * G * V : nullptr;   // this sequence's draft logits
-  if (from_parts && tid < gb) {
-    d_i = __ldg(p.draft + b * G + tid);
-    u_i = __ldg(p.uniforms + b * G1 + tid);
-    if (d_i >= 0 && d_i < V) {
-      l_d = TR::get(load_slot<T>(static_cast<const T*>(p.logits) + ((size_t)b * G1 + tid) * V, d_i, 1, false), 0);
-      if (qlb)
-        ql_d = TR::get(load_slot<T>(qlb + (size_t)tid * V, d_i, 1, false), 0);
-      else
-        q_d = p.q ? __ldg(p.q + ((size_t)b * G + tid) * V + d_i) : 1.f;   // NULL: one-hot draft
-    }
-  }
-  pdl_wait();
-  SeqState st;
-  if (from_parts) {
-    // merge the row partials, accept/reject, scan (every CTA of the sequence
-    // computes the same values; chunk 0 writes the per-draft outputs)
-    merge_row_parts<MODE_SOFTMAX>(p, b, G1, gb, sm.rM, sm.rS, nullptr, sm.rBad);
-    if (qlb)   // the draft rows' statistics: q_i = 2^((x - m_i) c) / s_i
-      merge_row_parts_at<MODE_SOFTMAX>(p, p.qpart + (size_t)b * G * stream_np(p), G, gb, false, sm.qM, sm.qS, nullptr,
-                                       sm.qBad);
-    if (tid == 0) sm.rStatus = 0;
-    __syncthreads();
-    float a = 0.f;
-    if (qlb && tid < gb && d_i >= 0 && d_i < V)
-      q_d = sm.qBad[tid] ? 0.f : q_weight(ql_d, sm.qM[tid], p.c, p.c_lo) * (float)(1.0 / sm.qS[tid]);
-    if (tid < gb) {
-      int bits = 0;
-      const float ssum = (float)sm.rS[tid];
-      if (d_i < 0 || d_i >= V) {
-        bits |= SEQ_OOB;
-      } else {
-        const float pd = sm.rBad[tid] ? 0.f : exp2f((l_d - sm.rM[tid]) * p.c) / ssum;
-        if (q_d > 0.f) {
-          a = fminf(1.f, pd / q_d);
-        } else {
-          a = pd > 0.f ? 1.f : 0.f;
-          bits |= SEQ_QBAD;
-        }
-      }
-      sm.rRej[tid] = !(u_i < a);
-      if (bits) atomicOr(&sm.rStatus, bits);
-    }
-    __syncthreads();
-    if (tid < 32) {
-      bool anybad = false;
-      const int n0 = first_flag_w0(sm.rRej, gb, sm.rBad, gb, &anybad);
-      if (tid == 0) {
-        sm.rN = n0;
-        if (anybad) sm.rStatus |= SEQ_BADROW;
-      }
-    }
-    __syncthreads();
-    st.n = sm.rN;
-    st.status = sm.rStatus;
-    st.M = sm.rM[st.n];
-    st.s = sm.rS[st.n];
-    if (c == 0) {
-      if (tid == 0) p.out_n[b] = st.n;
-      if (p.out_a && tid < G) p.out_a[b * G + tid] = tid < gb ? a : 0.f;
-      if (tid < G1 && tid != st.n) p.out_tokens[b * G1 + tid] = tid < st.n ? d_i : -1;
-    }
-  } else {
-    st.n = __ldcg(&p.seq[b].n);
-    st.status = __ldcg(&p.seq[b].status);
-    st.M = __ldcg(&p.seq[b].M);
-    st.s = __ldcg(&p.seq[b].s);
-  }
-  const int n = st.n;
-  const bool resid = n < gb;
-  const bool bad = (st.status & SEQ_BADROW) != 0;
-  const T* row = static_cast<const T*>(p.logits) + ((size_t)b * G1 + n) * V;
-  const float* qrow = (resid && p.q) ? p.q + ((size_t)b * G + n) * V : nullptr;
-  // q from the draft's logits: row n of them and its statistics
-  const T* qlrow = (resid && qlb) ? qlb + (size_t)n * V : nullptr;
-  QLrow qlr{0.f, 0.f, true};
-  if (qlrow) qlr = QLrow{sm.qM[n], (float)(1.0 / sm.qS[n]), sm.qBad[n] != 0};
-  // deterministic drafts (q == NULL): q_n is one-hot at d_n
-  const int xq = (resid && !p.q && !qlb) ? __ldg(p.draft + b * G + n) : -1;
-  const float M = st.M;
-  const float s_a = (float)st.s;
-  const bool vec_ok = (V % VW) == 0;
-  // per sequence: [S block | A block | Q block], C two-float entries each
-  F2* cS = reinterpret_cast<F2*>(p.chunk_mass) + (size_t)b * 3 * C;
-  F2* cA = cS + C;
-  F2* cQ = cA + C;
-
-  // ---- (S, A, Q) of this chunk
-  RunAcc acc;
-  acc.zero();
-  if (!bad)
-    run_accumulate<T>(row, qrow, xq, c * p.CL + tid * EPT, NS, V, vec_ok, resid, M, p.c, p.c_lo, s_a, stage, &acc,
-                      sm.tab, qlrow, qlr);
-  {
-    const F2x3 t = block_sum_f2x3_w0(F2x3{acc.S(), acc.A(), F2{acc.q, 0.f}}, sm.red);
-    if (tid == 0) {
-      cS[c] = t.a;
-      cA[c] = t.b;
-      cQ[c] = t.c;
-    }
-  }
-  if (!arrive_last(p.seq_ticket2 + b, C, &sm.flag, true)) return;
-
-  // ---- last CTA of sequence b: exact normaliser, masses, chunk -> thread -> token
-  int status = st.status;
-  const float u = u_fin;
-  if (C <= kPickChunks) {
-    if (tid < 32) {
-      const ChunkPick pk = chunk_pick_w0(cS, cA, cQ, C, resid, bad, s_a, u);
-      if (tid == 0) {
-        sm.sub = pk.sub;
-        sm.base = pk.base;
-        sm.target = pk.target;
-        sm.token = -1;
-        sm.use_q = resid && !pk.resid0;
-        sm.ds = pk.ds;
-        sm.owner = 0x7fffffff;
-        sm.lastpos = -1;
-        sm.flag = pk.resid0;
-      }
-    }
-    __syncthreads();
-    if (sm.flag) status |= SEQ_RESID0;
-  } else {
-    // many chunks (very large vocabularies): the block-wide search
-    F2 sl{0.f, 0.f};
-    for (int k2 = tid; k2 < C; k2 += kThreads) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(cS) + k2);
-      sl = f2_add(sl, F2{v.x, v.y});
-    }
-    const F2 s = block_sum_f2(sl, sm.f2red);
-    const F2 ds = f2_add(s, F2{-s_a, 0.f});          // s - s', tiny
-    if (resid) {
-      // residual masses A - (s - s') Q overwrite the A block
-      for (int k2 = tid; k2 < C; k2 += kThreads) {
-        const float2 a2 = __ldcg(reinterpret_cast<const float2*>(cA) + k2);
-        const float2 q2 = __ldcg(reinterpret_cast<const float2*>(cQ) + k2);
-        F2 m = f2_add(F2{a2.x, a2.y}, f2_neg(f2_mul(ds, F2{q2.x, q2.y})));
-        if (m.hi < 0.f) m = F2{0.f, 0.f};
-        cA[k2] = m;
-      }
-      __threadfence_block();
-      __syncthreads();
-    }
-    F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
-    bool use_q = resid;
-    int sub = locate(resid ? cA : cS, C, u, &R, &base, &tgt, sm.loc, true);
-    if (resid && !bad && !f2_pos(R)) {
-      // zero residual mass (only through rounding): draw from p_n instead
-      status |= SEQ_RESID0;
-      use_q = false;
-      sub = locate(cS, C, u, &R, &base, &tgt, sm.loc, true);
-    }
-    if (tid == 0) {
-      sm.sub = (bad || !f2_pos(R)) ? -1 : sub;
-      sm.base = base;
-      sm.target = tgt;
-      sm.token = -1;
-      sm.use_q = use_q;
-      sm.ds = ds;
-      sm.owner = 0x7fffffff;
-      sm.lastpos = -1;
-    }
-  }
-  __syncthreads();
-  int token = 0;
-  if (sm.sub >= 0) {
-    const bool uq = sm.use_q != 0;
-    const int c0 = sm.sub * p.CL;
-    RunAcc r;
-    r.zero();
-    run_accumulate<T>(row, uq ? qrow : nullptr, xq, c0 + tid * EPT, NS, V, vec_ok, uq, M, p.c, p.c_lo, s_a, stage,
-                      &r, sm.tab, uq ? qlrow : nullptr, qlr);
-    F2 mine = r.mass(uq, sm.ds);
-    if (mine.hi < 0.f) mine = F2{0.f, 0.f};
-    F2 total;
-    const F2 ex = block_exclusive_f2(mine, sm.f2red, &total);
-    const F2 tbase = f2_add(sm.base, ex);
-    const bool pos = f2_pos(mine);
-    if (pos && !f2_lt(sm.target, tbase) && f2_lt(sm.target, f2_add(tbase, mine))) atomicMin(&sm.owner, tid);
-    if (pos) atomicMax(&sm.lastpos, tid);
-    __syncthreads();
-    // rounding can leave no run above the target: take the last positive one
-    const bool take_last = sm.owner == 0x7fffffff;
-    const int owner = take_last ? sm.lastpos : sm.owner;
-    if (tid == owner) sm.tbase = tbase;
-    __syncthreads();
-    if (owner >= 0 && tid < 32) {
-      // warp 0 walks the owner's run, one token per lane (EPT <= 32)
-      const int e = c0 + owner * EPT + lane;
-      F2 m{0.f, 0.f};
-      if (lane < EPT && e < V) {
-        // the owner's run is still staged in shared memory (run_accumulate)
-        const int j = lane / VW, t = lane - j * VW;
-        const float x = TR::get(stage[j * kThreads + owner], t);
-        const float qv =
-            !uq    ? 0.f
-            : qlrow ? qlr.q(TR::get(stage[(ResStage<T>::NL + j) * kThreads + owner], t), p.c, p.c_lo)
-            : qrow  ? __uint_as_float(word_of(stage[(ResStage<T>::NL + j * (VW / 4) + t / 4) * kThreads + owner], t & 3))
-                    : (e == xq ? INFINITY : 0.f);
-        m = token_mass<sizeof(T) == 2>(x, qv, uq, M, p.c, p.c_lo, s_a, sm.ds, sm.tab);
-      }
-      const F2 inc = warp_incl_scan_f2(m);
-      F2 excl = f2_shfl_up(inc, 1);
-      if (lane == 0) excl = F2{0.f, 0.f};
-      const F2 lb = f2_add(sm.tbase, excl);
-      const bool live = f2_pos(m);
-      const unsigned hit = __ballot_sync(0xffffffffu, live && !take_last && !f2_lt(sm.target, lb) &&
-                                                          f2_lt(sm.target, f2_add(lb, m)));
-      const unsigned any = __ballot_sync(0xffffffffu, live);
-      const int pick = hit ? __ffs(hit) - 1 : (any ? 31 - __clz(any) : -1);
-      if (lane == 0) sm.token = pick >= 0 ? c0 + owner * EPT + pick : -1;
-    }
-    __syncthreads();
-    token = sm.token < 0 ? 0 : sm.token;
-  }
-  for (int k2 = tid; k2 < 3 * C; k2 += kThreads) cS[k2] = F2{0.f, 0.f};
-  if (from_parts) {
-    // every CTA of the sequence has read the row partials: zero them (the
-    // draft rows' too, when q is formed from the draft's logits)
-    const int E = G1 * stream_np(p);
-    for (int e = tid; e < E; e += kThreads) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (qlb) {
-      const int Eq = G * stream_np(p);
-      for (int e = tid; e < Eq; e += kThreads) p.qpart[(size_t)b * Eq + e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  if (tid == 0) {
-    p.out_tokens[b * G1 + n] = token;
-    if (p.out_status) p.out_status[b] = status;
-    SeqState z;
-    z.n = 0; z.status = 0; z.M = 0.f; z.pad = 0; z.s = 0.0;
-    p.seq[b] = z;
-  }
 }
 
 }  // namespace sv

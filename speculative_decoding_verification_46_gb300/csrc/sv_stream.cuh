@@ -10,18 +10,19 @@
 // finished.  The ring is private to the thread that filled it (the thread
 // copies and later reads its own slots), so completion is tracked per thread
 // with cp.async.wait_group: there are no cross-thread waits, no mbarriers and
-// no spin loops.  The dense kernel splits rows into H parts (2, or 4 for
-// small batches) dealt round-robin to one CTA per slot; the top-k kernel
-// claims whole rows from a counter as its CTAs get through them.  With q
-// formed from the draft's logits, the draft rows follow the target rows
-// through both kernels.
+// no spin loops.  The dense kernel gives every CTA the same number of
+// vectors (the rows laid end to end and cut into equal ranges, so a row may
+// be split between consecutive CTAs); the top-k kernel claims whole rows from
+// a counter as its CTAs get through them.  With q formed from the draft's
+// logits, the draft rows follow the target rows through both kernels.
 //
-//   greedy   per-warp argmax of each row part (ties -> lowest index; NaN
-//            flagged); stream_greedy_finish_kernel merges the parts, scans
-//            the drafts and emits the tokens
-//   softmax  per-warp online max / sum of 2^((L - m) c) with rescaling when
-//            the running max grows; residual_kernel merges the parts,
-//            computes p(d_i) and a_i, scans and makes the final draw
+//   greedy   argmax of each row segment (ties -> lowest index; NaN
+//            flagged); stream_greedy_finish_kernel merges the segments,
+//            scans the drafts and emits the tokens
+//   softmax  online max / sum of 2^((L - m) c) with rescaling when the
+//            running max grows; final_draw_kernel merges the segments,
+//            computes p(d_i) and a_i, scans and sums the final draw's items,
+//            final_pick_kernel locates the drawn token (sv_final.cuh)
 //   top-k    pass 1 keeps per-thread maxima (and the two best vectors); the
 //            k-th largest is a lower bound tau of the row's k-th value; only
 //            threads with a third vector reaching tau are re-read (L2);
@@ -31,8 +32,8 @@
 //            (atomic ticket, no waiting) runs the acceptance scan and the
 //            final draw.
 //
-// The dense kernel ends a row part with warp shuffles and one store per warp:
-// no block barrier, so no warp waits for another between rows.
+// The dense kernel ends a row segment with warp shuffles and one block
+// barrier (a CTA ends at most H + 1 segments); chunks in between take none.
 #pragma once
 
 #include "sv_device.cuh"
@@ -55,10 +56,12 @@ __device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_gro
 template <int N>
 __device__ __forceinline__ void cpa_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// The dense streaming kernel keeps no block-wide state: each warp ends a row
-// part on its own (shuffles and one store).
+// The dense streaming kernel's block-wide state: the warps' partials at the
+// end of a segment, double-buffered by segment parity (so that one barrier
+// per segment suffices: warp 0 has read buffer k before it reaches segment
+// k + 1's barrier, after which buffer k is written again at segment k + 2).
 struct StreamSmem {
-  int unused;
+  float4 red[2][kWarps];
 };
 
 // Per-thread sequence of ring items: (j-th row of this CTA, pass, chunk c),
@@ -163,11 +166,34 @@ __global__ void __launch_bounds__(kSt) stream_greedy_finish_kernel(const Params 
   for (int e = tid; e < E; e += kSt) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Maximum of the kStU vectors x (NaN-free: the softmax path treats NaN rows
+// through the merged statistics), 16-bit types reduced as packed pairs.
+template <typename T>
+__device__ __forceinline__ float chunk_max(const uint4 (&x)[kStU]) {
+  using TR = Tr<T>;
+  if constexpr (TR::VW == 8) {
+    using H2 = typename std::conditional<std::is_same<T, __half>::value, __half2, __nv_bfloat162>::type;
+    H2 acc = *reinterpret_cast<const H2*>(&x[0].x);
+#pragma unroll
+    for (int u = 0; u < kStU; ++u) {
+      const H2 a = *reinterpret_cast<const H2*>(&x[u].x), b = *reinterpret_cast<const H2*>(&x[u].y);
+      const H2 c = *reinterpret_cast<const H2*>(&x[u].z), d = *reinterpret_cast<const H2*>(&x[u].w);
+      acc = __hmax2(acc, __hmax2(__hmax2(a, b), __hmax2(c, d)));
+    }
+    return fmaxf(__low2float(acc), __high2float(acc));
+  } else {
+    float m = TR::template vmax<false>(x[0]);
+#pragma unroll
+    for (int u = 1; u < kStU; ++u) m = fmaxf(m, TR::template vmax<false>(x[u]));
+    return m;
+  }
+}
+
 // Greedy helpers over one ring stage (this thread's kStU vectors, element
 // index (c0 + u*kSt + tid)*VW + t).  stage_max: the maximum, NaN if any element
 // is NaN, -inf if the stage holds no real vector.  16-bit types reduce packed
 // pairs first and convert once.
-template <typename T>
+template <typename T, bool FULL>
 __device__ __forceinline__ float stage_max(const uint4* slot, int c0, int NV) {
   using TR = Tr<T>;
   const int tid = threadIdx.x;
@@ -177,7 +203,7 @@ __device__ __forceinline__ float stage_max(const uint4* slot, int c0, int NV) {
     H2 acc = *reinterpret_cast<const H2*>(&padw);
 #pragma unroll
     for (int u = 0; u < kStU; ++u) {
-      if (c0 + u * kSt + tid < NV) {
+      if (FULL || c0 + u * kSt + tid < NV) {
         const uint4 x = slot[u * kSt + tid];
         const H2 a = *reinterpret_cast<const H2*>(&x.x), b = *reinterpret_cast<const H2*>(&x.y);
         const H2 cc = *reinterpret_cast<const H2*>(&x.z), d = *reinterpret_cast<const H2*>(&x.w);
@@ -192,7 +218,7 @@ __device__ __forceinline__ float stage_max(const uint4* slot, int c0, int NV) {
     bool nan = false;
 #pragma unroll
     for (int u = 0; u < kStU; ++u) {
-      if (c0 + u * kSt + tid < NV) {
+      if (FULL || c0 + u * kSt + tid < NV) {
         const float vm = TR::template vmax<true>(slot[u * kSt + tid]);
         nan |= (vm != vm);
         m = fmaxf(m, vm);
@@ -218,6 +244,47 @@ __device__ __noinline__ int stage_first_index(const uint4* slot, int c0, int NV,
 }
 
 // ---- greedy / softmax streaming kernel
+//
+// Every CTA streams the same number of 16-byte vectors: CTA j takes the range
+// [start(j), start(j + 1)) of the flattened [rows][vectors] space, start(j) =
+// floor(j * NVT / grid), whatever the row boundaries.  A row is thus split
+// into at most H segments (consecutive CTAs), and each segment leaves one
+// partial in slot row * H + segment, segment = j - seg_cta(row * NV) (its
+// warps' partials combined by warp 0 after one block barrier; a CTA ends at
+// most H + 1 segments).  Chunks of the ring never cross a row boundary.
+//
+// A walk over this CTA's range [v0, v1) of the flattened rows in chunks of
+// at most CH vectors that end at a row boundary or the range's end: row r,
+// vectors [v, ve) of it.  32-bit arithmetic inside a row.
+struct SegWalk {
+  int r, v, ve;         // current chunk: row r, vectors [v, min(v + CH, ve))
+  int r1, e1;           // last row of the range and the range's end in it
+  int NV, CH;
+  __device__ __forceinline__ void init(long long v0, long long v1, int NV_, int CH_) {
+    NV = NV_;
+    CH = CH_;
+    r = (int)(v0 / NV_);
+    v = (int)(v0 - (long long)r * NV_);
+    r1 = (int)((v1 - 1) / NV_);
+    e1 = (int)(v1 - (long long)r1 * NV_);
+    ve = r == r1 ? e1 : NV_;
+    if (v0 >= v1) r = r1 + 1;   // an empty range
+  }
+  __device__ __forceinline__ bool live() const { return r <= r1; }
+  // the current chunk (row, [vb, ce)); then advance
+  __device__ __forceinline__ void take(int* row, int* vb, int* ce) {
+    *row = r;
+    *vb = v;
+    *ce = min(v + CH, ve);
+    v = *ce;
+    if (v >= ve) {
+      ++r;
+      v = 0;
+      ve = r == r1 ? e1 : NV;
+    }
+  }
+};
+
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kSt, 3)
 stream_dense_kernel(const Params p) {
@@ -226,100 +293,187 @@ stream_dense_kernel(const Params p) {
   constexpr int S = kStS;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   uint4* ring = reinterpret_cast<uint4*>(smem_raw);
+  StreamSmem& sred = *reinterpret_cast<StreamSmem*>(smem_raw + (size_t)S * kStU * kSt * sizeof(uint4));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G1 = p.gamma + 1, V = p.V;
   // the kernel that merges the partials may start its input-only prologue now
   pdl_launch_dependents();
-  RowWalk w;
-  // target rows, then (q formed from the draft's logits) the draft rows
-  w.R = p.B * G1 + (p.ql ? p.B * p.gamma : 0);
-  w.Rt = p.B * G1;
-  w.ql = p.ql;
-  w.G1 = G1;
-  w.NV = V / VW;
-  w.H = p.H;                              // parts per row (items = R * H)
-  w.NVP = (w.NV + w.H - 1) / w.H;
-  w.CH = kStU * kSt;
-  w.NCH = (w.NVP + w.CH - 1) / w.CH;
-  w.nrows = (w.R * w.H - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int NV = V / VW;
+  int par = 0;   // segment parity: the red buffer in use
+  const int Rt = p.B * G1;          // target rows; draft rows (q formed from their logits) follow
   const T* logits = static_cast<const T*>(p.logits);
-
-  Issuer<T, S, 1> iss;
-  iss.start(logits, V, w);
-#pragma unroll
-  for (int s2 = 0; s2 < S; ++s2) iss.issue(ring, logits, V, w);
-  int stage = 0;
-  for (int j = 0; j < w.nrows; ++j) {
+  const T* ql = static_cast<const T*>(p.ql);
+  const long long NVT = p.NVT;
+  const long long v0 = (long long)blockIdx.x * NVT / gridDim.x;
+  const long long v1 = (long long)(blockIdx.x + 1) * NVT / gridDim.x;
+  const int CH = kStU * kSt;
+  auto rowptr = [&](int r) -> const T* {
+    return r < Rt ? logits + (size_t)r * V : ql + (size_t)(r - Rt) * V;
+  };
+  // issuer: S chunks ahead of the consumer
+  SegWalk iw;
+  iw.init(v0, v1, NV, CH);
+  int istage = 0;
+  auto issue = [&]() {
     int r, vb, ve;
-    w.item(j, &r, &vb, &ve);
-    float best = -INFINITY;          // greedy: this thread's max, its first index, NaN seen
-    int best_i = 0x7fffffff, nan_seen = 0;
-    float m = -INFINITY, s0 = 0.f, s1 = 0.f;   // softmax: running max and sums
-    for (int c = 0; c < w.NCH; ++c) {
-      cpa_wait<S - 1>();
-      const uint4* slot = ring + (size_t)stage * kStU * kSt;
-      if (MODE == MODE_GREEDY) {
-        // one max over the stage's kStU vectors; only a new best looks further
-        const float cm = stage_max<T>(slot, vb + c * w.CH, ve);
-        nan_seen |= (cm != cm);
-        if (cm > best) {
-          best = cm;
-          best_i = stage_first_index<T>(slot, vb + c * w.CH, ve, cm);
-        }
-      } else {
+    if (iw.live()) {
+      iw.take(&r, &vb, &ve);
+      uint4* slot = ring + (size_t)istage * kStU * kSt + tid;
+      const T* row = rowptr(r);
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) {
+        const int v = vb + u * kSt + tid;
+        if (v < ve) cpa16(slot + u * kSt, row + (size_t)v * VW);
+      }
+    }
+    cpa_commit();   // empty groups keep every thread's group count in step
+    istage = istage + 1 == S ? 0 : istage + 1;
+  };
+#pragma unroll
+  for (int s2 = 0; s2 < S; ++s2) issue();
+  SegWalk cw;
+  cw.init(v0, v1, NV, CH);
+  int stage = 0;
+  float best = -INFINITY;          // greedy: this thread's max, its first index, NaN seen
+  int best_i = 0x7fffffff, nan_seen = 0;
+  float m = -INFINITY, s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;   // softmax: running max and sums
+  int r, vb, ve;
+  while (cw.live()) {
+    cw.take(&r, &vb, &ve);
+    cpa_wait<S - 1>();
+    const uint4* slot = ring + (size_t)stage * kStU * kSt;
+    const bool fullc = ve - vb == CH;   // every thread has all kStU vectors of the chunk
+    if (MODE == MODE_GREEDY) {
+      // one max over the chunk's vectors of this thread; only a new best looks further
+      const float cm = fullc ? stage_max<T, true>(slot, vb, ve) : stage_max<T, false>(slot, vb, ve);
+      nan_seen |= (cm != cm);
+      if (cm > best) {
+        best = cm;
+        best_i = stage_first_index<T>(slot, vb, ve, cm);
+      }
+    } else if (fullc) {
+      // one maximum and at most one rescale per chunk, then the chunk's
+      // elements into four independent sums
+      uint4 x[kStU];
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) x[u] = slot[u * kSt + tid];
+      const float cm = chunk_max<T>(x);
+      if (cm > m) {
+        const float sc = (m == -INFINITY) ? 0.f : ex2_approx((m - cm) * p.c);
+        s0 *= sc;
+        s1 *= sc;
+        s2 *= sc;
+        s3 *= sc;
+        m = cm;
+      }
+      if (m > -INFINITY) {
+        const float mc = m * p.c;
 #pragma unroll
         for (int u = 0; u < kStU; ++u) {
-          const int v = vb + c * w.CH + u * kSt + tid;
-          if (v < ve) {
-            const uint4 x = slot[u * kSt + tid];
-            const float vm = TR::template vmax<false>(x);
-            if (vm > m) {
-              const float sc = (m == -INFINITY) ? 0.f : ex2_approx((m - vm) * p.c);
-              s0 *= sc;
-              s1 *= sc;
-              m = vm;
-            }
-            if (m > -INFINITY) {
-              const float mc = m * p.c;
 #pragma unroll
-              for (int t = 0; t < VW; t += 2) {
-                s0 += ex2_approx(fmaf(TR::get(x, t), p.c, -mc));
-                s1 += ex2_approx(fmaf(TR::get(x, t + 1), p.c, -mc));
-              }
+          for (int t = 0; t < VW; t += 4) {
+            s0 += ex2_approx(fmaf(TR::get(x[u], t), p.c, -mc));
+            s1 += ex2_approx(fmaf(TR::get(x[u], t + 1), p.c, -mc));
+            s2 += ex2_approx(fmaf(TR::get(x[u], t + 2), p.c, -mc));
+            s3 += ex2_approx(fmaf(TR::get(x[u], t + 3), p.c, -mc));
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kStU; ++u) {
+        const int v = vb + u * kSt + tid;
+        if (v < ve) {
+          const uint4 x = slot[u * kSt + tid];
+          const float vm = TR::template vmax<false>(x);
+          if (vm > m) {
+            const float sc = (m == -INFINITY) ? 0.f : ex2_approx((m - vm) * p.c);
+            s0 *= sc;
+            s1 *= sc;
+            s2 *= sc;
+            s3 *= sc;
+            m = vm;
+          }
+          if (m > -INFINITY) {
+            // four independent sums: short dependency chains
+            const float mc = m * p.c;
+#pragma unroll
+            for (int t = 0; t < VW; t += 4) {
+              s0 += ex2_approx(fmaf(TR::get(x, t), p.c, -mc));
+              s1 += ex2_approx(fmaf(TR::get(x, t + 1), p.c, -mc));
+              s2 += ex2_approx(fmaf(TR::get(x, t + 2), p.c, -mc));
+              s3 += ex2_approx(fmaf(TR::get(x, t + 3), p.c, -mc));
             }
           }
         }
       }
-      iss.issue(ring, logits, V, w);
-      stage = (stage + 1 == S) ? 0 : stage + 1;
     }
-    // ---- this warp's partial of the row part: shuffles and one store, no
-    // block-wide step (the merge is the next kernel's)
-    float4* slot = (r < w.Rt ? p.part + ((size_t)r * w.H + vb / w.NVP) * (kSt / 32)
-                             : p.qpart + ((size_t)(r - w.Rt) * w.H + vb / w.NVP) * (kSt / 32)) + warp;
-    if (MODE == MODE_GREEDY) {
-      int bi = best_i;
-      float bv = best;
-      if (__any_sync(0xffffffffu, nan_seen)) bv = __int_as_float(0x7fffffff);   // a NaN flags the row
+    issue();
+    stage = stage + 1 == S ? 0 : stage + 1;
+    if (ve == NV || !cw.live()) {
+      // ---- the end of this CTA's segment of row r (the same chunk in every
+      // thread): warp partials by shuffles, then warp 0 combines the 8 and
+      // stores the segment's partial
+      const int seg = (int)blockIdx.x - seg_cta((long long)r * NV, NVT, gridDim.x);
+      float4* out = r < Rt ? p.part + (size_t)r * p.H + seg : p.qpart + (size_t)(r - Rt) * p.H + seg;
+      if (MODE == MODE_GREEDY) {
+        int bi = best_i;
+        float bv = best;
+        if (__any_sync(0xffffffffu, nan_seen)) bv = __int_as_float(0x7fffffff);   // a NaN flags the row
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        for (int o = 16; o >= 1; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) sred.red[par][warp] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+        __syncthreads();
+        if (warp == 0) {
+          const float4 v = lane < kWarps ? sred.red[par][lane] : make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.f, 0.f);
+          bv = v.x;
+          bi = __float_as_int(v.y);
+#pragma unroll
+          for (int o = kWarps >> 1; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (argmax_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+          }
+          if (lane == 0) *out = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+        }
+        best = -INFINITY;
+        best_i = 0x7fffffff;
+        nan_seen = 0;
+      } else {
+        float M = m;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        F2 acc{0.f, 0.f};
+        if (m > -INFINITY && M < INFINITY) {
+          const float sc = ex2_approx((m - M) * p.c);
+          acc = f2_add(f2_add(F2{s0 * sc, 0.f}, F2{s1 * sc, 0.f}), f2_add(F2{s2 * sc, 0.f}, F2{s3 * sc, 0.f}));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc = f2_add(acc, f2_shfl_xor(acc, o));
+        if (lane == 0) sred.red[par][warp] = make_float4(M, acc.hi, acc.lo, 0.f);
+        __syncthreads();
+        if (warp == 0) {
+          const float4 v = lane < kWarps ? sred.red[par][lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+          float Mb = v.x;
+#pragma unroll
+          for (int o = kWarps >> 1; o >= 1; o >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
+          F2 t{0.f, 0.f};
+          if (v.x > -INFINITY && Mb < INFINITY) {
+            const float sc = ex2_approx((v.x - Mb) * p.c);
+            t = f2_add(F2{v.y * sc, 0.f}, F2{v.z * sc, 0.f});
+          }
+#pragma unroll
+          for (int o = kWarps >> 1; o >= 1; o >>= 1) t = f2_add(t, f2_shfl_xor(t, o));
+          if (lane == 0) *out = make_float4(Mb, t.hi, t.lo, 0.f);
+        }
+        m = -INFINITY;
+        s0 = s1 = s2 = s3 = 0.f;
       }
-      if (lane == 0) *slot = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
-    } else {
-      float M = m;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      F2 acc{0.f, 0.f};
-      if (m > -INFINITY && M < INFINITY) {
-        const float sc = ex2_approx((m - M) * p.c);
-        acc = f2_add(F2{s0 * sc, 0.f}, F2{s1 * sc, 0.f});
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) acc = f2_add(acc, f2_shfl_xor(acc, o));
-      if (lane == 0) *slot = make_float4(M, acc.hi, acc.lo, 0.f);
+      par ^= 1;
     }
   }
   cpa_wait<0>();
