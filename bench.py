@@ -131,12 +131,15 @@ def algorithmic_bytes(w, n_accepted: np.ndarray, kept_rejected: int = 0, gamma_b
     plus the q row of a rejected sequence.  q as the draft's logits: every
     draft row once more (to form q) and q elements counted at the logits'
     size; the float32 q the library may form from them is the
-    implementation's own traffic.  With top-k / top-p the final draw of a
+    implementation's own traffic.  With top-k (then top-p) the final draw of a
     rejected sequence reads q only at the kept candidates of row n:
     kept_rejected is their total over the batch (read inside the streaming
-    kernel's sequence finisher).  Deterministic drafts (q one-hot, passed as
-    None) read no q bytes.  A ragged round (gamma_b given) needs only rows
-    0..gamma_b of each sequence."""
+    kernel's sequence finisher).  Top-p alone ranks the whole row: the final
+    draw reads row n's logits again and q at its kept tokens (its own
+    threshold passes over the rows are the implementation's traffic).
+    Deterministic drafts (q one-hot, passed as None) read no q bytes.  A
+    ragged round (gamma_b given) needs only rows 0..gamma_b of each
+    sequence."""
     s = _elt_bytes(w)
     B, G, V = len(n_accepted), w.gamma, w.V
     qb = _q_elt_bytes(w)
@@ -146,9 +149,11 @@ def algorithmic_bytes(w, n_accepted: np.ndarray, kept_rejected: int = 0, gamma_b
     stream = (gsum + B) * V * s + gsum * (qb + s)
     if w.qlogits:
         stream += gsum * V * s           # the draft rows, read once to form their q
-    if w.top_k > 0 or w.top_p < 1.0:
+    if w.top_k > 0:
         return {"stream": stream + int(kept_rejected) * qb, "final": 0}
     gb = np.asarray(gamma_b) if gamma_b is not None else np.full(B, G)
+    if w.top_p < 1.0:
+        return {"stream": stream, "final": B * V * s + int(kept_rejected) * qb}
     rejected = int((n_accepted < gb).sum())
     final = rejected * V * (qb + s) + (B - rejected) * V * s
     return {"stream": stream, "final": final}

@@ -288,7 +288,7 @@ const char* sv_status_string(sv_status s);
 /*
  * Names of the kernels the last sv_verify_sample / sv_verify_greedy call made
  * on this host thread launched, comma-separated in launch order (for example
- * "cluster_kernel", or "stream_dense_kernel,final_draw_kernel,final_pick_kernel");
+ * "cluster_kernel", or "stream_dense_kernel,final_draw_kernel");
  * "" before the first call, after
  * a call that launched nothing (B = 0, an argument error) or a launch failure.
  * Static storage owned by the library; thread-local.

@@ -16,6 +16,7 @@
 #include "sv_device.cuh"
 #include "sv_final.cuh"
 #include "sv_qsoftmax.cuh"
+#include "sv_topp.cuh"
 #include "sv_stream.cuh"
 #include "sv_truncate.cuh"
 #include "sv_topk.cuh"
@@ -42,7 +43,7 @@ int list_len(int V, int top_k) {
 }
 
 struct Layout {
-  size_t seq_ticket, seq_ticket2, row_ticket, ctr, seq, acc, part, lists, rowres, fd_part, fd_q, total;
+  size_t seq_ticket, seq_ticket2, row_ticket, ctr, seq, acc, part, lists, rowres, fd_part, fd_q, tp, total;
   int S_part, S_list, FC, klist;
 };
 
@@ -71,6 +72,7 @@ Layout make_layout(int B, int gamma, int V, int top_k) {
   L.rowres = o;      o += up(L.klist > 0 ? sizeof(int2) * (size_t)R * (L.klist + 1) : 0);
   L.fd_part = o;     o += up(sizeof(float4) * (size_t)B * L.FC);
   L.fd_q = o;        o += up(sizeof(float) * (size_t)B * L.FC);
+  L.tp = o;          o += up(sizeof(sv::TpRow) * (size_t)R);
   L.total = o;
   return L;
 }
@@ -110,6 +112,7 @@ void bind_workspace(sv::Params& p, const Layout& L, void* ws) {
   p.fd_part = reinterpret_cast<float4*>(w + L.fd_part);
   p.fd_q = reinterpret_cast<float*>(w + L.fd_q);
   p.FC = L.FC;
+  p.tp = reinterpret_cast<sv::TpRow*>(w + L.tp);
 }
 
 // Rows-kernel slicing: 8 vectors per thread unless that leaves fewer than two
@@ -159,11 +162,11 @@ sv_status launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, const sv::Param
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// The final draw: persistent CTAs (as many as fit, at most one warp per
-// item); each warp takes a contiguous range of the B * FC items.
-template <typename T>
+// The final draw: Z CTAs per sequence (one part of row n each; persistent
+// when the units exceed the CTAs that fit), the last part's CTA searches.
+template <typename T, bool MASK = false>
 sv_status launch_final_draw(const sv::Params& p, cudaStream_t stream) {
-  auto kern = sv::final_draw_kernel<T>;
+  auto kern = sv::final_draw_kernel<T, MASK>;
   const size_t smem = sv::FdRing<T>::bytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
@@ -175,12 +178,13 @@ sv_status launch_final_draw(const sv::Params& p, cudaStream_t stream) {
     cudaGetLastError();
     per_sm = 1;
   }
-  const long long items = (long long)p.B * p.FC;
-  const long long grid = std::max(1ll, std::min((long long)per_sm * sm_count(), ceil_div(items, sv::kFdWarps)));
-  const sv_status st = launch_pdl(kern, dim3((unsigned)grid), dim3(sv::kFdThreads), smem, p, stream);
-  if (st != SV_OK) return st;
-  // the search: one CTA per sequence
-  return launch_pdl(sv::final_pick_kernel<T>, dim3((unsigned)p.B), dim3(sv::kPickThreads), 0, p, stream);
+  // parts per sequence: the B * Z units fill the CTA slots once (at most one
+  // part per 4 items)
+  const long long slots = (long long)per_sm * sm_count();
+  sv::Params q = p;
+  q.FZ = (int)std::max(1ll, std::min(slots / std::max(1, p.B), ceil_div(p.FC, 4)));
+  const long long grid = std::max(1ll, std::min(slots, (long long)p.B * q.FZ));
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(sv::kFdThreads), smem, q, stream);
 }
 
 // ---------------------------------------------------------------- cluster path
@@ -197,11 +201,12 @@ int path_override() {
   if (!std::strcmp(e, "grid")) return 1;
   if (!std::strcmp(e, "cluster")) return 2;
   if (!std::strcmp(e, "slices")) return 3;   // top-k: the per-slice kernel instead of the per-row one
+  if (!std::strcmp(e, "topp")) return 4;     // top-p alone: the per-row threshold path at any V
   return 0;
 }
 
 bool plan_cluster(const sv::Params& p, sv_dtype dt, int mode, sv::ClusterParams* cp, size_t* smem) {
-  if (mode == sv::MODE_TOPK || p.ql) return false;   // q from draft logits: the streaming path
+  if (mode == sv::MODE_TOPK || mode == sv::MODE_TOPP || p.ql) return false;   // q from draft logits: the streaming path
   const int ov = path_override();
   if (ov == 1) return false;
   const int VW = vec_width(dt);
@@ -383,6 +388,23 @@ sv_status dispatch(sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
   }
   timing_record(0, stream);
   sv_status st = SV_OK;
+  if (mode == sv::MODE_TOPP) {
+    // top-p alone: the rows' kept sets, then the final draw under the mask
+    const size_t smem = sizeof(sv::TpSmem);
+    auto tk = sv::topp_row_kernel<T>;
+    if (cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return SV_ERR_CUDA;
+    }
+    tk<<<(unsigned)((long long)p.B * (p.gamma + 1)), sv::kTpThreads, smem, stream>>>(p, p.tp);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    timing_record(1, stream);
+    p.H = 0;
+    st = launch_final_draw<T, true>(p, stream);
+    timing_record(2, stream);
+    g_last_kernels = st == SV_OK ? "topp_row_kernel,final_draw_kernel" : "";
+    return st;
+  }
   const bool streamable = p.V % vec_width(dt) == 0 && path_override() != 3;
   if (mode == sv::MODE_GREEDY) {
     st = streamable ? launch_stream_dense<T, sv::MODE_GREEDY>(p, stream) : launch_rows<T, sv::MODE_GREEDY>(p, stream);
@@ -392,8 +414,7 @@ sv_status dispatch(sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
     g_last_kernels = streamable ? "stream_topk_kernel" : "rows_kernel";
   } else {
     st = streamable ? launch_stream_dense<T, sv::MODE_SOFTMAX>(p, stream) : launch_rows<T, sv::MODE_SOFTMAX>(p, stream);
-    g_last_kernels = streamable ? "stream_dense_kernel,final_draw_kernel,final_pick_kernel"
-                                  : "rows_kernel,final_draw_kernel,final_pick_kernel";
+    g_last_kernels = streamable ? "stream_dense_kernel,final_draw_kernel" : "rows_kernel,final_draw_kernel";
   }
   if (st != SV_OK) {
     g_last_kernels = "";
@@ -464,11 +485,14 @@ sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dty
   if (gamma > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;   // q == NULL: deterministic drafts
   if (!aligned16(logits) || (q && !aligned16(q))) return SV_ERR_INVALID_ARG;
 
-  // top-k below V, or top-p: the candidate-list path.  top-p without an
-  // effective top-k ranks the whole vocabulary, supported for V <= SV_MAX_TOP_K.
+  // top-k below V (then top-p on its list): the candidate-list path.  top-p
+  // without an effective top-k: the list path for V <= SV_MAX_TOP_K, else the
+  // per-row threshold path (any V; q from draft logits excepted).
   const bool truncate = (top_k > 0 && top_k < V) || top_p < 1.0f;
+  const bool topp_only = truncate && !(top_k > 0 && top_k < V);
+  const bool topp_rows = topp_only && !ql && (V > SV_MAX_TOP_K || path_override() == 4);
   int klist = 0;
-  if (truncate) {
+  if (truncate && !topp_rows) {
     klist = (top_k > 0 && top_k < V) ? top_k : V;
     if (klist > SV_MAX_TOP_K) return SV_ERR_UNSUPPORTED;
   }
@@ -496,9 +520,9 @@ sv_status verify_sample_impl(int B, int gamma, int V, const void* logits, sv_dty
   p.out_n = out_num_accepted;
   p.out_a = out_accept_prob;
   p.out_status = out_status;
-  // list_len(V, top_k) == klist whenever truncate holds
-  return run(p, logits_dtype, truncate ? sv::MODE_TOPK : sv::MODE_SOFTMAX, workspace, workspace_bytes, top_k,
-             reinterpret_cast<cudaStream_t>(stream));
+  // list_len(V, top_k) == klist whenever the list path runs
+  const int mode = topp_rows ? sv::MODE_TOPP : (truncate ? sv::MODE_TOPK : sv::MODE_SOFTMAX);
+  return run(p, logits_dtype, mode, workspace, workspace_bytes, top_k, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sv_status verify_greedy_impl(int B, int gamma, int V, const void* logits, sv_dtype logits_dtype,

@@ -56,12 +56,15 @@ struct SeqState {
   double s;       // sum_v 2^((L_v - M) c) of the row the final draw uses
   float qinv;     // 1 / its sum of 2^((x - qm) c),
   int qbad;       // and whether it defines no distribution
+  uint32_t tpK;   // top-p alone: the kept set of the row (key > tpK, or
+  int tpIdx;      // key == tpK and index <= tpIdx)
 };
 
 struct Params {
   int B, gamma, V;
   int S, U, SL;          // rows kernel: slices per row, vectors per thread, slice length
   int FC;                // final draw: 512-token items per row
+  int FZ;                // final draw: parts (CTAs) per sequence
   int top_k;             // top-k list length (top-k mode)
   int H;                 // streaming kernel: partial slots (segments) per row, 1, 2 or 4
   int SG;                // streaming kernel: its grid (CTA j streams vectors [j NVT / SG, (j+1) NVT / SG))
@@ -94,6 +97,7 @@ struct Params {
                                   // from them in the streaming path, else nullptr
   float4* qpart;                  // [B * gamma][H][kWarps] the draft rows' streaming partials (with ql)
   int2* qrowres;                  // [B * gamma][top_k + 1] the draft rows' kept lists (with ql and top-k / top-p)
+  struct TpRow* tp;               // [B][gamma + 1] top-p alone: each row's kept set, mass and a_i
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -664,7 +668,7 @@ __device__ __forceinline__ bool arrive_last(int* ticket, int count, int* s_flag,
 
 // ------------------------------------------------------------------ rows kernel
 
-enum { MODE_GREEDY = 0, MODE_SOFTMAX = 1, MODE_TOPK = 2 };
+enum { MODE_GREEDY = 0, MODE_SOFTMAX = 1, MODE_TOPK = 2, MODE_TOPP = 3 };
 
 struct RowsSmem {
   float fred[kWarps];
@@ -800,6 +804,8 @@ __device__ void finish_sequence_dense(const Params& p, int b, RowsSmem& sm) {
       st.s = sm.s[n];
       st.qinv = 0.f;
       st.qbad = 0;
+      st.tpK = 0u;
+      st.tpIdx = 0;
       p.seq[b] = st;
     }
     sm.n = n;

@@ -5,48 +5,50 @@
 // Decoding", speculative-sampling paragraph).  The draw is the inverse CDF in
 // token-index order: the smallest v with sum_{w <= v} r(w) > u * sum(r).
 //
-// Two kernels follow the row statistics (streaming kernel or rows kernel):
-//
-//   final_draw_kernel persistent; every WARP works through its own
-//                     contiguous range of items (sequence b, 512 tokens of row
-//                     n_b) with a lane-private cp.async ring of kFdStages
-//                     items: no block barriers and no cross-warp waits.  When
-//                     a warp reaches a new sequence it merges that
-//                     sequence's per-warp row partials (streaming path; the
-//                     rows path leaves the merged state), forms p_i(d_i) and
-//                     a_i = min(1, p_i(d_i) / q_i(d_i)) and scans for the first
-//                     rejection n (the drafts, their logits and q values are
-//                     gathered before the dependency wait); the warp holding
-//                     the sequence's first item writes every output but the
-//                     drawn token.  Per item it sums (S, A, Q): the weights
-//                     w = 2^((x - M) c), and over the residual support
-//                     {w > s' q} the differences w - s' q and q (s' the float
-//                     normaliser); lane 0 stores them.
-//   final_pick_kernel one CTA per sequence: the inverse-CDF search item ->
-//                     token over the item sums, then over the 512 tokens of
-//                     the one item the target falls in (re-read from L2).
+// One kernel follows the row statistics (streaming kernel, rows kernel, or
+// the top-p rows kernel): final_draw_kernel, one CTA per sequence (persistent
+// over sequences), 16 warps.
+//   - Every warp takes sequence b's state: it merges the streaming kernel's
+//     row partials, forms p_i(d_i) and a_i = min(1, p_i(d_i) / q_i(d_i)) and
+//     scans for the first rejection n (the first sequence's drafts, their
+//     logits and q values are gathered before the dependency wait); warp 0
+//     writes every output but the drawn token.
+//   - Sequence b's row n is cut into items of 2048 tokens and the items into
+//     Z parts, one CTA each.  Warp w of a part sums its items w, w + 16, ...
+//     chunk by chunk (512 tokens) through a lane-private cp.async ring: no
+//     block barriers and no cross-warp waits.
+//     Per item: the weights w = 2^((x - M) c) (S), and over the residual
+//     support {w > s' q} the differences w - s' q (A) and q (Q), s' the float
+//     normaliser; four items' warp totals at a time by a transposed
+//     butterfly.
+//   - The CTA that completes a sequence's last part (an acquire-release
+//     ticket) searches: exact normaliser s = sum S, item masses, the item
+//     holding u * R, then the token among its 2048 (re-read from L2, four
+//     per thread).
 //
 // Precision (the draw is compared with a float64 reference over up to 10^5
 // CDF steps).  Tokens whose exponent (x - M) c is above -8 carry most of the
 // mass: their weights and residuals are two-float (Tang's table exp2; the
 // residual formed exactly).  Every other token's weight is ex2.approx with a
 // first-order correction for the exponent's low part, and a lane adds its 16
-// such tokens of an item in float32: each is below 2^-8 of the largest
+// such tokens of a chunk in float32: each is below 2^-8 of the largest
 // weight, so the rounding of these short sums stays at the level of the
-// weights' own error.  Lane sums and everything above them are two-float.
+// weights' own error.  Chunk sums, lane sums and everything above them are
+// two-float.
 // The exact normaliser s = sum S is formed at the end; the residual mass of
 // an item is A - (s - s') Q.
 #pragma once
 
 #include "sv_device.cuh"
+#include "sv_topp.cuh"
 
 namespace sv {
 
-constexpr int kFdThreads = 256;            // 8 independent warps per CTA
+constexpr int kFdThreads = 512;            // one CTA per sequence, 16 warps
 constexpr int kFdWarps = kFdThreads / 32;
-constexpr int kFdStages = 4;               // ring stages (items) per lane
-constexpr int kFdTok = 512;                // tokens per item: 4 groups x 32 lanes x 4 tokens
-constexpr int kPickThreads = 256;          // final_pick_kernel: 2 tokens of the item per thread
+constexpr int kFdChunk = 512;              // tokens per ring stage: 4 groups x 32 lanes x 4 tokens
+constexpr int kFdChunks = 4;               // chunks per item
+constexpr int kFdTok = kFdChunk * kFdChunks;   // tokens per item (one stored sum)
 
 enum { FD_NONE = 0, FD_DENSE = 1, FD_DET = 2, FD_QL = 3, FD_SKIP = 4 };
 
@@ -59,7 +61,8 @@ struct FdRing {
   static constexpr int QB = 16;
   static constexpr int lane_bytes = 4 * LB + 4 * QB;
   static constexpr int stage_bytes = 32 * lane_bytes;   // one warp's stage
-  static constexpr size_t bytes = (size_t)kFdWarps * kFdStages * stage_bytes;
+  static constexpr int S = sizeof(T) == 4 ? 3 : 4;        // stages (items) per warp: 192 KB in all
+  static constexpr size_t bytes = (size_t)kFdWarps * S * stage_bytes;
 };
 
 __device__ __forceinline__ void fd_cp16(void* smem, const void* gmem) {
@@ -71,8 +74,19 @@ __device__ __forceinline__ void fd_cp8(void* smem, const void* gmem) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(sa), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void fd_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int S>
 __device__ __forceinline__ void fd_wait_ring() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(kFdStages - 1) : "memory");
+  asm volatile("cp.async.wait_group %0;" ::"n"(S - 1) : "memory");
+}
+
+// Warp-wide two-float sum (every lane gets it), and lane l's value in every lane.
+__device__ __forceinline__ F2 warp_sum_f2(F2 v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = f2_add(v, f2_shfl_xor(v, m));
+  return v;
+}
+__device__ __forceinline__ F2 f2_bcast(F2 v, int l) {
+  return F2{__shfl_sync(0xffffffffu, v.hi, l), __shfl_sync(0xffffffffu, v.lo, l)};
 }
 
 // What the final draw needs about one sequence: row n, how q is given, the
@@ -84,6 +98,8 @@ struct FdSeq {
   double s;             // row n's normaliser as merged
   int xq;               // deterministic draft: the rejected draft's token
   QLrow qlr;            // q formed from the draft's logits: row n's statistics
+  uint32_t K;           // top-p alone: row n's kept set (key > K, or key == K
+  int idx;              // and index <= idx)
   const T* row;         // logits row n
   const float* qrow;    // q row n (FD_DENSE)
   const T* qlrow;       // draft logits row n (FD_QL)
@@ -116,7 +132,7 @@ __device__ __forceinline__ void fd_bind(const Params& p, int b, FdSeq<T>& s) {
 }
 
 // The state a previous kernel left for sequence b (the rows path's finisher,
-// or final_draw_kernel's scanning warp for final_pick_kernel).
+// or final_draw_kernel's scanning warp, for the search).
 template <typename T>
 __device__ __forceinline__ void fd_load_state(const Params& p, int b, FdSeq<T>& s) {
   const SeqState* sp = p.seq + b;
@@ -127,6 +143,8 @@ __device__ __forceinline__ void fd_load_state(const Params& p, int b, FdSeq<T>& 
   s.s = __ldcg(&sp->s);
   s.s_a = (float)s.s;
   s.qlr = QLrow{__ldcg(&sp->qm), __ldcg(&sp->qinv), __ldcg(&sp->qbad) != 0};
+  s.K = __ldcg(&sp->tpK);
+  s.idx = __ldcg(&sp->tpIdx);
   fd_bind(p, b, s);
 }
 
@@ -215,8 +233,7 @@ __device__ __forceinline__ void fd_merge_rows(const Params& p, const float4* bas
 // The acceptance scan of sequence b by one warp (streaming path): row
 // statistics merged from the partials, a_i for i < gamma_b, n = the first
 // rejected position (gamma_b if none), the status bits, and row n's state
-// in s.  `writer`: this warp holds the sequence's first item and writes the
-// outputs (all but the drawn token) and the state final_pick_kernel reads.
+// in s.  `writer`: this warp writes the outputs (all but the drawn token).
 template <typename T>
 __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& g, bool writer, FdSeq<T>& s) {
   const int lane = threadIdx.x & 31;
@@ -273,6 +290,8 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
   s.s = (double)Sh + (double)Sl;
   s.s_a = (float)s.s;
   s.qlr = QLrow{0.f, 0.f, true};
+  s.K = 0u;
+  s.idx = 0;
   if (p.ql) {
     const float qm = __shfl_sync(0xffffffffu, hn ? qM[1] : qM[0], ln);
     const float qh = __shfl_sync(0xffffffffu, hn ? qS[1].hi : qS[0].hi, ln);
@@ -288,18 +307,59 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
       if (p.out_a && i < G) p.out_a[b * G + i] = i < gb ? a[h] : 0.f;
       if (i < G1 && i != n) p.out_tokens[b * G1 + i] = i < n ? g.d[h] : -1;
     }
-    if (lane == 0) {
-      p.out_n[b] = n;
-      SeqState st;
-      st.n = n;
-      st.status = bits;
-      st.M = s.M;
-      st.s = s.s;
-      st.qm = s.qlr.m;
-      st.qinv = s.qlr.inv;
-      st.qbad = s.qlr.bad ? 1 : 0;
-      p.seq[b] = st;
+    if (lane == 0) p.out_n[b] = n;
+  }
+}
+
+// The acceptance scan of sequence b by one warp for top-p alone: the rows'
+// records from topp_row_kernel hold a_i and the status bits; n = the first
+// rejected position; row n's kept set and mass give the state.  `writer` as
+// in fd_scan.
+template <typename T>
+__device__ __forceinline__ void fd_scan_tp(const Params& p, int b, bool writer, FdSeq<T>& s) {
+  const int lane = threadIdx.x & 31;
+  const int G = p.gamma, G1 = G + 1;
+  const int gb = seq_gamma(p, b);
+  const TpRow* tr = p.tp + (size_t)b * G1;
+  int bits = 0, d[2] = {-1, -1};
+  float a[2] = {0.f, 0.f};
+  unsigned rej[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
+    bool r = false;
+    if (i <= gb) {
+      const int st = __ldcg(&tr[i].status);
+      bits |= st & SEQ_BADROW;
+      if (i < gb) {
+        bits |= st & (SEQ_OOB | SEQ_QBAD);
+        a[h] = __ldcg(&tr[i].a);
+        d[h] = __ldg(p.draft + b * G + i);
+        r = !(__ldg(p.uniforms + b * G1 + i) < a[h]);
+      }
     }
+    rej[h] = __ballot_sync(0xffffffffu, r);
+  }
+  const int n = rej[0] ? __ffs(rej[0]) - 1 : (rej[1] ? 32 + __ffs(rej[1]) - 1 : gb);
+  bits = __reduce_or_sync(0xffffffffu, bits);
+  s.n = n;
+  s.gb = gb;
+  s.status = bits;
+  s.M = __ldcg(&tr[n].M);
+  s.s = (double)__ldcg(&tr[n].Wh) + (double)__ldcg(&tr[n].Wl);
+  s.s_a = (float)s.s;
+  s.qlr = QLrow{0.f, 0.f, true};
+  s.K = __ldcg(&tr[n].K);
+  s.idx = __ldcg(&tr[n].idx);
+  fd_bind(p, b, s);
+  if (writer) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lane + 32 * h;
+      if (p.out_a && i < G) p.out_a[b * G + i] = i < gb ? a[h] : 0.f;
+      if (i < G1 && i != n) p.out_tokens[b * G1 + i] = i < n ? d[h] : -1;
+    }
+    if (lane == 0) p.out_n[b] = n;
   }
 }
 
@@ -309,37 +369,60 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
 template <typename T>
 __device__ __noinline__ void fd_scalar_group(const T* row, const float* qrow, const T* qlrow, int t0, int V,
                                              unsigned char* ld, unsigned char* qd) {
+  const uint32_t pad = Tr<T>::kPadWord;   // -inf in the logits' type
   for (int t = 0; t < 4; ++t) {
-    if (t0 + t < V) {
-      if (sizeof(T) == 4) reinterpret_cast<uint32_t*>(ld)[t] = Tr<T>::scalar_bits(row + t0 + t);
-      else reinterpret_cast<unsigned short*>(ld)[t] = (unsigned short)Tr<T>::scalar_bits(row + t0 + t);
-      if (qrow) {
-        reinterpret_cast<float*>(qd)[t] = __ldg(qrow + t0 + t);
-      } else if (qlrow) {
-        if (sizeof(T) == 4) reinterpret_cast<uint32_t*>(qd)[t] = Tr<T>::scalar_bits(qlrow + t0 + t);
-        else reinterpret_cast<unsigned short*>(qd)[t] = (unsigned short)Tr<T>::scalar_bits(qlrow + t0 + t);
-      }
+    const bool in = t0 + t < V;
+    if (sizeof(T) == 4) reinterpret_cast<uint32_t*>(ld)[t] = in ? Tr<T>::scalar_bits(row + t0 + t) : pad;
+    else reinterpret_cast<unsigned short*>(ld)[t] = (unsigned short)(in ? Tr<T>::scalar_bits(row + t0 + t) : pad);
+    if (qrow) {
+      reinterpret_cast<float*>(qd)[t] = in ? __ldg(qrow + t0 + t) : 0.f;
+    } else if (qlrow) {
+      if (sizeof(T) == 4) reinterpret_cast<uint32_t*>(qd)[t] = in ? Tr<T>::scalar_bits(qlrow + t0 + t) : pad;
+      else reinterpret_cast<unsigned short*>(qd)[t] = (unsigned short)(in ? Tr<T>::scalar_bits(qlrow + t0 + t) : pad);
     }
   }
 }
 
-// Issue this lane's copies of item c of sequence s into one ring stage:
-// logits groups g = 0..3 (tokens c*512 + 128 g + 4 lane .. + 3) and, for a
+// Issue this lane's copies of the chunk starting at token tc of sequence s
+// into one ring stage: logits groups g = 0..3 (tokens tc + 128 g + 4 lane ..
+// + 3) and, for a
 // residual, the matching q (or draft logit) groups.  vec: 4-token groups are
 // aligned (V % 4 == 0); otherwise the in-range tokens are loaded one by one.
-// Groups past the end of the row are not read (the sweep gives them weight 0).
+// Tokens past the end of the row are not read: their slots are filled with
+// -inf logits and zero q, which the sweep gives weight 0 with no test.
 template <typename T>
-__device__ __forceinline__ void fd_issue(const FdSeq<T>& s, int c, int V, bool vec, unsigned char* st) {
+__device__ __forceinline__ void fd_issue(const FdSeq<T>& s, int tc, int V, bool vec, unsigned char* st) {
   using R = FdRing<T>;
   if (s.mode == FD_SKIP) return;
   const int lane = threadIdx.x & 31;
-  unsigned char* lg = st;
-  unsigned char* qg = st + 4 * 32 * R::LB;
+  unsigned char* lg = st + lane * R::LB;
+  unsigned char* qg = st + 4 * 32 * R::LB + lane * R::QB;
+  const int tl = tc + 4 * lane;   // this lane's first token; group g adds 128 g
+  if (vec && tc + kFdChunk <= V) {
+    // the whole chunk is inside the row: base addresses plus constant offsets
+    const T* lrow = s.row + tl;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (R::LB == 16) fd_cp16(lg + g * 32 * R::LB, lrow + 128 * g); else fd_cp8(lg + g * 32 * R::LB, lrow + 128 * g);
+    }
+    if (s.mode == FD_DENSE) {
+      const float* qr = s.qrow + tl;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) fd_cp16(qg + g * 32 * R::QB, qr + 128 * g);
+    } else if (s.mode == FD_QL) {
+      const T* qr = s.qlrow + tl;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (R::LB == 16) fd_cp16(qg + g * 32 * R::QB, qr + 128 * g); else fd_cp8(qg + g * 32 * R::QB, qr + 128 * g);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const int t0 = c * kFdTok + 128 * g + 4 * lane;
-    unsigned char* ld = lg + (g * 32 + lane) * R::LB;
-    unsigned char* qd = qg + (g * 32 + lane) * R::QB;
+    const int t0 = tl + 128 * g;
+    unsigned char* ld = lg + g * 32 * R::LB;
+    unsigned char* qd = qg + g * 32 * R::QB;
     if (vec) {
       if (t0 < V) {
         if (R::LB == 16) fd_cp16(ld, s.row + t0); else fd_cp8(ld, s.row + t0);
@@ -347,6 +430,16 @@ __device__ __forceinline__ void fd_issue(const FdSeq<T>& s, int c, int V, bool v
           fd_cp16(qd, s.qrow + t0);
         } else if (s.mode == FD_QL) {
           if (R::LB == 16) fd_cp16(qd, s.qlrow + t0); else fd_cp8(qd, s.qlrow + t0);
+        }
+      } else {
+        const uint32_t pad = Tr<T>::kPadWord;
+        if (R::LB == 16) *reinterpret_cast<uint4*>(ld) = make_uint4(pad, pad, pad, pad);
+        else *reinterpret_cast<uint2*>(ld) = make_uint2(pad, pad);
+        if (s.mode == FD_DENSE) {
+          *reinterpret_cast<uint4*>(qd) = make_uint4(0u, 0u, 0u, 0u);
+        } else if (s.mode == FD_QL) {
+          if (R::LB == 16) *reinterpret_cast<uint4*>(qd) = make_uint4(pad, pad, pad, pad);
+          else *reinterpret_cast<uint2*>(qd) = make_uint2(pad, pad);
         }
       }
     } else {
@@ -410,12 +503,12 @@ struct FdAcc {
   RunAcc top;
 };
 
-// One item's 16 tokens of this lane.  The per-token formulas are those of
-// run_tail / run_top, so token_mass reproduces each token's share.  FULL: the
-// whole item lies inside the row.
-template <typename T, int MODE, bool FULL>
-__device__ __forceinline__ void fd_sweep(const FdSeq<T>& s, const unsigned char* st, int c, int V, float cc,
-                                         float c_lo, const float* tab, FdAcc& acc) {
+// One chunk's 16 tokens of this lane (tokens past the row's end arrive as
+// -inf logits with zero q).  The per-token formulas are those of run_tail /
+// run_top, so token_mass reproduces each token's share.
+template <typename T, int MODE, bool MASK>
+__device__ __forceinline__ void fd_sweep(const FdSeq<T>& s, const unsigned char* st, int tc, float cc, float c_lo,
+                                         const float* tab, FdAcc& acc) {
   using R = FdRing<T>;
   constexpr bool EXACT = sizeof(T) == 2;
   const int lane = threadIdx.x & 31;
@@ -423,39 +516,46 @@ __device__ __forceinline__ void fd_sweep(const FdSeq<T>& s, const unsigned char*
   const unsigned char* qg = st + 4 * 32 * R::LB;
   const float M = s.M, s_a = s.s_a;
   uint32_t near = 0u;
-  // rolled over the 4 groups (the 4 tokens of a group are independent): the
-  // kernel holds 8 variants of this sweep, and unrolled they overflow the
-  // instruction cache
-#pragma unroll 1
+#pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const int t0 = c * kFdTok + 128 * g + 4 * lane;
-    float x[4], q[4];
+    const int t0 = tc + 128 * g + 4 * lane;
+    float x[4], q[4], p[4], w[4];
     fd_unpack<T>(lg + (g * 32 + lane) * R::LB, x);
     fd_qgroup<T, MODE>(s, qg + (g * 32 + lane) * R::QB, t0, cc, c_lo, q);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      if (!FULL && t0 + t >= V) {
-        x[t] = -INFINITY;
-        q[t] = 0.f;
-      }
-      float e, p;
+      // top-p alone: a token outside the kept set has p~ = 0 (weight 0, and
+      // max(0 - q, 0) = 0)
+      if (MASK && !tp_kept<T>(x[t], t0 + t, s.K, s.idx)) x[t] = -INFINITY;
+      float e;
       if (EXACT) {
         const float dh = fmaxf(x[t] - M, -1.0e4f);   // exact for 16-bit logits; -inf flushes to 0 below
-        p = dh * cc;
-        e = fmaf(dh, c_lo, fmaf(dh, cc, -p));
+        p[t] = dh * cc;
+        e = fmaf(dh, c_lo, fmaf(dh, cc, -p[t]));
       } else {
-        p = tok_exponent<false>(x[t], M, cc, c_lo, &e);
+        p[t] = tok_exponent<false>(x[t], M, cc, c_lo, &e);
       }
-      const bool hi = p > -8.f;
-      const float y = ex2_approx(p);
-      float w = fmaf(y * 6.931471825e-01f, e, y);
-      if (!EXACT) w = p > -1.0e30f ? w : 0.f;   // -inf (float32 logits)
-      w = hi ? 0.f : w;
-      near |= (uint32_t)hi << (4 * g + t);
-      acc.S[t & 1] += w;
+      const float y = ex2_approx(p[t]);
+      w[t] = fmaf(y * 6.931471825e-01f, e, y);
+      if (!EXACT) w[t] = p[t] > -1.0e30f ? w[t] : 0.f;   // -inf (float32 logits)
+    }
+    // a token near the maximum (exponent above -8) is rare: it leaves the
+    // float32 sums and is added in two-float after the sweep
+    if (fmaxf(fmaxf(p[0], p[1]), fmaxf(p[2], p[3])) > -8.f) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (p[t] > -8.f) {
+          w[t] = 0.f;
+          near |= 1u << (4 * g + t);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      acc.S[t & 1] += w[t];
       if (MODE != FD_NONE) {
         // the residual support {w > s' q}: the sign of w - s' q rounded once
-        const float d = fmaf(-s_a, q[t], w);
+        const float d = fmaf(-s_a, q[t], w[t]);
         acc.A[t & 1] += fmaxf(d, 0.f);
         acc.Q[t & 1] += d > 0.f ? q[t] : 0.f;
       }
@@ -465,7 +565,7 @@ __device__ __forceinline__ void fd_sweep(const FdSeq<T>& s, const unsigned char*
     const int o = __ffs(near) - 1;
     near &= near - 1;
     const int g = o >> 2, t = o & 3;
-    const int t0 = c * kFdTok + 128 * g + 4 * lane;
+    const int t0 = tc + 128 * g + 4 * lane;
     float x[4], q[4];
     fd_unpack<T>(lg + (g * 32 + lane) * R::LB, x);
     fd_qgroup<T, MODE>(s, qg + (g * 32 + lane) * R::QB, t0, cc, c_lo, q);
@@ -515,423 +615,325 @@ __device__ __forceinline__ IT5 it5_reduce4(const IT5 slot[4]) {
   return t;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kFdThreads, 2) final_draw_kernel(const Params p) {
-  using R = FdRing<T>;
-  extern __shared__ __align__(16) unsigned char fd_dyn[];
-  __shared__ float tab[128];
-  load_exp2_table(tab);
-  __syncthreads();   // the only block barrier: the warps are independent from here on
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned char* ring = fd_dyn + (size_t)warp * kFdStages * R::stage_bytes;
-  const int V = p.V, C = p.FC;
-  const long long N = (long long)p.B * C;
-  const long long NW = (long long)gridDim.x * kFdWarps;
-  const long long g = (long long)blockIdx.x * kFdWarps + warp;
-  const int i0 = (int)(g * N / NW), i1 = (int)((g + 1) * N / NW);
-  if (i0 >= i1) {
-    pdl_wait();
-    return;
+// Block-wide inclusive scan of two-float values in thread order (every
+// thread gets its inclusive prefix, its exclusive prefix and the total).
+__device__ __forceinline__ void fd_block_scan(F2 v, F2* wsum, F2* inc_out, F2* ex_out, F2* tot_out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const F2 inc = warp_incl_scan_f2(v);
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  F2 off{0.f, 0.f}, tot{0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < kFdWarps; ++w) {
+    if (w < warp) off = f2_add(off, wsum[w]);
+    tot = f2_add(tot, wsum[w]);
   }
+  F2 below = f2_shfl_up(inc, 1);
+  if (lane == 0) below = F2{0.f, 0.f};
+  *ex_out = f2_add(off, below);
+  *inc_out = f2_add(off, inc);
+  *tot_out = tot;
+  __syncthreads();   // wsum may be reused right after
+}
+
+struct FdSmem {
+  float tab[128];            // exp2_f2 table
+  F2 wsum[kFdWarps];
+  int found, last, owner, lastpos;
+  F2 base, lastbase, tbase;
+  int token;
+  int is_last;               // this CTA completed the sequence (ticket)
+};
+
+// The inverse-CDF search of sequence s (b) by its CTA, after every warp
+// stored its items' sums: the exact normaliser s = sum S, the item masses
+// (A - (s - s') Q for a residual, S for the bonus draw or the fallback to p_n
+// when the residual has no mass), a block scan over the items (its total is
+// R, so the search agrees with it), the item holding u * R, then the token
+// among the item's 2048 (thread t the four at 4 t).  If rounding leaves no interval
+// holding the target, the last positive one is taken, at each level.
+template <typename T, bool MASK>
+__device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq<T>& s, FdSmem& sm, int* resid0_out) {
+  constexpr bool EXACT = sizeof(T) == 2;
+  const int tid = threadIdx.x;
+  const int G1 = p.gamma + 1, V = p.V, C = p.FC;
+  const float u = __ldg(p.uniforms + b * G1 + s.gb);
+  const float4* SA = p.fd_part + (size_t)b * C;
+  const float* QQ = p.fd_q + (size_t)b * C;
+  *resid0_out = 0;
+  if (s.mode == FD_SKIP) return 0;
+  const bool resid = s.n < s.gb;
+  F2 sl{0.f, 0.f};
+  for (int k = tid; k < C; k += kFdThreads) {
+    const float4 v = __ldcg(SA + k);
+    sl = f2_add(sl, F2{v.x, v.y});
+  }
+  F2 inc, ex, tot;
+  fd_block_scan(sl, sm.wsum, &inc, &ex, &tot);   // its total: the exact normaliser s
+  const F2 ds = f2_add(tot, F2{-s.s_a, 0.f});     // s - s', tiny
+  bool use_q = resid;
+  auto mass = [&](int k) -> F2 {
+    const float4 v = __ldcg(SA + k);
+    if (!use_q) return F2{v.x, v.y};
+    F2 m = f2_add(F2{v.z, v.w}, f2_neg(f2_scale(ds, __ldcg(QQ + k))));
+    if (m.hi < 0.f) m = F2{0.f, 0.f};
+    return m;
+  };
+  // items k = round * 512 + tid, rounds chained by a carry; two passes: the
+  // total R, then the search (the same additions)
+  F2 R{0.f, 0.f}, target{0.f, 0.f};
+  int item = -1;
+  F2 ibase{0.f, 0.f};
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    for (int pass = 0; pass < 2; ++pass) {
+      __syncthreads();   // every thread has read the previous pass's result
+      if (tid == 0) {
+        sm.found = 0x7fffffff;
+        sm.last = -1;
+      }
+      F2 carry{0.f, 0.f};
+      for (int k0 = 0; k0 < C; k0 += kFdThreads) {
+        const int k = k0 + tid;
+        const F2 m = k < C ? mass(k) : F2{0.f, 0.f};
+        fd_block_scan(m, sm.wsum, &inc, &ex, &tot);
+        ex = f2_add(carry, ex);
+        if (pass == 1 && k < C && f2_pos(m)) {
+          if (!f2_lt(target, ex) && f2_lt(target, f2_add(ex, m))) {
+            sm.found = k;   // at most one k
+            sm.base = ex;
+          }
+          atomicMax(&sm.last, k);
+        }
+        __syncthreads();
+        if (pass == 1 && k == sm.last) sm.lastbase = ex;
+        carry = f2_add(carry, tot);
+        __syncthreads();
+        if (pass == 1 && sm.found != 0x7fffffff) break;
+      }
+      if (pass == 0) {
+        R = carry;
+        target = f2_scale(R, u);
+      }
+    }
+    if (resid && use_q && !f2_pos(R)) {
+      *resid0_out = 1;   // zero residual mass (only through rounding): draw from p_n
+      use_q = false;
+      continue;
+    }
+    break;
+  }
+  if (!f2_pos(R)) return 0;
+  const bool take_last = sm.found == 0x7fffffff;
+  item = take_last ? sm.last : sm.found;
+  ibase = take_last ? sm.lastbase : sm.base;
+  if (item < 0) return 0;
+  // ---- the token: thread t has the TPT consecutive tokens at item * kFdTok + TPT t
+  constexpr int TPT = kFdTok / kFdThreads;
+  const int mode = use_q ? s.mode : FD_NONE;
+  const int v0 = item * kFdTok + TPT * tid;
+  F2 tm[TPT];
+  F2 m{0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < TPT; ++j) {
+    const int v = v0 + j;
+    tm[j] = F2{0.f, 0.f};
+    if (v < V) {
+      const float x = Tr<T>::get(load_slot<T>(s.row, v, 1, false), 0);
+      if (!MASK || tp_kept<T>(x, v, s.K, s.idx)) {
+        float qv = 0.f;
+        if (mode == FD_DENSE) qv = __ldcg(s.qrow + v);
+        else if (mode == FD_QL) qv = s.qlr.q(Tr<T>::get(load_slot<T>(s.qlrow, v, 1, false), 0), p.c, p.c_lo);
+        else if (mode == FD_DET) qv = v == s.xq ? INFINITY : 0.f;
+        tm[j] = token_mass<EXACT>(x, qv, use_q, s.M, p.c, p.c_lo, s.s_a, ds, sm.tab);
+      }
+    }
+    m = f2_add(m, tm[j]);
+  }
+  fd_block_scan(m, sm.wsum, &inc, &ex, &tot);
+  ex = f2_add(ibase, ex);
+  if (tid == 0) {
+    sm.owner = 0x7fffffff;
+    sm.lastpos = -1;
+  }
+  __syncthreads();
+  if (f2_pos(m)) {
+    if (!take_last && !f2_lt(target, ex) && f2_lt(target, f2_add(ex, m))) atomicMin(&sm.owner, tid);
+    atomicMax(&sm.lastpos, tid);
+  }
+  __syncthreads();
+  const bool tlast = sm.owner == 0x7fffffff;
+  const int owner = tlast ? sm.lastpos : sm.owner;
+  if (tid == owner) {
+    // the token within this thread's run (the same additions as its total)
+    F2 lb = ex;
+    int first = -1, lastp = -1;
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) {
+      if (f2_pos(tm[j])) {
+        if (first < 0 && !take_last && !tlast && !f2_lt(target, lb) && f2_lt(target, f2_add(lb, tm[j]))) first = j;
+        lastp = j;
+      }
+      lb = f2_add(lb, tm[j]);
+    }
+    sm.token = v0 + (first >= 0 ? first : lastp);
+  }
+  __syncthreads();
+  return owner >= 0 ? sm.token : 0;
+}
+
+// MASK: top-p alone (the rows' records come from topp_row_kernel).
+// Work unit u = (sequence b = u / Z, part z = u % Z): part z sums items
+// [z C / Z, (z + 1) C / Z) of row n; the CTA that completes a sequence's last
+// part (an acquire-release ticket) runs its search.  Z = p.FZ parts per
+// sequence, so that B * Z units fill the GPU's SMs once.
+template <typename T, bool MASK>
+__global__ void __launch_bounds__(kFdThreads, 1) final_draw_kernel(const Params p) {
+  using R = FdRing<T>;
+  constexpr int S = R::S;
+  extern __shared__ __align__(16) unsigned char fd_dyn[];
+  __shared__ FdSmem sm;
+  load_exp2_table(sm.tab);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* ring = fd_dyn + (size_t)warp * S * R::stage_bytes;
+  const int G = p.gamma, G1 = G + 1, V = p.V, C = p.FC, Z = p.FZ;
+  const int U = p.B * Z;
   const bool vec = (V & 3) == 0;
-  const bool scan = p.H > 0;   // streaming path: the row partials are merged here
-  const int b0 = i0 / C;
-  // inputs of the first sequence's acceptance tests, before the wait
+  const bool scan = !MASK && p.H > 0;   // streaming path: the row partials are merged here
+  // the first unit's acceptance inputs, before the dependency wait
   FdDrafts dr;
-  int dr_b = -1;   // the sequence dr holds
-  if (scan) {
-    fd_gather<T>(p, b0, dr);
-    dr_b = b0;
+  int dr_b = -1;
+  if (scan && (int)blockIdx.x < U) {
+    dr_b = blockIdx.x / Z;
+    fd_gather<T>(p, dr_b, dr);
   }
   pdl_wait();   // the row statistics come from the previous kernel
-  // The issuer runs up to kFdStages items ahead of the consumer; it reaches
-  // each sequence first (and scans it), the consumer takes a copy of its state.
-  FdSeq<T> is, cs;
-  int is_b = -1, cs_b = -1;
-  auto reach = [&](int b) {
-    if (scan) {
+  __syncthreads();
+  for (int u = blockIdx.x; u < U; u += gridDim.x) {
+    const int b = u / Z, z = u - b * Z;
+    const int k0 = (int)((long long)z * C / Z), k1 = (int)((long long)(z + 1) * C / Z);
+    // every warp: sequence b's state (part 0's warp 0 writes the outputs but the token)
+    FdSeq<T> s;
+    const bool writer = z == 0 && warp == 0;
+    if (MASK) {
+      fd_scan_tp<T>(p, b, writer, s);
+    } else if (scan) {
       if (b != dr_b) {
         fd_gather<T>(p, b, dr);
         dr_b = b;
       }
-      fd_scan<T>(p, b, dr, (long long)b * C >= i0, is);
+      fd_scan<T>(p, b, dr, writer, s);
     } else {
-      fd_load_state<T>(p, b, is);
+      fd_load_state<T>(p, b, s);
     }
-    is_b = b;
-  };
-  int ki = i0;
-#pragma unroll 1
-  for (int st = 0; st < kFdStages; ++st) {
-    if (ki < i1) {
-      const int b = ki / C;
-      if (b != is_b) reach(b);
-      fd_issue(is, ki - b * C, V, vec, ring + st * R::stage_bytes);
-      ++ki;
-    }
-    fd_commit();
-  }
-  int stage = 0;
-  int cs_end = -1;   // first item past the consumer's sequence
-  // Items are reduced across the warp four at a time (transposed butterfly):
-  // the lane sums of the batch's items sit in slots 0..3 (slot 0 the latest).
-  for (int kb = i0; kb < i1; kb += 4) {
-    const int nb = min(4, i1 - kb);
-    IT5 slot[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) slot[j] = IT5{};
-#pragma unroll 1
-    for (int kc = kb; kc < kb + nb; ++kc) {
-      fd_wait_ring();
-      if (kc >= cs_end) {
-        // the consumer reaches a new sequence: the issuer is on it unless it
-        // has already moved on (fewer than kFdStages items of this sequence
-        // left in the range), in which case the state is rebuilt
-        const int b = kc / C;
-        if (b != is_b) {
-          const int keep_b = is_b;
-          FdSeq<T> keep = is;
-          reach(b);
-          cs = is;
-          is = keep;
-          is_b = keep_b;
-        } else {
-          cs = is;
+    // ---- warp w sums items k0 + w, k0 + w + 16, ... of the part, chunk by
+    // chunk through its ring (the issuer S chunks ahead of the consumer)
+    int ki = k0 + warp, kj = 0, stage = 0;
+    auto issue_next = [&](unsigned char* dst) {
+      if (ki < k1) {
+        fd_issue(s, ki * kFdTok + kj * kFdChunk, V, vec, dst);
+        if (++kj == kFdChunks) {
+          kj = 0;
+          ki += kFdWarps;
         }
-        cs_b = b;
-        cs_end = (b + 1) * C;
-      }
-      const int c = kc - cs_b * C;
-      unsigned char* st = ring + stage * R::stage_bytes;
-      FdAcc acc;
-      acc.S[0] = acc.S[1] = acc.A[0] = acc.A[1] = acc.Q[0] = acc.Q[1] = 0.f;
-      acc.top.zero();
-      const bool full = (c + 1) * kFdTok <= V;
-      switch (cs.mode * 2 + (full ? 1 : 0)) {
-        case FD_NONE * 2 + 1: fd_sweep<T, FD_NONE, true>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        case FD_NONE * 2: fd_sweep<T, FD_NONE, false>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        case FD_DENSE * 2 + 1: fd_sweep<T, FD_DENSE, true>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        case FD_DENSE * 2: fd_sweep<T, FD_DENSE, false>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        case FD_DET * 2 + 1: fd_sweep<T, FD_DET, true>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        case FD_DET * 2: fd_sweep<T, FD_DET, false>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        case FD_QL * 2 + 1: fd_sweep<T, FD_QL, true>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        case FD_QL * 2: fd_sweep<T, FD_QL, false>(cs, st, c, V, p.c, p.c_lo, tab, acc); break;
-        default: break;   // a bad row: nothing was read
-      }
-      // this stage has been read: refill it with the item kFdStages ahead
-      if (ki < i1) {
-        const int b2 = ki / C;
-        if (b2 != is_b) reach(b2);
-        fd_issue(is, ki - b2 * C, V, vec, st);
-        ++ki;
       }
       fd_commit();
-      stage = stage + 1 == kFdStages ? 0 : stage + 1;
-      slot[3] = slot[2];
-      slot[2] = slot[1];
-      slot[1] = slot[0];
-      slot[0] = IT5::of(f2_add(f2_add(F2{acc.S[0], 0.f}, F2{acc.S[1], 0.f}), acc.top.S()),
-                        f2_add(f2_add(F2{acc.A[0], 0.f}, F2{acc.A[1], 0.f}), acc.top.A()),
-                        acc.Q[0] + acc.Q[1] + acc.top.q);
+    };
+#pragma unroll 1
+    for (int st = 0; st < S; ++st) issue_next(ring + st * R::stage_bytes);
+    for (int kb = k0 + warp; kb < k1; kb += 4 * kFdWarps) {
+      const int nb = min(4, (k1 - kb + kFdWarps - 1) / kFdWarps);
+      IT5 slot[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) slot[j] = IT5{};
+#pragma unroll 1
+      for (int j = 0; j < nb; ++j) {
+        const int c = kb + j * kFdWarps;
+        // the item's lane sums: the float32 sums of each chunk folded into two-float
+        F2 iS{0.f, 0.f}, iA{0.f, 0.f};
+        float iQ = 0.f;
+        RunAcc top;
+        top.zero();
+#pragma unroll 1
+        for (int h = 0; h < kFdChunks; ++h) {
+          fd_wait_ring<S>();
+          unsigned char* stp = ring + stage * R::stage_bytes;
+          FdAcc acc;
+          acc.S[0] = acc.S[1] = acc.A[0] = acc.A[1] = acc.Q[0] = acc.Q[1] = 0.f;
+          acc.top = top;
+          const int tc = c * kFdTok + h * kFdChunk;
+          switch (s.mode) {
+            case FD_NONE: fd_sweep<T, FD_NONE, MASK>(s, stp, tc, p.c, p.c_lo, sm.tab, acc); break;
+            case FD_DENSE: fd_sweep<T, FD_DENSE, MASK>(s, stp, tc, p.c, p.c_lo, sm.tab, acc); break;
+            case FD_DET: fd_sweep<T, FD_DET, MASK>(s, stp, tc, p.c, p.c_lo, sm.tab, acc); break;
+            case FD_QL: fd_sweep<T, FD_QL, MASK>(s, stp, tc, p.c, p.c_lo, sm.tab, acc); break;
+            default: break;   // a bad row: nothing was read
+          }
+          // this stage has been read: refill it S chunks ahead
+          issue_next(stp);
+          stage = stage + 1 == S ? 0 : stage + 1;
+          top = acc.top;
+          iS = f2_add(iS, F2{acc.S[0] + acc.S[1], 0.f});
+          iA = f2_add(iA, F2{acc.A[0] + acc.A[1], 0.f});
+          iQ += acc.Q[0] + acc.Q[1];
+        }
+        slot[3] = slot[2];
+        slot[2] = slot[1];
+        slot[1] = slot[0];
+        slot[0] = IT5::of(f2_add(iS, top.S()), f2_add(iA, top.A()), iQ + top.q);
+      }
+      // slot j holds item kb + (nb - 1 - j) * 16; every lane of group
+      // g = lane / 8 then holds slot g's warp total
+      const IT5 tot = it5_reduce4(slot);
+      const int g = lane >> 3;
+      if ((lane & 7) == 0 && g < nb) {
+        const int c = kb + (nb - 1 - g) * kFdWarps;
+        p.fd_part[(size_t)b * C + c] = make_float4(tot.S.hi, tot.S.lo, tot.A.hi, tot.A.lo);
+        p.fd_q[(size_t)b * C + c] = tot.Q;
+      }
     }
-    // slot j holds item kb + nb - 1 - j; after the butterfly every lane of
-    // group g = lane / 8 holds slot g's warp total
-    const IT5 tot = it5_reduce4(slot);
-    const int g = lane >> 3;
-    if ((lane & 7) == 0 && g < nb) {
-      const int k = kb + nb - 1 - g;
-      const int b = k / C, c = k - b * C;
-      p.fd_part[(size_t)b * C + c] = make_float4(tot.S.hi, tot.S.lo, tot.A.hi, tot.A.lo);
-      p.fd_q[(size_t)b * C + c] = tot.Q;
-    }
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- the search
-
-struct PickSmem {
-  float tab[128];
-  F2 wsum[kPickThreads / 32];
-  F2 carry;
-  F2 base, lastbase;
-  int found, last;
-  int owner, lastpos;
-  int token;
-};
-
-// Block-wide inverse-CDF search over NT two-float masses mass(k) in index
-// order: the total R, then the first k whose running interval [prefix_k,
-// prefix_k + m_k) holds t = u * R (both passes add in the same order), else
-// the last k with positive mass.  Returns k (-1 if R <= 0) and its exclusive
-// prefix in *base_out, R in *R_out and t in *t_out, in every thread.
-template <typename F>
-__device__ int pick_locate(F mass, int NT, float u, F2* R_out, F2* base_out, F2* t_out, PickSmem& ls) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int nw = kPickThreads / 32;
-  F2 R{0.f, 0.f}, t{0.f, 0.f};
-  for (int pass = 0; pass < 2; ++pass) {
-    t = f2_scale(R, u);
+    // ---- the part is summed: the last part of the sequence searches
     __syncthreads();
     if (tid == 0) {
-      ls.carry = F2{0.f, 0.f};
-      ls.found = 0x7fffffff;
-      ls.last = -1;
-      ls.lastbase = F2{0.f, 0.f};
+      // release: this part's item sums; acquire: the other parts' (last arrival)
+      const int prev = Z > 1 ? atomic_add_acq_rel_gpu(p.seq_ticket2 + b, 1) : Z - 1;
+      sm.is_last = prev == Z - 1;
     }
     __syncthreads();
-    for (int c0 = 0; c0 < NT; c0 += kPickThreads) {
-      const int k = c0 + tid;
-      const F2 m = k < NT ? mass(k) : F2{0.f, 0.f};
-      const F2 inc = warp_incl_scan_f2(m);
-      if (lane == 31) ls.wsum[warp] = inc;
-      __syncthreads();
-      F2 off = ls.carry, tot = ls.carry;
-#pragma unroll
-      for (int w = 0; w < nw; ++w) {
-        if (w < warp) off = f2_add(off, ls.wsum[w]);
-        tot = f2_add(tot, ls.wsum[w]);
+    if (sm.is_last) {
+      int resid0 = 0;
+      const int token = fd_pick_block<T, MASK>(p, b, s, sm, &resid0);
+      // the output; the item sums, the row partials, the row records, the
+      // ticket and the state zeroed behind it
+      for (int k = tid; k < C; k += kFdThreads) {
+        p.fd_part[(size_t)b * C + k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.fd_q[(size_t)b * C + k] = 0.f;
       }
-      F2 below = f2_shfl_up(inc, 1);
-      if (lane == 0) below = F2{0.f, 0.f};
-      const F2 excl = f2_add(off, below);
-      if (pass == 1 && k < NT && f2_pos(m)) {
-        if (!f2_lt(t, excl) && f2_lt(t, f2_add(excl, m))) atomicMin(&ls.found, k);
-        atomicMax(&ls.last, k);
-      }
-      __syncthreads();
-      if (pass == 1 && k < NT) {
-        if (ls.found == k) ls.base = excl;
-        if (ls.last == k) ls.lastbase = excl;
-      }
-      if (tid == 0) ls.carry = tot;
-      __syncthreads();
-      if (pass == 1 && ls.found != 0x7fffffff) break;
-    }
-    if (pass == 0) R = ls.carry;
-  }
-  __syncthreads();
-  *R_out = R;
-  *t_out = t;
-  if (!f2_pos(R)) return -1;
-  if (ls.found != 0x7fffffff) {
-    *base_out = ls.base;
-    return ls.found;
-  }
-  *base_out = ls.lastbase;
-  return ls.last;
-}
-
-// The item search with every item's sums read once into registers (thread t
-// holds items t, t + 256, ...; C <= 256 * kPickRegItems): the masses, one
-// block-wide inclusive scan per 256 items chained by a carry (its total is
-// R, so the search and the total agree), and the first item whose interval
-// holds u * R, else the last positive one.  Same results as pick_locate.
-template <int KP>
-__device__ int pick_items_fast_t(const float4* SA, const float* QQ, int C, bool use_q, F2 ds, float u, F2* R_out,
-                                 F2* base_out, F2* t_out, PickSmem& ls) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int nw = kPickThreads / 32;
-  F2 m[KP], ex[KP];
-#pragma unroll
-  for (int j = 0; j < KP; ++j) {
-    const int k = j * kPickThreads + tid;
-    m[j] = F2{0.f, 0.f};
-    if (k < C) {
-      const float4 v = __ldcg(SA + k);
-      if (!use_q) {
-        m[j] = F2{v.x, v.y};
-      } else {
-        m[j] = f2_add(F2{v.z, v.w}, f2_neg(f2_scale(ds, __ldcg(QQ + k))));
-        if (m[j].hi < 0.f) m[j] = F2{0.f, 0.f};
-      }
-    }
-  }
-  F2 carry{0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < KP; ++j) {
-    if (j * kPickThreads >= C) break;
-    const F2 inc = warp_incl_scan_f2(m[j]);
-    __syncthreads();   // wsum of the previous round has been read
-    if (lane == 31) ls.wsum[warp] = inc;
-    __syncthreads();
-    F2 off = carry, tot = carry;
-#pragma unroll
-    for (int w = 0; w < nw; ++w) {
-      if (w < warp) off = f2_add(off, ls.wsum[w]);
-      tot = f2_add(tot, ls.wsum[w]);
-    }
-    F2 below = f2_shfl_up(inc, 1);
-    if (lane == 0) below = F2{0.f, 0.f};
-    ex[j] = f2_add(off, below);
-    carry = tot;
-  }
-  const F2 R = carry;
-  const F2 t = f2_scale(R, u);
-  if (tid == 0) {
-    ls.found = 0x7fffffff;
-    ls.last = -1;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < KP; ++j) {
-    const int k = j * kPickThreads + tid;
-    if (k < C && f2_pos(m[j])) {
-      if (!f2_lt(t, ex[j]) && f2_lt(t, f2_add(ex[j], m[j]))) atomicMin(&ls.found, k);
-      atomicMax(&ls.last, k);
-    }
-  }
-  __syncthreads();
-  const int found = ls.found, last = ls.last;
-#pragma unroll
-  for (int j = 0; j < KP; ++j) {
-    const int k = j * kPickThreads + tid;
-    if (k == found) ls.base = ex[j];
-    if (k == last) ls.lastbase = ex[j];
-  }
-  __syncthreads();
-  *R_out = R;
-  *t_out = t;
-  const int item = !f2_pos(R) ? -1 : (found != 0x7fffffff ? found : last);
-  *base_out = found != 0x7fffffff ? ls.base : ls.lastbase;
-  __syncthreads();   // ls may be reused right after
-  return item;
-}
-constexpr int kPickRegItems = 4;
-__device__ __forceinline__ int pick_items_fast(const float4* SA, const float* QQ, int C, bool use_q, F2 ds, float u,
-                                               F2* R_out, F2* base_out, F2* t_out, PickSmem& ls) {
-  if (C <= kPickThreads) return pick_items_fast_t<1>(SA, QQ, C, use_q, ds, u, R_out, base_out, t_out, ls);
-  return pick_items_fast_t<kPickRegItems>(SA, QQ, C, use_q, ds, u, R_out, base_out, t_out, ls);
-}
-
-// One CTA per sequence after final_draw_kernel: the exact normaliser
-// s = sum S, the item masses (A - (s - s') Q for a residual, S for the bonus
-// or the fallback to p_n), the item holding u * R, then the token inside it
-// (each thread two consecutive tokens of the item), the output, and the
-// workspace zeroed behind it.
-template <typename T>
-__global__ void __launch_bounds__(kPickThreads) final_pick_kernel(const Params p) {
-  constexpr bool EXACT = sizeof(T) == 2;
-  __shared__ PickSmem sm;
-  const int tid = threadIdx.x;
-  const int b = blockIdx.x;
-  const int G = p.gamma, G1 = G + 1, V = p.V, C = p.FC;
-  load_exp2_table(sm.tab);
-  const int gb = seq_gamma(p, b);
-  const float u = __ldg(p.uniforms + b * G1 + gb);   // an input: before the wait
-  pdl_wait();
-  __syncthreads();
-  FdSeq<T> s;
-  fd_load_state<T>(p, b, s);
-  const bool bad = s.mode == FD_SKIP;
-  const bool resid = s.n < gb;
-  float4* SA = p.fd_part + (size_t)b * C;
-  float* QQ = p.fd_q + (size_t)b * C;
-  int token = 0, resid0 = 0;
-  if (!bad) {
-    F2 sl{0.f, 0.f};
-    for (int k = tid; k < C; k += kPickThreads) {
-      const float4 v = __ldcg(SA + k);
-      sl = f2_add(sl, F2{v.x, v.y});
-    }
-    const F2 sum = block_sum_f2(sl, sm.wsum);
-    const F2 ds = f2_add(sum, F2{-s.s_a, 0.f});   // s - s', tiny
-    bool use_q = resid;
-    auto mass = [&](int k) -> F2 {
-      const float4 v = __ldcg(SA + k);
-      if (!use_q) return F2{v.x, v.y};
-      F2 m = f2_add(F2{v.z, v.w}, f2_neg(f2_scale(ds, __ldcg(QQ + k))));
-      if (m.hi < 0.f) m = F2{0.f, 0.f};
-      return m;
-    };
-    F2 R{0.f, 0.f}, base{0.f, 0.f}, target{0.f, 0.f};
-    int item;
-    if (C <= kPickThreads * kPickRegItems) {
-      item = pick_items_fast(SA, QQ, C, use_q, ds, u, &R, &base, &target, sm);
-      if (resid && !f2_pos(R)) {
-        resid0 = 1;   // zero residual mass (only through rounding): draw from p_n
-        use_q = false;
-        item = pick_items_fast(SA, QQ, C, use_q, ds, u, &R, &base, &target, sm);
-      }
-    } else {
-      item = pick_locate(mass, C, u, &R, &base, &target, sm);
-      if (resid && !f2_pos(R)) {
-        resid0 = 1;
-        use_q = false;
-        item = pick_locate(mass, C, u, &R, &base, &target, sm);
-      }
-    }
-    if (item >= 0) {
-      // ---- the item's tokens: this thread's two, their masses
-      const int mode = use_q ? s.mode : FD_NONE;
-      const int t0 = item * kFdTok + 2 * tid;
-      F2 tm[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int v = t0 + j;
-        tm[j] = F2{0.f, 0.f};
-        if (v < V) {
-          const float x = Tr<T>::get(load_slot<T>(s.row, v, 1, false), 0);
-          float qv = 0.f;
-          if (mode == FD_DENSE) qv = __ldcg(s.qrow + v);
-          else if (mode == FD_QL) qv = s.qlr.q(Tr<T>::get(load_slot<T>(s.qlrow, v, 1, false), 0), p.c, p.c_lo);
-          else if (mode == FD_DET) qv = v == s.xq ? INFINITY : 0.f;
-          tm[j] = token_mass<EXACT>(x, qv, use_q, s.M, p.c, p.c_lo, s.s_a, ds, sm.tab);
+      if (scan) {
+        const int E = G1 * stream_np(p);
+        for (int e = tid; e < E; e += kFdThreads) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.ql) {
+          const int Eq = G * stream_np(p);
+          for (int e = tid; e < Eq; e += kFdThreads) p.qpart[(size_t)b * Eq + e] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      const F2 mine = f2_add(tm[0], tm[1]);
-      F2 total;
-      const F2 ex = block_exclusive_f2(mine, sm.wsum, &total);
-      const F2 tb = f2_add(base, ex);
+      if (MASK) {
+        for (int e = tid; e < G1 * (int)(sizeof(TpRow) / 4); e += kFdThreads)
+          reinterpret_cast<int*>(p.tp + (size_t)b * G1)[e] = 0;
+      }
       if (tid == 0) {
-        sm.owner = 0x7fffffff;
-        sm.lastpos = -1;
-      }
-      __syncthreads();
-      const bool pos = f2_pos(mine);
-      if (pos && !f2_lt(target, tb) && f2_lt(target, f2_add(tb, mine))) atomicMin(&sm.owner, tid);
-      if (pos) atomicMax(&sm.lastpos, tid);
-      __syncthreads();
-      // rounding can leave no thread's interval holding the target: take the last positive one
-      const bool take_last = sm.owner == 0x7fffffff;
-      const int owner = take_last ? sm.lastpos : sm.owner;
-      if (tid == owner) {
-        int pick = -1, lastp = -1;
-        F2 lb = tb;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if (f2_pos(tm[j])) {
-            if (pick < 0 && !take_last && !f2_lt(target, lb) && f2_lt(target, f2_add(lb, tm[j]))) pick = j;
-            lastp = j;
-          }
-          lb = f2_add(lb, tm[j]);
+        p.out_tokens[b * G1 + s.n] = token;
+        if (p.out_status) p.out_status[b] = s.status | (resid0 ? SEQ_RESID0 : 0);
+        p.seq_ticket2[b] = 0;
+        if (!scan && !MASK) {   // the rows kernel's state
+          SeqState zs;
+          zs.n = 0; zs.status = 0; zs.M = 0.f; zs.qm = 0.f; zs.s = 0.0; zs.qinv = 0.f; zs.qbad = 0; zs.tpK = 0u; zs.tpIdx = 0;
+          p.seq[b] = zs;
         }
-        sm.token = t0 + (pick >= 0 ? pick : lastp);
       }
-      __syncthreads();
-      token = owner >= 0 ? sm.token : 0;
     }
+    __syncthreads();   // shared state reused by the next unit
   }
-  // the output; the item sums, the row partials and the state zeroed behind it
-  for (int k = tid; k < C; k += kPickThreads) {
-    SA[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    QQ[k] = 0.f;
-  }
-  if (p.H > 0) {
-    const int E = G1 * stream_np(p);
-    for (int e = tid; e < E; e += kPickThreads) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (p.ql) {
-      const int Eq = G * stream_np(p);
-      for (int e = tid; e < Eq; e += kPickThreads) p.qpart[(size_t)b * Eq + e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  if (tid == 0) {
-    p.out_tokens[b * G1 + s.n] = token;
-    if (p.out_status) p.out_status[b] = s.status | (resid0 ? SEQ_RESID0 : 0);
-    SeqState z;
-    z.n = 0; z.status = 0; z.M = 0.f; z.qm = 0.f; z.s = 0.0; z.qinv = 0.f; z.qbad = 0;
-    p.seq[b] = z;
-  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 }  // namespace sv

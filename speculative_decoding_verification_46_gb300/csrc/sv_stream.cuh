@@ -21,8 +21,8 @@
 //            scans the drafts and emits the tokens
 //   softmax  online max / sum of 2^((L - m) c) with rescaling when the
 //            running max grows; final_draw_kernel merges the segments,
-//            computes p(d_i) and a_i, scans and sums the final draw's items,
-//            final_pick_kernel locates the drawn token (sv_final.cuh)
+//            computes p(d_i) and a_i, scans, sums the final draw's items and
+//            locates the drawn token (sv_final.cuh)
 //   top-k    pass 1 keeps per-thread maxima (and the two best vectors); the
 //            k-th largest is a lower bound tau of the row's k-th value; only
 //            threads with a third vector reaching tau are re-read (L2);

@@ -1,0 +1,291 @@
+// Top-p without top-k, for any vocabulary ("11.1 核心原理", section 11.1.2:
+// top-p is applied to p before the test; the kept set is the shortest prefix
+// of the ranking by (logit descending, index ascending) whose renormalised
+// mass reaches top_p, the crossing token included).
+//
+// topp_row_kernel: one CTA per row of logits.  The kept set is
+//   { v : key(v) > K }  U  { v : key(v) = K and v <= idx }
+// with key the order-preserving key of the logit.  K and idx are found
+// exactly, without sorting:
+//   1. the row maximum M (a row holding NaN or +inf, or only -inf, defines no
+//      distribution);
+//   2. mass-weighted bisection over the key: each pass reads the row, adds
+//      the weight w = 2^((x - M) c) of every token whose key lies in the
+//      current key range into one of 16 buckets (a thread-private column of a
+//      shared-memory histogram: no atomics, a fixed order of additions), sums
+//      the columns in two-float and keeps the bucket where the mass above it
+//      plus the bucket's own first reaches top_p * (total); 4 key bits per
+//      pass until a single key K remains (bf16: 4 passes; float16 5; float32
+//      8);
+//   3. the tokens with key K all have one weight w_K: the first
+//      j = ceil((top_p * total - mass above K) / w_K) of them in index order
+//      are kept (a block scan of per-thread counts over contiguous index
+//      ranges finds the j-th), idx = its index.
+// The kept mass W (two-float), and for a drafted row its acceptance
+// probability a_i = min(1, (w(d_i) / W) / q_i(d_i)) (0 if d_i is not kept),
+// go to the row's record; final_draw_kernel<T, true> then scans, and draws
+// from max(p~_n - q_n, 0) (or p~_gamma) with the same mask.
+#pragma once
+
+#include "sv_device.cuh"
+
+namespace sv {
+
+constexpr int kTpThreads = 512;
+constexpr int kTpBits = 4;
+constexpr int kTpBuckets = 1 << kTpBits;
+
+// Per-row result of topp_row_kernel.
+struct TpRow {
+  float M;         // row maximum
+  uint32_t K;      // crossing key (okey(x) >> KEY_LOW_BIT)
+  int idx;         // last kept index among the tokens with key K
+  float a;         // acceptance probability of the row's draft (rows i < gamma_b)
+  float Wh, Wl;    // kept mass: sum over kept v of 2^((x_v - M) c), two-float
+  int status;      // SEQ_OOB / SEQ_QBAD of the row's test; SEQ_BADROW
+  int pad;
+};
+
+struct TpSmem {
+  float hist[kTpBuckets][kTpThreads];   // thread-private bucket columns
+  F2 tot[kTpBuckets];
+  F2 wred[kTpThreads / 32];
+  float fred[kTpThreads / 32];
+  int ired[kTpThreads / 32];
+  uint32_t lo;
+  int width, pick, bad;
+  F2 above;
+  int cnt_base[kTpThreads / 32];
+  int idx;
+  float weq;
+};
+
+// Order-preserving key of a logit of type T (the bits that can differ).
+template <typename T>
+__device__ __forceinline__ uint32_t tp_key(float x) {
+  return okey(x) >> Tr<T>::KEY_LOW_BIT;
+}
+// Is token v (logit x) in the kept set (K, idx)?
+template <typename T>
+__device__ __forceinline__ bool tp_kept(float x, int v, uint32_t K, int idx) {
+  const uint32_t k = tp_key<T>(x);
+  return k > K || (k == K && v <= idx);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTpThreads) topp_row_kernel(const Params p, TpRow* rows) {
+  using TR = Tr<T>;
+  constexpr int VW = TR::VW;
+  constexpr int NB = 32 - TR::KEY_LOW_BIT;   // key bits
+  extern __shared__ __align__(16) unsigned char tp_dyn[];
+  TpSmem& sm = *reinterpret_cast<TpSmem*>(tp_dyn);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int nw = kTpThreads / 32;
+  const int G = p.gamma, G1 = G + 1, V = p.V;
+  const int r = blockIdx.x;
+  const int b = r / G1, i = r - b * G1;
+  const int gb = seq_gamma(p, b);
+  if (i > gb) return;   // not part of this round (uniform over the block)
+  const T* row = static_cast<const T*>(p.logits) + (size_t)r * V;
+  const bool vec = (V % VW) == 0;
+  const int NVv = (V + VW - 1) / VW;   // 16-byte slots (the last one partial when !vec)
+  auto slot = [&](int j) -> uint4 {
+    const int e = j * VW;
+    const int nv = min(VW, V - e);
+    return load_slot<T>(row, e, nv, vec && nv == VW);
+  };
+  // the draft's inputs, before anything else (their loads overlap the passes)
+  int d = -1;
+  float qd = 0.f, ld = 0.f;
+  if (tid == 0 && i < gb) {
+    d = __ldg(p.draft + b * G + i);
+    if (d >= 0 && d < V) {
+      ld = TR::get(load_slot<T>(row, d, 1, false), 0);
+      qd = p.q ? __ldg(p.q + ((size_t)b * G + i) * V + d) : 1.f;   // NULL: one-hot draft
+    }
+  }
+  // ---- 1. maximum; NaN / +inf / only -inf: no distribution
+  float m = -INFINITY;
+  int nan = 0;
+  for (int j = tid; j < NVv; j += kTpThreads) {
+    const uint4 v = slot(j);
+    const float vm = TR::template vmax<true>(v);
+    nan |= (vm != vm);
+    m = fmaxf(m, vm);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+  }
+  if (lane == 0) {
+    sm.fred[warp] = m;
+    sm.ired[warp] = nan;
+  }
+  __syncthreads();
+  float M = sm.fred[0];
+  int anynan = sm.ired[0];
+  for (int w = 1; w < nw; ++w) {
+    M = fmaxf(M, sm.fred[w]);
+    anynan |= sm.ired[w];
+  }
+  const bool bad = anynan || !(M > -INFINITY && M < INFINITY);
+  if (bad) {
+    if (tid == 0) {
+      TpRow o{};
+      o.M = 0.f;
+      o.a = 0.f;
+      o.status = SEQ_BADROW | ((i < gb && (d < 0 || d >= V)) ? SEQ_OOB : 0);
+      rows[r] = o;
+    }
+    return;
+  }
+  const float Mc = M * p.c;
+  // ---- 2. mass-weighted bisection over the key
+  uint32_t lo = 0u;
+  int width = NB;
+  F2 above{0.f, 0.f};
+  F2 total{0.f, 0.f};
+  F2 target{0.f, 0.f};
+  bool first = true;
+  while (width > 0) {
+    const int bits = min(kTpBits, width);
+    const int sh = width - bits;
+    const uint64_t span = 1ull << width;
+#pragma unroll
+    for (int k = 0; k < kTpBuckets; ++k) sm.hist[k][tid] = 0.f;
+    for (int j = tid; j < NVv; j += kTpThreads) {
+      const uint4 v = slot(j);
+#pragma unroll
+      for (int t = 0; t < VW; ++t) {
+        if (j * VW + t < V) {
+          const float x = TR::get(v, t);
+          const uint32_t key = tp_key<T>(x);
+          if (key >= lo && (uint64_t)(key - lo) < span) {
+            const float w = ex2_approx(fmaf(x, p.c, -Mc));
+            sm.hist[(key - lo) >> sh][tid] += w;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    // bucket totals: warp w sums bucket w (nw == kTpBuckets) over the columns
+    {
+      F2 acc{0.f, 0.f};
+      for (int c = lane; c < kTpThreads; c += 32) acc = f2_add(acc, F2{sm.hist[warp][c], 0.f});
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc = f2_add(acc, f2_shfl_xor(acc, o));
+      if (lane == 0) sm.tot[warp] = acc;
+    }
+    __syncthreads();
+    if (first) {
+      // the first pass covers every key: the row's total mass
+      total = F2{0.f, 0.f};
+      for (int k = 0; k < kTpBuckets; ++k) total = f2_add(total, sm.tot[k]);
+      target = f2_scale(total, p.top_p);
+      first = false;
+    }
+    // the crossing bucket, from the top: the first whose mass, added to the
+    // mass above it, reaches the target (if rounding leaves none, the lowest
+    // bucket with mass)
+    int pick = -1, lowest = 0;
+    F2 cum = above, cum_low = above;
+    for (int k = (1 << bits) - 1; k >= 0; --k) {
+      if (f2_pos(sm.tot[k])) {
+        lowest = k;
+        cum_low = cum;
+      }
+      const F2 nc = f2_add(cum, sm.tot[k]);
+      if (!f2_lt(nc, target)) {
+        pick = k;
+        break;
+      }
+      cum = nc;
+    }
+    if (pick < 0) {
+      pick = lowest;
+      cum = cum_low;
+    }
+    above = cum;
+    lo += (uint32_t)pick << sh;
+    width = sh;
+    __syncthreads();   // every thread has read tot before the next pass writes hist
+  }
+  const uint32_t K = lo;
+  // ---- 3. ties at K: the j-th in index order; contiguous index ranges per thread
+  const int L = (V + kTpThreads - 1) / kTpThreads;
+  const int v0 = min(tid * L, V), v1 = min(v0 + L, V);
+  int cnt = 0;
+  float weq = 0.f;
+  for (int v = v0; v < v1; ++v) {
+    const float x = TR::get(load_slot<T>(row, v, 1, false), 0);
+    if (tp_key<T>(x) == K) {
+      ++cnt;
+      weq = ex2_approx(fmaf(x, p.c, -Mc));
+    }
+  }
+  // exclusive prefix of the counts
+  int inc = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) sm.ired[warp] = inc;
+  if (cnt > 0) sm.weq = weq;   // every tied token has this weight
+  if (tid == 0) sm.idx = V - 1;
+  __syncthreads();
+  int base = 0, neq = 0;
+  for (int w = 0; w < nw; ++w) {
+    if (w < warp) base += sm.ired[w];
+    neq += sm.ired[w];
+  }
+  base += inc - cnt;
+  const float wK = sm.weq;
+  const F2 need = f2_add(target, f2_neg(above));
+  int jk = (int)ceilf((need.hi + need.lo) / wK);
+  jk = max(1, min(jk, neq));
+  // the thread holding the jk-th tied token finds its index
+  if (cnt > 0 && base < jk && jk <= base + cnt) {
+    int seen = base;
+    for (int v = v0; v < v1; ++v) {
+      const float x = TR::get(load_slot<T>(row, v, 1, false), 0);
+      if (tp_key<T>(x) == K && ++seen == jk) {
+        sm.idx = v;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int idx = sm.idx;
+    const F2 W = f2_add(above, f2_scale(F2{wK, 0.f}, (float)jk));
+    TpRow o{};
+    o.M = M;
+    o.K = K;
+    o.idx = idx;
+    o.Wh = W.hi;
+    o.Wl = W.lo;
+    int st = 0;
+    float a = 0.f;
+    if (i < gb) {
+      if (d < 0 || d >= V) {
+        st |= SEQ_OOB;
+      } else {
+        const bool kept = tp_kept<T>(ld, d, K, idx);
+        const float pd = kept ? exp2f((ld - M) * p.c) / (W.hi + W.lo) : 0.f;
+        if (qd > 0.f) {
+          a = fminf(1.f, pd / qd);
+        } else {
+          a = pd > 0.f ? 1.f : 0.f;
+          st |= SEQ_QBAD;
+        }
+      }
+    }
+    o.a = a;
+    o.status = st;
+    rows[r] = o;
+  }
+}
+
+}  // namespace sv

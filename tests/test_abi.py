@@ -92,8 +92,9 @@ def test_sample_workspace_and_unsupported(sv):
     assert _sample(sv, workspace=None) == sv.SV_ERR_WORKSPACE
     assert _sample(sv, workspace_bytes=16) == sv.SV_ERR_WORKSPACE
     assert _sample(sv, workspace=A + 3) == sv.SV_ERR_WORKSPACE
-    # top-p without top-k over a vocabulary larger than the largest list
-    assert _sample(sv, V=5000, top_k=0, top_p=0.9) == sv.SV_ERR_UNSUPPORTED
+    # top-p without top-k over a vocabulary larger than the largest list: the
+    # per-row threshold path, which validates its workspace before any launch
+    assert _sample(sv, V=5000, top_k=0, top_p=0.9, workspace_bytes=16) == sv.SV_ERR_WORKSPACE
     # gamma = 0 needs neither q nor drafts; B = 0 is an empty call
     assert _sample(sv, B=0) == sv.SV_OK
     assert _sample(sv, gamma=0, q=None, draft_tokens=None, workspace_bytes=16) == sv.SV_ERR_WORKSPACE
@@ -182,7 +183,7 @@ def test_qlogits_validation(sv):
                                            a["d"], a["u"], a["T"], a["k"], a["p"], a["tok"], a["n"], None, None,
                                            a["ws"], a["wsb"], None)
     assert call(k=2000) == sv.SV_ERR_INVALID_ARG             # top_k above SV_MAX_TOP_K
-    assert call(V=2000, p=0.9) == sv.SV_ERR_UNSUPPORTED       # top-p over more than SV_MAX_TOP_K tokens
+    assert call(V=2000, p=0.9) == sv.SV_ERR_UNSUPPORTED       # q from draft logits: top-p alone over > SV_MAX_TOP_K
     assert call(k=10, wsb=sv.sv_qlogits_workspace_bytes(B, G, V, 10) - 256) == sv.SV_ERR_WORKSPACE
     assert call(qdt=7) == sv.SV_ERR_INVALID_ARG
     assert call(T=0.0) == sv.SV_ERR_INVALID_ARG

@@ -112,3 +112,8 @@ def test_algorithmic_bytes_counts_kept_q_reads():
     t = workloads.WORKLOADS["topk50_topp0.9_b256_g8_v152064_bf16"]
     base = bench.algorithmic_bytes(t, np.zeros(256, int))["stream"]
     assert bench.algorithmic_bytes(t, np.zeros(256, int), kept_rejected=1000)["stream"] == base + 4000
+    # top-p alone: row n's logits again, q at the kept tokens of rejected rows
+    tp = workloads.WORKLOADS["topp0.9_b64_g4_v128256_bf16"]
+    ab = bench.algorithmic_bytes(tp, np.zeros(64, int), kept_rejected=1000)
+    assert ab["stream"] == 64 * 5 * 128256 * 2 + 64 * 4 * 6
+    assert ab["final"] == 64 * 128256 * 2 + 4000

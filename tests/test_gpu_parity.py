@@ -203,6 +203,49 @@ def test_topk_small(sv, topk_path, dt, V, G, B, k, tp):
     P.compare_sample(out, P.oracle_sample(inp, 0.8, k, tp), V)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("V,G,B,tp,T", [(40003, 4, 6, 0.9, 1.0), (128256, 4, 4, 0.5, 1.0), (152064, 8, 2, 0.99, 0.8),
+                                        (5000, 3, 10, 0.95, 0.7), (1030, 2, 12, 0.6, 1.3)])
+def test_topp_only_any_vocab(sv, dt, V, G, B, tp, T):
+    """top-p with no top-k beyond SV_MAX_TOP_K tokens (the per-row threshold
+    path): Zipf-like rows with heavy tails (large kept sets) and exact ties."""
+    w = workloads.Workload("topp", B, G, V, dt, "sample", T, top_k=0, top_p=tp, draft_sigma=0.7, seed=V + G)
+    inp = workloads.make_inputs(w, seed=V + int(tp * 100))
+    g = _gpu(inp)
+    out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], T, 0, tp)
+    assert sv.sv_last_kernels() == ["topp_row_kernel", "final_draw_kernel"]
+    P.compare_sample(out, P.oracle_sample(inp, T, 0, tp), V)
+
+
+@pytest.mark.parametrize("V,G,B,tp", [(7, 2, 40, 0.8), (600, 2, 20, 0.9), (1024, 4, 10, 0.5)])
+def test_topp_only_threshold_path_forced_small_vocab(sv, monkeypatch, V, G, B, tp):
+    """The threshold path forced where the list path would run, with many
+    exact ties (rounded logits) and deterministic drafts too."""
+    monkeypatch.setenv("SPECVERIFY_PATH", "topp")
+    inp = _random_case(700 + V, B, G, V, torch.bfloat16, T=0.9, ties=True, spread=1.0, top_k=0, top_p=tp)
+    g = _gpu(inp)
+    out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], 0.9, 0, tp)
+    assert sv.sv_last_kernels() == ["topp_row_kernel", "final_draw_kernel"]
+    P.compare_sample(out, P.oracle_sample(inp, 0.9, 0, tp), V)
+    out = sv.verify_sample(g["logits"], None, g["draft"], g["uniforms"], 0.9, 0, tp)
+    P.compare_sample(out, P.oracle_sample(dict(inp, q=None), 0.9, 0, tp), V)
+
+
+def test_topp_only_degenerate_rows(sv):
+    B, G, V = 6, 3, 3000
+    inp = _random_case(17, B, G, V, torch.float32, top_k=0, top_p=0.9)
+    inp["logits"][0, 2, 100] = float("nan")
+    inp["logits"][1, 0, :] = -float("inf")
+    inp["logits"][2, 1, 5] = float("inf")
+    inp["draft"][3, 1] = V
+    inp["logits"][4, :, 1000:] = -float("inf")
+    for dt in DTYPES.values():
+        case = dict(inp, logits=inp["logits"].to(dt))
+        g = _gpu(case)
+        out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], 1.0, 0, 0.9)
+        P.compare_sample(out, P.oracle_sample(case, 1.0, 0, 0.9), V)
+
+
 def test_topk_heavy_ties_take_the_exact_fallback(sv):
     """All-equal rows: every element ties at the threshold, the candidate
     buffers overflow and the exact (value, index) bisection must pick the

@@ -102,7 +102,7 @@ def test_qlogits_full_size(sv):
     g = _gpu(inp)
     out = sv.verify_sample_qlogits(g["logits"], g["q_logits"], g["draft"], g["uniforms"], T)
     # one dtype on both sides and 16-byte rows: the fused path (q never written out)
-    assert sv.sv_last_kernels() == ["stream_dense_kernel", "final_draw_kernel", "final_pick_kernel"]
+    assert sv.sv_last_kernels() == ["stream_dense_kernel", "final_draw_kernel"]
     arrays = [P.to_np(inp[k]) for k in ("logits", "q_logits", "draft", "uniforms")]
     st = P.compare_sample(out, P.oracle_pool("qlogits", arrays, (T, 0, 1.0)), V)
     assert st["sequences"] == B
@@ -168,7 +168,7 @@ def test_qlogits_leaves_workspace_zero_filled(sv, kind):
     elif kind == "materialised":
         assert names[0] == "q_softmax_kernel", names
     else:
-        assert names == ["stream_dense_kernel", "final_draw_kernel", "final_pick_kernel"], names
+        assert names == ["stream_dense_kernel", "final_draw_kernel"], names
 
 
 def test_qlogits_workspace_shared_with_plain_calls(sv):

@@ -67,8 +67,9 @@ class Workload:
 
 # The five workloads of the verify step (sizes and distributions as stated for
 # the step's headline measurements), plus the two other draft-noise levels of
-# the B=64 sweep, the deterministic-draft (q one-hot, passed as None) case and
-# a ragged round (per-sequence gamma_b, stop tokens, token budgets).
+# the B=64 sweep, the deterministic-draft (q one-hot, passed as None) case, a
+# ragged round (per-sequence gamma_b, stop tokens, token budgets), q given as
+# the draft's logits, and top-p alone over the whole vocabulary.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -93,6 +94,8 @@ WORKLOADS = {
                  draft_sigma=0.7, seed=54, qlogits=True),
         Workload("topk50_topp0.9_qlogits_b256_g8_v152064_bf16", 256, 8, 152064, "bf16", "sample", 0.8,
                  top_k=50, top_p=0.9, draft_sigma=0.7, seed=55, qlogits=True),
+        Workload("topp0.9_b64_g4_v128256_bf16", 64, 4, 128256, "bf16", "sample", 1.0,
+                 top_p=0.9, draft_sigma=0.7, seed=56),
     ]
 }
 
