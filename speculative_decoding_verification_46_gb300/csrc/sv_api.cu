@@ -168,6 +168,9 @@ template <typename T, bool MASK = false>
 sv_status launch_final_draw(const sv::Params& p, cudaStream_t stream) {
   auto kern = sv::final_draw_kernel<T, MASK>;
   const size_t smem = sv::FdRing<T>::bytes;
+  // the search stages a sequence's item sums (float4 + float each) in the ring
+  static_assert(sv::FdRing<T>::bytes >= (size_t)((SV_MAX_VOCAB + sv::kFdTok - 1) / sv::kFdTok) * 20,
+                "ring too small for the item sums of the largest vocabulary");
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_CUDA;

@@ -385,6 +385,15 @@ __device__ __forceinline__ F2 f2_scale(F2 a, float u) {
   const float h = p + e;
   return F2{h, e - (h - p)};
 }
+// 1 / (a.hi + a.lo) in float32: the reciprocal of hi refined by one Newton
+// step against the two-float value (within an ulp of the exact reciprocal).
+// hi = 0 gives +inf, an infinite hi 0.
+__device__ __forceinline__ float f2_rcp(F2 a) {
+  const float r = 1.f / a.hi;
+  float e = fmaf(-r, a.hi, 1.f);
+  e = fmaf(-r, a.lo, e);
+  return e == e ? fmaf(r, e, r) : r;
+}
 __device__ __forceinline__ F2 f2_shfl_xor(F2 a, int m) {
   return F2{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
 }

@@ -94,8 +94,7 @@ __device__ __forceinline__ F2 f2_bcast(F2 v, int l) {
 template <typename T>
 struct FdSeq {
   int n, gb, mode, status;
-  float M, s_a;         // row n's maximum and float normaliser
-  double s;             // row n's normaliser as merged
+  float M, s_a;         // row n's maximum and normaliser (float32 of the merged two-float sum)
   int xq;               // deterministic draft: the rejected draft's token
   QLrow qlr;            // q formed from the draft's logits: row n's statistics
   uint32_t K;           // top-p alone: row n's kept set (key > K, or key == K
@@ -140,8 +139,7 @@ __device__ __forceinline__ void fd_load_state(const Params& p, int b, FdSeq<T>& 
   s.gb = seq_gamma(p, b);
   s.status = __ldcg(&sp->status);
   s.M = __ldcg(&sp->M);
-  s.s = __ldcg(&sp->s);
-  s.s_a = (float)s.s;
+  s.s_a = (float)__ldcg(&sp->s);
   s.qlr = QLrow{__ldcg(&sp->qm), __ldcg(&sp->qinv), __ldcg(&sp->qbad) != 0};
   s.K = __ldcg(&sp->tpK);
   s.idx = __ldcg(&sp->tpIdx);
@@ -223,8 +221,8 @@ __device__ __forceinline__ void fd_merge_rows(const Params& p, const float4* bas
       if (mine) {
         m[h] = Mr;
         s[h] = F2{th, tl};
-        const double sum = (double)th + (double)tl;
-        bad[h] = !(Mr > -INFINITY && Mr < INFINITY) || !(sum > 0.0 && sum < 1e300);
+        // (th, tl) is normalised: the sum is positive and finite exactly when th is
+        bad[h] = !(Mr > -INFINITY && Mr < INFINITY) || !(th > 0.f && th < INFINITY);
       }
     }
   }
@@ -258,11 +256,8 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
         bits |= SEQ_OOB;
       } else {
         float qd = g.q[h];
-        if (p.ql) {
-          const double qs = (double)qS[h].hi + (double)qS[h].lo;
-          qd = qBad[h] ? 0.f : q_weight(qd, qM[h], p.c, p.c_lo) * (float)(1.0 / qs);
-        }
-        const float ssum = (float)((double)rS[h].hi + (double)rS[h].lo);
+        if (p.ql) qd = qBad[h] ? 0.f : q_weight(qd, qM[h], p.c, p.c_lo) * f2_rcp(qS[h]);
+        const float ssum = rS[h].hi + rS[h].lo;   // the float32 rounding of the two-float sum
         const float pd = rBad[h] ? 0.f : exp2f((g.l[h] - rM[h]) * p.c) / ssum;
         if (qd > 0.f) {
           a[h] = fminf(1.f, pd / qd);
@@ -287,8 +282,7 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
   s.gb = gb;
   s.status = bits;
   s.M = Mn;
-  s.s = (double)Sh + (double)Sl;
-  s.s_a = (float)s.s;
+  s.s_a = Sh + Sl;
   s.qlr = QLrow{0.f, 0.f, true};
   s.K = 0u;
   s.idx = 0;
@@ -297,7 +291,7 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
     const float qh = __shfl_sync(0xffffffffu, hn ? qS[1].hi : qS[0].hi, ln);
     const float ql = __shfl_sync(0xffffffffu, hn ? qS[1].lo : qS[0].lo, ln);
     const int qb = __shfl_sync(0xffffffffu, hn ? qBad[1] : qBad[0], ln);
-    if (n < gb) s.qlr = QLrow{qm, (float)(1.0 / ((double)qh + (double)ql)), qb != 0};
+    if (n < gb) s.qlr = QLrow{qm, f2_rcp(F2{qh, ql}), qb != 0};
   }
   fd_bind(p, b, s);
   if (writer) {
@@ -346,8 +340,7 @@ __device__ __forceinline__ void fd_scan_tp(const Params& p, int b, bool writer, 
   s.gb = gb;
   s.status = bits;
   s.M = __ldcg(&tr[n].M);
-  s.s = (double)__ldcg(&tr[n].Wh) + (double)__ldcg(&tr[n].Wl);
-  s.s_a = (float)s.s;
+  s.s_a = __ldcg(&tr[n].Wh) + __ldcg(&tr[n].Wl);
   s.qlr = QLrow{0.f, 0.f, true};
   s.K = __ldcg(&tr[n].K);
   s.idx = __ldcg(&tr[n].idx);
@@ -615,119 +608,119 @@ __device__ __forceinline__ IT5 it5_reduce4(const IT5 slot[4]) {
   return t;
 }
 
-// Block-wide inclusive scan of two-float values in thread order (every
-// thread gets its inclusive prefix, its exclusive prefix and the total).
-__device__ __forceinline__ void fd_block_scan(F2 v, F2* wsum, F2* inc_out, F2* ex_out, F2* tot_out) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const F2 inc = warp_incl_scan_f2(v);
-  if (lane == 31) wsum[warp] = inc;
-  __syncthreads();
-  F2 off{0.f, 0.f}, tot{0.f, 0.f};
-#pragma unroll
-  for (int w = 0; w < kFdWarps; ++w) {
-    if (w < warp) off = f2_add(off, wsum[w]);
-    tot = f2_add(tot, wsum[w]);
-  }
-  F2 below = f2_shfl_up(inc, 1);
-  if (lane == 0) below = F2{0.f, 0.f};
-  *ex_out = f2_add(off, below);
-  *inc_out = f2_add(off, inc);
-  *tot_out = tot;
-  __syncthreads();   // wsum may be reused right after
-}
-
 struct FdSmem {
   float tab[128];            // exp2_f2 table
-  F2 wsum[kFdWarps];
-  int found, last, owner, lastpos;
-  F2 base, lastbase, tbase;
-  int token;
+  F2 wsum[kFdWarps];         // token phase: warp totals, then their exclusive prefixes
+  int wcand[kFdWarps];       // token phase: each warp's candidate
+  int item, use_q, resid0;   // item phase results (warp 0)
+  F2 ibase, target, ds;
   int is_last;               // this CTA completed the sequence (ticket)
 };
 
-// The inverse-CDF search of sequence s (b) by its CTA, after every warp
-// stored its items' sums: the exact normaliser s = sum S, the item masses
-// (A - (s - s') Q for a residual, S for the bonus draw or the fallback to p_n
-// when the residual has no mass), a block scan over the items (its total is
-// R, so the search agrees with it), the item holding u * R, then the token
-// among the item's 2048 (thread t the four at 4 t).  If rounding leaves no interval
-// holding the target, the last positive one is taken, at each level.
+// The inverse-CDF search of sequence s (b), by the CTA that completed it.
+//   1. Every thread: the C item sums from global memory into `stash` (the
+//      drained ring), zeroing them behind.
+//   2. Warp 0 alone: the exact normaliser s = sum S, the item masses m_k
+//      (A_k - (s - s') Q_k for a residual, clamped at 0; S_k for the bonus
+//      draw, or for the fallback to p_n when the residual has no mass), their
+//      total R, the target t = u R and the item.  Lane l holds items
+//      [l P, l P + P): its sum, one warp scan of the lane sums, then each lane
+//      walks its own items.
+//   3. Every thread: four of the item's 2048 tokens (re-read from L2), their
+//      masses, a block scan of the thread sums, and the token.
+// At both levels the pick is the last entry of positive mass whose start
+// (the sum of the masses before it) is <= t: the inverse CDF (the smallest
+// entry whose cumulative mass exceeds t), written so that it always names a
+// positive-mass entry and rounding can leave t in no gap between intervals.
+// Four block barriers in all.
 template <typename T, bool MASK>
-__device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq<T>& s, FdSmem& sm, int* resid0_out) {
+__device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq<T>& s, FdSmem& sm,
+                                             unsigned char* stash, int* resid0_out) {
   constexpr bool EXACT = sizeof(T) == 2;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G1 = p.gamma + 1, V = p.V, C = p.FC;
-  const float u = __ldg(p.uniforms + b * G1 + s.gb);
-  const float4* SA = p.fd_part + (size_t)b * C;
-  const float* QQ = p.fd_q + (size_t)b * C;
+  float4* sSA = reinterpret_cast<float4*>(stash);
+  float* sQ = reinterpret_cast<float*>(stash + (size_t)C * sizeof(float4));
+  float4* gSA = p.fd_part + (size_t)b * C;
+  float* gQ = p.fd_q + (size_t)b * C;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");   // the ring is drained (its last groups are empty)
+  for (int k = tid; k < C; k += kFdThreads) {
+    sSA[k] = __ldcg(gSA + k);
+    sQ[k] = __ldcg(gQ + k);
+    gSA[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    gQ[k] = 0.f;
+  }
   *resid0_out = 0;
+  if (tid == 0) sm.item = -1;
+  __syncthreads();
   if (s.mode == FD_SKIP) return 0;
   const bool resid = s.n < s.gb;
-  F2 sl{0.f, 0.f};
-  for (int k = tid; k < C; k += kFdThreads) {
-    const float4 v = __ldcg(SA + k);
-    sl = f2_add(sl, F2{v.x, v.y});
-  }
-  F2 inc, ex, tot;
-  fd_block_scan(sl, sm.wsum, &inc, &ex, &tot);   // its total: the exact normaliser s
-  const F2 ds = f2_add(tot, F2{-s.s_a, 0.f});     // s - s', tiny
-  bool use_q = resid;
-  auto mass = [&](int k) -> F2 {
-    const float4 v = __ldcg(SA + k);
-    if (!use_q) return F2{v.x, v.y};
-    F2 m = f2_add(F2{v.z, v.w}, f2_neg(f2_scale(ds, __ldcg(QQ + k))));
-    if (m.hi < 0.f) m = F2{0.f, 0.f};
-    return m;
-  };
-  // items k = round * 512 + tid, rounds chained by a carry; two passes: the
-  // total R, then the search (the same additions)
-  F2 R{0.f, 0.f}, target{0.f, 0.f};
-  int item = -1;
-  F2 ibase{0.f, 0.f};
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    for (int pass = 0; pass < 2; ++pass) {
-      __syncthreads();   // every thread has read the previous pass's result
-      if (tid == 0) {
-        sm.found = 0x7fffffff;
-        sm.last = -1;
+  // ---- 2. the item (warp 0)
+  if (warp == 0) {
+    const int P = (C + 31) / 32;
+    const int k0 = min(C, lane * P), k1 = min(C, k0 + P);
+    F2 sl{0.f, 0.f};
+    for (int k = k0; k < k1; ++k) sl = f2_add(sl, F2{sSA[k].x, sSA[k].y});
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sl = f2_add(sl, f2_shfl_xor(sl, o));
+    const F2 ds = f2_add(sl, F2{-s.s_a, 0.f});   // s - s', tiny
+    bool use_q = resid;
+    int resid0 = 0;
+    auto mass = [&](int k) -> F2 {
+      const float4 v = sSA[k];
+      if (!use_q) return F2{v.x, v.y};
+      F2 m = f2_add(F2{v.z, v.w}, f2_neg(f2_scale(ds, sQ[k])));
+      if (m.hi < 0.f) m = F2{0.f, 0.f};
+      return m;
+    };
+    F2 R{0.f, 0.f}, lex{0.f, 0.f};
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      F2 lt{0.f, 0.f};
+      for (int k = k0; k < k1; ++k) lt = f2_add(lt, mass(k));
+      const F2 inc = warp_incl_scan_f2(lt);
+      R = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+      lex = f2_shfl_up(inc, 1);
+      if (lane == 0) lex = F2{0.f, 0.f};
+      if (resid && use_q && !f2_pos(R)) {   // (warp-uniform) zero residual mass, only through rounding
+        resid0 = 1;
+        use_q = false;
+        continue;
       }
-      F2 carry{0.f, 0.f};
-      for (int k0 = 0; k0 < C; k0 += kFdThreads) {
-        const int k = k0 + tid;
-        const F2 m = k < C ? mass(k) : F2{0.f, 0.f};
-        fd_block_scan(m, sm.wsum, &inc, &ex, &tot);
-        ex = f2_add(carry, ex);
-        if (pass == 1 && k < C && f2_pos(m)) {
-          if (!f2_lt(target, ex) && f2_lt(target, f2_add(ex, m))) {
-            sm.found = k;   // at most one k
-            sm.base = ex;
-          }
-          atomicMax(&sm.last, k);
+      break;
+    }
+    const float u = __ldg(p.uniforms + b * G1 + s.gb);
+    const F2 t = f2_scale(R, u);
+    int best = -1;
+    F2 bstart{0.f, 0.f}, e = lex;
+    if (f2_pos(R)) {
+      for (int k = k0; k < k1; ++k) {
+        const F2 m = mass(k);
+        if (f2_pos(m) && !f2_lt(t, e)) {
+          best = k;
+          bstart = e;
         }
-        __syncthreads();
-        if (pass == 1 && k == sm.last) sm.lastbase = ex;
-        carry = f2_add(carry, tot);
-        __syncthreads();
-        if (pass == 1 && sm.found != 0x7fffffff) break;
-      }
-      if (pass == 0) {
-        R = carry;
-        target = f2_scale(R, u);
+        e = f2_add(e, m);
       }
     }
-    if (resid && use_q && !f2_pos(R)) {
-      *resid0_out = 1;   // zero residual mass (only through rounding): draw from p_n
-      use_q = false;
-      continue;
+    const int top = __reduce_max_sync(0xffffffffu, best);
+    if (best >= 0 && best == top) {   // one lane: the lanes' items are disjoint
+      sm.item = best;
+      sm.ibase = bstart;
     }
-    break;
+    if (lane == 0) {
+      sm.use_q = use_q;
+      sm.resid0 = resid0;
+      sm.target = t;
+      sm.ds = ds;
+    }
   }
-  if (!f2_pos(R)) return 0;
-  const bool take_last = sm.found == 0x7fffffff;
-  item = take_last ? sm.last : sm.found;
-  ibase = take_last ? sm.lastbase : sm.base;
-  if (item < 0) return 0;
-  // ---- the token: thread t has the TPT consecutive tokens at item * kFdTok + TPT t
+  __syncthreads();
+  const int item = sm.item;
+  if (item < 0) return 0;   // no positive mass (rounding)
+  *resid0_out = sm.resid0;
+  const bool use_q = sm.use_q != 0;
+  const F2 t = sm.target, ds = sm.ds;
+  // ---- 3. the token: thread t has the TPT consecutive tokens at item * kFdTok + TPT t
   constexpr int TPT = kFdTok / kFdThreads;
   const int mode = use_q ? s.mode : FD_NONE;
   const int v0 = item * kFdTok + TPT * tid;
@@ -749,36 +742,34 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
     }
     m = f2_add(m, tm[j]);
   }
-  fd_block_scan(m, sm.wsum, &inc, &ex, &tot);
-  ex = f2_add(ibase, ex);
-  if (tid == 0) {
-    sm.owner = 0x7fffffff;
-    sm.lastpos = -1;
+  // block exclusive scan of the thread sums: warp scans, warp 0 scans the warp totals
+  const F2 inc = warp_incl_scan_f2(m);
+  if (lane == 31) sm.wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const F2 w = warp_incl_scan_f2(lane < kFdWarps ? sm.wsum[lane] : F2{0.f, 0.f});
+    F2 wx = f2_shfl_up(w, 1);
+    if (lane == 0) wx = F2{0.f, 0.f};
+    __syncwarp();
+    if (lane < kFdWarps) sm.wsum[lane] = wx;
   }
   __syncthreads();
-  if (f2_pos(m)) {
-    if (!take_last && !f2_lt(target, ex) && f2_lt(target, f2_add(ex, m))) atomicMin(&sm.owner, tid);
-    atomicMax(&sm.lastpos, tid);
-  }
-  __syncthreads();
-  const bool tlast = sm.owner == 0x7fffffff;
-  const int owner = tlast ? sm.lastpos : sm.owner;
-  if (tid == owner) {
-    // the token within this thread's run (the same additions as its total)
-    F2 lb = ex;
-    int first = -1, lastp = -1;
+  F2 below = f2_shfl_up(inc, 1);
+  if (lane == 0) below = F2{0.f, 0.f};
+  F2 e = f2_add(f2_add(sm.ibase, sm.wsum[warp]), below);   // this thread's first token's start
+  int cand = -1;
 #pragma unroll
-    for (int j = 0; j < TPT; ++j) {
-      if (f2_pos(tm[j])) {
-        if (first < 0 && !take_last && !tlast && !f2_lt(target, lb) && f2_lt(target, f2_add(lb, tm[j]))) first = j;
-        lastp = j;
-      }
-      lb = f2_add(lb, tm[j]);
-    }
-    sm.token = v0 + (first >= 0 ? first : lastp);
+  for (int j = 0; j < TPT; ++j) {
+    if (f2_pos(tm[j]) && !f2_lt(t, e)) cand = v0 + j;
+    e = f2_add(e, tm[j]);
   }
+  cand = __reduce_max_sync(0xffffffffu, cand);
+  if (lane == 0) sm.wcand[warp] = cand;
   __syncthreads();
-  return owner >= 0 ? sm.token : 0;
+  int tok = -1;
+#pragma unroll
+  for (int w = 0; w < kFdWarps; ++w) tok = max(tok, sm.wcand[w]);
+  return tok >= 0 ? tok : 0;
 }
 
 // MASK: top-p alone (the rows' records come from topp_row_kernel).
@@ -901,13 +892,9 @@ __global__ void __launch_bounds__(kFdThreads, 1) final_draw_kernel(const Params 
     __syncthreads();
     if (sm.is_last) {
       int resid0 = 0;
-      const int token = fd_pick_block<T, MASK>(p, b, s, sm, &resid0);
-      // the output; the item sums, the row partials, the row records, the
-      // ticket and the state zeroed behind it
-      for (int k = tid; k < C; k += kFdThreads) {
-        p.fd_part[(size_t)b * C + k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.fd_q[(size_t)b * C + k] = 0.f;
-      }
+      const int token = fd_pick_block<T, MASK>(p, b, s, sm, fd_dyn, &resid0);
+      // the output; the row partials, the row records, the ticket and the
+      // state zeroed behind it (the item sums were zeroed as they were read)
       if (scan) {
         const int E = G1 * stream_np(p);
         for (int e = tid; e < E; e += kFdThreads) p.part[(size_t)b * E + e] = make_float4(0.f, 0.f, 0.f, 0.f);
