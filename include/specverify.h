@@ -120,9 +120,11 @@ size_t sv_workspace_bytes(int B, int gamma, int V, int top_k);
  *   uniforms         [B][gamma+1] float32 in [0, 1)
  *   temperature      > 0 and finite
  *   top_k            0 = off, else 1..SV_MAX_TOP_K
- *   top_p            in (0, 1]; 1 = off.  top_p < 1 with top_k = 0 is
- *                    supported only for V <= SV_MAX_TOP_K (else
- *                    SV_ERR_UNSUPPORTED).
+ *   top_p            in (0, 1]; 1 = off.  With top_k = 0 (or top_k >= V) the
+ *                    kept set of each row is found by a mass-weighted
+ *                    bisection over the logits' order-preserving keys (any
+ *                    V; ties at the crossing logit kept in index order), and
+ *                    the final draw runs under that mask.
  *   out_tokens       [B][gamma+1] int32: d_0..d_{n-1}, the drawn token, then -1
  *   out_num_accepted [B] int32: n in 0..gamma (n+1 tokens were emitted)
  *   out_accept_prob  [B][gamma] float32 a_i for every position, or NULL
@@ -307,6 +309,75 @@ const char* sv_last_kernels(void);
  * Returns SV_ERR_INVALID_ARG for n other than 0 or 3 or NULL events.
  */
 sv_status sv_set_timing_events(void* const* events, int n);
+
+/*
+ * Vocabulary-sharded verify.  When a row's logits (and q) are split by token
+ * range across processes - the layout a tensor-parallel output layer leaves -
+ * each process calls these steps on its own range [v0, v0 + V) of the Vg
+ * tokens, and the caller moves a few records between them.  The result is
+ * the one sv_verify_sample / sv_verify_greedy gives on the whole rows (same
+ * method, section 11.1.2 and listing 10-1): the softmax normaliser of every
+ * row and the inverse CDF of the final draw are sums over tokens, so every
+ * shard reduces its own range.  Supported: greedy, and sampling without
+ * truncation (q dense or NULL).  Per call, every shard in the same order:
+ *
+ *   1. sv_shard_row_stats           -> stats_local [B][gamma+1][SV_SHARD_STAT_WORDS]
+ *   2. all-gather of stats_local    -> stats_all [nshard][B][gamma+1][...],
+ *                                      shards in token order (v0 ascending)
+ *   3. sv_shard_scan                -> every output; for sampling all but
+ *                                      out_tokens[b][n] and out_status
+ *      (greedy ends here)
+ *   4. sv_shard_draw_sums           -> totals_local [B][SV_SHARD_TOTAL_WORDS]
+ *   5. all-gather of totals_local   -> totals_all [nshard][B][...]
+ *   6. sv_shard_draw_pick           -> out_tokens[b][n]: the drawn token on
+ *                                      the shard whose range holds it, -1 on
+ *                                      every other shard; out_status
+ *   7. element-wise maximum of out_tokens over the shards (all-reduce MAX).
+ *
+ * Every shard computes identical outputs in steps 3 and 6 (the merges run in
+ * shard order), so only the token of step 6 needs the reduction.  Arguments
+ * as in sv_verify_sample, with: V = this shard's token count (>= 1), v0 its
+ * first token, Vg the vocabulary (v0 + V <= Vg); logits [B][gamma+1][V] and
+ * q [B][gamma][V] are this shard's columns, contiguous; draft_tokens and
+ * uniforms hold GLOBAL token ids and are the same on every shard; nshard in
+ * 1..SV_MAX_SHARDS, rank = this shard's position in token order.  greedy != 0
+ * selects the greedy rule (temperature and q ignored).  The workspace (at
+ * least sv_shard_workspace_bytes(B, gamma, V), zero-filled before first use
+ * and left zero-filled) carries the state from step 3 to steps 4 and 6; steps
+ * 1-6 of one call must run in order on one stream.  Record buffers are
+ * device memory, 16-byte aligned.  Status bits as in sv_verify_sample; a draft
+ * id outside [0, Vg) sets SV_SEQ_DRAFT_OUT_OF_RANGE.
+ */
+#define SV_MAX_SHARDS 32
+#define SV_SHARD_STAT_WORDS 8   /* 32-bit words per row record */
+#define SV_SHARD_TOTAL_WORDS 8  /* 32-bit words per sequence total */
+size_t sv_shard_workspace_bytes(int B, int gamma, int V);
+sv_status sv_shard_row_stats(int B, int gamma, int V, int v0, int Vg,
+                             const void* logits, sv_dtype logits_dtype,
+                             const float* q, const int32_t* draft_tokens,
+                             float temperature, int greedy,
+                             void* stats_local, sv_stream_t stream);
+sv_status sv_shard_scan(int nshard, int B, int gamma, int V, int Vg,
+                        const void* stats_all, const int32_t* draft_tokens,
+                        const float* uniforms, float temperature, int greedy,
+                        int32_t* out_tokens, int32_t* out_num_accepted,
+                        float* out_accept_prob, int32_t* out_status,
+                        void* workspace, size_t workspace_bytes,
+                        sv_stream_t stream);
+sv_status sv_shard_draw_sums(int B, int gamma, int V, int v0, int Vg,
+                             const void* logits, sv_dtype logits_dtype,
+                             const float* q, const int32_t* draft_tokens,
+                             float temperature, void* totals_local,
+                             void* workspace, size_t workspace_bytes,
+                             sv_stream_t stream);
+sv_status sv_shard_draw_pick(int nshard, int rank, int B, int gamma, int V,
+                             int v0, int Vg, const void* logits,
+                             sv_dtype logits_dtype, const float* q,
+                             const int32_t* draft_tokens,
+                             const float* uniforms, float temperature,
+                             const void* totals_all, int32_t* out_tokens,
+                             int32_t* out_status, void* workspace,
+                             size_t workspace_bytes, sv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -92,6 +92,21 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                              _c_float, _c_int, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
                                              _c_ptr, _c_size, _c_ptr]
     lib.sv_verify_sample_qlogits.restype = _c_int
+    lib.sv_shard_workspace_bytes.argtypes = [_c_int, _c_int, _c_int]
+    lib.sv_shard_workspace_bytes.restype = _c_size
+    lib.sv_shard_row_stats.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr,
+                                       _c_float, _c_int, _c_ptr, _c_ptr]
+    lib.sv_shard_row_stats.restype = _c_int
+    lib.sv_shard_scan.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_float, _c_int,
+                                  _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]
+    lib.sv_shard_scan.restype = _c_int
+    lib.sv_shard_draw_sums.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr,
+                                       _c_float, _c_ptr, _c_ptr, _c_size, _c_ptr]
+    lib.sv_shard_draw_sums.restype = _c_int
+    lib.sv_shard_draw_pick.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int,
+                                       _c_ptr, _c_ptr, _c_ptr, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size,
+                                       _c_ptr]
+    lib.sv_shard_draw_pick.restype = _c_int
     _lib = lib
     return lib
 
@@ -113,6 +128,42 @@ def sv_verify_sample_qlogits(B, gamma, V, logits, logits_dtype, q_logits, q_logi
                                                         draft_tokens, uniforms, float(temperature), int(top_k),
                                                         float(top_p), out_tokens, out_num_accepted, out_accept_prob,
                                                         out_status, workspace, workspace_bytes, stream))
+
+
+SV_MAX_SHARDS = 32
+SV_SHARD_STAT_WORDS = 8
+SV_SHARD_TOTAL_WORDS = 8
+
+
+def sv_shard_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return int(load_library().sv_shard_workspace_bytes(B, gamma, V))
+
+
+def sv_shard_row_stats(B, gamma, V, v0, Vg, logits, logits_dtype, q, draft_tokens, temperature, greedy, stats_local,
+                       stream) -> int:
+    return int(load_library().sv_shard_row_stats(B, gamma, V, v0, Vg, logits, logits_dtype, q, draft_tokens,
+                                                  float(temperature), int(greedy), stats_local, stream))
+
+
+def sv_shard_scan(nshard, B, gamma, V, Vg, stats_all, draft_tokens, uniforms, temperature, greedy, out_tokens,
+                  out_num_accepted, out_accept_prob, out_status, workspace, workspace_bytes, stream) -> int:
+    return int(load_library().sv_shard_scan(nshard, B, gamma, V, Vg, stats_all, draft_tokens, uniforms,
+                                             float(temperature), int(greedy), out_tokens, out_num_accepted,
+                                             out_accept_prob, out_status, workspace, workspace_bytes, stream))
+
+
+def sv_shard_draw_sums(B, gamma, V, v0, Vg, logits, logits_dtype, q, draft_tokens, temperature, totals_local,
+                       workspace, workspace_bytes, stream) -> int:
+    return int(load_library().sv_shard_draw_sums(B, gamma, V, v0, Vg, logits, logits_dtype, q, draft_tokens,
+                                                  float(temperature), totals_local, workspace, workspace_bytes,
+                                                  stream))
+
+
+def sv_shard_draw_pick(nshard, rank, B, gamma, V, v0, Vg, logits, logits_dtype, q, draft_tokens, uniforms,
+                       temperature, totals_all, out_tokens, out_status, workspace, workspace_bytes, stream) -> int:
+    return int(load_library().sv_shard_draw_pick(nshard, rank, B, gamma, V, v0, Vg, logits, logits_dtype, q,
+                                                  draft_tokens, uniforms, float(temperature), totals_all,
+                                                  out_tokens, out_status, workspace, workspace_bytes, stream))
 
 
 def sv_status_string(status: int) -> str:

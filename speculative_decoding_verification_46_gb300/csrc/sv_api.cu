@@ -20,6 +20,7 @@
 #include "sv_stream.cuh"
 #include "sv_truncate.cuh"
 #include "sv_topk.cuh"
+#include "sv_shard.cuh"
 
 namespace {
 
@@ -747,4 +748,189 @@ extern "C" sv_status sv_set_timing_events(void* const* events, int n) {
   for (int i = 0; i < 3; ++i) g_timing[i] = reinterpret_cast<cudaEvent_t>(events[i]);
   g_timing_on = true;
   return SV_OK;
+}
+
+// ------------------------------------------------------- vocabulary shards
+// The steps of sv_shard.cuh behind the C entry points of include/specverify.h.
+namespace {
+
+bool shard_args_ok(int B, int gamma, int V, int v0, int Vg) {
+  return sizes_ok(B, gamma, Vg) && V >= 1 && v0 >= 0 && (long long)v0 + V <= Vg;
+}
+
+// Parameters of this shard's slice: the layout of a call on V tokens.
+sv_status shard_params(sv::Params& p, int B, int gamma, int V, int v0, int Vg, float temperature, void* workspace,
+                       size_t workspace_bytes) {
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.v0 = v0;
+  p.Vg = Vg;
+  p.top_p = 1.0f;
+  const double c = 1.4426950408889634 / (double)temperature;
+  p.c = (float)c;
+  p.c_lo = (float)(c - (double)p.c);
+  if (workspace) {
+    const Layout L = make_layout(B, gamma, V, 0);
+    if (workspace_bytes < L.total || !aligned16(workspace)) return SV_ERR_WORKSPACE;
+    bind_workspace(p, L, workspace);
+  }
+  return SV_OK;
+}
+
+template <typename T>
+sv_status launch_shard_stats(const sv::Params& p, bool greedy, cudaStream_t st) {
+  const unsigned grid = (unsigned)((long long)p.B * (p.gamma + 1));
+  if (greedy) sv::shard_stats_kernel<T, true><<<grid, sv::kShThreads, 0, st>>>(p);
+  else sv::shard_stats_kernel<T, false><<<grid, sv::kShThreads, 0, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+template <typename T>
+sv_status launch_shard_pick(const sv::Params& p, cudaStream_t st) {
+  auto kern = sv::shard_pick_kernel<T>;
+  const size_t smem = std::max<size_t>(16, (size_t)p.FC * 20);   // the staged item sums
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  kern<<<(unsigned)p.B, sv::kFdThreads, smem, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" size_t sv_shard_workspace_bytes(int B, int gamma, int V) {
+  if (!sizes_ok(B, gamma, V)) return 0;
+  return make_layout(B, gamma, V, 0).total;
+}
+
+extern "C" sv_status sv_shard_row_stats(int B, int gamma, int V, int v0, int Vg, const void* logits,
+                                        sv_dtype logits_dtype, const float* q, const int32_t* draft_tokens,
+                                        float temperature, int greedy, void* stats_out, sv_stream_t stream) {
+  g_last_kernels = "";
+  if (!shard_args_ok(B, gamma, V, v0, Vg)) return SV_ERR_INVALID_ARG;
+  if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
+    return SV_ERR_INVALID_ARG;
+  if (!greedy && (!(temperature > 0.0f) || !std::isfinite(temperature))) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !stats_out || (gamma > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
+  if (!aligned16(logits) || (q && !aligned16(q))) return SV_ERR_INVALID_ARG;
+  sv::Params p{};
+  shard_params(p, B, gamma, V, v0, Vg, greedy ? 1.0f : temperature, nullptr, 0);
+  p.logits = logits;
+  p.q = greedy ? nullptr : q;
+  p.draft = draft_tokens;
+  p.sh_out = stats_out;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  sv_status r = SV_ERR_INVALID_ARG;
+  switch (logits_dtype) {
+    case SV_DTYPE_F32: r = launch_shard_stats<float>(p, greedy != 0, st); break;
+    case SV_DTYPE_BF16: r = launch_shard_stats<__nv_bfloat16>(p, greedy != 0, st); break;
+    case SV_DTYPE_F16: r = launch_shard_stats<__half>(p, greedy != 0, st); break;
+  }
+  if (r == SV_OK) g_last_kernels = "shard_stats_kernel";
+  return r;
+}
+
+extern "C" sv_status sv_shard_scan(int nshard, int B, int gamma, int V, int Vg, const void* stats_all,
+                                   const int32_t* draft_tokens, const float* uniforms, float temperature, int greedy,
+                                   int32_t* out_tokens, int32_t* out_num_accepted, float* out_accept_prob,
+                                   int32_t* out_status, void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  g_last_kernels = "";
+  if (nshard < 1 || nshard > sv::kMaxShards || !shard_args_ok(B, gamma, V, 0, Vg)) return SV_ERR_INVALID_ARG;
+  if (!greedy && (!(temperature > 0.0f) || !std::isfinite(temperature))) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!stats_all || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
+  if (!greedy && !uniforms) return SV_ERR_INVALID_ARG;
+  sv::Params p{};
+  const sv_status ws = shard_params(p, B, gamma, V, 0, Vg, greedy ? 1.0f : temperature, greedy ? nullptr : workspace,
+                                    workspace_bytes);
+  if (ws != SV_OK) return ws;
+  if (!greedy && !workspace) return SV_ERR_WORKSPACE;
+  p.nshard = nshard;
+  p.sh_in = stats_all;
+  p.draft = draft_tokens;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.out_n = out_num_accepted;
+  p.out_a = greedy ? nullptr : out_accept_prob;
+  p.out_status = out_status;
+  const unsigned grid = (unsigned)((B + sv::kShWarps - 1) / sv::kShWarps);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (greedy) sv::shard_scan_kernel<true><<<grid, sv::kShThreads, 0, st>>>(p);
+  else sv::shard_scan_kernel<false><<<grid, sv::kShThreads, 0, st>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  g_last_kernels = "shard_scan_kernel";
+  return SV_OK;
+}
+
+extern "C" sv_status sv_shard_draw_sums(int B, int gamma, int V, int v0, int Vg, const void* logits,
+                                        sv_dtype logits_dtype, const float* q, const int32_t* draft_tokens,
+                                        float temperature, void* totals_out, void* workspace, size_t workspace_bytes,
+                                        sv_stream_t stream) {
+  g_last_kernels = "";
+  if (!shard_args_ok(B, gamma, V, v0, Vg)) return SV_ERR_INVALID_ARG;
+  if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
+    return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !totals_out || !workspace || (gamma > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
+  if (!aligned16(logits) || (q && !aligned16(q)) || !aligned16(totals_out)) return SV_ERR_INVALID_ARG;
+  sv::Params p{};
+  const sv_status ws = shard_params(p, B, gamma, V, v0, Vg, temperature, workspace, workspace_bytes);
+  if (ws != SV_OK) return ws;
+  p.logits = logits;
+  p.q = q;
+  p.draft = draft_tokens;
+  p.H = 0;          // the state comes from sv_shard_scan
+  p.shard = 1;      // totals, no search
+  p.sh_out = totals_out;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  sv_status r = SV_ERR_INVALID_ARG;
+  switch (logits_dtype) {
+    case SV_DTYPE_F32: r = launch_final_draw<float, false>(p, st); break;
+    case SV_DTYPE_BF16: r = launch_final_draw<__nv_bfloat16, false>(p, st); break;
+    case SV_DTYPE_F16: r = launch_final_draw<__half, false>(p, st); break;
+  }
+  if (r == SV_OK) g_last_kernels = "final_draw_kernel";
+  return r;
+}
+
+extern "C" sv_status sv_shard_draw_pick(int nshard, int rank, int B, int gamma, int V, int v0, int Vg,
+                                        const void* logits, sv_dtype logits_dtype, const float* q,
+                                        const int32_t* draft_tokens, const float* uniforms, float temperature,
+                                        const void* totals_all, int32_t* out_tokens, int32_t* out_status,
+                                        void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  g_last_kernels = "";
+  if (nshard < 1 || nshard > sv::kMaxShards || rank < 0 || rank >= nshard) return SV_ERR_INVALID_ARG;
+  if (!shard_args_ok(B, gamma, V, v0, Vg)) return SV_ERR_INVALID_ARG;
+  if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
+    return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !uniforms || !totals_all || !out_tokens || !workspace || (gamma > 0 && !draft_tokens))
+    return SV_ERR_INVALID_ARG;
+  if (!aligned16(logits) || (q && !aligned16(q)) || !aligned16(totals_all)) return SV_ERR_INVALID_ARG;
+  sv::Params p{};
+  const sv_status ws = shard_params(p, B, gamma, V, v0, Vg, temperature, workspace, workspace_bytes);
+  if (ws != SV_OK) return ws;
+  p.nshard = nshard;
+  p.rank = rank;
+  p.logits = logits;
+  p.q = q;
+  p.draft = draft_tokens;
+  p.uniforms = uniforms;
+  p.sh_in = totals_all;
+  p.out_tokens = out_tokens;
+  p.out_status = out_status;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  sv_status r = SV_ERR_INVALID_ARG;
+  switch (logits_dtype) {
+    case SV_DTYPE_F32: r = launch_shard_pick<float>(p, st); break;
+    case SV_DTYPE_BF16: r = launch_shard_pick<__nv_bfloat16>(p, st); break;
+    case SV_DTYPE_F16: r = launch_shard_pick<__half>(p, st); break;
+  }
+  if (r == SV_OK) g_last_kernels = "shard_pick_kernel";
+  return r;
 }

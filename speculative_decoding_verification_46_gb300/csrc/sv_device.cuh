@@ -98,6 +98,12 @@ struct Params {
   float4* qpart;                  // [B * gamma][H][kWarps] the draft rows' streaming partials (with ql)
   int2* qrowres;                  // [B * gamma][top_k + 1] the draft rows' kept lists (with ql and top-k / top-p)
   struct TpRow* tp;               // [B][gamma + 1] top-p alone: each row's kept set, mass and a_i
+  // vocabulary-sharded verify (this process holds tokens [v0, v0 + V) of Vg)
+  int v0, Vg;
+  int nshard, rank;               // shards and this one's index (shards in token order)
+  int shard;                      // final draw: 0 = whole row; 1 = write this shard's row-n totals, no search
+  const void* sh_in;              // all shards' records (gathered by the caller)
+  void* sh_out;                   // this shard's records
 };
 
 // ------------------------------------------------------------------ PTX helpers

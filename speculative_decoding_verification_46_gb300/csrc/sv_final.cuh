@@ -126,7 +126,7 @@ __device__ __forceinline__ void fd_bind(const Params& p, int b, FdSeq<T>& s) {
     s.qrow = p.q + ((size_t)b * G + s.n) * V;
   } else {
     s.mode = FD_DET;
-    s.xq = __ldg(p.draft + b * G + s.n);
+    s.xq = __ldg(p.draft + b * G + s.n) - p.v0;   // a token index of this row (of the shard's slice)
   }
 }
 
@@ -633,9 +633,15 @@ struct FdSmem {
 // entry whose cumulative mass exceeds t), written so that it always names a
 // positive-mass entry and rounding can leave t in no gap between intervals.
 // Four block barriers in all.
+// `given` (vocabulary shards): s - s', the kind of mass and the target are
+// fixed by all shards' totals; the search runs over this shard's items only.
+struct FdGiven {
+  int on, use_q;
+  F2 ds, t;
+};
 template <typename T, bool MASK>
 __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq<T>& s, FdSmem& sm,
-                                             unsigned char* stash, int* resid0_out) {
+                                             unsigned char* stash, int* resid0_out, FdGiven given = FdGiven{}) {
   constexpr bool EXACT = sizeof(T) == 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G1 = p.gamma + 1, V = p.V, C = p.FC;
@@ -663,8 +669,8 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
     for (int k = k0; k < k1; ++k) sl = f2_add(sl, F2{sSA[k].x, sSA[k].y});
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) sl = f2_add(sl, f2_shfl_xor(sl, o));
-    const F2 ds = f2_add(sl, F2{-s.s_a, 0.f});   // s - s', tiny
-    bool use_q = resid;
+    const F2 ds = given.on ? given.ds : f2_add(sl, F2{-s.s_a, 0.f});   // s - s', tiny
+    bool use_q = given.on ? given.use_q != 0 : resid;
     int resid0 = 0;
     auto mass = [&](int k) -> F2 {
       const float4 v = sSA[k];
@@ -681,15 +687,14 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
       R = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
       lex = f2_shfl_up(inc, 1);
       if (lane == 0) lex = F2{0.f, 0.f};
-      if (resid && use_q && !f2_pos(R)) {   // (warp-uniform) zero residual mass, only through rounding
+      if (!given.on && resid && use_q && !f2_pos(R)) {   // (warp-uniform) zero residual mass, only through rounding
         resid0 = 1;
         use_q = false;
         continue;
       }
       break;
     }
-    const float u = __ldg(p.uniforms + b * G1 + s.gb);
-    const F2 t = f2_scale(R, u);
+    const F2 t = given.on ? given.t : f2_scale(R, __ldg(p.uniforms + b * G1 + s.gb));
     int best = -1;
     F2 bstart{0.f, 0.f}, e = lex;
     if (f2_pos(R)) {
@@ -770,6 +775,50 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
 #pragma unroll
   for (int w = 0; w < kFdWarps; ++w) tok = max(tok, sm.wcand[w]);
   return tok >= 0 ? tok : 0;
+}
+
+// One vocabulary shard's totals of sequence b's row-n items: sum S and sum A
+// (two-float) and sum Q, written as 8 floats (S.hi, S.lo, A.hi, A.lo, Q, 0,
+// 0, 0) to sh_out[b].  Items in thread order, warps in order: the same
+// additions on every call.
+__device__ __forceinline__ void fd_shard_totals(const Params& p, int b, FdSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = p.FC;
+  F2 S{0.f, 0.f}, A{0.f, 0.f}, Q{0.f, 0.f};
+  for (int k = tid; k < C; k += kFdThreads) {
+    const float4 v = __ldcg(p.fd_part + (size_t)b * C + k);
+    S = f2_add(S, F2{v.x, v.y});
+    A = f2_add(A, F2{v.z, v.w});
+    Q = f2_add(Q, F2{__ldcg(p.fd_q + (size_t)b * C + k), 0.f});
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    S = f2_add(S, f2_shfl_xor(S, o));
+    A = f2_add(A, f2_shfl_xor(A, o));
+    Q = f2_add(Q, f2_shfl_xor(Q, o));
+  }
+  // three two-float totals per warp through wsum (16 entries): S, then A and Q
+  if (lane == 0) sm.wsum[warp] = S;
+  __syncthreads();
+  F2 tS{0.f, 0.f};
+  if (tid == 0)
+    for (int w = 0; w < kFdWarps; ++w) tS = f2_add(tS, sm.wsum[w]);
+  __syncthreads();
+  if (lane == 0) sm.wsum[warp] = A;
+  __syncthreads();
+  F2 tA{0.f, 0.f};
+  if (tid == 0)
+    for (int w = 0; w < kFdWarps; ++w) tA = f2_add(tA, sm.wsum[w]);
+  __syncthreads();
+  if (lane == 0) sm.wsum[warp] = Q;
+  __syncthreads();
+  if (tid == 0) {
+    F2 tQ{0.f, 0.f};
+    for (int w = 0; w < kFdWarps; ++w) tQ = f2_add(tQ, sm.wsum[w]);
+    float* o = static_cast<float*>(p.sh_out) + (size_t)b * 8;
+    *reinterpret_cast<float4*>(o) = make_float4(tS.hi, tS.lo, tA.hi, tA.lo);
+    *reinterpret_cast<float4*>(o + 4) = make_float4(tQ.hi + tQ.lo, 0.f, 0.f, 0.f);
+  }
 }
 
 // MASK: top-p alone (the rows' records come from topp_row_kernel).
@@ -890,7 +939,11 @@ __global__ void __launch_bounds__(kFdThreads, 1) final_draw_kernel(const Params 
       sm.is_last = prev == Z - 1;
     }
     __syncthreads();
-    if (sm.is_last) {
+    if (sm.is_last && p.shard == 1) {
+      // vocabulary shard: this shard's row-n totals; the items stay for the search
+      fd_shard_totals(p, b, sm);
+      if (tid == 0) p.seq_ticket2[b] = 0;
+    } else if (sm.is_last) {
       int resid0 = 0;
       const int token = fd_pick_block<T, MASK>(p, b, s, sm, fd_dyn, &resid0);
       // the output; the row partials, the row records, the ticket and the
