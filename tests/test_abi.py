@@ -35,7 +35,8 @@ def test_exports_every_declared_symbol(sv):
     assert set(names) == {"sv_workspace_bytes", "sv_verify_sample", "sv_verify_greedy", "sv_status_string",
                           "sv_set_timing_events", "sv_verify_greedy_noalloc", "sv_last_kernels",
                           "sv_verify_sample_ragged", "sv_verify_greedy_ragged", "sv_truncate_emitted",
-                          "sv_qlogits_workspace_bytes", "sv_verify_sample_qlogits"}
+                          "sv_qlogits_workspace_bytes", "sv_verify_sample_qlogits", "sv_shard_workspace_bytes",
+                          "sv_shard_row_stats", "sv_shard_scan", "sv_shard_draw_sums", "sv_shard_draw_pick"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -200,3 +201,36 @@ def test_noalloc_scratch_size_matches_header(sv):
     m = re.search(r"#define\s+SV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
     assert m, "SV_NOALLOC_SCRATCH_BYTES not found in the header"
     assert sv.SV_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_shard_entry_points_validate_before_launch(sv):
+    """Invalid shard arguments are refused on the host (no device needed):
+    shard counts and ranks, ranges outside the vocabulary, dtypes, missing
+    pointers, workspaces too small."""
+    bf = sv.SV_DTYPE_BF16
+    ok = sv.SV_ERR_INVALID_ARG
+    # row stats: v0 + V beyond Vg, negative v0, V = 0, bad dtype, bad temperature, NULL output
+    assert sv.sv_shard_row_stats(4, 4, 100, 950, 1000, A, bf, A, A, 1.0, 0, A, None) == ok
+    assert sv.sv_shard_row_stats(4, 4, 100, -1, 1000, A, bf, A, A, 1.0, 0, A, None) == ok
+    assert sv.sv_shard_row_stats(4, 4, 0, 0, 1000, A, bf, A, A, 1.0, 0, A, None) == ok
+    assert sv.sv_shard_row_stats(4, 4, 100, 0, 1000, A, 7, A, A, 1.0, 0, A, None) == ok
+    assert sv.sv_shard_row_stats(4, 4, 100, 0, 1000, A, bf, A, A, 0.0, 0, A, None) == ok
+    assert sv.sv_shard_row_stats(4, 4, 100, 0, 1000, A, bf, A, A, 1.0, 0, None, None) == ok
+    assert sv.sv_shard_row_stats(4, 4, 100, 0, 1000, A + 4, bf, A, A, 1.0, 0, A, None) == ok   # misaligned
+    assert sv.sv_shard_row_stats(0, 4, 100, 0, 1000, None, bf, None, None, 1.0, 0, None, None) == sv.SV_OK
+    # scan: shard counts
+    for S in (0, sv.SV_MAX_SHARDS + 1):
+        assert sv.sv_shard_scan(S, 4, 4, 100, 1000, A, A, A, 1.0, 0, A, A, A, A, A, 1 << 20, None) == ok
+    ws_need = sv.sv_shard_workspace_bytes(4, 4, 100)
+    assert ws_need > 0
+    assert sv.sv_shard_scan(2, 4, 4, 100, 1000, A, A, A, 1.0, 0, A, A, A, A, A, ws_need - 1, None) == \
+        sv.SV_ERR_WORKSPACE
+    assert sv.sv_shard_scan(2, 4, 4, 100, 1000, A, A, None, 1.0, 0, A, A, A, A, A, ws_need, None) == ok
+    # pick: rank outside [0, nshard)
+    for rank in (-1, 2):
+        assert sv.sv_shard_draw_pick(2, rank, 4, 4, 100, 0, 1000, A, bf, A, A, A, 1.0, A, A, A, A, ws_need,
+                                     None) == ok
+    # draw sums: NULL totals, workspace too small
+    assert sv.sv_shard_draw_sums(4, 4, 100, 0, 1000, A, bf, A, A, 1.0, None, A, ws_need, None) == ok
+    assert sv.sv_shard_draw_sums(4, 4, 100, 0, 1000, A, bf, A, A, 1.0, A, A, ws_need - 1, None) == \
+        sv.SV_ERR_WORKSPACE
