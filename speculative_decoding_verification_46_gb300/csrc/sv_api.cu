@@ -168,10 +168,8 @@ sv_status launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, const sv::Param
 template <typename T, bool MASK = false>
 sv_status launch_final_draw(const sv::Params& p, cudaStream_t stream) {
   auto kern = sv::final_draw_kernel<T, MASK>;
-  const size_t smem = sv::FdRing<T>::bytes;
-  // the search stages a sequence's item sums (float4 + float each) in the ring
-  static_assert(sv::FdRing<T>::bytes >= (size_t)((SV_MAX_VOCAB + sv::kFdTok - 1) / sv::kFdTok) * 20,
-                "ring too small for the item sums of the largest vocabulary");
+  // the ring; the search stages a sequence's item sums (float4 + float each) in it
+  const size_t smem = std::max(sv::FdRing<T>::bytes, sv::fd_stash_bytes(p.FC));
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_CUDA;
@@ -789,7 +787,7 @@ sv_status launch_shard_stats(const sv::Params& p, bool greedy, cudaStream_t st) 
 template <typename T>
 sv_status launch_shard_pick(const sv::Params& p, cudaStream_t st) {
   auto kern = sv::shard_pick_kernel<T>;
-  const size_t smem = std::max<size_t>(16, (size_t)p.FC * 20);   // the staged item sums
+  const size_t smem = sv::fd_stash_bytes(p.FC);   // the staged item sums and token masses
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_CUDA;

@@ -44,7 +44,7 @@
 
 namespace sv {
 
-constexpr int kFdThreads = 512;            // one CTA per sequence, 16 warps
+constexpr int kFdThreads = 512;            // 16 warps, one CTA per SM
 constexpr int kFdWarps = kFdThreads / 32;
 constexpr int kFdChunk = 512;              // tokens per ring stage: 4 groups x 32 lanes x 4 tokens
 constexpr int kFdChunks = 4;               // chunks per item
@@ -96,6 +96,7 @@ struct FdSeq {
   int n, gb, mode, status;
   float M, s_a;         // row n's maximum and normaliser (float32 of the merged two-float sum)
   int xq;               // deterministic draft: the rejected draft's token
+  float u;              // the final draw's uniform
   QLrow qlr;            // q formed from the draft's logits: row n's statistics
   uint32_t K;           // top-p alone: row n's kept set (key > K, or key == K
   int idx;              // and index <= idx)
@@ -143,6 +144,8 @@ __device__ __forceinline__ void fd_load_state(const Params& p, int b, FdSeq<T>& 
   s.qlr = QLrow{__ldcg(&sp->qm), __ldcg(&sp->qinv), __ldcg(&sp->qbad) != 0};
   s.K = __ldcg(&sp->tpK);
   s.idx = __ldcg(&sp->tpIdx);
+  // (the shard totals step has no uniforms: it draws nothing)
+  s.u = p.uniforms ? __ldg(p.uniforms + b * (p.gamma + 1) + s.gb) : 0.f;
   fd_bind(p, b, s);
 }
 
@@ -153,12 +156,14 @@ __device__ __forceinline__ void fd_load_state(const Params& p, int b, FdSeq<T>& 
 struct FdDrafts {
   int d[2];
   float u[2], l[2], q[2];
+  float uf;   // the final draw's uniform
 };
 template <typename T>
 __device__ __forceinline__ void fd_gather(const Params& p, int b, FdDrafts& g) {
   const int lane = threadIdx.x & 31;
   const int G = p.gamma, G1 = G + 1, V = p.V;
   const int gb = seq_gamma(p, b);
+  g.uf = __ldg(p.uniforms + b * G1 + gb);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int i = lane + 32 * h;
@@ -281,6 +286,7 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
   s.n = n;
   s.gb = gb;
   s.status = bits;
+  s.u = g.uf;
   s.M = Mn;
   s.s_a = Sh + Sl;
   s.qlr = QLrow{0.f, 0.f, true};
@@ -344,6 +350,7 @@ __device__ __forceinline__ void fd_scan_tp(const Params& p, int b, bool writer, 
   s.qlr = QLrow{0.f, 0.f, true};
   s.K = __ldcg(&tr[n].K);
   s.idx = __ldcg(&tr[n].idx);
+  s.u = __ldg(p.uniforms + b * G1 + gb);
   fd_bind(p, b, s);
   if (writer) {
 #pragma unroll
@@ -608,14 +615,63 @@ __device__ __forceinline__ IT5 it5_reduce4(const IT5 slot[4]) {
   return t;
 }
 
+// Shared memory the search stages in: C item sums (float4 + float each),
+// then the 2048 token masses of the chosen item (64-bit fixed point).
+__host__ __device__ constexpr size_t fd_stash_bytes(int C) {
+  return (((size_t)C * 20 + 15) & ~(size_t)15) + (size_t)kFdTok * sizeof(long long);
+}
+
 struct FdSmem {
   float tab[128];            // exp2_f2 table
-  F2 wsum[kFdWarps];         // token phase: warp totals, then their exclusive prefixes
+  F2 wsum[kFdWarps];         // shard totals: warp sums
+  long long wll[kFdWarps];   // token phase: warp totals, then their exclusive prefixes
   int wcand[kFdWarps];       // token phase: each warp's candidate
-  int item, use_q, resid0;   // item phase results (warp 0)
-  F2 ibase, target, ds;
+  int item, use_q, resid0, e;   // item phase results (warp 0); e: the fixed-point scale
+  long long ibase, target;   // the item's start and the target, in units of 2^-e
+  F2 ds;
   int is_last;               // this CTA completed the sequence (ticket)
 };
+
+// Fixed point for the search: a non-negative two-float v as round(v * 2^e)
+// (hi and lo rounded apart; callers keep v * 2^e below 2^62), and the scale
+// e that puts a positive float R in [2^60, 2^61).  Prefix sums of such
+// integers are exact: every start and every comparison with the target is
+// exact, whatever the order of the additions.
+// round(x 2^e) for a float x with |x 2^e| < 2^62, from its bits on the
+// integer pipes: the 24-bit significand shifted by the exponent, rounded to
+// nearest (ties away from zero) when bits fall off.
+__device__ __forceinline__ long long fx_float(float x, int e) {
+  const uint32_t u = __float_as_uint(x);
+  const int be = (int)((u >> 23) & 0xffu);
+  if (be == 0) return 0;                                   // zero (and subnormals: far below 2^-e)
+  const long long m = (long long)((u & 0x7fffffu) | 0x800000u);
+  const int sh = be - 150 + e;                             // x 2^e = m 2^sh
+  long long r;
+  if (sh >= 0) r = m << sh;
+  else if (sh > -25) r = (m + (1ll << (-sh - 1))) >> -sh;
+  else r = 0;
+  return (u >> 31) ? -r : r;
+}
+__device__ __forceinline__ long long fx_of(F2 v, int e) { return fx_float(v.hi, e) + fx_float(v.lo, e); }
+__device__ __forceinline__ int fx_scale(float R) {
+  int ex;
+  frexpf(R, &ex);   // R = f 2^ex, f in [0.5, 1)
+  return 61 - ex;
+}
+__device__ __forceinline__ long long warp_incl_scan_ll(long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const long long o = __shfl_up_sync(0xffffffffu, v, m);
+    if (lane >= m) v += o;
+  }
+  return v;
+}
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
 
 // The inverse-CDF search of sequence s (b), by the CTA that completed it.
 //   1. Every thread: the C item sums from global memory into `stash` (the
@@ -628,11 +684,12 @@ struct FdSmem {
 //      walks its own items.
 //   3. Every thread: four of the item's 2048 tokens (re-read from L2), their
 //      masses, a block scan of the thread sums, and the token.
-// At both levels the pick is the last entry of positive mass whose start
-// (the sum of the masses before it) is <= t: the inverse CDF (the smallest
-// entry whose cumulative mass exceeds t), written so that it always names a
-// positive-mass entry and rounding can leave t in no gap between intervals.
-// Four block barriers in all.
+// The sums, scans and comparisons run in 64-bit fixed point (fx_of, with
+// the scale of R: each mass rounded to 2^-61 R), so the prefixes are exact
+// and t = floor(R u) is an exact product.  At both levels the pick is the
+// last entry of positive mass whose start is <= t, which is the smallest
+// entry whose cumulative mass exceeds t (the inverse CDF); a target past the
+// item's token sum takes its last positive token.  Four block barriers.
 // `given` (vocabulary shards): s - s', the kind of mass and the target are
 // fixed by all shards' totals; the search runs over this shard's items only.
 struct FdGiven {
@@ -644,7 +701,7 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
                                              unsigned char* stash, int* resid0_out, FdGiven given = FdGiven{}) {
   constexpr bool EXACT = sizeof(T) == 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G1 = p.gamma + 1, V = p.V, C = p.FC;
+  const int V = p.V, C = p.FC;
   float4* sSA = reinterpret_cast<float4*>(stash);
   float* sQ = reinterpret_cast<float*>(stash + (size_t)C * sizeof(float4));
   float4* gSA = p.fd_part + (size_t)b * C;
@@ -665,12 +722,20 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
   if (warp == 0) {
     const int P = (C + 31) / 32;
     const int k0 = min(C, lane * P), k1 = min(C, k0 + P);
-    F2 sl{0.f, 0.f};
-    for (int k = k0; k < k1; ++k) sl = f2_add(sl, F2{sSA[k].x, sSA[k].y});
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) sl = f2_add(sl, f2_shfl_xor(sl, o));
-    const F2 ds = given.on ? given.ds : f2_add(sl, F2{-s.s_a, 0.f});   // s - s', tiny
-    bool use_q = given.on ? given.use_q != 0 : resid;
+    F2 ds;
+    bool use_q;
+    if (given.on) {
+      ds = given.ds;
+      use_q = given.use_q != 0;
+    } else {
+      // s exactly, at the scale of s' (every S_k <= s ~ s')
+      const int es = fx_scale(s.s_a > 0.f ? s.s_a : 1.f);
+      long long sl = 0;
+      for (int k = k0; k < k1; ++k) sl += fx_of(F2{sSA[k].x, sSA[k].y}, es);
+      sl = warp_sum_ll(sl);
+      ds = F2{ldexpf((float)(sl - fx_float(s.s_a, es)), -es), 0.f};   // s - s', tiny
+      use_q = resid;
+    }
     int resid0 = 0;
     auto mass = [&](int k) -> F2 {
       const float4 v = sSA[k];
@@ -679,32 +744,43 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
       if (m.hi < 0.f) m = F2{0.f, 0.f};
       return m;
     };
-    F2 R{0.f, 0.f}, lex{0.f, 0.f};
+    float Rf = 0.f;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      F2 lt{0.f, 0.f};
-      for (int k = k0; k < k1; ++k) lt = f2_add(lt, mass(k));
-      const F2 inc = warp_incl_scan_f2(lt);
-      R = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
-      lex = f2_shfl_up(inc, 1);
-      if (lane == 0) lex = F2{0.f, 0.f};
-      if (!given.on && resid && use_q && !f2_pos(R)) {   // (warp-uniform) zero residual mass, only through rounding
+      Rf = 0.f;
+      for (int k = k0; k < k1; ++k) Rf += mass(k).hi;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) Rf += __shfl_xor_sync(0xffffffffu, Rf, o);
+      if (!given.on && resid && use_q && !(Rf > 0.f)) {   // (warp-uniform) zero residual mass, only through rounding
         resid0 = 1;
         use_q = false;
         continue;
       }
       break;
     }
-    const F2 t = given.on ? given.t : f2_scale(R, __ldg(p.uniforms + b * G1 + s.gb));
     int best = -1;
-    F2 bstart{0.f, 0.f}, e = lex;
-    if (f2_pos(R)) {
+    long long bstart = 0, t = 0;
+    const int e = fx_scale(Rf > 0.f ? Rf : 1.f);
+    if (Rf > 0.f) {
+      long long lt = 0;
+      for (int k = k0; k < k1; ++k) lt += fx_of(mass(k), e);
+      const long long inc = warp_incl_scan_ll(lt);
+      const long long R = __shfl_sync(0xffffffffu, inc, 31);
+      if (given.on) {
+        t = fx_of(given.t, e);
+        if (t < 0) t = 0;
+      } else {
+        // u 2^64 (u in [0, 1); a u of 2^-40 or less rounds to a multiple of 2^-64)
+        const unsigned long long ufx = s.u > 0.f ? (unsigned long long)fx_float(s.u, 62) << 2 : 0ull;
+        t = (long long)__umul64hi((unsigned long long)R, ufx);             // floor(R u)
+      }
+      long long st = inc - lt;
       for (int k = k0; k < k1; ++k) {
-        const F2 m = mass(k);
-        if (f2_pos(m) && !f2_lt(t, e)) {
+        const long long m = fx_of(mass(k), e);
+        if (m > 0 && st <= t) {
           best = k;
-          bstart = e;
+          bstart = st;
         }
-        e = f2_add(e, m);
+        st += m;
       }
     }
     const int top = __reduce_max_sync(0xffffffffu, best);
@@ -716,6 +792,7 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
       sm.use_q = use_q;
       sm.resid0 = resid0;
       sm.target = t;
+      sm.e = e;
       sm.ds = ds;
     }
   }
@@ -724,49 +801,91 @@ __device__ __forceinline__ int fd_pick_block(const Params& p, int b, const FdSeq
   if (item < 0) return 0;   // no positive mass (rounding)
   *resid0_out = sm.resid0;
   const bool use_q = sm.use_q != 0;
-  const F2 t = sm.target, ds = sm.ds;
-  // ---- 3. the token: thread t has the TPT consecutive tokens at item * kFdTok + TPT t
+  const F2 ds = sm.ds;
+  const int e = sm.e;
+  // ---- 3. the token: thread t has the TPT consecutive tokens at item * kFdTok + TPT t.
+  // Their logits and q are loaded first (one round trip: a vector load each
+  // when the row allows), then the masses, kept in shared memory after the
+  // item sums across the scan.
   constexpr int TPT = kFdTok / kFdThreads;
+  static_assert(TPT == 4, "four tokens per thread: one 4-token group");
   const int mode = use_q ? s.mode : FD_NONE;
   const int v0 = item * kFdTok + TPT * tid;
-  F2 tm[TPT];
-  F2 m{0.f, 0.f};
+  const bool full = ((V & 3) == 0) && v0 + TPT <= V;
+  float x[TPT], qv[TPT];
+  if (full) {
+    if (sizeof(T) == 4) {
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(s.row + v0));
+      fd_unpack<T>(reinterpret_cast<const unsigned char*>(&w), x);
+    } else {
+      const uint2 w = __ldcg(reinterpret_cast<const uint2*>(s.row + v0));
+      fd_unpack<T>(reinterpret_cast<const unsigned char*>(&w), x);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < TPT; ++j)
+      x[j] = v0 + j < V ? Tr<T>::get(load_slot<T>(s.row, v0 + j, 1, false), 0) : -INFINITY;
+  }
+#pragma unroll
+  for (int j = 0; j < TPT; ++j) qv[j] = 0.f;
+  if (mode == FD_DENSE) {
+    if (full) {
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(s.qrow + v0));
+      qv[0] = w.x; qv[1] = w.y; qv[2] = w.z; qv[3] = w.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < TPT; ++j) qv[j] = v0 + j < V ? __ldcg(s.qrow + v0 + j) : 0.f;
+    }
+  } else if (mode == FD_QL) {
+    float y[TPT];
+    if (full) {
+      if (sizeof(T) == 4) {
+        const float4 w = __ldcg(reinterpret_cast<const float4*>(s.qlrow + v0));
+        fd_unpack<T>(reinterpret_cast<const unsigned char*>(&w), y);
+      } else {
+        const uint2 w = __ldcg(reinterpret_cast<const uint2*>(s.qlrow + v0));
+        fd_unpack<T>(reinterpret_cast<const unsigned char*>(&w), y);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < TPT; ++j)
+        y[j] = v0 + j < V ? Tr<T>::get(load_slot<T>(s.qlrow, v0 + j, 1, false), 0) : -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) qv[j] = s.qlr.q(y[j], p.c, p.c_lo);
+  } else if (mode == FD_DET) {
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) qv[j] = v0 + j == s.xq ? INFINITY : 0.f;
+  }
+  long long* tmS = reinterpret_cast<long long*>(stash + fd_stash_bytes(C) - (size_t)kFdTok * sizeof(long long));
+  long long m = 0;
 #pragma unroll
   for (int j = 0; j < TPT; ++j) {
     const int v = v0 + j;
-    tm[j] = F2{0.f, 0.f};
-    if (v < V) {
-      const float x = Tr<T>::get(load_slot<T>(s.row, v, 1, false), 0);
-      if (!MASK || tp_kept<T>(x, v, s.K, s.idx)) {
-        float qv = 0.f;
-        if (mode == FD_DENSE) qv = __ldcg(s.qrow + v);
-        else if (mode == FD_QL) qv = s.qlr.q(Tr<T>::get(load_slot<T>(s.qlrow, v, 1, false), 0), p.c, p.c_lo);
-        else if (mode == FD_DET) qv = v == s.xq ? INFINITY : 0.f;
-        tm[j] = token_mass<EXACT>(x, qv, use_q, s.M, p.c, p.c_lo, s.s_a, ds, sm.tab);
-      }
-    }
-    m = f2_add(m, tm[j]);
+    long long tj = 0;
+    if (v < V && (!MASK || tp_kept<T>(x[j], v, s.K, s.idx)))
+      tj = fx_of(token_mass<EXACT>(x[j], qv[j], use_q, s.M, p.c, p.c_lo, s.s_a, ds, sm.tab), e);
+    tmS[j * kFdThreads + tid] = tj;
+    m += tj;
   }
   // block exclusive scan of the thread sums: warp scans, warp 0 scans the warp totals
-  const F2 inc = warp_incl_scan_f2(m);
-  if (lane == 31) sm.wsum[warp] = inc;
+  const long long inc = warp_incl_scan_ll(m);
+  if (lane == 31) sm.wll[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    const F2 w = warp_incl_scan_f2(lane < kFdWarps ? sm.wsum[lane] : F2{0.f, 0.f});
-    F2 wx = f2_shfl_up(w, 1);
-    if (lane == 0) wx = F2{0.f, 0.f};
+    const long long w = warp_incl_scan_ll(lane < kFdWarps ? sm.wll[lane] : 0ll);
     __syncwarp();
-    if (lane < kFdWarps) sm.wsum[lane] = wx;
+    if (lane < kFdWarps) sm.wll[lane] = w - sm.wll[lane];
   }
   __syncthreads();
-  F2 below = f2_shfl_up(inc, 1);
-  if (lane == 0) below = F2{0.f, 0.f};
-  F2 e = f2_add(f2_add(sm.ibase, sm.wsum[warp]), below);   // this thread's first token's start
+  long long st = sm.ibase + sm.wll[warp] + (inc - m);   // this thread's first token's start
+  const long long t = sm.target;
   int cand = -1;
 #pragma unroll
   for (int j = 0; j < TPT; ++j) {
-    if (f2_pos(tm[j]) && !f2_lt(t, e)) cand = v0 + j;
-    e = f2_add(e, tm[j]);
+    const long long tj = tmS[j * kFdThreads + tid];
+    if (tj > 0 && st <= t) cand = v0 + j;
+    st += tj;
   }
   cand = __reduce_max_sync(0xffffffffu, cand);
   if (lane == 0) sm.wcand[warp] = cand;
