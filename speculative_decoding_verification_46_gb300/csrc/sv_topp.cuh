@@ -34,6 +34,7 @@ namespace sv {
 constexpr int kTpThreads = 512;
 constexpr int kTpBits = 4;
 constexpr int kTpBuckets = 1 << kTpBits;
+constexpr int kTpU = 8;   // vectors per thread whose loads are in flight together
 
 // Per-row result of topp_row_kernel.
 struct TpRow {
@@ -94,6 +95,24 @@ __global__ void __launch_bounds__(kTpThreads) topp_row_kernel(const Params p, Tp
     const int nv = min(VW, V - e);
     return load_slot<T>(row, e, nv, vec && nv == VW);
   };
+  // the row in batches of kTpU vectors per thread, their loads issued
+  // together (the passes re-read the row from L2; one load at a time per
+  // thread would leave them latency-bound)
+  auto sweep = [&](auto&& body) {
+    for (int j0 = tid; j0 < NVv; j0 += kTpThreads * kTpU) {
+      uint4 x[kTpU];
+#pragma unroll
+      for (int u = 0; u < kTpU; ++u) {
+        const int j = j0 + u * kTpThreads;
+        x[u] = j < NVv ? slot(j) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kTpU; ++u) {
+        const int j = j0 + u * kTpThreads;
+        if (j < NVv) body(j, x[u]);
+      }
+    }
+  };
   // the draft's inputs, before anything else (their loads overlap the passes)
   int d = -1;
   float qd = 0.f, ld = 0.f;
@@ -107,12 +126,11 @@ __global__ void __launch_bounds__(kTpThreads) topp_row_kernel(const Params p, Tp
   // ---- 1. maximum; NaN / +inf / only -inf: no distribution
   float m = -INFINITY;
   int nan = 0;
-  for (int j = tid; j < NVv; j += kTpThreads) {
-    const uint4 v = slot(j);
+  sweep([&](int j, const uint4& v) {
     const float vm = TR::template vmax<true>(v);
     nan |= (vm != vm);
     m = fmaxf(m, vm);
-  }
+  });
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -154,8 +172,7 @@ __global__ void __launch_bounds__(kTpThreads) topp_row_kernel(const Params p, Tp
     const uint64_t span = 1ull << width;
 #pragma unroll
     for (int k = 0; k < kTpBuckets; ++k) sm.hist[k][tid] = 0.f;
-    for (int j = tid; j < NVv; j += kTpThreads) {
-      const uint4 v = slot(j);
+    sweep([&](int j, const uint4& v) {
 #pragma unroll
       for (int t = 0; t < VW; ++t) {
         if (j * VW + t < V) {
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(kTpThreads) topp_row_kernel(const Params p, Tp
           }
         }
       }
-    }
+    });
     __syncthreads();
     // bucket totals: warp w sums bucket w (nw == kTpBuckets) over the columns
     {
@@ -212,18 +229,37 @@ __global__ void __launch_bounds__(kTpThreads) topp_row_kernel(const Params p, Tp
     __syncthreads();   // every thread has read tot before the next pass writes hist
   }
   const uint32_t K = lo;
-  // ---- 3. ties at K: the j-th in index order; contiguous index ranges per thread
-  const int L = (V + kTpThreads - 1) / kTpThreads;
-  const int v0 = min(tid * L, V), v1 = min(v0 + L, V);
+  // ---- 3. ties at K: the j-th in index order; contiguous ranges of whole
+  // vectors per thread (token order), loaded kTpU at a time
+  const int Lv = (NVv + kTpThreads - 1) / kTpThreads;
+  const int j0 = min(tid * Lv, NVv), j1 = min(j0 + Lv, NVv);
+  // visit(e, x) for every token e of this thread's range in order; stops when it returns true
+  auto ranged = [&](auto&& visit) {
+    for (int jb = j0; jb < j1; jb += kTpU) {
+      uint4 xv[kTpU];
+#pragma unroll
+      for (int u = 0; u < kTpU; ++u) xv[u] = jb + u < j1 ? slot(jb + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < kTpU; ++u) {
+        if (jb + u < j1) {
+#pragma unroll
+          for (int t = 0; t < VW; ++t) {
+            const int e = (jb + u) * VW + t;
+            if (e < V && visit(e, TR::get(xv[u], t))) return;
+          }
+        }
+      }
+    }
+  };
   int cnt = 0;
   float weq = 0.f;
-  for (int v = v0; v < v1; ++v) {
-    const float x = TR::get(load_slot<T>(row, v, 1, false), 0);
+  ranged([&](int e, float x) {
     if (tp_key<T>(x) == K) {
       ++cnt;
       weq = ex2_approx(fmaf(x, p.c, -Mc));
     }
-  }
+    return false;
+  });
   // exclusive prefix of the counts
   int inc = cnt;
 #pragma unroll
@@ -248,13 +284,13 @@ __global__ void __launch_bounds__(kTpThreads) topp_row_kernel(const Params p, Tp
   // the thread holding the jk-th tied token finds its index
   if (cnt > 0 && base < jk && jk <= base + cnt) {
     int seen = base;
-    for (int v = v0; v < v1; ++v) {
-      const float x = TR::get(load_slot<T>(row, v, 1, false), 0);
+    ranged([&](int e, float x) {
       if (tp_key<T>(x) == K && ++seen == jk) {
-        sm.idx = v;
-        break;
+        sm.idx = e;
+        return true;
       }
-    }
+      return false;
+    });
   }
   __syncthreads();
   if (tid == 0) {
