@@ -191,10 +191,19 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int2* o
     for (int e = tid; e < kk; e += nt) sm.w[e] = bad ? 0.f : exp2f((sm.w[e] - m0) * p.c);
     __syncthreads();
     if (warp == 0) {
-      F2 W{0.f, 0.f};
-      for (int e = lane; e < kk; e += 32) W = f2_add(W, F2{sm.w[e], 0.f});
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) W = f2_add(W, f2_shfl_xor(W, m));
+      // one inclusive two-float scan of the k weights in rank order: its last
+      // value is the total W, and the prefixes (kept in cand, free by now)
+      // give the top-p cut without a second pass of shuffles
+      F2* pre = reinterpret_cast<F2*>(sm.cand);
+      F2 carry{0.f, 0.f};
+      for (int c0 = 0; c0 < kk; c0 += 32) {
+        const int e = c0 + lane;
+        const F2 inc = f2_add(carry, warp_incl_scan_f2(F2{e < kk ? sm.w[e] : 0.f, 0.f}));
+        if (e < kk) pre[e] = inc;
+        carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+      }
+      __syncwarp();
+      const F2 W = carry;
       int J = kk;
       F2 WJ = W;
       if (bad || kk == 0) {
@@ -203,11 +212,9 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int2* o
         if (lane == 0 && J > 0) sm.w[0] = 1.f;
       } else if (p.top_p < 1.0f) {
         const F2 target = f2_scale(W, p.top_p);   // cumulative mass / W >= top_p
-        F2 carry{0.f, 0.f};
-        J = kk;
         for (int c0 = 0; c0 < kk; c0 += 32) {
           const int e = c0 + lane;
-          const F2 inc = f2_add(carry, warp_incl_scan_f2(F2{e < kk ? sm.w[e] : 0.f, 0.f}));
+          const F2 inc = e < kk ? pre[e] : W;
           const unsigned hit = __ballot_sync(0xffffffffu, e < kk && !f2_lt(inc, target));
           if (hit) {
             const int first = __ffs(hit) - 1;
@@ -215,13 +222,42 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int2* o
             WJ = F2{__shfl_sync(0xffffffffu, inc.hi, first), __shfl_sync(0xffffffffu, inc.lo, first)};
             break;
           }
-          carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+        }
+      }
+      const float wj = WJ.hi + WJ.lo;
+      // the acceptance probability of this row's draft (thread 0 holds d_row, q_row)
+      const int d = __shfl_sync(0xffffffffu, d_row, 0);
+      float pd = 0.f;
+      if (i < gb && !draft_row && !p.ql && d >= 0 && d < V) {
+        for (int c0 = 0; c0 < J; c0 += 32) {
+          const int e = c0 + lane;
+          const unsigned hit = __ballot_sync(0xffffffffu, e < J && sm.widx[e] == d);
+          if (hit) {
+            const int l = __ffs(hit) - 1;
+            pd = __shfl_sync(0xffffffffu, e < J ? sm.w[e] : 0.f, l) / wj;
+            break;
+          }
         }
       }
       if (lane == 0) {
         sm.J = J;
-        sm.WJ = WJ.hi + WJ.lo;
+        sm.WJ = wj;
         if (bad && i <= gb && !draft_row) atomicOr(&p.seq[b].status, SEQ_BADROW);
+        if (i < gb && !draft_row && !p.ql) {
+          float a = 0.f;
+          int st = 0;
+          if (d < 0 || d >= V) {
+            st |= SEQ_OOB;
+          } else if (q_row > 0.0f) {
+            a = fminf(1.f, pd / q_row);
+          } else {
+            a = pd > 0.f ? 1.f : 0.f;
+            st |= SEQ_QBAD;
+          }
+          if (st) atomicOr(&p.seq[b].status, st);
+          p.acc[b * G + i] = (double)a;
+          if (p.out_a) p.out_a[b * G + i] = a;
+        }
       }
     }
     __syncthreads();
@@ -229,38 +265,6 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int2* o
     const float WJ = sm.WJ;
     if (tid == 0) out[0] = make_int2(J, 0);
     for (int e = tid; e < J; e += nt) out[1 + e] = make_int2(sm.widx[e], __float_as_int(sm.w[e] / WJ));
-    // ---- acceptance probability of this row's draft
-    if (i < gb && !draft_row && !p.ql) {
-      if (tid == 0) {
-        sm.pd = 0.f;
-        sm.token = d_row;
-      }
-      __syncthreads();
-      const int d = sm.token;
-      if (d >= 0 && d < V)
-        for (int e = tid; e < J; e += nt)
-          if (sm.widx[e] == d) sm.pd = sm.w[e] / WJ;
-      __syncthreads();
-      if (tid == 0) {
-        float a = 0.f;
-        int st = 0;
-        if (d < 0 || d >= V) {
-          st |= SEQ_OOB;
-        } else {
-          const float pd = sm.pd;
-          const float qd = q_row;
-          if (qd > 0.0f) {
-            a = fminf(1.f, pd / qd);
-          } else {
-            a = pd > 0.f ? 1.f : 0.f;
-            st |= SEQ_QBAD;
-          }
-        }
-        if (st) atomicOr(&p.seq[b].status, st);
-        p.acc[b * G + i] = (double)a;
-        if (p.out_a) p.out_a[b * G + i] = a;
-      }
-    }
 }
 
 }  // namespace sv
