@@ -379,6 +379,43 @@ sv_status sv_shard_draw_pick(int nshard, int rank, int B, int gamma, int V,
                              int32_t* out_status, void* workspace,
                              size_t workspace_bytes, sv_stream_t stream);
 
+/*
+ * Vocabulary shards with truncation (top_k in 1..SV_MAX_TOP_K, then
+ * top_p): every token of a row's global top-k is in the top-k of the shard
+ * holding it, so the shards' candidate lists hold the whole truncated
+ * distribution and the q it needs (section 11.1.2: the transforms of p; q
+ * used as given).  Per call, every shard:
+ *
+ *   1. sv_shard_topk_candidates  -> cand_local [B][gamma+1][top_k+1] entries
+ *                                   of SV_SHARD_CAND_BYTES: the row's local
+ *                                   top-k by (logit, lowest index) with q of
+ *                                   the drafted row at each (one-hot at d_i
+ *                                   when q is NULL), after a header entry
+ *   2. all-gather of cand_local  -> cand_all [nshard][...], token order
+ *   3. sv_shard_topk_finish      -> every output (identical on every shard)
+ *
+ * Requirements: V a multiple of 8 (16-bit logits) or 4 (float32) (else
+ * SV_ERR_UNSUPPORTED); nshard * top_k <= 2048 (else SV_ERR_UNSUPPORTED).
+ * The workspace of step 1 is at least sv_workspace_bytes(B, gamma, V, top_k)
+ * (zero-filled, left zero-filled); step 3 needs none.  Top-p without top-k
+ * is not offered sharded.
+ */
+#define SV_SHARD_CAND_BYTES 16
+sv_status sv_shard_topk_candidates(int B, int gamma, int V, int v0, int Vg,
+                                   const void* logits, sv_dtype logits_dtype,
+                                   const float* q, const int32_t* draft_tokens,
+                                   float temperature, int top_k,
+                                   void* cand_local, void* workspace,
+                                   size_t workspace_bytes, sv_stream_t stream);
+sv_status sv_shard_topk_finish(int nshard, int B, int gamma, int Vg,
+                               const void* cand_all,
+                               const int32_t* draft_tokens,
+                               const float* uniforms, float temperature,
+                               int top_k, float top_p, int32_t* out_tokens,
+                               int32_t* out_num_accepted,
+                               float* out_accept_prob, int32_t* out_status,
+                               sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -107,6 +107,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                        _c_ptr, _c_ptr, _c_ptr, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size,
                                        _c_ptr]
     lib.sv_shard_draw_pick.restype = _c_int
+    lib.sv_shard_topk_candidates.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr,
+                                             _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr]
+    lib.sv_shard_topk_candidates.restype = _c_int
+    lib.sv_shard_topk_finish.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_float, _c_int,
+                                         _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr]
+    lib.sv_shard_topk_finish.restype = _c_int
     _lib = lib
     return lib
 
@@ -164,6 +170,23 @@ def sv_shard_draw_pick(nshard, rank, B, gamma, V, v0, Vg, logits, logits_dtype, 
     return int(load_library().sv_shard_draw_pick(nshard, rank, B, gamma, V, v0, Vg, logits, logits_dtype, q,
                                                   draft_tokens, uniforms, float(temperature), totals_all,
                                                   out_tokens, out_status, workspace, workspace_bytes, stream))
+
+
+SV_SHARD_CAND_BYTES = 16
+
+
+def sv_shard_topk_candidates(B, gamma, V, v0, Vg, logits, logits_dtype, q, draft_tokens, temperature, top_k,
+                             cand_local, workspace, workspace_bytes, stream) -> int:
+    return int(load_library().sv_shard_topk_candidates(B, gamma, V, v0, Vg, logits, logits_dtype, q, draft_tokens,
+                                                        float(temperature), int(top_k), cand_local, workspace,
+                                                        workspace_bytes, stream))
+
+
+def sv_shard_topk_finish(nshard, B, gamma, Vg, cand_all, draft_tokens, uniforms, temperature, top_k, top_p,
+                         out_tokens, out_num_accepted, out_accept_prob, out_status, stream) -> int:
+    return int(load_library().sv_shard_topk_finish(nshard, B, gamma, Vg, cand_all, draft_tokens, uniforms,
+                                                    float(temperature), int(top_k), float(top_p), out_tokens,
+                                                    out_num_accepted, out_accept_prob, out_status, stream))
 
 
 def sv_status_string(status: int) -> str:

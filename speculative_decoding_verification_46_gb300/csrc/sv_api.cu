@@ -932,3 +932,89 @@ extern "C" sv_status sv_shard_draw_pick(int nshard, int rank, int B, int gamma, 
   if (r == SV_OK) g_last_kernels = "shard_pick_kernel";
   return r;
 }
+
+// ------------------------------------------- vocabulary shards, truncated sampling
+extern "C" sv_status sv_shard_topk_candidates(int B, int gamma, int V, int v0, int Vg, const void* logits,
+                                              sv_dtype logits_dtype, const float* q, const int32_t* draft_tokens,
+                                              float temperature, int top_k, void* cand_local, void* workspace,
+                                              size_t workspace_bytes, sv_stream_t stream) {
+  g_last_kernels = "";
+  if (!shard_args_ok(B, gamma, V, v0, Vg)) return SV_ERR_INVALID_ARG;
+  if (logits_dtype != SV_DTYPE_F32 && logits_dtype != SV_DTYPE_BF16 && logits_dtype != SV_DTYPE_F16)
+    return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > SV_MAX_TOP_K) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !cand_local || !workspace || (gamma > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
+  if (!aligned16(logits) || (q && !aligned16(q)) || !aligned16(cand_local)) return SV_ERR_INVALID_ARG;
+  if (V % vec_width(logits_dtype) != 0) return SV_ERR_UNSUPPORTED;   // the streaming top-k kernel's rows
+  sv::Params p{};
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.v0 = v0;
+  p.Vg = Vg;
+  p.top_k = top_k;
+  p.top_p = 1.0f;
+  const double c = 1.4426950408889634 / (double)temperature;
+  p.c = (float)c;
+  p.c_lo = (float)(c - (double)p.c);
+  const Layout L = make_layout(B, gamma, V, top_k);
+  if (workspace_bytes < L.total || !aligned16(workspace)) return SV_ERR_WORKSPACE;
+  bind_workspace(p, L, workspace);
+  p.logits = logits;
+  p.q = q;
+  p.draft = draft_tokens;
+  p.shard = 2;
+  p.sh_out = cand_local;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  sv_status r = SV_ERR_INVALID_ARG;
+  switch (logits_dtype) {
+    case SV_DTYPE_F32: r = launch_stream_topk<float>(p, st); break;
+    case SV_DTYPE_BF16: r = launch_stream_topk<__nv_bfloat16>(p, st); break;
+    case SV_DTYPE_F16: r = launch_stream_topk<__half>(p, st); break;
+  }
+  if (r == SV_OK) g_last_kernels = "stream_topk_kernel";
+  return r;
+}
+
+extern "C" sv_status sv_shard_topk_finish(int nshard, int B, int gamma, int Vg, const void* cand_all,
+                                          const int32_t* draft_tokens, const float* uniforms, float temperature,
+                                          int top_k, float top_p, int32_t* out_tokens, int32_t* out_num_accepted,
+                                          float* out_accept_prob, int32_t* out_status, sv_stream_t stream) {
+  g_last_kernels = "";
+  if (nshard < 1 || nshard > sv::kMaxShards || !sizes_ok(B, gamma, Vg)) return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > SV_MAX_TOP_K || !(top_p > 0.0f && top_p <= 1.0f)) return SV_ERR_INVALID_ARG;
+  if ((long long)nshard * top_k > sv::kShCandMax) return SV_ERR_UNSUPPORTED;
+  if (B == 0) return SV_OK;
+  if (!cand_all || !uniforms || !out_tokens || !out_num_accepted || (gamma > 0 && !draft_tokens))
+    return SV_ERR_INVALID_ARG;
+  sv::Params p{};
+  p.B = B;
+  p.gamma = gamma;
+  p.Vg = Vg;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  const double c = 1.4426950408889634 / (double)temperature;
+  p.c = (float)c;
+  p.c_lo = (float)(c - (double)p.c);
+  p.nshard = nshard;
+  p.sh_in = cand_all;
+  p.draft = draft_tokens;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.out_n = out_num_accepted;
+  p.out_a = out_accept_prob;
+  p.out_status = out_status;
+  const size_t smem = sizeof(sv::ShTopkSmem);
+  if (cudaFuncSetAttribute(sv::shard_topk_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  sv::shard_topk_finish_kernel<<<(unsigned)B, sv::kShThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  g_last_kernels = "shard_topk_finish_kernel";
+  return SV_OK;
+}

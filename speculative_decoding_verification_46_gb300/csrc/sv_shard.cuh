@@ -27,6 +27,7 @@
 
 #include "sv_device.cuh"
 #include "sv_final.cuh"
+#include "sv_topk.cuh"
 
 namespace sv {
 
@@ -406,6 +407,220 @@ __global__ void __launch_bounds__(kFdThreads, 1) shard_pick_kernel(const Params 
     zs.n = 0; zs.status = 0; zs.M = 0.f; zs.qm = 0.f; zs.s = 0.0; zs.qinv = 0.f; zs.qbad = 0; zs.tpK = 0u; zs.tpIdx = 0;
     p.seq[b] = zs;
   }
+}
+
+// ---- truncated sampling over vocabulary shards (top-k, then top-p)
+//
+// Every token of a row's global top-k is in the top-k of the shard holding
+// it, so the shards' candidate lists (stream_topk_kernel in shard mode 2:
+// each list the shard's k best by (logit, lowest index), with q of the
+// drafted row at each) hold the whole truncated distribution and the q it
+// needs: one all-gather, then shard_topk_finish_kernel runs the rest of the
+// round identically on every shard.
+constexpr int kShCandMax = 2048;   // nshard * top_k entries merged per row
+
+struct ShTopkSmem {
+  unsigned long long key[kShCandMax];
+  float q[kShCandMax];
+  unsigned long long tkey[kMaxK];   // the row's top-k in rank order
+  float tq[kMaxK];
+  float w[kMaxK];                   // their weights, then the kept probabilities
+  F2 rs[kMaxK];                     // final draw: residual weights in token order
+  int sidx[kMaxK];
+  float a[kMaxG1];
+  LocateSmem loc;
+  int N, J, nan, bad, hasd, n, status, token;
+  float qd, WJ;
+};
+
+// Row i of sequence b: merge the shards' lists into the top-k (exact ranks
+// over the union), softmax over them, the top-p cut; leaves the kept
+// probabilities in w[0..J) (rank order) with tkey / tq, J, and the row's NaN
+// flag and the draft's q (from the shard holding it) in sm.  Returns J.
+__device__ int sh_topk_row(const Params& p, int b, int i, ShTopkSmem& sm) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int S = p.nshard, k = p.top_k, G1 = p.gamma + 1;
+  const ShardCand* all = static_cast<const ShardCand*>(p.sh_in);
+  const size_t rowrec = (size_t)(k + 1), shardrec = (size_t)p.B * G1 * rowrec;
+  if (tid == 0) {
+    sm.nan = 0;
+    sm.hasd = 0;
+    sm.qd = 0.f;
+    sm.N = 0;
+  }
+  __syncthreads();
+  for (int e = tid; e < S * k; e += nt) {
+    const int r = e / k, j = e - r * k;
+    const ShardCand c = all[r * shardrec + ((size_t)b * G1 + i) * rowrec + 1 + j];
+    sm.key[e] = c.key;
+    sm.q[e] = c.q;
+  }
+  if (tid < S) {
+    const ShardCand h = all[tid * shardrec + ((size_t)b * G1 + i) * rowrec];
+    if (h.aux & 2) atomicOr(&sm.nan, 1);
+    if (h.aux & 1) {   // at most one shard holds the draft token
+      sm.hasd = 1;
+      sm.qd = h.q;
+    }
+  }
+  __syncthreads();
+  // exact ranks among the union (keys are distinct: the index is in them)
+  int cnt = 0;
+  for (int e = tid; e < S * k; e += nt) {
+    const unsigned long long me = sm.key[e];
+    if (me == 0ull) continue;
+    ++cnt;
+    int rank = 0;
+    for (int j = 0; j < S * k; ++j) rank += sm.key[j] > me;
+    if (rank < k) {
+      sm.tkey[rank] = me;
+      sm.tq[rank] = sm.q[e];
+    }
+  }
+  if (cnt) atomicAdd(&sm.N, cnt);
+  __syncthreads();
+  const int kk = min(k, sm.N);
+  // softmax(./T) over the top-k, then the top-p cut (the unsharded epilogue's rule)
+  const float m0 = kk > 0 ? comp_val(sm.tkey[0]) : -INFINITY;
+  const bool bad = sm.nan || !(m0 > -INFINITY && m0 < INFINITY);
+  for (int e = tid; e < kk; e += nt) sm.w[e] = bad ? 0.f : exp2f((comp_val(sm.tkey[e]) - m0) * p.c);
+  if (tid == 0) sm.bad = bad;
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    F2* pre = sm.rs;   // scratch for the prefixes
+    F2 carry{0.f, 0.f};
+    for (int c0 = 0; c0 < kk; c0 += 32) {
+      const int e = c0 + lane;
+      const F2 inc = f2_add(carry, warp_incl_scan_f2(F2{e < kk ? sm.w[e] : 0.f, 0.f}));
+      if (e < kk) pre[e] = inc;
+      carry = F2{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
+    }
+    __syncwarp();
+    const F2 W = carry;
+    int J = kk;
+    F2 WJ = W;
+    if (bad || kk == 0) {
+      J = kk > 0 ? 1 : 0;
+      WJ = F2{1.f, 0.f};
+      if (lane == 0 && J > 0) sm.w[0] = 1.f;
+    } else if (p.top_p < 1.0f) {
+      const F2 target = f2_scale(W, p.top_p);
+      for (int c0 = 0; c0 < kk; c0 += 32) {
+        const int e = c0 + lane;
+        const F2 inc = e < kk ? pre[e] : W;
+        const unsigned hit = __ballot_sync(0xffffffffu, e < kk && !f2_lt(inc, target));
+        if (hit) {
+          const int first = __ffs(hit) - 1;
+          J = c0 + first + 1;
+          WJ = F2{__shfl_sync(0xffffffffu, inc.hi, first), __shfl_sync(0xffffffffu, inc.lo, first)};
+          break;
+        }
+      }
+    }
+    if (lane == 0) {
+      sm.J = J;
+      sm.WJ = WJ.hi + WJ.lo;
+    }
+  }
+  __syncthreads();
+  const int J = sm.J;
+  const float WJ = sm.WJ;
+  for (int e = tid; e < J; e += nt) sm.w[e] = sm.w[e] / WJ;
+  __syncthreads();
+  return J;
+}
+
+// One CTA per sequence: rows 0..gamma through sh_topk_row, a_i, n, then the
+// final draw over row n's kept list in token order (residual max(p - q, 0)
+// with q from the candidate entries, or p_gamma); every output.
+__global__ void __launch_bounds__(kShThreads) shard_topk_finish_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char shk_dyn[];
+  ShTopkSmem& sm = *reinterpret_cast<ShTopkSmem*>(shk_dyn);
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int b = blockIdx.x;
+  const int G = p.gamma, G1 = G + 1, Vg = p.Vg;
+  const int gb = G;
+  if (tid == 0) sm.status = 0;
+  for (int i = 0; i < gb; ++i) {
+    const int J = sh_topk_row(p, b, i, sm);
+    if (tid == 0) {
+      int st = sm.bad ? SEQ_BADROW : 0;
+      const int d = __ldg(p.draft + b * G + i);
+      float a = 0.f;
+      if (d < 0 || d >= Vg || !sm.hasd) {
+        st |= SEQ_OOB;
+      } else {
+        float pd = 0.f;
+        for (int e = 0; e < J; ++e)
+          if (comp_idx(sm.tkey[e]) == d) pd = sm.w[e];
+        if (sm.qd > 0.f) {
+          a = fminf(1.f, pd / sm.qd);
+        } else {
+          a = pd > 0.f ? 1.f : 0.f;
+          st |= SEQ_QBAD;
+        }
+      }
+      sm.a[i] = a;
+      sm.status |= st;
+      if (p.out_a) p.out_a[b * G + i] = a;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    int n = gb;
+    for (int i = 0; i < gb; ++i)
+      if (!(__ldg(p.uniforms + b * G1 + i) < sm.a[i])) { n = i; break; }
+    sm.n = n;
+  }
+  __syncthreads();
+  const int n = sm.n;
+  // the bonus row defines no distribution: the round is flagged as the
+  // unsharded path flags it (every row 0..gamma counts)
+  if (n < gb) {
+    sh_topk_row(p, b, gb, sm);
+    if (tid == 0 && sm.bad) sm.status |= SEQ_BADROW;
+    __syncthreads();
+  }
+  const int J = sh_topk_row(p, b, n, sm);
+  if (tid == 0 && sm.bad) sm.status |= SEQ_BADROW;
+  const bool resid = n < gb;
+  // kept entries in token order: r = max(p - q, 0) after a rejection, else p
+  for (int e = tid; e < J; e += nt) {
+    const int me = comp_idx(sm.tkey[e]);
+    int rank = 0;
+    for (int j = 0; j < J; ++j) rank += comp_idx(sm.tkey[j]) < me;
+    const float pe = sm.w[e];
+    const float qm = sm.tq[e];   // q_n at the token (one-hot at d_n for NULL q: set by the candidates step)
+    sm.sidx[rank] = me;
+    sm.rs[rank] = F2{resid ? fmaxf(__fsub_rn(pe, qm), 0.f) : pe, 0.f};
+  }
+  __syncthreads();
+  const float u = __ldg(p.uniforms + b * G1 + gb);
+  F2 R{0.f, 0.f}, base{0.f, 0.f}, tgt{0.f, 0.f};
+  int pos = locate(sm.rs, J, u, &R, &base, &tgt, sm.loc, false);
+  int status = sm.status;
+  if (resid && !f2_pos(R)) {
+    status |= SEQ_RESID0;   // zero residual mass (rounding only): draw from p_n
+    for (int e = tid; e < J; e += nt) {
+      const int me = comp_idx(sm.tkey[e]);
+      int rank = 0;
+      for (int j = 0; j < J; ++j) rank += comp_idx(sm.tkey[j]) < me;
+      sm.rs[rank] = F2{sm.w[e], 0.f};
+    }
+    __syncthreads();
+    pos = locate(sm.rs, J, u, &R, &base, &tgt, sm.loc, false);
+  }
+  if (tid == 0) {
+    int tok = pos >= 0 ? sm.sidx[pos] : (J > 0 ? sm.sidx[0] : 0);
+    if (tok < 0 || tok >= Vg) tok = 0;
+    sm.token = tok;
+    p.out_n[b] = n;
+    if (p.out_status) p.out_status[b] = status;
+  }
+  __syncthreads();
+  for (int j = tid; j < G1; j += nt)
+    p.out_tokens[b * G1 + j] = j < n ? __ldg(p.draft + b * G + j) : (j == n ? sm.token : -1);
 }
 
 }  // namespace sv

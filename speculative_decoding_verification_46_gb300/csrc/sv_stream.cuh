@@ -619,7 +619,8 @@ stream_topk_kernel(const Params p) {
     // loading both here would hold warp 0 for two round trips)
     int d_row = -1;
     float q_row = 0.f;
-    if (tid == 0 && i < gb && !p.ql) d_row = __ldg(p.draft + b * G + i);   // with ql: a_i in the finisher
+    // (a vocabulary shard holds tokens from p.v0 on: the draft's index in its range)
+    if (tid == 0 && i < gb && !p.ql) d_row = __ldg(p.draft + b * G + i) - p.v0;   // with ql: a_i in the finisher
     // ---- pass 1 through the ring: per thread its two best 16-byte vectors
     // (by maximum; the first such vector on ties) kept in registers with
     // their maxima m1 >= m2, and m3 = the largest maximum of its other vectors
@@ -781,6 +782,11 @@ stream_topk_kernel(const Params p) {
       }
     }
     __syncthreads();
+    if (p.shard == 2) {
+      // vocabulary shard: the row's local top-k and q there, merged across shards later
+      topk_shard_candidates(p, r, b, i, min(k, N), bad_nan != 0, d_row, q_row, sm);
+      continue;
+    }
     topk_row_epilogue(p, b, i, gb,
                       draft_row ? p.qrowres + (size_t)rd * (k + 1) : p.rowres + (size_t)r * (k + 1),
                       min(k, N), bad_nan != 0, d_row, q_row, sm, draft_row);

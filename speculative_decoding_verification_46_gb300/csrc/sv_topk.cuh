@@ -267,4 +267,49 @@ __device__ void topk_row_epilogue(const Params& p, int b, int i, int gb, int2* o
     for (int e = tid; e < J; e += nt) out[1 + e] = make_int2(sm.widx[e], __float_as_int(sm.w[e] / WJ));
 }
 
+// One entry of a vocabulary shard's candidate list (16 bytes): the
+// comparison key of (logit, global index) (comp_key; 0 = empty) and, for a
+// drafted row, q at that token.  Entry 0 of a row's record is its header:
+// key = number of entries, q = q at the row's draft token (when the shard
+// holds it), aux = SH_HAS_D | SH_NAN.
+struct ShardCand {
+  unsigned long long key;
+  float q;
+  int aux;
+};
+
+// Record of row r for the shard steps: the row's top min(k, N) in rank
+// order (sm.w logits, sm.widx local indices) with q of draft row i at each
+// (one-hot at d_i when q is NULL), then empty entries up to k.
+__device__ void topk_shard_candidates(const Params& p, int r, int b, int i, int kk, bool bad_nan, int d_row,
+                                      float q_row, TopkSmem& sm) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int k = p.top_k, G = p.gamma, V = p.V;
+  ShardCand* rec = static_cast<ShardCand*>(p.sh_out) + (size_t)r * (k + 1);
+  if (tid == 0) {
+    const bool has = i < G && d_row >= 0 && d_row < V;
+    ShardCand h;
+    h.key = (unsigned long long)kk;
+    h.q = has ? q_row : 0.f;
+    h.aux = (has ? 1 : 0) | (bad_nan ? 2 : 0);   // SH_HAS_D, SH_NAN
+    rec[0] = h;
+    sm.token = d_row;
+  }
+  __syncthreads();
+  const int dl = sm.token;
+  const float* qrow = (i < G && p.q) ? p.q + ((size_t)b * G + i) * V : nullptr;
+  for (int e = tid; e < k; e += nt) {
+    ShardCand c;
+    c.key = 0ull;
+    c.q = 0.f;
+    c.aux = 0;
+    if (e < kk) {
+      const int idx = sm.widx[e];
+      c.key = comp_key(sm.w[e], p.v0 + idx);
+      if (i < G) c.q = qrow ? __ldg(qrow + idx) : (idx == dl ? 1.f : 0.f);
+    }
+    rec[1 + e] = c;
+  }
+}
+
 }  // namespace sv

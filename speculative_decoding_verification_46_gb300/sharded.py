@@ -12,6 +12,10 @@ the shards exchange a few records per row:
   3. row-n sums of the local range             -> all-gather
   4. the shard holding the draw picks its token -> all-reduce MAX of the tokens
 
+With top-k (then top-p) the rows' candidate lists replace all of this: each
+shard's top-k per row with q there -> all-gather -> every shard finishes the
+round on the merged lists (one exchange).
+
 The driver below runs these steps for a list of shards held by this process:
 one shard per process with ``TorchDistributedExchange`` (NCCL or gloo), or
 all shards of a problem in one process with ``LocalExchange`` (their records
@@ -138,6 +142,38 @@ class CudaSteps:
                "sv_shard_draw_sums")
         return tot
 
+    def topk_candidates(self, sh: Shard, temperature: float, top_k: int) -> torch.Tensor:
+        B, G1, V = sh.logits.shape
+        G = G1 - 1
+        dev = sh.logits.device
+        cand = torch.empty(B, G1, top_k + 1, sv.SV_SHARD_CAND_BYTES // 4, dtype=torch.int32, device=dev)
+        if sh.workspace is None:
+            sh.workspace = sv.alloc_workspace(B, G, V, top_k, dev)
+        ws = sh.workspace
+        _check(sv.sv_shard_topk_candidates(B, G, V, sh.v0, sh.Vg, sh.logits.data_ptr(),
+                                           sv._TORCH_DTYPE[sh.logits.dtype],
+                                           None if (sh.q is None or G == 0) else sh.q.data_ptr(),
+                                           sh.draft.data_ptr() if G > 0 else None, temperature, top_k,
+                                           cand.data_ptr(), ws.data_ptr(), ws.numel(), sv._stream_handle(dev, None)),
+               "sv_shard_topk_candidates")
+        return cand
+
+    def topk_finish(self, sh: Shard, cand_all: torch.Tensor, temperature: float, top_k: int, top_p: float,
+                    nshard: int) -> None:
+        B, G1, V = sh.logits.shape
+        G = G1 - 1
+        dev = sh.logits.device
+        o = sh.out
+        o["tokens"] = torch.empty(B, G1, dtype=torch.int32, device=dev)
+        o["n"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["a"] = None if G == 0 else torch.empty(B, G, dtype=torch.float32, device=dev)
+        o["status"] = torch.empty(B, dtype=torch.int32, device=dev)
+        _check(sv.sv_shard_topk_finish(nshard, B, G, sh.Vg, cand_all.data_ptr(),
+                                       sh.draft.data_ptr() if G > 0 else None, sh.uniforms.data_ptr(), temperature,
+                                       top_k, top_p, o["tokens"].data_ptr(), o["n"].data_ptr(), sv._addr(o["a"]),
+                                       o["status"].data_ptr(), sv._stream_handle(dev, None)),
+               "sv_shard_topk_finish")
+
     def draw_pick(self, sh: Shard, totals_all: torch.Tensor, temperature: float, nshard: int) -> None:
         B, G1, V = sh.logits.shape
         G = G1 - 1
@@ -162,12 +198,24 @@ def alloc_shard_workspace(B: int, gamma: int, V: int, device=None) -> torch.Tens
 
 
 def run_shards(shards: Sequence[Shard], exchange, nshard: int, *, greedy: bool, temperature: float = 1.0,
-               steps=None):
+               top_k: int = 0, top_p: float = 1.0, steps=None):
     """The sharded verify of one call for the shards this process holds.
 
-    Returns, per shard, (out_tokens [B, gamma+1], n [B], accept_prob [B, gamma]
-    or None, status [B]); every shard's result is the whole problem's."""
+    top_k (1..1024, then top_p) truncates p as the unsharded path does; top-p
+    without top-k is not offered sharded.  Returns, per shard, (out_tokens
+    [B, gamma+1], n [B], accept_prob [B, gamma] or None, status [B]); every
+    shard's result is the whole problem's."""
     steps = CudaSteps() if steps is None else steps
+    Vg = shards[0].Vg if shards else 0
+    truncate = not greedy and ((0 < top_k < Vg) or top_p < 1.0)
+    if truncate:
+        if not 0 < top_k < Vg:
+            raise sv.SvError(sv.SV_ERR_UNSUPPORTED, "sharded verify: top-p without top-k")
+        cands = [steps.topk_candidates(sh, temperature, top_k) for sh in shards]
+        cands_all = exchange.all_gather(cands)
+        for sh, ca in zip(shards, cands_all):
+            steps.topk_finish(sh, ca, temperature, top_k, top_p, nshard)
+        return [(sh.out["tokens"], sh.out["n"], sh.out["a"], sh.out["status"]) for sh in shards]
     stats = [steps.row_stats(sh, greedy, temperature) for sh in shards]
     stats_all = exchange.all_gather(stats)
     for sh, st in zip(shards, stats_all):
@@ -181,21 +229,25 @@ def run_shards(shards: Sequence[Shard], exchange, nshard: int, *, greedy: bool, 
     return [(sh.out["tokens"], sh.out["n"], sh.out["a"], sh.out["status"]) for sh in shards]
 
 
-def split_vocab(V: int, nshard: int) -> List[tuple]:
-    """Contiguous token ranges [(v0, V_r)] of a vocabulary split nshard ways."""
-    bounds = [V * r // nshard for r in range(nshard + 1)]
+def split_vocab(V: int, nshard: int, align: int = 1) -> List[tuple]:
+    """Contiguous token ranges [(v0, V_r)] of a vocabulary split nshard ways,
+    every boundary a multiple of `align` (the truncated path wants ranges of
+    whole 16-byte vectors: 8 for 16-bit logits, 4 for float32)."""
+    bounds = [min(V, (V * r // nshard) // align * align) for r in range(nshard)] + [V]
     return [(bounds[r], bounds[r + 1] - bounds[r]) for r in range(nshard)]
 
 
-def simulate(logits, q, draft, uniforms, nshard: int, *, greedy: bool, temperature: float = 1.0, steps=None):
+def simulate(logits, q, draft, uniforms, nshard: int, *, greedy: bool, temperature: float = 1.0, top_k: int = 0,
+             top_p: float = 1.0, align: int = 1, steps=None):
     """All nshard shards of one problem in this process (whole-row tensors in,
     the shards' column slices copied out): the sharded path's result, which
     equals verify_sample / verify_greedy on the whole rows."""
     B, G1, Vg = logits.shape
     shards = []
-    for r, (v0, Vr) in enumerate(split_vocab(Vg, nshard)):
+    for r, (v0, Vr) in enumerate(split_vocab(Vg, nshard, align)):
         shards.append(Shard(logits=logits[:, :, v0:v0 + Vr].contiguous(),
                             q=None if (q is None or greedy) else q[:, :, v0:v0 + Vr].contiguous(),
                             draft=draft, uniforms=uniforms, v0=v0, Vg=Vg, rank=r))
-    res = run_shards(shards, LocalExchange(), nshard, greedy=greedy, temperature=temperature, steps=steps)
+    res = run_shards(shards, LocalExchange(), nshard, greedy=greedy, temperature=temperature, top_k=top_k,
+                     top_p=top_p, steps=steps)
     return res[0]

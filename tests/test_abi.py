@@ -36,7 +36,8 @@ def test_exports_every_declared_symbol(sv):
                           "sv_set_timing_events", "sv_verify_greedy_noalloc", "sv_last_kernels",
                           "sv_verify_sample_ragged", "sv_verify_greedy_ragged", "sv_truncate_emitted",
                           "sv_qlogits_workspace_bytes", "sv_verify_sample_qlogits", "sv_shard_workspace_bytes",
-                          "sv_shard_row_stats", "sv_shard_scan", "sv_shard_draw_sums", "sv_shard_draw_pick"}
+                          "sv_shard_row_stats", "sv_shard_scan", "sv_shard_draw_sums", "sv_shard_draw_pick",
+                          "sv_shard_topk_candidates", "sv_shard_topk_finish"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -234,3 +235,20 @@ def test_shard_entry_points_validate_before_launch(sv):
     assert sv.sv_shard_draw_sums(4, 4, 100, 0, 1000, A, bf, A, A, 1.0, None, A, ws_need, None) == ok
     assert sv.sv_shard_draw_sums(4, 4, 100, 0, 1000, A, bf, A, A, 1.0, A, A, ws_need - 1, None) == \
         sv.SV_ERR_WORKSPACE
+
+
+def test_shard_topk_entry_points_validate_before_launch(sv):
+    bf = sv.SV_DTYPE_BF16
+    ws = sv.sv_workspace_bytes(4, 4, 1024, 50)
+    # top_k outside 1..1024, a range not of whole 16-byte vectors, too many candidates to merge
+    assert sv.sv_shard_topk_candidates(4, 4, 1024, 0, 4096, A, bf, A, A, 1.0, 0, A, A, ws, None) == \
+        sv.SV_ERR_INVALID_ARG
+    assert sv.sv_shard_topk_candidates(4, 4, 1020, 0, 4096, A, bf, A, A, 1.0, 50, A, A, ws, None) == \
+        sv.SV_ERR_UNSUPPORTED
+    assert sv.sv_shard_topk_candidates(4, 4, 1024, 0, 4096, A, bf, A, A, 1.0, 50, A, A, ws - 1, None) == \
+        sv.SV_ERR_WORKSPACE
+    assert sv.sv_shard_topk_finish(4, 4, 4, 4096, A, A, A, 1.0, 1024, 0.9, A, A, A, A, None) == \
+        sv.SV_ERR_UNSUPPORTED
+    assert sv.sv_shard_topk_finish(2, 4, 4, 4096, A, A, A, 1.0, 50, 0.0, A, A, A, A, None) == sv.SV_ERR_INVALID_ARG
+    assert sv.sv_shard_topk_finish(2, 4, 4, 4096, A, A, None, 1.0, 50, 0.9, A, A, A, A, None) == \
+        sv.SV_ERR_INVALID_ARG

@@ -176,3 +176,86 @@ def test_sharded_steps_launch_the_library_kernels(sv, sharded):
     assert ["final_draw_kernel"] in seen and ["shard_pick_kernel"] in seen
     for ws in (sh.workspace for sh in shards):
         assert int(ws.count_nonzero()) == 0
+
+
+# ------------------------------------------------------------ truncation (top-k, then top-p)
+
+def _case_trunc(seed, B, G, V, dtype, T, top_k, top_p, one_hot=False):
+    g = torch.Generator().manual_seed(seed)
+    L = (torch.randn(B, G + 1, V, generator=g) * 2.0).to(dtype)
+    w = workloads.Workload("case", B, G, V, "f32", "sample", T, top_k=top_k, top_p=top_p, draft_sigma=1.0)
+    q = workloads._draft_proposal(w, L[:, :G].float(), g)
+    draft = torch.multinomial(q.view(B * G, V), 1, generator=g).view(B, G).to(torch.int32)
+    u = torch.rand(B, G + 1, generator=g)
+    return dict(logits=L.contiguous(), q=None if one_hot else q.contiguous(), draft=draft, uniforms=u)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("dt", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("V,G,B,k,p", [(1000, 4, 9, 50, 0.9), (40000, 4, 5, 50, 1.0), (152064, 8, 3, 50, 0.9),
+                                       (4096, 3, 6, 200, 0.8), (20000, 2, 4, 1, 1.0)])
+def test_sharded_topk_topp_matches_oracle(sharded, S, dt, V, G, B, k, p):
+    align = 4 if dt == "f32" else 8
+    if S * k > 2048:
+        pytest.skip("more candidates than one merge holds")
+    inp = _case_trunc(3000 + S + V + k, B, G, V, DTYPES[dt], 0.8, k, p)
+    d = _dev(inp)
+    got = sharded.simulate(d["logits"], d["q"], d["draft"], d["uniforms"], S, greedy=False, temperature=0.8,
+                           top_k=k, top_p=p, align=align)
+    torch.cuda.synchronize()
+    P.compare_sample(got, P.oracle_sample(inp, 0.8, k, p), V)
+
+
+@pytest.mark.parametrize("S", [2, 4])
+def test_sharded_topk_one_hot_drafts(sharded, S):
+    inp = _case_trunc(91 + S, 8, 4, 32000, torch.bfloat16, 1.0, 50, 0.9, one_hot=True)
+    d = _dev(inp)
+    got = sharded.simulate(d["logits"], None, d["draft"], d["uniforms"], S, greedy=False, temperature=1.0,
+                           top_k=50, top_p=0.9, align=8)
+    torch.cuda.synchronize()
+    P.compare_sample(got, P.oracle_sample(inp, 1.0, 50, 0.9), 32000)
+
+
+@pytest.mark.parametrize("S", [2, 4])
+def test_sharded_topk_full_size_b256(sharded, S):
+    """The top-k 50 then top-p 0.9 workload (B=256, gamma=8, V=152064): every
+    sequence against the oracle (process pool)."""
+    w = workloads.WORKLOADS["topk50_topp0.9_b256_g8_v152064_bf16"]
+    inp = workloads.make_inputs(w, device=DEV)
+    got = sharded.simulate(inp["logits"], inp["q"], inp["draft"], inp["uniforms"], S, greedy=False,
+                           temperature=w.temperature, top_k=w.top_k, top_p=w.top_p, align=8)
+    torch.cuda.synchronize()
+    stats = P.compare_sample(got, P.oracle_sample_pool(inp, w.temperature, w.top_k, w.top_p), w.V)
+    assert stats["sequences"] == w.B
+
+
+def test_sharded_topk_launches_and_leaves_workspace_zeroed(sv, sharded):
+    inp = _dev(_case_trunc(5, 4, 4, 8192, torch.bfloat16, 1.0, 50, 0.9))
+    shards = []
+    for r, (v0, Vr) in enumerate(sharded.split_vocab(8192, 2, 8)):
+        shards.append(sharded.Shard(logits=inp["logits"][:, :, v0:v0 + Vr].contiguous(),
+                                    q=inp["q"][:, :, v0:v0 + Vr].contiguous(), draft=inp["draft"],
+                                    uniforms=inp["uniforms"], v0=v0, Vg=8192, rank=r))
+    steps = sharded.CudaSteps()
+    seen = []
+
+    class Spy:
+        def __getattr__(self, name):
+            fn = getattr(steps, name)
+
+            def call(*a, **k):
+                out = fn(*a, **k)
+                seen.append(sv.sv_last_kernels())
+                return out
+            return call
+
+    r1 = sharded.run_shards(shards, sharded.LocalExchange(), 2, greedy=False, temperature=1.0, top_k=50, top_p=0.9,
+                            steps=Spy())
+    first = [t.clone() for t in r1[0] if t is not None]
+    r2 = sharded.run_shards(shards, sharded.LocalExchange(), 2, greedy=False, temperature=1.0, top_k=50, top_p=0.9)
+    torch.cuda.synchronize()
+    for a, b in zip(first, [t for t in r2[0] if t is not None]):
+        assert torch.equal(a, b)
+    assert ["stream_topk_kernel"] in seen and ["shard_topk_finish_kernel"] in seen
+    for sh in shards:
+        assert int(sh.workspace.count_nonzero()) == 0
