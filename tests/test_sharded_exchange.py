@@ -147,6 +147,101 @@ class CpuSteps:
             tot[b, :3] = (w.sum(), A, Q)
         return torch.from_numpy(tot)
 
+    # ---- truncated protocol: candidate lists (value, global index, q, valid)
+    def topk_candidates(self, sh, T, k):
+        L = sh.logits.double().numpy()
+        B, G1, V = L.shape
+        G = G1 - 1
+        d = sh.draft.numpy()
+        q = None if sh.q is None else sh.q.double().numpy()
+        rec = np.zeros((B, G1, k + 1, 4))
+        for b in range(B):
+            for i in range(G1):
+                x = L[b, i]
+                nan = bool(np.isnan(x).any())
+                ok = np.nonzero(~np.isnan(x) & (x > -np.inf))[0]
+                order = ok[np.lexsort((ok, -x[ok]))][:k]       # value descending, index ascending
+                has, qd = 0, 0.0
+                if i < G:
+                    dl = int(d[b, i]) - sh.v0
+                    if d[b, i] >= 0 and 0 <= dl < V:
+                        has, qd = 1, (1.0 if q is None else q[b, i, dl])
+                rec[b, i, 0] = (len(order), qd, has, nan)
+                for e, v in enumerate(order):
+                    qv = 0.0
+                    if i < G:
+                        qv = (1.0 if v + sh.v0 == d[b, i] else 0.0) if q is None else q[b, i, v]
+                    rec[b, i, 1 + e] = (x[v], sh.v0 + v, qv, 1)
+        return torch.from_numpy(rec)
+
+    def topk_finish(self, sh, cand_all, T, k, top_p, nshard):
+        C = cand_all.numpy()                       # [S, B, G1, k+1, 4]
+        S, B, G1 = C.shape[:3]
+        G = G1 - 1
+        d = sh.draft.numpy()
+        u = sh.uniforms.double().numpy()
+        tok = np.full((B, G1), -1, np.int32)
+        n_out = np.zeros(B, np.int32)
+        a_out = np.zeros((B, G), np.float32)
+        st_out = np.zeros(B, np.int32)
+
+        def row(b, i):
+            ent = [C[r, b, i, 1 + e] for r in range(S) for e in range(k) if C[r, b, i, 1 + e, 3]]
+            nan = any(C[r, b, i, 0, 3] for r in range(S))
+            ent.sort(key=lambda t: (-t[0], t[1]))
+            ent = ent[:k]
+            if nan or not ent or not np.isfinite(ent[0][0]):
+                return [], nan or True, 0.0, 0
+            w = np.exp(np.array([t[0] for t in ent]) / T - ent[0][0] / T)
+            W = w.sum()
+            J = len(ent)
+            if top_p < 1.0:
+                cum = np.cumsum(w)
+                J = int(np.argmax(cum >= top_p * W)) + 1
+            pk = w[:J] / w[:J].sum()
+            hd = [C[r, b, i, 0] for r in range(S) if C[r, b, i, 0, 2]]
+            qd, has = (hd[0][1], 1) if hd else (0.0, 0)
+            return [(int(t[1]), pk[j], t[2]) for j, t in enumerate(ent[:J])], False, qd, has
+
+        for b in range(B):
+            bits = 0
+            a = np.zeros(G)
+            for i in range(G):
+                kept, bad, qd, has = row(b, i)
+                if bad:
+                    bits |= SEQ_BADROW
+                di = int(d[b, i])
+                if di < 0 or di >= sh.Vg or not has:
+                    bits |= SEQ_OOB
+                    continue
+                pd = next((pv for v, pv, _ in kept if v == di), 0.0)
+                if qd > 0:
+                    a[i] = min(1.0, pd / qd)
+                else:
+                    a[i] = 1.0 if pd > 0 else 0.0
+                    bits |= SEQ_QBAD
+            rej = [i for i in range(G) if not (u[b, i] < a[i])]
+            n = rej[0] if rej else G
+            if row(b, G)[1]:
+                bits |= SEQ_BADROW
+            kept = sorted(row(b, n)[0])
+            r = np.array([max(pv - qv, 0.0) if n < G else pv for _, pv, qv in kept]) if kept else np.zeros(0)
+            if n < G and not r.sum() > 0:
+                bits |= SEQ_RESID0
+                r = np.array([pv for _, pv, _ in kept])
+            t = u[b, G] * r.sum()
+            c = np.cumsum(r)
+            hit = np.nonzero(c > t)[0]
+            pos = np.nonzero(r > 0)[0]
+            token = kept[hit[0]][0] if len(hit) else (kept[pos[-1]][0] if len(pos) else 0)
+            tok[b, :n] = d[b, :n]
+            tok[b, n] = token
+            n_out[b] = n
+            a_out[b] = a
+            st_out[b] = bits
+        sh.out.update(tokens=torch.from_numpy(tok), n=torch.from_numpy(n_out),
+                      a=None if G == 0 else torch.from_numpy(a_out), status=torch.from_numpy(st_out))
+
     def draw_pick(self, sh, totals_all, T, nshard):
         Tt = totals_all.numpy()                   # [S, B, 8]
         L = sh.logits.double().numpy()
@@ -205,6 +300,21 @@ def _case(B=5, G=4, V=1001, seed=11):
     return dict(logits=L, q=q.float(), draft=draft, draft_g=draft_g, uniforms=u)
 
 
+def _case_trunc(B=5, G=4, V=1000, seed=23, k=20, p=0.8):
+    g = torch.Generator().manual_seed(seed)
+    L = torch.randn(B, G + 1, V, generator=g) * 2.0
+    z = (L[:, :G] + torch.randn(B, G, V, generator=g)) / 0.9
+    vals, idx = torch.topk(z, k, dim=-1)
+    pk = torch.softmax(vals.double(), -1)
+    cum = pk.cumsum(-1)
+    pk = pk.masked_fill((cum - pk) >= p, 0.0)
+    pk = pk / pk.sum(-1, keepdim=True)
+    q = torch.zeros(B, G, V, dtype=torch.float64).scatter_(-1, idx, pk).float()
+    draft = torch.multinomial(q.reshape(B * G, V), 1, generator=g).view(B, G).to(torch.int32)
+    u = torch.rand(B, G + 1, generator=g)
+    return dict(logits=L, q=q, draft=draft, draft_g=draft, uniforms=u)
+
+
 def _shard_of(inp, rank, nshard, greedy):
     V = inp["logits"].shape[2]
     v0, Vr = sharded.split_vocab(V, nshard)[rank]
@@ -233,6 +343,11 @@ def _worker(rank, ws, port, queue):
             (res,) = sharded.run_shards([sh], sharded.TorchDistributedExchange(), ws, greedy=greedy,
                                         temperature=0.9, steps=CpuSteps())
             out[greedy] = [None if t is None else t.numpy().copy() for t in res]
+        tin = _case_trunc()
+        sh = _shard_of(tin, rank, ws, False)
+        (res,) = sharded.run_shards([sh], sharded.TorchDistributedExchange(), ws, greedy=False, temperature=0.9,
+                                    top_k=20, top_p=0.8, steps=CpuSteps())
+        out["trunc"] = [None if t is None else t.numpy().copy() for t in res]
         queue.put((rank, out))
         dist.barrier()
     finally:
@@ -267,11 +382,20 @@ def test_two_gloo_ranks_reach_the_whole_problem_result():
             _compare(got[r][greedy], inp, greedy)
         for x, y in zip(got[0][greedy], got[1][greedy]):
             assert (x is None and y is None) or np.array_equal(x, y)
+    tin = _case_trunc()
+    ref = svref.verify_sample(tin["logits"].numpy(), tin["q"].numpy(), tin["draft"].numpy(), tin["uniforms"].numpy(),
+                              0.9, 20, 0.8)
+    for r in (0, 1):
+        tok, n, a, st = (None if x is None else torch.from_numpy(x) for x in got[r]["trunc"])
+        P.compare_sample((tok, n, a, st), ref, 1000)
+    for x, y in zip(got[0]["trunc"], got[1]["trunc"]):
+        assert (x is None and y is None) or np.array_equal(x, y)
 
 
 @pytest.mark.parametrize("nshard", [1, 3, 7])
 def test_local_exchange_with_cpu_steps(nshard):
-    """The same driver with all shards in one process (LocalExchange)."""
+    """The same driver with all shards in one process (LocalExchange),
+    untruncated, greedy, and top-k then top-p."""
     inp = _case(B=6, V=503, seed=nshard)
     for greedy in (False, True):
         shards = [_shard_of(inp, r, nshard, greedy) for r in range(nshard)]
@@ -279,3 +403,12 @@ def test_local_exchange_with_cpu_steps(nshard):
                                  steps=CpuSteps())
         for r in range(nshard):
             _compare([None if t is None else t.numpy() for t in res[r]], inp, greedy)
+    tin = _case_trunc(seed=40 + nshard)
+    shards = [_shard_of(tin, r, nshard, False) for r in range(nshard)]
+    res = sharded.run_shards(shards, sharded.LocalExchange(), nshard, greedy=False, temperature=0.9, top_k=20,
+                             top_p=0.8, steps=CpuSteps())
+    ref = svref.verify_sample(tin["logits"].numpy(), tin["q"].numpy(), tin["draft"].numpy(), tin["uniforms"].numpy(),
+                              0.9, 20, 0.8)
+    for r in range(nshard):
+        tok, n, a, st = (None if t is None else t for t in res[r])
+        P.compare_sample((tok, n, a, st), ref, 1000)
