@@ -190,17 +190,17 @@ __device__ __forceinline__ void fd_gather(const Params& p, int b, FdDrafts& g) {
 // skipped) into
 // each row's maximum and two-float sum, delivered to lane (row mod 32) in
 // entry (row / 32) of m / s / bad (a row with no maximum, an infinite one or
-// no positive sum defines no distribution).  One aligned lane segment merges
-// one row.
+// no positive sum defines no distribution; nrows <= 65: three entries).  One
+// aligned lane segment merges one row.
 __device__ __forceinline__ void fd_merge_rows(const Params& p, const float4* base, long long r0g, int nrows,
-                                              float m[2], F2 s[2], int bad[2]) {
+                                              float m[3], F2 s[3], int bad[3]) {
   const int lane = threadIdx.x & 31;
   const int NP = stream_np(p);
   const int per = 32 / NP;   // rows merged per pass
   const int E = nrows * NP;
-  m[0] = m[1] = -INFINITY;
-  s[0] = s[1] = F2{0.f, 0.f};
-  bad[0] = bad[1] = 1;
+  m[0] = m[1] = m[2] = -INFINITY;
+  s[0] = s[1] = s[2] = F2{0.f, 0.f};
+  bad[0] = bad[1] = bad[2] = 1;
   for (int e0 = 0; e0 < E; e0 += 32) {
     const int e = e0 + lane;
     const bool ok = e < E && seg_valid(p, r0g + e / NP, e % NP);
@@ -216,7 +216,7 @@ __device__ __forceinline__ void fd_merge_rows(const Params& p, const float4* bas
     // row r0 + j's result is in lane j * NP; lane (row mod 32) takes it
     const int r0 = e0 / NP;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < 3; ++h) {
       const int row = lane + 32 * h;
       const int j = row - r0;
       const bool mine = j >= 0 && j < per && row < nrows;
@@ -243,9 +243,9 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
   const int G = p.gamma, G1 = G + 1, V = p.V;
   const int gb = seq_gamma(p, b);
   const int NP = stream_np(p);
-  float rM[2], qM[2];
-  F2 rS[2], qS[2];
-  int rBad[2], qBad[2];
+  float rM[3], qM[3];
+  F2 rS[3], qS[3];
+  int rBad[3], qBad[3];
   fd_merge_rows(p, p.part + (size_t)b * G1 * NP, (long long)b * G1, gb + 1, rM, rS, rBad);
   if (p.ql) fd_merge_rows(p, p.qpart + (size_t)b * G * NP, (long long)p.B * G1 + (long long)b * G, gb, qM, qS, qBad);
   int bits = 0;
@@ -277,12 +277,13 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
   }
   const int n = rej[0] ? __ffs(rej[0]) - 1 : (rej[1] ? 32 + __ffs(rej[1]) - 1 : gb);
   bits = __reduce_or_sync(0xffffffffu, bits);
-  if (__any_sync(0xffffffffu, (lane <= gb && rBad[0]) || (lane + 32 <= gb && rBad[1]))) bits |= SEQ_BADROW;
+  if (__any_sync(0xffffffffu, (lane <= gb && rBad[0]) || (lane + 32 <= gb && rBad[1]) || (lane + 64 <= gb && rBad[2])))
+    bits |= SEQ_BADROW;
   // row n's statistics (and its draft row's, with q from draft logits) from lane n mod 32
   const int hn = n >> 5, ln = n & 31;
-  const float Mn = __shfl_sync(0xffffffffu, hn ? rM[1] : rM[0], ln);
-  const float Sh = __shfl_sync(0xffffffffu, hn ? rS[1].hi : rS[0].hi, ln);
-  const float Sl = __shfl_sync(0xffffffffu, hn ? rS[1].lo : rS[0].lo, ln);
+  const float Mn = __shfl_sync(0xffffffffu, hn == 0 ? rM[0] : (hn == 1 ? rM[1] : rM[2]), ln);
+  const float Sh = __shfl_sync(0xffffffffu, hn == 0 ? rS[0].hi : (hn == 1 ? rS[1].hi : rS[2].hi), ln);
+  const float Sl = __shfl_sync(0xffffffffu, hn == 0 ? rS[0].lo : (hn == 1 ? rS[1].lo : rS[2].lo), ln);
   s.n = n;
   s.gb = gb;
   s.status = bits;
@@ -293,6 +294,7 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
   s.K = 0u;
   s.idx = 0;
   if (p.ql) {
+    // (draft rows: n < gb <= 64 when they are read, so entries 0 and 1)
     const float qm = __shfl_sync(0xffffffffu, hn ? qM[1] : qM[0], ln);
     const float qh = __shfl_sync(0xffffffffu, hn ? qS[1].hi : qS[0].hi, ln);
     const float ql = __shfl_sync(0xffffffffu, hn ? qS[1].lo : qS[0].lo, ln);
@@ -307,6 +309,8 @@ __device__ __forceinline__ void fd_scan(const Params& p, int b, const FdDrafts& 
       if (p.out_a && i < G) p.out_a[b * G + i] = i < gb ? a[h] : 0.f;
       if (i < G1 && i != n) p.out_tokens[b * G1 + i] = i < n ? g.d[h] : -1;
     }
+    // position 64 (gamma = 64): after a rejection at n < 64 it is padding
+    if (lane == 0 && G1 > 64 && n != 64) p.out_tokens[b * G1 + 64] = -1;
     if (lane == 0) p.out_n[b] = n;
   }
 }
@@ -340,6 +344,7 @@ __device__ __forceinline__ void fd_scan_tp(const Params& p, int b, bool writer, 
     }
     rej[h] = __ballot_sync(0xffffffffu, r);
   }
+  if (lane == 0 && gb >= 64) bits |= __ldcg(&tr[64].status) & SEQ_BADROW;   // the bonus row of gamma_b = 64
   const int n = rej[0] ? __ffs(rej[0]) - 1 : (rej[1] ? 32 + __ffs(rej[1]) - 1 : gb);
   bits = __reduce_or_sync(0xffffffffu, bits);
   s.n = n;
@@ -359,6 +364,8 @@ __device__ __forceinline__ void fd_scan_tp(const Params& p, int b, bool writer, 
       if (p.out_a && i < G) p.out_a[b * G + i] = i < gb ? a[h] : 0.f;
       if (i < G1 && i != n) p.out_tokens[b * G1 + i] = i < n ? d[h] : -1;
     }
+    // position 64 (gamma = 64): after a rejection at n < 64 it is padding
+    if (lane == 0 && G1 > 64 && n != 64) p.out_tokens[b * G1 + 64] = -1;
     if (lane == 0) p.out_n[b] = n;
   }
 }

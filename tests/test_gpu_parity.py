@@ -379,3 +379,48 @@ def test_gpu_expected_tokens_closed_form(sv, alpha, gamma):
     e = svref.expected_tokens_per_round(alpha, gamma)
     assert abs(emitted.mean() - e) < 4 * emitted.std(ddof=1) / np.sqrt(B)
     np.testing.assert_allclose(P.to_np(a), alpha, rtol=1e-6)
+
+
+# ------------------------------------------------------------------ gamma = 64 (the largest: 65 rows)
+
+@pytest.mark.parametrize("mode", ["sample", "topk", "topp", "greedy"])
+@pytest.mark.parametrize("V,B,forced", [(4096, 20, None), (4096, 20, "slices"), (1000, 2, "cluster")])
+def test_gamma_64_bonus_row(sv, monkeypatch, mode, V, B, forced):
+    """gamma = 64: row 64 is the bonus row.  Half the sequences have q = p
+    (every draft accepted, the bonus drawn from row 64), half a noisy q."""
+    if forced:
+        monkeypatch.setenv("SPECVERIFY_PATH", forced)
+    else:
+        monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
+    G, T = 64, 0.9
+    top_k, top_p = {"sample": (0, 1.0), "topk": (40, 0.9), "topp": (0, 0.8), "greedy": (0, 1.0)}[mode]
+    if mode == "topp" and forced == "cluster":
+        pytest.skip("top-p alone has its own rows path")
+    g = torch.Generator().manual_seed(64 + V + B)
+    L = (torch.randn(B, G + 1, V, generator=g) * 2.0).to(torch.bfloat16)
+    w = workloads.Workload("case", B, G, V, "f32", "sample", T, top_k=top_k, top_p=top_p, draft_sigma=1.0)
+    q = workloads._draft_proposal(w, L[:, :G].float(), g)
+    same = workloads.Workload("case", B, G, V, "f32", "sample", T, top_k=top_k, top_p=top_p, draft_sigma=0.0)
+    q_exact = workloads._proposal_of(same, L[:, :G].float() / T)
+    half = B // 2
+    q[:half] = q_exact[:half]
+    draft = torch.multinomial(q.reshape(B * G, V), 1, generator=g).view(B, G).to(torch.int32)
+    if mode == "greedy":
+        am = L[:, :G].float().argmax(-1).to(torch.int32)
+        draft[:half] = am[:half]
+    u = torch.rand(B, G + 1, generator=g)
+    inp = dict(logits=L.contiguous(), q=q.contiguous(), draft=draft, uniforms=u)
+    d = _gpu(inp)
+    if mode == "greedy":
+        got = sv.verify_greedy(d["logits"], d["draft"])
+        torch.cuda.synchronize()
+        ref = P.oracle_greedy(inp)
+        P.compare_greedy(got, ref, V)
+        assert (ref["n_accepted"][:half] == G).all()
+        return
+    got = sv.verify_sample(d["logits"], d["q"], d["draft"], d["uniforms"], T, top_k, top_p)
+    torch.cuda.synchronize()
+    ref = P.oracle_sample(inp, T, top_k, top_p)
+    P.compare_sample(got, ref, V)
+    # the bonus row is drawn from (q = p up to the draft's own tie order at the cut)
+    assert (ref["n_accepted"][:half] == G).sum() >= (half - 1 if mode == "sample" else min(2, half))

@@ -62,7 +62,8 @@ def _dev(inp):
 
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("V,G,B", [(8, 3, 7), (1001, 4, 9), (40003, 4, 5), (32000, 8, 3), (128256, 4, 4)])
+@pytest.mark.parametrize("V,G,B", [(8, 3, 7), (1001, 4, 9), (40003, 4, 5), (32000, 8, 3), (128256, 4, 4),
+                                   (2048, 64, 3)])
 def test_sharded_sample_matches_oracle(sharded, S, dt, V, G, B):
     if S > V:
         pytest.skip("more shards than tokens")
@@ -76,7 +77,7 @@ def test_sharded_sample_matches_oracle(sharded, S, dt, V, G, B):
 
 @pytest.mark.parametrize("S", [1, 2, 5, 8])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("V,G,B", [(9, 2, 6), (1000, 4, 17), (40003, 8, 5), (128256, 4, 6)])
+@pytest.mark.parametrize("V,G,B", [(9, 2, 6), (1000, 4, 17), (40003, 8, 5), (128256, 4, 6), (2048, 64, 4)])
 def test_sharded_greedy_matches_oracle(sharded, S, dt, V, G, B):
     inp = _case(2000 + S + V + G, B, G, V, DTYPES[dt], ties=True)
     L = inp["logits"].float()
@@ -193,7 +194,7 @@ def _case_trunc(seed, B, G, V, dtype, T, top_k, top_p, one_hot=False):
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("dt", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("V,G,B,k,p", [(1000, 4, 9, 50, 0.9), (40000, 4, 5, 50, 1.0), (152064, 8, 3, 50, 0.9),
-                                       (4096, 3, 6, 200, 0.8), (20000, 2, 4, 1, 1.0)])
+                                       (4096, 3, 6, 200, 0.8), (20000, 2, 4, 1, 1.0), (2048, 64, 3, 30, 0.9)])
 def test_sharded_topk_topp_matches_oracle(sharded, S, dt, V, G, B, k, p):
     align = 4 if dt == "f32" else 8
     if S * k > 2048:
