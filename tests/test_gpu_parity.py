@@ -424,3 +424,23 @@ def test_gamma_64_bonus_row(sv, monkeypatch, mode, V, B, forced):
     P.compare_sample(got, ref, V)
     # the bonus row is drawn from (q = p up to the draft's own tie order at the cut)
     assert (ref["n_accepted"][:half] == G).sum() >= (half - 1 if mode == "sample" else min(2, half))
+
+
+# ------------------------------------------------------------------ the largest vocabulary
+
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_max_vocabulary(sv, monkeypatch, mode):
+    """V = SV_MAX_VOCAB (2^24): 8192 final-draw items per row, the largest
+    search stash, the streaming kernel's shortest grid."""
+    monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
+    V, G, B = 1 << 24, 2, 2
+    inp = _random_case(24, B, G, V, torch.bfloat16, T=1.0, spread=3.0)
+    d = _gpu(inp)
+    if mode == "greedy":
+        got = sv.verify_greedy(d["logits"], d["draft"])
+        torch.cuda.synchronize()
+        P.compare_greedy(got, P.oracle_greedy(inp), V)
+    else:
+        got = sv.verify_sample(d["logits"], d["q"], d["draft"], d["uniforms"], 1.0)
+        torch.cuda.synchronize()
+        P.compare_sample(got, P.oracle_sample(inp, 1.0), V)

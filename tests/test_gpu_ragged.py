@@ -74,7 +74,7 @@ def _oracle(inp, gb, T, top_k=0, top_p=1.0):
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("V,G,B,T", [(7, 3, 40, 1.0), (1000, 4, 12, 0.7), (40003, 5, 6, 1.0), (32000, 5, 4, 0.7),
-                                     (128256, 4, 4, 1.0)])
+                                     (128256, 4, 4, 1.0), (4096, 64, 20, 0.9)])
 @pytest.mark.parametrize("det", [False, True])
 def test_ragged_sample(sv, path, dt, V, G, B, T, det):
     inp, gb = _case(700 + V + G, B, G, V, DTYPES[dt], T, deterministic=det)
@@ -88,7 +88,7 @@ def test_ragged_sample(sv, path, dt, V, G, B, T, det):
 
 
 @pytest.mark.parametrize("tk_path", ["auto", "slices"])
-@pytest.mark.parametrize("V,G,B,k,tp", [(5000, 4, 12, 50, 0.9), (40000, 8, 6, 50, 0.9)])
+@pytest.mark.parametrize("V,G,B,k,tp", [(5000, 4, 12, 50, 0.9), (40000, 8, 6, 50, 0.9), (4096, 64, 12, 30, 0.9)])
 def test_ragged_topk(sv, monkeypatch, tk_path, V, G, B, k, tp):
     if tk_path == "slices":
         monkeypatch.setenv("SPECVERIFY_PATH", "slices")
@@ -100,7 +100,7 @@ def test_ragged_topk(sv, monkeypatch, tk_path, V, G, B, k, tp):
     P.compare_sample(out, _oracle(inp, gb, 0.8, k, tp), V)
 
 
-@pytest.mark.parametrize("V,G,B", [(7, 4, 33), (40003, 4, 9), (128256, 4, 6), (32000, 5, 3)])
+@pytest.mark.parametrize("V,G,B", [(7, 4, 33), (40003, 4, 9), (128256, 4, 6), (32000, 5, 3), (4096, 64, 16)])
 def test_ragged_greedy(sv, path, V, G, B):
     inp, gb = _case(1100 + V, B, G, V, torch.bfloat16)
     L = inp["logits"].float()
