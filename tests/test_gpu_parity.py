@@ -195,7 +195,7 @@ def topk_path(request, monkeypatch):
 @pytest.mark.parametrize("V,G,B,k,tp", [(7, 2, 50, 3, 1.0), (100, 4, 30, 1, 1.0), (5000, 4, 12, 50, 0.9),
                                         (40003, 8, 4, 50, 0.9), (40003, 3, 4, 200, 0.5), (600, 2, 20, 0, 0.8),
                                         (33, 3, 40, 40, 0.95), (40000, 8, 6, 50, 0.9), (16384, 4, 8, 600, 0.7),
-                                        (1024, 2, 16, 1000, 0.99)])
+                                        (1024, 2, 16, 1000, 0.99), (152064, 4, 4, 1024, 0.95)])
 def test_topk_small(sv, topk_path, dt, V, G, B, k, tp):
     inp = _random_case(300 + V + k, B, G, V, DTYPES[dt], T=0.8, ties=True, spread=1.0, top_k=k, top_p=tp)
     g = _gpu(inp)
@@ -444,3 +444,20 @@ def test_max_vocabulary(sv, monkeypatch, mode):
         got = sv.verify_sample(d["logits"], d["q"], d["draft"], d["uniforms"], 1.0)
         torch.cuda.synchronize()
         P.compare_sample(got, P.oracle_sample(inp, 1.0), V)
+
+
+def test_large_batch(sv, monkeypatch):
+    """B = 4096 sequences (V = 1024, gamma = 4): the grids and workspace of a
+    large batch; every sequence against the oracle (process pool)."""
+    monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
+    V, G, B = 1024, 4, 4096
+    inp = _random_case(4096, B, G, V, torch.float32, T=0.9)
+    d = _gpu(inp)
+    got = sv.verify_sample(d["logits"], d["q"], d["draft"], d["uniforms"], 0.9)
+    torch.cuda.synchronize()
+    ref = P.oracle_sample_pool(inp, 0.9)
+    stats = P.compare_sample(got, ref, V)
+    assert stats["sequences"] == B
+    got_g = sv.verify_greedy(d["logits"], d["draft"])
+    torch.cuda.synchronize()
+    P.compare_greedy(got_g, P.oracle_greedy(inp), V)

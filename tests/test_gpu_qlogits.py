@@ -66,7 +66,8 @@ def _oracle(inp, T, rows=None):
 
 @pytest.mark.parametrize("ldt,qdt", [("bf16", "bf16"), ("f32", "f32"), ("f16", "bf16"), ("bf16", "f32")])
 @pytest.mark.parametrize("V,G,B,T", [(257, 3, 16, 1.0), (1000, 4, 12, 0.7), (32000, 5, 3, 0.7),
-                                     (128256, 4, 4, 1.0), (4096, 0, 5, 1.0), (4096, 1, 30, 1.3)])
+                                     (128256, 4, 4, 1.0), (4096, 0, 5, 1.0), (4096, 1, 30, 1.3),
+                                     (4096, 64, 6, 0.9)])
 def test_qlogits_small(sv, path, ldt, qdt, V, G, B, T):
     inp = _ql_case(3000 + V + G, B, G, V, DTYPES[ldt], DTYPES[qdt])
     g = _gpu(inp)

@@ -260,3 +260,17 @@ def test_sharded_topk_launches_and_leaves_workspace_zeroed(sv, sharded):
     assert ["stream_topk_kernel"] in seen and ["shard_topk_finish_kernel"] in seen
     for sh in shards:
         assert int(sh.workspace.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_sharded_max_shards(sharded, greedy):
+    """SV_MAX_SHARDS (32) shards of V = 128256."""
+    inp = _case(32, 6, 4, 128256, torch.bfloat16, T=1.0)
+    d = _dev(inp)
+    got = sharded.simulate(d["logits"], None if greedy else d["q"], d["draft"], None if greedy else d["uniforms"], 32,
+                           greedy=greedy, temperature=1.0)
+    torch.cuda.synchronize()
+    if greedy:
+        P.compare_greedy(got[:2] + (got[3],), P.oracle_greedy(inp), 128256)
+    else:
+        P.compare_sample(got, P.oracle_sample(inp, 1.0), 128256)
