@@ -204,6 +204,7 @@ int path_override() {
   if (!std::strcmp(e, "cluster")) return 2;
   if (!std::strcmp(e, "slices")) return 3;   // top-k: the per-slice kernel instead of the per-row one
   if (!std::strcmp(e, "topp")) return 4;     // top-p alone: the per-row threshold path at any V
+  if (!std::strcmp(e, "topprow")) return 5;  // top-p alone, threshold path, and one CTA per row (no cluster)
   return 0;
 }
 
@@ -370,6 +371,49 @@ sv_status launch_greedy_finish(const sv::Params& p, cudaStream_t stream) {
 // Kernels launched by the last call on this host thread (sv_last_kernels).
 thread_local const char* g_last_kernels = "";
 
+// Top-p alone with each row resident in a cluster's shared memory
+// (topp_cluster_kernel): rows of whole 16-byte vectors, at most kTcMaxC
+// slices of kTcSliceBytes.  *launched = false: not applicable here (the
+// per-row kernel runs instead).
+template <typename T>
+sv_status launch_topp_cluster(const sv::Params& p, cudaStream_t stream, bool* launched) {
+  *launched = false;
+  const int VW = (int)(16 / sizeof(T));
+  if (path_override() == 5 || p.V % VW != 0 || !aligned16(p.logits)) return SV_OK;
+  const long long C = ceil_div((long long)p.V * (long long)sizeof(T), (long long)sv::kTcSliceBytes);
+  if (C > sv::kTcMaxC) return SV_OK;
+  const long long Vc = ceil_div(ceil_div((long long)p.V, C), (long long)VW) * VW;
+  const size_t smem = sv::tc_head_bytes() + (size_t)Vc * sizeof(T);
+  auto kern = sv::topp_cluster_kernel<T>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_OK;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long long)p.B * (p.gamma + 1) * C));
+  cfg.blockDim = dim3(sv::kTpThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters < 1) {
+    cudaGetLastError();
+    return SV_OK;
+  }
+  if (cudaLaunchKernelEx(&cfg, kern, p, p.tp, (int)Vc) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  *launched = true;
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 template <typename T>
 sv_status dispatch(sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
   sv::ClusterParams cp;
@@ -392,19 +436,25 @@ sv_status dispatch(sv::Params& p, int mode, cudaStream_t stream, sv_dtype dt) {
   sv_status st = SV_OK;
   if (mode == sv::MODE_TOPP) {
     // top-p alone: the rows' kept sets, then the final draw under the mask
-    const size_t smem = sizeof(sv::TpSmem);
-    auto tk = sv::topp_row_kernel<T>;
-    if (cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-      cudaGetLastError();
-      return SV_ERR_CUDA;
+    bool in_cluster = false;
+    st = launch_topp_cluster<T>(p, stream, &in_cluster);
+    if (st != SV_OK) return st;
+    if (!in_cluster) {
+      const size_t smem = sizeof(sv::TpSmem);
+      auto tk = sv::topp_row_kernel<T>;
+      if (cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+      }
+      tk<<<(unsigned)((long long)p.B * (p.gamma + 1)), sv::kTpThreads, smem, stream>>>(p, p.tp);
+      if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     }
-    tk<<<(unsigned)((long long)p.B * (p.gamma + 1)), sv::kTpThreads, smem, stream>>>(p, p.tp);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     timing_record(1, stream);
     p.H = 0;
     st = launch_final_draw<T, true>(p, stream);
     timing_record(2, stream);
-    g_last_kernels = st == SV_OK ? "topp_row_kernel,final_draw_kernel" : "";
+    g_last_kernels = st != SV_OK ? "" : (in_cluster ? "topp_cluster_kernel,final_draw_kernel"
+                                                     : "topp_row_kernel,final_draw_kernel");
     return st;
   }
   const bool streamable = p.V % vec_width(dt) == 0 && path_override() != 3;

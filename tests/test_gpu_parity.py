@@ -203,17 +203,34 @@ def test_topk_small(sv, topk_path, dt, V, G, B, k, tp):
     P.compare_sample(out, P.oracle_sample(inp, 0.8, k, tp), V)
 
 
+def _topp_kernel(V, esize, forced_row=False):
+    """The threshold kernel the library runs for top-p alone: a row of whole
+    16-byte vectors that fits 8 slices of 64 KB sits in a cluster's shared
+    memory; any other row streams through one CTA."""
+    fits = V % (16 // esize) == 0 and -(-V * esize // 65536) <= 8
+    return "topp_cluster_kernel" if fits and not forced_row else "topp_row_kernel"
+
+
+@pytest.mark.parametrize("path", ["auto", "topprow"])
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("V,G,B,tp,T", [(40003, 4, 6, 0.9, 1.0), (128256, 4, 4, 0.5, 1.0), (152064, 8, 2, 0.99, 0.8),
-                                        (5000, 3, 10, 0.95, 0.7), (1030, 2, 12, 0.6, 1.3)])
-def test_topp_only_any_vocab(sv, dt, V, G, B, tp, T):
-    """top-p with no top-k beyond SV_MAX_TOP_K tokens (the per-row threshold
-    path): Zipf-like rows with heavy tails (large kept sets) and exact ties."""
+                                        (5000, 3, 10, 0.95, 0.7), (1030, 2, 12, 0.6, 1.3), (32768, 2, 5, 0.9, 1.0),
+                                        (65544, 3, 4, 0.8, 1.0)])
+def test_topp_only_any_vocab(sv, monkeypatch, path, dt, V, G, B, tp, T):
+    """top-p with no top-k beyond SV_MAX_TOP_K tokens (the threshold path):
+    Zipf-like rows with heavy tails (large kept sets) and exact ties; the
+    cluster-resident kernel (1 to 8 slices, the last one short) and the
+    per-row kernel on the same inputs."""
+    if path == "topprow":
+        monkeypatch.setenv("SPECVERIFY_PATH", "topprow")
+    else:
+        monkeypatch.delenv("SPECVERIFY_PATH", raising=False)
     w = workloads.Workload("topp", B, G, V, dt, "sample", T, top_k=0, top_p=tp, draft_sigma=0.7, seed=V + G)
     inp = workloads.make_inputs(w, seed=V + int(tp * 100))
     g = _gpu(inp)
     out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], T, 0, tp)
-    assert sv.sv_last_kernels() == ["topp_row_kernel", "final_draw_kernel"]
+    esize = {"bf16": 2, "f16": 2, "f32": 4}[dt]
+    assert sv.sv_last_kernels() == [_topp_kernel(V, esize, path == "topprow"), "final_draw_kernel"]
     P.compare_sample(out, P.oracle_sample(inp, T, 0, tp), V)
 
 
@@ -225,7 +242,7 @@ def test_topp_only_threshold_path_forced_small_vocab(sv, monkeypatch, V, G, B, t
     inp = _random_case(700 + V, B, G, V, torch.bfloat16, T=0.9, ties=True, spread=1.0, top_k=0, top_p=tp)
     g = _gpu(inp)
     out = sv.verify_sample(g["logits"], g["q"], g["draft"], g["uniforms"], 0.9, 0, tp)
-    assert sv.sv_last_kernels() == ["topp_row_kernel", "final_draw_kernel"]
+    assert sv.sv_last_kernels() == [_topp_kernel(V, 2), "final_draw_kernel"]
     P.compare_sample(out, P.oracle_sample(inp, 0.9, 0, tp), V)
     out = sv.verify_sample(g["logits"], None, g["draft"], g["uniforms"], 0.9, 0, tp)
     P.compare_sample(out, P.oracle_sample(dict(inp, q=None), 0.9, 0, tp), V)
