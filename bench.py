@@ -174,6 +174,34 @@ def kept_counts(logits_rows: torch.Tensor, temperature: float, top_k: int, top_p
     return (before < top_p).sum(-1)
 
 
+def kept_rows_q(w, st, out):
+    """Kept candidates over the rejected sequences' rows n (the q entries a
+    truncated final draw reads), for one input set and its outputs."""
+    if w.mode != "sample" or (w.top_k <= 0 and w.top_p >= 1.0) or _q_elt_bytes(w) == 0:
+        return 0
+    n = out[1].long()
+    rej = n < w.gamma
+    if not rej.any():
+        return 0
+    rows = st["logits"][torch.nonzero(rej).flatten(), n[rej]]
+    return int(kept_counts(rows, w.temperature, w.top_k, w.top_p).sum().item())
+
+
+def q_bytes_read(w, n_accepted: np.ndarray, st, kept_rejected: int) -> int:
+    """Bytes of q the kernels read for one input set: q(d_i) at every tested
+    position, then q at the kept candidates of each rejected sequence's row
+    n (top-k / top-p) or that whole row (untruncated)."""
+    qb = _q_elt_bytes(w)
+    if w.mode != "sample" or qb == 0 or w.qlogits:
+        return 0
+    gb = st["gamma_b"].cpu().numpy() if w.ragged else np.full(len(n_accepted), w.gamma)
+    gsum = int(gb.sum())
+    if w.top_k > 0 or w.top_p < 1.0:
+        return (gsum + int(kept_rejected)) * qb
+    rejected = int((n_accepted < gb).sum())
+    return (gsum + rejected * w.V) * qb
+
+
 class Clocks:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -531,46 +559,74 @@ def run_gb300(args, rank, ws_n, local):
     # step.  The step's inputs sit in one pinned host buffer and its outputs in
     # one device buffer (views at 256-byte offsets), so one copy moves each way;
     # copy in, call, copy out are captured in a CUDA graph replayed per step.
-    ins = dict(rn.sets[0])
-    if w.mode == "greedy":
-        ins["uniforms"] = None                     # greedy reads no uniforms
-    host_in, dev_in_buf, dev_in = _packed(ins, dev)
-    out_named = {str(i): x for i, x in enumerate(rn.outs[0])}
-    if w.mode == "greedy":
-        out_named["2"] = None                      # greedy writes no accept_prob
-    host_out, dev_out_buf, dev_out_v = _packed(out_named, dev)
-    dev_out = tuple(dev_out_v[str(i)] for i in range(len(rn.outs[0])))
-    h2d = host_in.numel()
-    d2h = host_out.numel()
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
+    # q (the draft's probabilities) may stay in pinned host memory: the
+    # kernels read it in place, only where the method needs it (q(d_i), the
+    # kept candidates, a rejected sequence's residual row).  Both ways are
+    # measured; the headline e2e leaves q on the host.
+    def e2e_run(q_in_place):
+        ins = dict(rn.sets[0])
+        if w.mode == "greedy":
+            ins["uniforms"] = None                 # greedy reads no uniforms
+        q_host = None
+        if q_in_place and ins.get("q") is not None:
+            q_host = ins.pop("q").cpu().pin_memory()
+        host_in, dev_in_buf, dev_in = _packed(ins, dev)
+        if q_host is not None:
+            dev_in["q"] = q_host
+        out_named = {str(i): x for i, x in enumerate(rn.outs[0])}
+        if w.mode == "greedy":
+            out_named["2"] = None                  # greedy writes no accept_prob
+        host_out, dev_out_buf, dev_out_v = _packed(out_named, dev)
+        dev_out = tuple(dev_out_v[str(i)] for i in range(len(rn.outs[0])))
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                dev_in_buf.copy_(host_in, non_blocking=True)
+                _call(sv, w, dev_in, dev_out, rn.ws, stream)
+                host_out.copy_(dev_out_buf, non_blocking=True)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g_e2e, stream=stream):
             dev_in_buf.copy_(host_in, non_blocking=True)
             _call(sv, w, dev_in, dev_out, rn.ws, stream)
             host_out.copy_(dev_out_buf, non_blocking=True)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        dev_in_buf.copy_(host_in, non_blocking=True)
-        _call(sv, w, dev_in, dev_out, rn.ws, stream)
-        host_out.copy_(dev_out_buf, non_blocking=True)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            g_e2e.replay()
-    torch.cuda.synchronize()
-    est_e2e = (time.perf_counter() - t0) / 3
-    n_e2e = max(3, min(steps, 2000, int(2.0 / max(est_e2e, 1e-6))))
-    with torch.cuda.stream(stream):
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(n_e2e):
-            g_e2e.replay()
-        f1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, ws_n, dev)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_e2e.replay()
+        torch.cuda.synchronize()
+        est_e2e = (time.perf_counter() - t0) / 3
+        n_e2e = max(3, min(steps, 2000, int(2.0 / max(est_e2e, 1e-6))))
+        with torch.cuda.stream(stream):
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(n_e2e):
+                g_e2e.replay()
+            f1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, ws_n, dev)
+        res = (ms_e2e, n_e2e, host_in.numel(), host_out.numel(), q_host is not None)
+        del host_in, dev_in_buf, host_out, dev_out_buf, g_e2e, q_host
+        return res
+
     pos_e2e = float((rn.sets[0]["gamma_b"].sum() + B).item()) if w.ragged else positions   # the input set used
-    del host_in, dev_in_buf, host_out, dev_out_buf, g_e2e
+    ms_e2e, n_e2e, h2d_copied, d2h, q_kept_on_host = e2e_run(True)
+    ms_all, n_all, h2d_all = (e2e_run(False)[:3] if q_kept_on_host else (ms_e2e, n_e2e, h2d_copied))
+    # q bytes the kernels read across the host link (the method's q reads,
+    # for the input set used)
+    q_link = 0
+    if q_kept_on_host:
+        q_link = q_bytes_read(w, rn.outs[0][1].cpu().numpy(), rn.sets[0], kept_rows_q(w, rn.sets[0], rn.outs[0]))
+    e2e = {"value": pos_e2e * ws_n / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d_copied + q_link,
+           "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e,
+           "h2d_copied_bytes": h2d_copied, "q_read_in_place_bytes": q_link,
+           "how": ("logits, drafts and uniforms in one pinned host buffer copied in; q left in pinned host "
+                   "memory and read in place by the kernels; outputs in one device buffer copied out; "
+                   "captured in a CUDA graph and replayed once per step") if q_kept_on_host else
+                  ("inputs in one pinned host buffer, outputs in one device buffer; copy in, call, copy out "
+                   "captured in a CUDA graph and replayed once per step"),
+           "all_inputs_copied": {"value": pos_e2e * ws_n / (ms_all / 1e3), "ms_per_step": ms_all,
+                                 "h2d_bytes_per_step": h2d_all, "steps": n_all}}
 
     line = {
         "metric": METRIC,
@@ -602,10 +658,7 @@ def run_gb300(args, rank, ws_n, local):
         "kernel_us": _kernel_us(kernel_names, t_stream, t_final),
         "algorithmic_bytes_per_step": ab,
         "acceptance": acc,
-        "e2e": {"value": pos_e2e * ws_n / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": n_e2e,
-                "how": "inputs in one pinned host buffer, outputs in one device buffer; copy in, call, copy out "
-                       "captured in a CUDA graph and replayed once per step"},
+        "e2e": e2e,
         "gpu_launches": steps * kernels_per_call,
         "clocks": clk,
     }

@@ -110,7 +110,13 @@ size_t sv_workspace_bytes(int B, int gamma, int V, int top_k);
  *   logits           [B][gamma+1][V] of logits_dtype; row i predicts the token
  *                    at draft position i, row gamma the bonus position
  *   q                [B][gamma][V] float32, the draft's actual proposal
- *                    probabilities (non-negative), 16-byte aligned; or NULL:
+ *                    probabilities (non-negative), 16-byte aligned, in device
+ *                    memory or in pinned host memory the device reads at the
+ *                    same address (sv_pointer_device_readable): the kernels
+ *                    read q only at the drafted tokens, at the kept
+ *                    candidates (top-k / top-p) and along the residual row
+ *                    of a rejected sequence, so host-resident q crosses the
+ *                    host link only there; or NULL:
  *                    deterministic drafts (n-gram, prompt lookup), each q_i
  *                    one-hot at d_i.  Then a_i = p_i(d_i) and a rejection at
  *                    i draws from p_i with d_i removed, renormalised; no q
@@ -296,6 +302,15 @@ const char* sv_status_string(sv_status s);
  * Static storage owned by the library; thread-local.
  */
 const char* sv_last_kernels(void);
+
+/*
+ * 1 if the device reads p at the same address: device memory, managed
+ * memory, or host memory that is pinned and mapped (cudaHostAlloc under
+ * unified addressing); else 0 (pageable host memory, a foreign pointer,
+ * NULL).  Launches nothing; clears the CUDA error it may raise.  Callers use
+ * it before passing q in host memory (see sv_verify_sample).
+ */
+int sv_pointer_device_readable(const void* p);
 
 /*
  * Measurement hook (outside the verify computation; used by the benchmark to

@@ -86,6 +86,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sv_truncate_emitted.restype = _c_int
     lib.sv_last_kernels.argtypes = []
     lib.sv_last_kernels.restype = ctypes.c_char_p
+    lib.sv_pointer_device_readable.argtypes = [_c_ptr]
+    lib.sv_pointer_device_readable.restype = ctypes.c_int
     lib.sv_qlogits_workspace_bytes.argtypes = [_c_int, _c_int, _c_int, _c_int]
     lib.sv_qlogits_workspace_bytes.restype = _c_size
     lib.sv_verify_sample_qlogits.argtypes = [_c_int, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr,
@@ -238,6 +240,12 @@ def sv_truncate_emitted(B, gamma, tokens, num_accepted, stop_tokens, n_stop, max
                                                    out_num_emitted, stream))
 
 
+def sv_pointer_device_readable(ptr) -> bool:
+    """True if the device reads this address as is (device memory, managed
+    memory, or pinned host memory mapped at the same address)."""
+    return bool(load_library().sv_pointer_device_readable(ptr))
+
+
 def sv_last_kernels() -> list:
     """Kernels launched by the last verify call on this thread, in order."""
     names = load_library().sv_last_kernels().decode()
@@ -271,6 +279,21 @@ def _need_cuda(name, t, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _need_readable(name, t, dtype=None):
+    """A CUDA tensor, or a host tensor in pinned memory the device reads at
+    the same address (q may stay on the host: the kernels read only the
+    entries the method needs)."""
+    if t is None or t.is_cuda:
+        _need_cuda(name, t, dtype)
+        return
+    if not t.is_pinned() or not sv_pointer_device_readable(t.data_ptr()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory the device can read")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
 def alloc_workspace(B: int, gamma: int, V: int, top_k: int = 0, device=None) -> torch.Tensor:
     """A zero-filled device workspace large enough for (B, gamma, V, top_k)."""
     n = sv_workspace_bytes(B, gamma, V, top_k)
@@ -290,9 +313,11 @@ def verify_sample(logits, q, draft, uniforms, temperature=1.0, top_k=0, top_p=1.
 
     logits [B, gamma+1, V] (float32 / bfloat16 / float16), q [B, gamma, V]
     float32 (or None: deterministic drafts, q one-hot at each drafted token),
-    draft [B, gamma] int32, uniforms [B, gamma+1] float32, all CUDA tensors.
-    gamma_b [B] int32 (CUDA) makes the round ragged: sequence b drafted only
-    gamma_b[b] tokens (sv_verify_sample_ragged).
+    draft [B, gamma] int32, uniforms [B, gamma+1] float32, all CUDA tensors
+    except q, which may also be a pinned host tensor (read in place: only
+    q(d_i), the kept candidates and a rejected sequence's residual row cross
+    the host link).  gamma_b [B] int32 (CUDA) makes the round ragged:
+    sequence b drafted only gamma_b[b] tokens (sv_verify_sample_ragged).
     Returns (out_tokens [B, gamma+1] int32, n_accepted [B] int32, accept_prob
     [B, gamma] float32 or None, status [B] int32).
     """
@@ -302,7 +327,7 @@ def verify_sample(logits, q, draft, uniforms, temperature=1.0, top_k=0, top_p=1.
     _need_cuda("logits", logits)
     if logits.dtype not in _TORCH_DTYPE:
         raise ValueError(f"unsupported logits dtype {logits.dtype}")
-    _need_cuda("q", q if G > 0 else None, torch.float32)
+    _need_readable("q", q if G > 0 else None, torch.float32)
     _need_cuda("draft", draft if G > 0 else None, torch.int32)
     _need_cuda("uniforms", uniforms, torch.float32)
     if outputs is None:

@@ -786,6 +786,17 @@ extern "C" const char* sv_status_string(sv_status s) {
 
 extern "C" const char* sv_last_kernels(void) { return g_last_kernels; }
 
+extern "C" int sv_pointer_device_readable(const void* p) {
+  if (p == nullptr) return 0;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return 1;
+  return at.type == cudaMemoryTypeHost && at.devicePointer == p ? 1 : 0;
+}
+
 extern "C" sv_status sv_set_timing_events(void* const* events, int n) {
   if (n == 0) {
     g_timing_on = false;

@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(sv):
                           "sv_verify_sample_ragged", "sv_verify_greedy_ragged", "sv_truncate_emitted",
                           "sv_qlogits_workspace_bytes", "sv_verify_sample_qlogits", "sv_shard_workspace_bytes",
                           "sv_shard_row_stats", "sv_shard_scan", "sv_shard_draw_sums", "sv_shard_draw_pick",
-                          "sv_shard_topk_candidates", "sv_shard_topk_finish"}
+                          "sv_shard_topk_candidates", "sv_shard_topk_finish", "sv_pointer_device_readable"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -252,3 +252,13 @@ def test_shard_topk_entry_points_validate_before_launch(sv):
     assert sv.sv_shard_topk_finish(2, 4, 4, 4096, A, A, A, 1.0, 50, 0.0, A, A, A, A, None) == sv.SV_ERR_INVALID_ARG
     assert sv.sv_shard_topk_finish(2, 4, 4, 4096, A, A, None, 1.0, 50, 0.9, A, A, A, A, None) == \
         sv.SV_ERR_INVALID_ARG
+
+
+def test_pointer_device_readable_on_host_memory(sv):
+    """No device pointer on a machine without a usable GPU (or NULL / a
+    pageable host address anywhere): 0, and no CUDA error is left behind."""
+    import numpy as np
+
+    buf = np.zeros(64, np.uint8)
+    assert not sv.sv_pointer_device_readable(None)
+    assert not sv.sv_pointer_device_readable(buf.ctypes.data)

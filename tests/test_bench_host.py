@@ -117,3 +117,22 @@ def test_algorithmic_bytes_counts_kept_q_reads():
     ab = bench.algorithmic_bytes(tp, np.zeros(64, int), kept_rejected=1000)
     assert ab["stream"] == 64 * 5 * 128256 * 2 + 64 * 4 * 6
     assert ab["final"] == 64 * 128256 * 2 + 4000
+
+
+def test_q_bytes_read_in_place():
+    """q bytes the kernels read when q stays in host memory (the e2e arm):
+    q(d_i) at every tested position, then row n's kept candidates
+    (truncated) or the whole row n (untruncated) of each rejected sequence."""
+    import torch
+
+    w = workloads.WORKLOADS["sample_b64_g4_v128256_bf16_s0.7"]
+    n = np.array([4] * 10 + [1] * 54)
+    assert bench.q_bytes_read(w, n, {}, 0) == (64 * 4 + 54 * 128256) * 4
+    t = workloads.WORKLOADS["topk50_topp0.9_b256_g8_v152064_bf16"]
+    assert bench.q_bytes_read(t, np.zeros(256, int), {}, 1000) == (256 * 8 + 1000) * 4
+    for name in ("greedy_b512_g4_v128256_bf16", "sample_det_b64_g4_v128256_bf16", "sample_qlogits_b64_g4_v128256_bf16"):
+        assert bench.q_bytes_read(workloads.WORKLOADS[name], n, {}, 0) == 0
+    r = workloads.WORKLOADS["sample_ragged_b64_g8_v128256_bf16"]
+    gb = torch.tensor([8] * 32 + [2] * 32, dtype=torch.int32)
+    nr = np.array([8] * 32 + [0] * 32)
+    assert bench.q_bytes_read(r, nr, {"gamma_b": gb}, 0) == (32 * 8 + 32 * 2 + 32 * 128256) * 4
