@@ -530,25 +530,41 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_cluster_kernel(const Param
     const uint64_t span = 1ull << width;
 #pragma unroll
     for (int k = 0; k < kTpBuckets; ++k) sm.hist[k][tid] = 0.f;
-    const TpFilter<T> flt = tp_filter<T>(lo, (uint32_t)((uint64_t)lo + span - 1));
-    for (int j = tid; j < nvec; j += kTpThreads) {
-      const uint4 v = sl[j];
-      if (!first && !flt.any(v)) continue;
+    if (first) {
+      // every key is in range (lo = 0)
+      for (int j = tid; j < nvec; j += kTpThreads) {
+        const uint4 v = sl[j];
 #pragma unroll
-      for (int t = 0; t < VW; ++t) {
-        const float x = TR::get(v, t);
-        const uint32_t key = tp_key<T>(x);
-        if (key >= lo && (uint64_t)(key - lo) < span) {
-          const float w = ex2_approx(fmaf(x, p.c, -Mc));
-          sm.hist[(key - lo) >> sh][tid] += w;
+        for (int t = 0; t < VW; ++t) {
+          const float x = TR::get(v, t);
+          sm.hist[tp_key<T>(x) >> sh][tid] += ex2_approx(fmaf(x, p.c, -Mc));
+        }
+      }
+    } else {
+      const TpFilter<T> flt = tp_filter<T>(lo, (uint32_t)((uint64_t)lo + span - 1));
+      for (int j = tid; j < nvec; j += kTpThreads) {
+        const uint4 v = sl[j];
+        if (!flt.any(v)) continue;
+#pragma unroll
+        for (int t = 0; t < VW; ++t) {
+          const float x = TR::get(v, t);
+          const uint32_t key = tp_key<T>(x);
+          if (key >= lo && (uint64_t)(key - lo) < span) {
+            const float w = ex2_approx(fmaf(x, p.c, -Mc));
+            sm.hist[(key - lo) >> sh][tid] += w;
+          }
         }
       }
     }
     __syncthreads();
     // this CTA's bucket totals (warp w sums bucket w over the columns), pushed to every rank
     {
-      F2 acc{0.f, 0.f};
-      for (int c = lane; c < kTpThreads; c += 32) acc = f2_add(acc, F2{sm.hist[warp][c], 0.f});
+      F2 a0{0.f, 0.f}, a1{0.f, 0.f};   // two chains: half the dependent additions
+      for (int c = lane; c < kTpThreads; c += 64) {
+        a0 = f2_add(a0, F2{sm.hist[warp][c], 0.f});
+        a1 = f2_add(a1, F2{sm.hist[warp][c + 32], 0.f});
+      }
+      F2 acc = f2_add(a0, a1);
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) acc = f2_add(acc, f2_shfl_xor(acc, o));
       if (lane < C) *cl.map_shared_rank(&sm.ctot[pass & 1][rank][warp], lane) = acc;
@@ -560,32 +576,25 @@ __global__ void __launch_bounds__(kTpThreads, 2) topp_cluster_kernel(const Param
       sm.tot[tid] = t;
     }
     __syncthreads();
+    // the crossing bucket, in every warp at once: lane l holds bucket 15 - l
+    // (from the top), a two-float scan gives the mass above each bucket and
+    // through it; the pick is the first bucket whose cumulative mass reaches
+    // the target (if rounding leaves none, the lowest bucket with mass)
+    const F2 tk = lane < kTpBuckets ? sm.tot[kTpBuckets - 1 - lane] : F2{0.f, 0.f};
+    const F2 inc = warp_incl_scan_f2(tk);
     if (first) {
-      total = F2{0.f, 0.f};
-      for (int k = 0; k < kTpBuckets; ++k) total = f2_add(total, sm.tot[k]);
+      total = F2{__shfl_sync(0xffffffffu, inc.hi, kTpBuckets - 1), __shfl_sync(0xffffffffu, inc.lo, kTpBuckets - 1)};
       target = f2_scale(total, p.top_p);
       first = false;
     }
-    // the crossing bucket, from the top (as in topp_row_kernel)
-    int pick = -1, lowest = 0;
-    F2 cum = above, cum_low = above;
-    for (int k = (1 << bits) - 1; k >= 0; --k) {
-      if (f2_pos(sm.tot[k])) {
-        lowest = k;
-        cum_low = cum;
-      }
-      const F2 nc = f2_add(cum, sm.tot[k]);
-      if (!f2_lt(nc, target)) {
-        pick = k;
-        break;
-      }
-      cum = nc;
-    }
-    if (pick < 0) {
-      pick = lowest;
-      cum = cum_low;
-    }
-    above = cum;
+    F2 excl{__shfl_up_sync(0xffffffffu, inc.hi, 1), __shfl_up_sync(0xffffffffu, inc.lo, 1)};
+    if (lane == 0) excl = F2{0.f, 0.f};
+    const F2 cin = f2_add(above, inc), cex = f2_add(above, excl);
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < kTpBuckets && !f2_lt(cin, target));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < kTpBuckets && f2_pos(tk));
+    const int pl = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    const int pick = pl >= 0 ? kTpBuckets - 1 - pl : 0;
+    if (pl >= 0) above = F2{__shfl_sync(0xffffffffu, cex.hi, pl), __shfl_sync(0xffffffffu, cex.lo, pl)};
     lo += (uint32_t)pick << sh;
     width = sh;
     ++pass;
