@@ -215,7 +215,7 @@ def _topp_kernel(V, esize, forced_row=False):
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("V,G,B,tp,T", [(40003, 4, 6, 0.9, 1.0), (128256, 4, 4, 0.5, 1.0), (152064, 8, 2, 0.99, 0.8),
                                         (5000, 3, 10, 0.95, 0.7), (1030, 2, 12, 0.6, 1.3), (32768, 2, 5, 0.9, 1.0),
-                                        (65544, 3, 4, 0.8, 1.0)])
+                                        (65544, 3, 4, 0.8, 1.0), (262144, 2, 2, 0.9, 1.0), (262152, 2, 2, 0.9, 1.0)])
 def test_topp_only_any_vocab(sv, monkeypatch, path, dt, V, G, B, tp, T):
     """top-p with no top-k beyond SV_MAX_TOP_K tokens (the threshold path):
     Zipf-like rows with heavy tails (large kept sets) and exact ties; the
