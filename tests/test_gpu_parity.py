@@ -215,12 +215,15 @@ def _topp_kernel(V, esize, forced_row=False):
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("V,G,B,tp,T", [(40003, 4, 6, 0.9, 1.0), (128256, 4, 4, 0.5, 1.0), (152064, 8, 2, 0.99, 0.8),
                                         (5000, 3, 10, 0.95, 0.7), (1030, 2, 12, 0.6, 1.3), (32768, 2, 5, 0.9, 1.0),
-                                        (65544, 3, 4, 0.8, 1.0), (262144, 2, 2, 0.9, 1.0), (262152, 2, 2, 0.9, 1.0)])
+                                        (65544, 3, 4, 0.8, 1.0), (262144, 2, 2, 0.9, 0.5), (262152, 2, 2, 0.9, 0.5)])
 def test_topp_only_any_vocab(sv, monkeypatch, path, dt, V, G, B, tp, T):
     """top-p with no top-k beyond SV_MAX_TOP_K tokens (the threshold path):
     Zipf-like rows with heavy tails (large kept sets) and exact ties; the
     cluster-resident kernel (1 to 8 slices, the last one short) and the
-    per-row kernel on the same inputs."""
+    per-row kernel on the same inputs.  The largest rows (2^18 tokens, the
+    cluster kernel's limit and one vector past it) run at T = 0.5: with a
+    few draws per case, a flatter row would put one of them within 1e-6 of
+    a CDF step more often than the 1e-4 boundary-mismatch bound allows."""
     if path == "topprow":
         monkeypatch.setenv("SPECVERIFY_PATH", "topprow")
     else:
