@@ -717,3 +717,18 @@ def test_qlogits_bad_draft_row_is_a_zero_q():
     r = svref.verify_sample_qlogits(L, Q, d, u, 1.0)
     assert np.all(r["accept_prob"][:, 0] == 1.0)          # q_0(d_0) = 0 with p_0(d_0) > 0
     assert np.all(r["status"] & svref.SEQ_Q_NOT_POSITIVE)
+
+
+def test_inverse_cdf_fallback_when_no_step_exceeds_the_target():
+    """The branch where no running sum exceeds t = u R: all-zero weights draw
+    index 0 (no mass anywhere); a target at the total (u = 1, outside the
+    uniforms' range, the case rounding can reach) takes the last entry of
+    positive mass, the same token as u just below 1, and skips trailing
+    zero-weight entries."""
+    assert svref.inverse_cdf([0.0, 0.0, 0.0], 0.5) == (0, False)
+    w = [0.2, 0.5, 0.3, 0.0, 0.0]
+    v_end, _ = svref.inverse_cdf(w, 1.0)
+    v_below, _ = svref.inverse_cdf(w, float(np.float32(1.0) - np.float32(2.0 ** -24)))
+    assert v_end == 2 and v_below == 2
+    # the ordinary branch next to it: the smallest v whose running sum exceeds u R
+    assert svref.inverse_cdf(w, 0.25)[0] == 1 and svref.inverse_cdf(w, 0.1)[0] == 0
